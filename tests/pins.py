@@ -1,0 +1,277 @@
+"""Pins for the CPU oracle: facts fixed by the format definition or by
+mathematics, independent of the oracle's own code.
+
+Each check takes the loaded oracle library, so the same pins can be run
+against deliberately broken copies of the oracle (tests/test_oracle_mutants.py).
+A check returns None when it holds and raises AssertionError otherwise.
+"""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+
+import oracle as ora
+from weight_streaming_q4_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _block(d_bits: int, codes) -> np.ndarray:
+    b = np.zeros(18, dtype=np.uint8)
+    b[0] = d_bits & 0xFF
+    b[1] = d_bits >> 8
+    b[2:] = np.asarray(codes, dtype=np.uint8)
+    return b
+
+
+def _f16(v) -> np.ndarray:
+    return np.asarray(v, dtype=np.float16).view(np.uint16)
+
+
+def golden_blocks():
+    """(block bytes, expected weights) pairs from the hand-built fixture."""
+    out, blk = [], None
+    with open(os.path.join(GOLDEN, "q4_0_hand_blocks.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            tag, rest = line.split(None, 1)
+            if tag == "block":
+                blk = np.frombuffer(bytes.fromhex(rest), dtype=np.uint8).copy()
+            elif tag == "weights":
+                out.append((blk, np.array([float(t) for t in rest.split()])))
+    return out
+
+
+def golden_gemv():
+    vals = {}
+    with open(os.path.join(GOLDEN, "q4_0_hand_gemv.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            tag, rest = line.split(None, 1)
+            vals[tag] = rest
+    w = np.frombuffer(bytes.fromhex(vals["row"].replace(" ", "")), dtype=np.uint8).copy()
+    xs = []
+    for tok in vals["x"].split():
+        hexv, _, rep = tok.partition("*")
+        xs += [int(hexv, 16)] * (int(rep) if rep else 1)
+    return w, np.array(xs, dtype=np.uint16), float(vals["y"]), float(vals["s"])
+
+
+# ------------------------------------------------------------------ binary16
+
+def pin_half_decode_exhaustive(lib):
+    bits = np.arange(65536, dtype=np.uint16)
+    got = ora.half_to_double(bits, lib=lib)
+    ref = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+def pin_half_encode(lib):
+    rng = np.random.default_rng(1)
+    # every finite binary16 value, the midpoints between neighbours (ties), and
+    # random doubles over the whole range, including overflow and subnormals
+    fin = np.arange(65536, dtype=np.uint16).view(np.float16)
+    fin = fin[np.isfinite(fin)].astype(np.float64)
+    fin = np.unique(fin)
+    mids = (fin[:-1] + fin[1:]) / 2
+    rnd = np.concatenate([rng.standard_normal(20000) * 10.0 ** rng.integers(-9, 6, 20000),
+                          [0.0, -0.0, 65519.99, 65520.0, -65520.0, 1e6, 2.0 ** -25, 2.0 ** -26,
+                           3 * 2.0 ** -26, np.inf, -np.inf]])
+    v = np.concatenate([fin, mids, rnd])
+    got = ora.double_to_half(v, lib=lib)
+    with np.errstate(over="ignore"):
+        ref = v.astype(np.float16).view(np.uint16)
+    assert np.array_equal(got, ref)
+
+
+# ------------------------------------------------------------------ Q4_0 layout
+
+def pin_golden_blocks(lib):
+    for blk, expect in golden_blocks():
+        got = ora.dequant(blk, 1, 32, lib=lib).ravel()
+        assert np.array_equal(got, expect), (got, expect)
+
+
+def pin_distinct_positions(lib):
+    # every element of a block carries a distinct value: element j<16 comes
+    # from the low nibble of byte j and element j+16 from its high nibble
+    rng = np.random.default_rng(2)
+    for _ in range(20):
+        codes = rng.integers(0, 256, 16, dtype=np.uint8)
+        d = float(rng.uniform(0.01, 2.0))
+        dbits = int(_f16(d))
+        dd = float(np.uint16(dbits).view(np.float16))
+        got = ora.dequant(_block(dbits, codes), 1, 32, lib=lib).ravel()
+        lo = (codes & 15).astype(np.float64) - 8
+        hi = (codes >> 4).astype(np.float64) - 8
+        assert np.array_equal(got, np.concatenate([lo, hi]) * dd)
+
+
+def pin_block_indexing(lib):
+    # block i of row n sits at byte offset (n * K/32 + i) * 18: give every
+    # block a distinct scale and all-15 codes, so W[n][k] = 7 * d[n][k // 32]
+    n_rows, k_dim = 3, 96
+    nb = n_rows * k_dim // 32
+    scales = _f16(np.arange(1, nb + 1) / 8.0)
+    w = np.concatenate([_block(int(s), [0xFF] * 16) for s in scales])
+    got = ora.dequant(w, n_rows, k_dim, lib=lib)
+    ds = scales.view(np.float16).astype(np.float64).reshape(n_rows, k_dim // 32)
+    assert np.array_equal(got, 7.0 * np.repeat(ds, 32, axis=1))
+
+
+# ------------------------------------------------------------------ product closed forms
+
+def pin_golden_gemv(lib):
+    w, x, y_exp, s_exp = golden_gemv()
+    y, s = ora.gemv(w, x, 1, 64, lib=lib)
+    assert y[0, 0] == y_exp and s[0, 0] == s_exp, (y, s)
+
+
+def pin_all_eight_is_zero(lib):
+    rng = np.random.default_rng(3)
+    n_rows, k_dim = 5, 256
+    blocks = [_block(int(_f16(rng.uniform(-3, 3))), [0x88] * 16) for _ in range(n_rows * k_dim // 32)]
+    w = np.concatenate(blocks)
+    x = _f16(rng.standard_normal((2, k_dim)))
+    y, s = ora.gemv(w, x, n_rows, k_dim, batch=2, lib=lib)
+    assert np.all(y == 0.0) and np.all(s == 0.0)
+
+
+def pin_single_nonzero(lib):
+    # one code differs from 8 in the whole matrix: y = (q-8) * d * x exactly
+    rng = np.random.default_rng(4)
+    n_rows, k_dim = 4, 128
+    for trial in range(30):
+        nb = n_rows * k_dim // 32
+        w = np.concatenate([_block(int(_f16(rng.uniform(0.001, 1))), [0x88] * 16) for _ in range(nb)])
+        n = int(rng.integers(n_rows))
+        k = int(rng.integers(k_dim))
+        q = int(rng.choice([c for c in range(16) if c != 8]))
+        blk = (n * (k_dim // 32) + k // 32) * 18
+        j = k % 32
+        byte = blk + 2 + (j % 16)
+        if j < 16:
+            w[byte] = (w[byte] & 0xF0) | q
+        else:
+            w[byte] = (w[byte] & 0x0F) | (q << 4)
+        x = _f16(rng.standard_normal(k_dim))
+        y, _ = ora.gemv(w, x, n_rows, k_dim, lib=lib)
+        d = float(w[blk:blk + 2].view(np.uint16).view(np.float16)[0])
+        xv = float(x.view(np.float16)[k])
+        expect = np.zeros(n_rows)
+        expect[n] = (q - 8) * d * xv  # exact in double: <= 4+11+11 significant bits
+        assert np.array_equal(y[0], expect), (trial, y, expect)
+
+
+def pin_constant_codes(lib):
+    # all codes 15 (or 0) and x = 1: y = 7*32*d (or -8*32*d) per block
+    rng = np.random.default_rng(5)
+    for code, fac in ((0xFF, 7), (0x00, -8)):
+        ds = rng.uniform(0.01, 1, 6)
+        dbits = _f16(ds)
+        w = np.concatenate([_block(int(b), [code] * 16) for b in dbits])
+        x = _f16(np.ones(32 * 6))
+        y, _ = ora.gemv(w, x, 1, 32 * 6, lib=lib)
+        exact = sum(fac * 32 * float(b.view(np.float16)) for b in dbits)
+        assert abs(y[0, 0] - exact) <= 1e-15 * abs(exact)
+
+
+def _numpy_dense(w: np.ndarray, n_rows: int, k_dim: int) -> np.ndarray:
+    # an independent vectorised dequantiser (numpy's own binary16 decode)
+    blk = w.reshape(n_rows * k_dim // 32, 18)
+    d = blk[:, :2].copy().view(np.uint16).view(np.float16).astype(np.float64)
+    codes = blk[:, 2:]
+    q = np.concatenate([codes & 15, codes >> 4], axis=1).astype(np.float64)
+    return ((q - 8) * d).reshape(n_rows, k_dim)
+
+
+def pin_brute_force(lib):
+    for (n_rows, k_dim, batch, seed) in ((1, 32, 1, 0), (3, 64, 2, 1), (17, 256, 3, 2), (8, 1024, 1, 3)):
+        w = synth.q4_matrix(n_rows, k_dim, seed, 9)
+        x = synth.activations(batch, k_dim, seed)
+        dense = _numpy_dense(w, n_rows, k_dim)
+        xd = x.view(np.float16).astype(np.float64)
+        ref = xd @ dense.T
+        mag = np.abs(xd) @ np.abs(dense).T
+        y, s = ora.gemv(w, x, n_rows, k_dim, batch=batch, lib=lib)
+        assert np.all(np.abs(y - ref) <= 1e-12 * mag + 1e-300), (n_rows, k_dim)
+        assert np.allclose(s, mag, rtol=1e-12, atol=0)
+
+
+# ------------------------------------------------------------------ invariants
+
+def pin_invariants(lib):
+    n_rows, k_dim, seed = 12, 512, 7
+    w = synth.q4_matrix(n_rows, k_dim, seed, 3)
+    x = synth.activations(2, k_dim, seed)
+    y, s = ora.gemv(w, x, n_rows, k_dim, batch=2, lib=lib)
+    # linearity in x for a power-of-two factor: exact
+    x2 = _f16(x.view(np.float16).astype(np.float64) * 2.0)
+    y2, _ = ora.gemv(w, x2, n_rows, k_dim, batch=2, lib=lib)
+    assert np.array_equal(y2, 2.0 * y)
+    # row permutation of W permutes y
+    perm = np.random.default_rng(0).permutation(n_rows)
+    wp = w.reshape(n_rows, -1)[perm].reshape(-1)
+    yp, _ = ora.gemv(wp, x, n_rows, k_dim, batch=2, lib=lib)
+    assert np.array_equal(yp, y[:, perm])
+    # flipping the sign bit of every scale negates y
+    wn = w.reshape(-1, 18).copy()
+    wn[:, 1] ^= 0x80
+    yn, _ = ora.gemv(wn.reshape(-1), x, n_rows, k_dim, batch=2, lib=lib)
+    assert np.array_equal(yn, -y)
+    # a batch is its rows stacked
+    for b in range(2):
+        yb, sb = ora.gemv(w, x[b], n_rows, k_dim, batch=1, lib=lib)
+        assert np.array_equal(yb[0], y[b]) and np.array_equal(sb[0], s[b])
+    # selected rows agree with the full product
+    rows = np.array([11, 0, 5])
+    yr, sr = ora.gemv_rows(w, x, n_rows, k_dim, rows, batch=2, lib=lib)
+    assert np.array_equal(yr, y[:, rows]) and np.array_equal(sr, s[:, rows])
+
+
+# ------------------------------------------------------------------ glue
+
+def pin_glue(lib):
+    # RMSNorm of a constant vector c: c / sqrt(c^2 + eps)
+    c = 0.5
+    h = _f16(np.full(64, c))
+    x = ora.rmsnorm(h, 1, 64, 1e-5, lib=lib)
+    assert np.all(x == _f16(c / np.sqrt(c * c + 1e-5)))
+    # RMSNorm is invariant to a power-of-two rescale of h (up to the eps term)
+    rng = np.random.default_rng(6)
+    hv = rng.standard_normal((2, 256))
+    a = ora.rmsnorm(_f16(hv), 2, 256, 0.0, lib=lib)
+    b = ora.rmsnorm(_f16(hv * 4), 2, 256, 0.0, lib=lib)
+    assert np.array_equal(a, b)
+    # unit RMS output: mean(x^2) == 1 within binary16 rounding
+    xv = a.view(np.float16).astype(np.float64)
+    assert np.all(np.abs((xv ** 2).mean(axis=1) - 1) < 2e-3)
+    # SiLU gate: silu(0) = 0; silu(g) -> g for large g; silu(-g) = silu(g) - g
+    g = np.array([0.0, 30.0, -30.0, 1.0, -1.0])
+    u = np.array([5.0, 1.0, 1.0, 1.0, 1.0])
+    act = ora.silu_mul(g, u, lib=lib).view(np.float16).astype(np.float64)
+    assert act[0] == 0 and act[1] == 30.0 and abs(act[2]) < 1e-9
+    assert abs(act[3] - 0.7310585786) < 1e-3 and abs(act[4] + 0.2689414214) < 1e-3
+    # residual add of small integers is exact
+    hr = _f16(np.arange(-4, 4, dtype=np.float64))
+    r = ora.residual(hr, np.full(8, 2.0), lib=lib)
+    assert np.array_equal(r, _f16(np.arange(-2, 6, dtype=np.float64)))
+    # context-1 attention: query head qh reads value head qh // group
+    q_dim, kv_dim, hd = 8 * 4, 2 * 4, 4          # 8 query heads, 2 value heads
+    v = np.arange(kv_dim, dtype=np.float64)       # value head j holds 4j..4j+3
+    att = ora.attn_ctx1(v, 1, q_dim, kv_dim, hd, lib=lib).view(np.float16).astype(np.float64)
+    expect = np.concatenate([v[(qh // 4) * hd:(qh // 4) * hd + hd] for qh in range(8)])
+    assert np.array_equal(att.ravel(), expect)
+
+
+ALL_PINS = [pin_half_decode_exhaustive, pin_half_encode, pin_golden_blocks, pin_distinct_positions,
+            pin_block_indexing, pin_golden_gemv, pin_all_eight_is_zero, pin_single_nonzero,
+            pin_constant_codes, pin_brute_force, pin_invariants, pin_glue]

@@ -1,0 +1,54 @@
+"""Plant a mistake in a copy of the oracle and check that the pins catch it.
+
+Each mutant is a one-line edit of q4_oracle.c (a plausible slip: a wrong
+nibble order, a dropped term, a wrong sign or index, a transposed operand),
+compiled on the CPU into a temporary library.  The pins must reject every
+one of them; a mutant that passes all pins would mean the pins leave that
+part of the oracle unchecked.
+"""
+import os
+
+import pytest
+
+import oracle as ora
+from pins import ALL_PINS
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "q4_oracle.c")
+
+MUTANTS = {
+    "interleaved_nibbles": ("int q = (j < 16) ? (qs[j] & 0x0F) : (qs[j - 16] >> 4);",
+                            "int q = (j % 2 == 0) ? (qs[j / 2] & 0x0F) : (qs[j / 2] >> 4);"),
+    "swapped_nibbles": ("(qs[j] & 0x0F) : (qs[j - 16] >> 4)", "(qs[j] >> 4) : (qs[j - 16] & 0x0F)"),
+    "no_offset": ("return (double)(q - 8) *", "return (double)(q) *"),
+    "offset_7": ("return (double)(q - 8) *", "return (double)(q - 7) *"),
+    "big_endian_scale": ("blk[0] | (blk[1] << 8)", "blk[1] | (blk[0] << 8)"),
+    "flush_subnormals": ("v = ldexp((double)m, -24);", "v = 0.0;"),
+    "exponent_bias": ("e - 25);", "e - 24);"),
+    "ties_away": ("double m = rint(ldexp(a, 10 - e));", "double m = round(ldexp(a, 10 - e));"),
+    "block_stride_16": ("#define ORA_BLOCK_BYTES 18", "#define ORA_BLOCK_BYTES 16"),
+    "x_transposed": ("double p = ora_weight(w, k_dim, n, k) * ora_half_to_double(xb[k]);\n                acc += p;\n                mag += fabs(p);\n            }\n            y[(int64_t)b * n_rows + n] = acc;",
+                     "double p = ora_weight(w, k_dim, n, k) * ora_half_to_double(x[k * batch + b]);\n                acc += p;\n                mag += fabs(p);\n            }\n            y[(int64_t)b * n_rows + n] = acc;"),
+    "signed_magnitude": ("mag += fabs(p);", "mag += p;"),
+    "attn_modulo": ("(qh / group) * head_dim", "(qh % n_kv) * head_dim"),
+    "norm_no_mean": ("sqrt(ss / (double)dim + eps)", "sqrt(ss + eps)"),
+    "silu_sign": ("exp(-g[i])", "exp(g[i])"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    text = open(SRC).read()
+    assert text.count(old) >= 1, f"mutation site for {name} not found"
+    src = tmp_path / f"mut_{name}.c"
+    src.write_text(text.replace(old, new, 1))
+    lib = ora.load(ora.compile_oracle(str(src), str(tmp_path / f"mut_{name}.so")))
+    caught = []
+    for pin in ALL_PINS:
+        try:
+            pin(lib)
+        except AssertionError:
+            caught.append(pin.__name__)
+        except Exception as e:  # a crash in a pin also rejects the mutant
+            caught.append(f"{pin.__name__}:{type(e).__name__}")
+    assert caught, f"mutant {name} passed every pin"
