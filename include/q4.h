@@ -1,0 +1,265 @@
+/*
+ * q4.h -- C ABI of libq4.so: the decode-step matrix-vector product over
+ * GGUF Q4_0 weights on one GB300 GPU (sm_103a), run one matrix, one decoder
+ * layer stack, or a stack streamed from pinned host memory.
+ *
+ * Sources of the operations (the pages this library follows):
+ *   - "PIPO: Pipelined Offloading for Efficient Inference on Consumer
+ *     Devices" (paper summary page), Method: "Computation optimization"
+ *     (matrix-vector products computed directly on 4-bit weights, without
+ *     dequantisation, at small batch), "Automatic configuration" (that kernel
+ *     is used for batch sizes below 16), "Offloading architecture" and
+ *     "Pipeline design" (only one or a few layers resident, per-layer
+ *     schedule: load the next layer, synchronise the current one, compute),
+ *     "Two pipeline modes" (performance-optimised mode keeps two layers in
+ *     GPU memory), "Data transfer suite" (a layer's tensors merged into one
+ *     buffer and one transfer).
+ *   - "PipeLLM: Faster Local LLM Inference Than llama.cpp via System-Level
+ *     Optimizations" (forum post), "Layer 1: CUDA Graph Compilation" (the
+ *     decode loop captured as a static graph) and "Layer 2: Asynchronous
+ *     Weight Prefetching" (two CUDA streams, a fixed pinned buffer pool,
+ *     double-buffered weight staging).
+ *   - The GGUF file format both pages load (PipeLLM, compatibility
+ *     paragraph).  Q4_0 block: 32 weights as a little-endian IEEE binary16
+ *     scale d followed by 16 code bytes; byte j holds element j in its low
+ *     nibble and element j+16 in its high nibble; weight = (q - 8) * d.
+ *     18 bytes per block, blocks of a row consecutive, rows consecutive.
+ *
+ * Conventions for every call:
+ *   - Pointers named "device" are CUDA device (or managed) memory of the
+ *     current device; the caller allocates and owns every buffer.  Handles
+ *     own only CUDA streams, events and graphs, which destroy() releases.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
+ *     Calls are asynchronous on it unless stated otherwise.
+ *   - Return value: Q4_OK or a negative Q4_ERR_* code; nothing is launched
+ *     when an argument check fails.  A CUDA error seen by the library is
+ *     kept for q4_last_cuda_error().  Kernels never trap: a wait that runs
+ *     out sets a status bit that q4_device_status() / the *_status() calls
+ *     report, and the kernel returns.
+ *   - Weight, x and y pointers must be 16-byte aligned (Q4_ERR_ALIGN).
+ *   - k must be a multiple of 32 (one block); the streaming kernel needs k in
+ *     {256, 512, 1024} or a multiple of 2048 up to 16384, or a multiple of
+ *     4096 up to 32768; other k use a plain (slower) kernel.
+ *   - x is binary16 [batch][k] row-major, y is fp32 [batch][n] row-major and
+ *     is overwritten, not accumulated.  1 <= batch <= 16.
+ *   - Accuracy: |y - sum_k w*x| <= 1e-3 * sum_k |w*x| + 1e-5 per element;
+ *     every product (q - 8) * x is formed exactly, so a block whose codes are
+ *     all 8 contributes exactly zero.
+ */
+#ifndef Q4_H
+#define Q4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ----------------------------------------------------------------- status */
+
+#define Q4_OK 0
+#define Q4_ERR_ARG (-1)      /* bad size, null pointer, unsupported shape */
+#define Q4_ERR_ALIGN (-2)    /* pointer not 16-byte aligned */
+#define Q4_ERR_CUDA (-3)     /* a CUDA runtime call failed; see q4_last_cuda_error() */
+#define Q4_ERR_TIMEOUT (-4)  /* a host-side wait ran out */
+#define Q4_ERR_OOM (-5)      /* the caller's workspace is too small */
+#define Q4_ERR_DEVICE (-6)   /* a kernel reported a failed wait in its status word */
+
+/* Text for a status code (static storage). */
+const char *q4_status_string(int status);
+
+/* The last cudaError_t value the library saw (0 if none); reading clears it. */
+int q4_last_cuda_error(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int q4_version(void);
+
+/* Bytes of one row-major Q4_0 matrix with n rows and k columns: n * k / 32 * 18. */
+size_t q4_matrix_bytes(int n, int k);
+
+/* ------------------------------------------------------- one product */
+
+/* Kernel choice for q4_gemv_ex. */
+#define Q4_KERNEL_AUTO 0     /* what q4_gemv uses */
+#define Q4_KERNEL_STREAM 1   /* persistent TMA-ring kernel, CUDA-core exact products (batch 1) */
+#define Q4_KERNEL_SIMPLE 2   /* one warp per row, plain loads (any k % 32 == 0, any batch) */
+#define Q4_KERNEL_MMA 3      /* persistent TMA-ring kernel, tensor-core products (batch 1..16) */
+
+/*
+ * y[b][n] = sum_k W[n][k] * x[b][k], W dequantisation-free from its Q4_0 blocks
+ * (PIPO summary, Method, "Computation optimization").
+ *   w      device, Q4_0 [n][k/32] blocks (q4_matrix_bytes(n, k) bytes), read only
+ *   x      device, binary16 [batch][k], read only
+ *   y      device, fp32 [batch][n], written
+ *   n      rows (>= 1); k columns (>= 32, multiple of 32); 1 <= batch <= 16
+ * Errors: Q4_ERR_ARG, Q4_ERR_ALIGN, Q4_ERR_CUDA (launch failure).
+ */
+int q4_gemv(const void *w, const uint16_t *x, float *y, int n, int k, int batch, void *stream);
+
+/* q4_gemv with an explicit kernel (Q4_KERNEL_*); Q4_ERR_ARG if that kernel
+ * cannot run the shape (see the conventions above). */
+int q4_gemv_ex(const void *w, const uint16_t *x, float *y, int n, int k, int batch, int kernel,
+               void *stream);
+
+/* Status bits set by q4_gemv kernels whose internal waits ran out since the
+ * last call (0 = none); synchronises the device and clears the bits. */
+int q4_device_status(void);
+
+/*
+ * Debug: w_out[n][k] = (q - 8) * d as fp32 for every weight (exact: every
+ * such value is a float).  Checks the block layout bit for bit.
+ *   w      device, Q4_0 [n][k/32] blocks; w_out device, fp32 [n][k]
+ * Errors: Q4_ERR_ARG, Q4_ERR_ALIGN, Q4_ERR_CUDA.
+ */
+int q4_dequant_debug(const void *w, float *w_out, int n, int k, void *stream);
+
+/* ------------------------------------------------------- decoder layers */
+
+/*
+ * Shape of one Llama-style decoder layer.  The layer (the plainest reading of
+ * "a layer's projections in sequence"; the pages name the projections only by
+ * the model families they run) is, per batch row, with h the binary16
+ * residual stream:
+ *   x  = f16(h / sqrt(mean(h^2) + eps))              RMSNorm, unit weight
+ *   q, k, v = Wq x, Wk x, Wv x                       (fp32)
+ *   a  = f16(v of the value head each query head is grouped with)
+ *        (attention over a context of one token: softmax of one score is 1)
+ *   h  = f16(h + Wo a)
+ *   x  = f16(h / sqrt(mean(h^2) + eps))
+ *   act = f16(silu(Wgate x) * (Wup x))
+ *   h  = f16(h + Wdown act)
+ */
+typedef struct q4_layer_shape {
+  int hidden;     /* model width (4096 for 8B, 8192 for 70B) */
+  int q_dim;      /* rows of Wq, columns of Wo */
+  int kv_dim;     /* rows of Wk and Wv */
+  int ffn;        /* rows of Wgate and Wup, columns of Wdown */
+  int head_dim;   /* 128 */
+  float eps;      /* RMSNorm epsilon (1e-5) */
+} q4_layer_shape;
+
+#define Q4_PROJ_Q 0
+#define Q4_PROJ_K 1
+#define Q4_PROJ_V 2
+#define Q4_PROJ_O 3
+#define Q4_PROJ_GATE 4
+#define Q4_PROJ_UP 5
+#define Q4_PROJ_DOWN 6
+
+/*
+ * Layout of one merged layer block (PIPO summary, "Data transfer suite":
+ * data merging): the seven projections q, k, v, o, gate, up, down, each a
+ * row-major Q4_0 matrix, back to back in that order.  offsets[7] receives
+ * each projection's byte offset and *layer_bytes the block's size.
+ * Errors: Q4_ERR_ARG (null or inconsistent shape).
+ */
+int q4_layer_offsets(const q4_layer_shape *shape, size_t offsets[7], size_t *layer_bytes);
+
+/* Regions of a decoder or stream workspace (index into offsets[]). */
+#define Q4_WS_CONTROL 0   /* barrier count and status word (zeroed at create) */
+#define Q4_WS_PROGRAM 1   /* phase descriptors */
+#define Q4_WS_QKV 2       /* fp32 [batch][q_dim + 2 kv_dim]: q, k, v of the last layer run */
+#define Q4_WS_O 3         /* fp32 [batch][hidden]: Wo a */
+#define Q4_WS_GATE 4      /* fp32 [batch][ffn] */
+#define Q4_WS_UP 5        /* fp32 [batch][ffn] */
+#define Q4_WS_DOWN 6      /* fp32 [batch][hidden] */
+#define Q4_WS_ACT 7       /* binary16 [batch][ffn] */
+#define Q4_WS_X 8         /* binary16 [batch][hidden]: first normalised input */
+#define Q4_WS_ATTN 9      /* binary16 [batch][q_dim]: attention output */
+#define Q4_WS_X2 10       /* binary16 [batch][hidden]: second normalised input */
+#define Q4_WS_HMID 11     /* binary16 [batch][hidden]: h after the attention residual */
+#define Q4_WS_COUNT 12
+
+/*
+ * Byte offsets of the workspace regions for a decoder of n_layers layers
+ * (use n_layers = 2 for a stream ring) and the total size needed.  The
+ * intermediate regions hold the values of the last layer run (for checks).
+ * Errors: Q4_ERR_ARG.
+ */
+int q4_workspace_layout(const q4_layer_shape *shape, int n_layers, int batch,
+                        size_t offsets[Q4_WS_COUNT], size_t *total_bytes);
+
+typedef struct q4_decoder q4_decoder;
+
+#define Q4_DEC_FUSED 0      /* the whole stack is one persistent launch (one graph node) */
+#define Q4_DEC_PER_LAYER 1  /* one launch per layer (one graph node per layer) */
+
+/*
+ * Create a decoder over n_layers HBM-resident layers and capture its CUDA
+ * graph (PipeLLM, "Layer 1: CUDA Graph Compilation").
+ *   shape          layer shape; layer_weights[i] = device pointer of layer
+ *                  i's merged block (q4_layer_offsets layout), 256-byte aligned
+ *   n_layers       >= 1; batch: 1 <= batch <= 16
+ *   workspace      device, >= q4_workspace_layout() bytes, 256-byte aligned;
+ *                  owned by the caller, must outlive the decoder
+ *   mode           Q4_DEC_FUSED or Q4_DEC_PER_LAYER
+ *   stream         used for the workspace initialisation (synchronised)
+ * Errors: Q4_ERR_ARG, Q4_ERR_ALIGN, Q4_ERR_OOM (workspace too small), Q4_ERR_CUDA.
+ */
+int q4_decoder_create(q4_decoder **out, const q4_layer_shape *shape, const void *const *layer_weights,
+                      int n_layers, int batch, void *workspace, size_t workspace_bytes, int mode,
+                      void *stream);
+
+/*
+ * Run all layers once on hidden_io (device, binary16 [batch][hidden], updated
+ * in place) by replaying the captured graph on `stream`.  The first call with
+ * a new hidden_io pointer rewrites the phase descriptors (stream-ordered).
+ * Errors: Q4_ERR_ARG, Q4_ERR_ALIGN, Q4_ERR_CUDA.
+ */
+int q4_layer_decode(q4_decoder *dec, uint16_t *hidden_io, void *stream);
+
+/* The same launches as q4_layer_decode, issued directly (no graph). */
+int q4_layer_decode_eager(q4_decoder *dec, uint16_t *hidden_io, void *stream);
+
+/* Status word of the decoder's kernels (synchronises `stream`): 0 = every
+ * wait completed; otherwise bit flags; clears it.  Errors: Q4_ERR_CUDA. */
+int q4_decoder_status(q4_decoder *dec, void *stream, int *status_out);
+
+int q4_decoder_destroy(q4_decoder *dec);
+
+/* ------------------------------------------------------- streamed layers */
+
+typedef struct q4_stream q4_stream;
+
+#define Q4_STREAM_POISON 1   /* after a layer's compute, overwrite its staging buffer's
+                                scales with NaN before the next copy lands (race check) */
+
+/*
+ * Create a double-buffered copy/compute ring (PipeLLM, "Layer 2"; PIPO,
+ * "Pipeline design" and the performance-optimised mode of "Two pipeline
+ * modes"): every layer's merged block lives in pinned host memory and only
+ * two layer buffers live in HBM.
+ *   host_layers[i]   pinned host pointer (cudaHostAlloc or registered) of
+ *                    layer i's merged block, 16-byte aligned, read only
+ *   n_layers >= 1;  batch 1..16
+ *   dev_buf0/1       device, buf_bytes >= one layer block each, 256-byte aligned
+ *   workspace        device, >= q4_workspace_layout(shape, 2, batch) bytes
+ *   flags            0 or Q4_STREAM_POISON
+ * The handle creates its own copy stream and events.
+ * Errors: Q4_ERR_ARG, Q4_ERR_ALIGN, Q4_ERR_OOM, Q4_ERR_CUDA.
+ */
+int q4_stream_create(q4_stream **out, const q4_layer_shape *shape, const void *const *host_layers,
+                     int n_layers, int batch, void *dev_buf0, void *dev_buf1, size_t buf_bytes,
+                     void *workspace, size_t workspace_bytes, int flags);
+
+/*
+ * Run all layers once on hidden_io (device, binary16 [batch][hidden]) while
+ * the copy stream prefetches layer i+1 into the other buffer as layer i
+ * computes on `compute_stream`.  Everything is enqueued asynchronously; if
+ * timeout_us > 0 the call then waits for completion, polling, and returns
+ * Q4_ERR_TIMEOUT if it has not finished after timeout_us microseconds (the
+ * work stays queued).  Errors: Q4_ERR_ARG, Q4_ERR_ALIGN, Q4_ERR_CUDA, Q4_ERR_TIMEOUT.
+ */
+int q4_stream_layers(q4_stream *st, uint16_t *hidden_io, void *compute_stream, int64_t timeout_us);
+
+/* Status word of the ring's kernels (synchronises compute_stream); clears it. */
+int q4_stream_status(q4_stream *st, void *compute_stream, int *status_out);
+
+int q4_stream_destroy(q4_stream *st);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q4_H */

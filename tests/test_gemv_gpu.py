@@ -1,0 +1,150 @@
+"""q4_gemv and q4_dequant_debug on the GPU against the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as ora
+import weight_streaming_q4_gb300 as q4
+from weight_streaming_q4_gb300 import build, synth
+from gpu_util import assert_within_tol, dev_u8, dev_u16, host_f32
+from pins import golden_blocks
+
+pytestmark = pytest.mark.gpu
+
+KERNELS = {"stream": q4.Q4_KERNEL_STREAM, "simple": q4.Q4_KERNEL_SIMPLE}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+    ora.build()
+
+
+def run(w_np, x_np, n, k, batch, kernel):
+    w = dev_u8(w_np)
+    x = dev_u16(x_np.reshape(-1))
+    y = torch.full((batch * n,), float("nan"), dtype=torch.float32, device="cuda")
+    q4.q4_gemv_ex(w, x, y, n, k, batch, kernel)
+    torch.cuda.synchronize()
+    return host_f32(y).reshape(batch, n)
+
+
+# ------------------------------------------------------------------ layout, bit for bit
+
+@pytest.mark.parametrize("n,k", [(1, 32), (3, 64), (17, 256), (64, 4096), (5, 14336)])
+def test_dequant_bit_exact(n, k):
+    w = synth.q4_matrix(n, k, 1, 2)
+    out = torch.empty(n * k, dtype=torch.float32, device="cuda")
+    q4.q4_dequant_debug(dev_u8(w), out, n, k)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().reshape(n, k)
+    ref = ora.dequant(w, n, k).astype(np.float32)   # every (q-8)*d is a float: exact
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+def test_dequant_golden_blocks():
+    for blk, expect in golden_blocks():
+        out = torch.empty(32, dtype=torch.float32, device="cuda")
+        q4.q4_dequant_debug(dev_u8(np.concatenate([blk, np.zeros(14, np.uint8)])), out, 1, 32)
+        torch.cuda.synchronize()
+        assert np.array_equal(out.cpu().numpy().astype(np.float64), expect)
+
+
+# ------------------------------------------------------------------ closed forms, exact
+
+def _const_matrix(n, k, d, code_byte):
+    blk = np.zeros(18, np.uint8)
+    blk[0:2] = np.array([d], np.float16).view(np.uint8)
+    blk[2:] = code_byte
+    return np.tile(blk, n * k // 32)
+
+
+@pytest.mark.parametrize("kernel", list(KERNELS))
+def test_all_eight_is_exactly_zero(kernel):
+    n, k = 40, 4096
+    w = _const_matrix(n, k, 0.75, 0x88)
+    x = synth.activations(1, k, 5)
+    y = run(w, x, n, k, 1, KERNELS[kernel])
+    assert np.all(y == 0.0)
+
+
+@pytest.mark.parametrize("kernel", list(KERNELS))
+def test_single_nonzero_is_exact(kernel):
+    rng = np.random.default_rng(7)
+    n, k = 16, 4096
+    for _ in range(6):
+        w = _const_matrix(n, k, 1.0, 0x88).copy().reshape(-1, 18)
+        w[:, 0:2] = np.asarray(rng.uniform(0.001, 0.05, n * k // 32), np.float16).view(np.uint8).reshape(-1, 2)
+        row, col = int(rng.integers(n)), int(rng.integers(k))
+        code = int(rng.choice([c for c in range(16) if c != 8]))
+        b = row * (k // 32) + col // 32
+        j = col % 32
+        byte = w[b, 2 + (j % 16)]
+        w[b, 2 + (j % 16)] = (byte & 0xF0) | code if j < 16 else (byte & 0x0F) | (code << 4)
+        x = synth.activations(1, k, int(rng.integers(1000)))
+        y = run(w.reshape(-1), x, n, k, 1, KERNELS[kernel])
+        d = float(w[b, 0:2].view(np.float16)[0])
+        xv = float(x.view(np.float16)[0, col])
+        expect = np.zeros(n, np.float32)
+        expect[row] = np.float32((code - 8) * d * xv)   # the exact product rounded once to fp32
+        assert np.array_equal(y[0].astype(np.float32), expect)
+
+
+# ------------------------------------------------------------------ parity with the oracle
+
+STREAM_SHAPES = [(1, 256), (7, 256), (33, 512), (100, 1024), (129, 2048), (300, 4096), (61, 14336), (17, 28672),
+                 (1000, 8192)]
+
+
+@pytest.mark.parametrize("n,k", STREAM_SHAPES)
+def test_stream_kernel_parity(n, k):
+    w = synth.q4_matrix(n, k, 3, synth.GEMV_TID)
+    x = synth.activations(1, k, 4)
+    y = run(w, x, n, k, 1, q4.Q4_KERNEL_STREAM)
+    y_ref, s_ref = ora.gemv(w, x, n, k, threads=8)
+    assert_within_tol(y, y_ref, s_ref, f"stream {n}x{k}")
+
+
+@pytest.mark.parametrize("n,k,batch", [(1, 32, 1), (9, 96, 2), (40, 800, 5), (65, 4096, 16), (33, 2048, 3)])
+def test_simple_kernel_parity(n, k, batch):
+    w = synth.q4_matrix(n, k, 8, 9)
+    x = synth.activations(batch, k, 10)
+    y = run(w, x, n, k, batch, q4.Q4_KERNEL_SIMPLE)
+    y_ref, s_ref = ora.gemv(w, x, n, k, batch=batch)
+    assert_within_tol(y, y_ref, s_ref, f"simple {n}x{k}x{batch}")
+
+
+def test_full_size_gemv_all_rows():
+    # the single-product workload: N = K = 4096, batch 1, every row against the oracle
+    n = k = 4096
+    w = synth.q4_matrix(n, k, 0, synth.GEMV_TID)
+    x = synth.activations(1, k, 0)
+    y = run(w, x, n, k, 1, q4.Q4_KERNEL_AUTO)
+    y_ref, s_ref = ora.gemv(w, x, n, k, threads=8)
+    assert_within_tol(y, y_ref, s_ref, "gemv 4096x4096")
+    assert q4.q4_device_status() == 0
+
+
+def test_deterministic_and_auto_is_stream():
+    n, k = 512, 4096
+    w = synth.q4_matrix(n, k, 1, synth.GEMV_TID)
+    x = synth.activations(1, k, 1)
+    a = run(w, x, n, k, 1, q4.Q4_KERNEL_AUTO)
+    b = run(w, x, n, k, 1, q4.Q4_KERNEL_STREAM)
+    c = run(w, x, n, k, 1, q4.Q4_KERNEL_STREAM)
+    assert np.array_equal(a, b) and np.array_equal(b, c)
+
+
+def test_large_rows_sampled():
+    # gate/up-shaped (14336 x 4096) and down-shaped (4096 x 14336) matrices on sampled rows
+    for (n, k) in ((14336, 4096), (4096, 14336), (8192, 28672)):
+        wd = torch.empty(q4.q4_matrix_bytes(n, k), dtype=torch.uint8, device="cuda")
+        synth.device_fill_q4(wd.data_ptr(), n * k // 32, seed=2, tid=synth.GEMV_TID)
+        x = synth.activations(1, k, 2)
+        y = torch.empty(n, dtype=torch.float32, device="cuda")
+        q4.q4_gemv(wd, dev_u16(x.reshape(-1)), y, n, k, 1)
+        torch.cuda.synchronize()
+        rows = np.sort(np.random.default_rng(n).choice(n, 256, replace=False))
+        wr = synth.q4_rows(rows, k, 2, synth.GEMV_TID)
+        y_ref, s_ref = ora.gemv(wr.reshape(-1), x, len(rows), k)
+        assert_within_tol(host_f32(y)[rows], y_ref[0], s_ref[0], f"{n}x{k} sampled")

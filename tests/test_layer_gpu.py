@@ -1,0 +1,128 @@
+"""q4_layer_decode (HBM-resident decoder stack under CUDA-graph capture)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as ora
+import weight_streaming_q4_gb300 as q4
+from weight_streaming_q4_gb300 import build, model, synth
+from gpu_util import dev_u16, f16_ulps, host_u16
+from layer_check import check_layer, read_ws, sampled_rows
+
+pytestmark = pytest.mark.gpu
+
+TINY = dict(hidden=256, q_dim=256, kv_dim=128, ffn=1024, head_dim=64)
+SMALL = dict(hidden=2048, q_dim=2048, kv_dim=512, ffn=4096, head_dim=128)
+MID = dict(hidden=1024, q_dim=1024, kv_dim=256, ffn=14336, head_dim=128)   # down rows 14336 wide
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+    ora.build()
+
+
+class Stack:
+    def __init__(self, cfg, n_layers, seed, mode=q4.Q4_DEC_FUSED):
+        self.cfg = cfg
+        self.shape = q4.LayerShape.of(**cfg)
+        self.wbuf, self.ptrs = model.resident_layers(self.shape, n_layers, seed)
+        self.ws, self.offs, self.ws_bytes = model.workspace(self.shape, n_layers, 1)
+        self.dec = q4.q4_decoder_create(self.shape, self.ptrs, 1, self.ws, self.ws_bytes, mode)
+
+    def run(self, h_np, graph=True, reps=1):
+        h = dev_u16(h_np.reshape(-1))
+        for _ in range(reps):
+            (q4.q4_layer_decode if graph else q4.q4_layer_decode_eager)(self.dec, h)
+        torch.cuda.synchronize()
+        assert q4.q4_decoder_status(self.dec) == 0
+        return host_u16(h).reshape(1, -1)
+
+    def close(self):
+        q4.q4_decoder_destroy(self.dec)
+
+
+@pytest.mark.parametrize("cfg", [TINY, SMALL, MID], ids=["tiny", "small", "mid"])
+def test_one_layer_step_by_step(cfg):
+    st = Stack(cfg, 1, seed=21)
+    h0 = synth.activations(1, cfg["hidden"], 22)
+    h1 = st.run(h0)
+    check_layer(cfg, 21, 0, h0, h1, read_ws(st.ws, st.offs, cfg))
+    st.close()
+
+
+def test_last_layer_of_a_stack_and_drift():
+    cfg, L = SMALL, 4
+    st = Stack(cfg, L, seed=5)
+    h0 = synth.activations(1, cfg["hidden"], 6)
+    # GPU: all layers at once; the workspace then holds the last layer's intermediates
+    hL = st.run(h0)
+    # the input of the last layer: run the first L-1 layers on their own
+    st_prev = Stack(cfg, L - 1, seed=5)
+    h_prev = st_prev.run(h0)
+    check_layer(cfg, 5, L - 1, h_prev, hL, read_ws(st.ws, st.offs, cfg))
+    # end-to-end against the oracle's own layer chain: drift stays small
+    ref = h0
+    for l in range(L):
+        ws = [synth.q4_matrix(n, k, 5, synth.tensor_id(l, p))
+              for p, (n, k) in enumerate(synth.layer_dims(cfg["hidden"], cfg["q_dim"], cfg["kv_dim"], cfg["ffn"]))]
+        ref = ora.layer(ws, ref, 1, cfg["hidden"], cfg["q_dim"], cfg["kv_dim"], cfg["ffn"], cfg["head_dim"])
+    a = hL.view(np.float16).astype(np.float64)
+    b = ref.view(np.float16).astype(np.float64)
+    assert np.linalg.norm(a - b) / np.linalg.norm(b) < 1e-2
+    st.close()
+    st_prev.close()
+
+
+def test_graph_eager_modes_identical():
+    cfg = TINY
+    h0 = synth.activations(1, cfg["hidden"], 30)
+    fused = Stack(cfg, 3, seed=31)
+    per = Stack(cfg, 3, seed=31, mode=q4.Q4_DEC_PER_LAYER)
+    a = fused.run(h0, graph=True, reps=2)
+    b = fused.run(h0, graph=False, reps=2)
+    c = per.run(h0, graph=True, reps=2)
+    d = per.run(h0, graph=False, reps=2)
+    assert np.array_equal(a, b) and np.array_equal(a, c) and np.array_equal(a, d)
+    fused.close()
+    per.close()
+
+
+def test_new_hidden_pointer_rewrites_program():
+    cfg = TINY
+    st = Stack(cfg, 2, seed=40)
+    h0 = synth.activations(1, cfg["hidden"], 41)
+    a = st.run(h0)
+    b = st.run(h0)     # a new tensor, hence a new pointer
+    assert np.array_equal(a, b)
+    st.close()
+
+
+def _full_stack(cfg, n_layers, seed, count):
+    st = Stack(cfg, n_layers, seed)
+    h0 = synth.activations(1, cfg["hidden"], seed + 1)
+    hL = st.run(h0)
+    stats = read_ws(st.ws, st.offs, cfg)
+    # the last layer's own input: the state after n_layers-1 layers, from a second
+    # decoder over the same device weights
+    prev = q4.q4_decoder_create(st.shape, st.ptrs[:-1], 1, st.ws, st.ws_bytes, q4.Q4_DEC_FUSED)
+    h = dev_u16(h0.reshape(-1))
+    q4.q4_layer_decode(prev, h)
+    torch.cuda.synchronize()
+    h_prev = host_u16(h).reshape(1, -1)
+    q4.q4_decoder_destroy(prev)
+    check_layer(cfg, seed, n_layers - 1, h_prev, hL, stats, rows=sampled_rows(count, seed))
+    assert np.all(np.isfinite(hL.view(np.float16).astype(np.float64)))
+    st.close()
+
+
+def test_8b_stack_full_size():
+    cfg = dict(synth.LLAMA_8B)
+    L = cfg.pop("n_layers")
+    _full_stack(cfg, L, seed=0, count=192)
+
+
+def test_70b_stack_full_size():
+    cfg = dict(synth.LLAMA_70B)
+    L = cfg.pop("n_layers")
+    _full_stack(cfg, L, seed=0, count=96)

@@ -1,0 +1,88 @@
+"""q4_stream_layers: the double-buffered copy/compute ring from pinned host memory."""
+import numpy as np
+import pytest
+import torch
+
+import weight_streaming_q4_gb300 as q4
+from weight_streaming_q4_gb300 import build, model, synth
+from gpu_util import dev_u16, host_u16
+
+pytestmark = pytest.mark.gpu
+
+TINY = dict(hidden=256, q_dim=256, kv_dim=128, ffn=1024, head_dim=64)
+SMALL = dict(hidden=2048, q_dim=2048, kv_dim=512, ffn=4096, head_dim=128)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+
+
+class Ring:
+    def __init__(self, cfg, n_layers, seed, flags=0, distinct=None):
+        self.shape = q4.LayerShape.of(**cfg)
+        self.blocks, self.hptrs = model.host_layers(self.shape, n_layers, seed, distinct=distinct)
+        stride = model.layer_stride(self.shape)
+        self.bufs = [torch.empty(stride, dtype=torch.uint8, device="cuda") for _ in range(2)]
+        self.ws, self.offs, self.ws_bytes = model.workspace(self.shape, 2, 1)
+        self.h = q4.q4_stream_create(self.shape, self.hptrs, 1, self.bufs[0], self.bufs[1], stride, self.ws,
+                                     self.ws_bytes, flags)
+
+    def run(self, h_np, tokens=1, timeout_us=0):
+        h = dev_u16(h_np.reshape(-1))
+        for _ in range(tokens):
+            q4.q4_stream_layers(self.h, h, timeout_us=timeout_us)
+        torch.cuda.synchronize()
+        assert q4.q4_stream_status(self.h) == 0
+        return host_u16(h).reshape(1, -1)
+
+    def close(self):
+        q4.q4_stream_destroy(self.h)
+
+
+def resident(cfg, n_layers, seed, h_np, tokens=1):
+    shape = q4.LayerShape.of(**cfg)
+    wbuf, ptrs = model.resident_layers(shape, n_layers, seed)
+    ws, offs, nb = model.workspace(shape, n_layers, 1)
+    dec = q4.q4_decoder_create(shape, ptrs, 1, ws, nb, q4.Q4_DEC_PER_LAYER)
+    h = dev_u16(h_np.reshape(-1))
+    for _ in range(tokens):
+        q4.q4_layer_decode(dec, h)
+    torch.cuda.synchronize()
+    q4.q4_decoder_destroy(dec)
+    return host_u16(h).reshape(1, -1)
+
+
+@pytest.mark.parametrize("cfg,n_layers", [(TINY, 5), (SMALL, 4)], ids=["tiny5", "small4"])
+@pytest.mark.parametrize("flags", [0, q4.Q4_STREAM_POISON], ids=["plain", "poison"])
+def test_streamed_equals_resident(cfg, n_layers, flags):
+    h0 = synth.activations(1, cfg["hidden"], 50)
+    ring = Ring(cfg, n_layers, seed=51, flags=flags)
+    got = ring.run(h0, tokens=2)
+    ref = resident(cfg, n_layers, 51, h0, tokens=2)
+    assert np.array_equal(got, ref)
+    assert np.all(np.isfinite(got.view(np.float16).astype(np.float64)))
+    ring.close()
+
+
+def test_streamed_70b_layers_equal_resident():
+    cfg = dict(synth.LLAMA_70B)
+    cfg.pop("n_layers")
+    h0 = synth.activations(1, cfg["hidden"], 60)
+    ring = Ring(cfg, 3, seed=61, flags=q4.Q4_STREAM_POISON)
+    got = ring.run(h0)
+    ref = resident(cfg, 3, 61, h0)
+    assert np.array_equal(got, ref)
+    ring.close()
+
+
+def test_host_timeout_returns_and_work_completes():
+    cfg = SMALL
+    ring = Ring(cfg, 6, seed=70)
+    h = dev_u16(synth.activations(1, cfg["hidden"], 71).reshape(-1))
+    with pytest.raises(q4.Q4Error) as e:
+        q4.q4_stream_layers(ring.h, h, timeout_us=1)
+    assert e.value.status == q4.Q4_ERR_TIMEOUT
+    torch.cuda.synchronize()                     # the queued work still finishes
+    assert q4.q4_stream_status(ring.h) == 0
+    ring.close()

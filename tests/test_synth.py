@@ -41,6 +41,6 @@ def test_layer_block_layout():
     blk = synth.layer_block(2, 256, 256, 128, 768, seed=3)
     assert blk.size == total
     for p, (n, k) in enumerate(dims):
-        assert offs[p] % 256 == 0
+        assert offs[p] % 16 == 0
         m = synth.q4_matrix(n, k, 3, synth.tensor_id(2, p))
         assert np.array_equal(blk[offs[p]:offs[p] + m.size], m)

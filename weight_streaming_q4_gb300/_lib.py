@@ -1,0 +1,233 @@
+"""ctypes binding of libq4.so with the C ABI's own names (include/q4.h).
+
+Argument marshalling only: tensors become their data pointers, streams their
+cudaStream_t handles, and a negative status becomes a Q4Error.  Every step of
+the computation runs in the library's CUDA kernels; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+from . import build as _build
+
+_lib = None
+
+c_p = ctypes.c_void_p
+c_int = ctypes.c_int
+c_size = ctypes.c_size_t
+c_i64 = ctypes.c_int64
+
+Q4_OK = 0
+Q4_ERR_ARG = -1
+Q4_ERR_ALIGN = -2
+Q4_ERR_CUDA = -3
+Q4_ERR_TIMEOUT = -4
+Q4_ERR_OOM = -5
+Q4_ERR_DEVICE = -6
+
+Q4_KERNEL_AUTO = 0
+Q4_KERNEL_STREAM = 1
+Q4_KERNEL_SIMPLE = 2
+Q4_KERNEL_MMA = 3
+
+Q4_DEC_FUSED = 0
+Q4_DEC_PER_LAYER = 1
+Q4_STREAM_POISON = 1
+
+WS_NAMES = ("control", "program", "qkv", "o", "gate", "up", "down", "act", "x", "attn", "x2", "hmid")
+WS_COUNT = len(WS_NAMES)
+
+
+class Q4Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        msg = status_string(status) if _lib is not None else str(status)
+        extra = ""
+        if status == Q4_ERR_CUDA and _lib is not None:
+            extra = f" (cudaError {_lib.q4_last_cuda_error()})"
+        super().__init__(f"{what}: {msg}{extra}")
+
+
+class LayerShape(ctypes.Structure):
+    """q4_layer_shape."""
+    _fields_ = [("hidden", c_int), ("q_dim", c_int), ("kv_dim", c_int), ("ffn", c_int),
+                ("head_dim", c_int), ("eps", ctypes.c_float)]
+
+    @classmethod
+    def of(cls, hidden, q_dim, kv_dim, ffn, head_dim=128, eps=1e-5, **_):
+        return cls(hidden, q_dim, kv_dim, ffn, head_dim, eps)
+
+
+def _declare(lib):
+    sig = {
+        "q4_status_string": ([c_int], ctypes.c_char_p),
+        "q4_last_cuda_error": ([], c_int),
+        "q4_version": ([], c_int),
+        "q4_matrix_bytes": ([c_int, c_int], c_size),
+        "q4_gemv": ([c_p, c_p, c_p, c_int, c_int, c_int, c_p], c_int),
+        "q4_gemv_ex": ([c_p, c_p, c_p, c_int, c_int, c_int, c_int, c_p], c_int),
+        "q4_device_status": ([], c_int),
+        "q4_dequant_debug": ([c_p, c_p, c_int, c_int, c_p], c_int),
+        "q4_layer_offsets": ([ctypes.POINTER(LayerShape), ctypes.POINTER(c_size), ctypes.POINTER(c_size)], c_int),
+        "q4_workspace_layout": ([ctypes.POINTER(LayerShape), c_int, c_int, ctypes.POINTER(c_size),
+                                 ctypes.POINTER(c_size)], c_int),
+        "q4_decoder_create": ([ctypes.POINTER(c_p), ctypes.POINTER(LayerShape), ctypes.POINTER(c_p), c_int, c_int,
+                               c_p, c_size, c_int, c_p], c_int),
+        "q4_layer_decode": ([c_p, c_p, c_p], c_int),
+        "q4_layer_decode_eager": ([c_p, c_p, c_p], c_int),
+        "q4_decoder_status": ([c_p, c_p, ctypes.POINTER(c_int)], c_int),
+        "q4_decoder_destroy": ([c_p], c_int),
+        "q4_stream_create": ([ctypes.POINTER(c_p), ctypes.POINTER(LayerShape), ctypes.POINTER(c_p), c_int, c_int,
+                              c_p, c_p, c_size, c_p, c_size, c_int], c_int),
+        "q4_stream_layers": ([c_p, c_p, c_p, c_i64], c_int),
+        "q4_stream_status": ([c_p, c_p, ctypes.POINTER(c_int)], c_int),
+        "q4_stream_destroy": ([c_p], c_int),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+    return lib
+
+
+def lib():
+    """The loaded libq4.so; raises if it has not been built (no fallback exists)."""
+    global _lib
+    if _lib is None:
+        path = _build.lib_path("libq4.so")
+        if not os.path.exists(path):
+            raise ImportError(f"libq4.so is not built ({path}); run weight_streaming_q4_gb300.build.build()")
+        _lib = _declare(ctypes.CDLL(path))
+    return _lib
+
+
+def header_functions() -> list:
+    """Names of the functions include/q4.h declares."""
+    text = open(os.path.join(_build.INCLUDE, "q4.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(q4_[a-z0-9_]+)\s*\(", text)))
+
+
+# ------------------------------------------------------------------ marshalling
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(st: int, what: str):
+    if st < 0:
+        raise Q4Error(st, what)
+    return st
+
+
+def status_string(st: int) -> str:
+    return lib().q4_status_string(st).decode()
+
+
+def q4_last_cuda_error() -> int:
+    return lib().q4_last_cuda_error()
+
+
+def q4_version() -> int:
+    return lib().q4_version()
+
+
+def q4_matrix_bytes(n: int, k: int) -> int:
+    return lib().q4_matrix_bytes(n, k)
+
+
+def q4_gemv(w, x, y, n: int, k: int, batch: int = 1, stream=None):
+    _check(lib().q4_gemv(_ptr(w), _ptr(x), _ptr(y), n, k, batch, _stream(stream)), "q4_gemv")
+
+
+def q4_gemv_ex(w, x, y, n: int, k: int, batch: int, kernel: int, stream=None):
+    _check(lib().q4_gemv_ex(_ptr(w), _ptr(x), _ptr(y), n, k, batch, kernel, _stream(stream)), "q4_gemv_ex")
+
+
+def q4_device_status() -> int:
+    return _check(lib().q4_device_status(), "q4_device_status")
+
+
+def q4_dequant_debug(w, out, n: int, k: int, stream=None):
+    _check(lib().q4_dequant_debug(_ptr(w), _ptr(out), n, k, _stream(stream)), "q4_dequant_debug")
+
+
+def q4_layer_offsets(shape: LayerShape):
+    offs = (c_size * 7)()
+    total = c_size(0)
+    _check(lib().q4_layer_offsets(ctypes.byref(shape), offs, ctypes.byref(total)), "q4_layer_offsets")
+    return list(offs), total.value
+
+
+def q4_workspace_layout(shape: LayerShape, n_layers: int, batch: int):
+    offs = (c_size * WS_COUNT)()
+    total = c_size(0)
+    _check(lib().q4_workspace_layout(ctypes.byref(shape), n_layers, batch, offs, ctypes.byref(total)),
+           "q4_workspace_layout")
+    return dict(zip(WS_NAMES, list(offs))), total.value
+
+
+def q4_decoder_create(shape: LayerShape, layer_ptrs, batch: int, workspace, workspace_bytes: int,
+                      mode: int = Q4_DEC_FUSED, stream=None):
+    h = c_p()
+    arr = (c_p * len(layer_ptrs))(*[int(p) for p in layer_ptrs])
+    _check(lib().q4_decoder_create(ctypes.byref(h), ctypes.byref(shape), arr, len(layer_ptrs), batch,
+                                   _ptr(workspace), workspace_bytes, mode, _stream(stream)), "q4_decoder_create")
+    return h
+
+
+def q4_layer_decode(dec, hidden, stream=None):
+    _check(lib().q4_layer_decode(dec, _ptr(hidden), _stream(stream)), "q4_layer_decode")
+
+
+def q4_layer_decode_eager(dec, hidden, stream=None):
+    _check(lib().q4_layer_decode_eager(dec, _ptr(hidden), _stream(stream)), "q4_layer_decode_eager")
+
+
+def q4_decoder_status(dec, stream=None) -> int:
+    v = c_int(0)
+    _check(lib().q4_decoder_status(dec, _stream(stream), ctypes.byref(v)), "q4_decoder_status")
+    return v.value
+
+
+def q4_decoder_destroy(dec):
+    _check(lib().q4_decoder_destroy(dec), "q4_decoder_destroy")
+
+
+def q4_stream_create(shape: LayerShape, host_ptrs, batch: int, buf0, buf1, buf_bytes: int, workspace,
+                     workspace_bytes: int, flags: int = 0):
+    h = c_p()
+    arr = (c_p * len(host_ptrs))(*[int(p) for p in host_ptrs])
+    _check(lib().q4_stream_create(ctypes.byref(h), ctypes.byref(shape), arr, len(host_ptrs), batch, _ptr(buf0),
+                                  _ptr(buf1), buf_bytes, _ptr(workspace), workspace_bytes, flags),
+           "q4_stream_create")
+    return h
+
+
+def q4_stream_layers(st, hidden, stream=None, timeout_us: int = 0):
+    return _check(lib().q4_stream_layers(st, _ptr(hidden), _stream(stream), timeout_us), "q4_stream_layers")
+
+
+def q4_stream_status(st, stream=None) -> int:
+    v = c_int(0)
+    _check(lib().q4_stream_status(st, _stream(stream), ctypes.byref(v)), "q4_stream_status")
+    return v.value
+
+
+def q4_stream_destroy(st):
+    _check(lib().q4_stream_destroy(st), "q4_stream_destroy")

@@ -1,0 +1,614 @@
+// C ABI of libq4.so (declared in include/q4.h): argument checks, launch
+// configuration, the decoder (phase programs + CUDA-graph capture) and the
+// double-buffered copy/compute ring.  Host code only; every arithmetic step
+// of the decode runs in the kernels of q4_engine.cu and q4_aux.cu.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <atomic>
+#include <chrono>
+#include <mutex>
+#include <thread>
+#include <vector>
+
+#include "q4.h"
+#include "q4_device.cuh"
+
+using q4::Control;
+using q4::EngineArgs;
+using q4::Phase;
+
+namespace {
+
+std::atomic<int> g_last_cuda{0};
+
+int cuda_fail(cudaError_t e) {
+  g_last_cuda.store(static_cast<int>(e));
+  return Q4_ERR_CUDA;
+}
+
+#define Q4_CUDA(call)                              \
+  do {                                             \
+    cudaError_t e_ = (call);                       \
+    if (e_ != cudaSuccess) return cuda_fail(e_);   \
+  } while (0)
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Wait limit of one in-kernel wait, in polls (a poll suspends for tens to
+// hundreds of nanoseconds): about a second, far above any legitimate wait.
+constexpr uint32_t kWaitLimit = 1u << 22;
+
+struct DeviceInfo {
+  bool ready = false;
+  int sm_count = 0;
+  int engine_blocks_per_sm = 0;
+};
+
+std::mutex g_dev_mutex;
+DeviceInfo g_dev[64];
+
+int device_info(DeviceInfo** out) {
+  int dev = 0;
+  Q4_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return Q4_ERR_ARG;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    Q4_CUDA(cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev));
+    Q4_CUDA(q4::engine_prepare());
+    Q4_CUDA(q4::engine_occupancy(&d.engine_blocks_per_sm));
+    if (d.engine_blocks_per_sm < 1) return Q4_ERR_CUDA;
+    d.ready = true;
+  }
+  *out = &d;
+  return Q4_OK;
+}
+
+// Columns per consumer thread for the streaming engine, or 0 if the engine
+// cannot run rows of this width (then the plain kernel is used).
+int engine_kt(int k, bool dual) {
+  if (k < 256 || k % 256 != 0) return 0;   // rows must start 16-byte aligned
+  if (k <= 16384) {
+    const int team = k / 64;
+    if (team % 32 == 0 || 32 % team == 0) return 64;
+    return 0;
+  }
+  if (!dual && k <= 32768 && k % 4096 == 0) return 128;
+  return 0;
+}
+
+// Fill the tiling fields of a phase (kt, rows per unit, units).
+bool tile_phase(Phase& ph) {
+  const bool dual = ph.epi_kind == q4::EPI_SILU;
+  const int kt = engine_kt(ph.k, dual);
+  if (kt == 0) return false;
+  const int team = ph.k / kt;
+  const int teams = q4::kConsumerThreads / team;
+  const int rpt = kt == 64 ? 2 : 1;
+  ph.kt = kt;
+  ph.rows_per_unit = dual ? teams : teams * rpt;
+  ph.units = (ph.n_rows + ph.rows_per_unit - 1) / ph.rows_per_unit;
+  return true;
+}
+
+}  // namespace
+
+// ===================================================================== misc
+
+extern "C" const char* q4_status_string(int s) {
+  switch (s) {
+    case Q4_OK: return "ok";
+    case Q4_ERR_ARG: return "invalid argument";
+    case Q4_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case Q4_ERR_CUDA: return "CUDA runtime error";
+    case Q4_ERR_TIMEOUT: return "timed out";
+    case Q4_ERR_OOM: return "workspace too small";
+    case Q4_ERR_DEVICE: return "a kernel wait failed";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int q4_last_cuda_error(void) { return g_last_cuda.exchange(0); }
+
+extern "C" int q4_version(void) { return 100; }
+
+extern "C" size_t q4_matrix_bytes(int n, int k) {
+  if (n <= 0 || k <= 0 || k % q4::kQK) return 0;
+  return static_cast<size_t>(n) * (k / q4::kQK) * q4::kBlockBytes;
+}
+
+// ===================================================================== one product
+
+static int check_gemv(const void* w, const uint16_t* x, const float* y, int n, int k, int batch) {
+  if (!w || !x || !y) return Q4_ERR_ARG;
+  if (n < 1 || k < q4::kQK || k % q4::kQK || batch < 1 || batch > q4::kMaxBatch) return Q4_ERR_ARG;
+  if (!aligned(w, 16) || !aligned(x, 16) || !aligned(y, 16)) return Q4_ERR_ALIGN;
+  return Q4_OK;
+}
+
+extern "C" int q4_gemv_ex(const void* w, const uint16_t* x, float* y, int n, int k, int batch, int kernel,
+                          void* stream) {
+  int st = check_gemv(w, x, y, n, k, batch);
+  if (st != Q4_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (kernel == Q4_KERNEL_AUTO) kernel = (batch == 1 && engine_kt(k, false)) ? Q4_KERNEL_STREAM : Q4_KERNEL_SIMPLE;
+  if (kernel == Q4_KERNEL_SIMPLE) {
+    Q4_CUDA(q4::simple_launch(static_cast<const uint8_t*>(w), x, y, n, k, batch, s));
+    return Q4_OK;
+  }
+  if (kernel != Q4_KERNEL_STREAM || batch != 1 || !engine_kt(k, false)) return Q4_ERR_ARG;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != Q4_OK) return st;
+  EngineArgs a;
+  memset(&a, 0, sizeof(a));
+  Phase& ph = a.one;
+  ph.w0 = static_cast<const uint8_t*>(w);
+  ph.x_src = x;
+  ph.y = y;
+  ph.n_rows = n;
+  ph.k = k;
+  ph.x_kind = q4::X_F16;
+  ph.epi_kind = q4::EPI_F32;
+  ph.x_ld = k;
+  if (!tile_phase(ph)) return Q4_ERR_ARG;
+  a.phases = nullptr;
+  a.n_phases = 1;
+  a.ctl = nullptr;
+  a.wait_limit = kWaitLimit;
+  const int grid = ph.units < dev->sm_count ? ph.units : dev->sm_count;
+  Q4_CUDA(q4::engine_launch(a, grid, false, s));
+  return Q4_OK;
+}
+
+extern "C" int q4_gemv(const void* w, const uint16_t* x, float* y, int n, int k, int batch, void* stream) {
+  return q4_gemv_ex(w, x, y, n, k, batch, Q4_KERNEL_AUTO, stream);
+}
+
+extern "C" int q4_device_status(void) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return cuda_fail(cudaGetLastError());
+  int v = 0;
+  Q4_CUDA(q4::engine_read_status(&v));
+  return v;
+}
+
+extern "C" int q4_dequant_debug(const void* w, float* w_out, int n, int k, void* stream) {
+  if (!w || !w_out || n < 1 || k < q4::kQK || k % q4::kQK) return Q4_ERR_ARG;
+  if (!aligned(w, 16) || !aligned(w_out, 16)) return Q4_ERR_ALIGN;
+  Q4_CUDA(q4::dequant_launch(static_cast<const uint8_t*>(w), w_out, n, k, static_cast<cudaStream_t>(stream)));
+  return Q4_OK;
+}
+
+// ===================================================================== layers
+
+static bool shape_ok(const q4_layer_shape* s) {
+  if (!s) return false;
+  if (s->hidden < 32 || s->q_dim < 32 || s->kv_dim < 32 || s->ffn < 32 || s->head_dim < 1) return false;
+  if (s->hidden % 32 || s->q_dim % 32 || s->kv_dim % 32 || s->ffn % 32) return false;
+  if (s->q_dim % s->head_dim || s->kv_dim % s->head_dim) return false;
+  if ((s->q_dim / s->head_dim) % (s->kv_dim / s->head_dim)) return false;
+  return s->eps >= 0.f;
+}
+
+extern "C" int q4_layer_offsets(const q4_layer_shape* s, size_t offsets[7], size_t* layer_bytes) {
+  if (!shape_ok(s) || !offsets) return Q4_ERR_ARG;
+  const int dims[7][2] = {{s->q_dim, s->hidden}, {s->kv_dim, s->hidden}, {s->kv_dim, s->hidden},
+                          {s->hidden, s->q_dim}, {s->ffn, s->hidden},    {s->ffn, s->hidden},
+                          {s->hidden, s->ffn}};
+  size_t pos = 0;
+  for (int p = 0; p < 7; ++p) {
+    offsets[p] = pos;
+    pos += q4_matrix_bytes(dims[p][0], dims[p][1]);
+  }
+  if (layer_bytes) *layer_bytes = pos;
+  return Q4_OK;
+}
+
+extern "C" int q4_workspace_layout(const q4_layer_shape* s, int n_layers, int batch, size_t offsets[Q4_WS_COUNT],
+                                   size_t* total_bytes) {
+  if (!shape_ok(s) || n_layers < 1 || batch < 1 || batch > q4::kMaxBatch || !offsets) return Q4_ERR_ARG;
+  const size_t B = static_cast<size_t>(batch);
+  const size_t sizes[Q4_WS_COUNT] = {
+      sizeof(Control),
+      sizeof(Phase) * 4 * static_cast<size_t>(n_layers),
+      4 * B * (s->q_dim + 2 * s->kv_dim),
+      4 * B * s->hidden,
+      4 * B * s->ffn,
+      4 * B * s->ffn,
+      4 * B * s->hidden,
+      2 * B * s->ffn,
+      2 * B * s->hidden,
+      2 * B * s->q_dim,
+      2 * B * s->hidden,
+      2 * B * s->hidden,
+  };
+  size_t pos = 0;
+  for (int i = 0; i < Q4_WS_COUNT; ++i) {
+    offsets[i] = pos;
+    pos += (sizes[i] + 255) / 256 * 256;
+  }
+  if (total_bytes) *total_bytes = pos;
+  return Q4_OK;
+}
+
+namespace {
+
+// Pointers into a workspace.
+struct Work {
+  Control* ctl;
+  Phase* prog;
+  float *qkv, *o, *g, *u, *dn;
+  uint16_t *act, *x, *attn, *x2, *hmid;
+};
+
+Work carve(void* ws, const size_t* off) {
+  char* b = static_cast<char*>(ws);
+  Work w;
+  w.ctl = reinterpret_cast<Control*>(b + off[Q4_WS_CONTROL]);
+  w.prog = reinterpret_cast<Phase*>(b + off[Q4_WS_PROGRAM]);
+  w.qkv = reinterpret_cast<float*>(b + off[Q4_WS_QKV]);
+  w.o = reinterpret_cast<float*>(b + off[Q4_WS_O]);
+  w.g = reinterpret_cast<float*>(b + off[Q4_WS_GATE]);
+  w.u = reinterpret_cast<float*>(b + off[Q4_WS_UP]);
+  w.dn = reinterpret_cast<float*>(b + off[Q4_WS_DOWN]);
+  w.act = reinterpret_cast<uint16_t*>(b + off[Q4_WS_ACT]);
+  w.x = reinterpret_cast<uint16_t*>(b + off[Q4_WS_X]);
+  w.attn = reinterpret_cast<uint16_t*>(b + off[Q4_WS_ATTN]);
+  w.x2 = reinterpret_cast<uint16_t*>(b + off[Q4_WS_X2]);
+  w.hmid = reinterpret_cast<uint16_t*>(b + off[Q4_WS_HMID]);
+  return w;
+}
+
+// The four phases of one decoder layer whose merged weight block is `wl`
+// (PIPO summary, "Offloading architecture": the layer is the unit).
+bool layer_phases(const q4_layer_shape& s, const uint8_t* wl, uint16_t* h, const Work& w, Phase out[4]) {
+  size_t off[7];
+  if (q4_layer_offsets(&s, off, nullptr) != Q4_OK) return false;
+  memset(out, 0, 4 * sizeof(Phase));
+  // q, k, v: one matrix of q_dim + 2 kv_dim rows (they are consecutive in the block)
+  Phase& a = out[0];
+  a.w0 = wl + off[Q4_PROJ_Q];
+  a.x_src = h;
+  a.y = w.qkv;
+  a.n_rows = s.q_dim + 2 * s.kv_dim;
+  a.k = s.hidden;
+  a.x_kind = q4::X_RMSNORM;
+  a.epi_kind = q4::EPI_F32;
+  a.x_ld = s.hidden;
+  a.eps = s.eps;
+  a.x_dbg = w.x;
+  // o, with the context-1 attention as its input and the residual add as its output
+  Phase& b = out[1];
+  b.w0 = wl + off[Q4_PROJ_O];
+  b.x_src = w.qkv;
+  b.y = w.o;
+  b.h = h;
+  b.aux16 = w.hmid;
+  b.n_rows = s.hidden;
+  b.k = s.q_dim;
+  b.x_kind = q4::X_ATTN;
+  b.epi_kind = q4::EPI_RESID;
+  b.x_ld = s.q_dim + 2 * s.kv_dim;
+  b.attn_off = s.q_dim + s.kv_dim;
+  b.head_dim = s.head_dim;
+  b.group = (s.q_dim / s.head_dim) / (s.kv_dim / s.head_dim);
+  b.x_dbg = w.attn;
+  // gate and up together, SiLU-gated product as the output
+  Phase& c = out[2];
+  c.w0 = wl + off[Q4_PROJ_GATE];
+  c.w1 = wl + off[Q4_PROJ_UP];
+  c.x_src = h;
+  c.y = w.g;
+  c.y2 = w.u;
+  c.aux16 = w.act;
+  c.n_rows = s.ffn;
+  c.k = s.hidden;
+  c.x_kind = q4::X_RMSNORM;
+  c.epi_kind = q4::EPI_SILU;
+  c.x_ld = s.hidden;
+  c.eps = s.eps;
+  c.x_dbg = w.x2;
+  // down, with the residual add
+  Phase& d = out[3];
+  d.w0 = wl + off[Q4_PROJ_DOWN];
+  d.x_src = w.act;
+  d.y = w.dn;
+  d.h = h;
+  d.n_rows = s.hidden;
+  d.k = s.ffn;
+  d.x_kind = q4::X_F16;
+  d.epi_kind = q4::EPI_RESID;
+  d.x_ld = s.ffn;
+  for (int i = 0; i < 4; ++i)
+    if (!tile_phase(out[i])) return false;
+  return true;
+}
+
+int check_layer_shape_for_engine(const q4_layer_shape& s) {
+  Phase tmp[4];
+  Work w;
+  memset(&w, 0, sizeof(w));
+  return layer_phases(s, nullptr, nullptr, w, tmp) ? Q4_OK : Q4_ERR_ARG;
+}
+
+int launch_layers(const Work& w, int first_phase, int n_phases, int grid, cudaStream_t s) {
+  EngineArgs a;
+  memset(&a, 0, sizeof(a));
+  a.phases = w.prog + first_phase;
+  a.n_phases = n_phases;
+  a.ctl = w.ctl;
+  a.wait_limit = kWaitLimit;
+  Q4_CUDA(q4::engine_launch(a, grid, true, s));
+  return Q4_OK;
+}
+
+int read_status(Control* ctl, cudaStream_t s, int* out) {
+  int v = 0;
+  Q4_CUDA(cudaMemcpyAsync(&v, &ctl->status, sizeof(int), cudaMemcpyDeviceToHost, s));
+  Q4_CUDA(cudaStreamSynchronize(s));
+  if (v) Q4_CUDA(cudaMemsetAsync(&ctl->status, 0, sizeof(int), s));
+  Q4_CUDA(cudaStreamSynchronize(s));
+  *out = v;
+  return Q4_OK;
+}
+
+}  // namespace
+
+struct q4_decoder {
+  q4_layer_shape shape;
+  int n_layers = 0, batch = 1, mode = Q4_DEC_FUSED, grid = 0;
+  std::vector<const uint8_t*> layers;
+  Work w;
+  uint16_t* cur_h = nullptr;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+};
+
+static int decoder_write_program(q4_decoder* d, uint16_t* h, cudaStream_t s) {
+  std::vector<Phase> prog(4 * static_cast<size_t>(d->n_layers));
+  for (int l = 0; l < d->n_layers; ++l)
+    if (!layer_phases(d->shape, d->layers[l], h, d->w, &prog[4 * l])) return Q4_ERR_ARG;
+  // pageable source: the runtime stages it before returning, so `prog` may go
+  Q4_CUDA(cudaMemcpyAsync(d->w.prog, prog.data(), prog.size() * sizeof(Phase), cudaMemcpyHostToDevice, s));
+  d->cur_h = h;
+  return Q4_OK;
+}
+
+static int decoder_enqueue(q4_decoder* d, cudaStream_t s) {
+  if (d->mode == Q4_DEC_FUSED) return launch_layers(d->w, 0, 4 * d->n_layers, d->grid, s);
+  for (int l = 0; l < d->n_layers; ++l) {
+    int st = launch_layers(d->w, 4 * l, 4, d->grid, s);
+    if (st != Q4_OK) return st;
+  }
+  return Q4_OK;
+}
+
+extern "C" int q4_decoder_create(q4_decoder** out, const q4_layer_shape* shape, const void* const* layer_weights,
+                                 int n_layers, int batch, void* workspace, size_t workspace_bytes, int mode,
+                                 void* stream) {
+  if (!out || !shape_ok(shape) || !layer_weights || n_layers < 1 || !workspace) return Q4_ERR_ARG;
+  if (batch != 1) return Q4_ERR_ARG;   // the persistent engine's exact CUDA-core path is batch 1
+  if (mode != Q4_DEC_FUSED && mode != Q4_DEC_PER_LAYER) return Q4_ERR_ARG;
+  if (check_layer_shape_for_engine(*shape) != Q4_OK) return Q4_ERR_ARG;
+  if (!aligned(workspace, 256)) return Q4_ERR_ALIGN;
+  for (int l = 0; l < n_layers; ++l) {
+    if (!layer_weights[l]) return Q4_ERR_ARG;
+    if (!aligned(layer_weights[l], 256)) return Q4_ERR_ALIGN;
+  }
+  size_t off[Q4_WS_COUNT], need = 0;
+  int st = q4_workspace_layout(shape, n_layers, batch, off, &need);
+  if (st != Q4_OK) return st;
+  if (workspace_bytes < need) return Q4_ERR_OOM;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != Q4_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  q4_decoder* d = new q4_decoder();
+  d->shape = *shape;
+  d->n_layers = n_layers;
+  d->batch = batch;
+  d->mode = mode;
+  d->grid = dev->sm_count;   // one persistent CTA per SM (co-resident: cooperative launch)
+  d->layers.assign(reinterpret_cast<const uint8_t* const*>(layer_weights),
+                   reinterpret_cast<const uint8_t* const*>(layer_weights) + n_layers);
+  d->w = carve(workspace, off);
+  cudaError_t e = cudaMemsetAsync(workspace, 0, need, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) {
+    delete d;
+    return cuda_fail(e);
+  }
+  *out = d;
+  return Q4_OK;
+}
+
+static int decoder_capture(q4_decoder* d) {
+  cudaStream_t cap = nullptr;
+  Q4_CUDA(cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking));
+  cudaError_t e = cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal);
+  int st = Q4_OK;
+  if (e == cudaSuccess) {
+    st = decoder_enqueue(d, cap);
+    cudaGraph_t g = nullptr;
+    e = cudaStreamEndCapture(cap, &g);
+    if (e == cudaSuccess && st == Q4_OK) {
+      d->graph = g;
+      e = cudaGraphInstantiateWithFlags(&d->exec, g, 0);
+    } else if (g) {
+      cudaGraphDestroy(g);
+    }
+  }
+  cudaStreamDestroy(cap);
+  if (st != Q4_OK) return st;
+  if (e != cudaSuccess) return cuda_fail(e);
+  return Q4_OK;
+}
+
+static int decoder_prepare(q4_decoder* d, uint16_t* h, cudaStream_t s) {
+  if (!d || !h) return Q4_ERR_ARG;
+  if (!aligned(h, 16)) return Q4_ERR_ALIGN;
+  if (h != d->cur_h) {
+    int st = decoder_write_program(d, h, s);
+    if (st != Q4_OK) return st;
+  }
+  return Q4_OK;
+}
+
+extern "C" int q4_layer_decode(q4_decoder* d, uint16_t* hidden_io, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int st = decoder_prepare(d, hidden_io, s);
+  if (st != Q4_OK) return st;
+  if (!d->exec && (st = decoder_capture(d)) != Q4_OK) return st;
+  Q4_CUDA(cudaGraphLaunch(d->exec, s));
+  return Q4_OK;
+}
+
+extern "C" int q4_layer_decode_eager(q4_decoder* d, uint16_t* hidden_io, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int st = decoder_prepare(d, hidden_io, s);
+  if (st != Q4_OK) return st;
+  return decoder_enqueue(d, s);
+}
+
+extern "C" int q4_decoder_status(q4_decoder* d, void* stream, int* status_out) {
+  if (!d || !status_out) return Q4_ERR_ARG;
+  return read_status(d->w.ctl, static_cast<cudaStream_t>(stream), status_out);
+}
+
+extern "C" int q4_decoder_destroy(q4_decoder* d) {
+  if (!d) return Q4_OK;
+  if (d->exec) cudaGraphExecDestroy(d->exec);
+  if (d->graph) cudaGraphDestroy(d->graph);
+  delete d;
+  return Q4_OK;
+}
+
+// ===================================================================== streamed layers
+
+struct q4_stream {
+  q4_layer_shape shape;
+  int n_layers = 0, batch = 1, flags = 0, grid = 0;
+  std::vector<const void*> host;
+  uint8_t* buf[2] = {nullptr, nullptr};
+  size_t layer_bytes = 0;
+  Work w;
+  uint16_t* cur_h = nullptr;
+  cudaStream_t copy = nullptr;
+  cudaEvent_t loaded[2] = {nullptr, nullptr}, freed[2] = {nullptr, nullptr};
+  cudaEvent_t start = nullptr, done = nullptr;
+};
+
+extern "C" int q4_stream_create(q4_stream** out, const q4_layer_shape* shape, const void* const* host_layers,
+                                int n_layers, int batch, void* dev_buf0, void* dev_buf1, size_t buf_bytes,
+                                void* workspace, size_t workspace_bytes, int flags) {
+  if (!out || !shape_ok(shape) || !host_layers || n_layers < 1 || !dev_buf0 || !dev_buf1 || !workspace)
+    return Q4_ERR_ARG;
+  if (batch != 1 || (flags & ~Q4_STREAM_POISON)) return Q4_ERR_ARG;
+  if (check_layer_shape_for_engine(*shape) != Q4_OK) return Q4_ERR_ARG;
+  if (!aligned(dev_buf0, 256) || !aligned(dev_buf1, 256) || !aligned(workspace, 256)) return Q4_ERR_ALIGN;
+  size_t lo[7], layer_bytes = 0;
+  q4_layer_offsets(shape, lo, &layer_bytes);
+  if (buf_bytes < layer_bytes) return Q4_ERR_OOM;
+  for (int l = 0; l < n_layers; ++l) {
+    if (!host_layers[l]) return Q4_ERR_ARG;
+    if (!aligned(host_layers[l], 16)) return Q4_ERR_ALIGN;
+  }
+  size_t off[Q4_WS_COUNT], need = 0;
+  int st = q4_workspace_layout(shape, 2, batch, off, &need);
+  if (st != Q4_OK) return st;
+  if (workspace_bytes < need) return Q4_ERR_OOM;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != Q4_OK) return st;
+
+  q4_stream* r = new q4_stream();
+  r->shape = *shape;
+  r->n_layers = n_layers;
+  r->batch = batch;
+  r->flags = flags;
+  r->grid = dev->sm_count;
+  r->host.assign(host_layers, host_layers + n_layers);
+  r->buf[0] = static_cast<uint8_t*>(dev_buf0);
+  r->buf[1] = static_cast<uint8_t*>(dev_buf1);
+  r->layer_bytes = layer_bytes;
+  r->w = carve(workspace, off);
+  cudaError_t e = cudaStreamCreateWithFlags(&r->copy, cudaStreamNonBlocking);
+  for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+    e = cudaEventCreateWithFlags(&r->loaded[i], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&r->freed[i], cudaEventDisableTiming);
+  }
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&r->start, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&r->done, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaMemset(workspace, 0, need);
+  if (e != cudaSuccess) {
+    q4_stream_destroy(r);
+    return cuda_fail(e);
+  }
+  *out = r;
+  return Q4_OK;
+}
+
+extern "C" int q4_stream_layers(q4_stream* r, uint16_t* hidden_io, void* compute_stream, int64_t timeout_us) {
+  if (!r || !hidden_io) return Q4_ERR_ARG;
+  if (!aligned(hidden_io, 16)) return Q4_ERR_ALIGN;
+  cudaStream_t cs = static_cast<cudaStream_t>(compute_stream);
+  if (hidden_io != r->cur_h) {
+    // one 4-phase program per staging buffer, both reading/writing hidden_io
+    std::vector<Phase> prog(8);
+    for (int b = 0; b < 2; ++b)
+      if (!layer_phases(r->shape, r->buf[b], hidden_io, r->w, &prog[4 * b])) return Q4_ERR_ARG;
+    Q4_CUDA(cudaMemcpyAsync(r->w.prog, prog.data(), prog.size() * sizeof(Phase), cudaMemcpyHostToDevice, cs));
+    r->cur_h = hidden_io;
+  }
+  // The copy stream may only overwrite a buffer once everything queued on the
+  // compute stream before this call (earlier tokens) has finished with it.
+  Q4_CUDA(cudaEventRecord(r->start, cs));
+  Q4_CUDA(cudaStreamWaitEvent(r->copy, r->start, 0));
+  const size_t n_blocks = r->layer_bytes / q4::kBlockBytes;
+  for (int i = 0; i < r->n_layers; ++i) {
+    const int b = i & 1;
+    // copy stream: layer i into buffer b once layer i-2 has released it
+    if (i >= 2) Q4_CUDA(cudaStreamWaitEvent(r->copy, r->freed[b], 0));
+    Q4_CUDA(cudaMemcpyAsync(r->buf[b], r->host[i], r->layer_bytes, cudaMemcpyHostToDevice, r->copy));
+    Q4_CUDA(cudaEventRecord(r->loaded[b], r->copy));
+    // compute stream: layer i once its weights have landed
+    Q4_CUDA(cudaStreamWaitEvent(cs, r->loaded[b], 0));
+    int st = launch_layers(r->w, 4 * b, 4, r->grid, cs);
+    if (st != Q4_OK) return st;
+    if (r->flags & Q4_STREAM_POISON) Q4_CUDA(q4::poison_launch(r->buf[b], n_blocks, cs));
+    Q4_CUDA(cudaEventRecord(r->freed[b], cs));
+  }
+  // the next call's copies wait on `start`, which follows this call's compute
+  if (timeout_us > 0) {
+    Q4_CUDA(cudaEventRecord(r->done, cs));
+    const auto t0 = std::chrono::steady_clock::now();
+    for (;;) {
+      cudaError_t q = cudaEventQuery(r->done);
+      if (q == cudaSuccess) break;
+      if (q != cudaErrorNotReady) return cuda_fail(q);
+      const auto us = std::chrono::duration_cast<std::chrono::microseconds>(std::chrono::steady_clock::now() - t0).count();
+      if (us > timeout_us) return Q4_ERR_TIMEOUT;
+      std::this_thread::sleep_for(std::chrono::microseconds(20));
+    }
+  }
+  return Q4_OK;
+}
+
+extern "C" int q4_stream_status(q4_stream* r, void* compute_stream, int* status_out) {
+  if (!r || !status_out) return Q4_ERR_ARG;
+  return read_status(r->w.ctl, static_cast<cudaStream_t>(compute_stream), status_out);
+}
+
+extern "C" int q4_stream_destroy(q4_stream* r) {
+  if (!r) return Q4_OK;
+  if (r->copy) cudaStreamSynchronize(r->copy);
+  for (int i = 0; i < 2; ++i) {
+    if (r->loaded[i]) cudaEventDestroy(r->loaded[i]);
+    if (r->freed[i]) cudaEventDestroy(r->freed[i]);
+  }
+  if (r->start) cudaEventDestroy(r->start);
+  if (r->done) cudaEventDestroy(r->done);
+  if (r->copy) cudaStreamDestroy(r->copy);
+  delete r;
+  return Q4_OK;
+}

@@ -1,0 +1,178 @@
+// Device-side building blocks for the Q4_0 decode kernels (sm_103a):
+// the phase descriptor shared by host and device, and thin inline-PTX
+// wrappers for mbarriers, 1-D bulk TMA copies and bounded waits.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace q4 {
+
+constexpr int kQK = 32;              // weights per Q4_0 block
+constexpr int kBlockBytes = 18;      // binary16 scale + 16 code bytes
+constexpr int kConsumerWarps = 8;    // warps doing the arithmetic
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kThreads = kConsumerThreads + 32;   // + one producer warp
+constexpr int kStageBytes = 18432;   // one work unit of weights in shared memory
+constexpr int kStages = 11;          // ring depth (11 * 18 KB = 198 KB)
+constexpr int kMaxBatch = 16;
+
+// How the input vector x of a phase is formed (per batch row).
+enum XKind : int {
+  X_F16 = 0,      // x = src (binary16 [batch][k])
+  X_RMSNORM = 1,  // x = f16(h * rsqrt(mean(h^2) + eps)), h = src (binary16 [batch][k])
+  X_ATTN = 2,     // context-1 attention: x[i] = f16(v[(i/hd)/group*hd + i%hd]), v = fp32 src
+};
+
+// What the epilogue does with the row sums.
+enum EpiKind : int {
+  EPI_F32 = 0,    // y[b][n] = sum
+  EPI_RESID = 1,  // y[b][n] = sum; h[b][n] = f16(h[b][n] + sum); hcopy[b][n] = new h
+  EPI_SILU = 2,   // two matrices: y = g, y2 = u, act[b][n] = f16(silu(g) * u)
+};
+
+// One phase = one matrix-vector product over a row-major Q4_0 matrix
+// (or two matrices with the same shape for EPI_SILU), with its input
+// prologue and output epilogue.  Plain data, identical on host and device.
+struct Phase {
+  const uint8_t* w0;      // Q4_0 matrix [n_rows][k / 32] blocks
+  const uint8_t* w1;      // second matrix (EPI_SILU only)
+  const void* x_src;      // input per XKind
+  float* y;               // fp32 [batch][n_rows]
+  float* y2;              // fp32 [batch][n_rows] (EPI_SILU: u)
+  uint16_t* h;            // EPI_RESID: residual stream binary16 [batch][n_rows], updated in place
+  uint16_t* aux16;        // EPI_RESID: copy of the new h; EPI_SILU: act binary16 [batch][n_rows]
+  uint16_t* x_dbg;        // if not null, CTA 0 stores the formed x here (binary16 [batch][k])
+  int n_rows;
+  int k;
+  int x_kind;
+  int epi_kind;
+  int x_ld;               // row stride (elements) of x_src per batch row
+  int attn_off;           // X_ATTN: element offset of v inside a row of x_src
+  int head_dim;           // X_ATTN
+  int group;              // X_ATTN: query heads per value head
+  float eps;              // X_RMSNORM
+  int kt;                 // columns per consumer thread: 64 or 128
+  int units;              // work units in this phase
+  int rows_per_unit;      // rows of each matrix per unit
+  int pad_[2];
+};
+
+// Per-launch control block in device memory (decoder workspace).
+struct Control {
+  unsigned long long barrier;   // grid-barrier arrivals, never reset
+  int status;                   // bit flags set by kernels on a failed wait
+  int pad_;
+};
+
+// Arguments of one launch of the engine kernel: either a device array of
+// phases or a single phase passed by value.
+struct EngineArgs {
+  const Phase* phases;     // device array, or null to run `one`
+  int n_phases;
+  Control* ctl;            // required when n_phases > 1
+  uint32_t wait_limit;     // polls of one wait before it is declared failed
+  Phase one;
+};
+
+enum StatusBits : int {
+  ST_GRID_TIMEOUT = 1,
+  ST_FULL_TIMEOUT = 2,
+  ST_EMPTY_TIMEOUT = 4,
+  ST_DRAIN_TIMEOUT = 8,
+};
+
+// ------------------------------------------------------------------ PTX
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the given phase parity of an mbarrier, giving up after
+// `limit` polls (each poll may suspend the thread for a short while).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (i > 64) __nanosleep(64);
+  }
+  return false;
+}
+
+// 1-D bulk copy global -> shared, completion counted on an mbarrier.
+// src, dst 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Packed fp32x2 arithmetic (sm_100 family).
+__device__ __forceinline__ float2 f2_add(float2 a, float2 b) {
+  unsigned long long ra = *reinterpret_cast<unsigned long long*>(&a);
+  unsigned long long rb = *reinterpret_cast<unsigned long long*>(&b);
+  unsigned long long rd;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(rd) : "l"(ra), "l"(rb));
+  return *reinterpret_cast<float2*>(&rd);
+}
+
+__device__ __forceinline__ float2 f2_fma(float2 a, float2 b, float2 c) {
+  unsigned long long ra = *reinterpret_cast<unsigned long long*>(&a);
+  unsigned long long rb = *reinterpret_cast<unsigned long long*>(&b);
+  unsigned long long rc = *reinterpret_cast<unsigned long long*>(&c);
+  unsigned long long rd;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
+  return *reinterpret_cast<float2*>(&rd);
+}
+
+// Host-side launchers (q4_engine.cu, q4_aux.cu).
+cudaError_t engine_prepare();
+cudaError_t engine_launch(const EngineArgs& a, int grid, bool cooperative, cudaStream_t stream);
+cudaError_t engine_occupancy(int* blocks_per_sm);
+cudaError_t engine_read_status(int* out);
+cudaError_t simple_launch(const uint8_t* w, const uint16_t* x, float* y, int n, int k, int batch,
+                          cudaStream_t stream);
+cudaError_t dequant_launch(const uint8_t* w, float* out, int n, int k, cudaStream_t stream);
+cudaError_t poison_launch(uint8_t* buf, size_t n_blocks, cudaStream_t stream);
+
+}  // namespace q4

@@ -1,0 +1,408 @@
+// Persistent, warp-specialised Q4_0 matrix-vector engine for sm_103a.
+//
+// One CTA per SM.  Warp 8 is the producer: one lane streams the CTA's work
+// units (consecutive weight rows, contiguous in the GGUF row-major layout)
+// from HBM into an 11-deep ring of 18 KB shared-memory stages with 1-D bulk
+// TMA copies (cp.async.bulk) whose completion is counted on one mbarrier
+// per stage.  Warps 0-7 are the consumers: each thread keeps a fixed slice
+// of 64 or 128 columns of the input vector x in registers, reads its slice
+// of each staged row, unpacks the 4-bit codes in registers and accumulates
+// the exact products (q - 8) * x in fp32; the row sums are reduced with warp
+// shuffles (and, for rows wider than one warp's slice, through shared
+// memory in a fixed order).  The work of a launch is a list of phases
+// (matrix-vector products with an input prologue and an output epilogue);
+// consecutive phases are separated by a grid barrier, while the producer
+// keeps streaming the next phase's weights, which never depend on the
+// activations.
+//
+// The method: PIPO's dequantisation-free 4-bit matrix-vector product
+// ("PIPO: Pipelined Offloading for Efficient Inference on Consumer
+// Devices", Method, "Computation optimization") run layer by layer (same
+// page, "Offloading architecture"), with the weights of the next unit
+// prefetched while the current one computes (PipeLLM page, "Layer 2:
+// Asynchronous Weight Prefetching").
+//
+// Exactness of the block dot product: a code q is placed in the mantissa of
+// 2^23 (bits p..p+3 for p in {0,4,8,12,16}), so the float equals 2^23 + q*2^p
+// exactly; subtracting 2^23 + 8*2^p gives (q - 8)*2^p exactly, and the matching
+// x was stored pre-multiplied by 2^-p (exact).  Each product (q - 8) * x is
+// therefore exact, a block of all-8 codes contributes exactly zero, and a
+// block with one non-8 code contributes exactly fl(d * (q - 8) * x).
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "q4_device.cuh"
+
+namespace q4 {
+
+__device__ int g_status;   // status bits of launches without a control block
+
+
+// Column order of the 8 codes of one 32-bit word of a block's code bytes
+// (bytes 4m..4m+3 hold elements 4m..4m+3 low and 4m+16..4m+19 high), and the
+// bit position each code is extracted at.
+__device__ __forceinline__ constexpr int elem_off(int e) {
+  return (e & 1) ? 16 + (e >> 1) : (e >> 1);
+}
+__device__ __forceinline__ constexpr int elem_shift(int e) {
+  return e == 0 ? 0 : e == 1 ? 4 : e == 2 ? 8 : e == 3 ? 12 : e == 4 ? 16 : e == 5 ? 8 : e == 6 ? 12 : 16;
+}
+
+constexpr uint32_t kMagic = 0x4B000000u;   // 2^23 as float bits
+
+__device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+
+// Accumulate the 8 exact products of one code word into acc (two lanes).
+__device__ __forceinline__ float2 word_dot(uint32_t w, const float2* xs, float2 acc) {
+  const float M = 8388608.0f;
+  const uint32_t u = w >> 12;
+  float2 v01 = make_float2(u2f((w & 0xFu) | kMagic), u2f((w & 0xF0u) | kMagic));
+  float2 v23 = make_float2(u2f((w & 0xF00u) | kMagic), u2f((w & 0xF000u) | kMagic));
+  float2 v45 = make_float2(u2f((w & 0xF0000u) | kMagic), u2f((u & 0xF00u) | kMagic));
+  float2 v67 = make_float2(u2f((u & 0xF000u) | kMagic), u2f((u & 0xF0000u) | kMagic));
+  v01 = f2_add(v01, make_float2(-(M + 8.0f), -(M + 128.0f)));
+  v23 = f2_add(v23, make_float2(-(M + 2048.0f), -(M + 32768.0f)));
+  v45 = f2_add(v45, make_float2(-(M + 524288.0f), -(M + 2048.0f)));
+  v67 = f2_add(v67, make_float2(-(M + 32768.0f), -(M + 524288.0f)));
+  acc = f2_fma(v01, xs[0], acc);
+  acc = f2_fma(v23, xs[1], acc);
+  acc = f2_fma(v45, xs[2], acc);
+  acc = f2_fma(v67, xs[3], acc);
+  return acc;
+}
+
+// Dot product of one 64-column slice (two blocks = 36 bytes starting at a
+// 4-byte aligned shared-memory address) with the thread's 32 float2 of x.
+__device__ __forceinline__ float pair_dot(const uint8_t* p, const float2* xs, float tot) {
+  const uint32_t* pw = reinterpret_cast<const uint32_t*>(p);
+  uint32_t W[9];
+#pragma unroll
+  for (int i = 0; i < 9; ++i) W[i] = pw[i];
+  const float d0 = __half2float(__ushort_as_half(static_cast<unsigned short>(W[0] & 0xFFFFu)));
+  const float d1 = __half2float(__ushort_as_half(static_cast<unsigned short>(W[4] >> 16)));
+  float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+  float2 b0 = make_float2(0.f, 0.f), b1 = make_float2(0.f, 0.f);
+  // block 0: code bytes start 2 bytes into word 0
+  a0 = word_dot(__funnelshift_r(W[0], W[1], 16), xs + 0, a0);
+  a1 = word_dot(__funnelshift_r(W[1], W[2], 16), xs + 4, a1);
+  a0 = word_dot(__funnelshift_r(W[2], W[3], 16), xs + 8, a0);
+  a1 = word_dot(__funnelshift_r(W[3], W[4], 16), xs + 12, a1);
+  // block 1: code bytes are words 5..8
+  b0 = word_dot(W[5], xs + 16, b0);
+  b1 = word_dot(W[6], xs + 20, b1);
+  b0 = word_dot(W[7], xs + 24, b0);
+  b1 = word_dot(W[8], xs + 28, b1);
+  const float s0 = (a0.x + a0.y) + (a1.x + a1.y);
+  const float s1 = (b0.x + b0.y) + (b1.x + b1.y);
+  tot = fmaf(d0, s0, tot);
+  tot = fmaf(d1, s1, tot);
+  return tot;
+}
+
+__device__ __forceinline__ void set_status(Control* ctl, int bits) {
+  atomicOr(ctl ? &ctl->status : &g_status, bits);
+}
+
+// Form the thread's slice of x for a phase: xs2 receives kt/2 float2 in the
+// order pair_dot expects, each value pre-scaled by 2^-shift.
+__device__ void form_x(const Phase& ph, int j, int kt, float2* xs2, float* red_ss, bool write_dbg) {
+  const int ct = threadIdx.x;   // consumer thread 0..255
+  float r = 1.0f;
+  if (ph.x_kind == X_RMSNORM) {
+    const __half* h = static_cast<const __half*>(ph.x_src);
+    float ss = 0.f;
+    for (int i = ct; i < ph.k; i += kConsumerThreads) {
+      const float v = __half2float(h[i]);
+      ss = fmaf(v, v, ss);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((ct & 31) == 0) red_ss[ct >> 5] = ss;
+    named_bar_sync(1, kConsumerThreads);
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) tot += red_ss[w];
+    r = rsqrtf(tot / static_cast<float>(ph.k) + ph.eps);
+    named_bar_sync(1, kConsumerThreads);   // red_ss is reused by the next phase
+  }
+  const int k0 = j * kt;
+#pragma unroll
+  for (int blk = 0; blk < 4; ++blk) {
+    if (blk * 32 >= kt) break;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        float v2[2];
+#pragma unroll
+        for (int l = 0; l < 2; ++l) {
+          const int col = k0 + blk * 32 + 4 * m + elem_off(e + l);
+          __half xv;
+          if (ph.x_kind == X_F16) {
+            xv = static_cast<const __half*>(ph.x_src)[col];
+          } else if (ph.x_kind == X_RMSNORM) {
+            xv = __float2half_rn(__half2float(static_cast<const __half*>(ph.x_src)[col]) * r);
+          } else {
+            const int hd = ph.head_dim;
+            const int src = ph.attn_off + ((col / hd) / ph.group) * hd + (col % hd);
+            xv = __float2half_rn(static_cast<const float*>(ph.x_src)[src]);
+          }
+          if (write_dbg) ph.x_dbg[col] = __half_as_ushort(xv);
+          v2[l] = __half2float(xv) * (1.0f / static_cast<float>(1 << elem_shift(e + l)));
+        }
+        xs2[blk * 16 + m * 4 + e / 2] = make_float2(v2[0], v2[1]);
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
+// Row epilogue for one output row n of a phase (batch row 0).
+__device__ __forceinline__ void epilogue(const Phase& ph, int n, float s, float s2) {
+  if (ph.epi_kind == EPI_F32) {
+    ph.y[n] = s;
+  } else if (ph.epi_kind == EPI_RESID) {
+    ph.y[n] = s;
+    const float hv = __half2float(__ushort_as_half(ph.h[n])) + s;
+    const unsigned short hb = __half_as_ushort(__float2half_rn(hv));
+    ph.h[n] = hb;
+    if (ph.aux16) ph.aux16[n] = hb;
+  } else {
+    ph.y[n] = s;
+    ph.y2[n] = s2;
+    ph.aux16[n] = __half_as_ushort(__float2half_rn(silu_mul(s, s2)));
+  }
+}
+
+__device__ bool grid_barrier(Control* ctl, unsigned long long target, uint32_t limit) {
+  __threadfence();
+  atomicAdd(&ctl->barrier, 1ull);
+  for (uint32_t i = 0; i < limit; ++i) {
+    if (ld_acquire_u64(&ctl->barrier) >= target) {
+      __threadfence();
+      return true;
+    }
+    __nanosleep(i < 256 ? 32 : 256);
+  }
+  return false;
+}
+
+extern __shared__ __align__(128) uint8_t g_ring[];
+
+__global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_constant__ EngineArgs a) {
+  __shared__ __align__(8) uint64_t full_bar[kStages];
+  __shared__ __align__(8) uint64_t empty_bar[kStages];
+  __shared__ float red[2][kConsumerWarps][2];
+  __shared__ float red_ss[kConsumerWarps];
+  __shared__ volatile int abort_flag;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int G = gridDim.x, cta = blockIdx.x;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], kConsumerWarps);
+    }
+    fence_mbar_init();
+    abort_flag = 0;
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      int base = 0;   // (global index of the phase's first unit) mod G
+      for (int p = 0; p < a.n_phases && !abort_flag; ++p) {
+        const Phase ph = a.phases ? a.phases[p] : a.one;
+        const uint32_t row_bytes = static_cast<uint32_t>(ph.k / kQK) * kBlockBytes;
+        const int u0 = (cta - base + G) % G;
+        for (int u = u0; u < ph.units; u += G) {
+          const int stage = it % kStages;
+          const uint32_t n = it / kStages;
+          if (n > 0 && !mbar_wait_bounded(&empty_bar[stage], (n - 1) & 1, a.wait_limit)) {
+            set_status(a.ctl, ST_EMPTY_TIMEOUT);
+            abort_flag = 1;
+            break;
+          }
+          if (abort_flag) break;
+          const int row0 = u * ph.rows_per_unit;
+          const int rows = min(ph.rows_per_unit, ph.n_rows - row0);
+          const uint32_t bytes = static_cast<uint32_t>(rows) * row_bytes;
+          uint8_t* dst = g_ring + static_cast<size_t>(stage) * kStageBytes;
+          const bool dual = ph.epi_kind == EPI_SILU;
+          mbar_arrive_expect_tx(&full_bar[stage], dual ? 2 * bytes : bytes);
+          bulk_g2s(dst, ph.w0 + static_cast<size_t>(row0) * row_bytes, bytes, &full_bar[stage]);
+          if (dual)
+            bulk_g2s(dst + static_cast<size_t>(ph.rows_per_unit) * row_bytes,
+                     ph.w1 + static_cast<size_t>(row0) * row_bytes, bytes, &full_bar[stage]);
+          ++it;
+        }
+        base = (base + ph.units) % G;
+      }
+      // Drain: no copy may still be in flight when the CTA exits.
+      const uint32_t issued = it;
+      for (int s = 0; s < kStages && static_cast<uint32_t>(s) < issued; ++s) {
+        const uint32_t last = (issued - 1 - s) / kStages;   // uses of stage s minus one
+        if (!mbar_wait_bounded(&full_bar[s], last & 1, a.wait_limit)) set_status(a.ctl, ST_DRAIN_TIMEOUT);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ consumers
+    float2 xs2[64];
+    uint32_t it = 0;
+    int base = 0;
+    for (int p = 0; p < a.n_phases; ++p) {
+      const Phase ph = a.phases ? a.phases[p] : a.one;
+      if (p > 0) {
+        named_bar_sync(1, kConsumerThreads);   // this CTA's writes of the last phase are done
+        if (tid == 0 && !grid_barrier(a.ctl, static_cast<unsigned long long>(p) * G, a.wait_limit)) {
+          set_status(a.ctl, ST_GRID_TIMEOUT);
+          abort_flag = 1;
+        }
+        named_bar_sync(1, kConsumerThreads);
+        if (abort_flag) break;
+      }
+      const int kt = ph.kt;
+      const int team_threads = ph.k / kt;
+      const int teams = kConsumerThreads / team_threads;
+      const int team = tid / team_threads, j = tid % team_threads;
+      const bool active = team < teams;
+      const int rpt = (kt == 64) ? 2 : 1;
+      const bool dual = ph.epi_kind == EPI_SILU;
+      const uint32_t row_bytes = static_cast<uint32_t>(ph.k / kQK) * kBlockBytes;
+      const int u0 = (cta - base + G) % G;
+      const bool has_work = u0 < ph.units;
+      if (has_work || (ph.x_dbg && cta == 0)) {
+        // every consumer thread takes part (the RMS reduction is CTA-wide)
+        form_x(ph, active ? j : 0, kt, xs2, red_ss, ph.x_dbg != nullptr && cta == 0 && team == 0);
+      }
+      for (int u = u0; u < ph.units; u += G) {
+        const int stage = it % kStages;
+        const uint32_t n = it / kStages;
+        // After a failed wait the CTA keeps walking its units without waiting
+        // (reading whatever the stage holds) so that every team barrier is
+        // still reached; the launch then reports the failure in its status.
+        if (!abort_flag && !mbar_wait_bounded(&full_bar[stage], n & 1, a.wait_limit)) {
+          set_status(a.ctl, ST_FULL_TIMEOUT);
+          abort_flag = 1;
+        }
+        const uint8_t* sb = g_ring + static_cast<size_t>(stage) * kStageBytes;
+        const int row0 = u * ph.rows_per_unit;
+        float t0 = 0.f, t1 = 0.f;
+        int ra = -1, rb = -1;     // output rows of this team (-1: none)
+        if (active) {
+          const uint8_t *pa, *pb = nullptr;
+          if (dual) {
+            ra = row0 + team;
+            pa = sb + static_cast<size_t>(team) * row_bytes;
+            pb = sb + static_cast<size_t>(ph.rows_per_unit + team) * row_bytes;
+            rb = ra;
+          } else {
+            ra = row0 + team * rpt;
+            pa = sb + static_cast<size_t>(team * rpt) * row_bytes;
+            if (rpt == 2) {
+              rb = ra + 1;
+              pb = pa + row_bytes;
+            }
+          }
+          if (ra >= ph.n_rows) ra = -1;
+          if (rb >= ph.n_rows) rb = -1;
+          if (kt == 64) {
+            if (ra >= 0) t0 = pair_dot(pa + static_cast<size_t>(j) * 36, xs2, 0.f);
+            if (rb >= 0) t1 = pair_dot(pb + static_cast<size_t>(j) * 36, xs2, 0.f);
+          } else if (ra >= 0) {
+            t0 = pair_dot(pa + static_cast<size_t>(2 * j) * 36, xs2, 0.f);
+            t0 = pair_dot(pa + static_cast<size_t>(2 * j + 1) * 36, xs2 + 32, t0);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[stage]);
+        ++it;
+        if (!active) continue;
+        // reduce the team's partial sums
+        const int width = team_threads < 32 ? team_threads : 32;
+        for (int o = width >> 1; o > 0; o >>= 1) {
+          t0 += __shfl_xor_sync(0xffffffffu, t0, o);
+          t1 += __shfl_xor_sync(0xffffffffu, t1, o);
+        }
+        if (team_threads <= 32) {
+          if (j == 0 && ra >= 0) {
+            if (dual) epilogue(ph, ra, t0, t1);
+            else {
+              epilogue(ph, ra, t0, 0.f);
+              if (rb >= 0) epilogue(ph, rb, t1, 0.f);
+            }
+          }
+        } else {
+          const int slot = it & 1;
+          if (lane == 0) {
+            red[slot][warp][0] = t0;
+            red[slot][warp][1] = t1;
+          }
+          named_bar_sync(2 + team, team_threads);
+          if (j == 0 && ra >= 0) {
+            const int w0 = team * (team_threads >> 5);
+            float s0 = 0.f, s1 = 0.f;
+            for (int w = 0; w < (team_threads >> 5); ++w) {
+              s0 += red[slot][w0 + w][0];
+              s1 += red[slot][w0 + w][1];
+            }
+            if (dual) epilogue(ph, ra, s0, s1);
+            else {
+              epilogue(ph, ra, s0, 0.f);
+              if (rb >= 0) epilogue(ph, rb, s1, 0.f);
+            }
+          }
+        }
+      }
+      base = (base + ph.units) % G;
+    }
+  }
+
+  __syncthreads();
+  if (a.n_phases > 1 && tid == 0) {
+    // The last CTA to leave resets the barrier count for the next launch.
+    __threadfence();
+    const unsigned long long left = atomicAdd(&a.ctl->barrier, 1ull << 40) >> 40;
+    if (left == static_cast<unsigned long long>(G) - 1) {
+      atomicExch(&a.ctl->barrier, 0ull);
+    }
+  }
+}
+
+cudaError_t engine_prepare() {
+  return cudaFuncSetAttribute(engine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kStages * kStageBytes);
+}
+
+cudaError_t engine_launch(const EngineArgs& a, int grid, bool cooperative, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kStages * kStageBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = cooperative ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, engine_kernel, a);
+}
+
+cudaError_t engine_occupancy(int* blocks_per_sm) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, engine_kernel, kThreads,
+                                                       kStages * kStageBytes);
+}
+
+cudaError_t engine_read_status(int* out) {
+  int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_status, sizeof(int));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_status, &zero, sizeof(int));
+}
+
+}  // namespace q4

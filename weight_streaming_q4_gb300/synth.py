@@ -144,14 +144,13 @@ def layer_dims(hidden: int, q_dim: int, kv_dim: int, ffn: int):
 def layer_offsets(hidden: int, q_dim: int, kv_dim: int, ffn: int):
     """Byte offsets of the seven projections inside one merged layer block, and its size.
 
-    Each projection is a contiguous GGUF-order Q4_0 matrix; each offset is
-    rounded up to 256 bytes.
+    Each projection is a contiguous GGUF-order Q4_0 matrix, and they follow
+    one another with no gap (the library's q4_layer_offsets layout).
     """
     offs, pos = [], 0
     for (n, k) in layer_dims(hidden, q_dim, kv_dim, ffn):
         offs.append(pos)
         pos += q4_bytes(n, k)
-        pos = (pos + 255) // 256 * 256
     return offs, pos
 
 
@@ -167,3 +166,58 @@ def layer_block(layer: int, hidden: int, q_dim: int, kv_dim: int, ffn: int, seed
 
 LLAMA_8B = dict(hidden=4096, q_dim=4096, kv_dim=1024, ffn=14336, head_dim=128, n_layers=32)
 LLAMA_70B = dict(hidden=8192, q_dim=8192, kv_dim=1024, ffn=28672, head_dim=128, n_layers=80)
+
+
+# ------------------------------------------------------------------ device filler
+
+_synth_lib = None
+
+
+def _device_lib():
+    global _synth_lib
+    if _synth_lib is None:
+        import ctypes
+        import os
+
+        from . import build as _build
+        path = _build.lib_path("libq4synth.so")
+        if not os.path.exists(path):
+            raise ImportError(f"libq4synth.so is not built ({path})")
+        lib = ctypes.CDLL(path)
+        u64, u32, vp = ctypes.c_uint64, ctypes.c_uint32, ctypes.c_void_p
+        lib.q4s_fill_q4_0.argtypes = [vp, u64, u64, u32, u32, ctypes.c_double, vp]
+        lib.q4s_fill_normal_f16.argtypes = [vp, u64, u64, u32, u32, ctypes.c_double, vp]
+        lib.q4s_philox.argtypes = [vp, u32, u32, u32, u32, u32, u32, vp]
+        for f in (lib.q4s_fill_q4_0, lib.q4s_fill_normal_f16, lib.q4s_philox):
+            f.restype = ctypes.c_int
+        _synth_lib = lib
+    return _synth_lib
+
+
+def _cur_stream(stream):
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream if isinstance(stream, int) else stream.cuda_stream
+
+
+def device_fill_q4(dst_ptr: int, n_blocks: int, seed: int, tid: int, block0: int = 0, stream=None):
+    """Write blocks block0.. of tensor ``tid`` (same bytes as ``q4_blocks``) to device memory."""
+    e = _device_lib().q4s_fill_q4_0(dst_ptr, n_blocks, block0, seed & 0xFFFFFFFF, tid & 0xFFFFFFFF,
+                                    SCALE_SIGMA, _cur_stream(stream))
+    if e != 0:
+        raise RuntimeError(f"q4s_fill_q4_0 failed: cudaError {e}")
+
+
+def device_fill_normal_f16(dst_ptr: int, n: int, seed: int, tid: int, sigma: float = X_SIGMA, start: int = 0,
+                           stream=None):
+    e = _device_lib().q4s_fill_normal_f16(dst_ptr, n, start, seed & 0xFFFFFFFF, tid & 0xFFFFFFFF, sigma,
+                                          _cur_stream(stream))
+    if e != 0:
+        raise RuntimeError(f"q4s_fill_normal_f16 failed: cudaError {e}")
+
+
+def device_philox(out_ptr: int, c0, c1, c2, c3, k0, k1, stream=None):
+    e = _device_lib().q4s_philox(out_ptr, c0, c1, c2, c3, k0, k1, _cur_stream(stream))
+    if e != 0:
+        raise RuntimeError(f"q4s_philox failed: cudaError {e}")
