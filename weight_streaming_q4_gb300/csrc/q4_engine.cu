@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
       uint32_t it = 0;
       int base = 0;   // (global index of the phase's first unit) mod G
       for (int p = 0; p < a.n_phases && !abort_flag; ++p) {
-        const Phase ph = a.phases ? a.phases[p] : a.one;
+        const Phase& ph = a.phases ? a.phases[p] : a.one;
         const uint32_t row_bytes = static_cast<uint32_t>(ph.k / kQK) * kBlockBytes;
         const int u0 = (cta - base + G) % G;
         for (int u = u0; u < ph.units; u += G) {
@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
     uint32_t it = 0;
     int base = 0;
     for (int p = 0; p < a.n_phases; ++p) {
-      const Phase ph = a.phases ? a.phases[p] : a.one;
+      const Phase& ph = a.phases ? a.phases[p] : a.one;
       if (p > 0) {
         named_bar_sync(1, kConsumerThreads);   // this CTA's writes of the last phase are done
         if (tid == 0 && !grid_barrier(a.ctl, static_cast<unsigned long long>(p) * G, a.wait_limit)) {
@@ -274,13 +274,14 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
       const int rpt = (kt == 64) ? 2 : 1;
       const bool dual = ph.epi_kind == EPI_SILU;
       const uint32_t row_bytes = static_cast<uint32_t>(ph.k / kQK) * kBlockBytes;
+      const int units = ph.units, rows_per_unit = ph.rows_per_unit, n_rows = ph.n_rows;
       const int u0 = (cta - base + G) % G;
-      const bool has_work = u0 < ph.units;
+      const bool has_work = u0 < units;
       if (has_work || (ph.x_dbg && cta == 0)) {
         // every consumer thread takes part (the RMS reduction is CTA-wide)
         form_x(ph, active ? j : 0, kt, xs2, red_ss, ph.x_dbg != nullptr && cta == 0 && team == 0);
       }
-      for (int u = u0; u < ph.units; u += G) {
+      for (int u = u0; u < units; u += G) {
         const int stage = it % kStages;
         const uint32_t n = it / kStages;
         // After a failed wait the CTA keeps walking its units without waiting
@@ -291,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
           abort_flag = 1;
         }
         const uint8_t* sb = g_ring + static_cast<size_t>(stage) * kStageBytes;
-        const int row0 = u * ph.rows_per_unit;
+        const int row0 = u * rows_per_unit;
         float t0 = 0.f, t1 = 0.f;
         int ra = -1, rb = -1;     // output rows of this team (-1: none)
         if (active) {
@@ -299,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
           if (dual) {
             ra = row0 + team;
             pa = sb + static_cast<size_t>(team) * row_bytes;
-            pb = sb + static_cast<size_t>(ph.rows_per_unit + team) * row_bytes;
+            pb = sb + static_cast<size_t>(rows_per_unit + team) * row_bytes;
             rb = ra;
           } else {
             ra = row0 + team * rpt;
@@ -309,8 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
               pb = pa + row_bytes;
             }
           }
-          if (ra >= ph.n_rows) ra = -1;
-          if (rb >= ph.n_rows) rb = -1;
+          if (ra >= n_rows) ra = -1;
+          if (rb >= n_rows) rb = -1;
           if (kt == 64) {
             if (ra >= 0) t0 = pair_dot(pa + static_cast<size_t>(j) * 36, xs2, 0.f);
             if (rb >= 0) t1 = pair_dot(pb + static_cast<size_t>(j) * 36, xs2, 0.f);
@@ -359,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
           }
         }
       }
-      base = (base + ph.units) % G;
+      base = (base + units) % G;
     }
   }
 
