@@ -117,18 +117,22 @@ int q4_dequant_debug(const void *w, float *w_out, int n, int k, void *stream);
 /* ------------------------------------------------------- decoder layers */
 
 /*
- * Shape of one Llama-style decoder layer.  The layer (the plainest reading of
- * "a layer's projections in sequence"; the pages name the projections only by
- * the model families they run) is, per batch row, with h the binary16
- * residual stream:
- *   x  = f16(h / sqrt(mean(h^2) + eps))              RMSNorm, unit weight
- *   q, k, v = Wq x, Wk x, Wv x                       (fp32)
- *   a  = f16(v of the value head each query head is grouped with)
- *        (attention over a context of one token: softmax of one score is 1)
- *   h  = f16(h + Wo a)
- *   x  = f16(h / sqrt(mean(h^2) + eps))
- *   act = f16(silu(Wgate x) * (Wup x))
- *   h  = f16(h + Wdown act)
+ * Shape of one Llama-shaped decoder layer.  The pages name the projections
+ * only by the model families they run, so the glue between them is this
+ * library's reading, per batch row, with z the layer's normalised binary16
+ * input (RMSNorm with unit weight: norm(t) = t / sqrt(mean(t^2) + eps)):
+ *   q, k, v = Wq z, Wk z, Wv z                                       (fp32)
+ *   a   = f16(v of the value head each query head is grouped with)
+ *         (attention over a context of one token: softmax of one score is 1,
+ *          rotary position 0 is the identity)
+ *   t1  = z + Wo a            (fp32)      z1  = f16(norm(t1))
+ *   act = f16(silu(Wgate z1) * (Wup z1))
+ *   t2  = z1 + Wdown act      (fp32)      next layer's z = f16(norm(t2))
+ * The residual sum is normalised after each add (post-norm): the specified
+ * synthetic weights have a nonzero mean, and a pre-norm residual stream
+ * overflows binary16 within two 8B-shaped layers.  The first layer's z is
+ * f16(norm(h)) of the caller's hidden state h; after the last layer the
+ * caller's buffer receives the last z.
  */
 typedef struct q4_layer_shape {
   int hidden;     /* model width (4096 for 8B, 8192 for 70B) */
@@ -165,16 +169,17 @@ int q4_layer_offsets(const q4_layer_shape *shape, size_t offsets[7], size_t *lay
 #define Q4_WS_UP 5        /* fp32 [batch][ffn] */
 #define Q4_WS_DOWN 6      /* fp32 [batch][hidden] */
 #define Q4_WS_ACT 7       /* binary16 [batch][ffn] */
-#define Q4_WS_X 8         /* binary16 [batch][hidden]: first normalised input */
-#define Q4_WS_ATTN 9      /* binary16 [batch][q_dim]: attention output */
-#define Q4_WS_X2 10       /* binary16 [batch][hidden]: second normalised input */
-#define Q4_WS_HMID 11     /* binary16 [batch][hidden]: h after the attention residual */
-#define Q4_WS_COUNT 12
+#define Q4_WS_X 8         /* binary16 [batch][hidden]: z, the layer's normalised input */
+#define Q4_WS_ATTN 9      /* binary16 [batch][q_dim]: attention output a */
+#define Q4_WS_X2 10       /* binary16 [batch][hidden]: z1 = f16(norm(t1)) */
+#define Q4_WS_T1 11       /* fp32 [batch][hidden]: t1 = z + Wo a */
+#define Q4_WS_T2 12       /* fp32 [batch][hidden]: t2 = z1 + Wdown act */
+#define Q4_WS_COUNT 13
 
 /*
- * Byte offsets of the workspace regions for a decoder of n_layers layers
- * (use n_layers = 2 for a stream ring) and the total size needed.  The
- * intermediate regions hold the values of the last layer run (for checks).
+ * Byte offsets of the workspace regions for a decoder or a stream ring of
+ * n_layers layers and the total size needed.  The intermediate regions hold
+ * the values of the last layer run (for checks).
  * Errors: Q4_ERR_ARG.
  */
 int q4_workspace_layout(const q4_layer_shape *shape, int n_layers, int batch,
@@ -202,8 +207,9 @@ int q4_decoder_create(q4_decoder **out, const q4_layer_shape *shape, const void 
                       void *stream);
 
 /*
- * Run all layers once on hidden_io (device, binary16 [batch][hidden], updated
- * in place) by replaying the captured graph on `stream`.  The first call with
+ * Run all layers once on hidden_io (device, binary16 [batch][hidden]: read as
+ * the first layer's input, overwritten with the last layer's normalised
+ * output) by replaying the captured graph on `stream`.  The first call with
  * a new hidden_io pointer rewrites the phase descriptors (stream-ordered).
  * Errors: Q4_ERR_ARG, Q4_ERR_ALIGN, Q4_ERR_CUDA.
  */
@@ -234,7 +240,7 @@ typedef struct q4_stream q4_stream;
  *                    layer i's merged block, 16-byte aligned, read only
  *   n_layers >= 1;  batch 1..16
  *   dev_buf0/1       device, buf_bytes >= one layer block each, 256-byte aligned
- *   workspace        device, >= q4_workspace_layout(shape, 2, batch) bytes
+ *   workspace        device, >= q4_workspace_layout(shape, n_layers, batch) bytes
  *   flags            0 or Q4_STREAM_POISON
  * The handle creates its own copy stream and events.
  * Errors: Q4_ERR_ARG, Q4_ERR_ALIGN, Q4_ERR_OOM, Q4_ERR_CUDA.

@@ -61,11 +61,12 @@ def _declare(lib):
     lib.ora_gemv_rows.argtypes = [_P, _P, _I64, _I64, _INT, _P, _I64, _P, _P]
     lib.ora_rmsnorm.argtypes = [_P, _INT, _I64, _DBL, _P]
     lib.ora_attn_ctx1.argtypes = [_P, _INT, _I64, _I64, _I64, _P]
-    lib.ora_residual.argtypes = [_P, _P, _I64, _P]
+    lib.ora_rmsnorm_d.argtypes = [_P, _INT, _I64, _DBL, _P]
+    lib.ora_add.argtypes = [_P, _P, _I64, _P]
     lib.ora_silu_mul.argtypes = [_P, _P, _I64, _P]
-    lib.ora_layer.argtypes = [_P, _P, _INT, _I64, _I64, _I64, _I64, _I64, _DBL, _P, _P, _P]
+    lib.ora_layer.argtypes = [_P, _P, _INT, _I64, _I64, _I64, _I64, _I64, _DBL, _P, _P, _P, _P]
     for name in ("ora_half_to_double_n", "ora_double_to_half_n", "ora_dequant", "ora_gemv",
-                 "ora_gemv_rows", "ora_rmsnorm", "ora_attn_ctx1", "ora_residual",
+                 "ora_gemv_rows", "ora_rmsnorm", "ora_rmsnorm_d", "ora_attn_ctx1", "ora_add",
                  "ora_silu_mul", "ora_layer"):
         getattr(lib, name).restype = None
     return lib
@@ -183,13 +184,23 @@ def attn_ctx1(v, batch: int, q_dim: int, kv_dim: int, head_dim: int, lib=None) -
     return out
 
 
-def residual(h, o, lib=None) -> np.ndarray:
+def rmsnorm_d(t, batch: int, dim: int, eps: float = 1e-5, lib=None) -> np.ndarray:
+    """RMSNorm of double vectors (residual sums), rounded to binary16 bits."""
     lib = lib or load()
-    hb = _u16(h)
+    tb = np.ascontiguousarray(t, dtype=np.float64).reshape(batch, dim)
+    out = np.empty((batch, dim), dtype=np.uint16)
+    lib.ora_rmsnorm_d(_ptr(tb), batch, dim, eps, _ptr(out))
+    return out
+
+
+def add(z, o, lib=None) -> np.ndarray:
+    """Residual sum t = z + o (z binary16 bits, o double) in double."""
+    lib = lib or load()
+    zb = _u16(z)
     ob = np.ascontiguousarray(o, dtype=np.float64)
-    assert hb.size == ob.size
-    out = np.empty(hb.shape, dtype=np.uint16)
-    lib.ora_residual(_ptr(hb), _ptr(ob), hb.size, _ptr(out))
+    assert zb.size == ob.size
+    out = np.empty(zb.shape, dtype=np.float64)
+    lib.ora_add(_ptr(zb), _ptr(ob), zb.size, _ptr(out))
     return out
 
 
@@ -202,19 +213,21 @@ def silu_mul(g, u, lib=None) -> np.ndarray:
     return out
 
 
-def layer(weights, h, batch: int, hidden: int, q_dim: int, kv_dim: int, ffn: int,
-          head_dim: int = 128, eps: float = 1e-5, lib=None) -> np.ndarray:
-    """One decoder layer; ``weights`` = 7 byte arrays (q, k, v, o, gate, up, down)."""
+def layer(weights, z, batch: int, hidden: int, q_dim: int, kv_dim: int, ffn: int,
+          head_dim: int = 128, eps: float = 1e-5, lib=None):
+    """One decoder layer from its normalised binary16 input z; ``weights`` = 7
+    byte arrays (q, k, v, o, gate, up, down).  Returns (z_out bits, t2 doubles)."""
     lib = lib or load()
     ws = [_u8(w) for w in weights]
     arr = (ctypes.c_void_p * 7)(*[w.ctypes.data for w in ws])
-    hb = _u16(h).reshape(batch, hidden)
-    work = np.empty(batch * (q_dim + 2 * kv_dim + hidden + 2 * ffn), dtype=np.float64)
-    work16 = np.empty(batch * (2 * hidden + q_dim + ffn), dtype=np.uint16)
+    zb = _u16(z).reshape(batch, hidden)
+    work = np.empty(batch * (q_dim + 2 * kv_dim + 3 * hidden + 2 * ffn), dtype=np.float64)
+    work16 = np.empty(batch * (hidden + q_dim + ffn), dtype=np.uint16)
+    t2 = np.empty((batch, hidden), dtype=np.float64)
     out = np.empty((batch, hidden), dtype=np.uint16)
-    lib.ora_layer(arr, _ptr(hb), batch, hidden, q_dim, kv_dim, ffn, head_dim, eps,
-                  _ptr(work), _ptr(work16), _ptr(out))
-    return out
+    lib.ora_layer(arr, _ptr(zb), batch, hidden, q_dim, kv_dim, ffn, head_dim, eps,
+                  _ptr(work), _ptr(work16), _ptr(t2), _ptr(out))
+    return out, t2
 
 
 def tolerance(s) -> np.ndarray:

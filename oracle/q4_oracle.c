@@ -25,7 +25,10 @@
  *     transformer layer's q/k/v/o/gate/up/down projections in sequence"
  *     (PIPO summary, Method, "Offloading architecture": the layer is the unit
  *     of the schedule).  Activations are rounded to binary16 at the points
- *     where the GPU stores binary16.
+ *     where the GPU stores binary16.  The residual sum is normalised after
+ *     each add (post-norm); with the workloads' weights (codes uniform on
+ *     0..15, so E[q - 8] = -1/2) a pre-norm residual stream overflows
+ *     binary16 within two 8B-shaped layers.
  *
  * All floating-point work here is double precision.  The binary16 decoder
  * and the round-to-nearest-even encoder are written out below from the IEEE
@@ -206,11 +209,25 @@ void ora_attn_ctx1(const double *v, int batch, int64_t q_dim, int64_t kv_dim, in
                     ora_double_to_half(v[(int64_t)b * kv_dim + (qh / group) * head_dim + i]);
 }
 
-/* Residual add: h_out = f16(h + o). */
-void ora_residual(const uint16_t *h, const double *o, int64_t n, uint16_t *h_out)
+/* RMSNorm of a double vector (a residual sum): x = f16(t / sqrt(mean(t^2) + eps)). */
+void ora_rmsnorm_d(const double *t, int batch, int64_t dim, double eps, uint16_t *x_out)
+{
+    for (int b = 0; b < batch; b++) {
+        const double *tb = t + (int64_t)b * dim;
+        double ss = 0.0;
+        for (int64_t i = 0; i < dim; i++)
+            ss += tb[i] * tb[i];
+        double r = 1.0 / sqrt(ss / (double)dim + eps);
+        for (int64_t i = 0; i < dim; i++)
+            x_out[(int64_t)b * dim + i] = ora_double_to_half(tb[i] * r);
+    }
+}
+
+/* Residual sum: t = z + o (z binary16, o and t double). */
+void ora_add(const uint16_t *z, const double *o, int64_t n, double *t)
 {
     for (int64_t i = 0; i < n; i++)
-        h_out[i] = ora_double_to_half(ora_half_to_double(h[i]) + o[i]);
+        t[i] = ora_half_to_double(z[i]) + o[i];
 }
 
 /* SiLU-gated product: act = f16(g / (1 + exp(-g)) * u). */
@@ -220,40 +237,40 @@ void ora_silu_mul(const double *g, const double *u, int64_t n, uint16_t *act)
         act[i] = ora_double_to_half(g[i] / (1.0 + exp(-g[i])) * u[i]);
 }
 
-/* One decoder layer, batch rows independent.  Weight order: q, k, v, o,
- * gate, up, down (row-major Q4_0 each).  h is read and the result written
- * to h_out (binary16 [batch][hidden]).  work must hold
- * batch*(q_dim + 2*kv_dim + hidden + 2*ffn) doubles and
- * batch*(2*hidden + q_dim + ffn) binary16 values in work16. */
-void ora_layer(const uint8_t *const *wts, const uint16_t *h, int batch, int64_t hidden,
+/* One decoder layer, batch rows independent, with the residual sum
+ * normalised after each add.  z is the layer's normalised binary16 input
+ * [batch][hidden]; weight order q, k, v, o, gate, up, down (row-major Q4_0
+ * each).  Writes t2 (double [batch][hidden], the last residual sum) and
+ * z_out = f16(norm(t2)), the next layer's input.  work must hold
+ * batch*(q_dim + 2*kv_dim + 3*hidden + 2*ffn) doubles and
+ * batch*(hidden + q_dim + ffn) binary16 values in work16. */
+void ora_layer(const uint8_t *const *wts, const uint16_t *z, int batch, int64_t hidden,
                int64_t q_dim, int64_t kv_dim, int64_t ffn, int64_t head_dim, double eps,
-               double *work, uint16_t *work16, uint16_t *h_out)
+               double *work, uint16_t *work16, double *t2, uint16_t *z_out)
 {
     double *q = work;
     double *k = q + (int64_t)batch * q_dim;
     double *v = k + (int64_t)batch * kv_dim;
     double *o = v + (int64_t)batch * kv_dim;
-    double *g = o + (int64_t)batch * hidden;
+    double *t1 = o + (int64_t)batch * hidden;
+    double *dn = t1 + (int64_t)batch * hidden;
+    double *g = dn + (int64_t)batch * hidden;
     double *u = g + (int64_t)batch * ffn;
-    double *dn = q; /* reuse: q is dead by then and large enough only if q_dim >= hidden */
-    uint16_t *x = work16;
-    uint16_t *attn = x + (int64_t)batch * hidden;
-    uint16_t *h1 = attn + (int64_t)batch * q_dim;
-    uint16_t *act = h1 + (int64_t)batch * hidden;
+    uint16_t *attn = work16;
+    uint16_t *z1 = attn + (int64_t)batch * q_dim;
+    uint16_t *act = z1 + (int64_t)batch * hidden;
 
-    ora_rmsnorm(h, batch, hidden, eps, x);
-    ora_gemv(wts[0], x, q_dim, hidden, batch, 0, q_dim, q, 0);
-    ora_gemv(wts[1], x, kv_dim, hidden, batch, 0, kv_dim, k, 0);
-    ora_gemv(wts[2], x, kv_dim, hidden, batch, 0, kv_dim, v, 0);
+    ora_gemv(wts[0], z, q_dim, hidden, batch, 0, q_dim, q, 0);
+    ora_gemv(wts[1], z, kv_dim, hidden, batch, 0, kv_dim, k, 0);
+    ora_gemv(wts[2], z, kv_dim, hidden, batch, 0, kv_dim, v, 0);
     ora_attn_ctx1(v, batch, q_dim, kv_dim, head_dim, attn);
     ora_gemv(wts[3], attn, hidden, q_dim, batch, 0, hidden, o, 0);
-    ora_residual(h, o, (int64_t)batch * hidden, h1);
-    ora_rmsnorm(h1, batch, hidden, eps, x);
-    ora_gemv(wts[4], x, ffn, hidden, batch, 0, ffn, g, 0);
-    ora_gemv(wts[5], x, ffn, hidden, batch, 0, ffn, u, 0);
+    ora_add(z, o, (int64_t)batch * hidden, t1);
+    ora_rmsnorm_d(t1, batch, hidden, eps, z1);
+    ora_gemv(wts[4], z1, ffn, hidden, batch, 0, ffn, g, 0);
+    ora_gemv(wts[5], z1, ffn, hidden, batch, 0, ffn, u, 0);
     ora_silu_mul(g, u, (int64_t)batch * ffn, act);
-    if (q_dim < hidden)
-        dn = g; /* g is dead after silu_mul and ffn >= hidden in every Llama shape */
     ora_gemv(wts[6], act, hidden, ffn, batch, 0, hidden, dn, 0);
-    ora_residual(h1, dn, (int64_t)batch * hidden, h_out);
+    ora_add(z1, dn, (int64_t)batch * hidden, t2);
+    ora_rmsnorm_d(t2, batch, hidden, eps, z_out);
 }

@@ -260,10 +260,33 @@ def pin_glue(lib):
     act = ora.silu_mul(g, u, lib=lib).view(np.float16).astype(np.float64)
     assert act[0] == 0 and act[1] == 30.0 and abs(act[2]) < 1e-9
     assert abs(act[3] - 0.7310585786) < 1e-3 and abs(act[4] + 0.2689414214) < 1e-3
-    # residual add of small integers is exact
+    # residual sum of small integers is exact
     hr = _f16(np.arange(-4, 4, dtype=np.float64))
-    r = ora.residual(hr, np.full(8, 2.0), lib=lib)
-    assert np.array_equal(r, _f16(np.arange(-2, 6, dtype=np.float64)))
+    r = ora.add(hr, np.full(8, 2.5), lib=lib)
+    assert np.array_equal(r, np.arange(-4, 4, dtype=np.float64) + 2.5)
+    # RMSNorm of a double vector agrees with the binary16 one on binary16 inputs,
+    # and is invariant to a power-of-two scale
+    t = hv[0].astype(np.float16).astype(np.float64)
+    assert np.array_equal(ora.rmsnorm_d(t, 1, 256, 1e-5, lib=lib), ora.rmsnorm(_f16(t), 1, 256, 1e-5, lib=lib))
+    assert np.array_equal(ora.rmsnorm_d(t * 8, 1, 256, 0.0, lib=lib), ora.rmsnorm_d(t, 1, 256, 0.0, lib=lib))
+    # a layer of all-8 codes has every projection zero: t1 = z, z1 = norm(z),
+    # act = 0, t2 = z1, so the output is norm(norm(z))
+    hid, qd, kvd, ffn, hd = 64, 64, 32, 128, 16
+    zero_w = []
+    for (n, k) in synth.layer_dims(hid, qd, kvd, ffn):
+        blk = np.concatenate([[0x00, 0x3C], [0x88] * 16]).astype(np.uint8)
+        zero_w.append(np.tile(blk, n * k // 32))
+    z = ora.rmsnorm(_f16(rng.standard_normal((1, hid))), 1, hid, 1e-5, lib=lib)
+    zo, t2 = ora.layer(zero_w, z, 1, hid, qd, kvd, ffn, hd, lib=lib)
+    z1 = ora.rmsnorm(z, 1, hid, 1e-5, lib=lib)
+    assert np.array_equal(t2, z1.view(np.float16).astype(np.float64))
+    assert np.array_equal(zo, ora.rmsnorm(z1, 1, hid, 1e-5, lib=lib))
+    # with random weights the layer output is still unit-RMS (it is a
+    # normalised residual sum) and t2 is not
+    rnd_w = [synth.q4_matrix(n, k, 4, p) for p, (n, k) in enumerate(synth.layer_dims(hid, qd, kvd, ffn))]
+    zo, t2 = ora.layer(rnd_w, z, 1, hid, qd, kvd, ffn, hd, lib=lib)
+    zv = zo.view(np.float16).astype(np.float64)
+    assert abs((zv ** 2).mean() - 1) < 2e-3 and abs((t2 ** 2).mean() - 1) > 0.1
     # context-1 attention: query head qh reads value head qh // group
     q_dim, kv_dim, hd = 8 * 4, 2 * 4, 4          # 8 query heads, 2 value heads
     v = np.arange(kv_dim, dtype=np.float64)       # value head j holds 4j..4j+3

@@ -66,7 +66,7 @@ def test_workspace_layout(lib):
     vals = [offs[n] for n in q4.WS_NAMES]
     assert vals == sorted(vals) and all(v % 256 == 0 for v in vals)
     assert offs["qkv"] - offs["program"] >= 32 * 4 * 64
-    assert total - offs["hmid"] >= 2 * 4096
+    assert total - offs["t2"] >= 4 * 4096
     with pytest.raises(q4.Q4Error):
         q4.q4_workspace_layout(shape, 0, 1)
     with pytest.raises(q4.Q4Error):

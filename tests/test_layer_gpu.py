@@ -47,28 +47,29 @@ def test_one_layer_step_by_step(cfg):
     st = Stack(cfg, 1, seed=21)
     h0 = synth.activations(1, cfg["hidden"], 22)
     h1 = st.run(h0)
-    check_layer(cfg, 21, 0, h0, h1, read_ws(st.ws, st.offs, cfg))
+    check_layer(cfg, 21, 0, read_ws(st.ws, st.offs, cfg), h1, h_in16=h0)
     st.close()
 
 
 def test_last_layer_of_a_stack_and_drift():
     cfg, L = SMALL, 4
-    st = Stack(cfg, L, seed=5)
     h0 = synth.activations(1, cfg["hidden"], 6)
-    # GPU: all layers at once; the workspace then holds the last layer's intermediates
-    hL = st.run(h0)
-    # the input of the last layer: run the first L-1 layers on their own
+    # the input of the last layer: the residual sum after the first L-1 layers
     st_prev = Stack(cfg, L - 1, seed=5)
-    h_prev = st_prev.run(h0)
-    check_layer(cfg, 5, L - 1, h_prev, hL, read_ws(st.ws, st.offs, cfg))
+    st_prev.run(h0)
+    t_prev = read_ws(st_prev.ws, st_prev.offs, cfg)["t2"]
+    # GPU: all layers at once; the workspace then holds the last layer's intermediates
+    st = Stack(cfg, L, seed=5)
+    hL = st.run(h0)
+    check_layer(cfg, 5, L - 1, read_ws(st.ws, st.offs, cfg), hL, t_prev=t_prev)
     # end-to-end against the oracle's own layer chain: drift stays small
-    ref = h0
+    z = ora.rmsnorm(h0, 1, cfg["hidden"])
     for l in range(L):
         ws = [synth.q4_matrix(n, k, 5, synth.tensor_id(l, p))
               for p, (n, k) in enumerate(synth.layer_dims(cfg["hidden"], cfg["q_dim"], cfg["kv_dim"], cfg["ffn"]))]
-        ref = ora.layer(ws, ref, 1, cfg["hidden"], cfg["q_dim"], cfg["kv_dim"], cfg["ffn"], cfg["head_dim"])
+        z, _ = ora.layer(ws, z, 1, cfg["hidden"], cfg["q_dim"], cfg["kv_dim"], cfg["ffn"], cfg["head_dim"])
     a = hL.view(np.float16).astype(np.float64)
-    b = ref.view(np.float16).astype(np.float64)
+    b = z.view(np.float16).astype(np.float64)
     assert np.linalg.norm(a - b) / np.linalg.norm(b) < 1e-2
     st.close()
     st_prev.close()
@@ -101,18 +102,22 @@ def test_new_hidden_pointer_rewrites_program():
 def _full_stack(cfg, n_layers, seed, count):
     st = Stack(cfg, n_layers, seed)
     h0 = synth.activations(1, cfg["hidden"], seed + 1)
-    hL = st.run(h0)
-    stats = read_ws(st.ws, st.offs, cfg)
-    # the last layer's own input: the state after n_layers-1 layers, from a second
-    # decoder over the same device weights
-    prev = q4.q4_decoder_create(st.shape, st.ptrs[:-1], 1, st.ws, st.ws_bytes, q4.Q4_DEC_FUSED)
+    # the last layer's own input: the residual sum after n_layers-1 layers, from a
+    # second decoder (own workspace) over the same device weights
+    ws2, offs2, nb2 = model.workspace(st.shape, n_layers - 1, 1)
+    prev = q4.q4_decoder_create(st.shape, st.ptrs[:-1], 1, ws2, nb2, q4.Q4_DEC_FUSED)
     h = dev_u16(h0.reshape(-1))
     q4.q4_layer_decode(prev, h)
     torch.cuda.synchronize()
-    h_prev = host_u16(h).reshape(1, -1)
+    assert q4.q4_decoder_status(prev) == 0
+    t_prev = read_ws(ws2, offs2, cfg)["t2"]
     q4.q4_decoder_destroy(prev)
-    check_layer(cfg, seed, n_layers - 1, h_prev, hL, stats, rows=sampled_rows(count, seed))
+    hL = st.run(h0)
+    stats = read_ws(st.ws, st.offs, cfg)
+    check_layer(cfg, seed, n_layers - 1, stats, hL, t_prev=t_prev, rows=sampled_rows(count, seed))
     assert np.all(np.isfinite(hL.view(np.float16).astype(np.float64)))
+    for name in ("qkv", "o", "g", "u", "dn", "t1", "t2"):
+        assert np.all(np.isfinite(stats[name])), name
     st.close()
 
 

@@ -31,6 +31,9 @@ MUTANTS = {
     "signed_magnitude": ("mag += fabs(p);", "mag += p;"),
     "attn_modulo": ("(qh / group) * head_dim", "(qh % n_kv) * head_dim"),
     "norm_no_mean": ("sqrt(ss / (double)dim + eps)", "sqrt(ss + eps)"),
+    "add_sign": ("t[i] = ora_half_to_double(z[i]) + o[i];", "t[i] = ora_half_to_double(z[i]) - o[i];"),
+    "layer_skips_norm": ("ora_add(z1, dn, (int64_t)batch * hidden, t2);\n    ora_rmsnorm_d(t2, batch, hidden, eps, z_out);",
+                         "ora_add(z1, dn, (int64_t)batch * hidden, t2);\n    ora_double_to_half_n(t2, (int64_t)batch * hidden, z_out);"),
     "silu_sign": ("exp(-g[i])", "exp(g[i])"),
 }
 

@@ -24,7 +24,7 @@ class Ring:
         self.blocks, self.hptrs = model.host_layers(self.shape, n_layers, seed, distinct=distinct)
         stride = model.layer_stride(self.shape)
         self.bufs = [torch.empty(stride, dtype=torch.uint8, device="cuda") for _ in range(2)]
-        self.ws, self.offs, self.ws_bytes = model.workspace(self.shape, 2, 1)
+        self.ws, self.offs, self.ws_bytes = model.workspace(self.shape, n_layers, 1)
         self.h = q4.q4_stream_create(self.shape, self.hptrs, 1, self.bufs[0], self.bufs[1], stride, self.ws,
                                      self.ws_bytes, flags)
 

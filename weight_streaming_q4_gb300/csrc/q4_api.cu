@@ -211,7 +211,7 @@ extern "C" int q4_workspace_layout(const q4_layer_shape* s, int n_layers, int ba
   const size_t B = static_cast<size_t>(batch);
   const size_t sizes[Q4_WS_COUNT] = {
       sizeof(Control),
-      sizeof(Phase) * 4 * static_cast<size_t>(n_layers),
+      sizeof(Phase) * (4 * static_cast<size_t>(n_layers) + 1),
       4 * B * (s->q_dim + 2 * s->kv_dim),
       4 * B * s->hidden,
       4 * B * s->ffn,
@@ -221,7 +221,8 @@ extern "C" int q4_workspace_layout(const q4_layer_shape* s, int n_layers, int ba
       2 * B * s->hidden,
       2 * B * s->q_dim,
       2 * B * s->hidden,
-      2 * B * s->hidden,
+      4 * B * s->hidden,
+      4 * B * s->hidden,
   };
   size_t pos = 0;
   for (int i = 0; i < Q4_WS_COUNT; ++i) {
@@ -238,8 +239,8 @@ namespace {
 struct Work {
   Control* ctl;
   Phase* prog;
-  float *qkv, *o, *g, *u, *dn;
-  uint16_t *act, *x, *attn, *x2, *hmid;
+  float *qkv, *o, *g, *u, *dn, *t1, *t2;
+  uint16_t *act, *x, *attn, *x2;
 };
 
 Work carve(void* ws, const size_t* off) {
@@ -256,35 +257,41 @@ Work carve(void* ws, const size_t* off) {
   w.x = reinterpret_cast<uint16_t*>(b + off[Q4_WS_X]);
   w.attn = reinterpret_cast<uint16_t*>(b + off[Q4_WS_ATTN]);
   w.x2 = reinterpret_cast<uint16_t*>(b + off[Q4_WS_X2]);
-  w.hmid = reinterpret_cast<uint16_t*>(b + off[Q4_WS_HMID]);
+  w.t1 = reinterpret_cast<float*>(b + off[Q4_WS_T1]);
+  w.t2 = reinterpret_cast<float*>(b + off[Q4_WS_T2]);
   return w;
 }
 
 // The four phases of one decoder layer whose merged weight block is `wl`
-// (PIPO summary, "Offloading architecture": the layer is the unit).
-bool layer_phases(const q4_layer_shape& s, const uint8_t* wl, uint16_t* h, const Work& w, Phase out[4]) {
+// (PIPO summary, "Offloading architecture": the layer is the unit).  The
+// layer input is normalised from `in16` (binary16, first layer) or from the
+// previous layer's fp32 residual sum (`in32`); the normalised input is kept
+// in w.x and is the residual base of the attention half, whose fp32 sum goes
+// to w.t1; the normalised w.t1 (w.x2) is the residual base of the feed-forward
+// half, whose fp32 sum goes to w.t2.
+bool layer_phases(const q4_layer_shape& s, const uint8_t* wl, const uint16_t* in16, const Work& w, Phase out[4]) {
   size_t off[7];
   if (q4_layer_offsets(&s, off, nullptr) != Q4_OK) return false;
   memset(out, 0, 4 * sizeof(Phase));
   // q, k, v: one matrix of q_dim + 2 kv_dim rows (they are consecutive in the block)
   Phase& a = out[0];
   a.w0 = wl + off[Q4_PROJ_Q];
-  a.x_src = h;
+  a.x_src = in16 ? static_cast<const void*>(in16) : static_cast<const void*>(w.t2);
   a.y = w.qkv;
   a.n_rows = s.q_dim + 2 * s.kv_dim;
   a.k = s.hidden;
-  a.x_kind = q4::X_RMSNORM;
+  a.x_kind = in16 ? q4::X_NORM16 : q4::X_NORM32;
   a.epi_kind = q4::EPI_F32;
   a.x_ld = s.hidden;
   a.eps = s.eps;
   a.x_dbg = w.x;
-  // o, with the context-1 attention as its input and the residual add as its output
+  // o, with the context-1 attention as its input and the residual sum as its output
   Phase& b = out[1];
   b.w0 = wl + off[Q4_PROJ_O];
   b.x_src = w.qkv;
   b.y = w.o;
-  b.h = h;
-  b.aux16 = w.hmid;
+  b.y2 = w.t1;
+  b.res = w.x;
   b.n_rows = s.hidden;
   b.k = s.q_dim;
   b.x_kind = q4::X_ATTN;
@@ -298,23 +305,24 @@ bool layer_phases(const q4_layer_shape& s, const uint8_t* wl, uint16_t* h, const
   Phase& c = out[2];
   c.w0 = wl + off[Q4_PROJ_GATE];
   c.w1 = wl + off[Q4_PROJ_UP];
-  c.x_src = h;
+  c.x_src = w.t1;
   c.y = w.g;
   c.y2 = w.u;
   c.aux16 = w.act;
   c.n_rows = s.ffn;
   c.k = s.hidden;
-  c.x_kind = q4::X_RMSNORM;
+  c.x_kind = q4::X_NORM32;
   c.epi_kind = q4::EPI_SILU;
   c.x_ld = s.hidden;
   c.eps = s.eps;
   c.x_dbg = w.x2;
-  // down, with the residual add
+  // down, with the residual sum
   Phase& d = out[3];
   d.w0 = wl + off[Q4_PROJ_DOWN];
   d.x_src = w.act;
   d.y = w.dn;
-  d.h = h;
+  d.y2 = w.t2;
+  d.res = w.x2;
   d.n_rows = s.hidden;
   d.k = s.ffn;
   d.x_kind = q4::X_F16;
@@ -325,11 +333,36 @@ bool layer_phases(const q4_layer_shape& s, const uint8_t* wl, uint16_t* h, const
   return true;
 }
 
+// The closing phase of a stack: no product, CTA 0 writes the normalised last
+// residual sum to the caller's hidden-state buffer.
+bool final_phase(const q4_layer_shape& s, uint16_t* h_out, const Work& w, Phase* out) {
+  memset(out, 0, sizeof(Phase));
+  out->x_src = w.t2;
+  out->n_rows = 0;
+  out->k = s.hidden;
+  out->x_kind = q4::X_NORM32;
+  out->epi_kind = q4::EPI_F32;
+  out->x_ld = s.hidden;
+  out->eps = s.eps;
+  out->x_dbg = h_out;
+  return tile_phase(*out);
+}
+
+// Phase program of a whole stack: 4 phases per layer and the closing phase.
+bool stack_program(const q4_layer_shape& s, const std::vector<const uint8_t*>& layers, uint16_t* h,
+                   const Work& w, std::vector<Phase>& prog) {
+  const int L = static_cast<int>(layers.size());
+  prog.assign(4 * static_cast<size_t>(L) + 1, Phase());
+  for (int l = 0; l < L; ++l)
+    if (!layer_phases(s, layers[l], l == 0 ? h : nullptr, w, &prog[4 * l])) return false;
+  return final_phase(s, h, w, &prog[4 * L]);
+}
+
 int check_layer_shape_for_engine(const q4_layer_shape& s) {
-  Phase tmp[4];
+  Phase tmp[5];
   Work w;
   memset(&w, 0, sizeof(w));
-  return layer_phases(s, nullptr, nullptr, w, tmp) ? Q4_OK : Q4_ERR_ARG;
+  return layer_phases(s, nullptr, nullptr, w, tmp) && final_phase(s, nullptr, w, &tmp[4]) ? Q4_OK : Q4_ERR_ARG;
 }
 
 int launch_layers(const Work& w, int first_phase, int n_phases, int grid, cudaStream_t s) {
@@ -366,9 +399,8 @@ struct q4_decoder {
 };
 
 static int decoder_write_program(q4_decoder* d, uint16_t* h, cudaStream_t s) {
-  std::vector<Phase> prog(4 * static_cast<size_t>(d->n_layers));
-  for (int l = 0; l < d->n_layers; ++l)
-    if (!layer_phases(d->shape, d->layers[l], h, d->w, &prog[4 * l])) return Q4_ERR_ARG;
+  std::vector<Phase> prog;
+  if (!stack_program(d->shape, d->layers, h, d->w, prog)) return Q4_ERR_ARG;
   // pageable source: the runtime stages it before returning, so `prog` may go
   Q4_CUDA(cudaMemcpyAsync(d->w.prog, prog.data(), prog.size() * sizeof(Phase), cudaMemcpyHostToDevice, s));
   d->cur_h = h;
@@ -376,9 +408,10 @@ static int decoder_write_program(q4_decoder* d, uint16_t* h, cudaStream_t s) {
 }
 
 static int decoder_enqueue(q4_decoder* d, cudaStream_t s) {
-  if (d->mode == Q4_DEC_FUSED) return launch_layers(d->w, 0, 4 * d->n_layers, d->grid, s);
-  for (int l = 0; l < d->n_layers; ++l) {
-    int st = launch_layers(d->w, 4 * l, 4, d->grid, s);
+  const int L = d->n_layers;
+  if (d->mode == Q4_DEC_FUSED) return launch_layers(d->w, 0, 4 * L + 1, d->grid, s);
+  for (int l = 0; l < L; ++l) {   // the last launch also runs the closing phase
+    int st = launch_layers(d->w, 4 * l, l == L - 1 ? 5 : 4, d->grid, s);
     if (st != Q4_OK) return st;
   }
   return Q4_OK;
@@ -515,7 +548,7 @@ extern "C" int q4_stream_create(q4_stream** out, const q4_layer_shape* shape, co
     if (!aligned(host_layers[l], 16)) return Q4_ERR_ALIGN;
   }
   size_t off[Q4_WS_COUNT], need = 0;
-  int st = q4_workspace_layout(shape, 2, batch, off, &need);
+  int st = q4_workspace_layout(shape, n_layers, batch, off, &need);
   if (st != Q4_OK) return st;
   if (workspace_bytes < need) return Q4_ERR_OOM;
   DeviceInfo* dev = nullptr;
@@ -553,10 +586,11 @@ extern "C" int q4_stream_layers(q4_stream* r, uint16_t* hidden_io, void* compute
   if (!aligned(hidden_io, 16)) return Q4_ERR_ALIGN;
   cudaStream_t cs = static_cast<cudaStream_t>(compute_stream);
   if (hidden_io != r->cur_h) {
-    // one 4-phase program per staging buffer, both reading/writing hidden_io
-    std::vector<Phase> prog(8);
-    for (int b = 0; b < 2; ++b)
-      if (!layer_phases(r->shape, r->buf[b], hidden_io, r->w, &prog[4 * b])) return Q4_ERR_ARG;
+    // layer i computes on staging buffer i % 2
+    std::vector<const uint8_t*> bufs(r->n_layers);
+    for (int i = 0; i < r->n_layers; ++i) bufs[i] = r->buf[i & 1];
+    std::vector<Phase> prog;
+    if (!stack_program(r->shape, bufs, hidden_io, r->w, prog)) return Q4_ERR_ARG;
     Q4_CUDA(cudaMemcpyAsync(r->w.prog, prog.data(), prog.size() * sizeof(Phase), cudaMemcpyHostToDevice, cs));
     r->cur_h = hidden_io;
   }
@@ -573,7 +607,7 @@ extern "C" int q4_stream_layers(q4_stream* r, uint16_t* hidden_io, void* compute
     Q4_CUDA(cudaEventRecord(r->loaded[b], r->copy));
     // compute stream: layer i once its weights have landed
     Q4_CUDA(cudaStreamWaitEvent(cs, r->loaded[b], 0));
-    int st = launch_layers(r->w, 4 * b, 4, r->grid, cs);
+    int st = launch_layers(r->w, 4 * i, i == r->n_layers - 1 ? 5 : 4, r->grid, cs);
     if (st != Q4_OK) return st;
     if (r->flags & Q4_STREAM_POISON) Q4_CUDA(q4::poison_launch(r->buf[b], n_blocks, cs));
     Q4_CUDA(cudaEventRecord(r->freed[b], cs));

@@ -20,14 +20,15 @@ constexpr int kMaxBatch = 16;
 // How the input vector x of a phase is formed (per batch row).
 enum XKind : int {
   X_F16 = 0,      // x = src (binary16 [batch][k])
-  X_RMSNORM = 1,  // x = f16(h * rsqrt(mean(h^2) + eps)), h = src (binary16 [batch][k])
+  X_NORM16 = 1,   // x = f16(t * rsqrt(mean(t^2) + eps)), t = src (binary16 [batch][k])
   X_ATTN = 2,     // context-1 attention: x[i] = f16(v[(i/hd)/group*hd + i%hd]), v = fp32 src
+  X_NORM32 = 3,   // as X_NORM16 with an fp32 src
 };
 
 // What the epilogue does with the row sums.
 enum EpiKind : int {
   EPI_F32 = 0,    // y[b][n] = sum
-  EPI_RESID = 1,  // y[b][n] = sum; h[b][n] = f16(h[b][n] + sum); hcopy[b][n] = new h
+  EPI_RESID = 1,  // y[b][n] = sum; y2[b][n] = res[b][n] + sum (fp32 residual sum)
   EPI_SILU = 2,   // two matrices: y = g, y2 = u, act[b][n] = f16(silu(g) * u)
 };
 
@@ -39,9 +40,9 @@ struct Phase {
   const uint8_t* w1;      // second matrix (EPI_SILU only)
   const void* x_src;      // input per XKind
   float* y;               // fp32 [batch][n_rows]
-  float* y2;              // fp32 [batch][n_rows] (EPI_SILU: u)
-  uint16_t* h;            // EPI_RESID: residual stream binary16 [batch][n_rows], updated in place
-  uint16_t* aux16;        // EPI_RESID: copy of the new h; EPI_SILU: act binary16 [batch][n_rows]
+  float* y2;              // fp32 [batch][n_rows]: EPI_SILU u, EPI_RESID the residual sum
+  const uint16_t* res;    // EPI_RESID: residual input binary16 [batch][n_rows]
+  uint16_t* aux16;        // EPI_SILU: act binary16 [batch][n_rows]
   uint16_t* x_dbg;        // if not null, CTA 0 stores the formed x here (binary16 [batch][k])
   int n_rows;
   int k;

@@ -108,11 +108,11 @@ __device__ __forceinline__ void set_status(Control* ctl, int bits) {
 __device__ void form_x(const Phase& ph, int j, int kt, float2* xs2, float* red_ss, bool write_dbg) {
   const int ct = threadIdx.x;   // consumer thread 0..255
   float r = 1.0f;
-  if (ph.x_kind == X_RMSNORM) {
-    const __half* h = static_cast<const __half*>(ph.x_src);
+  if (ph.x_kind == X_NORM16 || ph.x_kind == X_NORM32) {
     float ss = 0.f;
     for (int i = ct; i < ph.k; i += kConsumerThreads) {
-      const float v = __half2float(h[i]);
+      const float v = (ph.x_kind == X_NORM16) ? __half2float(static_cast<const __half*>(ph.x_src)[i])
+                                              : static_cast<const float*>(ph.x_src)[i];
       ss = fmaf(v, v, ss);
     }
 #pragma unroll
@@ -140,8 +140,10 @@ __device__ void form_x(const Phase& ph, int j, int kt, float2* xs2, float* red_s
           __half xv;
           if (ph.x_kind == X_F16) {
             xv = static_cast<const __half*>(ph.x_src)[col];
-          } else if (ph.x_kind == X_RMSNORM) {
+          } else if (ph.x_kind == X_NORM16) {
             xv = __float2half_rn(__half2float(static_cast<const __half*>(ph.x_src)[col]) * r);
+          } else if (ph.x_kind == X_NORM32) {
+            xv = __float2half_rn(static_cast<const float*>(ph.x_src)[col] * r);
           } else {
             const int hd = ph.head_dim;
             const int src = ph.attn_off + ((col / hd) / ph.group) * hd + (col % hd);
@@ -164,10 +166,7 @@ __device__ __forceinline__ void epilogue(const Phase& ph, int n, float s, float 
     ph.y[n] = s;
   } else if (ph.epi_kind == EPI_RESID) {
     ph.y[n] = s;
-    const float hv = __half2float(__ushort_as_half(ph.h[n])) + s;
-    const unsigned short hb = __half_as_ushort(__float2half_rn(hv));
-    ph.h[n] = hb;
-    if (ph.aux16) ph.aux16[n] = hb;
+    ph.y2[n] = __half2float(__ushort_as_half(ph.res[n])) + s;
   } else {
     ph.y[n] = s;
     ph.y2[n] = s2;

@@ -63,7 +63,7 @@ def host_layers(shape: _lib.LayerShape, n_layers: int, seed: int, distinct: int 
 
 
 def workspace(shape: _lib.LayerShape, n_layers: int, batch: int, device="cuda"):
-    """A device workspace for a decoder (n_layers) or a ring (n_layers=2): (tensor, offsets, bytes)."""
+    """A device workspace for a decoder or a ring of n_layers layers: (tensor, offsets, bytes)."""
     offs, total = _lib.q4_workspace_layout(shape, n_layers, batch)
     ws = torch.zeros(total, dtype=torch.uint8, device=device)
     return ws, offs, total
