@@ -103,56 +103,108 @@ __device__ __forceinline__ void set_status(Control* ctl, int bits) {
   atomicOr(ctl ? &ctl->status : &g_status, bits);
 }
 
-// Form the thread's slice of x for a phase: xs2 receives kt/2 float2 in the
-// order pair_dot expects, each value pre-scaled by 2^-shift.
-__device__ void form_x(const Phase& ph, int j, int kt, float2* xs2, float* red_ss, bool write_dbg) {
-  const int ct = threadIdx.x;   // consumer thread 0..255
-  float r = 1.0f;
-  if (ph.x_kind == X_NORM16 || ph.x_kind == X_NORM32) {
-    float ss = 0.f;
-    for (int i = ct; i < ph.k; i += kConsumerThreads) {
-      const float v = (ph.x_kind == X_NORM16) ? __half2float(static_cast<const __half*>(ph.x_src)[i])
-                                              : static_cast<const float*>(ph.x_src)[i];
-      ss = fmaf(v, v, ss);
+// Load 32 consecutive columns [c0, c0 + 32) of the phase input (before any
+// normalisation) as floats, with 16-byte vector loads.
+__device__ __forceinline__ void load_block_x(const Phase& ph, int c0, float* v) {
+  if (ph.x_kind == X_F16 || ph.x_kind == X_NORM16) {
+    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __half*>(ph.x_src) + c0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 u = p[i];
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[t]));
+        v[8 * i + 2 * t] = f.x;
+        v[8 * i + 2 * t + 1] = f.y;
+      }
     }
+  } else {
+    const float* src = static_cast<const float*>(ph.x_src);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if ((ct & 31) == 0) red_ss[ct >> 5] = ss;
-    named_bar_sync(1, kConsumerThreads);
-    float tot = 0.f;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) tot += red_ss[w];
-    r = rsqrtf(tot / static_cast<float>(ph.k) + ph.eps);
-    named_bar_sync(1, kConsumerThreads);   // red_ss is reused by the next phase
+    for (int i = 0; i < 8; ++i) {
+      int c = c0 + 4 * i;
+      if (ph.x_kind == X_ATTN) {
+        const int hd = ph.head_dim;
+        c = ph.attn_off + ((c / hd) / ph.group) * hd + (c % hd);   // 4 columns stay in one head
+      }
+      const float4 f = *reinterpret_cast<const float4*>(src + c);
+      v[4 * i] = f.x;
+      v[4 * i + 1] = f.y;
+      v[4 * i + 2] = f.z;
+      v[4 * i + 3] = f.w;
+    }
   }
+}
+
+// Sum of squares of the phase input over all k columns (CTA-wide, fixed order).
+__device__ float input_rms_scale(const Phase& ph, float* red_ss) {
+  const int ct = threadIdx.x;
+  float ss = 0.f;
+  if (ph.x_kind == X_NORM16) {
+    const uint4* p = reinterpret_cast<const uint4*>(ph.x_src);
+    for (int i = ct; i < ph.k / 8; i += kConsumerThreads) {
+      const uint4 u = p[i];
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[t]));
+        ss = fmaf(f.x, f.x, ss);
+        ss = fmaf(f.y, f.y, ss);
+      }
+    }
+  } else {
+    const float4* p = reinterpret_cast<const float4*>(ph.x_src);
+    for (int i = ct; i < ph.k / 4; i += kConsumerThreads) {
+      const float4 f = p[i];
+      ss = fmaf(f.x, f.x, ss);
+      ss = fmaf(f.y, f.y, ss);
+      ss = fmaf(f.z, f.z, ss);
+      ss = fmaf(f.w, f.w, ss);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((ct & 31) == 0) red_ss[ct >> 5] = ss;
+  named_bar_sync(1, kConsumerThreads);
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < kConsumerWarps; ++w) tot += red_ss[w];
+  named_bar_sync(1, kConsumerThreads);   // red_ss is reused by the next phase
+  return rsqrtf(tot / static_cast<float>(ph.k) + ph.eps);
+}
+
+// Form the thread's slice of x for a phase: xs2 receives kt/2 float2 in the
+// order pair_dot expects, each value pre-scaled by 2^-shift.  Columns
+// [j*kt, (j+1)*kt) belong to the thread.
+__device__ void form_x(const Phase& ph, int j, int kt, float2* xs2, float* red_ss, bool write_dbg) {
+  const bool norm = ph.x_kind == X_NORM16 || ph.x_kind == X_NORM32;
+  const float r = norm ? input_rms_scale(ph, red_ss) : 1.0f;
   const int k0 = j * kt;
 #pragma unroll
   for (int blk = 0; blk < 4; ++blk) {
     if (blk * 32 >= kt) break;
+    float v[32];
+    load_block_x(ph, k0 + blk * 32, v);
+    __half xv[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      // binary16 rounding of the input: exact for X_F16, RNE for the others
+      xv[e] = (ph.x_kind == X_F16) ? __float2half_rn(v[e]) : __float2half_rn(norm ? v[e] * r : v[e]);
+    }
+    if (write_dbg) {
+      uint4* d = reinterpret_cast<uint4*>(ph.x_dbg + k0 + blk * 32);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) d[i] = reinterpret_cast<const uint4*>(xv)[i];
+    }
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
 #pragma unroll
       for (int e = 0; e < 8; e += 2) {
-        float v2[2];
-#pragma unroll
-        for (int l = 0; l < 2; ++l) {
-          const int col = k0 + blk * 32 + 4 * m + elem_off(e + l);
-          __half xv;
-          if (ph.x_kind == X_F16) {
-            xv = static_cast<const __half*>(ph.x_src)[col];
-          } else if (ph.x_kind == X_NORM16) {
-            xv = __float2half_rn(__half2float(static_cast<const __half*>(ph.x_src)[col]) * r);
-          } else if (ph.x_kind == X_NORM32) {
-            xv = __float2half_rn(static_cast<const float*>(ph.x_src)[col] * r);
-          } else {
-            const int hd = ph.head_dim;
-            const int src = ph.attn_off + ((col / hd) / ph.group) * hd + (col % hd);
-            xv = __float2half_rn(static_cast<const float*>(ph.x_src)[src]);
-          }
-          if (write_dbg) ph.x_dbg[col] = __half_as_ushort(xv);
-          v2[l] = __half2float(xv) * (1.0f / static_cast<float>(1 << elem_shift(e + l)));
-        }
-        xs2[blk * 16 + m * 4 + e / 2] = make_float2(v2[0], v2[1]);
+        const float a = __half2float(xv[4 * m + elem_off(e)]) * (1.0f / static_cast<float>(1 << elem_shift(e)));
+        const float b =
+            __half2float(xv[4 * m + elem_off(e + 1)]) * (1.0f / static_cast<float>(1 << elem_shift(e + 1)));
+        xs2[blk * 16 + m * 4 + e / 2] = make_float2(a, b);
       }
     }
   }
