@@ -38,8 +38,8 @@
  *     report, and the kernel returns.
  *   - Weight, x and y pointers must be 16-byte aligned (Q4_ERR_ALIGN).
  *   - k must be a multiple of 32 (one block); the streaming kernel needs k in
- *     {256, 512, 1024} or a multiple of 2048 up to 16384, or a multiple of
- *     4096 up to 32768; other k use a plain (slower) kernel.
+ *     {256, 512, 1024} or a multiple of 2048 up to 30720; other k use a
+ *     plain (slower) kernel.
  *   - x is binary16 [batch][k] row-major, y is fp32 [batch][n] row-major and
  *     is overwritten, not accumulated.  1 <= batch <= 16.
  *   - Accuracy: |y - sum_k w*x| <= 1e-3 * sum_k |w*x| + 1e-5 per element;
@@ -174,7 +174,8 @@ int q4_layer_offsets(const q4_layer_shape *shape, size_t offsets[7], size_t *lay
 #define Q4_WS_X2 10       /* binary16 [batch][hidden]: z1 = f16(norm(t1)) */
 #define Q4_WS_T1 11       /* fp32 [batch][hidden]: t1 = z + Wo a */
 #define Q4_WS_T2 12       /* fp32 [batch][hidden]: t2 = z1 + Wdown act */
-#define Q4_WS_COUNT 13
+#define Q4_WS_SS 13       /* fp32 [2][256]: per-CTA sums of squares of t1 and t2 */
+#define Q4_WS_COUNT 14
 
 /*
  * Byte offsets of the workspace regions for a decoder or a stream ring of

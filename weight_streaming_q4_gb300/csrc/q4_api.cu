@@ -66,29 +66,28 @@ int device_info(DeviceInfo** out) {
   return Q4_OK;
 }
 
-// Columns per consumer thread for the streaming engine, or 0 if the engine
-// cannot run rows of this width (then the plain kernel is used).
-int engine_kt(int k, bool dual) {
-  if (k < 256 || k % 256 != 0) return 0;   // rows must start 16-byte aligned
-  if (k <= 16384) {
-    const int team = k / 64;
-    if (team % 32 == 0 || 32 % team == 0) return 64;
-    return 0;
-  }
-  if (!dual && k <= 32768 && k % 4096 == 0) return 128;
-  return 0;
+// Whether the streaming engine can run rows of width k: every consumer
+// thread owns 64 columns, a row team is k/64 threads, and a team either fills
+// whole warps or divides one; rows must start 16-byte aligned (k % 256 == 0).
+bool engine_ok(int k) {
+  if (k < 256 || k % 256 != 0) return false;
+  const int team = k / q4::kKT;
+  if (team > q4::kConsumerThreads) return false;
+  return team % 32 == 0 || 32 % team == 0;
 }
 
-// Fill the tiling fields of a phase (kt, rows per unit, units).
+// Fill the tiling fields of a phase: a work unit gives every team two rows
+// (two rows of one matrix, or the same row of both matrices of a pair).
 bool tile_phase(Phase& ph) {
-  const bool dual = ph.epi_kind == q4::EPI_SILU;
-  const int kt = engine_kt(ph.k, dual);
-  if (kt == 0) return false;
-  const int team = ph.k / kt;
-  const int teams = q4::kConsumerThreads / team;
-  const int rpt = kt == 64 ? 2 : 1;
-  ph.kt = kt;
-  ph.rows_per_unit = dual ? teams : teams * rpt;
+  if (!engine_ok(ph.k)) return false;
+  const int team = ph.k / q4::kKT;
+  const int row_bytes = ph.k / q4::kQK * q4::kBlockBytes;
+  int teams = q4::kConsumerThreads / team;
+  const int fit = q4::kStageBytes / (2 * row_bytes);
+  if (teams > fit) teams = fit;
+  if (teams < 1) return false;
+  ph.teams = teams;
+  ph.rows_per_unit = ph.epi_kind == q4::EPI_SILU ? teams : 2 * teams;
   ph.units = (ph.n_rows + ph.rows_per_unit - 1) / ph.rows_per_unit;
   return true;
 }
@@ -133,12 +132,12 @@ extern "C" int q4_gemv_ex(const void* w, const uint16_t* x, float* y, int n, int
   int st = check_gemv(w, x, y, n, k, batch);
   if (st != Q4_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (kernel == Q4_KERNEL_AUTO) kernel = (batch == 1 && engine_kt(k, false)) ? Q4_KERNEL_STREAM : Q4_KERNEL_SIMPLE;
+  if (kernel == Q4_KERNEL_AUTO) kernel = (batch == 1 && engine_ok(k)) ? Q4_KERNEL_STREAM : Q4_KERNEL_SIMPLE;
   if (kernel == Q4_KERNEL_SIMPLE) {
     Q4_CUDA(q4::simple_launch(static_cast<const uint8_t*>(w), x, y, n, k, batch, s));
     return Q4_OK;
   }
-  if (kernel != Q4_KERNEL_STREAM || batch != 1 || !engine_kt(k, false)) return Q4_ERR_ARG;
+  if (kernel != Q4_KERNEL_STREAM || batch != 1 || !engine_ok(k)) return Q4_ERR_ARG;
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != Q4_OK) return st;
   EngineArgs a;
@@ -223,6 +222,7 @@ extern "C" int q4_workspace_layout(const q4_layer_shape* s, int n_layers, int ba
       2 * B * s->hidden,
       4 * B * s->hidden,
       4 * B * s->hidden,
+      4 * 2 * static_cast<size_t>(q4::kMaxGrid),
   };
   size_t pos = 0;
   for (int i = 0; i < Q4_WS_COUNT; ++i) {
@@ -240,6 +240,7 @@ struct Work {
   Control* ctl;
   Phase* prog;
   float *qkv, *o, *g, *u, *dn, *t1, *t2;
+  float *ss1, *ss2;   // per-CTA sums of squares of t1 and t2
   uint16_t *act, *x, *attn, *x2;
 };
 
@@ -259,6 +260,8 @@ Work carve(void* ws, const size_t* off) {
   w.x2 = reinterpret_cast<uint16_t*>(b + off[Q4_WS_X2]);
   w.t1 = reinterpret_cast<float*>(b + off[Q4_WS_T1]);
   w.t2 = reinterpret_cast<float*>(b + off[Q4_WS_T2]);
+  w.ss1 = reinterpret_cast<float*>(b + off[Q4_WS_SS]);
+  w.ss2 = w.ss1 + q4::kMaxGrid;
   return w;
 }
 
@@ -281,6 +284,7 @@ bool layer_phases(const q4_layer_shape& s, const uint8_t* wl, const uint16_t* in
   a.n_rows = s.q_dim + 2 * s.kv_dim;
   a.k = s.hidden;
   a.x_kind = in16 ? q4::X_NORM16 : q4::X_NORM32;
+  a.ss_in = w.ss2;
   a.epi_kind = q4::EPI_F32;
   a.x_ld = s.hidden;
   a.eps = s.eps;
@@ -292,6 +296,7 @@ bool layer_phases(const q4_layer_shape& s, const uint8_t* wl, const uint16_t* in
   b.y = w.o;
   b.y2 = w.t1;
   b.res = w.x;
+  b.ss_out = w.ss1;
   b.n_rows = s.hidden;
   b.k = s.q_dim;
   b.x_kind = q4::X_ATTN;
@@ -312,6 +317,7 @@ bool layer_phases(const q4_layer_shape& s, const uint8_t* wl, const uint16_t* in
   c.n_rows = s.ffn;
   c.k = s.hidden;
   c.x_kind = q4::X_NORM32;
+  c.ss_in = w.ss1;
   c.epi_kind = q4::EPI_SILU;
   c.x_ld = s.hidden;
   c.eps = s.eps;
@@ -323,6 +329,7 @@ bool layer_phases(const q4_layer_shape& s, const uint8_t* wl, const uint16_t* in
   d.y = w.dn;
   d.y2 = w.t2;
   d.res = w.x2;
+  d.ss_out = w.ss2;
   d.n_rows = s.hidden;
   d.k = s.ffn;
   d.x_kind = q4::X_F16;
@@ -338,6 +345,7 @@ bool layer_phases(const q4_layer_shape& s, const uint8_t* wl, const uint16_t* in
 bool final_phase(const q4_layer_shape& s, uint16_t* h_out, const Work& w, Phase* out) {
   memset(out, 0, sizeof(Phase));
   out->x_src = w.t2;
+  out->ss_in = w.ss2;
   out->n_rows = 0;
   out->k = s.hidden;
   out->x_kind = q4::X_NORM32;
@@ -442,7 +450,7 @@ extern "C" int q4_decoder_create(q4_decoder** out, const q4_layer_shape* shape, 
   d->n_layers = n_layers;
   d->batch = batch;
   d->mode = mode;
-  d->grid = dev->sm_count;   // one persistent CTA per SM (co-resident: cooperative launch)
+  d->grid = dev->sm_count < q4::kMaxGrid ? dev->sm_count : q4::kMaxGrid;   // one CTA per SM, co-resident
   d->layers.assign(reinterpret_cast<const uint8_t* const*>(layer_weights),
                    reinterpret_cast<const uint8_t* const*>(layer_weights) + n_layers);
   d->w = carve(workspace, off);
@@ -559,7 +567,7 @@ extern "C" int q4_stream_create(q4_stream** out, const q4_layer_shape* shape, co
   r->n_layers = n_layers;
   r->batch = batch;
   r->flags = flags;
-  r->grid = dev->sm_count;
+  r->grid = dev->sm_count < q4::kMaxGrid ? dev->sm_count : q4::kMaxGrid;
   r->host.assign(host_layers, host_layers + n_layers);
   r->buf[0] = static_cast<uint8_t*>(dev_buf0);
   r->buf[1] = static_cast<uint8_t*>(dev_buf1);

@@ -10,11 +10,15 @@ namespace q4 {
 
 constexpr int kQK = 32;              // weights per Q4_0 block
 constexpr int kBlockBytes = 18;      // binary16 scale + 16 code bytes
-constexpr int kConsumerWarps = 8;    // warps doing the arithmetic
+constexpr int kConsumerWarps = 15;   // warps doing the arithmetic (4 warps per SM sub-partition
+                                     // with the producer, so up to 128 registers per thread)
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;   // + one producer warp
-constexpr int kStageBytes = 18432;   // one work unit of weights in shared memory
-constexpr int kStages = 11;          // ring depth (11 * 18 KB = 198 KB)
+constexpr int kKT = 64;              // input columns each consumer thread keeps in registers
+constexpr int kStageBytes = 32256;   // one work unit of weights in shared memory
+constexpr int kStages = 6;           // ring depth (6 * 31.5 KB = 189 KB)
+constexpr int kRedFloats = 6144;     // per-warp row partials buffered until the phase ends
+constexpr int kMaxGrid = 256;        // CTAs (one per SM) a launch may use
 constexpr int kMaxBatch = 16;
 
 // How the input vector x of a phase is formed (per batch row).
@@ -43,6 +47,8 @@ struct Phase {
   float* y2;              // fp32 [batch][n_rows]: EPI_SILU u, EPI_RESID the residual sum
   const uint16_t* res;    // EPI_RESID: residual input binary16 [batch][n_rows]
   uint16_t* aux16;        // EPI_SILU: act binary16 [batch][n_rows]
+  float* ss_out;          // EPI_RESID: per-CTA sums of squares of y2 ([gridDim.x] floats)
+  const float* ss_in;     // X_NORM32: the producing phase's per-CTA sums of squares
   uint16_t* x_dbg;        // if not null, CTA 0 stores the formed x here (binary16 [batch][k])
   int n_rows;
   int k;
@@ -53,10 +59,10 @@ struct Phase {
   int head_dim;           // X_ATTN
   int group;              // X_ATTN: query heads per value head
   float eps;              // X_RMSNORM
-  int kt;                 // columns per consumer thread: 64 or 128
+  int teams;              // row teams of k/64 threads working side by side
   int units;              // work units in this phase
   int rows_per_unit;      // rows of each matrix per unit
-  int pad_[2];
+  int pad_;
 };
 
 // Per-launch control block in device memory (decoder workspace).

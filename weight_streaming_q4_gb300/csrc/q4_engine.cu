@@ -1,15 +1,16 @@
 // Persistent, warp-specialised Q4_0 matrix-vector engine for sm_103a.
 //
-// One CTA per SM.  Warp 8 is the producer: one lane streams the CTA's work
+// One CTA per SM.  Warp 15 is the producer: one lane streams the CTA's work
 // units (consecutive weight rows, contiguous in the GGUF row-major layout)
-// from HBM into an 11-deep ring of 18 KB shared-memory stages with 1-D bulk
+// from HBM into a 6-deep ring of 31.5 KB shared-memory stages with 1-D bulk
 // TMA copies (cp.async.bulk) whose completion is counted on one mbarrier
-// per stage.  Warps 0-7 are the consumers: each thread keeps a fixed slice
-// of 64 or 128 columns of the input vector x in registers, reads its slice
-// of each staged row, unpacks the 4-bit codes in registers and accumulates
-// the exact products (q - 8) * x in fp32; the row sums are reduced with warp
-// shuffles (and, for rows wider than one warp's slice, through shared
-// memory in a fixed order).  The work of a launch is a list of phases
+// per stage.  Warps 0-14 are the consumers: each thread keeps a fixed slice
+// of 64 columns of the input vector x in registers, reads its slice of two
+// staged rows per unit, unpacks the 4-bit codes in registers and
+// accumulates the exact products (q - 8) * x in fp32.  Row sums are reduced
+// with warp shuffles; rows wider than one warp's slice leave one partial per
+// warp in shared memory, summed in a fixed order when the phase ends (no
+// barrier per unit).  The work of a launch is a list of phases
 // (matrix-vector products with an input prologue and an output epilogue);
 // consecutive phases are separated by a grid barrier, while the producer
 // keeps streaming the next phase's weights, which never depend on the
@@ -104,13 +105,14 @@ __device__ __forceinline__ void set_status(Control* ctl, int bits) {
 }
 
 // Load 32 consecutive columns [c0, c0 + 32) of the phase input (before any
-// normalisation) as floats, with 16-byte vector loads.
+// normalisation) as floats, with 16-byte loads that bypass L1 (the data was
+// written by other CTAs in an earlier phase).
 __device__ __forceinline__ void load_block_x(const Phase& ph, int c0, float* v) {
   if (ph.x_kind == X_F16 || ph.x_kind == X_NORM16) {
     const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __half*>(ph.x_src) + c0);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint4 u = p[i];
+      const uint4 u = __ldcg(p + i);
       const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
@@ -128,7 +130,7 @@ __device__ __forceinline__ void load_block_x(const Phase& ph, int c0, float* v) 
         const int hd = ph.head_dim;
         c = ph.attn_off + ((c / hd) / ph.group) * hd + (c % hd);   // 4 columns stay in one head
       }
-      const float4 f = *reinterpret_cast<const float4*>(src + c);
+      const float4 f = __ldcg(reinterpret_cast<const float4*>(src + c));
       v[4 * i] = f.x;
       v[4 * i + 1] = f.y;
       v[4 * i + 2] = f.z;
@@ -137,14 +139,24 @@ __device__ __forceinline__ void load_block_x(const Phase& ph, int c0, float* v) 
   }
 }
 
-// Sum of squares of the phase input over all k columns (CTA-wide, fixed order).
-__device__ float input_rms_scale(const Phase& ph, float* red_ss) {
-  const int ct = threadIdx.x;
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// 1 / sqrt(mean(t^2) + eps) of the phase input.  Every warp computes it on
+// its own, in the same fixed order, so no CTA barrier is needed: from the
+// producing phase's per-CTA sums of squares (X_NORM32), or over the whole
+// binary16 input vector (X_NORM16).
+__device__ float input_rms_scale(const Phase& ph, int lane) {
   float ss = 0.f;
-  if (ph.x_kind == X_NORM16) {
+  if (ph.x_kind == X_NORM32) {
+    for (int i = lane; i < static_cast<int>(gridDim.x); i += 32) ss += __ldcg(ph.ss_in + i);
+  } else {
     const uint4* p = reinterpret_cast<const uint4*>(ph.x_src);
-    for (int i = ct; i < ph.k / 8; i += kConsumerThreads) {
-      const uint4 u = p[i];
+    for (int i = lane; i < ph.k / 8; i += 32) {
+      const uint4 u = __ldcg(p + i);
       const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
@@ -153,45 +165,24 @@ __device__ float input_rms_scale(const Phase& ph, float* red_ss) {
         ss = fmaf(f.y, f.y, ss);
       }
     }
-  } else {
-    const float4* p = reinterpret_cast<const float4*>(ph.x_src);
-    for (int i = ct; i < ph.k / 4; i += kConsumerThreads) {
-      const float4 f = p[i];
-      ss = fmaf(f.x, f.x, ss);
-      ss = fmaf(f.y, f.y, ss);
-      ss = fmaf(f.z, f.z, ss);
-      ss = fmaf(f.w, f.w, ss);
-    }
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  if ((ct & 31) == 0) red_ss[ct >> 5] = ss;
-  named_bar_sync(1, kConsumerThreads);
-  float tot = 0.f;
-#pragma unroll
-  for (int w = 0; w < kConsumerWarps; ++w) tot += red_ss[w];
-  named_bar_sync(1, kConsumerThreads);   // red_ss is reused by the next phase
-  return rsqrtf(tot / static_cast<float>(ph.k) + ph.eps);
+  return rsqrtf(warp_sum(ss) / static_cast<float>(ph.k) + ph.eps);
 }
 
-// Form the thread's slice of x for a phase: xs2 receives kt/2 float2 in the
+// Form the thread's slice of x for a phase: xs2 receives 32 float2 in the
 // order pair_dot expects, each value pre-scaled by 2^-shift.  Columns
-// [j*kt, (j+1)*kt) belong to the thread.
-__device__ void form_x(const Phase& ph, int j, int kt, float2* xs2, float* red_ss, bool write_dbg) {
+// [64 j, 64 j + 64) belong to the thread.
+__device__ void form_x(const Phase& ph, int j, int lane, float2* xs2, bool write_dbg) {
   const bool norm = ph.x_kind == X_NORM16 || ph.x_kind == X_NORM32;
-  const float r = norm ? input_rms_scale(ph, red_ss) : 1.0f;
-  const int k0 = j * kt;
+  const float r = norm ? input_rms_scale(ph, lane) : 1.0f;
+  const int k0 = j * kKT;
 #pragma unroll
-  for (int blk = 0; blk < 4; ++blk) {
-    if (blk * 32 >= kt) break;
+  for (int blk = 0; blk < kKT / 32; ++blk) {
     float v[32];
     load_block_x(ph, k0 + blk * 32, v);
     __half xv[32];
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      // binary16 rounding of the input: exact for X_F16, RNE for the others
-      xv[e] = (ph.x_kind == X_F16) ? __float2half_rn(v[e]) : __float2half_rn(norm ? v[e] * r : v[e]);
-    }
+    for (int e = 0; e < 32; ++e) xv[e] = __float2half_rn(norm ? v[e] * r : v[e]);
     if (write_dbg) {
       uint4* d = reinterpret_cast<uint4*>(ph.x_dbg + k0 + blk * 32);
 #pragma unroll
@@ -212,20 +203,6 @@ __device__ void form_x(const Phase& ph, int j, int kt, float2* xs2, float* red_s
 
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
-// Row epilogue for one output row n of a phase (batch row 0).
-__device__ __forceinline__ void epilogue(const Phase& ph, int n, float s, float s2) {
-  if (ph.epi_kind == EPI_F32) {
-    ph.y[n] = s;
-  } else if (ph.epi_kind == EPI_RESID) {
-    ph.y[n] = s;
-    ph.y2[n] = __half2float(__ushort_as_half(ph.res[n])) + s;
-  } else {
-    ph.y[n] = s;
-    ph.y2[n] = s2;
-    ph.aux16[n] = __half_as_ushort(__float2half_rn(silu_mul(s, s2)));
-  }
-}
-
 __device__ bool grid_barrier(Control* ctl, unsigned long long target, uint32_t limit) {
   __threadfence();
   atomicAdd(&ctl->barrier, 1ull);
@@ -234,9 +211,76 @@ __device__ bool grid_barrier(Control* ctl, unsigned long long target, uint32_t l
       __threadfence();
       return true;
     }
-    __nanosleep(i < 256 ? 32 : 256);
+    if (i > 64) __nanosleep(64);
   }
   return false;
+}
+
+// Geometry of a phase as the consumers see it.
+struct Tile {
+  int team_threads, teams, team, j, tw, spu, rpu, w_in_team;
+  bool active, dual;
+  uint32_t row_bytes;
+};
+
+__device__ __forceinline__ Tile tile_of(const Phase& ph, int tid) {
+  Tile t;
+  t.team_threads = ph.k / kKT;
+  t.teams = ph.teams;
+  t.team = tid / t.team_threads;
+  t.j = tid % t.team_threads;
+  t.active = t.team < t.teams;
+  t.tw = t.team_threads >= 32 ? t.team_threads / 32 : 1;   // partials per row (one per warp)
+  t.w_in_team = t.team_threads >= 32 ? (tid / 32 - t.team * t.tw) : 0;
+  t.spu = 2 * t.teams;                                     // row slots per unit
+  t.dual = ph.epi_kind == EPI_SILU;
+  t.rpu = ph.rows_per_unit;
+  t.row_bytes = static_cast<uint32_t>(ph.k / kQK) * kBlockBytes;
+  return t;
+}
+
+// Sum the buffered per-warp partials of n_buf units (the CTA's units
+// u_first, u_first + G, ...) and run the epilogue of their rows.  All
+// consumer threads take part.  Returns the thread's sum of squares of the
+// residual sums it wrote (EPI_RESID), for the next phase's RMSNorm.
+__device__ float flush_rows(const Phase& ph, const Tile& t, const float* red, int n_buf, int u_first, int G,
+                            int tid) {
+  named_bar_sync(1, kConsumerThreads);
+  float ss = 0.f;
+  const int n_slots = n_buf * t.spu;
+  if (!t.dual) {
+    for (int s = tid; s < n_slots; s += kConsumerThreads) {
+      float v = 0.f;
+      for (int w = 0; w < t.tw; ++w) v += red[s * t.tw + w];
+      const int i = s / t.spu, rem = s % t.spu;
+      const int n = (u_first + i * G) * t.rpu + rem;   // rem = 2 * team + row of the team
+      if (n < ph.n_rows) {
+        ph.y[n] = v;
+        if (ph.epi_kind == EPI_RESID) {
+          const float tv = __half2float(__ushort_as_half(__ldcg(ph.res + n))) + v;
+          ph.y2[n] = tv;
+          ss = fmaf(tv, tv, ss);
+        }
+      }
+    }
+  } else {
+    for (int q = tid; q < n_slots / 2; q += kConsumerThreads) {
+      float g = 0.f, u = 0.f;
+      for (int w = 0; w < t.tw; ++w) {
+        g += red[(2 * q) * t.tw + w];
+        u += red[(2 * q + 1) * t.tw + w];
+      }
+      const int i = (2 * q) / t.spu, tm = ((2 * q) % t.spu) / 2;
+      const int n = (u_first + i * G) * t.rpu + tm;
+      if (n < ph.n_rows) {
+        ph.y[n] = g;
+        ph.y2[n] = u;
+        ph.aux16[n] = __half_as_ushort(__float2half_rn(silu_mul(g, u)));
+      }
+    }
+  }
+  named_bar_sync(1, kConsumerThreads);
+  return ss;
 }
 
 extern __shared__ __align__(128) uint8_t g_ring[];
@@ -244,8 +288,8 @@ extern __shared__ __align__(128) uint8_t g_ring[];
 __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_constant__ EngineArgs a) {
   __shared__ __align__(8) uint64_t full_bar[kStages];
   __shared__ __align__(8) uint64_t empty_bar[kStages];
-  __shared__ float red[2][kConsumerWarps][2];
-  __shared__ float red_ss[kConsumerWarps];
+  __shared__ float red[kRedFloats];
+  __shared__ float red_cta[kConsumerWarps];
   __shared__ volatile int abort_flag;
 
   const int tid = threadIdx.x;
@@ -270,6 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
       for (int p = 0; p < a.n_phases && !abort_flag; ++p) {
         const Phase& ph = a.phases ? a.phases[p] : a.one;
         const uint32_t row_bytes = static_cast<uint32_t>(ph.k / kQK) * kBlockBytes;
+        const bool dual = ph.epi_kind == EPI_SILU;
         const int u0 = (cta - base + G) % G;
         for (int u = u0; u < ph.units; u += G) {
           const int stage = it % kStages;
@@ -284,7 +329,6 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
           const int rows = min(ph.rows_per_unit, ph.n_rows - row0);
           const uint32_t bytes = static_cast<uint32_t>(rows) * row_bytes;
           uint8_t* dst = g_ring + static_cast<size_t>(stage) * kStageBytes;
-          const bool dual = ph.epi_kind == EPI_SILU;
           mbar_arrive_expect_tx(&full_bar[stage], dual ? 2 * bytes : bytes);
           bulk_g2s(dst, ph.w0 + static_cast<size_t>(row0) * row_bytes, bytes, &full_bar[stage]);
           if (dual)
@@ -303,113 +347,93 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
     }
   } else {
     // ------------------------------------------------------------ consumers
-    float2 xs2[64];
+    float2 xs2[kKT / 2];
     uint32_t it = 0;
     int base = 0;
     for (int p = 0; p < a.n_phases; ++p) {
       const Phase& ph = a.phases ? a.phases[p] : a.one;
-      if (p > 0) {
-        named_bar_sync(1, kConsumerThreads);   // this CTA's writes of the last phase are done
-        if (tid == 0 && !grid_barrier(a.ctl, static_cast<unsigned long long>(p) * G, a.wait_limit)) {
-          set_status(a.ctl, ST_GRID_TIMEOUT);
-          abort_flag = 1;
-        }
-        named_bar_sync(1, kConsumerThreads);
-        if (abort_flag) break;
-      }
-      const int kt = ph.kt;
-      const int team_threads = ph.k / kt;
-      const int teams = kConsumerThreads / team_threads;
-      const int team = tid / team_threads, j = tid % team_threads;
-      const bool active = team < teams;
-      const int rpt = (kt == 64) ? 2 : 1;
-      const bool dual = ph.epi_kind == EPI_SILU;
-      const uint32_t row_bytes = static_cast<uint32_t>(ph.k / kQK) * kBlockBytes;
-      const int units = ph.units, rows_per_unit = ph.rows_per_unit, n_rows = ph.n_rows;
+      const Tile t = tile_of(ph, tid);
+      const int units = ph.units, n_rows = ph.n_rows;
       const int u0 = (cta - base + G) % G;
-      const bool has_work = u0 < units;
-      if (has_work || (ph.x_dbg && cta == 0)) {
-        // every consumer thread takes part (the RMS reduction is CTA-wide)
-        form_x(ph, active ? j : 0, kt, xs2, red_ss, ph.x_dbg != nullptr && cta == 0 && team == 0);
-      }
+      if (u0 < units || (ph.x_dbg && cta == 0))
+        form_x(ph, t.active ? t.j : 0, lane, xs2, ph.x_dbg != nullptr && cta == 0 && t.team == 0);
+      const int cap = kRedFloats / (t.spu * t.tw);   // units buffered before a flush
+      int n_buf = 0, u_first = u0;
+      float ss = 0.f;
       for (int u = u0; u < units; u += G) {
+        if (n_buf == cap) {
+          ss += flush_rows(ph, t, red, n_buf, u_first, G, tid);
+          n_buf = 0;
+          u_first = u;
+        }
         const int stage = it % kStages;
         const uint32_t n = it / kStages;
         // After a failed wait the CTA keeps walking its units without waiting
-        // (reading whatever the stage holds) so that every team barrier is
-        // still reached; the launch then reports the failure in its status.
+        // (reading whatever the stage holds) so that every barrier is still
+        // reached; the launch then reports the failure in its status.
         if (!abort_flag && !mbar_wait_bounded(&full_bar[stage], n & 1, a.wait_limit)) {
           set_status(a.ctl, ST_FULL_TIMEOUT);
           abort_flag = 1;
         }
         const uint8_t* sb = g_ring + static_cast<size_t>(stage) * kStageBytes;
-        const int row0 = u * rows_per_unit;
+        const int row0 = u * t.rpu;
         float t0 = 0.f, t1 = 0.f;
-        int ra = -1, rb = -1;     // output rows of this team (-1: none)
-        if (active) {
-          const uint8_t *pa, *pb = nullptr;
-          if (dual) {
-            ra = row0 + team;
-            pa = sb + static_cast<size_t>(team) * row_bytes;
-            pb = sb + static_cast<size_t>(rows_per_unit + team) * row_bytes;
-            rb = ra;
+        if (t.active) {
+          const uint8_t *pa, *pb;
+          int ra, rb;
+          if (t.dual) {
+            ra = rb = row0 + t.team;
+            pa = sb + static_cast<size_t>(t.team) * t.row_bytes;
+            pb = sb + static_cast<size_t>(t.rpu + t.team) * t.row_bytes;
           } else {
-            ra = row0 + team * rpt;
-            pa = sb + static_cast<size_t>(team * rpt) * row_bytes;
-            if (rpt == 2) {
-              rb = ra + 1;
-              pb = pa + row_bytes;
-            }
+            ra = row0 + 2 * t.team;
+            rb = ra + 1;
+            pa = sb + static_cast<size_t>(2 * t.team) * t.row_bytes;
+            pb = pa + t.row_bytes;
           }
-          if (ra >= n_rows) ra = -1;
-          if (rb >= n_rows) rb = -1;
-          if (kt == 64) {
-            if (ra >= 0) t0 = pair_dot(pa + static_cast<size_t>(j) * 36, xs2, 0.f);
-            if (rb >= 0) t1 = pair_dot(pb + static_cast<size_t>(j) * 36, xs2, 0.f);
-          } else if (ra >= 0) {
-            t0 = pair_dot(pa + static_cast<size_t>(2 * j) * 36, xs2, 0.f);
-            t0 = pair_dot(pa + static_cast<size_t>(2 * j + 1) * 36, xs2 + 32, t0);
-          }
+          if (ra < n_rows) t0 = pair_dot(pa + static_cast<size_t>(t.j) * 36, xs2, 0.f);
+          if (rb < n_rows) t1 = pair_dot(pb + static_cast<size_t>(t.j) * 36, xs2, 0.f);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[stage]);
         ++it;
-        if (!active) continue;
-        // reduce the team's partial sums
-        const int width = team_threads < 32 ? team_threads : 32;
-        for (int o = width >> 1; o > 0; o >>= 1) {
-          t0 += __shfl_xor_sync(0xffffffffu, t0, o);
-          t1 += __shfl_xor_sync(0xffffffffu, t1, o);
-        }
-        if (team_threads <= 32) {
-          if (j == 0 && ra >= 0) {
-            if (dual) epilogue(ph, ra, t0, t1);
-            else {
-              epilogue(ph, ra, t0, 0.f);
-              if (rb >= 0) epilogue(ph, rb, t1, 0.f);
-            }
+        if (t.active) {
+          const int width = t.team_threads < 32 ? t.team_threads : 32;
+          for (int o = width >> 1; o > 0; o >>= 1) {
+            t0 += __shfl_xor_sync(0xffffffffu, t0, o);
+            t1 += __shfl_xor_sync(0xffffffffu, t1, o);
           }
-        } else {
-          const int slot = it & 1;
-          if (lane == 0) {
-            red[slot][warp][0] = t0;
-            red[slot][warp][1] = t1;
-          }
-          named_bar_sync(2 + team, team_threads);
-          if (j == 0 && ra >= 0) {
-            const int w0 = team * (team_threads >> 5);
-            float s0 = 0.f, s1 = 0.f;
-            for (int w = 0; w < (team_threads >> 5); ++w) {
-              s0 += red[slot][w0 + w][0];
-              s1 += red[slot][w0 + w][1];
-            }
-            if (dual) epilogue(ph, ra, s0, s1);
-            else {
-              epilogue(ph, ra, s0, 0.f);
-              if (rb >= 0) epilogue(ph, rb, s1, 0.f);
-            }
+          if ((t.team_threads >= 32 && lane == 0) || (t.team_threads < 32 && t.j == 0)) {
+            const int slot = n_buf * t.spu + 2 * t.team;
+            red[slot * t.tw + t.w_in_team] = t0;
+            red[(slot + 1) * t.tw + t.w_in_team] = t1;
           }
         }
+        ++n_buf;
+      }
+      ss += flush_rows(ph, t, red, n_buf, u_first, G, tid);
+      // phase end: per-CTA sum of squares for the next RMSNorm, then the grid barrier
+      const bool resid = ph.epi_kind == EPI_RESID && ph.ss_out != nullptr;
+      if (resid) {
+        ss = warp_sum(ss);
+        if (lane == 0) red_cta[warp] = ss;
+      }
+      if (p + 1 < a.n_phases || resid) {
+        named_bar_sync(1, kConsumerThreads);
+        if (tid == 0) {
+          if (resid) {
+            float tot = 0.f;
+            for (int w = 0; w < kConsumerWarps; ++w) tot += red_cta[w];
+            ph.ss_out[cta] = tot;
+          }
+          if (p + 1 < a.n_phases &&
+              !grid_barrier(a.ctl, static_cast<unsigned long long>(p + 1) * G, a.wait_limit)) {
+            set_status(a.ctl, ST_GRID_TIMEOUT);
+            abort_flag = 1;
+          }
+        }
+        named_bar_sync(1, kConsumerThreads);
+        if (abort_flag) break;
       }
       base = (base + units) % G;
     }
