@@ -152,7 +152,12 @@ __device__ __forceinline__ float warp_sum(float v) {
 __device__ float input_rms_scale(const Phase& ph, int lane) {
   float ss = 0.f;
   if (ph.x_kind == X_NORM32) {
-    for (int i = lane; i < static_cast<int>(gridDim.x); i += 32) ss += __ldcg(ph.ss_in + i);
+    const int G = static_cast<int>(gridDim.x);
+    float part[kMaxGrid / 32];
+#pragma unroll
+    for (int i = 0; i < kMaxGrid / 32; ++i) part[i] = (lane + 32 * i < G) ? __ldcg(ph.ss_in + lane + 32 * i) : 0.f;
+#pragma unroll
+    for (int i = 0; i < kMaxGrid / 32; ++i) ss += part[i];
   } else {
     const uint4* p = reinterpret_cast<const uint4*>(ph.x_src);
     for (int i = lane; i < ph.k / 8; i += 32) {
@@ -171,47 +176,48 @@ __device__ float input_rms_scale(const Phase& ph, int lane) {
 
 // Form the thread's slice of x for a phase: xs2 receives 32 float2 in the
 // order pair_dot expects, each value pre-scaled by 2^-shift.  Columns
-// [64 j, 64 j + 64) belong to the thread.
+// [64 j, 64 j + 64) belong to the thread.  All loads are issued before any
+// dependent arithmetic, so the prologue costs one round trip to L2.
 __device__ void form_x(const Phase& ph, int j, int lane, float2* xs2, bool write_dbg) {
   const bool norm = ph.x_kind == X_NORM16 || ph.x_kind == X_NORM32;
-  const float r = norm ? input_rms_scale(ph, lane) : 1.0f;
   const int k0 = j * kKT;
+  float v[kKT];
+  load_block_x(ph, k0, v);
+  load_block_x(ph, k0 + 32, v + 32);
+  const float r = norm ? input_rms_scale(ph, lane) : 1.0f;
+  __half xv[kKT];
+#pragma unroll
+  for (int e = 0; e < kKT; ++e) xv[e] = __float2half_rn(norm ? v[e] * r : v[e]);
 #pragma unroll
   for (int blk = 0; blk < kKT / 32; ++blk) {
-    float v[32];
-    load_block_x(ph, k0 + blk * 32, v);
-    __half xv[32];
-#pragma unroll
-    for (int e = 0; e < 32; ++e) xv[e] = __float2half_rn(norm ? v[e] * r : v[e]);
-    if (write_dbg) {
-      uint4* d = reinterpret_cast<uint4*>(ph.x_dbg + k0 + blk * 32);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) d[i] = reinterpret_cast<const uint4*>(xv)[i];
-    }
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
 #pragma unroll
       for (int e = 0; e < 8; e += 2) {
-        const float a = __half2float(xv[4 * m + elem_off(e)]) * (1.0f / static_cast<float>(1 << elem_shift(e)));
-        const float b =
-            __half2float(xv[4 * m + elem_off(e + 1)]) * (1.0f / static_cast<float>(1 << elem_shift(e + 1)));
+        const float a =
+            __half2float(xv[blk * 32 + 4 * m + elem_off(e)]) * (1.0f / static_cast<float>(1 << elem_shift(e)));
+        const float b = __half2float(xv[blk * 32 + 4 * m + elem_off(e + 1)]) *
+                        (1.0f / static_cast<float>(1 << elem_shift(e + 1)));
         xs2[blk * 16 + m * 4 + e / 2] = make_float2(a, b);
       }
     }
+  }
+  if (write_dbg) {
+    uint4* d = reinterpret_cast<uint4*>(ph.x_dbg + k0);
+#pragma unroll
+    for (int i = 0; i < kKT / 8; ++i) d[i] = reinterpret_cast<const uint4*>(xv)[i];
   }
 }
 
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
+// Arrive (release: this CTA's earlier global writes become visible first)
+// and wait until `target` arrivals are counted (acquire), at most `limit` polls.
 __device__ bool grid_barrier(Control* ctl, unsigned long long target, uint32_t limit) {
-  __threadfence();
-  atomicAdd(&ctl->barrier, 1ull);
+  asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(&ctl->barrier), "l"(1ull) : "memory");
   for (uint32_t i = 0; i < limit; ++i) {
-    if (ld_acquire_u64(&ctl->barrier) >= target) {
-      __threadfence();
-      return true;
-    }
-    if (i > 64) __nanosleep(64);
+    if (ld_acquire_u64(&ctl->barrier) >= target) return true;
+    if (i > 256) __nanosleep(32);
   }
   return false;
 }
@@ -244,7 +250,7 @@ __device__ __forceinline__ Tile tile_of(const Phase& ph, int tid) {
 // consumer threads take part.  Returns the thread's sum of squares of the
 // residual sums it wrote (EPI_RESID), for the next phase's RMSNorm.
 __device__ float flush_rows(const Phase& ph, const Tile& t, const float* red, int n_buf, int u_first, int G,
-                            int tid) {
+                            int tid, bool reuse) {
   named_bar_sync(1, kConsumerThreads);
   float ss = 0.f;
   const int n_slots = n_buf * t.spu;
@@ -279,7 +285,7 @@ __device__ float flush_rows(const Phase& ph, const Tile& t, const float* red, in
       }
     }
   }
-  named_bar_sync(1, kConsumerThreads);
+  if (reuse) named_bar_sync(1, kConsumerThreads);   // red is written again in this phase
   return ss;
 }
 
@@ -362,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
       float ss = 0.f;
       for (int u = u0; u < units; u += G) {
         if (n_buf == cap) {
-          ss += flush_rows(ph, t, red, n_buf, u_first, G, tid);
+          ss += flush_rows(ph, t, red, n_buf, u_first, G, tid, true);
           n_buf = 0;
           u_first = u;
         }
@@ -411,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
         }
         ++n_buf;
       }
-      ss += flush_rows(ph, t, red, n_buf, u_first, G, tid);
+      ss += flush_rows(ph, t, red, n_buf, u_first, G, tid, false);
       // phase end: per-CTA sum of squares for the next RMSNorm, then the grid barrier
       const bool resid = ph.epi_kind == EPI_RESID && ph.ss_out != nullptr;
       if (resid) {
