@@ -105,14 +105,16 @@ __device__ __forceinline__ void set_status(Control* ctl, int bits) {
 }
 
 // Load 32 consecutive columns [c0, c0 + 32) of the phase input (before any
-// normalisation) as floats, with 16-byte loads that bypass L1 (the data was
-// written by other CTAs in an earlier phase).
+// normalisation) as floats, with 16-byte loads through L1: the row teams of a
+// CTA share the same slices, so one line fill serves them all.  The data was
+// written by other CTAs before the grid barrier, whose acquire (thread 0)
+// and CTA barrier order these loads after those writes.
 __device__ __forceinline__ void load_block_x(const Phase& ph, int c0, float* v) {
   if (ph.x_kind == X_F16 || ph.x_kind == X_NORM16) {
     const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __half*>(ph.x_src) + c0);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint4 u = __ldcg(p + i);
+      const uint4 u = p[i];
       const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
@@ -130,7 +132,7 @@ __device__ __forceinline__ void load_block_x(const Phase& ph, int c0, float* v) 
         const int hd = ph.head_dim;
         c = ph.attn_off + ((c / hd) / ph.group) * hd + (c % hd);   // 4 columns stay in one head
       }
-      const float4 f = __ldcg(reinterpret_cast<const float4*>(src + c));
+      const float4 f = *reinterpret_cast<const float4*>(src + c);
       v[4 * i] = f.x;
       v[4 * i + 1] = f.y;
       v[4 * i + 2] = f.z;
