@@ -225,6 +225,39 @@ int q4_decoder_status(q4_decoder *dec, void *stream, int *status_out);
 
 int q4_decoder_destroy(q4_decoder *dec);
 
+/* ------------------------------------------------------- decoder without allocation */
+
+/*
+ * For callers that cannot allocate device memory -- code running where
+ * cudaMalloc is not allowed or not wanted (inside an allocator's own
+ * callbacks, in a process whose device memory is fully reserved up front,
+ * or a plugin host that hands out no workspace) -- the decoder stack can run
+ * with its scratch (phase program, control block, intermediate activations)
+ * in one array that the library holds in static device memory.  The paper
+ * has no counterpart to this entry point; it is a deployment convenience.
+ *
+ * The array is Q4_NOALLOC_SCRATCH_BYTES (1 MiB) on every GPU that loads the
+ * library, held until the process exits; it fits a batch-1 stack of the
+ * 70B shape with up to 1000 layers.  Larger stacks return Q4_ERR_OOM.
+ * The first call on a device looks up the array's device address on that
+ * device (make that first call before any stream capture).  Every call
+ * shares the one array and overwrites it, so calls whose work overlaps on
+ * the GPU (different streams, or different threads without ordering) race:
+ * issue them on one stream.  The control block is cleared by every call.
+ * Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
+ *   shape, layer_weights, n_layers   as for q4_decoder_create (batch 1)
+ *   hidden_io  device, binary16 [1][hidden], updated as by q4_layer_decode
+ *   stream     the work is enqueued asynchronously on it (eager launches)
+ * Errors: Q4_ERR_ARG, Q4_ERR_ALIGN, Q4_ERR_OOM (stack too large for the
+ * array), Q4_ERR_CUDA.
+ */
+#define Q4_NOALLOC_SCRATCH_BYTES (1u << 20)
+int q4_layer_decode_noalloc(const q4_layer_shape *shape, const void *const *layer_weights, int n_layers,
+                            uint16_t *hidden_io, void *stream);
+
+/* Size in bytes of the static scratch array used by q4_layer_decode_noalloc. */
+size_t q4_noalloc_scratch_bytes(void);
+
 /* ------------------------------------------------------- streamed layers */
 
 typedef struct q4_stream q4_stream;

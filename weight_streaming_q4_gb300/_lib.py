@@ -79,6 +79,8 @@ def _declare(lib):
         "q4_layer_decode_eager": ([c_p, c_p, c_p], c_int),
         "q4_decoder_status": ([c_p, c_p, ctypes.POINTER(c_int)], c_int),
         "q4_decoder_destroy": ([c_p], c_int),
+        "q4_layer_decode_noalloc": ([ctypes.POINTER(LayerShape), ctypes.POINTER(c_p), c_int, c_p, c_p], c_int),
+        "q4_noalloc_scratch_bytes": ([], c_size),
         "q4_stream_create": ([ctypes.POINTER(c_p), ctypes.POINTER(LayerShape), ctypes.POINTER(c_p), c_int, c_int,
                               c_p, c_p, c_size, c_p, c_size, c_int], c_int),
         "q4_stream_layers": ([c_p, c_p, c_p, c_i64], c_int),
@@ -207,6 +209,17 @@ def q4_decoder_status(dec, stream=None) -> int:
 
 def q4_decoder_destroy(dec):
     _check(lib().q4_decoder_destroy(dec), "q4_decoder_destroy")
+
+
+def q4_layer_decode_noalloc(shape: LayerShape, layer_ptrs, hidden, stream=None):
+    """The decoder stack with its scratch in the library's static device array (no allocation)."""
+    arr = (c_p * len(layer_ptrs))(*[int(p) for p in layer_ptrs])
+    _check(lib().q4_layer_decode_noalloc(ctypes.byref(shape), arr, len(layer_ptrs), _ptr(hidden), _stream(stream)),
+           "q4_layer_decode_noalloc")
+
+
+def q4_noalloc_scratch_bytes() -> int:
+    return lib().q4_noalloc_scratch_bytes()
 
 
 def q4_stream_create(shape: LayerShape, host_ptrs, batch: int, buf0, buf1, buf_bytes: int, workspace,

@@ -512,6 +512,40 @@ extern "C" int q4_layer_decode_eager(q4_decoder* d, uint16_t* hidden_io, void* s
   return decoder_enqueue(d, s);
 }
 
+namespace q4 {
+
+// Run an n_layers stack once, eagerly, with every scratch region inside the
+// given workspace (q4_workspace_layout order): phase program written
+// stream-ordered from host memory, control block cleared, one persistent
+// launch.  Allocates nothing.
+int run_stack_in_workspace(const q4_layer_shape* shape, const void* const* layer_weights, int n_layers,
+                           uint16_t* hidden_io, void* ws, size_t ws_bytes, cudaStream_t s) {
+  if (!shape_ok(shape) || !layer_weights || n_layers < 1 || !hidden_io || !ws) return Q4_ERR_ARG;
+  if (check_layer_shape_for_engine(*shape) != Q4_OK) return Q4_ERR_ARG;
+  if (!aligned(hidden_io, 16)) return Q4_ERR_ALIGN;
+  for (int l = 0; l < n_layers; ++l) {
+    if (!layer_weights[l]) return Q4_ERR_ARG;
+    if (!aligned(layer_weights[l], 256)) return Q4_ERR_ALIGN;
+  }
+  size_t off[Q4_WS_COUNT], need = 0;
+  int st = q4_workspace_layout(shape, n_layers, 1, off, &need);
+  if (st != Q4_OK) return st;
+  if (ws_bytes < need) return Q4_ERR_OOM;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != Q4_OK) return st;
+  const Work w = carve(ws, off);
+  std::vector<const uint8_t*> layers(reinterpret_cast<const uint8_t* const*>(layer_weights),
+                                     reinterpret_cast<const uint8_t* const*>(layer_weights) + n_layers);
+  std::vector<Phase> prog;
+  if (!stack_program(*shape, layers, hidden_io, w, prog)) return Q4_ERR_ARG;
+  Q4_CUDA(cudaMemcpyAsync(w.prog, prog.data(), prog.size() * sizeof(Phase), cudaMemcpyHostToDevice, s));
+  Q4_CUDA(cudaMemsetAsync(w.ctl, 0, sizeof(Control), s));
+  const int grid = dev->sm_count < kMaxGrid ? dev->sm_count : kMaxGrid;
+  return launch_layers(w, 0, static_cast<int>(prog.size()), grid, s);
+}
+
+}  // namespace q4
+
 extern "C" int q4_decoder_status(q4_decoder* d, void* stream, int* status_out) {
   if (!d || !status_out) return Q4_ERR_ARG;
   return read_status(d->w.ctl, static_cast<cudaStream_t>(stream), status_out);

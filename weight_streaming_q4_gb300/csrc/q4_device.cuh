@@ -183,3 +183,11 @@ cudaError_t dequant_launch(const uint8_t* w, float* out, int n, int k, cudaStrea
 cudaError_t poison_launch(uint8_t* buf, size_t n_blocks, cudaStream_t stream);
 
 }  // namespace q4
+
+struct q4_layer_shape;
+namespace q4 {
+// Host helper (q4_api.cu): one eager run of a layer stack inside a given workspace.
+int run_stack_in_workspace(const q4_layer_shape* shape, const void* const* layer_weights, int n_layers,
+                           uint16_t* hidden_io, void* ws, size_t ws_bytes, cudaStream_t s);
+
+}  // namespace q4
