@@ -174,7 +174,8 @@ int q4_layer_offsets(const q4_layer_shape *shape, size_t offsets[7], size_t *lay
 #define Q4_WS_X2 10       /* binary16 [batch][hidden]: z1 = f16(norm(t1)) */
 #define Q4_WS_T1 11       /* fp32 [batch][hidden]: t1 = z + Wo a */
 #define Q4_WS_T2 12       /* fp32 [batch][hidden]: t2 = z1 + Wdown act */
-#define Q4_WS_SS 13       /* fp32 [2][256]: per-CTA sums of squares of t1 and t2 */
+#define Q4_WS_FLAGS 13    /* u64 [2][256] per-CTA end-of-phase flags (tag, sum of squares), then
+                             fp32 [2][256] per-CTA sums of squares of t1 and t2 */
 #define Q4_WS_COUNT 14
 
 /*
@@ -196,7 +197,7 @@ typedef struct q4_decoder q4_decoder;
  * graph (PipeLLM, "Layer 1: CUDA Graph Compilation").
  *   shape          layer shape; layer_weights[i] = device pointer of layer
  *                  i's merged block (q4_layer_offsets layout), 256-byte aligned
- *   n_layers       >= 1; batch: 1 <= batch <= 16
+ *   n_layers       1..1023; batch: 1 <= batch <= 16
  *   workspace      device, >= q4_workspace_layout() bytes, 256-byte aligned;
  *                  owned by the caller, must outlive the decoder
  *   mode           Q4_DEC_FUSED or Q4_DEC_PER_LAYER

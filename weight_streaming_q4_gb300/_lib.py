@@ -36,7 +36,7 @@ Q4_DEC_FUSED = 0
 Q4_DEC_PER_LAYER = 1
 Q4_STREAM_POISON = 1
 
-WS_NAMES = ("control", "program", "qkv", "o", "gate", "up", "down", "act", "x", "attn", "x2", "t1", "t2", "ss")
+WS_NAMES = ("control", "program", "qkv", "o", "gate", "up", "down", "act", "x", "attn", "x2", "t1", "t2", "flags")
 WS_COUNT = len(WS_NAMES)
 
 

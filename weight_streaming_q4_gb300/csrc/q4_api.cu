@@ -222,7 +222,7 @@ extern "C" int q4_workspace_layout(const q4_layer_shape* s, int n_layers, int ba
       2 * B * s->hidden,
       4 * B * s->hidden,
       4 * B * s->hidden,
-      4 * 2 * static_cast<size_t>(q4::kMaxGrid),
+      8 * 2 * static_cast<size_t>(q4::kMaxGrid) + 4 * 2 * static_cast<size_t>(q4::kMaxGrid),
   };
   size_t pos = 0;
   for (int i = 0; i < Q4_WS_COUNT; ++i) {
@@ -240,7 +240,8 @@ struct Work {
   Control* ctl;
   Phase* prog;
   float *qkv, *o, *g, *u, *dn, *t1, *t2;
-  float *ss1, *ss2;   // per-CTA sums of squares of t1 and t2
+  unsigned long long* flags;   // [2][kMaxGrid] end-of-phase flags
+  float *ss1, *ss2;            // per-CTA sums of squares of t1 and t2
   uint16_t *act, *x, *attn, *x2;
 };
 
@@ -260,7 +261,8 @@ Work carve(void* ws, const size_t* off) {
   w.x2 = reinterpret_cast<uint16_t*>(b + off[Q4_WS_X2]);
   w.t1 = reinterpret_cast<float*>(b + off[Q4_WS_T1]);
   w.t2 = reinterpret_cast<float*>(b + off[Q4_WS_T2]);
-  w.ss1 = reinterpret_cast<float*>(b + off[Q4_WS_SS]);
+  w.flags = reinterpret_cast<unsigned long long*>(b + off[Q4_WS_FLAGS]);
+  w.ss1 = reinterpret_cast<float*>(w.flags + 2 * q4::kMaxGrid);
   w.ss2 = w.ss1 + q4::kMaxGrid;
   return w;
 }
@@ -379,6 +381,7 @@ int launch_layers(const Work& w, int first_phase, int n_phases, int grid, cudaSt
   a.phases = w.prog + first_phase;
   a.n_phases = n_phases;
   a.ctl = w.ctl;
+  a.flags = w.flags;
   a.wait_limit = kWaitLimit;
   Q4_CUDA(q4::engine_launch(a, grid, true, s));
   return Q4_OK;
@@ -430,6 +433,7 @@ extern "C" int q4_decoder_create(q4_decoder** out, const q4_layer_shape* shape, 
                                  void* stream) {
   if (!out || !shape_ok(shape) || !layer_weights || n_layers < 1 || !workspace) return Q4_ERR_ARG;
   if (batch != 1) return Q4_ERR_ARG;   // the persistent engine's exact CUDA-core path is batch 1
+  if (4 * n_layers + 1 > static_cast<int>(q4::kPhasesPerEpoch)) return Q4_ERR_ARG;
   if (mode != Q4_DEC_FUSED && mode != Q4_DEC_PER_LAYER) return Q4_ERR_ARG;
   if (check_layer_shape_for_engine(*shape) != Q4_OK) return Q4_ERR_ARG;
   if (!aligned(workspace, 256)) return Q4_ERR_ALIGN;
@@ -521,6 +525,7 @@ namespace q4 {
 int run_stack_in_workspace(const q4_layer_shape* shape, const void* const* layer_weights, int n_layers,
                            uint16_t* hidden_io, void* ws, size_t ws_bytes, cudaStream_t s) {
   if (!shape_ok(shape) || !layer_weights || n_layers < 1 || !hidden_io || !ws) return Q4_ERR_ARG;
+  if (4 * n_layers + 1 > static_cast<int>(kPhasesPerEpoch)) return Q4_ERR_ARG;
   if (check_layer_shape_for_engine(*shape) != Q4_OK) return Q4_ERR_ARG;
   if (!aligned(hidden_io, 16)) return Q4_ERR_ALIGN;
   for (int l = 0; l < n_layers; ++l) {
@@ -539,7 +544,9 @@ int run_stack_in_workspace(const q4_layer_shape* shape, const void* const* layer
   std::vector<Phase> prog;
   if (!stack_program(*shape, layers, hidden_io, w, prog)) return Q4_ERR_ARG;
   Q4_CUDA(cudaMemcpyAsync(w.prog, prog.data(), prog.size() * sizeof(Phase), cudaMemcpyHostToDevice, s));
+  // control block and phase flags start from zero (earlier calls left their tags)
   Q4_CUDA(cudaMemsetAsync(w.ctl, 0, sizeof(Control), s));
+  Q4_CUDA(cudaMemsetAsync(w.flags, 0, 2 * kMaxGrid * sizeof(unsigned long long), s));
   const int grid = dev->sm_count < kMaxGrid ? dev->sm_count : kMaxGrid;
   return launch_layers(w, 0, static_cast<int>(prog.size()), grid, s);
 }

@@ -47,8 +47,8 @@ struct Phase {
   float* y2;              // fp32 [batch][n_rows]: EPI_SILU u, EPI_RESID the residual sum
   const uint16_t* res;    // EPI_RESID: residual input binary16 [batch][n_rows]
   uint16_t* aux16;        // EPI_SILU: act binary16 [batch][n_rows]
-  float* ss_out;          // EPI_RESID: per-CTA sums of squares of y2 ([gridDim.x] floats)
-  const float* ss_in;     // X_NORM32: the producing phase's per-CTA sums of squares
+  float* ss_out;          // EPI_RESID: per-CTA sums of squares of y2 ([kMaxGrid] floats)
+  const float* ss_in;     // X_NORM32 in a launch's first phase: the producing phase's ss_out
   uint16_t* x_dbg;        // if not null, CTA 0 stores the formed x here (binary16 [batch][k])
   int n_rows;
   int k;
@@ -67,10 +67,15 @@ struct Phase {
 
 // Per-launch control block in device memory (decoder workspace).
 struct Control {
-  unsigned long long barrier;   // grid-barrier arrivals, never reset
+  unsigned long long depart;    // CTAs that left the current launch (reset by the last one)
+  unsigned int epoch;           // launches completed; phase tags of a launch derive from it
   int status;                   // bit flags set by kernels on a failed wait
-  int pad_;
 };
+
+// A CTA's end-of-phase flag: its sum of squares of the residual sums it wrote
+// (0 for other phases) in the low word, the phase tag in the high word.
+// flags[(p & 1) * kMaxGrid + cta] holds phase p's flag of CTA cta.
+constexpr unsigned kPhasesPerEpoch = 4096;
 
 // Arguments of one launch of the engine kernel: either a device array of
 // phases or a single phase passed by value.
@@ -78,12 +83,13 @@ struct EngineArgs {
   const Phase* phases;     // device array, or null to run `one`
   int n_phases;
   Control* ctl;            // required when n_phases > 1
+  unsigned long long* flags;  // [2][kMaxGrid] end-of-phase flags, required when n_phases > 1
   uint32_t wait_limit;     // polls of one wait before it is declared failed
   Phase one;
 };
 
 enum StatusBits : int {
-  ST_GRID_TIMEOUT = 1,
+  ST_FLAG_TIMEOUT = 1,
   ST_FULL_TIMEOUT = 2,
   ST_EMPTY_TIMEOUT = 4,
   ST_DRAIN_TIMEOUT = 8,
@@ -148,10 +154,14 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
   unsigned long long v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
+}
+
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 // Packed fp32x2 arithmetic (sm_100 family).

@@ -24,7 +24,7 @@
 // Asynchronous Weight Prefetching").
 //
 // Exactness of the block dot product: a code q is placed in the mantissa of
-// 2^23 (bits p..p+3 for p in {0,4,8,12,16}), so the float equals 2^23 + q*2^p
+// 2^23 (bits p..p+3 for p in {0,4,8,12}), so the float equals 2^23 + q*2^p
 // exactly; subtracting 2^23 + 8*2^p gives (q - 8)*2^p exactly, and the matching
 // x was stored pre-multiplied by 2^-p (exact).  Each product (q - 8) * x is
 // therefore exact, a block of all-8 codes contributes exactly zero, and a
@@ -40,63 +40,102 @@ __device__ int g_status;   // status bits of launches without a control block
 
 
 // Column order of the 8 codes of one 32-bit word of a block's code bytes
-// (bytes 4m..4m+3 hold elements 4m..4m+3 low and 4m+16..4m+19 high), and the
-// bit position each code is extracted at.
+// (bytes 4m..4m+3 hold elements 4m..4m+3 low and 4m+16..4m+19 high).  The
+// word and the word shifted right by 16 give the codes in pairs that sit at
+// the same bit position p: (4m, 4m+2) at p=0, (4m+16, 4m+18) at p=4,
+// (4m+1, 4m+3) at p=8, (4m+17, 4m+19) at p=12.
 __device__ __forceinline__ constexpr int elem_off(int e) {
-  return (e & 1) ? 16 + (e >> 1) : (e >> 1);
+  return e == 0 ? 0 : e == 1 ? 2 : e == 2 ? 16 : e == 3 ? 18 : e == 4 ? 1 : e == 5 ? 3 : e == 6 ? 17 : 19;
 }
-__device__ __forceinline__ constexpr int elem_shift(int e) {
-  return e == 0 ? 0 : e == 1 ? 4 : e == 2 ? 8 : e == 3 ? 12 : e == 4 ? 16 : e == 5 ? 8 : e == 6 ? 12 : 16;
+__device__ __forceinline__ constexpr int elem_shift(int e) { return 4 * (e >> 1); }
+
+typedef unsigned long long u64;
+
+// (a & MASK) | magic as one three-input logic op, the magic held in a register.
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t magic) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "n"(MASK), "r"(magic));
+  return d;
+}
+__device__ __forceinline__ u64 pack2(uint32_t lo, uint32_t hi) {
+  u64 d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+  return d;
+}
+__device__ __forceinline__ u64 add2(u64 a, u64 b) {
+  u64 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ u64 fma2(u64 a, u64 b, u64 c) {
+  u64 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ float hsum2(u64 a) {
+  return __uint_as_float(static_cast<uint32_t>(a)) + __uint_as_float(static_cast<uint32_t>(a >> 32));
 }
 
-constexpr uint32_t kMagic = 0x4B000000u;   // 2^23 as float bits
+// Constants of the exact unpack, kept in registers: the magic 2^23 and the
+// four bias pairs 2^23 + 8 * 2^p.
+struct Unpack {
+  uint32_t magic;
+  u64 bias[4];
+};
 
-__device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+__device__ __forceinline__ Unpack make_unpack() {
+  Unpack u;
+  asm volatile("mov.b32 %0, 0x4B000000;" : "=r"(u.magic));   // opaque: stays a register operand
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float b = -(8388608.0f + 8.0f * static_cast<float>(1 << (4 * i)));
+    const uint32_t bb = __float_as_uint(b);
+    asm volatile("mov.b64 %0, {%1, %1};" : "=l"(u.bias[i]) : "r"(bb));
+  }
+  return u;
+}
 
 // Accumulate the 8 exact products of one code word into acc (two lanes).
-__device__ __forceinline__ float2 word_dot(uint32_t w, const float2* xs, float2 acc) {
-  const float M = 8388608.0f;
-  const uint32_t u = w >> 12;
-  float2 v01 = make_float2(u2f((w & 0xFu) | kMagic), u2f((w & 0xF0u) | kMagic));
-  float2 v23 = make_float2(u2f((w & 0xF00u) | kMagic), u2f((w & 0xF000u) | kMagic));
-  float2 v45 = make_float2(u2f((w & 0xF0000u) | kMagic), u2f((u & 0xF00u) | kMagic));
-  float2 v67 = make_float2(u2f((u & 0xF000u) | kMagic), u2f((u & 0xF0000u) | kMagic));
-  v01 = f2_add(v01, make_float2(-(M + 8.0f), -(M + 128.0f)));
-  v23 = f2_add(v23, make_float2(-(M + 2048.0f), -(M + 32768.0f)));
-  v45 = f2_add(v45, make_float2(-(M + 524288.0f), -(M + 2048.0f)));
-  v67 = f2_add(v67, make_float2(-(M + 32768.0f), -(M + 524288.0f)));
-  acc = f2_fma(v01, xs[0], acc);
-  acc = f2_fma(v23, xs[1], acc);
-  acc = f2_fma(v45, xs[2], acc);
-  acc = f2_fma(v67, xs[3], acc);
+__device__ __forceinline__ u64 word_dot(uint32_t w, const u64* xs, u64 acc, const Unpack& k) {
+  const uint32_t h = w >> 16;
+  u64 v0 = pack2(and_or<0xFu>(w, k.magic), and_or<0xFu>(h, k.magic));
+  u64 v1 = pack2(and_or<0xF0u>(w, k.magic), and_or<0xF0u>(h, k.magic));
+  u64 v2 = pack2(and_or<0xF00u>(w, k.magic), and_or<0xF00u>(h, k.magic));
+  u64 v3 = pack2(and_or<0xF000u>(w, k.magic), and_or<0xF000u>(h, k.magic));
+  v0 = add2(v0, k.bias[0]);
+  v1 = add2(v1, k.bias[1]);
+  v2 = add2(v2, k.bias[2]);
+  v3 = add2(v3, k.bias[3]);
+  acc = fma2(v0, xs[0], acc);
+  acc = fma2(v1, xs[1], acc);
+  acc = fma2(v2, xs[2], acc);
+  acc = fma2(v3, xs[3], acc);
   return acc;
 }
 
 // Dot product of one 64-column slice (two blocks = 36 bytes starting at a
-// 4-byte aligned shared-memory address) with the thread's 32 float2 of x.
-__device__ __forceinline__ float pair_dot(const uint8_t* p, const float2* xs, float tot) {
+// 4-byte aligned shared-memory address) with the thread's 32 pairs of x.
+__device__ __forceinline__ float pair_dot(const uint8_t* p, const u64* xs, float tot, const Unpack& k) {
   const uint32_t* pw = reinterpret_cast<const uint32_t*>(p);
   uint32_t W[9];
 #pragma unroll
   for (int i = 0; i < 9; ++i) W[i] = pw[i];
   const float d0 = __half2float(__ushort_as_half(static_cast<unsigned short>(W[0] & 0xFFFFu)));
   const float d1 = __half2float(__ushort_as_half(static_cast<unsigned short>(W[4] >> 16)));
-  float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
-  float2 b0 = make_float2(0.f, 0.f), b1 = make_float2(0.f, 0.f);
+  u64 a0 = 0, a1 = 0, b0 = 0, b1 = 0;
   // block 0: code bytes start 2 bytes into word 0
-  a0 = word_dot(__funnelshift_r(W[0], W[1], 16), xs + 0, a0);
-  a1 = word_dot(__funnelshift_r(W[1], W[2], 16), xs + 4, a1);
-  a0 = word_dot(__funnelshift_r(W[2], W[3], 16), xs + 8, a0);
-  a1 = word_dot(__funnelshift_r(W[3], W[4], 16), xs + 12, a1);
+  a0 = word_dot(__funnelshift_r(W[0], W[1], 16), xs + 0, a0, k);
+  a1 = word_dot(__funnelshift_r(W[1], W[2], 16), xs + 4, a1, k);
+  a0 = word_dot(__funnelshift_r(W[2], W[3], 16), xs + 8, a0, k);
+  a1 = word_dot(__funnelshift_r(W[3], W[4], 16), xs + 12, a1, k);
   // block 1: code bytes are words 5..8
-  b0 = word_dot(W[5], xs + 16, b0);
-  b1 = word_dot(W[6], xs + 20, b1);
-  b0 = word_dot(W[7], xs + 24, b0);
-  b1 = word_dot(W[8], xs + 28, b1);
-  const float s0 = (a0.x + a0.y) + (a1.x + a1.y);
-  const float s1 = (b0.x + b0.y) + (b1.x + b1.y);
-  tot = fmaf(d0, s0, tot);
-  tot = fmaf(d1, s1, tot);
+  b0 = word_dot(W[5], xs + 16, b0, k);
+  b1 = word_dot(W[6], xs + 20, b1, k);
+  b0 = word_dot(W[7], xs + 24, b0, k);
+  b1 = word_dot(W[8], xs + 28, b1, k);
+  tot = fmaf(d0, hsum2(a0) + hsum2(a1), tot);
+  tot = fmaf(d1, hsum2(b0) + hsum2(b1), tot);
   return tot;
 }
 
@@ -147,46 +186,80 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// 1 / sqrt(mean(t^2) + eps) of the phase input.  Every warp computes it on
-// its own, in the same fixed order, so no CTA barrier is needed: from the
-// producing phase's per-CTA sums of squares (X_NORM32), or over the whole
-// binary16 input vector (X_NORM16).
-__device__ float input_rms_scale(const Phase& ph, int lane) {
-  float ss = 0.f;
-  if (ph.x_kind == X_NORM32) {
-    const int G = static_cast<int>(gridDim.x);
-    float part[kMaxGrid / 32];
+// Wait until every CTA has published phase `tag`'s flag (or a later one)
+// and return the sum of the sums of squares they carry, in a fixed order
+// (the same in every CTA).  One warp per CTA polls; after the flags are
+// seen, a fence orders later loads after the producers' writes.  Gives up
+// after `limit` polls (status bit set).
+__device__ float wait_phase_flags(const unsigned long long* flags, unsigned tag, int lane, uint32_t limit,
+                                  Control* ctl) {
+  const int G = static_cast<int>(gridDim.x);
+  float part[kMaxGrid / 32];
+  bool ok = false;
+  for (uint32_t it = 0; it < limit; ++it) {
+    bool mine = true;
 #pragma unroll
-    for (int i = 0; i < kMaxGrid / 32; ++i) part[i] = (lane + 32 * i < G) ? __ldcg(ph.ss_in + lane + 32 * i) : 0.f;
-#pragma unroll
-    for (int i = 0; i < kMaxGrid / 32; ++i) ss += part[i];
-  } else {
-    const uint4* p = reinterpret_cast<const uint4*>(ph.x_src);
-    for (int i = lane; i < ph.k / 8; i += 32) {
-      const uint4 u = __ldcg(p + i);
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[t]));
-        ss = fmaf(f.x, f.x, ss);
-        ss = fmaf(f.y, f.y, ss);
+    for (int i = 0; i < kMaxGrid / 32; ++i) {
+      part[i] = 0.f;
+      if (lane + 32 * i < G) {
+        const unsigned long long f = ld_relaxed_u64(flags + lane + 32 * i);
+        mine &= static_cast<int>(static_cast<unsigned>(f >> 32) - tag) >= 0;
+        part[i] = __uint_as_float(static_cast<unsigned>(f));
       }
     }
+    if (__all_sync(0xffffffffu, mine)) {
+      ok = true;
+      break;
+    }
+    if (it > 16) __nanosleep(64);
   }
-  return rsqrtf(warp_sum(ss) / static_cast<float>(ph.k) + ph.eps);
+  if (!ok && lane == 0) atomicOr(&ctl->status, ST_FLAG_TIMEOUT);
+  __threadfence();
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < kMaxGrid / 32; ++i) ss += part[i];
+  return warp_sum(ss);
+}
+
+// Sum of a per-CTA sums-of-squares array written by an earlier launch.
+__device__ float sum_ss_array(const float* ss, int lane) {
+  const int G = static_cast<int>(gridDim.x);
+  float part = 0.f;
+#pragma unroll
+  for (int i = 0; i < kMaxGrid / 32; ++i)
+    if (lane + 32 * i < G) part += __ldcg(ss + lane + 32 * i);
+  return warp_sum(part);
+}
+
+// Sum of squares of a binary16 input vector (every warp on its own).
+__device__ float input_sumsq16(const Phase& ph, int lane) {
+  float ss = 0.f;
+  const uint4* p = reinterpret_cast<const uint4*>(ph.x_src);
+  for (int i = lane; i < ph.k / 8; i += 32) {
+    const uint4 u = __ldcg(p + i);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[t]));
+      ss = fmaf(f.x, f.x, ss);
+      ss = fmaf(f.y, f.y, ss);
+    }
+  }
+  return warp_sum(ss);
 }
 
 // Form the thread's slice of x for a phase: xs2 receives 32 float2 in the
 // order pair_dot expects, each value pre-scaled by 2^-shift.  Columns
 // [64 j, 64 j + 64) belong to the thread.  All loads are issued before any
 // dependent arithmetic, so the prologue costs one round trip to L2.
-__device__ void form_x(const Phase& ph, int j, int lane, float2* xs2, bool write_dbg) {
+__device__ void form_x(const Phase& ph, int j, int lane, u64* xs2, bool write_dbg, float sumsq) {
   const bool norm = ph.x_kind == X_NORM16 || ph.x_kind == X_NORM32;
   const int k0 = j * kKT;
   float v[kKT];
   load_block_x(ph, k0, v);
   load_block_x(ph, k0 + 32, v + 32);
-  const float r = norm ? input_rms_scale(ph, lane) : 1.0f;
+  if (ph.x_kind == X_NORM16) sumsq = input_sumsq16(ph, lane);
+  const float r = norm ? rsqrtf(sumsq / static_cast<float>(ph.k) + ph.eps) : 1.0f;
   __half xv[kKT];
 #pragma unroll
   for (int e = 0; e < kKT; ++e) xv[e] = __float2half_rn(norm ? v[e] * r : v[e]);
@@ -200,7 +273,7 @@ __device__ void form_x(const Phase& ph, int j, int lane, float2* xs2, bool write
             __half2float(xv[blk * 32 + 4 * m + elem_off(e)]) * (1.0f / static_cast<float>(1 << elem_shift(e)));
         const float b = __half2float(xv[blk * 32 + 4 * m + elem_off(e + 1)]) *
                         (1.0f / static_cast<float>(1 << elem_shift(e + 1)));
-        xs2[blk * 16 + m * 4 + e / 2] = make_float2(a, b);
+        xs2[blk * 16 + m * 4 + e / 2] = pack2(__float_as_uint(a), __float_as_uint(b));
       }
     }
   }
@@ -212,17 +285,6 @@ __device__ void form_x(const Phase& ph, int j, int lane, float2* xs2, bool write
 }
 
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
-
-// Arrive (release: this CTA's earlier global writes become visible first)
-// and wait until `target` arrivals are counted (acquire), at most `limit` polls.
-__device__ bool grid_barrier(Control* ctl, unsigned long long target, uint32_t limit) {
-  asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(&ctl->barrier), "l"(1ull) : "memory");
-  for (uint32_t i = 0; i < limit; ++i) {
-    if (ld_acquire_u64(&ctl->barrier) >= target) return true;
-    if (i > 256) __nanosleep(32);
-  }
-  return false;
-}
 
 // Geometry of a phase as the consumers see it.
 struct Tile {
@@ -253,11 +315,25 @@ __device__ __forceinline__ Tile tile_of(const Phase& ph, int tid) {
 // residual sums it wrote (EPI_RESID), for the next phase's RMSNorm.
 __device__ float flush_rows(const Phase& ph, const Tile& t, const float* red, int n_buf, int u_first, int G,
                             int tid, bool reuse) {
-  named_bar_sync(1, kConsumerThreads);
-  float ss = 0.f;
+  constexpr int kPre = 4;   // residual inputs prefetched per thread (the rest load in the loop)
   const int n_slots = n_buf * t.spu;
+  float ss = 0.f;
   if (!t.dual) {
-    for (int s = tid; s < n_slots; s += kConsumerThreads) {
+    // residual inputs are loaded before the barrier so their latency overlaps it
+    unsigned short res[kPre];
+    if (ph.epi_kind == EPI_RESID) {
+#pragma unroll
+      for (int c = 0; c < kPre; ++c) {
+        const int s = tid + c * kConsumerThreads;
+        res[c] = 0;
+        if (s < n_slots) {
+          const int n = (u_first + (s / t.spu) * G) * t.rpu + s % t.spu;
+          if (n < ph.n_rows) res[c] = ph.res[n];
+        }
+      }
+    }
+    named_bar_sync(1, kConsumerThreads);
+    for (int c = 0, s = tid; s < n_slots; ++c, s += kConsumerThreads) {
       float v = 0.f;
       for (int w = 0; w < t.tw; ++w) v += red[s * t.tw + w];
       const int i = s / t.spu, rem = s % t.spu;
@@ -265,13 +341,15 @@ __device__ float flush_rows(const Phase& ph, const Tile& t, const float* red, in
       if (n < ph.n_rows) {
         ph.y[n] = v;
         if (ph.epi_kind == EPI_RESID) {
-          const float tv = __half2float(__ushort_as_half(__ldcg(ph.res + n))) + v;
+          const unsigned short rv = c < kPre ? res[c < kPre ? c : 0] : ph.res[n];
+          const float tv = __half2float(__ushort_as_half(rv)) + v;
           ph.y2[n] = tv;
           ss = fmaf(tv, tv, ss);
         }
       }
     }
   } else {
+    named_bar_sync(1, kConsumerThreads);
     for (int q = tid; q < n_slots / 2; q += kConsumerThreads) {
       float g = 0.f, u = 0.f;
       for (int w = 0; w < t.tw; ++w) {
@@ -355,16 +433,33 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
     }
   } else {
     // ------------------------------------------------------------ consumers
-    float2 xs2[kKT / 2];
+    u64 xs2[kKT / 2];
+    const Unpack kk = make_unpack();
     uint32_t it = 0;
     int base = 0;
+    const unsigned tag0 = a.n_phases > 1 ? a.ctl->epoch * kPhasesPerEpoch + 1u : 0u;   // tag of phase 0
     for (int p = 0; p < a.n_phases; ++p) {
       const Phase& ph = a.phases ? a.phases[p] : a.one;
       const Tile t = tile_of(ph, tid);
       const int units = ph.units, n_rows = ph.n_rows;
       const int u0 = (cta - base + G) % G;
-      if (u0 < units || (ph.x_dbg && cta == 0))
-        form_x(ph, t.active ? t.j : 0, lane, xs2, ph.x_dbg != nullptr && cta == 0 && t.team == 0);
+      if (u0 < units || (ph.x_dbg && cta == 0)) {
+        float sumsq = 0.f;
+        if (p > 0) {
+          // the input of a later phase is the previous phase's output: one warp
+          // waits for every CTA's flag, the CTA barrier releases the others
+          if (warp == 0) {
+            const float v = wait_phase_flags(a.flags + ((p - 1) & 1) * kMaxGrid, tag0 + (p - 1), lane,
+                                             a.wait_limit, a.ctl);
+            if (lane == 0) red_cta[0] = v;
+          }
+          named_bar_sync(1, kConsumerThreads);
+          sumsq = red_cta[0];
+        } else if (ph.x_kind == X_NORM32) {
+          sumsq = sum_ss_array(ph.ss_in, lane);   // written by an earlier launch
+        }
+        form_x(ph, t.active ? t.j : 0, lane, xs2, ph.x_dbg != nullptr && cta == 0 && t.team == 0, sumsq);
+      }
       const int cap = kRedFloats / (t.spu * t.tw);   // units buffered before a flush
       int n_buf = 0, u_first = u0;
       float ss = 0.f;
@@ -399,8 +494,8 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
             pa = sb + static_cast<size_t>(2 * t.team) * t.row_bytes;
             pb = pa + t.row_bytes;
           }
-          if (ra < n_rows) t0 = pair_dot(pa + static_cast<size_t>(t.j) * 36, xs2, 0.f);
-          if (rb < n_rows) t1 = pair_dot(pb + static_cast<size_t>(t.j) * 36, xs2, 0.f);
+          if (ra < n_rows) t0 = pair_dot(pa + static_cast<size_t>(t.j) * 36, xs2, 0.f, kk);
+          if (rb < n_rows) t1 = pair_dot(pb + static_cast<size_t>(t.j) * 36, xs2, 0.f, kk);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[stage]);
@@ -420,28 +515,24 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
         ++n_buf;
       }
       ss += flush_rows(ph, t, red, n_buf, u_first, G, tid, false);
-      // phase end: per-CTA sum of squares for the next RMSNorm, then the grid barrier
+      // phase end: publish this CTA's flag (its outputs are written; the sum of
+      // squares of its residual sums rides along for the next RMSNorm)
       const bool resid = ph.epi_kind == EPI_RESID && ph.ss_out != nullptr;
-      if (resid) {
+      if (p + 1 < a.n_phases || resid) {
         ss = warp_sum(ss);
         if (lane == 0) red_cta[warp] = ss;
-      }
-      if (p + 1 < a.n_phases || resid) {
         named_bar_sync(1, kConsumerThreads);
         if (tid == 0) {
-          if (resid) {
-            float tot = 0.f;
-            for (int w = 0; w < kConsumerWarps; ++w) tot += red_cta[w];
-            ph.ss_out[cta] = tot;
-          }
-          if (p + 1 < a.n_phases &&
-              !grid_barrier(a.ctl, static_cast<unsigned long long>(p + 1) * G, a.wait_limit)) {
-            set_status(a.ctl, ST_GRID_TIMEOUT);
-            abort_flag = 1;
+          float tot = 0.f;
+          for (int w = 0; w < kConsumerWarps; ++w) tot += red_cta[w];
+          if (resid) ph.ss_out[cta] = tot;
+          if (p + 1 < a.n_phases) {
+            const unsigned long long f =
+                (static_cast<unsigned long long>(tag0 + p) << 32) | __float_as_uint(tot);
+            st_release_u64(a.flags + (p & 1) * kMaxGrid + cta, f);
           }
         }
-        named_bar_sync(1, kConsumerThreads);
-        if (abort_flag) break;
+        named_bar_sync(1, kConsumerThreads);   // red_cta is read again at the next phase start
       }
       base = (base + units) % G;
     }
@@ -449,11 +540,13 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
 
   __syncthreads();
   if (a.n_phases > 1 && tid == 0) {
-    // The last CTA to leave resets the barrier count for the next launch.
+    // The last CTA to leave advances the epoch (so the next launch's tags are
+    // new) and resets the departure count.
     __threadfence();
-    const unsigned long long left = atomicAdd(&a.ctl->barrier, 1ull << 40) >> 40;
+    const unsigned long long left = atomicAdd(&a.ctl->depart, 1ull);
     if (left == static_cast<unsigned long long>(G) - 1) {
-      atomicExch(&a.ctl->barrier, 0ull);
+      a.ctl->depart = 0ull;
+      atomicAdd(&a.ctl->epoch, 1u);
     }
   }
 }
