@@ -151,6 +151,8 @@ def time_region(torch, stream, fn, steps, warmup, barrier, gpu_index):
 
 def run_stack(args, torch, q4, model, synth, stream, barrier, gpu_index):
     cfg, n_layers = stack_cfg(args.config)
+    if args.layers:
+        n_layers = args.layers   # a shorter stack of the same shape (small profiling case)
     shape = q4.LayerShape.of(**cfg)
     layer_bytes = q4.q4_layer_offsets(shape)[1]
     wbuf, ptrs = model.resident_layers(shape, n_layers, seed=0)
@@ -344,6 +346,8 @@ def main():
     ap.add_argument("--config", default="8b", choices=["8b", "gemv", "70b", "70b-stream"])
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--layers", type=int, default=0, help="run only this many layers of the stack (profiling)")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline (profiling runs)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank, world, local_rank = dist_env()
@@ -423,6 +427,10 @@ def main():
     out["gpu_launches"] = r["launches_per_step"] * steps
     out["clocks"] = r["clocks"]
     # the CPU oracle on a bounded sample of the same workload (rank 0 only)
+    if args.no_cpu:
+        out["cpu_baseline"] = None
+        print(json.dumps(out), flush=True)
+        return
     try:
         gbs_cpu, cores, nbytes, t = cpu_oracle_rate("gemv" if args.config == "gemv" else
                                                     ("8b" if args.config == "8b" else "70b"), args.cpu_budget)

@@ -369,6 +369,7 @@ bool stack_program(const q4_layer_shape& s, const std::vector<const uint8_t*>& l
 }
 
 int check_layer_shape_for_engine(const q4_layer_shape& s) {
+  if (s.head_dim % q4::kKT) return Q4_ERR_ARG;   // a thread's 64 attention columns stay in one head
   Phase tmp[5];
   Work w;
   memset(&w, 0, sizeof(w));

@@ -143,16 +143,17 @@ __device__ __forceinline__ void set_status(Control* ctl, int bits) {
   atomicOr(ctl ? &ctl->status : &g_status, bits);
 }
 
-// Load 32 consecutive columns [c0, c0 + 32) of the phase input (before any
-// normalisation) as floats, with 16-byte loads through L1: the row teams of a
-// CTA share the same slices, so one line fill serves them all.  The data was
-// written by other CTAs before the grid barrier, whose acquire (thread 0)
-// and CTA barrier order these loads after those writes.
-__device__ __forceinline__ void load_block_x(const Phase& ph, int c0, float* v) {
+// Load the thread's 64 consecutive columns [c0, c0 + 64) of the phase input
+// (before any normalisation) as floats, with 16-byte loads through L1: the
+// row teams of a CTA share the same slices, so one line fill serves them all.
+// The data was written by other CTAs before this phase's flags were seen.
+// For the attention gather the 64 columns lie in one query head (head_dim is
+// a multiple of 64), so they map to 64 consecutive values of one value head.
+__device__ __forceinline__ void load_x_slice(const Phase& ph, int c0, float* v) {
   if (ph.x_kind == X_F16 || ph.x_kind == X_NORM16) {
     const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __half*>(ph.x_src) + c0);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < kKT / 8; ++i) {
       const uint4 u = p[i];
       const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -163,15 +164,15 @@ __device__ __forceinline__ void load_block_x(const Phase& ph, int c0, float* v) 
       }
     }
   } else {
-    const float* src = static_cast<const float*>(ph.x_src);
+    int src0 = c0;
+    if (ph.x_kind == X_ATTN) {
+      const int hd = ph.head_dim;
+      src0 = ph.attn_off + ((c0 / hd) / ph.group) * hd + (c0 % hd);
+    }
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(ph.x_src) + src0);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      int c = c0 + 4 * i;
-      if (ph.x_kind == X_ATTN) {
-        const int hd = ph.head_dim;
-        c = ph.attn_off + ((c / hd) / ph.group) * hd + (c % hd);   // 4 columns stay in one head
-      }
-      const float4 f = *reinterpret_cast<const float4*>(src + c);
+    for (int i = 0; i < kKT / 4; ++i) {
+      const float4 f = p[i];
       v[4 * i] = f.x;
       v[4 * i + 1] = f.y;
       v[4 * i + 2] = f.z;
@@ -256,13 +257,16 @@ __device__ void form_x(const Phase& ph, int j, int lane, u64* xs2, bool write_db
   const bool norm = ph.x_kind == X_NORM16 || ph.x_kind == X_NORM32;
   const int k0 = j * kKT;
   float v[kKT];
-  load_block_x(ph, k0, v);
-  load_block_x(ph, k0 + 32, v + 32);
+  load_x_slice(ph, k0, v);
   if (ph.x_kind == X_NORM16) sumsq = input_sumsq16(ph, lane);
   const float r = norm ? rsqrtf(sumsq / static_cast<float>(ph.k) + ph.eps) : 1.0f;
   __half xv[kKT];
 #pragma unroll
-  for (int e = 0; e < kKT; ++e) xv[e] = __float2half_rn(norm ? v[e] * r : v[e]);
+  for (int e = 0; e < kKT; e += 2) {
+    const __half2 hp = norm ? __floats2half2_rn(v[e] * r, v[e + 1] * r) : __floats2half2_rn(v[e], v[e + 1]);
+    xv[e] = __low2half(hp);
+    xv[e + 1] = __high2half(hp);
+  }
 #pragma unroll
   for (int blk = 0; blk < kKT / 32; ++blk) {
 #pragma unroll
