@@ -7,7 +7,13 @@ token per step by replaying the decoder's CUDA graph (q4_layer_decode).  The
 weights are 30x larger than L2, so every step streams them from HBM.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config 8b|gemv|70b|70b-stream|sweep]
-                  [--impl reference]
+                  [--batch B] [--impl reference]
+
+--batch B (1..16) runs the stack or the streamed ring on B activation rows per
+step (weights read once per step; batch > 1 takes the tensor-core path).
+--config sweep times every projection of the resident 8B stack through the
+single-product call at B = 1, 2, 4, 8, 16 with each kernel and reports the
+fastest kernel per batch size.
 
 One JSON line per run on rank 0.  Under torchrun every rank runs its own
 replica (the product has no cross-GPU step): value = all ranks' bytes / the
@@ -153,13 +159,14 @@ def run_stack(args, torch, q4, model, synth, stream, barrier, gpu_index):
     cfg, n_layers = stack_cfg(args.config)
     if args.layers:
         n_layers = args.layers   # a shorter stack of the same shape (small profiling case)
+    B = args.batch
     shape = q4.LayerShape.of(**cfg)
     layer_bytes = q4.q4_layer_offsets(shape)[1]
     wbuf, ptrs = model.resident_layers(shape, n_layers, seed=0)
-    ws, offs, ws_bytes = model.workspace(shape, n_layers, 1)
+    ws, offs, ws_bytes = model.workspace(shape, n_layers, B)
     with torch.cuda.stream(stream):
-        dec = q4.q4_decoder_create(shape, ptrs, 1, ws, ws_bytes, q4.Q4_DEC_FUSED, stream=stream)
-        h0 = torch.from_numpy(synth.activations(1, cfg["hidden"], 0).reshape(-1).view("int16").copy())
+        dec = q4.q4_decoder_create(shape, ptrs, B, ws, ws_bytes, q4.Q4_DEC_FUSED, stream=stream)
+        h0 = torch.from_numpy(synth.activations(B, cfg["hidden"], 0).reshape(-1).view("int16").copy())
         h = h0.cuda()
     torch.cuda.synchronize()
 
@@ -192,11 +199,17 @@ def run_stack(args, torch, q4, model, synth, stream, barrier, gpu_index):
     e2e_secs = time.perf_counter() - t0
     q4.q4_decoder_destroy(dec)
     nbytes = layer_bytes * n_layers
-    return dict(secs=secs, clocks=clocks, bytes_per_step=nbytes, launches_per_step=1,
+    # batch 1: one persistent launch per token; batch B: per layer 5 tensor-core
+    # products + 4 glue launches, plus the first layer's input norm
+    launches = 1 if B == 1 else 9 * n_layers + 1
+    return dict(secs=secs, clocks=clocks, bytes_per_step=nbytes, launches_per_step=launches,
+                kernel_launches_per_step=1 if B == 1 else 5 * n_layers,
                 e2e_secs=e2e_secs, e2e_steps=e2e_steps, h2d=h0.numel() * 2, d2h=h0.numel() * 2,
                 workload=(f"{'8B' if args.config == '8b' else '70B'}-shaped decoder stack, {n_layers} layers, "
-                          f"batch 1, HBM-resident, one CUDA-graph replay per token"),
-                kernel_key=f"engine_kernel:{args.config}_stack", n_layers=n_layers, cfg=cfg)
+                          f"batch {B}, HBM-resident, one CUDA-graph replay per step"),
+                kernel="engine_kernel" if B == 1 else "mma_kernel",
+                kernel_key=f"engine_kernel:{args.config}_stack" if B == 1 else f"mma_kernel:{args.config}_stack_b{B}",
+                n_layers=n_layers, cfg=cfg)
 
 
 def run_gemv(args, torch, q4, model, synth, stream, barrier, gpu_index):
@@ -261,9 +274,10 @@ def run_stream(args, torch, q4, model, synth, stream, barrier, gpu_index):
     distinct = n_layers if avail > (n_layers + 8) * stride else max(2, int(avail * 0.6 // stride))
     blocks, hptrs = model.host_layers(shape, n_layers, seed=0, distinct=distinct)
     bufs = [torch.empty(stride, dtype=torch.uint8, device="cuda") for _ in range(2)]
-    ws, offs, ws_bytes = model.workspace(shape, n_layers, 1)
-    ring = q4.q4_stream_create(shape, hptrs, 1, bufs[0], bufs[1], stride, ws, ws_bytes, 0)
-    h = torch.from_numpy(synth.activations(1, cfg["hidden"], 0).reshape(-1).view("int16").copy()).cuda()
+    B = args.batch
+    ws, offs, ws_bytes = model.workspace(shape, n_layers, B)
+    ring = q4.q4_stream_create(shape, hptrs, B, bufs[0], bufs[1], stride, ws, ws_bytes, 0)
+    h = torch.from_numpy(synth.activations(B, cfg["hidden"], 0).reshape(-1).view("int16").copy()).cuda()
     # pinned host -> HBM copy peak, same transfer size as the ring
     cs = torch.cuda.Stream()
     best = 0.0
@@ -286,11 +300,68 @@ def run_stream(args, torch, q4, model, synth, stream, barrier, gpu_index):
     if q4.q4_stream_status(ring, stream=stream) != 0:
         raise RuntimeError("stream ring kernels reported a failed wait")
     q4.q4_stream_destroy(ring)
-    return dict(secs=secs, clocks=clocks, bytes_per_step=layer_bytes * n_layers, launches_per_step=n_layers,
+    return dict(secs=secs, clocks=clocks, bytes_per_step=layer_bytes * n_layers,
+                launches_per_step=n_layers if B == 1 else 9 * n_layers + 1,
+                kernel_launches_per_step=n_layers if B == 1 else 5 * n_layers,
                 steps_override=steps, warmup_override=warm, h2d_peak_gbs=best,
                 e2e_secs=None, workload=(f"70B-shaped stack, {n_layers} layers streamed from pinned host memory "
-                                         f"({distinct} distinct layer blocks), two HBM layer buffers, batch 1"),
-                kernel_key="engine_kernel:70b_stream", cfg=cfg, distinct=distinct)
+                                         f"({distinct} distinct layer blocks), two HBM layer buffers, batch {B}"),
+                kernel="engine_kernel" if B == 1 else "mma_kernel",
+                kernel_key="engine_kernel:70b_stream" if B == 1 else f"mma_kernel:70b_stream_b{B}", cfg=cfg,
+                distinct=distinct)
+
+
+def run_sweep(args, torch, q4, model, synth, stream, barrier, gpu_index):
+    """Every projection of the resident 8B stack through q4_gemv_ex, per batch
+    size and kernel, one CUDA graph per (batch, kernel) holding all 224 products."""
+    cfg, n_layers = stack_cfg("8b")
+    shape = q4.LayerShape.of(**cfg)
+    offs, layer_bytes = q4.q4_layer_offsets(shape)
+    wbuf, ptrs = model.resident_layers(shape, n_layers, seed=0)
+    dims = synth.layer_dims(cfg["hidden"], cfg["q_dim"], cfg["kv_dim"], cfg["ffn"])
+    kmax = max(k for _, k in dims)
+    nmax = max(n for n, _ in dims)
+    x = torch.from_numpy(synth.activations(16, kmax, 0).reshape(-1).view("int16").copy()).cuda()
+    y = torch.empty(16 * nmax, dtype=torch.float32, device="cuda")
+    kernels = {"engine": q4.Q4_KERNEL_STREAM, "mma": q4.Q4_KERNEL_MMA, "simple": q4.Q4_KERNEL_SIMPLE}
+    nbytes = layer_bytes * n_layers
+    steps = max(5, min(args.steps, 50))
+    results = {}
+    for B in (1, 2, 4, 8, 16):
+        for name, kern in kernels.items():
+            if name == "engine" and B != 1:
+                continue
+
+            def enqueue():
+                for p in ptrs:
+                    for j, (n, k) in enumerate(dims):
+                        q4.q4_gemv_ex(p + offs[j], x, y, n, k, B, kern, stream=stream)
+
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                enqueue()
+                stream.synchronize()
+                with torch.cuda.graph(g, stream=stream):
+                    enqueue()
+            with torch.cuda.stream(stream):
+                secs, clocks = time_region(torch, stream, g.replay, steps, 3, barrier, gpu_index)
+            if q4.q4_device_status() != 0:
+                raise RuntimeError(f"{name} kernel reported a failed wait at batch {B}")
+            t = secs / steps
+            results.setdefault(B, {})[name] = dict(ms_per_step=round(t * 1e3, 4),
+                                                   weight_gbs=round(nbytes / t / 1e9, 2),
+                                                   tokens_per_s=round(B / t, 1), clocks_mhz=clocks["sm_mhz"])
+            del g
+    best = {B: max(r, key=lambda k: r[k]["weight_gbs"]) for B, r in results.items()}
+    # headline of this config: batch 1 with its fastest kernel
+    b1 = results[1][best[1]]
+    return dict(secs=b1["ms_per_step"] * steps / 1e3, clocks=clocks, bytes_per_step=nbytes,
+                launches_per_step=7 * n_layers, kernel_launches_per_step=7 * n_layers,
+                steps_override=steps, warmup_override=3, e2e_secs=None,
+                workload=(f"8B-shaped projections ({n_layers} layers x 7, {nbytes} B), one single-product call each, "
+                          f"batch sweep 1-16"),
+                kernel=f"{best[1]} (q4_gemv_ex)", kernel_key=None, cfg=cfg,
+                sweep={str(B): dict(results[B], fastest=best[B]) for B in results})
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -343,7 +414,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--config", default="8b", choices=["8b", "gemv", "70b", "70b-stream"])
+    ap.add_argument("--config", default="8b", choices=["8b", "gemv", "70b", "70b-stream", "sweep"])
+    ap.add_argument("--batch", type=int, default=1, help="activation rows per step (1..16)")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--layers", type=int, default=0, help="run only this many layers of the stack (profiling)")
@@ -367,7 +439,10 @@ def main():
     else:
         barrier = lambda: None
     stream = torch.cuda.Stream()
-    runner = {"8b": run_stack, "70b": run_stack, "gemv": run_gemv, "70b-stream": run_stream}[args.config]
+    if not 1 <= args.batch <= 16 or (args.batch != 1 and args.config not in ("8b", "70b", "70b-stream")):
+        raise SystemExit("--batch: 1..16, for the 8b, 70b and 70b-stream configs")
+    runner = {"8b": run_stack, "70b": run_stack, "gemv": run_gemv, "70b-stream": run_stream,
+              "sweep": run_sweep}[args.config]
     r = runner(args, torch, q4, model, synth, stream, barrier, local_rank)
     steps = r.get("steps_override", args.steps)
     warmup = r.get("warmup_override", args.warmup)
@@ -385,8 +460,12 @@ def main():
             import torch.distributed as dist
             dist.destroy_process_group()
         return
-    per_launch_s = per_step / r["launches_per_step"]
-    bytes_per_launch = r["bytes_per_step"] / r["launches_per_step"]
+    # the dominant kernel's launches carry all the weight bytes; with one launch
+    # per step (batch 1 resident) its duration is the step's, otherwise the
+    # step time (glue launches included) divided among its launches bounds it
+    kl = r.get("kernel_launches_per_step", r["launches_per_step"])
+    per_launch_s = per_step / kl
+    bytes_per_launch = r["bytes_per_step"] / kl
     out = {
         "metric": METRIC,
         "value": round(gbs, 2),
@@ -400,15 +479,15 @@ def main():
         "vs_baseline": None,
         "dtype": "q4_0 weights x f16 activations, f32 accumulate",
         "data": "synthetic (seeded Philox: uniform 4-bit codes, |N(0,0.02)| binary16 scales, N(0,1) binary16 x)",
-        "config": {"workload": r["workload"], "batch": 1, "parallelism": f"replicas x{world}",
+        "config": {"workload": r["workload"], "batch": args.batch, "parallelism": f"replicas x{world}",
                    "l2": "weights per step exceed L2 (no flush needed)"},
     }
     if args.config in ("8b", "70b"):
-        out["tokens_per_s"] = round(world / per_step, 2)
+        out["tokens_per_s"] = round(world * args.batch / per_step, 2)
         out["config"]["n_layers"] = r["n_layers"]
         out["config"]["weight_bytes_per_token"] = r["bytes_per_step"]
     if args.config == "70b-stream":
-        out["tokens_per_s"] = round(world / per_step, 3)
+        out["tokens_per_s"] = round(world * args.batch / per_step, 3)
         out["host_link"] = {"achieved_gbs": round(r["bytes_per_step"] / per_step / 1e9, 2),
                             "pinned_h2d_peak_gbs": round(r["h2d_peak_gbs"], 2),
                             "frac": round(r["bytes_per_step"] / per_step / 1e9 / r["h2d_peak_gbs"], 4)}
@@ -417,8 +496,12 @@ def main():
     out["roofline"] = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                        "frac": round(achieved / peak, 4), "peak_source": f"hbm_gbs {peak_kind}",
                        "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
-                       "traffic": ncu_traffic(r["kernel_key"]), "kernel": "engine_kernel",
-                       "bytes_per_launch": int(bytes_per_launch)}
+                       "traffic": ncu_traffic(r["kernel_key"]) if r["kernel_key"] else None,
+                       "kernel": r.get("kernel", "engine_kernel"), "bytes_per_launch": int(bytes_per_launch)}
+    if kl != 1 or r["launches_per_step"] != 1:
+        out["roofline"]["timing"] = "step time / launches of the kernel per step (glue launches included)"
+    if "sweep" in r:
+        out["sweep"] = r["sweep"]
     if r.get("e2e_secs"):
         e2e_bytes = r.get("e2e_bytes_per_step", r["bytes_per_step"])
         out["e2e"] = {"value": round(e2e_bytes / (r["e2e_secs"] / r["e2e_steps"]) / 1e9, 2), "unit": "GB/s",
@@ -433,7 +516,8 @@ def main():
         return
     try:
         gbs_cpu, cores, nbytes, t = cpu_oracle_rate("gemv" if args.config == "gemv" else
-                                                    ("8b" if args.config == "8b" else "70b"), args.cpu_budget)
+                                                    ("8b" if args.config in ("8b", "sweep") else "70b"),
+                                                    args.cpu_budget)
         out["cpu_baseline"] = {"value": round(gbs_cpu, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                                "sample": f"{nbytes} weight bytes of row-sampled projections of the same "
                                          f"workload in {t:.1f} s, fp64, {cores} threads"}

@@ -1,0 +1,172 @@
+"""Decoder stack and streamed ring at batch 2..16 (tensor-core products + glue kernels)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as ora
+import weight_streaming_q4_gb300 as q4
+from weight_streaming_q4_gb300 import build, model, synth
+from gpu_util import dev_u16, host_u16
+from layer_check import check_layer, read_ws, sampled_rows
+
+pytestmark = pytest.mark.gpu
+
+TINY = dict(hidden=256, q_dim=256, kv_dim=128, ffn=1024, head_dim=64)
+SMALL = dict(hidden=2048, q_dim=2048, kv_dim=512, ffn=4096, head_dim=128)
+MID = dict(hidden=1024, q_dim=1024, kv_dim=256, ffn=14336, head_dim=128)
+ODD = dict(hidden=768, q_dim=768, kv_dim=192, ffn=2816, head_dim=64)   # 3 KV heads for 12 query heads
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+    ora.build()
+
+
+class Stack:
+    def __init__(self, cfg, n_layers, seed, batch, mode=q4.Q4_DEC_FUSED, ptrs=None):
+        self.cfg, self.batch = cfg, batch
+        self.shape = q4.LayerShape.of(**cfg)
+        if ptrs is None:
+            self.wbuf, self.ptrs = model.resident_layers(self.shape, n_layers, seed)
+        else:
+            self.ptrs = ptrs
+        self.ws, self.offs, self.ws_bytes = model.workspace(self.shape, n_layers, batch)
+        self.dec = q4.q4_decoder_create(self.shape, self.ptrs, batch, self.ws, self.ws_bytes, mode)
+
+    def run(self, h_np, graph=True, reps=1):
+        h = dev_u16(h_np.reshape(-1))
+        for _ in range(reps):
+            (q4.q4_layer_decode if graph else q4.q4_layer_decode_eager)(self.dec, h)
+        torch.cuda.synchronize()
+        assert q4.q4_decoder_status(self.dec) == 0
+        return host_u16(h).reshape(self.batch, -1)
+
+    def state(self):
+        return read_ws(self.ws, self.offs, self.cfg, self.batch)
+
+    def close(self):
+        q4.q4_decoder_destroy(self.dec)
+
+
+@pytest.mark.parametrize("batch", [2, 8, 9, 16])
+@pytest.mark.parametrize("cfg", [TINY, SMALL, ODD], ids=["tiny", "small", "odd"])
+def test_one_layer_step_by_step(cfg, batch):
+    st = Stack(cfg, 1, seed=81, batch=batch)
+    h0 = synth.activations(batch, cfg["hidden"], 82)
+    h1 = st.run(h0)
+    check_layer(cfg, 81, 0, st.state(), h1, h_in16=h0)
+    st.close()
+
+
+def test_last_layer_of_a_stack_wide_down():
+    cfg, L, B = MID, 3, 8
+    h0 = synth.activations(B, cfg["hidden"], 84)
+    st = Stack(cfg, L, seed=83, batch=B)
+    prev = Stack(cfg, L - 1, seed=83, batch=B, ptrs=st.ptrs[:-1])
+    prev.run(h0)
+    t_prev = prev.state()["t2"]
+    hL = st.run(h0)
+    check_layer(cfg, 83, L - 1, st.state(), hL, t_prev=t_prev, rows=sampled_rows(256, 1))
+    st.close()
+    prev.close()
+
+
+def test_rows_do_not_depend_on_the_batch():
+    """Each batch row's result is the same whatever the other rows hold and
+    whatever the batch size (one or two n-tiles of the tensor-core product)."""
+    cfg = SMALL
+    h16 = synth.activations(16, cfg["hidden"], 90)
+    full = Stack(cfg, 2, seed=91, batch=16)
+    a = full.run(h16)
+    for b in (2, 5, 8):
+        part = Stack(cfg, 2, seed=91, batch=b, ptrs=full.ptrs)
+        got = part.run(h16[:b])
+        assert np.array_equal(got, a[:b]), b
+        part.close()
+    # change the other rows: row 0 unchanged
+    h_mix = h16.copy()
+    h_mix[1:] = synth.activations(15, cfg["hidden"], 92)
+    assert np.array_equal(full.run(h_mix)[0], a[0])
+    full.close()
+
+
+def test_graph_eager_and_pointer_change_identical():
+    cfg, B = TINY, 4
+    h0 = synth.activations(B, cfg["hidden"], 93)
+    st = Stack(cfg, 3, seed=94, batch=B)
+    a = st.run(h0, graph=True, reps=2)
+    b = st.run(h0, graph=False, reps=2)
+    c = st.run(h0, graph=True, reps=2)     # a new buffer: captured again
+    assert np.array_equal(a, b) and np.array_equal(a, c)
+    st.close()
+
+
+def test_drift_against_oracle_chain():
+    cfg, L, B = SMALL, 3, 4
+    h0 = synth.activations(B, cfg["hidden"], 95)
+    st = Stack(cfg, L, seed=96, batch=B)
+    hL = st.run(h0)
+    z = ora.rmsnorm(h0, B, cfg["hidden"])
+    for l in range(L):
+        ws = [synth.q4_matrix(n, k, 96, synth.tensor_id(l, p))
+              for p, (n, k) in enumerate(synth.layer_dims(cfg["hidden"], cfg["q_dim"], cfg["kv_dim"], cfg["ffn"]))]
+        z, _ = ora.layer(ws, z, B, cfg["hidden"], cfg["q_dim"], cfg["kv_dim"], cfg["ffn"], cfg["head_dim"])
+    a = hL.view(np.float16).astype(np.float64)
+    b = z.view(np.float16).astype(np.float64)
+    for r in range(B):
+        assert np.linalg.norm(a[r] - b[r]) / np.linalg.norm(b[r]) < 1e-2, r
+    st.close()
+
+
+@pytest.mark.parametrize("flags", [0, q4.Q4_STREAM_POISON], ids=["plain", "poison"])
+def test_streamed_equals_resident(flags):
+    cfg, L, B = SMALL, 4, 8
+    shape = q4.LayerShape.of(**cfg)
+    h0 = synth.activations(B, cfg["hidden"], 97)
+    blocks, hptrs = model.host_layers(shape, L, 98)
+    stride = model.layer_stride(shape)
+    bufs = [torch.empty(stride, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    ws, offs, nb = model.workspace(shape, L, B)
+    ring = q4.q4_stream_create(shape, hptrs, B, bufs[0], bufs[1], stride, ws, nb, flags)
+    h = dev_u16(h0.reshape(-1))
+    for _ in range(2):
+        q4.q4_stream_layers(ring, h)
+    torch.cuda.synchronize()
+    assert q4.q4_stream_status(ring) == 0
+    got = host_u16(h).reshape(B, -1)
+    q4.q4_stream_destroy(ring)
+    ref = Stack(cfg, L, seed=98, batch=B)
+    want = ref.run(h0, reps=2)
+    assert np.array_equal(got, want)
+    ref.close()
+
+
+def test_8b_stack_batch8_full_size():
+    cfg = dict(synth.LLAMA_8B)
+    L = cfg.pop("n_layers")
+    B = 8
+    st = Stack(cfg, L, seed=0, batch=B)
+    prev = Stack(cfg, L - 1, seed=0, batch=B, ptrs=st.ptrs[:-1])
+    h0 = synth.activations(B, cfg["hidden"], 1)
+    prev.run(h0)
+    t_prev = prev.state()["t2"]
+    hL = st.run(h0)
+    stats = st.state()
+    check_layer(cfg, 0, L - 1, stats, hL, t_prev=t_prev, rows=sampled_rows(96, 2))
+    assert np.all(np.isfinite(hL.view(np.float16).astype(np.float64)))
+    for name in ("qkv", "o", "g", "u", "dn", "t1", "t2"):
+        assert np.all(np.isfinite(stats[name])), name
+    st.close()
+    prev.close()
+
+
+def test_batched_shape_limits():
+    shape = q4.LayerShape.of(**TINY)
+    wbuf, ptrs = model.resident_layers(shape, 1, 1)
+    ws, offs, nb = model.workspace(shape, 1, 16)
+    with pytest.raises(q4.Q4Error):
+        q4.q4_decoder_create(shape, ptrs, 17, ws, nb)
+    bad = q4.LayerShape.of(**dict(TINY, ffn=1056))     # ffn a multiple of 32, not of 256
+    with pytest.raises(q4.Q4Error):
+        q4.q4_decoder_create(bad, ptrs, 4, ws, nb)

@@ -11,7 +11,7 @@ from pins import golden_blocks
 
 pytestmark = pytest.mark.gpu
 
-KERNELS = {"stream": q4.Q4_KERNEL_STREAM, "simple": q4.Q4_KERNEL_SIMPLE}
+KERNELS = {"stream": q4.Q4_KERNEL_STREAM, "simple": q4.Q4_KERNEL_SIMPLE, "mma": q4.Q4_KERNEL_MMA}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -103,6 +103,39 @@ def test_stream_kernel_parity(n, k):
     y = run(w, x, n, k, 1, q4.Q4_KERNEL_STREAM)
     y_ref, s_ref = ora.gemv(w, x, n, k, threads=8)
     assert_within_tol(y, y_ref, s_ref, f"stream {n}x{k}")
+
+
+MMA_SHAPES = [(1, 256, 1), (16, 256, 2), (17, 512, 3), (100, 2048, 8), (129, 4096, 9), (300, 4096, 16),
+              (61, 14336, 4), (33, 28672, 1), (1000, 8192, 7), (64, 2304, 12)]
+
+
+@pytest.mark.parametrize("n,k,batch", MMA_SHAPES)
+def test_mma_kernel_parity(n, k, batch):
+    w = synth.q4_matrix(n, k, 12, synth.GEMV_TID)
+    x = synth.activations(batch, k, 13)
+    y = run(w, x, n, k, batch, q4.Q4_KERNEL_MMA)
+    y_ref, s_ref = ora.gemv(w, x, n, k, batch=batch, threads=8)
+    assert_within_tol(y, y_ref, s_ref, f"mma {n}x{k}x{batch}")
+    assert q4.q4_device_status() == 0
+
+
+@pytest.mark.parametrize("batch", [2, 8, 16])
+def test_mma_batch_rows_are_independent(batch):
+    # a batch gives, row for row, what each row gives alone (same kernel)
+    n, k = 96, 4096
+    w = synth.q4_matrix(n, k, 14, synth.GEMV_TID)
+    x = synth.activations(batch, k, 15)
+    y = run(w, x, n, k, batch, q4.Q4_KERNEL_MMA)
+    for b in (0, batch - 1):
+        yb = run(w, x[b:b + 1], n, k, 1, q4.Q4_KERNEL_MMA)
+        assert np.array_equal(y[b], yb[0])
+
+
+def test_auto_picks_mma_for_batches():
+    n, k, batch = 64, 4096, 4
+    w = synth.q4_matrix(n, k, 16, synth.GEMV_TID)
+    x = synth.activations(batch, k, 17)
+    assert np.array_equal(run(w, x, n, k, batch, q4.Q4_KERNEL_AUTO), run(w, x, n, k, batch, q4.Q4_KERNEL_MMA))
 
 
 @pytest.mark.parametrize("n,k,batch", [(1, 32, 1), (9, 96, 2), (40, 800, 5), (65, 4096, 16), (33, 2048, 3)])

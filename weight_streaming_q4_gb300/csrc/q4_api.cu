@@ -58,6 +58,7 @@ int device_info(DeviceInfo** out) {
   if (!d.ready) {
     Q4_CUDA(cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev));
     Q4_CUDA(q4::engine_prepare());
+    Q4_CUDA(q4::mma_prepare());
     Q4_CUDA(q4::engine_occupancy(&d.engine_blocks_per_sm));
     if (d.engine_blocks_per_sm < 1) return Q4_ERR_CUDA;
     d.ready = true;
@@ -132,9 +133,20 @@ extern "C" int q4_gemv_ex(const void* w, const uint16_t* x, float* y, int n, int
   int st = check_gemv(w, x, y, n, k, batch);
   if (st != Q4_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (kernel == Q4_KERNEL_AUTO) kernel = (batch == 1 && engine_ok(k)) ? Q4_KERNEL_STREAM : Q4_KERNEL_SIMPLE;
+  if (kernel == Q4_KERNEL_AUTO) {
+    if (batch == 1 && engine_ok(k)) kernel = Q4_KERNEL_STREAM;
+    else if (k % 256 == 0) kernel = Q4_KERNEL_MMA;
+    else kernel = Q4_KERNEL_SIMPLE;
+  }
   if (kernel == Q4_KERNEL_SIMPLE) {
     Q4_CUDA(q4::simple_launch(static_cast<const uint8_t*>(w), x, y, n, k, batch, s));
+    return Q4_OK;
+  }
+  if (kernel == Q4_KERNEL_MMA) {
+    if (k % 256 != 0) return Q4_ERR_ARG;   // row segments of a tile must start 16-byte aligned
+    DeviceInfo* dev = nullptr;
+    if ((st = device_info(&dev)) != Q4_OK) return st;
+    Q4_CUDA(q4::mma_launch(static_cast<const uint8_t*>(w), x, y, n, k, batch, dev->sm_count, kWaitLimit, nullptr, s));
     return Q4_OK;
   }
   if (kernel != Q4_KERNEL_STREAM || batch != 1 || !engine_ok(k)) return Q4_ERR_ARG;
@@ -167,9 +179,10 @@ extern "C" int q4_gemv(const void* w, const uint16_t* x, float* y, int n, int k,
 
 extern "C" int q4_device_status(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return cuda_fail(cudaGetLastError());
-  int v = 0;
+  int v = 0, m = 0;
   Q4_CUDA(q4::engine_read_status(&v));
-  return v;
+  Q4_CUDA(q4::mma_read_status(&m));
+  return v | m;
 }
 
 extern "C" int q4_dequant_debug(const void* w, float* w_out, int n, int k, void* stream) {
@@ -376,6 +389,36 @@ int check_layer_shape_for_engine(const q4_layer_shape& s) {
   return layer_phases(s, nullptr, nullptr, w, tmp) && final_phase(s, nullptr, w, &tmp[4]) ? Q4_OK : Q4_ERR_ARG;
 }
 
+// One layer for a batch of more than one row: the tensor-core product for each
+// projection and the glue kernels between them (the same arithmetic as the
+// batch-1 engine's phases).  The layer's input is the caller's binary16
+// state (first layer) or the previous layer's z in w.x; `out` receives the
+// normalised output of the last layer.
+int launch_layer_batched(const q4_layer_shape& sh, const uint8_t* wl, int layer, int n_layers, uint16_t* h,
+                         const Work& w, int batch, int grid, cudaStream_t s) {
+  size_t off[7];
+  if (q4_layer_offsets(&sh, off, nullptr) != Q4_OK) return Q4_ERR_ARG;
+  const int H = sh.hidden, Q = sh.q_dim, KV = sh.kv_dim, F = sh.ffn;
+  const int nqkv = Q + 2 * KV;
+  const int group = (Q / sh.head_dim) / (KV / sh.head_dim);
+  if (layer == 0) Q4_CUDA(q4::glue_norm(h, nullptr, batch, H, sh.eps, w.x, s));
+  Q4_CUDA(q4::mma_launch(wl + off[Q4_PROJ_Q], w.x, w.qkv, nqkv, H, batch, grid, kWaitLimit, &w.ctl->status, s));
+  Q4_CUDA(q4::glue_attn(w.qkv, batch, nqkv, Q, Q + KV, sh.head_dim, group, w.attn, s));
+  Q4_CUDA(q4::mma_launch(wl + off[Q4_PROJ_O], w.attn, w.o, H, Q, batch, grid, kWaitLimit, &w.ctl->status, s));
+  Q4_CUDA(q4::glue_resid_norm(w.x, w.o, batch, H, sh.eps, w.t1, w.x2, s));
+  Q4_CUDA(q4::mma_launch(wl + off[Q4_PROJ_GATE], w.x2, w.g, F, H, batch, grid, kWaitLimit, &w.ctl->status, s));
+  Q4_CUDA(q4::mma_launch(wl + off[Q4_PROJ_UP], w.x2, w.u, F, H, batch, grid, kWaitLimit, &w.ctl->status, s));
+  Q4_CUDA(q4::glue_silu(w.g, w.u, static_cast<size_t>(batch) * F, w.act, s));
+  Q4_CUDA(q4::mma_launch(wl + off[Q4_PROJ_DOWN], w.act, w.dn, H, F, batch, grid, kWaitLimit, &w.ctl->status, s));
+  // the next layer's z goes to w.x; the last layer's to the caller's buffer
+  Q4_CUDA(q4::glue_resid_norm(w.x2, w.dn, batch, H, sh.eps, w.t2, layer + 1 == n_layers ? h : w.x, s));
+  return Q4_OK;
+}
+
+bool batched_shape_ok(const q4_layer_shape& s) {
+  return s.hidden % 256 == 0 && s.q_dim % 256 == 0 && s.ffn % 256 == 0 && (s.q_dim + 2 * s.kv_dim) > 0;
+}
+
 int launch_layers(const Work& w, int first_phase, int n_phases, int grid, cudaStream_t s) {
   EngineArgs a;
   memset(&a, 0, sizeof(a));
@@ -411,6 +454,16 @@ struct q4_decoder {
 };
 
 static int decoder_write_program(q4_decoder* d, uint16_t* h, cudaStream_t s) {
+  if (d->batch > 1) {   // the batched path passes pointers as launch arguments
+    d->cur_h = h;
+    if (d->exec) {        // re-capture with the new buffer
+      cudaGraphExecDestroy(d->exec);
+      cudaGraphDestroy(d->graph);
+      d->exec = nullptr;
+      d->graph = nullptr;
+    }
+    return Q4_OK;
+  }
   std::vector<Phase> prog;
   if (!stack_program(d->shape, d->layers, h, d->w, prog)) return Q4_ERR_ARG;
   // pageable source: the runtime stages it before returning, so `prog` may go
@@ -421,6 +474,13 @@ static int decoder_write_program(q4_decoder* d, uint16_t* h, cudaStream_t s) {
 
 static int decoder_enqueue(q4_decoder* d, cudaStream_t s) {
   const int L = d->n_layers;
+  if (d->batch > 1) {
+    for (int l = 0; l < L; ++l) {
+      int st = launch_layer_batched(d->shape, d->layers[l], l, L, d->cur_h, d->w, d->batch, d->grid, s);
+      if (st != Q4_OK) return st;
+    }
+    return Q4_OK;
+  }
   if (d->mode == Q4_DEC_FUSED) return launch_layers(d->w, 0, 4 * L + 1, d->grid, s);
   for (int l = 0; l < L; ++l) {   // the last launch also runs the closing phase
     int st = launch_layers(d->w, 4 * l, l == L - 1 ? 5 : 4, d->grid, s);
@@ -433,10 +493,11 @@ extern "C" int q4_decoder_create(q4_decoder** out, const q4_layer_shape* shape, 
                                  int n_layers, int batch, void* workspace, size_t workspace_bytes, int mode,
                                  void* stream) {
   if (!out || !shape_ok(shape) || !layer_weights || n_layers < 1 || !workspace) return Q4_ERR_ARG;
-  if (batch != 1) return Q4_ERR_ARG;   // the persistent engine's exact CUDA-core path is batch 1
+  if (batch < 1 || batch > q4::kMaxBatch) return Q4_ERR_ARG;
   if (4 * n_layers + 1 > static_cast<int>(q4::kPhasesPerEpoch)) return Q4_ERR_ARG;
   if (mode != Q4_DEC_FUSED && mode != Q4_DEC_PER_LAYER) return Q4_ERR_ARG;
-  if (check_layer_shape_for_engine(*shape) != Q4_OK) return Q4_ERR_ARG;
+  // batch 1: the persistent exact CUDA-core engine; larger batches: tensor-core products + glue
+  if (batch == 1 ? check_layer_shape_for_engine(*shape) != Q4_OK : !batched_shape_ok(*shape)) return Q4_ERR_ARG;
   if (!aligned(workspace, 256)) return Q4_ERR_ALIGN;
   for (int l = 0; l < n_layers; ++l) {
     if (!layer_weights[l]) return Q4_ERR_ARG;
@@ -587,8 +648,9 @@ extern "C" int q4_stream_create(q4_stream** out, const q4_layer_shape* shape, co
                                 void* workspace, size_t workspace_bytes, int flags) {
   if (!out || !shape_ok(shape) || !host_layers || n_layers < 1 || !dev_buf0 || !dev_buf1 || !workspace)
     return Q4_ERR_ARG;
-  if (batch != 1 || (flags & ~Q4_STREAM_POISON)) return Q4_ERR_ARG;
-  if (check_layer_shape_for_engine(*shape) != Q4_OK) return Q4_ERR_ARG;
+  if (batch < 1 || batch > q4::kMaxBatch || (flags & ~Q4_STREAM_POISON)) return Q4_ERR_ARG;
+  if (4 * n_layers + 1 > static_cast<int>(q4::kPhasesPerEpoch)) return Q4_ERR_ARG;
+  if (batch == 1 ? check_layer_shape_for_engine(*shape) != Q4_OK : !batched_shape_ok(*shape)) return Q4_ERR_ARG;
   if (!aligned(dev_buf0, 256) || !aligned(dev_buf1, 256) || !aligned(workspace, 256)) return Q4_ERR_ALIGN;
   size_t lo[7], layer_bytes = 0;
   q4_layer_offsets(shape, lo, &layer_bytes);
@@ -635,7 +697,7 @@ extern "C" int q4_stream_layers(q4_stream* r, uint16_t* hidden_io, void* compute
   if (!r || !hidden_io) return Q4_ERR_ARG;
   if (!aligned(hidden_io, 16)) return Q4_ERR_ALIGN;
   cudaStream_t cs = static_cast<cudaStream_t>(compute_stream);
-  if (hidden_io != r->cur_h) {
+  if (hidden_io != r->cur_h && r->batch == 1) {
     // layer i computes on staging buffer i % 2
     std::vector<const uint8_t*> bufs(r->n_layers);
     for (int i = 0; i < r->n_layers; ++i) bufs[i] = r->buf[i & 1];
@@ -644,6 +706,7 @@ extern "C" int q4_stream_layers(q4_stream* r, uint16_t* hidden_io, void* compute
     Q4_CUDA(cudaMemcpyAsync(r->w.prog, prog.data(), prog.size() * sizeof(Phase), cudaMemcpyHostToDevice, cs));
     r->cur_h = hidden_io;
   }
+  if (r->batch > 1) r->cur_h = hidden_io;
   // The copy stream may only overwrite a buffer once everything queued on the
   // compute stream before this call (earlier tokens) has finished with it.
   Q4_CUDA(cudaEventRecord(r->start, cs));
@@ -657,7 +720,9 @@ extern "C" int q4_stream_layers(q4_stream* r, uint16_t* hidden_io, void* compute
     Q4_CUDA(cudaEventRecord(r->loaded[b], r->copy));
     // compute stream: layer i once its weights have landed
     Q4_CUDA(cudaStreamWaitEvent(cs, r->loaded[b], 0));
-    int st = launch_layers(r->w, 4 * i, i == r->n_layers - 1 ? 5 : 4, r->grid, cs);
+    int st = r->batch == 1
+                 ? launch_layers(r->w, 4 * i, i == r->n_layers - 1 ? 5 : 4, r->grid, cs)
+                 : launch_layer_batched(r->shape, r->buf[b], i, r->n_layers, hidden_io, r->w, r->batch, r->grid, cs);
     if (st != Q4_OK) return st;
     if (r->flags & Q4_STREAM_POISON) Q4_CUDA(q4::poison_launch(r->buf[b], n_blocks, cs));
     Q4_CUDA(cudaEventRecord(r->freed[b], cs));

@@ -191,6 +191,17 @@ cudaError_t simple_launch(const uint8_t* w, const uint16_t* x, float* y, int n, 
                           cudaStream_t stream);
 cudaError_t dequant_launch(const uint8_t* w, float* out, int n, int k, cudaStream_t stream);
 cudaError_t poison_launch(uint8_t* buf, size_t n_blocks, cudaStream_t stream);
+cudaError_t mma_prepare();
+cudaError_t mma_launch(const uint8_t* w, const uint16_t* x, float* y, int n, int k, int batch, int grid,
+                       uint32_t wait_limit, int* status, cudaStream_t stream);
+cudaError_t mma_read_status(int* out);
+cudaError_t glue_norm(const uint16_t* src16, const float* src32, int batch, int dim, float eps, uint16_t* z,
+                      cudaStream_t s);
+cudaError_t glue_resid_norm(const uint16_t* z, const float* o, int batch, int dim, float eps, float* t,
+                            uint16_t* z_out, cudaStream_t s);
+cudaError_t glue_attn(const float* qkv, int batch, int ld, int q_dim, int v_off, int hd, int group, uint16_t* a,
+                      cudaStream_t s);
+cudaError_t glue_silu(const float* g, const float* u, size_t n, uint16_t* act, cudaStream_t s);
 
 }  // namespace q4
 

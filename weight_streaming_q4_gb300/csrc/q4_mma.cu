@@ -1,0 +1,277 @@
+// Tensor-core Q4_0 matrix-vector product for batch 1..16 (sm_103a).
+//
+// y[b][n] = sum_k W[n][k] x[b][k] with the 4-bit codes turned into exact
+// binary16 values (q - 8) in registers and multiplied by binary16 x on the
+// tensor cores (mma.sync m16n8k16, fp32 accumulate): every product is exact,
+// the 16-term sums of one instruction are accumulated in fp32, and each
+// 32-weight block's sum is scaled by its d once, in fp32.  The batch is the
+// n dimension of the instruction (one n-tile of 8 columns for batch <= 8, two
+// for batch <= 16), so the weights are read once for every batch row
+// (PIPO summary, Method, "Computation optimization": 4-bit matrix-vector
+// products without dequantisation; "Automatic configuration": that kernel
+// serves batch sizes below 16).
+//
+// Persistent, one CTA per SM, 17 warps: warp 16 streams 16-row x 2048-column
+// tiles of the weights into a ring of shared-memory stages with 1-D bulk TMA
+// copies (one per row segment, rows padded to keep the code-word loads free of
+// bank conflicts); warps 0-15 each take 4 of the stage's 64 blocks.  A row
+// tile's partial sums stay in registers across its column chunks and are
+// summed over the 16 warps in a fixed order when the tile ends.
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "q4_device.cuh"
+
+namespace q4 {
+
+__device__ int g_status_mma;   // status bits of the tensor-core kernel's waits
+
+constexpr int kMmaWarps = 16;                    // consumer warps
+constexpr int kMmaThreads = (kMmaWarps + 1) * 32;
+constexpr int kMmaChunkBlocks = 64;              // 2048 columns per stage
+constexpr int kMmaRowPitch = kMmaChunkBlocks * kBlockBytes + 16;   // 1168 B: 292 words, rows 4 banks apart
+constexpr int kMmaStageBytes = 16 * kMmaRowPitch;                  // 18688 B
+constexpr int kMmaStages = 10;
+
+struct MmaArgs {
+  const uint8_t* w;   // Q4_0 [n][k/32]
+  const __half* x;    // binary16 [batch][k]
+  float* y;           // fp32 [batch][n]
+  int n, k, batch;
+  uint32_t wait_limit;
+  int* status;        // where timed-out waits are recorded (g_status_mma if none given)
+};
+
+__device__ __forceinline__ void mma16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Exact binary16 (q - 8) for the 8 codes of one code word w (bytes 4t..4t+3
+// of a block's code bytes: elements 4t..4t+3 low nibbles, 4t+16..4t+19 high).
+// The code in the low mantissa bits of 1024 gives 1024 + q (or 1024 + 16 q for
+// a high nibble); subtracting 1032 (or scaling by 1/16 and subtracting 72) is
+// exact.  Output half2 pairs, elements (4t, 4t+2), (4t+1, 4t+3),
+// (4t+16, 4t+18), (4t+17, 4t+19).
+__device__ __forceinline__ void unpack_word(uint32_t w, uint32_t magic, uint32_t& l02, uint32_t& l13,
+                                            uint32_t& h02, uint32_t& h13) {
+  const uint32_t w8 = w >> 8;
+  uint32_t a, b, c, d;
+  asm("lop3.b32 %0, %1, 0x000F000F, %2, 0xEA;" : "=r"(a) : "r"(w), "r"(magic));
+  asm("lop3.b32 %0, %1, 0x000F000F, %2, 0xEA;" : "=r"(b) : "r"(w8), "r"(magic));
+  asm("lop3.b32 %0, %1, 0x00F000F0, %2, 0xEA;" : "=r"(c) : "r"(w), "r"(magic));
+  asm("lop3.b32 %0, %1, 0x00F000F0, %2, 0xEA;" : "=r"(d) : "r"(w8), "r"(magic));
+  const __half2 k1032 = __floats2half2_rn(1032.f, 1032.f);
+  const __half2 k16 = __floats2half2_rn(0.0625f, 0.0625f);
+  const __half2 k72 = __floats2half2_rn(-72.f, -72.f);
+  __half2 A = __hsub2(*reinterpret_cast<__half2*>(&a), k1032);
+  __half2 B = __hsub2(*reinterpret_cast<__half2*>(&b), k1032);
+  __half2 C = __hfma2(*reinterpret_cast<__half2*>(&c), k16, k72);
+  __half2 D = __hfma2(*reinterpret_cast<__half2*>(&d), k16, k72);
+  l02 = *reinterpret_cast<uint32_t*>(&A);
+  l13 = *reinterpret_cast<uint32_t*>(&B);
+  h02 = *reinterpret_cast<uint32_t*>(&C);
+  h13 = *reinterpret_cast<uint32_t*>(&D);
+}
+
+// The B fragments of one block for batch column `col`: x elements in the
+// k order of unpack_word (zero for columns beyond the batch).
+__device__ __forceinline__ void x_frags(const __half* x, int k, int batch, int col, int blk, int t, uint32_t& s0b0,
+                                        uint32_t& s0b1, uint32_t& s1b0, uint32_t& s1b1) {
+  if (col < batch) {
+    const uint2 lo = *reinterpret_cast<const uint2*>(x + static_cast<size_t>(col) * k + blk * 32 + 4 * t);
+    const uint2 hi = *reinterpret_cast<const uint2*>(x + static_cast<size_t>(col) * k + blk * 32 + 16 + 4 * t);
+    s0b0 = __byte_perm(lo.x, lo.y, 0x5410);   // elements 4t, 4t+2
+    s0b1 = __byte_perm(lo.x, lo.y, 0x7632);   // elements 4t+1, 4t+3
+    s1b0 = __byte_perm(hi.x, hi.y, 0x5410);
+    s1b1 = __byte_perm(hi.x, hi.y, 0x7632);
+  } else {
+    s0b0 = s0b1 = s1b0 = s1b1 = 0u;
+  }
+}
+
+// Code word t of block b of a staged row and its scale.
+__device__ __forceinline__ uint32_t code_word(const uint8_t* row, int b, int t) {
+  const uint8_t* p = row + b * kBlockBytes + 2 + 4 * t;
+  if (b & 1) return *reinterpret_cast<const uint32_t*>(p);   // 4-byte aligned for odd blocks
+  const uint32_t lo = *reinterpret_cast<const uint32_t*>(p - 2);
+  const uint32_t hi = *reinterpret_cast<const uint32_t*>(p + 2);
+  return __funnelshift_r(lo, hi, 16);
+}
+
+__device__ __forceinline__ float row_scale(const uint8_t* row, int b) {
+  return __half2float(*reinterpret_cast<const __half*>(row + b * kBlockBytes));
+}
+
+extern __shared__ __align__(128) uint8_t g_mma_ring[];
+
+template <int NT>
+__global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const __grid_constant__ MmaArgs a) {
+  __shared__ __align__(8) uint64_t full_bar[kMmaStages];
+  __shared__ __align__(8) uint64_t empty_bar[kMmaStages];
+  __shared__ float red[kMmaWarps][32][4 * NT];
+  __shared__ volatile int abort_flag;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = gridDim.x, cta = blockIdx.x;
+  const int nb = a.k / kQK;                                   // blocks per row
+  const int chunks = (nb + kMmaChunkBlocks - 1) / kMmaChunkBlocks;
+  const int tiles = (a.n + 15) / 16;
+  const uint32_t row_bytes = static_cast<uint32_t>(nb) * kBlockBytes;
+
+  if (tid == 0) {
+    for (int s = 0; s < kMmaStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], kMmaWarps);
+    }
+    fence_mbar_init();
+    abort_flag = 0;
+  }
+  __syncthreads();
+
+  if (warp == kMmaWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      for (int tile = cta; tile < tiles && !abort_flag; tile += G) {
+        const int row0 = tile * 16;
+        const int rows = min(16, a.n - row0);
+        for (int c = 0; c < chunks; ++c) {
+          const int stage = it % kMmaStages;
+          const uint32_t n = it / kMmaStages;
+          if (n > 0 && !mbar_wait_bounded(&empty_bar[stage], (n - 1) & 1, a.wait_limit)) {
+            atomicOr(a.status, ST_EMPTY_TIMEOUT);
+            abort_flag = 1;
+            break;
+          }
+          const int blk0 = c * kMmaChunkBlocks;
+          const uint32_t seg = static_cast<uint32_t>(min(kMmaChunkBlocks, nb - blk0)) * kBlockBytes;
+          uint8_t* dst = g_mma_ring + static_cast<size_t>(stage) * kMmaStageBytes;
+          mbar_arrive_expect_tx(&full_bar[stage], seg * rows);
+          for (int r = 0; r < rows; ++r)
+            bulk_g2s(dst + r * kMmaRowPitch, a.w + static_cast<size_t>(row0 + r) * row_bytes + blk0 * kBlockBytes, seg,
+                     &full_bar[stage]);
+          ++it;
+        }
+      }
+      const uint32_t issued = it;
+      for (int s = 0; s < kMmaStages && static_cast<uint32_t>(s) < issued; ++s) {
+        const uint32_t last = (issued - 1 - s) / kMmaStages;
+        if (!mbar_wait_bounded(&full_bar[s], last & 1, a.wait_limit)) atomicOr(a.status, ST_DRAIN_TIMEOUT);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ consumers
+    const int g = lane >> 2, t = lane & 3;
+    uint32_t magic;
+    asm volatile("mov.b32 %0, 0x64006400;" : "=r"(magic));
+    uint32_t it = 0;
+    for (int tile = cta; tile < tiles; tile += G) {
+      float acc[NT][4];
+#pragma unroll
+      for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+      for (int c = 0; c < chunks; ++c) {
+        const int stage = it % kMmaStages;
+        const uint32_t n = it / kMmaStages;
+        if (!abort_flag && !mbar_wait_bounded(&full_bar[stage], n & 1, a.wait_limit)) {
+          atomicOr(a.status, ST_FULL_TIMEOUT);
+          abort_flag = 1;
+        }
+        const uint8_t* sb = g_mma_ring + static_cast<size_t>(stage) * kMmaStageBytes;
+        const uint8_t* rg = sb + g * kMmaRowPitch;
+        const uint8_t* rh = sb + (g + 8) * kMmaRowPitch;
+        const int nblk = min(kMmaChunkBlocks, nb - c * kMmaChunkBlocks);
+#pragma unroll
+        for (int i = 0; i < kMmaChunkBlocks / kMmaWarps; ++i) {
+          const int b = warp + kMmaWarps * i;       // block within the chunk (parity = warp parity)
+          if (b < nblk) {
+            const int blk = c * kMmaChunkBlocks + b;
+            uint32_t gl02, gl13, gh02, gh13, hl02, hl13, hh02, hh13;
+            unpack_word(code_word(rg, b, t), magic, gl02, gl13, gh02, gh13);
+            unpack_word(code_word(rh, b, t), magic, hl02, hl13, hh02, hh13);
+            const float dg = row_scale(rg, b), dh = row_scale(rh, b);
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+              uint32_t s0b0, s0b1, s1b0, s1b1;
+              x_frags(a.x, a.k, a.batch, 8 * j + g, blk, t, s0b0, s0b1, s1b0, s1b1);
+              float cb[4] = {0.f, 0.f, 0.f, 0.f};
+              mma16816(cb, gl02, hl02, gl13, hl13, s0b0, s0b1);
+              mma16816(cb, gh02, hh02, gh13, hh13, s1b0, s1b1);
+              acc[j][0] = fmaf(dg, cb[0], acc[j][0]);
+              acc[j][1] = fmaf(dg, cb[1], acc[j][1]);
+              acc[j][2] = fmaf(dh, cb[2], acc[j][2]);
+              acc[j][3] = fmaf(dh, cb[3], acc[j][3]);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[stage]);
+        ++it;
+      }
+      // the 16 warps' partial sums of this row tile, summed in a fixed order
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) red[warp][lane][4 * j + e] = acc[j][e];
+      named_bar_sync(1, kMmaWarps * 32);
+      const int row0 = tile * 16;
+      for (int o = tid; o < 16 * 8 * NT; o += kMmaWarps * 32) {
+        const int m = o % 16, col = o / 16;           // output row in the tile, batch column
+        const int j = col / 8, cc = col % 8;
+        // C fragment: lane (gm, tc) holds rows gm and gm+8, columns 2tc and 2tc+1
+        const int ln = (m % 8) * 4 + cc / 2;
+        const int e = (m >= 8 ? 2 : 0) + (cc & 1);
+        float s = 0.f;
+        for (int w = 0; w < kMmaWarps; ++w) s += red[w][ln][4 * j + e];
+        if (col < a.batch && row0 + m < a.n) a.y[static_cast<size_t>(col) * a.n + row0 + m] = s;
+      }
+      named_bar_sync(1, kMmaWarps * 32);
+    }
+  }
+  __syncthreads();
+}
+
+cudaError_t mma_read_status(int* out) {
+  int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_status_mma, sizeof(int));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_status_mma, &zero, sizeof(int));
+}
+
+cudaError_t mma_prepare() {
+  cudaError_t e = cudaFuncSetAttribute(mma_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kMmaStages * kMmaStageBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(mma_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kMmaStages * kMmaStageBytes);
+}
+
+cudaError_t mma_launch(const uint8_t* w, const uint16_t* x, float* y, int n, int k, int batch, int grid,
+                       uint32_t wait_limit, int* status, cudaStream_t stream) {
+  MmaArgs a;
+  if (!status) {
+    cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_status_mma);
+    if (e != cudaSuccess) return e;
+  }
+  a.status = status;
+  a.w = w;
+  a.x = reinterpret_cast<const __half*>(x);
+  a.y = y;
+  a.n = n;
+  a.k = k;
+  a.batch = batch;
+  a.wait_limit = wait_limit;
+  const int tiles = (n + 15) / 16;
+  if (grid > tiles) grid = tiles;
+  if (batch <= 8)
+    mma_kernel<1><<<grid, kMmaThreads, kMmaStages * kMmaStageBytes, stream>>>(a);
+  else
+    mma_kernel<2><<<grid, kMmaThreads, kMmaStages * kMmaStageBytes, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace q4
