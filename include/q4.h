@@ -85,6 +85,8 @@ size_t q4_matrix_bytes(int n, int k);
 #define Q4_KERNEL_STREAM 1   /* persistent TMA-ring kernel, CUDA-core exact products (batch 1) */
 #define Q4_KERNEL_SIMPLE 2   /* one warp per row, plain loads (any k % 32 == 0, any batch) */
 #define Q4_KERNEL_MMA 3      /* persistent TMA-ring kernel, tensor-core products (batch 1..16) */
+#define Q4_KERNEL_TC 4       /* the decoder's persistent tensor-core engine, one phase (batch 1,
+                                k % 256 == 0, k <= 30720) */
 
 /*
  * y[b][n] = sum_k W[n][k] * x[b][k], W dequantisation-free from its Q4_0 blocks
@@ -176,7 +178,10 @@ int q4_layer_offsets(const q4_layer_shape *shape, size_t offsets[7], size_t *lay
 #define Q4_WS_T2 12       /* fp32 [batch][hidden]: t2 = z1 + Wdown act */
 #define Q4_WS_FLAGS 13    /* u64 [2][256] per-CTA end-of-phase flags (tag, sum of squares), then
                              fp32 [2][256] per-CTA sums of squares of t1 and t2 */
-#define Q4_WS_COUNT 14
+#define Q4_WS_XT 14       /* fp32 [hidden]: t1, then t2, slice-transposed (batch-1 engine input) */
+#define Q4_WS_VT 15       /* fp32 [kv_dim]: v slice-transposed (batch-1 engine input) */
+#define Q4_WS_ACTT 16     /* binary16 [ffn]: act slice-transposed (batch-1 engine input) */
+#define Q4_WS_COUNT 17
 
 /*
  * Byte offsets of the workspace regions for a decoder or a stream ring of
@@ -191,6 +196,8 @@ typedef struct q4_decoder q4_decoder;
 
 #define Q4_DEC_FUSED 0      /* the whole stack is one persistent launch (one graph node) */
 #define Q4_DEC_PER_LAYER 1  /* one launch per layer (one graph node per layer) */
+#define Q4_DEC_TENSOR_CORE 2  /* or-ed into the mode: batch 1 runs the tensor-core engine
+                                 (q4_tc_engine) instead of the exact CUDA-core engine */
 
 /*
  * Create a decoder over n_layers HBM-resident layers and capture its CUDA
@@ -200,7 +207,12 @@ typedef struct q4_decoder q4_decoder;
  *   n_layers       1..1023; batch: 1 <= batch <= 16
  *   workspace      device, >= q4_workspace_layout() bytes, 256-byte aligned;
  *                  owned by the caller, must outlive the decoder
- *   mode           Q4_DEC_FUSED or Q4_DEC_PER_LAYER
+ *   mode           Q4_DEC_FUSED or Q4_DEC_PER_LAYER, optionally | Q4_DEC_TENSOR_CORE.
+ *                  Batch 1 runs one persistent engine (CUDA-core by default:
+ *                  head_dim % 64 == 0 and the widths of Q4_KERNEL_STREAM;
+ *                  tensor-core: head_dim % 4 == 0, hidden, q_dim, ffn multiples
+ *                  of 256 up to 30720); batch 2..16 runs one tensor-core product
+ *                  launch per projection with glue launches between them
  *   stream         used for the workspace initialisation (synchronised)
  * Errors: Q4_ERR_ARG, Q4_ERR_ALIGN, Q4_ERR_OOM (workspace too small), Q4_ERR_CUDA.
  */
@@ -265,6 +277,8 @@ typedef struct q4_stream q4_stream;
 
 #define Q4_STREAM_POISON 1   /* after a layer's compute, overwrite its staging buffer's
                                 scales with NaN before the next copy lands (race check) */
+#define Q4_STREAM_TENSOR_CORE 2 /* batch 1 runs the tensor-core engine instead of the
+                                   exact CUDA-core engine */
 
 /*
  * Create a double-buffered copy/compute ring (PipeLLM, "Layer 2"; PIPO,
@@ -276,7 +290,7 @@ typedef struct q4_stream q4_stream;
  *   n_layers >= 1;  batch 1..16
  *   dev_buf0/1       device, buf_bytes >= one layer block each, 256-byte aligned
  *   workspace        device, >= q4_workspace_layout(shape, n_layers, batch) bytes
- *   flags            0 or Q4_STREAM_POISON
+ *   flags            0, Q4_STREAM_POISON, Q4_STREAM_TENSOR_CORE (or-ed)
  * The handle creates its own copy stream and events.
  * Errors: Q4_ERR_ARG, Q4_ERR_ALIGN, Q4_ERR_OOM, Q4_ERR_CUDA.
  */

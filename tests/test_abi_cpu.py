@@ -86,6 +86,9 @@ def test_argument_checks_launch_nothing(lib):
     assert lib.q4_gemv_ex(A, A, A, 4, 96, 1, q4.Q4_KERNEL_STREAM, None) == q4.Q4_ERR_ARG  # engine needs k % 256
     assert lib.q4_gemv_ex(A, A, A, 4, 256, 2, q4.Q4_KERNEL_STREAM, None) == q4.Q4_ERR_ARG
     assert lib.q4_gemv_ex(A, A, A, 4, 256, 1, 99, None) == q4.Q4_ERR_ARG
+    assert lib.q4_gemv_ex(A, A, A, 4, 96, 1, q4.Q4_KERNEL_TC, None) == q4.Q4_ERR_ARG       # tc needs k % 256
+    assert lib.q4_gemv_ex(A, A, A, 4, 32768, 1, q4.Q4_KERNEL_TC, None) == q4.Q4_ERR_ARG    # x buffer limit
+    assert lib.q4_gemv_ex(A, A, A, 4, 256, 3, q4.Q4_KERNEL_TC, None) == q4.Q4_ERR_ARG      # batch 1 only
     assert lib.q4_dequant_debug(A, None, 4, 64, None) == q4.Q4_ERR_ARG
     assert lib.q4_dequant_debug(A + 1, A, 4, 64, None) == q4.Q4_ERR_ALIGN
 
@@ -105,7 +108,12 @@ def test_decoder_checks(lib):
     odd = q4.LayerShape.of(hidden=96, q_dim=96, kv_dim=96, ffn=96, head_dim=32)      # rows not 16-byte aligned
     assert f(ctypes.byref(h), ctypes.byref(odd), ptrs, 2, 1, 4096, ws_bytes, 0, None) == q4.Q4_ERR_ARG
     wide = q4.LayerShape.of(hidden=256, q_dim=256, kv_dim=128, ffn=768, head_dim=64)  # 768/64 threads: no team split
+    tc = q4.Q4_DEC_FUSED | q4.Q4_DEC_TENSOR_CORE
     assert f(ctypes.byref(h), ctypes.byref(wide), ptrs, 2, 1, 4096, ws_bytes, 0, None) == q4.Q4_ERR_ARG
+    ragged = q4.LayerShape.of(hidden=256, q_dim=256, kv_dim=128, ffn=1056, head_dim=64)  # ffn not 256-aligned
+    assert f(ctypes.byref(h), ctypes.byref(ragged), ptrs, 2, 1, 4096, ws_bytes, tc, None) == q4.Q4_ERR_ARG
+    heads = q4.LayerShape.of(hidden=256, q_dim=256, kv_dim=128, ffn=1024, head_dim=32)  # tc only
+    assert f(ctypes.byref(h), ctypes.byref(heads), ptrs, 2, 1, 4096, ws_bytes, 0, None) == q4.Q4_ERR_ARG
     # streaming ring
     s = ctypes.c_void_p()
     g = lib.q4_stream_create

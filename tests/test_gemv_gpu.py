@@ -11,7 +11,8 @@ from pins import golden_blocks
 
 pytestmark = pytest.mark.gpu
 
-KERNELS = {"stream": q4.Q4_KERNEL_STREAM, "simple": q4.Q4_KERNEL_SIMPLE, "mma": q4.Q4_KERNEL_MMA}
+KERNELS = {"stream": q4.Q4_KERNEL_STREAM, "simple": q4.Q4_KERNEL_SIMPLE, "mma": q4.Q4_KERNEL_MMA,
+           "tc": q4.Q4_KERNEL_TC}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -105,6 +106,32 @@ def test_stream_kernel_parity(n, k):
     assert_within_tol(y, y_ref, s_ref, f"stream {n}x{k}")
 
 
+TC_SHAPES = [(1, 256), (16, 256), (17, 512), (100, 2048), (129, 4096), (300, 4096), (61, 14336), (33, 28672),
+             (1000, 8192), (64, 2304), (5, 30720)]
+
+
+@pytest.mark.parametrize("n,k", TC_SHAPES)
+def test_tc_engine_parity(n, k):
+    w = synth.q4_matrix(n, k, 18, synth.GEMV_TID)
+    x = synth.activations(1, k, 19)
+    y = run(w, x, n, k, 1, q4.Q4_KERNEL_TC)
+    y_ref, s_ref = ora.gemv(w, x, n, k, threads=8)
+    assert_within_tol(y, y_ref, s_ref, f"tc {n}x{k}")
+    assert q4.q4_device_status() == 0
+
+
+def test_tc_engine_rejects_unsupported_widths():
+    x = torch.zeros(32768, dtype=torch.int16, device="cuda")
+    y = torch.zeros(64, dtype=torch.float32, device="cuda")
+    w = torch.zeros(q4.q4_matrix_bytes(4, 32768), dtype=torch.uint8, device="cuda")
+    for k in (96, 288, 32768):
+        with pytest.raises(q4.Q4Error) as e:
+            q4.q4_gemv_ex(w, x, y, 4, k, 1, q4.Q4_KERNEL_TC)
+        assert e.value.status == q4.Q4_ERR_ARG
+    with pytest.raises(q4.Q4Error):
+        q4.q4_gemv_ex(w, x, y, 4, 4096, 2, q4.Q4_KERNEL_TC)
+
+
 MMA_SHAPES = [(1, 256, 1), (16, 256, 2), (17, 512, 3), (100, 2048, 8), (129, 4096, 9), (300, 4096, 16),
               (61, 14336, 4), (33, 28672, 1), (1000, 8192, 7), (64, 2304, 12)]
 
@@ -166,6 +193,14 @@ def test_deterministic_and_auto_is_stream():
     b = run(w, x, n, k, 1, q4.Q4_KERNEL_STREAM)
     c = run(w, x, n, k, 1, q4.Q4_KERNEL_STREAM)
     assert np.array_equal(a, b) and np.array_equal(b, c)
+    d = run(w, x, n, k, 1, q4.Q4_KERNEL_TC)
+    e = run(w, x, n, k, 1, q4.Q4_KERNEL_TC)
+    assert np.array_equal(d, e)
+    # above the persistent engines' widths auto takes the tensor-core product kernel
+    n, k = 8, 32768
+    w = synth.q4_matrix(n, k, 1, synth.GEMV_TID)
+    x = synth.activations(1, k, 1)
+    assert np.array_equal(run(w, x, n, k, 1, q4.Q4_KERNEL_AUTO), run(w, x, n, k, 1, q4.Q4_KERNEL_MMA))
 
 
 def test_large_rows_sampled():

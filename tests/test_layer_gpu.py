@@ -42,9 +42,13 @@ class Stack:
         q4.q4_decoder_destroy(self.dec)
 
 
+ENGINES = {"core": 0, "tc": q4.Q4_DEC_TENSOR_CORE}
+
+
+@pytest.mark.parametrize("engine", list(ENGINES))
 @pytest.mark.parametrize("cfg", [TINY, SMALL, MID], ids=["tiny", "small", "mid"])
-def test_one_layer_step_by_step(cfg):
-    st = Stack(cfg, 1, seed=21)
+def test_one_layer_step_by_step(cfg, engine):
+    st = Stack(cfg, 1, seed=21, mode=q4.Q4_DEC_FUSED | ENGINES[engine])
     h0 = synth.activations(1, cfg["hidden"], 22)
     h1 = st.run(h0)
     check_layer(cfg, 21, 0, read_ws(st.ws, st.offs, cfg), h1, h_in16=h0)
@@ -75,11 +79,12 @@ def test_last_layer_of_a_stack_and_drift():
     st_prev.close()
 
 
-def test_graph_eager_modes_identical():
+@pytest.mark.parametrize("engine", list(ENGINES))
+def test_graph_eager_modes_identical(engine):
     cfg = TINY
     h0 = synth.activations(1, cfg["hidden"], 30)
-    fused = Stack(cfg, 3, seed=31)
-    per = Stack(cfg, 3, seed=31, mode=q4.Q4_DEC_PER_LAYER)
+    fused = Stack(cfg, 3, seed=31, mode=q4.Q4_DEC_FUSED | ENGINES[engine])
+    per = Stack(cfg, 3, seed=31, mode=q4.Q4_DEC_PER_LAYER | ENGINES[engine])
     a = fused.run(h0, graph=True, reps=2)
     b = fused.run(h0, graph=False, reps=2)
     c = per.run(h0, graph=True, reps=2)
@@ -87,6 +92,25 @@ def test_graph_eager_modes_identical():
     assert np.array_equal(a, b) and np.array_equal(a, c) and np.array_equal(a, d)
     fused.close()
     per.close()
+
+
+def test_engines_agree_and_tc_head_dims():
+    """The two batch-1 engines give the same layer within the products' error
+    bound (each is checked against the oracle step by step above); the
+    tensor-core engine also takes head dims that are not multiples of 64."""
+    cfg = SMALL
+    h0 = synth.activations(1, cfg["hidden"], 32)
+    a = Stack(cfg, 2, seed=33, mode=q4.Q4_DEC_TENSOR_CORE).run(h0).view(np.float16).astype(np.float64)
+    b = Stack(cfg, 2, seed=33).run(h0).view(np.float16).astype(np.float64)
+    assert np.linalg.norm(a - b) / np.linalg.norm(b) < 2e-3
+    odd = dict(hidden=768, q_dim=768, kv_dim=192, ffn=2816, head_dim=48)
+    st = Stack(odd, 1, seed=34, mode=q4.Q4_DEC_TENSOR_CORE)
+    h0 = synth.activations(1, odd["hidden"], 35)
+    h1 = st.run(h0)
+    check_layer(odd, 34, 0, read_ws(st.ws, st.offs, odd), h1, h_in16=h0)
+    st.close()
+    with pytest.raises(q4.Q4Error):
+        Stack(odd, 1, seed=34)
 
 
 def test_new_hidden_pointer_rewrites_program():

@@ -31,12 +31,15 @@ Q4_KERNEL_AUTO = 0
 Q4_KERNEL_STREAM = 1
 Q4_KERNEL_SIMPLE = 2
 Q4_KERNEL_MMA = 3
+Q4_KERNEL_TC = 4
 
 Q4_DEC_FUSED = 0
 Q4_DEC_PER_LAYER = 1
+Q4_DEC_TENSOR_CORE = 2
 Q4_STREAM_POISON = 1
+Q4_STREAM_TENSOR_CORE = 2
 
-WS_NAMES = ("control", "program", "qkv", "o", "gate", "up", "down", "act", "x", "attn", "x2", "t1", "t2", "flags")
+WS_NAMES = ("control", "program", "qkv", "o", "gate", "up", "down", "act", "x", "attn", "x2", "t1", "t2", "flags", "xt", "vt", "actt")
 WS_COUNT = len(WS_NAMES)
 
 

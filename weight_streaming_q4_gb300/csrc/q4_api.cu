@@ -6,6 +6,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <stdlib.h>
+
 #include <atomic>
 #include <chrono>
 #include <mutex>
@@ -59,6 +61,7 @@ int device_info(DeviceInfo** out) {
     Q4_CUDA(cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev));
     Q4_CUDA(q4::engine_prepare());
     Q4_CUDA(q4::mma_prepare());
+    Q4_CUDA(q4::tc_engine_prepare());
     Q4_CUDA(q4::engine_occupancy(&d.engine_blocks_per_sm));
     if (d.engine_blocks_per_sm < 1) return Q4_ERR_CUDA;
     d.ready = true;
@@ -77,9 +80,37 @@ bool engine_ok(int k) {
   return team % 32 == 0 || 32 % team == 0;
 }
 
-// Fill the tiling fields of a phase: a work unit gives every team two rows
-// (two rows of one matrix, or the same row of both matrices of a pair).
-bool tile_phase(Phase& ph) {
+// The two persistent engines: exact CUDA-core products (q4_engine.cu) and
+// tensor-core products (q4_tc_engine.cu).
+enum Engine { ENG_CORE = 0, ENG_TC = 1 };
+
+// Whether the tensor-core engine can run rows of width k: whole 8-block
+// groups (row segments start 16-byte aligned) and an input that fits its
+// shared-memory buffer.
+bool tc_ok(int k) { return k >= 256 && k % 256 == 0 && k <= 30720; }
+
+// Bytes of its upcoming weights each tensor-core CTA keeps requested into L2
+// beyond its ring; Q4_PREFETCH_BYTES in the environment overrides it.
+uint32_t tc_prefetch_bytes() {
+  static const uint32_t v = [] {
+    const char* e = getenv("Q4_PREFETCH_BYTES");
+    return e ? static_cast<uint32_t>(strtoul(e, nullptr, 10)) : 196608u;
+  }();
+  return v;
+}
+
+// Fill the tiling fields of a phase.  CUDA-core engine: a work unit gives
+// every team two rows (two rows of one matrix, or the same row of both
+// matrices of a pair).  Tensor-core engine: a unit is one 16-row tile (8 rows
+// of each matrix of a pair).
+bool tile_phase(Phase& ph, int engine = ENG_CORE) {
+  if (engine == ENG_TC) {
+    if (!tc_ok(ph.k)) return false;
+    ph.teams = 0;
+    ph.rows_per_unit = ph.epi_kind == q4::EPI_SILU ? 8 : 16;
+    ph.units = (ph.n_rows + ph.rows_per_unit - 1) / ph.rows_per_unit;
+    return true;
+  }
   if (!engine_ok(ph.k)) return false;
   const int team = ph.k / q4::kKT;
   const int row_bytes = ph.k / q4::kQK * q4::kBlockBytes;
@@ -149,7 +180,9 @@ extern "C" int q4_gemv_ex(const void* w, const uint16_t* x, float* y, int n, int
     Q4_CUDA(q4::mma_launch(static_cast<const uint8_t*>(w), x, y, n, k, batch, dev->sm_count, kWaitLimit, nullptr, s));
     return Q4_OK;
   }
-  if (kernel != Q4_KERNEL_STREAM || batch != 1 || !engine_ok(k)) return Q4_ERR_ARG;
+  if ((kernel != Q4_KERNEL_STREAM && kernel != Q4_KERNEL_TC) || batch != 1) return Q4_ERR_ARG;
+  const int engine = kernel == Q4_KERNEL_TC ? ENG_TC : ENG_CORE;
+  if (!(engine == ENG_TC ? tc_ok(k) : engine_ok(k))) return Q4_ERR_ARG;
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != Q4_OK) return st;
   EngineArgs a;
@@ -163,13 +196,17 @@ extern "C" int q4_gemv_ex(const void* w, const uint16_t* x, float* y, int n, int
   ph.x_kind = q4::X_F16;
   ph.epi_kind = q4::EPI_F32;
   ph.x_ld = k;
-  if (!tile_phase(ph)) return Q4_ERR_ARG;
+  if (!tile_phase(ph, engine)) return Q4_ERR_ARG;
   a.phases = nullptr;
   a.n_phases = 1;
   a.ctl = nullptr;
   a.wait_limit = kWaitLimit;
+  a.prefetch_bytes = engine == ENG_TC ? tc_prefetch_bytes() : 0;
   const int grid = ph.units < dev->sm_count ? ph.units : dev->sm_count;
-  Q4_CUDA(q4::engine_launch(a, grid, false, s));
+  if (engine == ENG_TC)
+    Q4_CUDA(q4::tc_engine_launch(a, grid, false, s));
+  else
+    Q4_CUDA(q4::engine_launch(a, grid, false, s));
   return Q4_OK;
 }
 
@@ -182,7 +219,9 @@ extern "C" int q4_device_status(void) {
   int v = 0, m = 0;
   Q4_CUDA(q4::engine_read_status(&v));
   Q4_CUDA(q4::mma_read_status(&m));
-  return v | m;
+  int tc = 0;
+  Q4_CUDA(q4::tc_engine_read_status(&tc));
+  return v | m | tc;
 }
 
 extern "C" int q4_dequant_debug(const void* w, float* w_out, int n, int k, void* stream) {
@@ -236,6 +275,9 @@ extern "C" int q4_workspace_layout(const q4_layer_shape* s, int n_layers, int ba
       4 * B * s->hidden,
       4 * B * s->hidden,
       8 * 2 * static_cast<size_t>(q4::kMaxGrid) + 4 * 2 * static_cast<size_t>(q4::kMaxGrid),
+      4 * static_cast<size_t>(s->hidden),
+      4 * static_cast<size_t>(s->kv_dim),
+      2 * static_cast<size_t>(s->ffn),
   };
   size_t pos = 0;
   for (int i = 0; i < Q4_WS_COUNT; ++i) {
@@ -256,6 +298,8 @@ struct Work {
   unsigned long long* flags;   // [2][kMaxGrid] end-of-phase flags
   float *ss1, *ss2;            // per-CTA sums of squares of t1 and t2
   uint16_t *act, *x, *attn, *x2;
+  float *xt, *vt;              // slice-transposed t1/t2 and v (CUDA-core engine inputs)
+  uint16_t* actt;              // slice-transposed act
 };
 
 Work carve(void* ws, const size_t* off) {
@@ -277,6 +321,9 @@ Work carve(void* ws, const size_t* off) {
   w.flags = reinterpret_cast<unsigned long long*>(b + off[Q4_WS_FLAGS]);
   w.ss1 = reinterpret_cast<float*>(w.flags + 2 * q4::kMaxGrid);
   w.ss2 = w.ss1 + q4::kMaxGrid;
+  w.xt = reinterpret_cast<float*>(b + off[Q4_WS_XT]);
+  w.vt = reinterpret_cast<float*>(b + off[Q4_WS_VT]);
+  w.actt = reinterpret_cast<uint16_t*>(b + off[Q4_WS_ACTT]);
   return w;
 }
 
@@ -287,7 +334,8 @@ Work carve(void* ws, const size_t* off) {
 // in w.x and is the residual base of the attention half, whose fp32 sum goes
 // to w.t1; the normalised w.t1 (w.x2) is the residual base of the feed-forward
 // half, whose fp32 sum goes to w.t2.
-bool layer_phases(const q4_layer_shape& s, const uint8_t* wl, const uint16_t* in16, const Work& w, Phase out[4]) {
+bool layer_phases(const q4_layer_shape& s, const uint8_t* wl, const uint16_t* in16, const Work& w, Phase out[4],
+                  int engine) {
   size_t off[7];
   if (q4_layer_offsets(&s, off, nullptr) != Q4_OK) return false;
   memset(out, 0, 4 * sizeof(Phase));
@@ -350,14 +398,41 @@ bool layer_phases(const q4_layer_shape& s, const uint8_t* wl, const uint16_t* in
   d.x_kind = q4::X_F16;
   d.epi_kind = q4::EPI_RESID;
   d.x_ld = s.ffn;
+  if (engine == ENG_CORE) {
+    // each phase also leaves the next phase's input slice-transposed, so that
+    // the consumer threads' x-slice loads are coalesced
+    if (!in16) {
+      a.x_src = w.xt;
+      a.x_t = 1;
+      a.x_ld = s.hidden / q4::kKT;
+    }
+    a.yt = w.vt;
+    a.yt_off = s.q_dim + s.kv_dim;
+    a.yt_n = s.kv_dim;
+    b.x_src = w.vt;
+    b.x_t = 1;
+    b.x_ld = s.kv_dim / q4::kKT;
+    b.yt = w.xt;
+    b.yt_n = s.hidden;
+    c.x_src = w.xt;
+    c.x_t = 1;
+    c.x_ld = s.hidden / q4::kKT;
+    c.yt = w.actt;
+    c.yt_n = s.ffn;
+    d.x_src = w.actt;
+    d.x_t = 1;
+    d.x_ld = s.ffn / q4::kKT;
+    d.yt = w.xt;
+    d.yt_n = s.hidden;
+  }
   for (int i = 0; i < 4; ++i)
-    if (!tile_phase(out[i])) return false;
+    if (!tile_phase(out[i], engine)) return false;
   return true;
 }
 
 // The closing phase of a stack: no product, CTA 0 writes the normalised last
 // residual sum to the caller's hidden-state buffer.
-bool final_phase(const q4_layer_shape& s, uint16_t* h_out, const Work& w, Phase* out) {
+bool final_phase(const q4_layer_shape& s, uint16_t* h_out, const Work& w, Phase* out, int engine) {
   memset(out, 0, sizeof(Phase));
   out->x_src = w.t2;
   out->ss_in = w.ss2;
@@ -368,25 +443,34 @@ bool final_phase(const q4_layer_shape& s, uint16_t* h_out, const Work& w, Phase*
   out->x_ld = s.hidden;
   out->eps = s.eps;
   out->x_dbg = h_out;
-  return tile_phase(*out);
+  if (engine == ENG_CORE) {
+    out->x_src = w.xt;
+    out->x_t = 1;
+    out->x_ld = s.hidden / q4::kKT;
+  }
+  return tile_phase(*out, engine);
 }
 
 // Phase program of a whole stack: 4 phases per layer and the closing phase.
 bool stack_program(const q4_layer_shape& s, const std::vector<const uint8_t*>& layers, uint16_t* h,
-                   const Work& w, std::vector<Phase>& prog) {
+                   const Work& w, std::vector<Phase>& prog, int engine) {
   const int L = static_cast<int>(layers.size());
   prog.assign(4 * static_cast<size_t>(L) + 1, Phase());
   for (int l = 0; l < L; ++l)
-    if (!layer_phases(s, layers[l], l == 0 ? h : nullptr, w, &prog[4 * l])) return false;
-  return final_phase(s, h, w, &prog[4 * L]);
+    if (!layer_phases(s, layers[l], l == 0 ? h : nullptr, w, &prog[4 * l], engine)) return false;
+  return final_phase(s, h, w, &prog[4 * L], engine);
 }
 
-int check_layer_shape_for_engine(const q4_layer_shape& s) {
-  if (s.head_dim % q4::kKT) return Q4_ERR_ARG;   // a thread's 64 attention columns stay in one head
+int check_layer_shape_for_engine(const q4_layer_shape& s, int engine) {
+  // CUDA-core engine: a thread's 64 attention columns stay in one head;
+  // tensor-core engine: runs of 4 columns do
+  if (s.head_dim % (engine == ENG_TC ? 4 : q4::kKT)) return Q4_ERR_ARG;
   Phase tmp[5];
   Work w;
   memset(&w, 0, sizeof(w));
-  return layer_phases(s, nullptr, nullptr, w, tmp) && final_phase(s, nullptr, w, &tmp[4]) ? Q4_OK : Q4_ERR_ARG;
+  return layer_phases(s, nullptr, nullptr, w, tmp, engine) && final_phase(s, nullptr, w, &tmp[4], engine)
+             ? Q4_OK
+             : Q4_ERR_ARG;
 }
 
 // One layer for a batch of more than one row: the tensor-core product for each
@@ -419,7 +503,7 @@ bool batched_shape_ok(const q4_layer_shape& s) {
   return s.hidden % 256 == 0 && s.q_dim % 256 == 0 && s.ffn % 256 == 0 && (s.q_dim + 2 * s.kv_dim) > 0;
 }
 
-int launch_layers(const Work& w, int first_phase, int n_phases, int grid, cudaStream_t s) {
+int launch_layers(const Work& w, int first_phase, int n_phases, int grid, cudaStream_t s, int engine) {
   EngineArgs a;
   memset(&a, 0, sizeof(a));
   a.phases = w.prog + first_phase;
@@ -427,7 +511,12 @@ int launch_layers(const Work& w, int first_phase, int n_phases, int grid, cudaSt
   a.ctl = w.ctl;
   a.flags = w.flags;
   a.wait_limit = kWaitLimit;
-  Q4_CUDA(q4::engine_launch(a, grid, true, s));
+  if (engine == ENG_TC) {
+    a.prefetch_bytes = tc_prefetch_bytes();
+    Q4_CUDA(q4::tc_engine_launch(a, grid, true, s));
+  } else {
+    Q4_CUDA(q4::engine_launch(a, grid, true, s));
+  }
   return Q4_OK;
 }
 
@@ -445,7 +534,7 @@ int read_status(Control* ctl, cudaStream_t s, int* out) {
 
 struct q4_decoder {
   q4_layer_shape shape;
-  int n_layers = 0, batch = 1, mode = Q4_DEC_FUSED, grid = 0;
+  int n_layers = 0, batch = 1, mode = Q4_DEC_FUSED, grid = 0, engine = ENG_CORE;
   std::vector<const uint8_t*> layers;
   Work w;
   uint16_t* cur_h = nullptr;
@@ -465,7 +554,7 @@ static int decoder_write_program(q4_decoder* d, uint16_t* h, cudaStream_t s) {
     return Q4_OK;
   }
   std::vector<Phase> prog;
-  if (!stack_program(d->shape, d->layers, h, d->w, prog)) return Q4_ERR_ARG;
+  if (!stack_program(d->shape, d->layers, h, d->w, prog, d->engine)) return Q4_ERR_ARG;
   // pageable source: the runtime stages it before returning, so `prog` may go
   Q4_CUDA(cudaMemcpyAsync(d->w.prog, prog.data(), prog.size() * sizeof(Phase), cudaMemcpyHostToDevice, s));
   d->cur_h = h;
@@ -481,9 +570,9 @@ static int decoder_enqueue(q4_decoder* d, cudaStream_t s) {
     }
     return Q4_OK;
   }
-  if (d->mode == Q4_DEC_FUSED) return launch_layers(d->w, 0, 4 * L + 1, d->grid, s);
+  if (d->mode == Q4_DEC_FUSED) return launch_layers(d->w, 0, 4 * L + 1, d->grid, s, d->engine);
   for (int l = 0; l < L; ++l) {   // the last launch also runs the closing phase
-    int st = launch_layers(d->w, 4 * l, l == L - 1 ? 5 : 4, d->grid, s);
+    int st = launch_layers(d->w, 4 * l, l == L - 1 ? 5 : 4, d->grid, s, d->engine);
     if (st != Q4_OK) return st;
   }
   return Q4_OK;
@@ -495,9 +584,12 @@ extern "C" int q4_decoder_create(q4_decoder** out, const q4_layer_shape* shape, 
   if (!out || !shape_ok(shape) || !layer_weights || n_layers < 1 || !workspace) return Q4_ERR_ARG;
   if (batch < 1 || batch > q4::kMaxBatch) return Q4_ERR_ARG;
   if (4 * n_layers + 1 > static_cast<int>(q4::kPhasesPerEpoch)) return Q4_ERR_ARG;
-  if (mode != Q4_DEC_FUSED && mode != Q4_DEC_PER_LAYER) return Q4_ERR_ARG;
-  // batch 1: the persistent exact CUDA-core engine; larger batches: tensor-core products + glue
-  if (batch == 1 ? check_layer_shape_for_engine(*shape) != Q4_OK : !batched_shape_ok(*shape)) return Q4_ERR_ARG;
+  if ((mode & ~Q4_DEC_TENSOR_CORE) != Q4_DEC_FUSED && (mode & ~Q4_DEC_TENSOR_CORE) != Q4_DEC_PER_LAYER)
+    return Q4_ERR_ARG;
+  const int engine = (mode & Q4_DEC_TENSOR_CORE) ? ENG_TC : ENG_CORE;
+  // batch 1: a persistent engine; larger batches: tensor-core products + glue
+  if (batch == 1 ? check_layer_shape_for_engine(*shape, engine) != Q4_OK : !batched_shape_ok(*shape))
+    return Q4_ERR_ARG;
   if (!aligned(workspace, 256)) return Q4_ERR_ALIGN;
   for (int l = 0; l < n_layers; ++l) {
     if (!layer_weights[l]) return Q4_ERR_ARG;
@@ -515,7 +607,8 @@ extern "C" int q4_decoder_create(q4_decoder** out, const q4_layer_shape* shape, 
   d->shape = *shape;
   d->n_layers = n_layers;
   d->batch = batch;
-  d->mode = mode;
+  d->mode = mode & ~Q4_DEC_TENSOR_CORE;
+  d->engine = engine;
   d->grid = dev->sm_count < q4::kMaxGrid ? dev->sm_count : q4::kMaxGrid;   // one CTA per SM, co-resident
   d->layers.assign(reinterpret_cast<const uint8_t* const*>(layer_weights),
                    reinterpret_cast<const uint8_t* const*>(layer_weights) + n_layers);
@@ -588,7 +681,7 @@ int run_stack_in_workspace(const q4_layer_shape* shape, const void* const* layer
                            uint16_t* hidden_io, void* ws, size_t ws_bytes, cudaStream_t s) {
   if (!shape_ok(shape) || !layer_weights || n_layers < 1 || !hidden_io || !ws) return Q4_ERR_ARG;
   if (4 * n_layers + 1 > static_cast<int>(kPhasesPerEpoch)) return Q4_ERR_ARG;
-  if (check_layer_shape_for_engine(*shape) != Q4_OK) return Q4_ERR_ARG;
+  if (check_layer_shape_for_engine(*shape, ENG_CORE) != Q4_OK) return Q4_ERR_ARG;
   if (!aligned(hidden_io, 16)) return Q4_ERR_ALIGN;
   for (int l = 0; l < n_layers; ++l) {
     if (!layer_weights[l]) return Q4_ERR_ARG;
@@ -604,13 +697,13 @@ int run_stack_in_workspace(const q4_layer_shape* shape, const void* const* layer
   std::vector<const uint8_t*> layers(reinterpret_cast<const uint8_t* const*>(layer_weights),
                                      reinterpret_cast<const uint8_t* const*>(layer_weights) + n_layers);
   std::vector<Phase> prog;
-  if (!stack_program(*shape, layers, hidden_io, w, prog)) return Q4_ERR_ARG;
+  if (!stack_program(*shape, layers, hidden_io, w, prog, ENG_CORE)) return Q4_ERR_ARG;
   Q4_CUDA(cudaMemcpyAsync(w.prog, prog.data(), prog.size() * sizeof(Phase), cudaMemcpyHostToDevice, s));
   // control block and phase flags start from zero (earlier calls left their tags)
   Q4_CUDA(cudaMemsetAsync(w.ctl, 0, sizeof(Control), s));
   Q4_CUDA(cudaMemsetAsync(w.flags, 0, 2 * kMaxGrid * sizeof(unsigned long long), s));
   const int grid = dev->sm_count < kMaxGrid ? dev->sm_count : kMaxGrid;
-  return launch_layers(w, 0, static_cast<int>(prog.size()), grid, s);
+  return launch_layers(w, 0, static_cast<int>(prog.size()), grid, s, ENG_CORE);
 }
 
 }  // namespace q4
@@ -632,7 +725,7 @@ extern "C" int q4_decoder_destroy(q4_decoder* d) {
 
 struct q4_stream {
   q4_layer_shape shape;
-  int n_layers = 0, batch = 1, flags = 0, grid = 0;
+  int n_layers = 0, batch = 1, flags = 0, grid = 0, engine = ENG_CORE;
   std::vector<const void*> host;
   uint8_t* buf[2] = {nullptr, nullptr};
   size_t layer_bytes = 0;
@@ -648,9 +741,11 @@ extern "C" int q4_stream_create(q4_stream** out, const q4_layer_shape* shape, co
                                 void* workspace, size_t workspace_bytes, int flags) {
   if (!out || !shape_ok(shape) || !host_layers || n_layers < 1 || !dev_buf0 || !dev_buf1 || !workspace)
     return Q4_ERR_ARG;
-  if (batch < 1 || batch > q4::kMaxBatch || (flags & ~Q4_STREAM_POISON)) return Q4_ERR_ARG;
+  if (batch < 1 || batch > q4::kMaxBatch || (flags & ~(Q4_STREAM_POISON | Q4_STREAM_TENSOR_CORE))) return Q4_ERR_ARG;
   if (4 * n_layers + 1 > static_cast<int>(q4::kPhasesPerEpoch)) return Q4_ERR_ARG;
-  if (batch == 1 ? check_layer_shape_for_engine(*shape) != Q4_OK : !batched_shape_ok(*shape)) return Q4_ERR_ARG;
+  const int engine = (flags & Q4_STREAM_TENSOR_CORE) ? ENG_TC : ENG_CORE;
+  if (batch == 1 ? check_layer_shape_for_engine(*shape, engine) != Q4_OK : !batched_shape_ok(*shape))
+    return Q4_ERR_ARG;
   if (!aligned(dev_buf0, 256) || !aligned(dev_buf1, 256) || !aligned(workspace, 256)) return Q4_ERR_ALIGN;
   size_t lo[7], layer_bytes = 0;
   q4_layer_offsets(shape, lo, &layer_bytes);
@@ -671,6 +766,7 @@ extern "C" int q4_stream_create(q4_stream** out, const q4_layer_shape* shape, co
   r->n_layers = n_layers;
   r->batch = batch;
   r->flags = flags;
+  r->engine = engine;
   r->grid = dev->sm_count < q4::kMaxGrid ? dev->sm_count : q4::kMaxGrid;
   r->host.assign(host_layers, host_layers + n_layers);
   r->buf[0] = static_cast<uint8_t*>(dev_buf0);
@@ -702,7 +798,7 @@ extern "C" int q4_stream_layers(q4_stream* r, uint16_t* hidden_io, void* compute
     std::vector<const uint8_t*> bufs(r->n_layers);
     for (int i = 0; i < r->n_layers; ++i) bufs[i] = r->buf[i & 1];
     std::vector<Phase> prog;
-    if (!stack_program(r->shape, bufs, hidden_io, r->w, prog)) return Q4_ERR_ARG;
+    if (!stack_program(r->shape, bufs, hidden_io, r->w, prog, r->engine)) return Q4_ERR_ARG;
     Q4_CUDA(cudaMemcpyAsync(r->w.prog, prog.data(), prog.size() * sizeof(Phase), cudaMemcpyHostToDevice, cs));
     r->cur_h = hidden_io;
   }
@@ -721,7 +817,7 @@ extern "C" int q4_stream_layers(q4_stream* r, uint16_t* hidden_io, void* compute
     // compute stream: layer i once its weights have landed
     Q4_CUDA(cudaStreamWaitEvent(cs, r->loaded[b], 0));
     int st = r->batch == 1
-                 ? launch_layers(r->w, 4 * i, i == r->n_layers - 1 ? 5 : 4, r->grid, cs)
+                 ? launch_layers(r->w, 4 * i, i == r->n_layers - 1 ? 5 : 4, r->grid, cs, r->engine)
                  : launch_layer_batched(r->shape, r->buf[b], i, r->n_layers, hidden_io, r->w, r->batch, r->grid, cs);
     if (st != Q4_OK) return st;
     if (r->flags & Q4_STREAM_POISON) Q4_CUDA(q4::poison_launch(r->buf[b], n_blocks, cs));

@@ -54,7 +54,8 @@ struct Phase {
   int k;
   int x_kind;
   int epi_kind;
-  int x_ld;               // row stride (elements) of x_src per batch row
+  int x_ld;               // row stride (elements) of x_src per batch row; with x_t, the
+                          // chunk stride T of the transposed layout
   int attn_off;           // X_ATTN: element offset of v inside a row of x_src
   int head_dim;           // X_ATTN
   int group;              // X_ATTN: query heads per value head
@@ -62,8 +63,20 @@ struct Phase {
   int teams;              // row teams of k/64 threads working side by side
   int units;              // work units in this phase
   int rows_per_unit;      // rows of each matrix per unit
-  int pad_;
+  int x_t;                // 1: x_src is slice-transposed (see below), stride x_ld chunks
+  // Slice-transposed copy written by the epilogue for the next phase's input
+  // (CUDA-core engine): rows [yt_off, yt_off + yt_n) of the output (y for
+  // EPI_F32, y2 for EPI_RESID, the SiLU product for EPI_SILU).  Element e of
+  // that range sits where consumer thread e / 64 reads it with coalesced
+  // 16-byte loads: fp32 at ((e % 64) / 4 * T + e / 64) * 4 + e % 4, binary16 at
+  // ((e % 64) / 8 * T + e / 64) * 8 + e % 8, with T = yt_n / 64.
+  void* yt;
+  int yt_off;
+  int yt_n;
 };
+
+__host__ __device__ __forceinline__ int slice_t32(int e, int T) { return ((e & 63) >> 2) * T * 4 + (e >> 6) * 4 + (e & 3); }
+__host__ __device__ __forceinline__ int slice_t16(int e, int T) { return ((e & 63) >> 3) * T * 8 + (e >> 6) * 8 + (e & 7); }
 
 // Per-launch control block in device memory (decoder workspace).
 struct Control {
@@ -85,6 +98,8 @@ struct EngineArgs {
   Control* ctl;            // required when n_phases > 1
   unsigned long long* flags;  // [2][kMaxGrid] end-of-phase flags, required when n_phases > 1
   uint32_t wait_limit;     // polls of one wait before it is declared failed
+  uint32_t prefetch_bytes; // tensor-core engine: weight bytes a CTA keeps requested into L2
+                           // beyond its shared-memory ring (0 = none)
   Phase one;
 };
 
@@ -150,6 +165,12 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// Ask for `bytes` at src to be brought into L2 (no completion tracking).
+// src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
@@ -191,6 +212,9 @@ cudaError_t simple_launch(const uint8_t* w, const uint16_t* x, float* y, int n, 
                           cudaStream_t stream);
 cudaError_t dequant_launch(const uint8_t* w, float* out, int n, int k, cudaStream_t stream);
 cudaError_t poison_launch(uint8_t* buf, size_t n_blocks, cudaStream_t stream);
+cudaError_t tc_engine_prepare();
+cudaError_t tc_engine_launch(const EngineArgs& a, int grid, bool cooperative, cudaStream_t stream);
+cudaError_t tc_engine_read_status(int* out);
 cudaError_t mma_prepare();
 cudaError_t mma_launch(const uint8_t* w, const uint16_t* x, float* y, int n, int k, int batch, int grid,
                        uint32_t wait_limit, int* status, cudaStream_t stream);

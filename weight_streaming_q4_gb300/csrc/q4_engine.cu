@@ -33,6 +33,7 @@
 #include <stdint.h>
 
 #include "q4_device.cuh"
+#include "q4_phase.cuh"
 
 namespace q4 {
 
@@ -151,10 +152,14 @@ __device__ __forceinline__ void set_status(Control* ctl, int bits) {
 // a multiple of 64), so they map to 64 consecutive values of one value head.
 __device__ __forceinline__ void load_x_slice(const Phase& ph, int c0, float* v) {
   if (ph.x_kind == X_F16 || ph.x_kind == X_NORM16) {
-    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __half*>(ph.x_src) + c0);
+    // natural layout: the thread's 128 bytes; slice-transposed: chunk i of
+    // slice j at (i * T + j) * 16 bytes, so a warp's loads are contiguous
+    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __half*>(ph.x_src) + (ph.x_t ? 0 : c0));
+    const int step = ph.x_t ? ph.x_ld : 1;
+    if (ph.x_t) p += c0 / kKT;
 #pragma unroll
     for (int i = 0; i < kKT / 8; ++i) {
-      const uint4 u = p[i];
+      const uint4 u = p[i * step];
       const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
@@ -167,86 +172,20 @@ __device__ __forceinline__ void load_x_slice(const Phase& ph, int c0, float* v) 
     int src0 = c0;
     if (ph.x_kind == X_ATTN) {
       const int hd = ph.head_dim;
-      src0 = ph.attn_off + ((c0 / hd) / ph.group) * hd + (c0 % hd);
+      src0 = (ph.x_t ? 0 : ph.attn_off) + ((c0 / hd) / ph.group) * hd + (c0 % hd);
     }
-    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(ph.x_src) + src0);
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(ph.x_src)) +
+                      (ph.x_t ? src0 / kKT : src0 / 4);
+    const int step = ph.x_t ? ph.x_ld : 1;
 #pragma unroll
     for (int i = 0; i < kKT / 4; ++i) {
-      const float4 f = p[i];
+      const float4 f = p[i * step];
       v[4 * i] = f.x;
       v[4 * i + 1] = f.y;
       v[4 * i + 2] = f.z;
       v[4 * i + 3] = f.w;
     }
   }
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-// Wait until every CTA has published phase `tag`'s flag (or a later one)
-// and return the sum of the sums of squares they carry, in a fixed order
-// (the same in every CTA).  One warp per CTA polls; after the flags are
-// seen, a fence orders later loads after the producers' writes.  Gives up
-// after `limit` polls (status bit set).
-__device__ float wait_phase_flags(const unsigned long long* flags, unsigned tag, int lane, uint32_t limit,
-                                  Control* ctl) {
-  const int G = static_cast<int>(gridDim.x);
-  float part[kMaxGrid / 32];
-  bool ok = false;
-  for (uint32_t it = 0; it < limit; ++it) {
-    bool mine = true;
-#pragma unroll
-    for (int i = 0; i < kMaxGrid / 32; ++i) {
-      part[i] = 0.f;
-      if (lane + 32 * i < G) {
-        const unsigned long long f = ld_relaxed_u64(flags + lane + 32 * i);
-        mine &= static_cast<int>(static_cast<unsigned>(f >> 32) - tag) >= 0;
-        part[i] = __uint_as_float(static_cast<unsigned>(f));
-      }
-    }
-    if (__all_sync(0xffffffffu, mine)) {
-      ok = true;
-      break;
-    }
-    if (it > 16) __nanosleep(64);
-  }
-  if (!ok && lane == 0) atomicOr(&ctl->status, ST_FLAG_TIMEOUT);
-  __threadfence();
-  float ss = 0.f;
-#pragma unroll
-  for (int i = 0; i < kMaxGrid / 32; ++i) ss += part[i];
-  return warp_sum(ss);
-}
-
-// Sum of a per-CTA sums-of-squares array written by an earlier launch.
-__device__ float sum_ss_array(const float* ss, int lane) {
-  const int G = static_cast<int>(gridDim.x);
-  float part = 0.f;
-#pragma unroll
-  for (int i = 0; i < kMaxGrid / 32; ++i)
-    if (lane + 32 * i < G) part += __ldcg(ss + lane + 32 * i);
-  return warp_sum(part);
-}
-
-// Sum of squares of a binary16 input vector (every warp on its own).
-__device__ float input_sumsq16(const Phase& ph, int lane) {
-  float ss = 0.f;
-  const uint4* p = reinterpret_cast<const uint4*>(ph.x_src);
-  for (int i = lane; i < ph.k / 8; i += 32) {
-    const uint4 u = __ldcg(p + i);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[t]));
-      ss = fmaf(f.x, f.x, ss);
-      ss = fmaf(f.y, f.y, ss);
-    }
-  }
-  return warp_sum(ss);
 }
 
 // Form the thread's slice of x for a phase: xs2 receives 32 float2 in the
@@ -288,7 +227,6 @@ __device__ void form_x(const Phase& ph, int j, int lane, u64* xs2, bool write_db
   }
 }
 
-__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
 // Geometry of a phase as the consumers see it.
 struct Tile {
@@ -344,12 +282,16 @@ __device__ float flush_rows(const Phase& ph, const Tile& t, const float* red, in
       const int n = (u_first + i * G) * t.rpu + rem;   // rem = 2 * team + row of the team
       if (n < ph.n_rows) {
         ph.y[n] = v;
+        float out = v;
         if (ph.epi_kind == EPI_RESID) {
           const unsigned short rv = c < kPre ? res[c < kPre ? c : 0] : ph.res[n];
           const float tv = __half2float(__ushort_as_half(rv)) + v;
           ph.y2[n] = tv;
           ss = fmaf(tv, tv, ss);
+          out = tv;
         }
+        const int e = n - ph.yt_off;
+        if (ph.yt && e >= 0 && e < ph.yt_n) static_cast<float*>(ph.yt)[slice_t32(e, ph.yt_n / kKT)] = out;
       }
     }
   } else {
@@ -365,7 +307,9 @@ __device__ float flush_rows(const Phase& ph, const Tile& t, const float* red, in
       if (n < ph.n_rows) {
         ph.y[n] = g;
         ph.y2[n] = u;
-        ph.aux16[n] = __half_as_ushort(__float2half_rn(silu_mul(g, u)));
+        const unsigned short a16 = __half_as_ushort(__float2half_rn(silu_mul(g, u)));
+        ph.aux16[n] = a16;
+        if (ph.yt) static_cast<unsigned short*>(ph.yt)[slice_t16(n, ph.yt_n / kKT)] = a16;
       }
     }
   }
