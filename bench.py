@@ -261,6 +261,11 @@ def run_gemv(args, torch, q4, model, synth, stream, barrier, gpu_index):
 
 
 def run_stream(args, torch, q4, model, synth, stream, barrier, gpu_index):
+    """70B-shaped stack through the copy/compute ring.  --resident-frac keeps
+    that fraction of the layers (a prefix) resident in HBM; --chunked copies
+    each streamed layer as four chunks with one event each.  --config
+    stream-sweep times resident fractions 0, 1/4, 1/2, 3/4 with merged and
+    chunked copies and reports them all."""
     cfg, n_layers = stack_cfg("70b")
     shape = q4.LayerShape.of(**cfg)
     layer_bytes = q4.q4_layer_offsets(shape)[1]
@@ -276,8 +281,8 @@ def run_stream(args, torch, q4, model, synth, stream, barrier, gpu_index):
     bufs = [torch.empty(stride, dtype=torch.uint8, device="cuda") for _ in range(2)]
     B = args.batch
     ws, offs, ws_bytes = model.workspace(shape, n_layers, B)
-    ring = q4.q4_stream_create(shape, hptrs, B, bufs[0], bufs[1], stride, ws, ws_bytes, 0)
-    h = torch.from_numpy(synth.activations(B, cfg["hidden"], 0).reshape(-1).view("int16").copy()).cuda()
+    h0 = torch.from_numpy(synth.activations(B, cfg["hidden"], 0).reshape(-1).view("int16").copy())
+    h = h0.cuda()
     # pinned host -> HBM copy peak, same transfer size as the ring
     cs = torch.cuda.Stream()
     best = 0.0
@@ -291,24 +296,73 @@ def run_stream(args, torch, q4, model, synth, stream, barrier, gpu_index):
         torch.cuda.synchronize()
         best = max(best, 4 * stride / (ev0.elapsed_time(ev1) / 1e3) / 1e9)
 
-    def step():
-        q4.q4_stream_layers(ring, h, stream=stream)
-
-    steps = min(args.steps, 20)
+    sweep = args.config == "stream-sweep"
+    fracs = [0.0, 0.25, 0.5, 0.75] if sweep else [args.resident_frac]
+    max_res = int(round(max(fracs) * n_layers))
+    dev_w, dptrs = (model.resident_layers(shape, max_res, seed=0) if max_res else (None, []))
+    steps = min(args.steps, 20 if not sweep else 6)
     warm = min(args.warmup, 3)
-    secs, clocks = time_region(torch, stream, step, steps, warm, barrier, gpu_index)
-    if q4.q4_stream_status(ring, stream=stream) != 0:
-        raise RuntimeError("stream ring kernels reported a failed wait")
-    q4.q4_stream_destroy(ring)
-    return dict(secs=secs, clocks=clocks, bytes_per_step=layer_bytes * n_layers,
-                launches_per_step=n_layers if B == 1 else 9 * n_layers + 1,
-                kernel_launches_per_step=n_layers if B == 1 else 5 * n_layers,
-                steps_override=steps, warmup_override=warm, h2d_peak_gbs=best,
-                e2e_secs=None, workload=(f"70B-shaped stack, {n_layers} layers streamed from pinned host memory "
-                                         f"({distinct} distinct layer blocks), two HBM layer buffers, batch {B}"),
-                kernel="engine_kernel" if B == 1 else "mma_kernel",
-                kernel_key="engine_kernel:70b_stream" if B == 1 else f"mma_kernel:70b_stream_b{B}", cfg=cfg,
-                distinct=distinct)
+    runs = []
+    for frac in fracs:
+        R = int(round(frac * n_layers))
+        for chunked in ([False, True] if sweep else [args.chunked]):
+            host = [0 if i < R else hptrs[i] for i in range(n_layers)]
+            res = [dptrs[i] if i < R else 0 for i in range(n_layers)]
+            flags = q4.Q4_STREAM_CHUNKED if chunked else 0
+            ring = q4.q4_stream_create_ex(shape, host, res, B, bufs[0], bufs[1], stride, ws, ws_bytes, flags)
+
+            def step():
+                q4.q4_stream_layers(ring, h, stream=stream)
+
+            secs, clocks = time_region(torch, stream, step, steps, warm, barrier, gpu_index)
+            if q4.q4_stream_status(ring, stream=stream) != 0:
+                raise RuntimeError("stream ring kernels reported a failed wait")
+            t = secs / steps
+            runs.append(dict(resident_layers=R, chunked=chunked, secs=secs, clocks=clocks,
+                             ms_per_token=round(t * 1e3, 3), tokens_per_s=round(B / t, 3),
+                             weight_gbs=round(layer_bytes * n_layers / t / 1e9, 2),
+                             host_link_gbs=round(layer_bytes * (n_layers - R) / t / 1e9, 2),
+                             host_link_frac=round(layer_bytes * (n_layers - R) / t / 1e9 / best, 4)))
+            last_ring = ring
+            if not (frac == fracs[-1] and chunked == (True if sweep else args.chunked)):
+                q4.q4_stream_destroy(ring)
+    head = runs[0]
+    # end to end through the public call: the step's input copied in from pinned
+    # host memory and its result read back, every step
+    hin = h0.pin_memory()
+    hout = torch.empty_like(hin).pin_memory()
+    e2e_steps = max(3, min(steps, 6))
+    with torch.cuda.stream(stream):
+        h.copy_(hin, non_blocking=True)
+        q4.q4_stream_layers(last_ring, h, stream=stream)
+        stream.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(e2e_steps):
+            h.copy_(hin, non_blocking=True)
+            q4.q4_stream_layers(last_ring, h, stream=stream)
+            hout.copy_(h, non_blocking=True)
+            stream.synchronize()
+    e2e_secs = time.perf_counter() - t0
+    q4.q4_stream_destroy(last_ring)
+    R = runs[-1]["resident_layers"]
+    desc = (f"70B-shaped stack, {n_layers} layers, {n_layers - head['resident_layers']} streamed from pinned host "
+            f"memory ({distinct} distinct layer blocks) through two HBM layer buffers"
+            f"{', ' + str(head['resident_layers']) + ' resident' if head['resident_layers'] else ''}, "
+            f"{'chunked' if head['chunked'] else 'merged'} copies, batch {B}")
+    out = dict(secs=head["secs"], clocks=head["clocks"], bytes_per_step=layer_bytes * n_layers,
+               streamed_bytes_per_step=layer_bytes * (n_layers - head["resident_layers"]),
+               launches_per_step=n_layers if B == 1 else 9 * n_layers + 1,
+               kernel_launches_per_step=n_layers if B == 1 else 5 * n_layers,
+               steps_override=steps, warmup_override=warm, h2d_peak_gbs=best,
+               e2e_secs=e2e_secs, e2e_steps=e2e_steps, h2d=h0.numel() * 2, d2h=h0.numel() * 2,
+               e2e_note=f"measured on the last configuration run ({R} resident layers)",
+               workload=desc, kernel="engine_kernel" if B == 1 else "mma_kernel",
+               kernel_key=None, cfg=cfg, distinct=distinct)
+    if sweep:
+        out["residency_sweep"] = [{k: v for k, v in r.items() if k not in ("secs", "clocks")} for r in runs]
+    return out
 
 
 def run_sweep(args, torch, q4, model, synth, stream, barrier, gpu_index):
@@ -414,7 +468,10 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--config", default="8b", choices=["8b", "gemv", "70b", "70b-stream", "sweep"])
+    ap.add_argument("--config", default="8b", choices=["8b", "gemv", "70b", "70b-stream", "stream-sweep", "sweep"])
+    ap.add_argument("--resident-frac", type=float, default=0.0,
+                    help="70b-stream: fraction of the layers (a prefix) kept resident in HBM")
+    ap.add_argument("--chunked", action="store_true", help="70b-stream: copy each layer as four chunks")
     ap.add_argument("--batch", type=int, default=1, help="activation rows per step (1..16)")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0)
@@ -439,10 +496,11 @@ def main():
     else:
         barrier = lambda: None
     stream = torch.cuda.Stream()
-    if not 1 <= args.batch <= 16 or (args.batch != 1 and args.config not in ("8b", "70b", "70b-stream")):
-        raise SystemExit("--batch: 1..16, for the 8b, 70b and 70b-stream configs")
+    if not 1 <= args.batch <= 16 or (args.batch != 1 and args.config not in ("8b", "70b", "70b-stream",
+                                                                               "stream-sweep")):
+        raise SystemExit("--batch: 1..16, for the 8b, 70b and stream configs")
     runner = {"8b": run_stack, "70b": run_stack, "gemv": run_gemv, "70b-stream": run_stream,
-              "sweep": run_sweep}[args.config]
+              "stream-sweep": run_stream, "sweep": run_sweep}[args.config]
     r = runner(args, torch, q4, model, synth, stream, barrier, local_rank)
     steps = r.get("steps_override", args.steps)
     warmup = r.get("warmup_override", args.warmup)
@@ -486,12 +544,16 @@ def main():
         out["tokens_per_s"] = round(world * args.batch / per_step, 2)
         out["config"]["n_layers"] = r["n_layers"]
         out["config"]["weight_bytes_per_token"] = r["bytes_per_step"]
-    if args.config == "70b-stream":
+    if args.config in ("70b-stream", "stream-sweep"):
         out["tokens_per_s"] = round(world * args.batch / per_step, 3)
-        out["host_link"] = {"achieved_gbs": round(r["bytes_per_step"] / per_step / 1e9, 2),
+        sb = r["streamed_bytes_per_step"]
+        out["host_link"] = {"achieved_gbs": round(sb / per_step / 1e9, 2),
                             "pinned_h2d_peak_gbs": round(r["h2d_peak_gbs"], 2),
-                            "frac": round(r["bytes_per_step"] / per_step / 1e9 / r["h2d_peak_gbs"], 4)}
+                            "frac": round(sb / per_step / 1e9 / r["h2d_peak_gbs"], 4) if sb else None,
+                            "streamed_bytes_per_token": sb}
         out["config"]["distinct_host_layers"] = r["distinct"]
+        if "residency_sweep" in r:
+            out["residency_sweep"] = r["residency_sweep"]
     achieved = bytes_per_launch / per_launch_s / 1e9
     out["roofline"] = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                        "frac": round(achieved / peak, 4), "peak_source": f"hbm_gbs {peak_kind}",
@@ -507,6 +569,8 @@ def main():
         out["e2e"] = {"value": round(e2e_bytes / (r["e2e_secs"] / r["e2e_steps"]) / 1e9, 2), "unit": "GB/s",
                       "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
                       "ms_per_step": round(r["e2e_secs"] / r["e2e_steps"] * 1e3, 4)}
+        if r.get("e2e_note"):
+            out["e2e"]["note"] = r["e2e_note"]
     out["gpu_launches"] = r["launches_per_step"] * steps
     out["clocks"] = r["clocks"]
     # the CPU oracle on a bounded sample of the same workload (rank 0 only)

@@ -279,6 +279,10 @@ typedef struct q4_stream q4_stream;
                                 scales with NaN before the next copy lands (race check) */
 #define Q4_STREAM_TENSOR_CORE 2 /* batch 1 runs the tensor-core engine instead of the
                                    exact CUDA-core engine */
+#define Q4_STREAM_CHUNKED 4   /* copy each streamed layer as four chunks (q|k|v, o, gate|up,
+                                 down), one event each; each of the layer's products starts as
+                                 soon as its own chunk has landed (PIPO, "Data transfer suite":
+                                 blockwise transfer) instead of after the whole block */
 
 /*
  * Create a double-buffered copy/compute ring (PipeLLM, "Layer 2"; PIPO,
@@ -290,13 +294,28 @@ typedef struct q4_stream q4_stream;
  *   n_layers >= 1;  batch 1..16
  *   dev_buf0/1       device, buf_bytes >= one layer block each, 256-byte aligned
  *   workspace        device, >= q4_workspace_layout(shape, n_layers, batch) bytes
- *   flags            0, Q4_STREAM_POISON, Q4_STREAM_TENSOR_CORE (or-ed)
+ *   flags            0, or Q4_STREAM_POISON | Q4_STREAM_TENSOR_CORE | Q4_STREAM_CHUNKED
  * The handle creates its own copy stream and events.
  * Errors: Q4_ERR_ARG, Q4_ERR_ALIGN, Q4_ERR_OOM, Q4_ERR_CUDA.
  */
 int q4_stream_create(q4_stream **out, const q4_layer_shape *shape, const void *const *host_layers,
                      int n_layers, int batch, void *dev_buf0, void *dev_buf1, size_t buf_bytes,
                      void *workspace, size_t workspace_bytes, int flags);
+
+/*
+ * q4_stream_create with partial residency (PIPO, "Two pipeline modes" and its
+ * Experiments, where part of a model stays in GPU memory and the rest is
+ * offloaded): resident_layers is null or holds n_layers device pointers;
+ * entry i non-null = layer i's merged block is resident in HBM at that address
+ * (256-byte aligned, caller-owned, read only) and is never copied, and
+ * host_layers[i] may then be null.  The streamed layers alternate between the
+ * two staging buffers in their own order; copies of the first streamed layers
+ * overlap the compute of the resident layers before them.
+ * Errors: as q4_stream_create.
+ */
+int q4_stream_create_ex(q4_stream **out, const q4_layer_shape *shape, const void *const *host_layers,
+                        const void *const *resident_layers, int n_layers, int batch, void *dev_buf0,
+                        void *dev_buf1, size_t buf_bytes, void *workspace, size_t workspace_bytes, int flags);
 
 /*
  * Run all layers once on hidden_io (device, binary16 [batch][hidden]) while

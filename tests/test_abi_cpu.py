@@ -121,5 +121,14 @@ def test_decoder_checks(lib):
     assert g(ctypes.byref(s), ctypes.byref(shape), ptrs, 2, 1, 4096, 8192, lb - 1, 4096, ws_bytes, 0) == q4.Q4_ERR_OOM
     assert g(ctypes.byref(s), ctypes.byref(shape), ptrs, 2, 1, 4096, 8192 + 16, lb, 4096, ws_bytes, 0) == q4.Q4_ERR_ALIGN
     assert g(ctypes.byref(s), ctypes.byref(shape), ptrs, 2, 1, 4096, 8192, lb, 4096, ws_bytes, 8) == q4.Q4_ERR_ARG
+    # partial residency: a layer needs a host block or a resident block; resident blocks 256-byte aligned
+    gx = lib.q4_stream_create_ex
+    none = (ctypes.c_void_p * 2)(None, None)
+    res_bad = (ctypes.c_void_p * 2)(4096 + 16, None)
+    assert gx(ctypes.byref(s), ctypes.byref(shape), none, None, 2, 1, 4096, 8192, lb, 4096, ws_bytes, 0) == q4.Q4_ERR_ARG
+    assert gx(ctypes.byref(s), ctypes.byref(shape), ptrs, res_bad, 2, 1, 4096, 8192, lb, 4096, ws_bytes,
+              0) == q4.Q4_ERR_ALIGN
+    assert gx(ctypes.byref(s), ctypes.byref(shape), none, (ctypes.c_void_p * 2)(4096, None), 2, 1, 4096, 8192, lb,
+              4096, ws_bytes, 0) == q4.Q4_ERR_ARG
     assert lib.q4_stream_layers(None, 4096, None, 0) == q4.Q4_ERR_ARG
     assert lib.q4_layer_decode(None, 4096, None) == q4.Q4_ERR_ARG

@@ -87,3 +87,92 @@ def test_host_timeout_returns_and_work_completes():
     torch.cuda.synchronize()                     # the queued work still finishes
     assert q4.q4_stream_status(ring.h) == 0
     ring.close()
+
+
+def _mixed_ring(cfg, n_layers, seed, resident_mask, flags, batch=1):
+    """A ring where layer i is resident (device block) when resident_mask[i], else streamed."""
+    shape = q4.LayerShape.of(**cfg)
+    blocks, hptrs = model.host_layers(shape, n_layers, seed)
+    wbuf, dptrs = model.resident_layers(shape, n_layers, seed)
+    stride = model.layer_stride(shape)
+    bufs = [torch.empty(stride, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    ws, offs, nb = model.workspace(shape, n_layers, batch)
+    host = [0 if m else hptrs[i] for i, m in enumerate(resident_mask)]
+    res = [dptrs[i] if m else 0 for i, m in enumerate(resident_mask)]
+    h = q4.q4_stream_create_ex(shape, host, res, batch, bufs[0], bufs[1], stride, ws, nb, flags)
+    return h, (blocks, wbuf, bufs, ws)
+
+
+@pytest.mark.parametrize("flags", [q4.Q4_STREAM_CHUNKED, q4.Q4_STREAM_CHUNKED | q4.Q4_STREAM_POISON,
+                                   q4.Q4_STREAM_CHUNKED | q4.Q4_STREAM_TENSOR_CORE],
+                         ids=["chunked", "chunked-poison", "chunked-tc"])
+def test_chunked_copies_equal_resident(flags):
+    cfg, L = SMALL, 4
+    h0 = synth.activations(1, cfg["hidden"], 80)
+    ring = Ring(cfg, L, seed=81, flags=flags)
+    got = ring.run(h0, tokens=2)
+    ref = resident(cfg, L, 81, h0, tokens=2, tc=bool(flags & q4.Q4_STREAM_TENSOR_CORE))
+    assert np.array_equal(got, ref)
+    ring.close()
+
+
+@pytest.mark.parametrize("mask", [(1, 1, 0, 0, 0), (0, 1, 0, 1, 0), (1, 1, 1, 1, 1), (0, 0, 0, 0, 1)],
+                         ids=["prefix", "alternate", "all", "last"])
+@pytest.mark.parametrize("flags", [0, q4.Q4_STREAM_CHUNKED | q4.Q4_STREAM_POISON], ids=["merged", "chunked"])
+def test_partial_residency_equals_resident(mask, flags):
+    cfg, L = SMALL, 5
+    h0 = synth.activations(1, cfg["hidden"], 82)
+    st, keep = _mixed_ring(cfg, L, 83, mask, flags)
+    h = dev_u16(h0.reshape(-1))
+    for _ in range(2):
+        q4.q4_stream_layers(st, h)
+    torch.cuda.synchronize()
+    assert q4.q4_stream_status(st) == 0
+    got = host_u16(h).reshape(1, -1)
+    q4.q4_stream_destroy(st)
+    assert np.array_equal(got, resident(cfg, L, 83, h0, tokens=2))
+
+
+def test_partial_residency_batch8_chunked():
+    cfg, L, B = SMALL, 4, 8
+    h0 = synth.activations(B, cfg["hidden"], 84)
+    st, keep = _mixed_ring(cfg, L, 85, (1, 0, 0, 1), q4.Q4_STREAM_CHUNKED | q4.Q4_STREAM_POISON, batch=B)
+    h = dev_u16(h0.reshape(-1))
+    for _ in range(2):
+        q4.q4_stream_layers(st, h)
+    torch.cuda.synchronize()
+    assert q4.q4_stream_status(st) == 0
+    got = host_u16(h).reshape(B, -1)
+    q4.q4_stream_destroy(st)
+    shape = q4.LayerShape.of(**cfg)
+    wbuf, ptrs = model.resident_layers(shape, L, 85)
+    ws, offs, nb = model.workspace(shape, L, B)
+    dec = q4.q4_decoder_create(shape, ptrs, B, ws, nb)
+    hr = dev_u16(h0.reshape(-1))
+    for _ in range(2):
+        q4.q4_layer_decode(dec, hr)
+    torch.cuda.synchronize()
+    q4.q4_decoder_destroy(dec)
+    assert np.array_equal(got, host_u16(hr).reshape(B, -1))
+
+
+@pytest.mark.parametrize("cfg", [SMALL, dict(hidden=1024, q_dim=1024, kv_dim=256, ffn=14336, head_dim=128)],
+                         ids=["small", "wide"])
+def test_fused_per_layer_and_per_phase_schedules_identical(cfg):
+    # one launch for the stack, one per layer, one per phase (chunked ring): same rows on the same CTAs
+    h0 = synth.activations(1, cfg["hidden"], 86)
+    shape = q4.LayerShape.of(**cfg)
+    wbuf, ptrs = model.resident_layers(shape, 3, 87)
+    outs = []
+    for mode in (q4.Q4_DEC_FUSED, q4.Q4_DEC_PER_LAYER):
+        ws, offs, nb = model.workspace(shape, 3, 1)
+        dec = q4.q4_decoder_create(shape, ptrs, 1, ws, nb, mode)
+        h = dev_u16(h0.reshape(-1))
+        q4.q4_layer_decode(dec, h)
+        torch.cuda.synchronize()
+        q4.q4_decoder_destroy(dec)
+        outs.append(host_u16(h).reshape(1, -1))
+    ring = Ring(cfg, 3, seed=87, flags=q4.Q4_STREAM_CHUNKED)
+    outs.append(ring.run(h0))
+    ring.close()
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])

@@ -38,6 +38,7 @@ Q4_DEC_PER_LAYER = 1
 Q4_DEC_TENSOR_CORE = 2
 Q4_STREAM_POISON = 1
 Q4_STREAM_TENSOR_CORE = 2
+Q4_STREAM_CHUNKED = 4
 
 WS_NAMES = ("control", "program", "qkv", "o", "gate", "up", "down", "act", "x", "attn", "x2", "t1", "t2", "flags", "xt", "vt", "actt")
 WS_COUNT = len(WS_NAMES)
@@ -86,6 +87,8 @@ def _declare(lib):
         "q4_noalloc_scratch_bytes": ([], c_size),
         "q4_stream_create": ([ctypes.POINTER(c_p), ctypes.POINTER(LayerShape), ctypes.POINTER(c_p), c_int, c_int,
                               c_p, c_p, c_size, c_p, c_size, c_int], c_int),
+        "q4_stream_create_ex": ([ctypes.POINTER(c_p), ctypes.POINTER(LayerShape), ctypes.POINTER(c_p),
+                                 ctypes.POINTER(c_p), c_int, c_int, c_p, c_p, c_size, c_p, c_size, c_int], c_int),
         "q4_stream_layers": ([c_p, c_p, c_p, c_i64], c_int),
         "q4_stream_status": ([c_p, c_p, ctypes.POINTER(c_int)], c_int),
         "q4_stream_destroy": ([c_p], c_int),
@@ -232,6 +235,19 @@ def q4_stream_create(shape: LayerShape, host_ptrs, batch: int, buf0, buf1, buf_b
     _check(lib().q4_stream_create(ctypes.byref(h), ctypes.byref(shape), arr, len(host_ptrs), batch, _ptr(buf0),
                                   _ptr(buf1), buf_bytes, _ptr(workspace), workspace_bytes, flags),
            "q4_stream_create")
+    return h
+
+
+def q4_stream_create_ex(shape: LayerShape, host_ptrs, resident_ptrs, batch: int, buf0, buf1, buf_bytes: int,
+                        workspace, workspace_bytes: int, flags: int = 0):
+    """host_ptrs[i] / resident_ptrs[i]: pinned host block or device block of layer i (0 = none)."""
+    h = c_p()
+    n = len(host_ptrs)
+    harr = (c_p * n)(*[int(p) if p else None for p in host_ptrs])
+    rarr = None if resident_ptrs is None else (c_p * n)(*[int(p) if p else None for p in resident_ptrs])
+    _check(lib().q4_stream_create_ex(ctypes.byref(h), ctypes.byref(shape), harr, rarr, n, batch, _ptr(buf0),
+                                     _ptr(buf1), buf_bytes, _ptr(workspace), workspace_bytes, flags),
+           "q4_stream_create_ex")
     return h
 
 

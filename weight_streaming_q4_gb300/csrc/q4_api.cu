@@ -117,6 +117,8 @@ bool tile_phase(Phase& ph, int engine = ENG_CORE) {
   int teams = q4::kConsumerThreads / team;
   const int fit = q4::kStageBytes / (2 * row_bytes);
   if (teams > fit) teams = fit;
+  // teams narrower than a warp fill whole warps (their shuffles span the warp)
+  if (team < 32) teams -= teams % (32 / team);
   if (teams < 1) return false;
   ph.teams = teams;
   ph.rows_per_unit = ph.epi_kind == q4::EPI_SILU ? teams : 2 * teams;
@@ -458,7 +460,15 @@ bool stack_program(const q4_layer_shape& s, const std::vector<const uint8_t*>& l
   prog.assign(4 * static_cast<size_t>(L) + 1, Phase());
   for (int l = 0; l < L; ++l)
     if (!layer_phases(s, layers[l], l == 0 ? h : nullptr, w, &prog[4 * l], engine)) return false;
-  return final_phase(s, h, w, &prog[4 * L], engine);
+  if (!final_phase(s, h, w, &prog[4 * L], engine)) return false;
+  // unit rotation over the whole program, so that any split into launches
+  // (fused, per layer, per phase) gives every CTA the same rows
+  int base = 0;
+  for (Phase& ph : prog) {
+    ph.base = base;
+    base += ph.units;
+  }
+  return true;
 }
 
 int check_layer_shape_for_engine(const q4_layer_shape& s, int engine) {
@@ -479,20 +489,26 @@ int check_layer_shape_for_engine(const q4_layer_shape& s, int engine) {
 // state (first layer) or the previous layer's z in w.x; `out` receives the
 // normalised output of the last layer.
 int launch_layer_batched(const q4_layer_shape& sh, const uint8_t* wl, int layer, int n_layers, uint16_t* h,
-                         const Work& w, int batch, int grid, cudaStream_t s) {
+                         const Work& w, int batch, int grid, cudaStream_t s, const cudaEvent_t* chunk = nullptr) {
   size_t off[7];
   if (q4_layer_offsets(&sh, off, nullptr) != Q4_OK) return Q4_ERR_ARG;
   const int H = sh.hidden, Q = sh.q_dim, KV = sh.kv_dim, F = sh.ffn;
   const int nqkv = Q + 2 * KV;
   const int group = (Q / sh.head_dim) / (KV / sh.head_dim);
+  // chunk c of the layer block (q|k|v, o, gate|up, down) must have landed before its product
+  auto wait = [&](int c) { return chunk ? cudaStreamWaitEvent(s, chunk[c], 0) : cudaSuccess; };
   if (layer == 0) Q4_CUDA(q4::glue_norm(h, nullptr, batch, H, sh.eps, w.x, s));
+  Q4_CUDA(wait(0));
   Q4_CUDA(q4::mma_launch(wl + off[Q4_PROJ_Q], w.x, w.qkv, nqkv, H, batch, grid, kWaitLimit, &w.ctl->status, s));
   Q4_CUDA(q4::glue_attn(w.qkv, batch, nqkv, Q, Q + KV, sh.head_dim, group, w.attn, s));
+  Q4_CUDA(wait(1));
   Q4_CUDA(q4::mma_launch(wl + off[Q4_PROJ_O], w.attn, w.o, H, Q, batch, grid, kWaitLimit, &w.ctl->status, s));
   Q4_CUDA(q4::glue_resid_norm(w.x, w.o, batch, H, sh.eps, w.t1, w.x2, s));
+  Q4_CUDA(wait(2));
   Q4_CUDA(q4::mma_launch(wl + off[Q4_PROJ_GATE], w.x2, w.g, F, H, batch, grid, kWaitLimit, &w.ctl->status, s));
   Q4_CUDA(q4::mma_launch(wl + off[Q4_PROJ_UP], w.x2, w.u, F, H, batch, grid, kWaitLimit, &w.ctl->status, s));
   Q4_CUDA(q4::glue_silu(w.g, w.u, static_cast<size_t>(batch) * F, w.act, s));
+  Q4_CUDA(wait(3));
   Q4_CUDA(q4::mma_launch(wl + off[Q4_PROJ_DOWN], w.act, w.dn, H, F, batch, grid, kWaitLimit, &w.ctl->status, s));
   // the next layer's z goes to w.x; the last layer's to the caller's buffer
   Q4_CUDA(q4::glue_resid_norm(w.x2, w.dn, batch, H, sh.eps, w.t2, layer + 1 == n_layers ? h : w.x, s));
@@ -727,21 +743,34 @@ struct q4_stream {
   q4_layer_shape shape;
   int n_layers = 0, batch = 1, flags = 0, grid = 0, engine = ENG_CORE;
   std::vector<const void*> host;
+  std::vector<const uint8_t*> resident;   // per layer: device block, or null if streamed
+  std::vector<int> slot;                  // per layer: staging buffer (0/1), or -1 if resident
   uint8_t* buf[2] = {nullptr, nullptr};
   size_t layer_bytes = 0;
+  size_t chunk_off[5] = {0, 0, 0, 0, 0};  // q|k|v, o, gate|up, down, end
   Work w;
   uint16_t* cur_h = nullptr;
   cudaStream_t copy = nullptr;
-  cudaEvent_t loaded[2] = {nullptr, nullptr}, freed[2] = {nullptr, nullptr};
+  cudaEvent_t loaded[2][4] = {}, freed[2] = {nullptr, nullptr};
   cudaEvent_t start = nullptr, done = nullptr;
 };
 
 extern "C" int q4_stream_create(q4_stream** out, const q4_layer_shape* shape, const void* const* host_layers,
                                 int n_layers, int batch, void* dev_buf0, void* dev_buf1, size_t buf_bytes,
                                 void* workspace, size_t workspace_bytes, int flags) {
+  return q4_stream_create_ex(out, shape, host_layers, nullptr, n_layers, batch, dev_buf0, dev_buf1, buf_bytes,
+                             workspace, workspace_bytes, flags);
+}
+
+extern "C" int q4_stream_create_ex(q4_stream** out, const q4_layer_shape* shape, const void* const* host_layers,
+                                   const void* const* resident_layers, int n_layers, int batch, void* dev_buf0,
+                                   void* dev_buf1, size_t buf_bytes, void* workspace, size_t workspace_bytes,
+                                   int flags) {
   if (!out || !shape_ok(shape) || !host_layers || n_layers < 1 || !dev_buf0 || !dev_buf1 || !workspace)
     return Q4_ERR_ARG;
-  if (batch < 1 || batch > q4::kMaxBatch || (flags & ~(Q4_STREAM_POISON | Q4_STREAM_TENSOR_CORE))) return Q4_ERR_ARG;
+  if (batch < 1 || batch > q4::kMaxBatch ||
+      (flags & ~(Q4_STREAM_POISON | Q4_STREAM_TENSOR_CORE | Q4_STREAM_CHUNKED)))
+    return Q4_ERR_ARG;
   if (4 * n_layers + 1 > static_cast<int>(q4::kPhasesPerEpoch)) return Q4_ERR_ARG;
   const int engine = (flags & Q4_STREAM_TENSOR_CORE) ? ENG_TC : ENG_CORE;
   if (batch == 1 ? check_layer_shape_for_engine(*shape, engine) != Q4_OK : !batched_shape_ok(*shape))
@@ -751,8 +780,13 @@ extern "C" int q4_stream_create(q4_stream** out, const q4_layer_shape* shape, co
   q4_layer_offsets(shape, lo, &layer_bytes);
   if (buf_bytes < layer_bytes) return Q4_ERR_OOM;
   for (int l = 0; l < n_layers; ++l) {
-    if (!host_layers[l]) return Q4_ERR_ARG;
-    if (!aligned(host_layers[l], 16)) return Q4_ERR_ALIGN;
+    const void* res = resident_layers ? resident_layers[l] : nullptr;
+    if (res) {
+      if (!aligned(res, 256)) return Q4_ERR_ALIGN;
+    } else {
+      if (!host_layers[l]) return Q4_ERR_ARG;
+      if (!aligned(host_layers[l], 16)) return Q4_ERR_ALIGN;
+    }
   }
   size_t off[Q4_WS_COUNT], need = 0;
   int st = q4_workspace_layout(shape, n_layers, batch, off, &need);
@@ -762,6 +796,20 @@ extern "C" int q4_stream_create(q4_stream** out, const q4_layer_shape* shape, co
   if ((st = device_info(&dev)) != Q4_OK) return st;
 
   q4_stream* r = new q4_stream();
+  r->resident.assign(n_layers, nullptr);
+  r->slot.assign(n_layers, -1);
+  for (int l = 0, si = 0; l < n_layers; ++l) {
+    const void* res = resident_layers ? resident_layers[l] : nullptr;
+    if (res)
+      r->resident[l] = static_cast<const uint8_t*>(res);
+    else
+      r->slot[l] = (si++) & 1;   // streamed layers alternate between the two buffers
+  }
+  r->chunk_off[0] = 0;
+  r->chunk_off[1] = lo[Q4_PROJ_O];
+  r->chunk_off[2] = lo[Q4_PROJ_GATE];
+  r->chunk_off[3] = lo[Q4_PROJ_DOWN];
+  r->chunk_off[4] = layer_bytes;
   r->shape = *shape;
   r->n_layers = n_layers;
   r->batch = batch;
@@ -775,7 +823,7 @@ extern "C" int q4_stream_create(q4_stream** out, const q4_layer_shape* shape, co
   r->w = carve(workspace, off);
   cudaError_t e = cudaStreamCreateWithFlags(&r->copy, cudaStreamNonBlocking);
   for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
-    e = cudaEventCreateWithFlags(&r->loaded[i], cudaEventDisableTiming);
+    for (int c = 0; c < 4 && e == cudaSuccess; ++c) e = cudaEventCreateWithFlags(&r->loaded[i][c], cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&r->freed[i], cudaEventDisableTiming);
   }
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&r->start, cudaEventDisableTiming);
@@ -796,7 +844,7 @@ extern "C" int q4_stream_layers(q4_stream* r, uint16_t* hidden_io, void* compute
   if (hidden_io != r->cur_h && r->batch == 1) {
     // layer i computes on staging buffer i % 2
     std::vector<const uint8_t*> bufs(r->n_layers);
-    for (int i = 0; i < r->n_layers; ++i) bufs[i] = r->buf[i & 1];
+    for (int i = 0; i < r->n_layers; ++i) bufs[i] = r->resident[i] ? r->resident[i] : r->buf[r->slot[i]];
     std::vector<Phase> prog;
     if (!stack_program(r->shape, bufs, hidden_io, r->w, prog, r->engine)) return Q4_ERR_ARG;
     Q4_CUDA(cudaMemcpyAsync(r->w.prog, prog.data(), prog.size() * sizeof(Phase), cudaMemcpyHostToDevice, cs));
@@ -808,20 +856,46 @@ extern "C" int q4_stream_layers(q4_stream* r, uint16_t* hidden_io, void* compute
   Q4_CUDA(cudaEventRecord(r->start, cs));
   Q4_CUDA(cudaStreamWaitEvent(r->copy, r->start, 0));
   const size_t n_blocks = r->layer_bytes / q4::kBlockBytes;
+  const bool chunked = (r->flags & Q4_STREAM_CHUNKED) != 0;
+  const int n_chunks = chunked ? 4 : 1;
+  int streamed = 0;   // streamed layers enqueued so far in this call
   for (int i = 0; i < r->n_layers; ++i) {
-    const int b = i & 1;
-    // copy stream: layer i into buffer b once layer i-2 has released it
-    if (i >= 2) Q4_CUDA(cudaStreamWaitEvent(r->copy, r->freed[b], 0));
-    Q4_CUDA(cudaMemcpyAsync(r->buf[b], r->host[i], r->layer_bytes, cudaMemcpyHostToDevice, r->copy));
-    Q4_CUDA(cudaEventRecord(r->loaded[b], r->copy));
-    // compute stream: layer i once its weights have landed
-    Q4_CUDA(cudaStreamWaitEvent(cs, r->loaded[b], 0));
-    int st = r->batch == 1
-                 ? launch_layers(r->w, 4 * i, i == r->n_layers - 1 ? 5 : 4, r->grid, cs, r->engine)
-                 : launch_layer_batched(r->shape, r->buf[b], i, r->n_layers, hidden_io, r->w, r->batch, r->grid, cs);
+    const int b = r->slot[i];
+    const uint8_t* wl = b < 0 ? r->resident[i] : r->buf[b];
+    if (b >= 0) {
+      // copy stream: layer i into buffer b once the streamed layer two before it has released it
+      if (streamed >= 2) Q4_CUDA(cudaStreamWaitEvent(r->copy, r->freed[b], 0));
+      for (int c = 0; c < n_chunks; ++c) {
+        const size_t lo = chunked ? r->chunk_off[c] : 0, hi = chunked ? r->chunk_off[c + 1] : r->layer_bytes;
+        Q4_CUDA(cudaMemcpyAsync(r->buf[b] + lo, static_cast<const uint8_t*>(r->host[i]) + lo, hi - lo,
+                                cudaMemcpyHostToDevice, r->copy));
+        Q4_CUDA(cudaEventRecord(r->loaded[b][c], r->copy));
+      }
+      ++streamed;
+    }
+    const bool last = i == r->n_layers - 1;
+    int st = Q4_OK;
+    if (r->batch > 1) {
+      // batched: each projection waits for its own chunk (or the whole block)
+      cudaEvent_t ev[4];
+      for (int c = 0; c < 4; ++c) ev[c] = r->loaded[b < 0 ? 0 : b][chunked ? c : 0];
+      st = launch_layer_batched(r->shape, wl, i, r->n_layers, hidden_io, r->w, r->batch, r->grid, cs,
+                                b < 0 ? nullptr : ev);
+    } else if (b < 0 || !chunked) {
+      if (b >= 0) Q4_CUDA(cudaStreamWaitEvent(cs, r->loaded[b][0], 0));
+      st = launch_layers(r->w, 4 * i, last ? 5 : 4, r->grid, cs, r->engine);
+    } else {
+      // chunked: phase p of the layer starts once chunk p has landed (one launch per phase)
+      for (int p = 0; p < 4 && st == Q4_OK; ++p) {
+        Q4_CUDA(cudaStreamWaitEvent(cs, r->loaded[b][p], 0));
+        st = launch_layers(r->w, 4 * i + p, (last && p == 3) ? 2 : 1, r->grid, cs, r->engine);
+      }
+    }
     if (st != Q4_OK) return st;
-    if (r->flags & Q4_STREAM_POISON) Q4_CUDA(q4::poison_launch(r->buf[b], n_blocks, cs));
-    Q4_CUDA(cudaEventRecord(r->freed[b], cs));
+    if (b >= 0) {
+      if (r->flags & Q4_STREAM_POISON) Q4_CUDA(q4::poison_launch(r->buf[b], n_blocks, cs));
+      Q4_CUDA(cudaEventRecord(r->freed[b], cs));
+    }
   }
   // the next call's copies wait on `start`, which follows this call's compute
   if (timeout_us > 0) {
@@ -848,7 +922,8 @@ extern "C" int q4_stream_destroy(q4_stream* r) {
   if (!r) return Q4_OK;
   if (r->copy) cudaStreamSynchronize(r->copy);
   for (int i = 0; i < 2; ++i) {
-    if (r->loaded[i]) cudaEventDestroy(r->loaded[i]);
+    for (int c = 0; c < 4; ++c)
+      if (r->loaded[i][c]) cudaEventDestroy(r->loaded[i][c]);
     if (r->freed[i]) cudaEventDestroy(r->freed[i]);
   }
   if (r->start) cudaEventDestroy(r->start);

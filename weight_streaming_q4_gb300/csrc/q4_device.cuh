@@ -73,6 +73,11 @@ struct Phase {
   void* yt;
   int yt_off;
   int yt_n;
+  // Units of all earlier phases of the whole program: unit u of this phase
+  // goes to CTA (base + u) mod G, the same in a fused, per-layer or
+  // per-phase launch, so every schedule gives bit-identical results.
+  int base;
+  int pad_;
 };
 
 __host__ __device__ __forceinline__ int slice_t32(int e, int T) { return ((e & 63) >> 2) * T * 4 + (e >> 6) * 4 + (e & 3); }

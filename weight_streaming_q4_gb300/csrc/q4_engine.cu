@@ -344,12 +344,11 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t it = 0;
-      int base = 0;   // (global index of the phase's first unit) mod G
       for (int p = 0; p < a.n_phases && !abort_flag; ++p) {
         const Phase& ph = a.phases ? a.phases[p] : a.one;
         const uint32_t row_bytes = static_cast<uint32_t>(ph.k / kQK) * kBlockBytes;
         const bool dual = ph.epi_kind == EPI_SILU;
-        const int u0 = (cta - base + G) % G;
+        const int u0 = (cta - ph.base % G + G) % G;
         for (int u = u0; u < ph.units; u += G) {
           const int stage = it % kStages;
           const uint32_t n = it / kStages;
@@ -370,7 +369,6 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
                      ph.w1 + static_cast<size_t>(row0) * row_bytes, bytes, &full_bar[stage]);
           ++it;
         }
-        base = (base + ph.units) % G;
       }
       // Drain: no copy may still be in flight when the CTA exits.
       const uint32_t issued = it;
@@ -384,13 +382,12 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
     u64 xs2[kKT / 2];
     const Unpack kk = make_unpack();
     uint32_t it = 0;
-    int base = 0;
     const unsigned tag0 = a.n_phases > 1 ? a.ctl->epoch * kPhasesPerEpoch + 1u : 0u;   // tag of phase 0
     for (int p = 0; p < a.n_phases; ++p) {
       const Phase& ph = a.phases ? a.phases[p] : a.one;
       const Tile t = tile_of(ph, tid);
       const int units = ph.units, n_rows = ph.n_rows;
-      const int u0 = (cta - base + G) % G;
+      const int u0 = (cta - ph.base % G + G) % G;
       if (u0 < units || (ph.x_dbg && cta == 0)) {
         float sumsq = 0.f;
         if (p > 0) {
@@ -449,15 +446,17 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
         if (lane == 0) mbar_arrive(&empty_bar[stage]);
         ++it;
         if (t.active) {
+          // both rows' sums over the width-lane group in one tree: the first
+          // exchange leaves row 0 partials in the lower half-group and row 1
+          // partials in the upper one, the remaining steps reduce each half
           const int width = t.team_threads < 32 ? t.team_threads : 32;
-          for (int o = width >> 1; o > 0; o >>= 1) {
-            t0 += __shfl_xor_sync(0xffffffffu, t0, o);
-            t1 += __shfl_xor_sync(0xffffffffu, t1, o);
-          }
-          if ((t.team_threads >= 32 && lane == 0) || (t.team_threads < 32 && t.j == 0)) {
-            const int slot = n_buf * t.spu + 2 * t.team;
-            red[slot * t.tw + t.w_in_team] = t0;
-            red[(slot + 1) * t.tw + t.w_in_team] = t1;
+          const int half = width >> 1;
+          const bool upper = (lane & half) != 0;
+          float r = (upper ? t1 : t0) + __shfl_xor_sync(0xffffffffu, upper ? t0 : t1, half);
+          for (int o = half >> 1; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+          if (((lane & (width - 1)) & ~half) == 0) {   // lane 0 (row 0) and lane `half` (row 1) of the group
+            const int slot = n_buf * t.spu + 2 * t.team + (upper ? 1 : 0);
+            red[slot * t.tw + t.w_in_team] = r;
           }
         }
         ++n_buf;
@@ -482,7 +481,6 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
         }
         named_bar_sync(1, kConsumerThreads);   // red_cta is read again at the next phase start
       }
-      base = (base + units) % G;
     }
   }
 

@@ -67,18 +67,19 @@ __device__ __forceinline__ const Phase& phase_at(const EngineArgs& a, int p) {
 }
 
 // This CTA's walk over its units of all phases (units u0, u0 + G, ... of each
-// phase, u0 rotating so that the phases' first units go to different CTAs).
+// phase, u0 = (cta - base) mod G rotating so that the phases' first units go
+// to different CTAs).
 struct Walk {
-  int p, u, base;
+  int p, u;
 };
+
+__device__ __forceinline__ int first_unit(const Phase& ph, int cta, int G) { return (cta - ph.base % G + G) % G; }
 
 __device__ __forceinline__ void walk_settle(Walk& w, const EngineArgs& a, int cta, int G) {
   while (w.p < a.n_phases) {
-    const int units = phase_at(a, w.p).units;
-    if (w.u < units) return;
-    w.base = (w.base + units) % G;
+    if (w.u < phase_at(a, w.p).units) return;
     ++w.p;
-    w.u = (cta - w.base + G) % G;
+    if (w.p < a.n_phases) w.u = first_unit(phase_at(a, w.p), cta, G);
   }
 }
 
@@ -239,11 +240,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_engine_kernel(const __grid_c
   if (warp == kTcWarps) {
     // ------------------------------------------------------------ producer
     uint32_t it = 0;
-    Walk pf{0, cta % G, 0};              // the L2 prefetch cursor runs ahead of the copies
+    Walk pf{0, first_unit(phase_at(a, 0), cta, G)};   // the L2 prefetch cursor runs ahead of the copies
     walk_settle(pf, a, cta, G);
     unsigned long long copied = 0, requested = 0;
     bool stop = false;
-    int base = 0;
     for (int p = 0; p < a.n_phases && !stop; ++p) {
       const Phase& ph = phase_at(a, p);
       const uint32_t row_bytes = static_cast<uint32_t>(ph.k / kQK) * kBlockBytes;
@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_engine_kernel(const __grid_c
       const int chunks = (nb + kTcChunk - 1) / kTcChunk;
       const bool dual = ph.epi_kind == EPI_SILU;
       const int rpu = ph.rows_per_unit;
-      for (int u = (cta - base + G) % G; u < ph.units && !stop; u += G) {
+      for (int u = first_unit(ph, cta, G); u < ph.units && !stop; u += G) {
         const int row0 = u * rpu;
         const int rows = min(rpu, ph.n_rows - row0);
         if (a.prefetch_bytes) {
@@ -292,7 +292,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_engine_kernel(const __grid_c
         }
         copied += static_cast<unsigned long long>(rows) * row_bytes * (dual ? 2 : 1);
       }
-      base = (base + ph.units) % G;
     }
     // Drain: no copy may still be in flight when the CTA exits.
     if (lane == 0) {
@@ -308,14 +307,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_engine_kernel(const __grid_c
     uint32_t magic;
     asm volatile("mov.b32 %0, 0x64006400;" : "=r"(magic));
     uint32_t it = 0;
-    int base = 0;
     const unsigned tag0 = a.n_phases > 1 ? a.ctl->epoch * kPhasesPerEpoch + 1u : 0u;   // tag of phase 0
     for (int p = 0; p < a.n_phases; ++p) {
       const Phase& ph = phase_at(a, p);
       const int units = ph.units;
       const int nb = ph.k / kQK;
       const int chunks = (nb + kTcChunk - 1) / kTcChunk;
-      const int u0 = (cta - base + G) % G;
+      const int u0 = first_unit(ph, cta, G);
       if (u0 < units || (ph.x_dbg && cta == 0)) {
         float sumsq = 0.f;
         if (p > 0) {
@@ -406,7 +404,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_engine_kernel(const __grid_c
         }
         named_bar_sync(1, kTcConsumers);   // red_cta is read again at the next phase start
       }
-      base = (base + units) % G;
     }
   }
 
