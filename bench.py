@@ -298,16 +298,33 @@ def run_stream(args, torch, q4, model, synth, stream, barrier, gpu_index):
 
     sweep = args.config == "stream-sweep"
     fracs = [0.0, 0.25, 0.5, 0.75] if sweep else [args.resident_frac]
-    max_res = int(round(max(fracs) * n_layers))
-    dev_w, dptrs = (model.resident_layers(shape, max_res, seed=0) if max_res else (None, []))
+    # device copies of every layer a configuration may keep resident (same seeded bytes as the host blocks)
+    need = set()
+    for frac in fracs:
+        for pat in (["prefix", "spread"] if sweep else [args.resident_pattern]):
+            need |= set(resident_set(n_layers, int(round(frac * n_layers)), pat))
+    dptrs = {}
+    dev_blocks = []
+    if need:
+        for l in sorted(need):
+            buf, ptr = model.resident_layers(shape, 1, seed=0, first_layer=l)
+            dev_blocks.append(buf)
+            dptrs[l] = ptr[0]
     steps = min(args.steps, 20 if not sweep else 6)
     warm = min(args.warmup, 3)
     runs = []
+    combos = []
     for frac in fracs:
         R = int(round(frac * n_layers))
-        for chunked in ([False, True] if sweep else [args.chunked]):
-            host = [0 if i < R else hptrs[i] for i in range(n_layers)]
-            res = [dptrs[i] if i < R else 0 for i in range(n_layers)]
+        if sweep:
+            combos += [(R, "prefix", False), (R, "prefix", True)] + ([(R, "spread", False)] if 0 < R < n_layers else [])
+        else:
+            combos.append((R, args.resident_pattern, args.chunked))
+    for ci, (R, pat, chunked) in enumerate(combos):
+        if True:
+            keep = set(resident_set(n_layers, R, pat))
+            host = [0 if i in keep else hptrs[i] for i in range(n_layers)]
+            res = [dptrs[i] if i in keep else 0 for i in range(n_layers)]
             flags = q4.Q4_STREAM_CHUNKED if chunked else 0
             ring = q4.q4_stream_create_ex(shape, host, res, B, bufs[0], bufs[1], stride, ws, ws_bytes, flags)
 
@@ -318,13 +335,13 @@ def run_stream(args, torch, q4, model, synth, stream, barrier, gpu_index):
             if q4.q4_stream_status(ring, stream=stream) != 0:
                 raise RuntimeError("stream ring kernels reported a failed wait")
             t = secs / steps
-            runs.append(dict(resident_layers=R, chunked=chunked, secs=secs, clocks=clocks,
+            runs.append(dict(resident_layers=R, placement=pat, chunked=chunked, secs=secs, clocks=clocks,
                              ms_per_token=round(t * 1e3, 3), tokens_per_s=round(B / t, 3),
                              weight_gbs=round(layer_bytes * n_layers / t / 1e9, 2),
                              host_link_gbs=round(layer_bytes * (n_layers - R) / t / 1e9, 2),
                              host_link_frac=round(layer_bytes * (n_layers - R) / t / 1e9 / best, 4)))
             last_ring = ring
-            if not (frac == fracs[-1] and chunked == (True if sweep else args.chunked)):
+            if ci != len(combos) - 1:
                 q4.q4_stream_destroy(ring)
     head = runs[0]
     # end to end through the public call: the step's input copied in from pinned
@@ -349,7 +366,7 @@ def run_stream(args, torch, q4, model, synth, stream, barrier, gpu_index):
     R = runs[-1]["resident_layers"]
     desc = (f"70B-shaped stack, {n_layers} layers, {n_layers - head['resident_layers']} streamed from pinned host "
             f"memory ({distinct} distinct layer blocks) through two HBM layer buffers"
-            f"{', ' + str(head['resident_layers']) + ' resident' if head['resident_layers'] else ''}, "
+            f"{', ' + str(head['resident_layers']) + ' resident (' + head['placement'] + ')' if head['resident_layers'] else ''}, "
             f"{'chunked' if head['chunked'] else 'merged'} copies, batch {B}")
     out = dict(secs=head["secs"], clocks=head["clocks"], bytes_per_step=layer_bytes * n_layers,
                streamed_bytes_per_step=layer_bytes * (n_layers - head["resident_layers"]),
@@ -363,6 +380,16 @@ def run_stream(args, torch, q4, model, synth, stream, barrier, gpu_index):
     if sweep:
         out["residency_sweep"] = [{k: v for k, v in r.items() if k not in ("secs", "clocks")} for r in runs]
     return out
+
+
+def resident_set(n_layers, n_res, pattern):
+    """Which layers stay resident: the first n_res ("prefix") or n_res spread evenly over the stack
+    ("spread", so the copies of the streamed layers are spaced out between resident ones)."""
+    if n_res <= 0:
+        return []
+    if pattern == "prefix":
+        return list(range(n_res))
+    return sorted({min(n_layers - 1, (i * n_layers) // n_res) for i in range(n_res)})
 
 
 def run_sweep(args, torch, q4, model, synth, stream, barrier, gpu_index):
@@ -472,6 +499,8 @@ def main():
     ap.add_argument("--resident-frac", type=float, default=0.0,
                     help="70b-stream: fraction of the layers (a prefix) kept resident in HBM")
     ap.add_argument("--chunked", action="store_true", help="70b-stream: copy each layer as four chunks")
+    ap.add_argument("--resident-pattern", default="prefix", choices=["prefix", "spread"],
+                    help="70b-stream: which layers stay resident")
     ap.add_argument("--batch", type=int, default=1, help="activation rows per step (1..16)")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0)

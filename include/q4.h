@@ -251,7 +251,8 @@ int q4_decoder_destroy(q4_decoder *dec);
  *
  * The array is Q4_NOALLOC_SCRATCH_BYTES (1 MiB) on every GPU that loads the
  * library, held until the process exits; it fits a batch-1 stack of the
- * 70B shape with up to 1000 layers.  Larger stacks return Q4_ERR_OOM.
+ * 70B shape with up to 687 layers (an 8B-shaped one with 1023).  Larger
+ * stacks return Q4_ERR_OOM.
  * The first call on a device looks up the array's device address on that
  * device (make that first call before any stream capture).  Every call
  * shares the one array and overwrites it, so calls whose work overlaps on

@@ -94,7 +94,7 @@ def test_single_nonzero_is_exact(kernel):
 # ------------------------------------------------------------------ parity with the oracle
 
 STREAM_SHAPES = [(1, 256), (7, 256), (33, 512), (100, 1024), (129, 2048), (300, 4096), (61, 14336), (17, 28672),
-                 (1000, 8192)]
+                 (1000, 8192), (9, 30720), (40, 6144)]
 
 
 @pytest.mark.parametrize("n,k", STREAM_SHAPES)
@@ -196,8 +196,8 @@ def test_deterministic_and_auto_is_stream():
     d = run(w, x, n, k, 1, q4.Q4_KERNEL_TC)
     e = run(w, x, n, k, 1, q4.Q4_KERNEL_TC)
     assert np.array_equal(d, e)
-    # above the persistent engines' widths auto takes the tensor-core product kernel
-    n, k = 8, 32768
+    # above the persistent engine's widths auto takes the tensor-core product kernel
+    n, k = 8, 34816
     w = synth.q4_matrix(n, k, 1, synth.GEMV_TID)
     x = synth.activations(1, k, 1)
     assert np.array_equal(run(w, x, n, k, 1, q4.Q4_KERNEL_AUTO), run(w, x, n, k, 1, q4.Q4_KERNEL_MMA))

@@ -753,6 +753,7 @@ struct q4_stream {
   cudaStream_t copy = nullptr;
   cudaEvent_t loaded[2][4] = {}, freed[2] = {nullptr, nullptr};
   cudaEvent_t start = nullptr, done = nullptr;
+  bool used[2] = {false, false};   // a buffer's `freed` event has been recorded
 };
 
 extern "C" int q4_stream_create(q4_stream** out, const q4_layer_shape* shape, const void* const* host_layers,
@@ -851,27 +852,26 @@ extern "C" int q4_stream_layers(q4_stream* r, uint16_t* hidden_io, void* compute
     r->cur_h = hidden_io;
   }
   if (r->batch > 1) r->cur_h = hidden_io;
-  // The copy stream may only overwrite a buffer once everything queued on the
-  // compute stream before this call (earlier tokens) has finished with it.
-  Q4_CUDA(cudaEventRecord(r->start, cs));
-  Q4_CUDA(cudaStreamWaitEvent(r->copy, r->start, 0));
+  // The copy stream may only overwrite a buffer once the compute that last read
+  // it (in this call or an earlier one) has finished: its `freed` event.  No
+  // wait on the whole previous token, so the next token's first copies overlap
+  // the end of this token and the compute of any resident layers before them.
   const size_t n_blocks = r->layer_bytes / q4::kBlockBytes;
   const bool chunked = (r->flags & Q4_STREAM_CHUNKED) != 0;
   const int n_chunks = chunked ? 4 : 1;
-  int streamed = 0;   // streamed layers enqueued so far in this call
   for (int i = 0; i < r->n_layers; ++i) {
     const int b = r->slot[i];
     const uint8_t* wl = b < 0 ? r->resident[i] : r->buf[b];
     if (b >= 0) {
-      // copy stream: layer i into buffer b once the streamed layer two before it has released it
-      if (streamed >= 2) Q4_CUDA(cudaStreamWaitEvent(r->copy, r->freed[b], 0));
+      // copy stream: layer i into buffer b once the last layer computed on b has released it
+      if (r->used[b]) Q4_CUDA(cudaStreamWaitEvent(r->copy, r->freed[b], 0));
+      r->used[b] = true;
       for (int c = 0; c < n_chunks; ++c) {
         const size_t lo = chunked ? r->chunk_off[c] : 0, hi = chunked ? r->chunk_off[c + 1] : r->layer_bytes;
         Q4_CUDA(cudaMemcpyAsync(r->buf[b] + lo, static_cast<const uint8_t*>(r->host[i]) + lo, hi - lo,
                                 cudaMemcpyHostToDevice, r->copy));
         Q4_CUDA(cudaEventRecord(r->loaded[b][c], r->copy));
       }
-      ++streamed;
     }
     const bool last = i == r->n_layers - 1;
     int st = Q4_OK;
@@ -897,7 +897,7 @@ extern "C" int q4_stream_layers(q4_stream* r, uint16_t* hidden_io, void* compute
       Q4_CUDA(cudaEventRecord(r->freed[b], cs));
     }
   }
-  // the next call's copies wait on `start`, which follows this call's compute
+  // the next call's copies wait on the `freed` events recorded above
   if (timeout_us > 0) {
     Q4_CUDA(cudaEventRecord(r->done, cs));
     const auto t0 = std::chrono::steady_clock::now();

@@ -388,21 +388,23 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
       const Tile t = tile_of(ph, tid);
       const int units = ph.units, n_rows = ph.n_rows;
       const int u0 = (cta - ph.base % G + G) % G;
-      if (u0 < units || (ph.x_dbg && cta == 0)) {
-        float sumsq = 0.f;
-        if (p > 0) {
-          // the input of a later phase is the previous phase's output: one warp
-          // waits for every CTA's flag, the CTA barrier releases the others
-          if (warp == 0) {
-            const float v = wait_phase_flags(a.flags + ((p - 1) & 1) * kMaxGrid, tag0 + (p - 1), lane,
-                                             a.wait_limit, a.ctl);
-            if (lane == 0) red_cta[0] = v;
-          }
-          named_bar_sync(1, kConsumerThreads);
-          sumsq = red_cta[0];
-        } else if (ph.x_kind == X_NORM32) {
-          sumsq = sum_ss_array(ph.ss_in, lane);   // written by an earlier launch
+      // Every CTA waits for all CTAs' flags of the previous phase, even with no
+      // units of its own here: a CTA may never publish phase p's flag while
+      // another can still be reading phase p - 2's flags from the same slot
+      // (the slots alternate), or that reader would take the wrong sum of squares.
+      float sumsq = 0.f;
+      if (p > 0) {
+        // one warp polls every CTA's flag, the CTA barrier releases the others
+        if (warp == 0) {
+          const float v = wait_phase_flags(a.flags + ((p - 1) & 1) * kMaxGrid, tag0 + (p - 1), lane,
+                                           a.wait_limit, a.ctl);
+          if (lane == 0) red_cta[0] = v;
         }
+        named_bar_sync(1, kConsumerThreads);
+        sumsq = red_cta[0];
+      }
+      if (u0 < units || (ph.x_dbg && cta == 0)) {
+        if (p == 0 && ph.x_kind == X_NORM32) sumsq = sum_ss_array(ph.ss_in, lane);   // from an earlier launch
         form_x(ph, t.active ? t.j : 0, lane, xs2, ph.x_dbg != nullptr && cta == 0 && t.team == 0, sumsq);
       }
       const int cap = kRedFloats / (t.spu * t.tw);   // units buffered before a flush
