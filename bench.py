@@ -51,9 +51,15 @@ def peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+KERNEL_SOURCES = {
+    "engine_kernel": ("q4_engine.cu", "q4_device.cuh", "q4_phase.cuh"),
+    "mma_kernel": ("q4_mma.cu", "q4_frag.cuh", "q4_device.cuh"),
+}
+
+
+def kernel_source_hash(kernel: str = "engine_kernel") -> str:
     h = hashlib.sha256()
-    for f in ("q4_engine.cu", "q4_device.cuh"):
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "weight_streaming_q4_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -67,7 +73,7 @@ def ncu_traffic(key: str):
     with open(path) as f:
         data = json.load(f)
     ent = data.get(key)
-    if not ent or ent.get("kernel_sha") != kernel_source_hash():
+    if not ent or ent.get("kernel_sha") != kernel_source_hash(key.split(":")[0]):
         return None
     return ent.get("bytes_per_launch")
 
