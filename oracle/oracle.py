@@ -61,12 +61,13 @@ def _declare(lib):
     lib.ora_gemv_rows.argtypes = [_P, _P, _I64, _I64, _INT, _P, _I64, _P, _P]
     lib.ora_rmsnorm.argtypes = [_P, _INT, _I64, _DBL, _P]
     lib.ora_attn_ctx1.argtypes = [_P, _INT, _I64, _I64, _I64, _P]
+    lib.ora_attn_decode.argtypes = [_P, _P, _P, _I64, _I64, _I64, _I64, _P, _P, _P]
     lib.ora_rmsnorm_d.argtypes = [_P, _INT, _I64, _DBL, _P]
     lib.ora_add.argtypes = [_P, _P, _I64, _P]
     lib.ora_silu_mul.argtypes = [_P, _P, _I64, _P]
     lib.ora_layer.argtypes = [_P, _P, _INT, _I64, _I64, _I64, _I64, _I64, _DBL, _P, _P, _P, _P]
     for name in ("ora_half_to_double_n", "ora_double_to_half_n", "ora_dequant", "ora_gemv",
-                 "ora_gemv_rows", "ora_rmsnorm", "ora_rmsnorm_d", "ora_attn_ctx1", "ora_add",
+                 "ora_gemv_rows", "ora_rmsnorm", "ora_rmsnorm_d", "ora_attn_ctx1", "ora_attn_decode", "ora_add",
                  "ora_silu_mul", "ora_layer"):
         getattr(lib, name).restype = None
     return lib
@@ -182,6 +183,22 @@ def attn_ctx1(v, batch: int, q_dim: int, kv_dim: int, head_dim: int, lib=None) -
     out = np.empty((batch, q_dim), dtype=np.uint16)
     lib.ora_attn_ctx1(_ptr(vb), batch, q_dim, kv_dim, head_dim, _ptr(out))
     return out
+
+
+def attn_decode(q, k_cache, v_cache, ctx: int, n_q: int, n_kv: int, head_dim: int, lib=None):
+    """Decode attention of one token over the first ctx rows of a binary16 KV
+    cache ([positions][n_kv * head_dim]); q double [n_q * head_dim].
+    Returns (o, sabs), each double [n_q * head_dim]."""
+    lib = lib or load()
+    qd = np.ascontiguousarray(q, dtype=np.float64).reshape(-1)
+    kc = _u16(k_cache).reshape(-1)
+    vc = _u16(v_cache).reshape(-1)
+    assert qd.size == n_q * head_dim and kc.size >= ctx * n_kv * head_dim and vc.size >= ctx * n_kv * head_dim
+    o = np.empty(n_q * head_dim, dtype=np.float64)
+    sabs = np.empty(n_q * head_dim, dtype=np.float64)
+    work = np.empty(max(ctx, 1), dtype=np.float64)
+    lib.ora_attn_decode(_ptr(qd), _ptr(kc), _ptr(vc), ctx, n_q, n_kv, head_dim, _ptr(o), _ptr(sabs), _ptr(work))
+    return o, sabs
 
 
 def rmsnorm_d(t, batch: int, dim: int, eps: float = 1e-5, lib=None) -> np.ndarray:

@@ -209,6 +209,51 @@ void ora_attn_ctx1(const double *v, int batch, int64_t q_dim, int64_t kv_dim, in
                     ora_double_to_half(v[(int64_t)b * kv_dim + (qh / group) * head_dim + i]);
 }
 
+/* Decode attention of one token over a KV cache (the decode loop over a
+ * growing context that PipeLLM captures per context-length bucket, "Layer 1:
+ * CUDA Graph Compilation"; the per-layer KV cache PIPO loads and saves with
+ * the layer, Method, "Offloading architecture").  The cache holds binary16
+ * keys and values, row t = position t, each row n_kv heads of head_dim
+ * values (keys already carry their position encoding, as a cache stores
+ * them).  For query head h and its value head g = h / (n_q / n_kv):
+ *   s_t = (sum_i q[h][i] * k[t][g][i]) / sqrt(head_dim),  t < ctx
+ *   p_t = exp(s_t - max_t s_t) / sum_t exp(s_t - max_t s_t)
+ *   o[h][i] = sum_t p_t * v[t][g][i]
+ * in double, q given in double.  sabs[h][i] = sum_t p_t |v[t][g][i]| (for the
+ * accepted error bound). */
+void ora_attn_decode(const double *q, const uint16_t *kc, const uint16_t *vc, int64_t ctx, int64_t n_q,
+                     int64_t n_kv, int64_t head_dim, double *o, double *sabs, double *work)
+{
+    int64_t group = n_q / n_kv, kv_dim = n_kv * head_dim;
+    double scale = 1.0 / sqrt((double)head_dim);
+    for (int64_t h = 0; h < n_q; h++) {
+        int64_t g = h / group;
+        double mx = -INFINITY;
+        for (int64_t t = 0; t < ctx; t++) {
+            double sc = 0.0;
+            for (int64_t i = 0; i < head_dim; i++)
+                sc += q[h * head_dim + i] * ora_half_to_double(kc[t * kv_dim + g * head_dim + i]);
+            work[t] = sc * scale;
+            if (work[t] > mx) mx = work[t];
+        }
+        double den = 0.0;
+        for (int64_t t = 0; t < ctx; t++) {
+            work[t] = exp(work[t] - mx);
+            den += work[t];
+        }
+        for (int64_t i = 0; i < head_dim; i++) {
+            double acc = 0.0, aabs = 0.0;
+            for (int64_t t = 0; t < ctx; t++) {
+                double v = ora_half_to_double(vc[t * kv_dim + g * head_dim + i]);
+                acc += work[t] / den * v;
+                aabs += work[t] / den * fabs(v);
+            }
+            o[h * head_dim + i] = acc;
+            sabs[h * head_dim + i] = aabs;
+        }
+    }
+}
+
 /* RMSNorm of a double vector (a residual sum): x = f16(t / sqrt(mean(t^2) + eps)). */
 void ora_rmsnorm_d(const double *t, int batch, int64_t dim, double eps, uint16_t *x_out)
 {

@@ -295,6 +295,60 @@ def pin_glue(lib):
     assert np.array_equal(att.ravel(), expect)
 
 
-ALL_PINS = [pin_half_decode_exhaustive, pin_half_encode, pin_golden_blocks, pin_distinct_positions,
+def pin_attn_decode(lib):
+    """Decode attention over a KV cache: closed forms of the softmax."""
+    rng = np.random.default_rng(11)
+    n_q, n_kv, hd = 8, 2, 16
+    group = n_q // n_kv
+    kv = n_kv * hd
+    # one position: the softmax over one key is 1, so head h reads value head h // group
+    # (also the context-1 stand-in of the layer, computed by another oracle function)
+    v1 = _f16(rng.normal(size=(1, kv)))
+    q = rng.normal(size=n_q * hd)
+    o, sabs = ora.attn_decode(q, _f16(rng.normal(size=(1, kv))), v1, 1, n_q, n_kv, hd, lib=lib)
+    vd = v1.view(np.float16).astype(np.float64).reshape(n_kv, hd)
+    expect = np.concatenate([vd[h // group] for h in range(n_q)])
+    assert np.array_equal(o, expect), "ctx 1: value head of the group"
+    assert np.array_equal(ora.double_to_half(o, lib=lib),
+                          ora.attn_ctx1(vd.reshape(1, -1), 1, n_q * hd, kv, hd, lib=lib).reshape(-1))
+    # equal keys: uniform weights, o = mean of the values, sabs = mean of |values|
+    ctx = 7
+    krow = _f16(rng.normal(size=(1, kv)))
+    kc = np.repeat(krow, ctx, axis=0)
+    vc = _f16(rng.normal(size=(ctx, kv)))
+    o, sabs = ora.attn_decode(q, kc, vc, ctx, n_q, n_kv, hd, lib=lib)
+    vv = vc.view(np.float16).astype(np.float64).reshape(ctx, n_kv, hd)
+    mean = np.concatenate([vv[:, h // group].mean(axis=0) for h in range(n_q)])
+    mabs = np.concatenate([np.abs(vv[:, h // group]).mean(axis=0) for h in range(n_q)])
+    assert np.allclose(o, mean, rtol=0, atol=1e-12), "equal keys: mean of values"
+    assert np.allclose(sabs, mabs, rtol=0, atol=1e-12), "equal keys: mean of |values|"
+    # two score levels: key 0 = e0, the others 0; q = a e0 per head:
+    # p0 = 1 / (1 + (ctx - 1) exp(-a / sqrt(hd)))
+    kc = np.zeros((ctx, kv), dtype=np.uint16)
+    kc[0, 0::hd] = _f16(1.0)            # component 0 of every value head's key at position 0
+    a = 3.0
+    q = np.zeros(n_q * hd)
+    q[0::hd] = a
+    o, _ = ora.attn_decode(q, kc, vc, ctx, n_q, n_kv, hd, lib=lib)
+    p0 = 1.0 / (1.0 + (ctx - 1) * np.exp(-a / np.sqrt(hd)))
+    expect = np.concatenate([p0 * vv[0, h // group] + (1 - p0) * vv[1:, h // group].mean(axis=0)
+                             for h in range(n_q)])
+    assert np.allclose(o, expect, rtol=0, atol=1e-12), "two score levels"
+    # a score of 1000 (exp overflows without the max shift): o = the value at that position
+    q[0::hd] = 1000.0 * np.sqrt(hd)
+    o, _ = ora.attn_decode(q, kc, vc, ctx, n_q, n_kv, hd, lib=lib)
+    assert np.all(np.isfinite(o))
+    assert np.allclose(o, np.concatenate([vv[0, h // group] for h in range(n_q)]), rtol=0, atol=1e-12)
+    # permuting the positions (keys and values together) leaves the result unchanged
+    kc = _f16(rng.normal(size=(ctx, kv)))
+    q = rng.normal(size=n_q * hd)
+    perm = rng.permutation(ctx)
+    o1, s1 = ora.attn_decode(q, kc, vc, ctx, n_q, n_kv, hd, lib=lib)
+    o2, s2 = ora.attn_decode(q, kc[perm], vc[perm], ctx, n_q, n_kv, hd, lib=lib)
+    assert np.allclose(o1, o2, rtol=0, atol=1e-12) and np.allclose(s1, s2, rtol=0, atol=1e-12)
+    assert np.all(s1 >= np.abs(o1) - 1e-15)
+
+
+ALL_PINS = [pin_attn_decode, pin_half_decode_exhaustive, pin_half_encode, pin_golden_blocks, pin_distinct_positions,
             pin_block_indexing, pin_golden_gemv, pin_all_eight_is_zero, pin_single_nonzero,
             pin_constant_codes, pin_brute_force, pin_invariants, pin_glue]

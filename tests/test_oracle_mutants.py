@@ -35,6 +35,13 @@ MUTANTS = {
     "layer_skips_norm": ("ora_add(z1, dn, (int64_t)batch * hidden, t2);\n    ora_rmsnorm_d(t2, batch, hidden, eps, z_out);",
                          "ora_add(z1, dn, (int64_t)batch * hidden, t2);\n    ora_double_to_half_n(t2, (int64_t)batch * hidden, z_out);"),
     "silu_sign": ("exp(-g[i])", "exp(g[i])"),
+    "attn_scale": ("double scale = 1.0 / sqrt((double)head_dim);", "double scale = 1.0 / (double)head_dim;"),
+    "attn_no_max_shift": ("work[t] = exp(work[t] - mx);", "work[t] = exp(work[t]);"),
+    "attn_group_modulo": ("int64_t g = h / group;", "int64_t g = h % n_kv;"),
+    "attn_cache_stride": ("kc[t * kv_dim + g * head_dim + i]", "kc[t * head_dim + g * head_dim + i]"),
+    "attn_signed_sabs": ("aabs += work[t] / den * fabs(v);", "aabs += work[t] / den * v;"),
+    "attn_value_key_swap": ("double v = ora_half_to_double(vc[t * kv_dim + g * head_dim + i]);",
+                            "double v = ora_half_to_double(kc[t * kv_dim + g * head_dim + i]);"),
 }
 
 
