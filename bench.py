@@ -402,6 +402,76 @@ def run_stream(args, torch, q4, model, synth, stream, barrier, gpu_index):
     return out
 
 
+def run_attn(args, torch, q4, model, synth, stream, barrier, gpu_index):
+    """Decode attention over the KV caches of all 32 layers of the 8B shape
+    (32 query heads, 8 value heads, head_dim 128), one CUDA graph per context
+    bucket (512, 1024, 2048, 4096), every position in use; the caches of one
+    step (32 layers x 2 x ctx x 1024 x 2 B) exceed L2 from the 1024 bucket up."""
+    import numpy as np
+    n_q, n_kv, hd, L = 32, 8, 128, 32
+    kv = n_kv * hd
+    buckets = [512, 1024, 2048, 4096]
+    cap = max(buckets)
+    kc = torch.empty(L, cap * kv, dtype=torch.int16, device="cuda")
+    vc = torch.empty(L, cap * kv, dtype=torch.int16, device="cuda")
+    for l in range(L):
+        synth.device_fill_normal_f16(kc[l].data_ptr(), cap * kv, seed=0, tid=0x40000000 + 2 * l)
+        synth.device_fill_normal_f16(vc[l].data_ptr(), cap * kv, seed=0, tid=0x40000001 + 2 * l)
+    q_host = torch.from_numpy((np.random.default_rng(0).normal(size=n_q * hd) * 0.25).astype(np.float32))
+    q = q_host.cuda()
+    out = torch.empty(L, n_q * hd, dtype=torch.int16, device="cuda")
+    ctx = torch.zeros(1, dtype=torch.int32, device="cuda")
+    wsb = q4.q4_attn_workspace_bytes(n_q, hd, cap)
+    ws = torch.empty(L, wsb, dtype=torch.uint8, device="cuda")
+    steps = max(10, min(args.steps, 200))
+    per = {}
+    for b in buckets:
+        ctx.fill_(b)
+
+        def enqueue():
+            for l in range(L):
+                q4.q4_attn_decode(q, kc[l], vc[l], ctx, b, n_q, n_kv, hd, out[l], ws[l], wsb, stream=stream)
+
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            enqueue()
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                enqueue()
+        with torch.cuda.stream(stream):
+            secs, clocks = time_region(torch, stream, g.replay, steps, 3, barrier, gpu_index)
+        t = secs / steps
+        nbytes = L * 2 * b * kv * 2
+        per[b] = dict(secs=secs, clocks=clocks, ms_per_step=round(t * 1e3, 4), kv_gbs=round(nbytes / t / 1e9, 2),
+                      bytes_per_step=nbytes)
+        last_graph = g
+    head = per[cap]
+    # end to end through the public call: q in from pinned memory, the outputs back, every step
+    qin = q_host.pin_memory()
+    oout = torch.empty(L, n_q * hd, dtype=torch.int16).pin_memory()
+    e2e_steps = max(10, steps // 4)
+    with torch.cuda.stream(stream):
+        q.copy_(qin, non_blocking=True)
+        last_graph.replay()
+        stream.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(e2e_steps):
+            q.copy_(qin, non_blocking=True)
+            last_graph.replay()
+            oout.copy_(out, non_blocking=True)
+            stream.synchronize()
+    e2e_secs = time.perf_counter() - t0
+    return dict(secs=head["secs"], clocks=head["clocks"], bytes_per_step=head["bytes_per_step"],
+                launches_per_step=2 * L, kernel_launches_per_step=L, steps_override=steps, warmup_override=3,
+                e2e_secs=e2e_secs, e2e_steps=e2e_steps, h2d=q_host.numel() * 4, d2h=out.numel() * 2,
+                workload=(f"decode attention, 8B heads (32 q, 8 kv, head_dim 128), {L} layers' binary16 KV caches, "
+                          f"context {cap} (bucket {cap}), one CUDA graph per bucket"),
+                kernel="attn_partial_kernel", kernel_key=None, cfg=dict(n_q=n_q, n_kv=n_kv, hd=hd),
+                attn_buckets={str(b): {k: v for k, v in r.items() if k not in ("secs", "clocks")}
+                              for b, r in per.items()})
+
+
 def resident_set(n_layers, n_res, pattern):
     """Which layers stay resident: the first n_res ("prefix") or n_res spread evenly over the stack
     ("spread", so the copies of the streamed layers are spaced out between resident ones)."""
@@ -508,6 +578,26 @@ def cpu_oracle_rate(cfg_name: str, budget_s: float, torch=None, q4=None, model=N
     return gbs, cores, done_bytes, t_total
 
 
+def cpu_attn_rate(budget_s: float):
+    """The oracle's decode attention (fp64) on 8B heads, context 4096, one
+    layer's cache after another until budget_s passes (one host thread)."""
+    import numpy as np
+
+    import oracle as ora
+    n_q, n_kv, hd, ctx = 32, 8, 128, 4096
+    rng = np.random.default_rng(0)
+    q = rng.normal(size=n_q * hd) * 0.25
+    done, t_total = 0, 0.0
+    while t_total < budget_s:
+        kc = rng.normal(size=(ctx, n_kv * hd)).astype(np.float16).view(np.uint16)
+        vc = rng.normal(size=(ctx, n_kv * hd)).astype(np.float16).view(np.uint16)
+        t0 = time.perf_counter()
+        ora.attn_decode(q, kc, vc, ctx, n_q, n_kv, hd)
+        t_total += time.perf_counter() - t0
+        done += 2 * ctx * n_kv * hd * 2
+    return done / t_total / 1e9, 1, done, t_total
+
+
 # ------------------------------------------------------------------ main
 
 def main():
@@ -515,7 +605,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--config", default="8b", choices=["8b", "gemv", "70b", "70b-stream", "stream-sweep", "sweep"])
+    ap.add_argument("--config", default="8b",
+                    choices=["8b", "gemv", "70b", "70b-stream", "stream-sweep", "sweep", "attn"])
     ap.add_argument("--resident-frac", type=float, default=0.0,
                     help="70b-stream: fraction of the layers (a prefix) kept resident in HBM")
     ap.add_argument("--chunked", action="store_true", help="70b-stream: copy each layer as four chunks")
@@ -549,7 +640,7 @@ def main():
                                                                                "stream-sweep")):
         raise SystemExit("--batch: 1..16, for the 8b, 70b and stream configs")
     runner = {"8b": run_stack, "70b": run_stack, "gemv": run_gemv, "70b-stream": run_stream,
-              "stream-sweep": run_stream, "sweep": run_sweep}[args.config]
+              "stream-sweep": run_stream, "sweep": run_sweep, "attn": run_attn}[args.config]
     r = runner(args, torch, q4, model, synth, stream, barrier, local_rank)
     steps = r.get("steps_override", args.steps)
     warmup = r.get("warmup_override", args.warmup)
@@ -610,6 +701,9 @@ def main():
         out["roofline"]["timing"] = "step time / launches of the kernel per step (glue launches included)"
     if "sweep" in r:
         out["sweep"] = r["sweep"]
+    if "attn_buckets" in r:
+        out["attn_buckets"] = r["attn_buckets"]
+        out["metric_note"] = "value = GB/s of KV-cache bytes read (keys and values), not weight bytes"
     if r.get("e2e_secs"):
         e2e_bytes = r.get("e2e_bytes_per_step", r["bytes_per_step"])
         out["e2e"] = {"value": round(e2e_bytes / (r["e2e_secs"] / r["e2e_steps"]) / 1e9, 2), "unit": "GB/s",
@@ -625,9 +719,12 @@ def main():
         print(json.dumps(out), flush=True)
         return
     try:
-        gbs_cpu, cores, nbytes, t = cpu_oracle_rate("gemv" if args.config == "gemv" else
-                                                    ("8b" if args.config in ("8b", "sweep") else "70b"),
-                                                    args.cpu_budget)
+        if args.config == "attn":
+            gbs_cpu, cores, nbytes, t = cpu_attn_rate(args.cpu_budget)
+        else:
+            gbs_cpu, cores, nbytes, t = cpu_oracle_rate("gemv" if args.config == "gemv" else
+                                                        ("8b" if args.config in ("8b", "sweep") else "70b"),
+                                                        args.cpu_budget)
         out["cpu_baseline"] = {"value": round(gbs_cpu, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                                "sample": f"{nbytes} weight bytes of row-sampled projections of the same "
                                          f"workload in {t:.1f} s, fp64, {cores} threads"}

@@ -90,6 +90,9 @@ def _declare(lib):
         "q4_stream_create_ex": ([ctypes.POINTER(c_p), ctypes.POINTER(LayerShape), ctypes.POINTER(c_p),
                                  ctypes.POINTER(c_p), c_int, c_int, c_p, c_p, c_size, c_p, c_size, c_int], c_int),
         "q4_stream_layers": ([c_p, c_p, c_p, c_i64], c_int),
+        "q4_attn_decode": ([c_p, c_p, c_p, c_p, c_int, c_int, c_int, c_int, c_p, c_p, c_size, c_p], c_int),
+        "q4_attn_workspace_bytes": ([c_int, c_int, c_int], c_size),
+        "q4_kv_append": ([c_p, c_p, c_p, c_p, c_p, c_int, c_int, c_p], c_int),
         "q4_stream_status": ([c_p, c_p, ctypes.POINTER(c_int)], c_int),
         "q4_stream_destroy": ([c_p], c_int),
     }
@@ -249,6 +252,22 @@ def q4_stream_create_ex(shape: LayerShape, host_ptrs, resident_ptrs, batch: int,
                                      _ptr(buf1), buf_bytes, _ptr(workspace), workspace_bytes, flags),
            "q4_stream_create_ex")
     return h
+
+
+def q4_attn_decode(q, k_cache, v_cache, ctx_len, capacity: int, n_q_heads: int, n_kv_heads: int, head_dim: int,
+                   out, workspace, workspace_bytes: int, stream=None):
+    _check(lib().q4_attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(ctx_len), capacity, n_q_heads,
+                                n_kv_heads, head_dim, _ptr(out), _ptr(workspace), workspace_bytes, _stream(stream)),
+           "q4_attn_decode")
+
+
+def q4_attn_workspace_bytes(n_q_heads: int, head_dim: int, capacity: int) -> int:
+    return lib().q4_attn_workspace_bytes(n_q_heads, head_dim, capacity)
+
+
+def q4_kv_append(k, v, k_cache, v_cache, pos, capacity: int, kv_dim: int, stream=None):
+    _check(lib().q4_kv_append(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(pos), capacity, kv_dim,
+                              _stream(stream)), "q4_kv_append")
 
 
 def q4_stream_layers(st, hidden, stream=None, timeout_us: int = 0):

@@ -62,6 +62,7 @@ int device_info(DeviceInfo** out) {
     Q4_CUDA(q4::engine_prepare());
     Q4_CUDA(q4::mma_prepare());
     Q4_CUDA(q4::tc_engine_prepare());
+    Q4_CUDA(q4::attn_prepare());
     Q4_CUDA(q4::engine_occupancy(&d.engine_blocks_per_sm));
     if (d.engine_blocks_per_sm < 1) return Q4_ERR_CUDA;
     d.ready = true;
@@ -930,5 +931,43 @@ extern "C" int q4_stream_destroy(q4_stream* r) {
   if (r->done) cudaEventDestroy(r->done);
   if (r->copy) cudaStreamDestroy(r->copy);
   delete r;
+  return Q4_OK;
+}
+
+// ===================================================================== decode attention
+
+static bool attn_shape_ok(int capacity, int n_q, int n_kv, int hd) {
+  if (capacity < 128 || capacity % 128 || capacity > (1 << 20)) return false;
+  if (n_kv < 1 || n_q < n_kv || n_q % n_kv || n_q / n_kv > 16) return false;
+  return hd >= 64 && hd <= 256 && hd % 64 == 0;
+}
+
+extern "C" size_t q4_attn_workspace_bytes(int n_q_heads, int head_dim, int capacity) {
+  if (n_q_heads < 1 || head_dim < 1 || capacity < 128 || capacity % 128) return 0;
+  return static_cast<size_t>(n_q_heads) * (capacity / 128) * (head_dim + 2) * sizeof(float);
+}
+
+extern "C" int q4_attn_decode(const float* q, const uint16_t* k_cache, const uint16_t* v_cache, const int* ctx_len,
+                              int capacity, int n_q_heads, int n_kv_heads, int head_dim, uint16_t* out,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !k_cache || !v_cache || !ctx_len || !out || !workspace) return Q4_ERR_ARG;
+  if (!attn_shape_ok(capacity, n_q_heads, n_kv_heads, head_dim)) return Q4_ERR_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(workspace, 16) || !aligned(ctx_len, 4))
+    return Q4_ERR_ALIGN;
+  if (workspace_bytes < q4_attn_workspace_bytes(n_q_heads, head_dim, capacity)) return Q4_ERR_OOM;
+  DeviceInfo* dev = nullptr;
+  int st = device_info(&dev);
+  if (st != Q4_OK) return st;
+  Q4_CUDA(q4::attn_launch(q, k_cache, v_cache, ctx_len, capacity, n_q_heads, n_kv_heads, head_dim, out,
+                          static_cast<float*>(workspace), static_cast<cudaStream_t>(stream)));
+  return Q4_OK;
+}
+
+extern "C" int q4_kv_append(const float* k, const float* v, uint16_t* k_cache, uint16_t* v_cache, const int* pos,
+                            int capacity, int kv_dim, void* stream) {
+  if (!k || !v || !k_cache || !v_cache || !pos || capacity < 1 || kv_dim < 1) return Q4_ERR_ARG;
+  if (!aligned(pos, 4)) return Q4_ERR_ALIGN;
+  Q4_CUDA(q4::kv_append_launch(k, v, k_cache, v_cache, pos, capacity, kv_dim, static_cast<cudaStream_t>(stream)));
   return Q4_OK;
 }
