@@ -421,8 +421,8 @@ def run_attn(args, torch, q4, model, synth, stream, barrier, gpu_index):
     q = q_host.cuda()
     out = torch.empty(L, n_q * hd, dtype=torch.int16, device="cuda")
     ctx = torch.zeros(1, dtype=torch.int32, device="cuda")
-    wsb = q4.q4_attn_workspace_bytes(n_q, hd, cap)
-    ws = torch.empty(L, wsb, dtype=torch.uint8, device="cuda")
+    wsb = q4.q4_attn_workspace_bytes(n_q, n_kv, hd, cap)
+    ws = torch.zeros(L, (wsb + 255) // 256 * 256, dtype=torch.uint8, device="cuda")
     steps = max(10, min(args.steps, 200))
     per = {}
     for b in buckets:

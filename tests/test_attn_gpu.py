@@ -34,8 +34,8 @@ class Attn:
         self.vc = torch.from_numpy(vc.view(np.int16).copy()).cuda()
         self.ctx = torch.zeros(1, dtype=torch.int32, device="cuda")
         self.out = torch.empty(n_q * hd, dtype=torch.int16, device="cuda")
-        self.wsb = q4.q4_attn_workspace_bytes(n_q, hd, capacity)
-        self.ws = torch.empty(self.wsb, dtype=torch.uint8, device="cuda")
+        self.wsb = q4.q4_attn_workspace_bytes(n_q, n_kv, hd, capacity)
+        self.ws = torch.zeros(self.wsb, dtype=torch.uint8, device="cuda")
 
     def run(self, ctx, stream=None):
         self.ctx.fill_(ctx)

@@ -91,7 +91,7 @@ def _declare(lib):
                                  ctypes.POINTER(c_p), c_int, c_int, c_p, c_p, c_size, c_p, c_size, c_int], c_int),
         "q4_stream_layers": ([c_p, c_p, c_p, c_i64], c_int),
         "q4_attn_decode": ([c_p, c_p, c_p, c_p, c_int, c_int, c_int, c_int, c_p, c_p, c_size, c_p], c_int),
-        "q4_attn_workspace_bytes": ([c_int, c_int, c_int], c_size),
+        "q4_attn_workspace_bytes": ([c_int, c_int, c_int, c_int], c_size),
         "q4_kv_append": ([c_p, c_p, c_p, c_p, c_p, c_int, c_int, c_p], c_int),
         "q4_stream_status": ([c_p, c_p, ctypes.POINTER(c_int)], c_int),
         "q4_stream_destroy": ([c_p], c_int),
@@ -261,8 +261,8 @@ def q4_attn_decode(q, k_cache, v_cache, ctx_len, capacity: int, n_q_heads: int, 
            "q4_attn_decode")
 
 
-def q4_attn_workspace_bytes(n_q_heads: int, head_dim: int, capacity: int) -> int:
-    return lib().q4_attn_workspace_bytes(n_q_heads, head_dim, capacity)
+def q4_attn_workspace_bytes(n_q_heads: int, n_kv_heads: int, head_dim: int, capacity: int) -> int:
+    return lib().q4_attn_workspace_bytes(n_q_heads, n_kv_heads, head_dim, capacity)
 
 
 def q4_kv_append(k, v, k_cache, v_cache, pos, capacity: int, kv_dim: int, stream=None):

@@ -937,14 +937,17 @@ extern "C" int q4_stream_destroy(q4_stream* r) {
 // ===================================================================== decode attention
 
 static bool attn_shape_ok(int capacity, int n_q, int n_kv, int hd) {
-  if (capacity < 128 || capacity % 128 || capacity > (1 << 20)) return false;
+  if (capacity < 128 || capacity % 128 || capacity > 65536) return false;
   if (n_kv < 1 || n_q < n_kv || n_q % n_kv || n_q / n_kv > 16) return false;
-  return hd >= 64 && hd <= 256 && hd % 64 == 0;
+  if (hd < 64 || hd > 256 || hd % 64) return false;
+  // the combining CTA keeps every chunk's max and sum of its group's heads in its key buffer
+  const int chunk = q4::attn_chunk(capacity, n_kv), group = n_q / n_kv;
+  return static_cast<size_t>(2 * group) * (capacity / chunk) * 4 + 4 * group <= static_cast<size_t>(chunk) * hd * 2;
 }
 
-extern "C" size_t q4_attn_workspace_bytes(int n_q_heads, int head_dim, int capacity) {
-  if (n_q_heads < 1 || head_dim < 1 || capacity < 128 || capacity % 128) return 0;
-  return static_cast<size_t>(n_q_heads) * (capacity / 128) * (head_dim + 2) * sizeof(float);
+extern "C" size_t q4_attn_workspace_bytes(int n_q_heads, int n_kv_heads, int head_dim, int capacity) {
+  if (!attn_shape_ok(capacity, n_q_heads, n_kv_heads, head_dim)) return 0;
+  return q4::attn_workspace_bytes(n_q_heads, n_kv_heads, head_dim, capacity);
 }
 
 extern "C" int q4_attn_decode(const float* q, const uint16_t* k_cache, const uint16_t* v_cache, const int* ctx_len,
@@ -955,12 +958,12 @@ extern "C" int q4_attn_decode(const float* q, const uint16_t* k_cache, const uin
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
       !aligned(workspace, 16) || !aligned(ctx_len, 4))
     return Q4_ERR_ALIGN;
-  if (workspace_bytes < q4_attn_workspace_bytes(n_q_heads, head_dim, capacity)) return Q4_ERR_OOM;
+  if (workspace_bytes < q4_attn_workspace_bytes(n_q_heads, n_kv_heads, head_dim, capacity)) return Q4_ERR_OOM;
   DeviceInfo* dev = nullptr;
   int st = device_info(&dev);
   if (st != Q4_OK) return st;
   Q4_CUDA(q4::attn_launch(q, k_cache, v_cache, ctx_len, capacity, n_q_heads, n_kv_heads, head_dim, out,
-                          static_cast<float*>(workspace), static_cast<cudaStream_t>(stream)));
+                          workspace, static_cast<cudaStream_t>(stream)));
   return Q4_OK;
 }
 

@@ -218,9 +218,10 @@ cudaError_t simple_launch(const uint8_t* w, const uint16_t* x, float* y, int n, 
 cudaError_t dequant_launch(const uint8_t* w, float* out, int n, int k, cudaStream_t stream);
 cudaError_t poison_launch(uint8_t* buf, size_t n_blocks, cudaStream_t stream);
 cudaError_t attn_prepare();
-size_t attn_smem_bytes(int group, int hd);
+size_t attn_workspace_bytes(int n_q, int n_kv, int hd, int capacity);
+int attn_chunk(int capacity, int n_kv);
 cudaError_t attn_launch(const float* q, const uint16_t* k, const uint16_t* v, const int* ctx_len, int capacity,
-                        int n_q, int n_kv, int hd, uint16_t* out, float* part, cudaStream_t s);
+                        int n_q, int n_kv, int hd, uint16_t* out, void* ws, cudaStream_t s);
 cudaError_t kv_append_launch(const float* k, const float* v, uint16_t* kc, uint16_t* vc, const int* pos, int capacity,
                              int kv_dim, cudaStream_t s);
 cudaError_t tc_engine_prepare();
