@@ -58,10 +58,15 @@ KERNEL_SOURCES = {
 
 
 def kernel_source_hash(kernel: str = "engine_kernel") -> str:
+    """Hash of the device code a kernel is built from (the shared header up to
+    its host-side declarations)."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "weight_streaming_q4_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+            text = fh.read()
+        if f == "q4_device.cuh":
+            text = text.split(b"// Host-side launchers")[0]
+        h.update(text)
     return h.hexdigest()[:16]
 
 
