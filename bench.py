@@ -321,6 +321,19 @@ def run_stream(args, torch, q4, model, synth, stream, barrier, gpu_index):
         torch.cuda.synchronize()
         best = max(best, 4 * stride / (ev0.elapsed_time(ev1) / 1e3) / 1e9)
 
+    # each host block's own copy speed (blocks in slow host memory show up here)
+    block_gbs = []
+    for i in range(len(blocks)):
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(cs)
+        with torch.cuda.stream(cs):
+            bufs[i & 1].copy_(blocks[i], non_blocking=True)
+        ev1.record(cs)
+        torch.cuda.synchronize()
+        block_gbs.append(stride / (ev0.elapsed_time(ev1) / 1e3) / 1e9)
+    med = statistics.median(block_gbs)
+    host_blocks = {"min_gbs": round(min(block_gbs), 2), "median_gbs": round(med, 2), "max_gbs": round(max(block_gbs), 2),
+                   "slow_blocks": [i for i, g_ in enumerate(block_gbs) if g_ < 0.8 * med]}
     sweep = args.config == "stream-sweep"
     fracs = [0.0, 0.25, 0.5, 0.75] if sweep else [args.resident_frac]
     # device copies of every layer a configuration may keep resident (same seeded bytes as the host blocks)
@@ -401,7 +414,7 @@ def run_stream(args, torch, q4, model, synth, stream, barrier, gpu_index):
                e2e_secs=e2e_secs, e2e_steps=e2e_steps, h2d=h0.numel() * 2, d2h=h0.numel() * 2,
                e2e_note=f"measured on the last configuration run ({R} resident layers)",
                workload=desc, kernel="engine_kernel" if B == 1 else "mma_kernel",
-               kernel_key=None, cfg=cfg, distinct=distinct)
+               kernel_key=None, cfg=cfg, distinct=distinct, host_blocks=host_blocks)
     if sweep:
         out["residency_sweep"] = [{k: v for k, v in r.items() if k not in ("secs", "clocks")} for r in runs]
     return out
@@ -566,7 +579,7 @@ def cpu_oracle_rate(cfg_name: str, budget_s: float, torch=None, q4=None, model=N
             mats = dims
         for (n, k, tid) in mats:
             # bounded row sample of this projection, rows spread over the matrix
-            rows = n if n * k <= (1 << 24) else max(64, (1 << 24) // k)
+            rows = n if n * k <= (1 << 26) else max(64, (1 << 26) // k)
             sel = np.linspace(0, n - 1, rows).astype(np.int64)
             w = synth.q4_rows(sel, k, 0, tid).reshape(-1)
             x = synth.activations(1, k, 0)
@@ -694,6 +707,7 @@ def main():
                             "frac": round(sb / per_step / 1e9 / r["h2d_peak_gbs"], 4) if sb else None,
                             "streamed_bytes_per_token": sb}
         out["config"]["distinct_host_layers"] = r["distinct"]
+        out["host_link"]["host_blocks"] = r["host_blocks"]
         if "residency_sweep" in r:
             out["residency_sweep"] = r["residency_sweep"]
     achieved = bytes_per_launch / per_launch_s / 1e9
@@ -730,9 +744,10 @@ def main():
             gbs_cpu, cores, nbytes, t = cpu_oracle_rate("gemv" if args.config == "gemv" else
                                                         ("8b" if args.config in ("8b", "sweep") else "70b"),
                                                         args.cpu_budget)
+        what = ("KV-cache bytes of whole 8B-head attention calls at context 4096" if args.config == "attn" else
+                "weight bytes of row-sampled projections of the same workload")
         out["cpu_baseline"] = {"value": round(gbs_cpu, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                               "sample": f"{nbytes} weight bytes of row-sampled projections of the same "
-                                         f"workload in {t:.1f} s, fp64, {cores} threads"}
+                               "sample": f"{nbytes} {what} in {t:.1f} s, fp64, {cores} threads"}
     except Exception as e:  # the baseline is context; never hide the GPU number
         out["cpu_baseline"] = {"value": None, "unit": "GB/s", "cores": 0, "kind": "oracle", "sample": f"failed: {e}"}
     print(json.dumps(out), flush=True)

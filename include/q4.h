@@ -38,7 +38,7 @@
  *     report, and the kernel returns.
  *   - Weight, x and y pointers must be 16-byte aligned (Q4_ERR_ALIGN).
  *   - k must be a multiple of 32 (one block); the streaming kernel needs k in
- *     {256, 512, 1024} or a multiple of 2048 up to 30720; other k use a
+ *     {256, 512, 1024} or a multiple of 2048 up to 28672; other k use a
  *     plain (slower) kernel.
  *   - x is binary16 [batch][k] row-major, y is fp32 [batch][n] row-major and
  *     is overwritten, not accumulated.  1 <= batch <= 16.

@@ -78,6 +78,8 @@ bool engine_ok(int k) {
   if (k < 256 || k % 256 != 0) return false;
   const int team = k / q4::kKT;
   if (team > q4::kConsumerThreads) return false;
+  // a unit holds two rows of every team: at least two rows must fit a stage
+  if (2 * (k / q4::kQK) * q4::kBlockBytes > q4::kStageBytes) return false;
   return team % 32 == 0 || 32 % team == 0;
 }
 
@@ -168,7 +170,9 @@ extern "C" int q4_gemv_ex(const void* w, const uint16_t* x, float* y, int n, int
   if (st != Q4_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (kernel == Q4_KERNEL_AUTO) {
-    if (batch == 1 && engine_ok(k)) kernel = Q4_KERNEL_STREAM;
+    // batch 1: the CUDA-core engine (plain kernel for widths it cannot take);
+    // batch 2..16: tensor cores when rows are 16-byte aligned
+    if (batch == 1) kernel = engine_ok(k) ? Q4_KERNEL_STREAM : Q4_KERNEL_SIMPLE;
     else if (k % 256 == 0) kernel = Q4_KERNEL_MMA;
     else kernel = Q4_KERNEL_SIMPLE;
   }
