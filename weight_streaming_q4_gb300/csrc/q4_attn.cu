@@ -11,9 +11,9 @@
 //
 // One kernel, split over the context (so a short query still spreads over
 // the whole GPU): one CTA per (value head g, chunk of 32/64/128 positions,
-// chosen per bucket so that there are at least 256 CTAs).  The chunk's keys
+// chosen per bucket so that there is a CTA for every SM), 256 threads.  The chunk's keys
 // and values of head g are copied to shared memory with 16-byte asynchronous
-// copies (all in flight at once); 128/chunk threads form each position's
+// copies (all in flight at once); 256/chunk threads form each position's
 // scores with the group's query heads (q pre-scaled by 1/sqrt(head_dim));
 // per head, the chunk's maximum m, l = sum exp(s - m) and
 // o[i] = sum exp(s - m) v[i] are written out.  The last chunk of a value head
@@ -31,7 +31,8 @@
 
 namespace q4 {
 
-constexpr int kAttnThreads = 128;
+constexpr int kAttnThreads = 256;
+constexpr int kAttnWarps = kAttnThreads / 32;
 constexpr int kAttnMaxChunk = 128;   // positions per CTA: 32, 64 or 128 (chosen per bucket)
 constexpr int kAttnMaxGroup = 16;
 
@@ -73,24 +74,24 @@ __device__ __forceinline__ void attn_reduce_heads(float* v, int group, float* re
         const float x = __shfl_xor_sync(0xffffffffu, v[j], o);
         v[j] = kMax ? fmaxf(v[j], x) : v[j] + x;
       }
-      if (lane == 0) red[j * 4 + w] = v[j];
+      if (lane == 0) red[j * kAttnWarps + w] = v[j];
     }
   }
   __syncthreads();
 #pragma unroll
   for (int j = 0; j < GMAX; ++j) {
     if (j < group) {
-      float r = red[j * 4];
+      float r = red[j * kAttnWarps];
 #pragma unroll
-      for (int i = 1; i < kAttnThreads / 32; ++i) r = kMax ? fmaxf(r, red[j * 4 + i]) : r + red[j * 4 + i];
+      for (int i = 1; i < kAttnWarps; ++i) r = kMax ? fmaxf(r, red[j * kAttnWarps + i]) : r + red[j * kAttnWarps + i];
       v[j] = r;
     }
   }
   __syncthreads();
 }
 
-// One CTA per (value head g, chunk c of `chunk` positions), 128 threads;
-// tp = 128 / chunk threads share a position's scores (each a slice of the
+// One CTA per (value head g, chunk c of `chunk` positions), 256 threads;
+// tp = 256 / chunk threads share a position's scores (each a slice of the
 // head dimension, summed with shuffles).
 template <int GMAX>
 __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const __grid_constant__ AttnArgs a) {
@@ -277,13 +278,13 @@ __global__ void kv_append_kernel(const float* k, const float* v, __half* kc, __h
 // contexts, 128 at large ones.
 int attn_chunk(int capacity, int n_kv) {
   int p = kAttnMaxChunk;
-  while (p > 32 && static_cast<long>(n_kv) * (capacity / p) < 256) p >>= 1;
+  while (p > 32 && static_cast<long>(n_kv) * (capacity / p) < 152) p >>= 1;
   return p;
 }
 
 size_t attn_smem_bytes(int group, int hd, int chunk) {
   return static_cast<size_t>(2) * chunk * hd * sizeof(__half) + static_cast<size_t>(group) * hd * sizeof(float) +
-         static_cast<size_t>(group) * chunk * sizeof(float) + kAttnMaxGroup * 4 * sizeof(float);
+         static_cast<size_t>(group) * chunk * sizeof(float) + kAttnMaxGroup * kAttnWarps * sizeof(float);
 }
 
 size_t attn_workspace_bytes(int n_q, int n_kv, int hd, int capacity) {
