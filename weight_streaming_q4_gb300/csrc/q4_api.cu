@@ -510,8 +510,9 @@ int launch_layer_batched(const q4_layer_shape& sh, const uint8_t* wl, int layer,
   Q4_CUDA(q4::mma_launch(wl + off[Q4_PROJ_O], w.attn, w.o, H, Q, batch, grid, kWaitLimit, &w.ctl->status, s));
   Q4_CUDA(q4::glue_resid_norm(w.x, w.o, batch, H, sh.eps, w.t1, w.x2, s));
   Q4_CUDA(wait(2));
-  Q4_CUDA(q4::mma_launch(wl + off[Q4_PROJ_GATE], w.x2, w.g, F, H, batch, grid, kWaitLimit, &w.ctl->status, s));
-  Q4_CUDA(q4::mma_launch(wl + off[Q4_PROJ_UP], w.x2, w.u, F, H, batch, grid, kWaitLimit, &w.ctl->status, s));
+  // gate and up are consecutive in the block: one product of 2 ffn rows, split into g and u
+  Q4_CUDA(q4::mma_launch(wl + off[Q4_PROJ_GATE], w.x2, w.g, 2 * F, H, batch, grid, kWaitLimit, &w.ctl->status, s,
+                         w.u, F));
   Q4_CUDA(q4::glue_silu(w.g, w.u, static_cast<size_t>(batch) * F, w.act, s));
   Q4_CUDA(wait(3));
   Q4_CUDA(q4::mma_launch(wl + off[Q4_PROJ_DOWN], w.act, w.dn, H, F, batch, grid, kWaitLimit, &w.ctl->status, s));

@@ -233,8 +233,9 @@ cudaError_t tc_engine_prepare();
 cudaError_t tc_engine_launch(const EngineArgs& a, int grid, bool cooperative, cudaStream_t stream);
 cudaError_t tc_engine_read_status(int* out);
 cudaError_t mma_prepare();
+// y2/split: rows from `split` on go to y2 ([batch][n - split]); rows before to y ([batch][split]).
 cudaError_t mma_launch(const uint8_t* w, const uint16_t* x, float* y, int n, int k, int batch, int grid,
-                       uint32_t wait_limit, int* status, cudaStream_t stream);
+                       uint32_t wait_limit, int* status, cudaStream_t stream, float* y2 = nullptr, int split = 0);
 cudaError_t mma_read_status(int* out);
 cudaError_t glue_norm(const uint16_t* src16, const float* src32, int batch, int dim, float eps, uint16_t* z,
                       cudaStream_t s);

@@ -37,8 +37,9 @@ constexpr int kMmaStages = 10;
 struct MmaArgs {
   const uint8_t* w;   // Q4_0 [n][k/32]
   const __half* x;    // binary16 [batch][k]
-  float* y;           // fp32 [batch][n]
-  int n, k, batch;
+  float* y;           // fp32 [batch][split]: rows below `split`
+  float* y2;          // fp32 [batch][n - split]: rows from `split` on (two matrices stored back to back)
+  int n, k, batch, split;
   uint32_t wait_limit;
   int* status;        // where timed-out waits are recorded (g_status_mma if none given)
 };
@@ -163,7 +164,13 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const __grid_consta
         const int e = (m >= 8 ? 2 : 0) + (cc & 1);
         float s = 0.f;
         for (int w = 0; w < kMmaWarps; ++w) s += red[w][ln][4 * j + e];
-        if (col < a.batch && row0 + m < a.n) a.y[static_cast<size_t>(col) * a.n + row0 + m] = s;
+        const int r = row0 + m;
+        if (col < a.batch && r < a.n) {
+          if (r < a.split)
+            a.y[static_cast<size_t>(col) * a.split + r] = s;
+          else
+            a.y2[static_cast<size_t>(col) * (a.n - a.split) + (r - a.split)] = s;
+        }
       }
       named_bar_sync(1, kMmaWarps * 32);
     }
@@ -187,8 +194,10 @@ cudaError_t mma_prepare() {
 }
 
 cudaError_t mma_launch(const uint8_t* w, const uint16_t* x, float* y, int n, int k, int batch, int grid,
-                       uint32_t wait_limit, int* status, cudaStream_t stream) {
+                       uint32_t wait_limit, int* status, cudaStream_t stream, float* y2, int split) {
   MmaArgs a;
+  a.y2 = y2;
+  a.split = (y2 && split > 0 && split < n) ? split : n;
   if (!status) {
     cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_status_mma);
     if (e != cudaSuccess) return e;
