@@ -190,7 +190,8 @@ def run_stack(args, torch, q4, model, synth, stream, barrier, gpu_index):
     wbuf, ptrs = model.resident_layers(shape, n_layers, seed=0)
     ws, offs, ws_bytes = model.workspace(shape, n_layers, B)
     with torch.cuda.stream(stream):
-        dec = q4.q4_decoder_create(shape, ptrs, B, ws, ws_bytes, q4.Q4_DEC_FUSED, stream=stream)
+        mode = q4.Q4_DEC_FUSED | (q4.Q4_DEC_BARRIER if args.barrier else 0)
+        dec = q4.q4_decoder_create(shape, ptrs, B, ws, ws_bytes, mode, stream=stream)
         h0 = torch.from_numpy(synth.activations(B, cfg["hidden"], 0).reshape(-1).view("int16").copy())
         h = h0.cuda()
     torch.cuda.synchronize()
@@ -222,6 +223,7 @@ def run_stack(args, torch, q4, model, synth, stream, barrier, gpu_index):
             hout.copy_(h, non_blocking=True)
             stream.synchronize()
     e2e_secs = time.perf_counter() - t0
+    tagged = q4.q4_decoder_tagged(dec)
     q4.q4_decoder_destroy(dec)
     nbytes = layer_bytes * n_layers
     # batch 1: one persistent launch per token; batch B: per layer 4 tensor-core
@@ -234,7 +236,7 @@ def run_stack(args, torch, q4, model, synth, stream, barrier, gpu_index):
                           f"batch {B}, HBM-resident, one CUDA-graph replay per step"),
                 kernel="engine_kernel" if B == 1 else "mma_kernel",
                 kernel_key=f"engine_kernel:{args.config}_stack" if B == 1 else f"mma_kernel:{args.config}_stack_b{B}",
-                n_layers=n_layers, cfg=cfg)
+                n_layers=n_layers, cfg=cfg, tagged=tagged)
 
 
 def run_gemv(args, torch, q4, model, synth, stream, barrier, gpu_index):
@@ -363,7 +365,7 @@ def run_stream(args, torch, q4, model, synth, stream, barrier, gpu_index):
             keep = set(resident_set(n_layers, R, pat))
             host = [0 if i in keep else hptrs[i] for i in range(n_layers)]
             res = [dptrs[i] if i in keep else 0 for i in range(n_layers)]
-            flags = q4.Q4_STREAM_CHUNKED if chunked else 0
+            flags = (q4.Q4_STREAM_CHUNKED if chunked else 0) | (q4.Q4_STREAM_BARRIER if args.barrier else 0)
             ring = q4.q4_stream_create_ex(shape, host, res, B, bufs[0], bufs[1], stride, ws, ws_bytes, flags)
 
             def step():
@@ -400,6 +402,7 @@ def run_stream(args, torch, q4, model, synth, stream, barrier, gpu_index):
             hout.copy_(h, non_blocking=True)
             stream.synchronize()
     e2e_secs = time.perf_counter() - t0
+    tagged = q4.q4_stream_tagged(last_ring)
     q4.q4_stream_destroy(last_ring)
     R = runs[-1]["resident_layers"]
     desc = (f"70B-shaped stack, {n_layers} layers, {n_layers - head['resident_layers']} streamed from pinned host "
@@ -414,7 +417,7 @@ def run_stream(args, torch, q4, model, synth, stream, barrier, gpu_index):
                e2e_secs=e2e_secs, e2e_steps=e2e_steps, h2d=h0.numel() * 2, d2h=h0.numel() * 2,
                e2e_note=f"measured on the last configuration run ({R} resident layers)",
                workload=desc, kernel="engine_kernel" if B == 1 else "mma_kernel",
-               kernel_key=None, cfg=cfg, distinct=distinct, host_blocks=host_blocks)
+               kernel_key=None, cfg=cfg, distinct=distinct, host_blocks=host_blocks, tagged=tagged)
     if sweep:
         out["residency_sweep"] = [{k: v for k, v in r.items() if k not in ("secs", "clocks")} for r in runs]
     return out
@@ -635,6 +638,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--layers", type=int, default=0, help="run only this many layers of the stack (profiling)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline (profiling runs)")
+    ap.add_argument("--barrier", action="store_true",
+                    help="batch-1 stacks: flag barrier after every phase instead of tagged words (comparison)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank, world, local_rank = dist_env()
@@ -695,6 +700,8 @@ def main():
         "config": {"workload": r["workload"], "batch": args.batch, "parallelism": f"replicas x{world}",
                    "l2": "weights per step exceed L2 (no flush needed)"},
     }
+    if "tagged" in r:
+        out["config"]["phase_sync"] = "tagged words" if r["tagged"] else "flag barrier per phase"
     if args.config in ("8b", "70b"):
         out["tokens_per_s"] = round(world * args.batch / per_step, 2)
         out["config"]["n_layers"] = r["n_layers"]

@@ -178,9 +178,12 @@ int q4_layer_offsets(const q4_layer_shape *shape, size_t offsets[7], size_t *lay
 #define Q4_WS_T2 12       /* fp32 [batch][hidden]: t2 = z1 + Wdown act */
 #define Q4_WS_FLAGS 13    /* u64 [2][256] per-CTA end-of-phase flags (tag, sum of squares), then
                              fp32 [2][256] per-CTA sums of squares of t1 and t2 */
-#define Q4_WS_XT 14       /* fp32 [hidden]: t1, then t2, slice-transposed (batch-1 engine input) */
-#define Q4_WS_VT 15       /* fp32 [kv_dim]: v slice-transposed (batch-1 engine input) */
-#define Q4_WS_ACTT 16     /* binary16 [ffn]: act slice-transposed (batch-1 engine input) */
+#define Q4_WS_XT 14       /* batch-1 engine inputs: t1 then t2 as tagged words (24 * hidden bytes:
+                             t1, t2 as 64-bit {fp32, tag}, z, z1 as 32-bit {binary16, tag}), or,
+                             with Q4_DEC_BARRIER, fp32 t1 / t2 slice-transposed */
+#define Q4_WS_VT 15       /* batch-1 engine input: v as 32-bit tagged words, or fp32 slice-transposed */
+#define Q4_WS_ACTT 16     /* batch-1 engine input: act as 32-bit tagged words, or binary16
+                             slice-transposed */
 #define Q4_WS_COUNT 17
 
 /*
@@ -198,6 +201,10 @@ typedef struct q4_decoder q4_decoder;
 #define Q4_DEC_PER_LAYER 1  /* one launch per layer (one graph node per layer) */
 #define Q4_DEC_TENSOR_CORE 2  /* or-ed into the mode: batch 1 runs the tensor-core engine
                                  (q4_tc_engine) instead of the exact CUDA-core engine */
+#define Q4_DEC_BARRIER 4    /* or-ed into the mode: the batch-1 CUDA-core engine meets at a flag
+                               barrier after every phase instead of passing tagged words (the
+                               default whenever hidden <= 9600 and kv_dim <= 14336); the two
+                               agree within the product error bound, not bit for bit */
 
 /*
  * Create a decoder over n_layers HBM-resident layers and capture its CUDA
@@ -207,7 +214,8 @@ typedef struct q4_decoder q4_decoder;
  *   n_layers       1..1023; batch: 1 <= batch <= 16
  *   workspace      device, >= q4_workspace_layout() bytes, 256-byte aligned;
  *                  owned by the caller, must outlive the decoder
- *   mode           Q4_DEC_FUSED or Q4_DEC_PER_LAYER, optionally | Q4_DEC_TENSOR_CORE.
+ *   mode           Q4_DEC_FUSED or Q4_DEC_PER_LAYER, optionally | Q4_DEC_TENSOR_CORE
+ *                  and | Q4_DEC_BARRIER.
  *                  Batch 1 runs one persistent engine (CUDA-core by default:
  *                  head_dim % 64 == 0 and the widths of Q4_KERNEL_STREAM;
  *                  tensor-core: head_dim % 4 == 0, hidden, q_dim, ffn multiples
@@ -236,6 +244,11 @@ int q4_layer_decode_eager(q4_decoder *dec, uint16_t *hidden_io, void *stream);
  * wait completed; otherwise bit flags; clears it.  Errors: Q4_ERR_CUDA. */
 int q4_decoder_status(q4_decoder *dec, void *stream, int *status_out);
 
+/* *tagged_out = 1 if the decoder's batch-1 CUDA-core engine passes tagged
+ * words between phases, 0 if it meets at a flag barrier after every phase (or
+ * runs another engine or batch).  Host only.  Errors: Q4_ERR_ARG. */
+int q4_decoder_tagged(const q4_decoder *dec, int *tagged_out);
+
 int q4_decoder_destroy(q4_decoder *dec);
 
 /* ------------------------------------------------------- decoder without allocation */
@@ -251,7 +264,7 @@ int q4_decoder_destroy(q4_decoder *dec);
  *
  * The array is Q4_NOALLOC_SCRATCH_BYTES (1 MiB) on every GPU that loads the
  * library, held until the process exits; it fits a batch-1 stack of the
- * 70B shape with up to 687 layers (an 8B-shaped one with 1023).  Larger
+ * 70B shape with up to 284 layers (an 8B-shaped one with 812).  Larger
  * stacks return Q4_ERR_OOM.
  * The first call on a device looks up the array's device address on that
  * device (make that first call before any stream capture).  Every call
@@ -328,6 +341,7 @@ typedef struct q4_stream q4_stream;
                                  down), one event each; each of the layer's products starts as
                                  soon as its own chunk has landed (PIPO, "Data transfer suite":
                                  blockwise transfer) instead of after the whole block */
+#define Q4_STREAM_BARRIER 8   /* as Q4_DEC_BARRIER for the ring's batch-1 CUDA-core engine */
 
 /*
  * Create a double-buffered copy/compute ring (PipeLLM, "Layer 2"; PIPO,
@@ -339,7 +353,8 @@ typedef struct q4_stream q4_stream;
  *   n_layers >= 1;  batch 1..16
  *   dev_buf0/1       device, buf_bytes >= one layer block each, 256-byte aligned
  *   workspace        device, >= q4_workspace_layout(shape, n_layers, batch) bytes
- *   flags            0, or Q4_STREAM_POISON | Q4_STREAM_TENSOR_CORE | Q4_STREAM_CHUNKED
+ *   flags            0, or Q4_STREAM_POISON | Q4_STREAM_TENSOR_CORE | Q4_STREAM_CHUNKED |
+ *                    Q4_STREAM_BARRIER
  * The handle creates its own copy stream and events.
  * Errors: Q4_ERR_ARG, Q4_ERR_ALIGN, Q4_ERR_OOM, Q4_ERR_CUDA.
  */
@@ -374,6 +389,9 @@ int q4_stream_layers(q4_stream *st, uint16_t *hidden_io, void *compute_stream, i
 
 /* Status word of the ring's kernels (synchronises compute_stream); clears it. */
 int q4_stream_status(q4_stream *st, void *compute_stream, int *status_out);
+
+/* As q4_decoder_tagged for a ring.  Host only.  Errors: Q4_ERR_ARG. */
+int q4_stream_tagged(const q4_stream *st, int *tagged_out);
 
 int q4_stream_destroy(q4_stream *st);
 

@@ -103,7 +103,7 @@ def test_decoder_checks(lib):
     assert f(ctypes.byref(h), ctypes.byref(shape), ptrs, 0, 1, 4096, ws_bytes, 0, None) == q4.Q4_ERR_ARG
     assert f(ctypes.byref(h), ctypes.byref(shape), ptrs, 2, 1, 4096 + 16, ws_bytes, 0, None) == q4.Q4_ERR_ALIGN
     assert f(ctypes.byref(h), ctypes.byref(shape), ptrs, 2, 1, 4096, ws_bytes - 1, 0, None) == q4.Q4_ERR_OOM
-    assert f(ctypes.byref(h), ctypes.byref(shape), ptrs, 2, 1, 4096, ws_bytes, 7, None) == q4.Q4_ERR_ARG
+    assert f(ctypes.byref(h), ctypes.byref(shape), ptrs, 2, 1, 4096, ws_bytes, 8, None) == q4.Q4_ERR_ARG   # unknown bit
     bad = q4.LayerShape.of(hidden=256, q_dim=256, kv_dim=96, ffn=1024, head_dim=64)   # kv not whole heads
     assert f(ctypes.byref(h), ctypes.byref(bad), ptrs, 2, 1, 4096, ws_bytes, 0, None) == q4.Q4_ERR_ARG
     odd = q4.LayerShape.of(hidden=96, q_dim=96, kv_dim=96, ffn=96, head_dim=32)      # rows not 16-byte aligned
@@ -121,7 +121,7 @@ def test_decoder_checks(lib):
     _, lb = q4.q4_layer_offsets(shape)
     assert g(ctypes.byref(s), ctypes.byref(shape), ptrs, 2, 1, 4096, 8192, lb - 1, 4096, ws_bytes, 0) == q4.Q4_ERR_OOM
     assert g(ctypes.byref(s), ctypes.byref(shape), ptrs, 2, 1, 4096, 8192 + 16, lb, 4096, ws_bytes, 0) == q4.Q4_ERR_ALIGN
-    assert g(ctypes.byref(s), ctypes.byref(shape), ptrs, 2, 1, 4096, 8192, lb, 4096, ws_bytes, 8) == q4.Q4_ERR_ARG
+    assert g(ctypes.byref(s), ctypes.byref(shape), ptrs, 2, 1, 4096, 8192, lb, 4096, ws_bytes, 16) == q4.Q4_ERR_ARG
     # partial residency: a layer needs a host block or a resident block; resident blocks 256-byte aligned
     gx = lib.q4_stream_create_ex
     none = (ctypes.c_void_p * 2)(None, None)

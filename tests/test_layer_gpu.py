@@ -14,6 +14,8 @@ pytestmark = pytest.mark.gpu
 TINY = dict(hidden=256, q_dim=256, kv_dim=128, ffn=1024, head_dim=64)
 SMALL = dict(hidden=2048, q_dim=2048, kv_dim=512, ffn=4096, head_dim=128)
 MID = dict(hidden=1024, q_dim=1024, kv_dim=256, ffn=14336, head_dim=128)   # down rows 14336 wide
+# down rows 20480 wide: the tagged down input is staged in two rounds, the second ragged
+WIDE = dict(hidden=1024, q_dim=1024, kv_dim=256, ffn=20480, head_dim=128)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -42,11 +44,13 @@ class Stack:
         q4.q4_decoder_destroy(self.dec)
 
 
-ENGINES = {"core": 0, "tc": q4.Q4_DEC_TENSOR_CORE}
+# the CUDA-core engine with tagged words between phases (default), the same
+# engine with a flag barrier after every phase, the tensor-core engine
+ENGINES = {"core": 0, "barrier": q4.Q4_DEC_BARRIER, "tc": q4.Q4_DEC_TENSOR_CORE}
 
 
 @pytest.mark.parametrize("engine", list(ENGINES))
-@pytest.mark.parametrize("cfg", [TINY, SMALL, MID], ids=["tiny", "small", "mid"])
+@pytest.mark.parametrize("cfg", [TINY, SMALL, MID, WIDE], ids=["tiny", "small", "mid", "wide"])
 def test_one_layer_step_by_step(cfg, engine):
     st = Stack(cfg, 1, seed=21, mode=q4.Q4_DEC_FUSED | ENGINES[engine])
     h0 = synth.activations(1, cfg["hidden"], 22)
@@ -111,6 +115,26 @@ def test_engines_agree_and_tc_head_dims():
     st.close()
     with pytest.raises(q4.Q4Error):
         Stack(odd, 1, seed=34)
+
+
+@pytest.mark.parametrize("cfg", [SMALL, WIDE], ids=["small", "wide"])
+def test_tagged_and_barrier_programs_agree(cfg):
+    """The tagged program and the flag-barrier program of the CUDA-core engine
+    compute the same layers; their RMSNorm sums of squares add up in different
+    orders, so they agree within the products' error bound, not bit for bit."""
+    h0 = synth.activations(1, cfg["hidden"], 36)
+    a = Stack(cfg, 3, seed=37).run(h0).view(np.float16).astype(np.float64)
+    b = Stack(cfg, 3, seed=37, mode=q4.Q4_DEC_BARRIER).run(h0).view(np.float16).astype(np.float64)
+    assert np.linalg.norm(a - b) / np.linalg.norm(b) < 2e-3
+
+
+def test_protocol_selection():
+    """Batch-1 CUDA-core decoders pass tagged words unless asked for the flag
+    barrier; the tensor-core engine always meets at flag barriers."""
+    assert Stack(SMALL, 1, seed=38).dec and q4.q4_decoder_tagged(Stack(SMALL, 1, seed=38).dec)
+    assert not q4.q4_decoder_tagged(Stack(SMALL, 1, seed=38, mode=q4.Q4_DEC_BARRIER).dec)
+    assert not q4.q4_decoder_tagged(Stack(SMALL, 1, seed=38, mode=q4.Q4_DEC_TENSOR_CORE).dec)
+    assert q4.q4_decoder_tagged(Stack(WIDE, 1, seed=38).dec)
 
 
 def test_new_hidden_pointer_rewrites_program():

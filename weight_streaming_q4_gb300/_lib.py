@@ -36,9 +36,11 @@ Q4_KERNEL_TC = 4
 Q4_DEC_FUSED = 0
 Q4_DEC_PER_LAYER = 1
 Q4_DEC_TENSOR_CORE = 2
+Q4_DEC_BARRIER = 4
 Q4_STREAM_POISON = 1
 Q4_STREAM_TENSOR_CORE = 2
 Q4_STREAM_CHUNKED = 4
+Q4_STREAM_BARRIER = 8
 
 WS_NAMES = ("control", "program", "qkv", "o", "gate", "up", "down", "act", "x", "attn", "x2", "t1", "t2", "flags", "xt", "vt", "actt")
 WS_COUNT = len(WS_NAMES)
@@ -82,6 +84,7 @@ def _declare(lib):
         "q4_layer_decode": ([c_p, c_p, c_p], c_int),
         "q4_layer_decode_eager": ([c_p, c_p, c_p], c_int),
         "q4_decoder_status": ([c_p, c_p, ctypes.POINTER(c_int)], c_int),
+        "q4_decoder_tagged": ([c_p, ctypes.POINTER(c_int)], c_int),
         "q4_decoder_destroy": ([c_p], c_int),
         "q4_layer_decode_noalloc": ([ctypes.POINTER(LayerShape), ctypes.POINTER(c_p), c_int, c_p, c_p], c_int),
         "q4_noalloc_scratch_bytes": ([], c_size),
@@ -94,6 +97,7 @@ def _declare(lib):
         "q4_attn_workspace_bytes": ([c_int, c_int, c_int, c_int], c_size),
         "q4_kv_append": ([c_p, c_p, c_p, c_p, c_p, c_int, c_int, c_p], c_int),
         "q4_stream_status": ([c_p, c_p, ctypes.POINTER(c_int)], c_int),
+        "q4_stream_tagged": ([c_p, ctypes.POINTER(c_int)], c_int),
         "q4_stream_destroy": ([c_p], c_int),
     }
     for name, (args, res) in sig.items():
@@ -216,6 +220,12 @@ def q4_decoder_status(dec, stream=None) -> int:
     return v.value
 
 
+def q4_decoder_tagged(dec) -> bool:
+    v = c_int(0)
+    _check(lib().q4_decoder_tagged(dec, ctypes.byref(v)), "q4_decoder_tagged")
+    return bool(v.value)
+
+
 def q4_decoder_destroy(dec):
     _check(lib().q4_decoder_destroy(dec), "q4_decoder_destroy")
 
@@ -272,6 +282,12 @@ def q4_kv_append(k, v, k_cache, v_cache, pos, capacity: int, kv_dim: int, stream
 
 def q4_stream_layers(st, hidden, stream=None, timeout_us: int = 0):
     return _check(lib().q4_stream_layers(st, _ptr(hidden), _stream(stream), timeout_us), "q4_stream_layers")
+
+
+def q4_stream_tagged(st) -> bool:
+    v = c_int(0)
+    _check(lib().q4_stream_tagged(st, ctypes.byref(v)), "q4_stream_tagged")
+    return bool(v.value)
 
 
 def q4_stream_status(st, stream=None) -> int:

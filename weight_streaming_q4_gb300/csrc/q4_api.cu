@@ -12,6 +12,7 @@
 #include <chrono>
 #include <mutex>
 #include <thread>
+#include <algorithm>
 #include <vector>
 
 #include "q4.h"
@@ -282,9 +283,11 @@ extern "C" int q4_workspace_layout(const q4_layer_shape* s, int n_layers, int ba
       4 * B * s->hidden,
       4 * B * s->hidden,
       8 * 2 * static_cast<size_t>(q4::kMaxGrid) + 4 * 2 * static_cast<size_t>(q4::kMaxGrid),
-      4 * static_cast<size_t>(s->hidden),
+      // batch-1 engine inputs: fp32 t1/t2 slice-transposed, or (tagged programs)
+      // tagged t1 and t2 (64-bit words) and the tagged residual bases z and z1
+      24 * static_cast<size_t>(s->hidden),
       4 * static_cast<size_t>(s->kv_dim),
-      2 * static_cast<size_t>(s->ffn),
+      4 * static_cast<size_t>(s->ffn),
   };
   size_t pos = 0;
   for (int i = 0; i < Q4_WS_COUNT; ++i) {
@@ -307,9 +310,12 @@ struct Work {
   uint16_t *act, *x, *attn, *x2;
   float *xt, *vt;              // slice-transposed t1/t2 and v (CUDA-core engine inputs)
   uint16_t* actt;              // slice-transposed act
+  // the same regions in a tagged program: tagged t1, t2 (fp32), z, z1, v, act (binary16)
+  unsigned long long *t1t, *t2t;
+  uint32_t *zt, *z1t, *vtag, *acttag;
 };
 
-Work carve(void* ws, const size_t* off) {
+Work carve(void* ws, const size_t* off, int hidden) {
   char* b = static_cast<char*>(ws);
   Work w;
   w.ctl = reinterpret_cast<Control*>(b + off[Q4_WS_CONTROL]);
@@ -331,6 +337,12 @@ Work carve(void* ws, const size_t* off) {
   w.xt = reinterpret_cast<float*>(b + off[Q4_WS_XT]);
   w.vt = reinterpret_cast<float*>(b + off[Q4_WS_VT]);
   w.actt = reinterpret_cast<uint16_t*>(b + off[Q4_WS_ACTT]);
+  w.t1t = reinterpret_cast<unsigned long long*>(b + off[Q4_WS_XT]);
+  w.t2t = w.t1t + hidden;
+  w.zt = reinterpret_cast<uint32_t*>(w.t2t + hidden);
+  w.z1t = w.zt + hidden;
+  w.vtag = reinterpret_cast<uint32_t*>(b + off[Q4_WS_VT]);
+  w.acttag = reinterpret_cast<uint32_t*>(b + off[Q4_WS_ACTT]);
   return w;
 }
 
@@ -458,19 +470,145 @@ bool final_phase(const q4_layer_shape& s, uint16_t* h_out, const Work& w, Phase*
   return tile_phase(*out, engine);
 }
 
+// Whether the CUDA-core engine can run a layer shape as a tagged program:
+// every phase input fits the per-CTA staging buffer and the chunk budget of
+// the staging loops.
+// Staging buffer of a tagged program (bytes): the widest phase input (fp32
+// hidden values for the norms, binary16 kv_dim and ffn values), and room for
+// the row partials.
+size_t tagged_xbuf_bytes(const q4_layer_shape& s) {
+  size_t b = 4 * static_cast<size_t>(q4::kRedFloats);
+  b = std::max(b, 4 * static_cast<size_t>(s.hidden));
+  b = std::max(b, 2 * static_cast<size_t>(s.kv_dim));
+  b = std::max(b, 2 * static_cast<size_t>(s.ffn));
+  return (b + 15) / 16 * 16;
+}
+
+// Ring depth of a tagged program: 6 stages when the staging buffer fits next
+// to them, else 5.
+int tagged_stages(const q4_layer_shape& s) {
+  return tagged_xbuf_bytes(s) <= static_cast<size_t>(q4::kXBufMaxBytes6) ? 6 : 5;
+}
+
+bool tagged_ok(const q4_layer_shape& s) {
+  return s.hidden <= q4::kNormMaxValues && s.kv_dim <= q4::kTag16MaxValues && s.ffn <= q4::kTag16MaxValues &&
+         tagged_xbuf_bytes(s) <= static_cast<size_t>(q4::kXBufMaxBytes5);
+}
+
+// The four phases of one layer as a tagged program (CUDA-core engine, batch
+// 1).  The same arithmetic as layer_phases; the values one phase hands to the
+// next travel as tagged words (t1, t2 fp32; v, act and the residual bases z, z1
+// binary16), so no phase waits at a barrier.  The plain intermediates are
+// written for the last layer only (the workspace keeps the last layer's).
+// Phase 1 publishes the flags that phase 2 waits for (SyncKind): every
+// tagged buffer is rewritten once per layer, and that single exchange, with
+// the data dependences between the phases, orders each rewrite after every
+// read of the previous values.
+bool layer_phases_tagged(const q4_layer_shape& s, const uint8_t* wl, const uint16_t* in16, const Work& w,
+                         Phase out[4], bool last) {
+  size_t off[7];
+  if (q4_layer_offsets(&s, off, nullptr) != Q4_OK) return false;
+  memset(out, 0, 4 * sizeof(Phase));
+  Phase& a = out[0];   // q, k, v
+  a.w0 = wl + off[Q4_PROJ_Q];
+  a.x_src = in16 ? static_cast<const void*>(in16) : static_cast<const void*>(w.t2t);
+  a.x_kind = in16 ? q4::X_NORM16 : q4::X_TAG32_NORM;
+  a.x_ld = s.hidden;
+  a.k = s.hidden;
+  a.eps = s.eps;
+  a.n_rows = s.q_dim + 2 * s.kv_dim;
+  a.epi_kind = q4::EPI_F32;
+  a.y = last ? w.qkv : nullptr;
+  a.x_dbg = last ? w.x : nullptr;
+  a.xr_out = w.zt;
+  a.yt = w.vtag;
+  a.yt_off = s.q_dim + s.kv_dim;
+  a.yt_n = s.kv_dim;
+  Phase& b = out[1];   // o, input: the context-1 attention of v, output: t1 = z + Wo a
+  b.w0 = wl + off[Q4_PROJ_O];
+  b.x_src = w.vtag;
+  b.x_kind = q4::X_TAG16_ATTN;
+  b.xt_n = s.kv_dim;
+  b.k = s.q_dim;
+  b.head_dim = s.head_dim;
+  b.group = (s.q_dim / s.head_dim) / (s.kv_dim / s.head_dim);
+  b.n_rows = s.hidden;
+  b.epi_kind = q4::EPI_RESID;
+  b.res_t = w.zt;
+  b.y = last ? w.o : nullptr;
+  b.y2 = last ? w.t1 : nullptr;
+  b.yt = w.t1t;
+  b.yt_n = s.hidden;
+  b.x_dbg = last ? w.attn : nullptr;
+  b.sync = q4::SYNC_PUBLISH;
+  Phase& c = out[2];   // gate | up, input z1 = f16(norm(t1)), output the SiLU-gated product
+  c.w0 = wl + off[Q4_PROJ_GATE];
+  c.w1 = wl + off[Q4_PROJ_UP];
+  c.x_src = w.t1t;
+  c.x_kind = q4::X_TAG32_NORM;
+  c.k = s.hidden;
+  c.eps = s.eps;
+  c.n_rows = s.ffn;
+  c.epi_kind = q4::EPI_SILU;
+  c.y = last ? w.g : nullptr;
+  c.y2 = last ? w.u : nullptr;
+  c.aux16 = last ? w.act : nullptr;
+  c.yt = w.acttag;
+  c.yt_n = s.ffn;
+  c.x_dbg = last ? w.x2 : nullptr;
+  c.xr_out = w.z1t;
+  c.sync = q4::SYNC_WAIT;
+  Phase& d = out[3];   // down, output t2 = z1 + Wdown act
+  d.w0 = wl + off[Q4_PROJ_DOWN];
+  d.x_src = w.acttag;
+  d.x_kind = q4::X_TAG16;
+  d.k = s.ffn;
+  d.n_rows = s.hidden;
+  d.epi_kind = q4::EPI_RESID;
+  d.res_t = w.z1t;
+  d.y = last ? w.dn : nullptr;
+  d.y2 = last ? w.t2 : nullptr;
+  d.yt = w.t2t;
+  d.yt_n = s.hidden;
+  for (int i = 0; i < 4; ++i)
+    if (!tile_phase(out[i], ENG_CORE)) return false;
+  return true;
+}
+
+// The closing phase of a tagged program: CTA 0 writes f16(norm(t2)) to the
+// caller's hidden-state buffer.
+bool final_phase_tagged(const q4_layer_shape& s, uint16_t* h_out, const Work& w, Phase* out) {
+  memset(out, 0, sizeof(Phase));
+  out->x_src = w.t2t;
+  out->x_kind = q4::X_TAG32_NORM;
+  out->k = s.hidden;
+  out->eps = s.eps;
+  out->n_rows = 0;
+  out->epi_kind = q4::EPI_F32;
+  out->x_dbg = h_out;
+  return tile_phase(*out, ENG_CORE);
+}
+
 // Phase program of a whole stack: 4 phases per layer and the closing phase.
 bool stack_program(const q4_layer_shape& s, const std::vector<const uint8_t*>& layers, uint16_t* h,
-                   const Work& w, std::vector<Phase>& prog, int engine) {
+                   const Work& w, std::vector<Phase>& prog, int engine, bool tagged) {
   const int L = static_cast<int>(layers.size());
   prog.assign(4 * static_cast<size_t>(L) + 1, Phase());
-  for (int l = 0; l < L; ++l)
-    if (!layer_phases(s, layers[l], l == 0 ? h : nullptr, w, &prog[4 * l], engine)) return false;
-  if (!final_phase(s, h, w, &prog[4 * L], engine)) return false;
+  for (int l = 0; l < L; ++l) {
+    const uint16_t* in16 = l == 0 ? h : nullptr;
+    if (!(tagged ? layer_phases_tagged(s, layers[l], in16, w, &prog[4 * l], l == L - 1)
+                 : layer_phases(s, layers[l], in16, w, &prog[4 * l], engine)))
+      return false;
+  }
+  if (!(tagged ? final_phase_tagged(s, h, w, &prog[4 * L]) : final_phase(s, h, w, &prog[4 * L], engine)))
+    return false;
   // unit rotation over the whole program, so that any split into launches
-  // (fused, per layer, per phase) gives every CTA the same rows
-  int base = 0;
+  // (fused, per layer, per phase) gives every CTA the same rows; the phase
+  // index fixes a tagged program's tags the same way
+  int base = 0, gidx = 0;
   for (Phase& ph : prog) {
     ph.base = base;
+    ph.gidx = gidx++;
     base += ph.units;
   }
   return true;
@@ -525,7 +663,10 @@ bool batched_shape_ok(const q4_layer_shape& s) {
   return s.hidden % 256 == 0 && s.q_dim % 256 == 0 && s.ffn % 256 == 0 && (s.q_dim + 2 * s.kv_dim) > 0;
 }
 
-int launch_layers(const Work& w, int first_phase, int n_phases, int grid, cudaStream_t s, int engine) {
+// Launch phases [first_phase, first_phase + n_phases) of the program in the
+// workspace; `end` = they include the program's last phase.
+int launch_layers(const Work& w, int first_phase, int n_phases, int grid, cudaStream_t s, int engine, bool tagged,
+                  bool end, const q4_layer_shape& shape) {
   EngineArgs a;
   memset(&a, 0, sizeof(a));
   a.phases = w.prog + first_phase;
@@ -533,6 +674,12 @@ int launch_layers(const Work& w, int first_phase, int n_phases, int grid, cudaSt
   a.ctl = w.ctl;
   a.flags = w.flags;
   a.wait_limit = kWaitLimit;
+  a.tagged = tagged ? 1 : 0;
+  a.end_of_program = end ? 1 : 0;
+  if (tagged) {
+    a.stages = tagged_stages(shape);
+    a.xbuf_floats = static_cast<int>(tagged_xbuf_bytes(shape) / 4);
+  }
   if (engine == ENG_TC) {
     a.prefetch_bytes = tc_prefetch_bytes();
     Q4_CUDA(q4::tc_engine_launch(a, grid, true, s));
@@ -557,6 +704,7 @@ int read_status(Control* ctl, cudaStream_t s, int* out) {
 struct q4_decoder {
   q4_layer_shape shape;
   int n_layers = 0, batch = 1, mode = Q4_DEC_FUSED, grid = 0, engine = ENG_CORE;
+  bool tagged = false;   // batch-1 CUDA-core engine with tagged words between phases
   std::vector<const uint8_t*> layers;
   Work w;
   uint16_t* cur_h = nullptr;
@@ -576,7 +724,7 @@ static int decoder_write_program(q4_decoder* d, uint16_t* h, cudaStream_t s) {
     return Q4_OK;
   }
   std::vector<Phase> prog;
-  if (!stack_program(d->shape, d->layers, h, d->w, prog, d->engine)) return Q4_ERR_ARG;
+  if (!stack_program(d->shape, d->layers, h, d->w, prog, d->engine, d->tagged)) return Q4_ERR_ARG;
   // pageable source: the runtime stages it before returning, so `prog` may go
   Q4_CUDA(cudaMemcpyAsync(d->w.prog, prog.data(), prog.size() * sizeof(Phase), cudaMemcpyHostToDevice, s));
   d->cur_h = h;
@@ -592,9 +740,9 @@ static int decoder_enqueue(q4_decoder* d, cudaStream_t s) {
     }
     return Q4_OK;
   }
-  if (d->mode == Q4_DEC_FUSED) return launch_layers(d->w, 0, 4 * L + 1, d->grid, s, d->engine);
+  if (d->mode == Q4_DEC_FUSED) return launch_layers(d->w, 0, 4 * L + 1, d->grid, s, d->engine, d->tagged, true, d->shape);
   for (int l = 0; l < L; ++l) {   // the last launch also runs the closing phase
-    int st = launch_layers(d->w, 4 * l, l == L - 1 ? 5 : 4, d->grid, s, d->engine);
+    int st = launch_layers(d->w, 4 * l, l == L - 1 ? 5 : 4, d->grid, s, d->engine, d->tagged, l == L - 1, d->shape);
     if (st != Q4_OK) return st;
   }
   return Q4_OK;
@@ -606,8 +754,8 @@ extern "C" int q4_decoder_create(q4_decoder** out, const q4_layer_shape* shape, 
   if (!out || !shape_ok(shape) || !layer_weights || n_layers < 1 || !workspace) return Q4_ERR_ARG;
   if (batch < 1 || batch > q4::kMaxBatch) return Q4_ERR_ARG;
   if (4 * n_layers + 1 > static_cast<int>(q4::kPhasesPerEpoch)) return Q4_ERR_ARG;
-  if ((mode & ~Q4_DEC_TENSOR_CORE) != Q4_DEC_FUSED && (mode & ~Q4_DEC_TENSOR_CORE) != Q4_DEC_PER_LAYER)
-    return Q4_ERR_ARG;
+  const int kind = mode & ~(Q4_DEC_TENSOR_CORE | Q4_DEC_BARRIER);
+  if (kind != Q4_DEC_FUSED && kind != Q4_DEC_PER_LAYER) return Q4_ERR_ARG;
   const int engine = (mode & Q4_DEC_TENSOR_CORE) ? ENG_TC : ENG_CORE;
   // batch 1: a persistent engine; larger batches: tensor-core products + glue
   if (batch == 1 ? check_layer_shape_for_engine(*shape, engine) != Q4_OK : !batched_shape_ok(*shape))
@@ -629,12 +777,13 @@ extern "C" int q4_decoder_create(q4_decoder** out, const q4_layer_shape* shape, 
   d->shape = *shape;
   d->n_layers = n_layers;
   d->batch = batch;
-  d->mode = mode & ~Q4_DEC_TENSOR_CORE;
+  d->mode = kind;
   d->engine = engine;
+  d->tagged = batch == 1 && engine == ENG_CORE && !(mode & Q4_DEC_BARRIER) && tagged_ok(*shape);
   d->grid = dev->sm_count < q4::kMaxGrid ? dev->sm_count : q4::kMaxGrid;   // one CTA per SM, co-resident
   d->layers.assign(reinterpret_cast<const uint8_t* const*>(layer_weights),
                    reinterpret_cast<const uint8_t* const*>(layer_weights) + n_layers);
-  d->w = carve(workspace, off);
+  d->w = carve(workspace, off, shape->hidden);
   cudaError_t e = cudaMemsetAsync(workspace, 0, need, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) {
@@ -715,17 +864,21 @@ int run_stack_in_workspace(const q4_layer_shape* shape, const void* const* layer
   if (ws_bytes < need) return Q4_ERR_OOM;
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != Q4_OK) return st;
-  const Work w = carve(ws, off);
+  const Work w = carve(ws, off, shape->hidden);
   std::vector<const uint8_t*> layers(reinterpret_cast<const uint8_t* const*>(layer_weights),
                                      reinterpret_cast<const uint8_t* const*>(layer_weights) + n_layers);
   std::vector<Phase> prog;
-  if (!stack_program(*shape, layers, hidden_io, w, prog, ENG_CORE)) return Q4_ERR_ARG;
+  const bool tagged = tagged_ok(*shape);
+  if (!stack_program(*shape, layers, hidden_io, w, prog, ENG_CORE, tagged)) return Q4_ERR_ARG;
   Q4_CUDA(cudaMemcpyAsync(w.prog, prog.data(), prog.size() * sizeof(Phase), cudaMemcpyHostToDevice, s));
-  // control block and phase flags start from zero (earlier calls left their tags)
+  // control block, phase flags and tagged words start from zero: earlier calls
+  // left their tags, and the epoch starts again at 0
   Q4_CUDA(cudaMemsetAsync(w.ctl, 0, sizeof(Control), s));
   Q4_CUDA(cudaMemsetAsync(w.flags, 0, 2 * kMaxGrid * sizeof(unsigned long long), s));
+  Q4_CUDA(cudaMemsetAsync(static_cast<char*>(ws) + off[Q4_WS_XT], 0, off[Q4_WS_COUNT - 1] - off[Q4_WS_XT] +
+                                                                       4 * static_cast<size_t>(shape->ffn), s));
   const int grid = dev->sm_count < kMaxGrid ? dev->sm_count : kMaxGrid;
-  return launch_layers(w, 0, static_cast<int>(prog.size()), grid, s, ENG_CORE);
+  return launch_layers(w, 0, static_cast<int>(prog.size()), grid, s, ENG_CORE, tagged, true, *shape);
 }
 
 }  // namespace q4
@@ -733,6 +886,12 @@ int run_stack_in_workspace(const q4_layer_shape* shape, const void* const* layer
 extern "C" int q4_decoder_status(q4_decoder* d, void* stream, int* status_out) {
   if (!d || !status_out) return Q4_ERR_ARG;
   return read_status(d->w.ctl, static_cast<cudaStream_t>(stream), status_out);
+}
+
+extern "C" int q4_decoder_tagged(const q4_decoder* d, int* tagged_out) {
+  if (!d || !tagged_out) return Q4_ERR_ARG;
+  *tagged_out = d->tagged ? 1 : 0;
+  return Q4_OK;
 }
 
 extern "C" int q4_decoder_destroy(q4_decoder* d) {
@@ -748,6 +907,7 @@ extern "C" int q4_decoder_destroy(q4_decoder* d) {
 struct q4_stream {
   q4_layer_shape shape;
   int n_layers = 0, batch = 1, flags = 0, grid = 0, engine = ENG_CORE;
+  bool tagged = false;
   std::vector<const void*> host;
   std::vector<const uint8_t*> resident;   // per layer: device block, or null if streamed
   std::vector<int> slot;                  // per layer: staging buffer (0/1), or -1 if resident
@@ -776,7 +936,7 @@ extern "C" int q4_stream_create_ex(q4_stream** out, const q4_layer_shape* shape,
   if (!out || !shape_ok(shape) || !host_layers || n_layers < 1 || !dev_buf0 || !dev_buf1 || !workspace)
     return Q4_ERR_ARG;
   if (batch < 1 || batch > q4::kMaxBatch ||
-      (flags & ~(Q4_STREAM_POISON | Q4_STREAM_TENSOR_CORE | Q4_STREAM_CHUNKED)))
+      (flags & ~(Q4_STREAM_POISON | Q4_STREAM_TENSOR_CORE | Q4_STREAM_CHUNKED | Q4_STREAM_BARRIER)))
     return Q4_ERR_ARG;
   if (4 * n_layers + 1 > static_cast<int>(q4::kPhasesPerEpoch)) return Q4_ERR_ARG;
   const int engine = (flags & Q4_STREAM_TENSOR_CORE) ? ENG_TC : ENG_CORE;
@@ -822,12 +982,13 @@ extern "C" int q4_stream_create_ex(q4_stream** out, const q4_layer_shape* shape,
   r->batch = batch;
   r->flags = flags;
   r->engine = engine;
+  r->tagged = batch == 1 && engine == ENG_CORE && !(flags & Q4_STREAM_BARRIER) && tagged_ok(*shape);
   r->grid = dev->sm_count < q4::kMaxGrid ? dev->sm_count : q4::kMaxGrid;
   r->host.assign(host_layers, host_layers + n_layers);
   r->buf[0] = static_cast<uint8_t*>(dev_buf0);
   r->buf[1] = static_cast<uint8_t*>(dev_buf1);
   r->layer_bytes = layer_bytes;
-  r->w = carve(workspace, off);
+  r->w = carve(workspace, off, shape->hidden);
   cudaError_t e = cudaStreamCreateWithFlags(&r->copy, cudaStreamNonBlocking);
   for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
     for (int c = 0; c < 4 && e == cudaSuccess; ++c) e = cudaEventCreateWithFlags(&r->loaded[i][c], cudaEventDisableTiming);
@@ -853,7 +1014,7 @@ extern "C" int q4_stream_layers(q4_stream* r, uint16_t* hidden_io, void* compute
     std::vector<const uint8_t*> bufs(r->n_layers);
     for (int i = 0; i < r->n_layers; ++i) bufs[i] = r->resident[i] ? r->resident[i] : r->buf[r->slot[i]];
     std::vector<Phase> prog;
-    if (!stack_program(r->shape, bufs, hidden_io, r->w, prog, r->engine)) return Q4_ERR_ARG;
+    if (!stack_program(r->shape, bufs, hidden_io, r->w, prog, r->engine, r->tagged)) return Q4_ERR_ARG;
     Q4_CUDA(cudaMemcpyAsync(r->w.prog, prog.data(), prog.size() * sizeof(Phase), cudaMemcpyHostToDevice, cs));
     r->cur_h = hidden_io;
   }
@@ -889,12 +1050,13 @@ extern "C" int q4_stream_layers(q4_stream* r, uint16_t* hidden_io, void* compute
                                 b < 0 ? nullptr : ev);
     } else if (b < 0 || !chunked) {
       if (b >= 0) Q4_CUDA(cudaStreamWaitEvent(cs, r->loaded[b][0], 0));
-      st = launch_layers(r->w, 4 * i, last ? 5 : 4, r->grid, cs, r->engine);
+      st = launch_layers(r->w, 4 * i, last ? 5 : 4, r->grid, cs, r->engine, r->tagged, last, r->shape);
     } else {
       // chunked: phase p of the layer starts once chunk p has landed (one launch per phase)
       for (int p = 0; p < 4 && st == Q4_OK; ++p) {
         Q4_CUDA(cudaStreamWaitEvent(cs, r->loaded[b][p], 0));
-        st = launch_layers(r->w, 4 * i + p, (last && p == 3) ? 2 : 1, r->grid, cs, r->engine);
+        st = launch_layers(r->w, 4 * i + p, (last && p == 3) ? 2 : 1, r->grid, cs, r->engine, r->tagged,
+                           last && p == 3, r->shape);
       }
     }
     if (st != Q4_OK) return st;
@@ -922,6 +1084,12 @@ extern "C" int q4_stream_layers(q4_stream* r, uint16_t* hidden_io, void* compute
 extern "C" int q4_stream_status(q4_stream* r, void* compute_stream, int* status_out) {
   if (!r || !status_out) return Q4_ERR_ARG;
   return read_status(r->w.ctl, static_cast<cudaStream_t>(compute_stream), status_out);
+}
+
+extern "C" int q4_stream_tagged(const q4_stream* r, int* tagged_out) {
+  if (!r || !tagged_out) return Q4_ERR_ARG;
+  *tagged_out = r->tagged ? 1 : 0;
+  return Q4_OK;
 }
 
 extern "C" int q4_stream_destroy(q4_stream* r) {

@@ -18,6 +18,15 @@ constexpr int kKT = 64;              // input columns each consumer thread keeps
 constexpr int kStageBytes = 32256;   // one work unit of weights in shared memory
 constexpr int kStages = 6;           // ring depth (6 * 31.5 KB = 189 KB)
 constexpr int kRedFloats = 6144;     // per-warp row partials buffered until the phase ends
+// Tagged programs stage a phase input per CTA in dynamic shared memory after
+// the ring (the buffer also holds the row partials): up to kNormMaxValues fp32
+// RMSNorm inputs or kTag16MaxValues binary16 inputs.  The ring then has 6
+// stages when the buffer takes at most kXBufMaxBytes6, else 5.
+constexpr int kNormMaxValues = 8192;
+constexpr int kTag16MaxValues = 28672;
+constexpr int kXBufMaxBytes6 = 37888;     // 6 * 32256 + 37888 = 231424 bytes
+constexpr int kXBufMaxBytes5 = 70144;     // 5 * 32256 + 70144 = 231424 bytes
+constexpr int kDynSmemMax = 231424;
 constexpr int kMaxGrid = 256;        // CTAs (one per SM) a launch may use
 constexpr int kMaxBatch = 16;
 
@@ -27,7 +36,27 @@ enum XKind : int {
   X_NORM16 = 1,   // x = f16(t * rsqrt(mean(t^2) + eps)), t = src (binary16 [batch][k])
   X_ATTN = 2,     // context-1 attention: x[i] = f16(v[(i/hd)/group*hd + i%hd]), v = fp32 src
   X_NORM32 = 3,   // as X_NORM16 with an fp32 src
+  // Tagged inputs (see TaggedWords): src holds one tagged word per value.
+  X_TAG16 = 4,       // x = the binary16 values of 32-bit words, k of them
+  X_TAG16_ATTN = 5,  // as X_ATTN over xt_n tagged binary16 values of v
+  X_TAG32_NORM = 6,  // as X_NORM32 over k tagged fp32 values (64-bit words)
 };
+
+// How a CTA takes part in the one flag exchange of a tagged layer program.
+enum SyncKind : int {
+  SYNC_NONE = 0,
+  SYNC_PUBLISH = 1,   // after its input is read, every CTA publishes the phase tag as its flag
+  SYNC_WAIT = 2,      // before writing anything, a CTA waits until every flag carries the
+                      // previous phase's tag (or a later one)
+};
+
+// Tagged words.  Inside a tagged layer program a value that one CTA hands to
+// another travels with the tag of the phase that produced it in one aligned
+// word: a binary16 value in the low half of a 32-bit word under the low 16
+// bits of the tag, or an fp32 value in the low half of a 64-bit word under the
+// 32-bit tag.  Aligned 32- and 64-bit accesses are single-copy atomic, so a
+// reader that sees the tag it expects also sees the value stored with it;
+// readers poll the words they need until every tag matches.
 
 // What the epilogue does with the row sums.
 enum EpiKind : int {
@@ -78,6 +107,13 @@ struct Phase {
   // per-phase launch, so every schedule gives bit-identical results.
   int base;
   int pad_;
+  // Tagged programs only.
+  const uint32_t* res_t;  // EPI_RESID: tagged binary16 residual input [n_rows]
+  uint32_t* xr_out;       // if not null, CTA 0 stores the formed x here as tagged binary16 [k]
+  int gidx;               // index of the phase in the whole program (its tag offset)
+  int sync;               // SyncKind
+  int xt_n;               // X_TAG16_ATTN: tagged values of v in x_src
+  int pad2_;
 };
 
 __host__ __device__ __forceinline__ int slice_t32(int e, int T) { return ((e & 63) >> 2) * T * 4 + (e >> 6) * 4 + (e & 3); }
@@ -86,13 +122,15 @@ __host__ __device__ __forceinline__ int slice_t16(int e, int T) { return ((e & 6
 // Per-launch control block in device memory (decoder workspace).
 struct Control {
   unsigned long long depart;    // CTAs that left the current launch (reset by the last one)
-  unsigned int epoch;           // launches completed; phase tags of a launch derive from it
+  unsigned int epoch;           // launches (tagged programs: whole programs) completed; the
+                                // phase tags derive from it
   int status;                   // bit flags set by kernels on a failed wait
 };
 
 // A CTA's end-of-phase flag: its sum of squares of the residual sums it wrote
 // (0 for other phases) in the low word, the phase tag in the high word.
-// flags[(p & 1) * kMaxGrid + cta] holds phase p's flag of CTA cta.
+// flags[(p & 1) * kMaxGrid + cta] holds phase p's flag of CTA cta.  Tagged
+// programs use flags[cta] alone, with a zero low word.
 constexpr unsigned kPhasesPerEpoch = 4096;
 
 // Arguments of one launch of the engine kernel: either a device array of
@@ -105,6 +143,13 @@ struct EngineArgs {
   uint32_t wait_limit;     // polls of one wait before it is declared failed
   uint32_t prefetch_bytes; // tensor-core engine: weight bytes a CTA keeps requested into L2
                            // beyond its shared-memory ring (0 = none)
+  int tagged;              // CUDA-core engine: the phases exchange tagged words (phase tag =
+                           // epoch * kPhasesPerEpoch + 1 + Phase::gidx) instead of meeting at
+                           // a flag barrier after every phase
+  int end_of_program;      // tagged: this launch runs the program's last phase, so the last
+                           // CTA to leave advances the epoch
+  int stages;              // tagged: ring depth (5 or 6)
+  int xbuf_floats;         // tagged: floats of the staging buffer after the ring
   Phase one;
 };
 
@@ -113,6 +158,7 @@ enum StatusBits : int {
   ST_FULL_TIMEOUT = 2,
   ST_EMPTY_TIMEOUT = 4,
   ST_DRAIN_TIMEOUT = 8,
+  ST_DATA_TIMEOUT = 16,    // a tagged input word never carried the expected tag
 };
 
 // ------------------------------------------------------------------ PTX
@@ -193,6 +239,37 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
 
 __device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
   asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Relaxed (morally strong, gpu scope) accesses of tagged words.  A vector
+// access is four independent 32-bit accesses, each single-copy atomic.
+__device__ __forceinline__ uint4 ld_relaxed_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed_b32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed_b32(void* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_relaxed_b64(void* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_relaxed_v4(void* p, uint4 v) {
+  asm volatile("st.relaxed.gpu.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
 }
 
 // Packed fp32x2 arithmetic (sm_100 family).
