@@ -2,7 +2,7 @@
 //
 // One CTA per SM.  Warp 15 is the producer: one lane streams the CTA's work
 // units (consecutive weight rows, contiguous in the GGUF row-major layout)
-// from HBM into a 6-deep ring of 31.5 KB shared-memory stages with 1-D bulk
+// from HBM into a 5- or 6-deep ring of 31.5 KB shared-memory stages with 1-D bulk
 // TMA copies (cp.async.bulk) whose completion is counted on one mbarrier
 // per stage.  Warps 0-14 are the consumers: each thread keeps a fixed slice
 // of 64 columns of the input vector x in registers, reads its slice of two
@@ -11,10 +11,13 @@
 // with warp shuffles; rows wider than one warp's slice leave one partial per
 // warp in shared memory, summed in a fixed order when the phase ends (no
 // barrier per unit).  The work of a launch is a list of phases
-// (matrix-vector products with an input prologue and an output epilogue);
-// consecutive phases are separated by a grid barrier, while the producer
-// keeps streaming the next phase's weights, which never depend on the
-// activations.
+// (matrix-vector products with an input prologue and an output epilogue),
+// while the producer keeps streaming the next phase's weights, which never
+// depend on the activations.  Two instantiations synchronise the phases
+// differently: engine_kernel<false> meets at a flag barrier after every
+// phase; engine_kernel<true> (tagged programs) passes every value one phase
+// hands to the next as a tagged word and has each CTA poll the words of its
+// own input, with one flag exchange per layer.
 //
 // The method: PIPO's dequantisation-free 4-bit matrix-vector product
 // ("PIPO: Pipelined Offloading for Efficient Inference on Consumer
