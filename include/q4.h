@@ -249,6 +249,19 @@ int q4_decoder_status(q4_decoder *dec, void *stream, int *status_out);
  * runs another engine or batch).  Host only.  Errors: Q4_ERR_ARG. */
 int q4_decoder_tagged(const q4_decoder *dec, int *tagged_out);
 
+/*
+ * Failure-detection hook for tests (tagged decoders, after one decode call):
+ * runs the decoder's o-projection phase alone with a wait limit of wait_limit
+ * polls.  Its tagged input was written under an earlier epoch, so no word
+ * ever carries the tag it waits for: every wait gives up after wait_limit
+ * polls, the kernel sets status bit 16 (a tagged input never arrived) and
+ * returns.  The call synchronises `stream`, reads and clears the status word
+ * into *status_out, and clears the tagged words so that the next decode call
+ * runs normally.  Errors: Q4_ERR_ARG (not a tagged decoder, no decode call
+ * yet, wait_limit 0), Q4_ERR_CUDA.
+ */
+int q4_decoder_debug_stall(q4_decoder *dec, uint32_t wait_limit, void *stream, int *status_out);
+
 int q4_decoder_destroy(q4_decoder *dec);
 
 /* ------------------------------------------------------- decoder without allocation */

@@ -137,6 +137,20 @@ def test_protocol_selection():
     assert q4.q4_decoder_tagged(Stack(WIDE, 1, seed=38).dec)
 
 
+def test_tagged_wait_runs_out_and_reports():
+    """A tagged input that never arrives: every wait gives up after its poll
+    limit, the status word carries bit 16, and the context and the decoder
+    stay usable (the next token is exact)."""
+    st = Stack(TINY, 2, seed=42)
+    h0 = synth.activations(1, TINY["hidden"], 43)
+    a = st.run(h0)
+    status = q4.q4_decoder_debug_stall(st.dec, 2000)
+    assert status & 16
+    b = st.run(h0)
+    assert np.array_equal(a, b)
+    st.close()
+
+
 def test_new_hidden_pointer_rewrites_program():
     cfg = TINY
     st = Stack(cfg, 2, seed=40)

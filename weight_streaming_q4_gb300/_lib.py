@@ -85,6 +85,7 @@ def _declare(lib):
         "q4_layer_decode_eager": ([c_p, c_p, c_p], c_int),
         "q4_decoder_status": ([c_p, c_p, ctypes.POINTER(c_int)], c_int),
         "q4_decoder_tagged": ([c_p, ctypes.POINTER(c_int)], c_int),
+        "q4_decoder_debug_stall": ([c_p, ctypes.c_uint32, c_p, ctypes.POINTER(c_int)], c_int),
         "q4_decoder_destroy": ([c_p], c_int),
         "q4_layer_decode_noalloc": ([ctypes.POINTER(LayerShape), ctypes.POINTER(c_p), c_int, c_p, c_p], c_int),
         "q4_noalloc_scratch_bytes": ([], c_size),
@@ -224,6 +225,12 @@ def q4_decoder_tagged(dec) -> bool:
     v = c_int(0)
     _check(lib().q4_decoder_tagged(dec, ctypes.byref(v)), "q4_decoder_tagged")
     return bool(v.value)
+
+
+def q4_decoder_debug_stall(dec, wait_limit, stream=None) -> int:
+    v = c_int(0)
+    _check(lib().q4_decoder_debug_stall(dec, wait_limit, _stream(stream), ctypes.byref(v)), "q4_decoder_debug_stall")
+    return v.value
 
 
 def q4_decoder_destroy(dec):

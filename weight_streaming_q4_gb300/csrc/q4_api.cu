@@ -666,14 +666,14 @@ bool batched_shape_ok(const q4_layer_shape& s) {
 // Launch phases [first_phase, first_phase + n_phases) of the program in the
 // workspace; `end` = they include the program's last phase.
 int launch_layers(const Work& w, int first_phase, int n_phases, int grid, cudaStream_t s, int engine, bool tagged,
-                  bool end, const q4_layer_shape& shape) {
+                  bool end, const q4_layer_shape& shape, uint32_t wait_limit = kWaitLimit) {
   EngineArgs a;
   memset(&a, 0, sizeof(a));
   a.phases = w.prog + first_phase;
   a.n_phases = n_phases;
   a.ctl = w.ctl;
   a.flags = w.flags;
-  a.wait_limit = kWaitLimit;
+  a.wait_limit = wait_limit;
   a.tagged = tagged ? 1 : 0;
   a.end_of_program = end ? 1 : 0;
   if (tagged) {
@@ -886,6 +886,25 @@ int run_stack_in_workspace(const q4_layer_shape* shape, const void* const* layer
 extern "C" int q4_decoder_status(q4_decoder* d, void* stream, int* status_out) {
   if (!d || !status_out) return Q4_ERR_ARG;
   return read_status(d->w.ctl, static_cast<cudaStream_t>(stream), status_out);
+}
+
+extern "C" int q4_decoder_debug_stall(q4_decoder* d, uint32_t wait_limit, void* stream, int* status_out) {
+  if (!d || !status_out || !d->tagged || !d->cur_h || wait_limit < 1) return Q4_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the o-projection phase alone: its tagged input (v) was written under an
+  // earlier epoch, so no word ever carries the tag it waits for
+  int st = launch_layers(d->w, 1, 1, d->grid, s, ENG_CORE, true, false, d->shape, wait_limit);
+  if (st != Q4_OK) return st;
+  if ((st = read_status(d->w.ctl, s, status_out)) != Q4_OK) return st;
+  // the launch left words under live tags: clear them and the flags
+  size_t off[Q4_WS_COUNT];
+  if (q4_workspace_layout(&d->shape, d->n_layers, 1, off, nullptr) != Q4_OK) return Q4_ERR_ARG;
+  char* base = reinterpret_cast<char*>(d->w.ctl) - off[Q4_WS_CONTROL];
+  Q4_CUDA(cudaMemsetAsync(base + off[Q4_WS_XT], 0,
+                          off[Q4_WS_COUNT - 1] - off[Q4_WS_XT] + 4 * static_cast<size_t>(d->shape.ffn), s));
+  Q4_CUDA(cudaMemsetAsync(d->w.flags, 0, 2 * q4::kMaxGrid * sizeof(unsigned long long), s));
+  Q4_CUDA(cudaStreamSynchronize(s));
+  return Q4_OK;
 }
 
 extern "C" int q4_decoder_tagged(const q4_decoder* d, int* tagged_out) {
