@@ -143,6 +143,48 @@ __device__ __forceinline__ float pair_dot(const uint8_t* p, const u64* xs, float
   return tot;
 }
 
+// The dot products of two rows' 64-column slices with the same x, word by
+// word for both rows so that the two rows' dependency chains interleave.
+__device__ __forceinline__ void pair_dot2(const uint8_t* pa, const uint8_t* pb, const u64* xs, float& ta, float& tb,
+                                          const Unpack& k) {
+  const uint32_t* qa = reinterpret_cast<const uint32_t*>(pa);
+  const uint32_t* qb = reinterpret_cast<const uint32_t*>(pb);
+  uint32_t A[9], B[9];
+#pragma unroll
+  for (int i = 0; i < 9; ++i) {
+    A[i] = qa[i];
+    B[i] = qb[i];
+  }
+  u64 a0 = 0, a1 = 0, b0 = 0, b1 = 0, c0 = 0, c1 = 0, e0 = 0, e1 = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t wa = __funnelshift_r(A[i], A[i + 1], 16), wb = __funnelshift_r(B[i], B[i + 1], 16);
+    if (i & 1) {
+      a1 = word_dot(wa, xs + 4 * i, a1, k);
+      c1 = word_dot(wb, xs + 4 * i, c1, k);
+    } else {
+      a0 = word_dot(wa, xs + 4 * i, a0, k);
+      c0 = word_dot(wb, xs + 4 * i, c0, k);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (i & 1) {
+      b1 = word_dot(A[5 + i], xs + 16 + 4 * i, b1, k);
+      e1 = word_dot(B[5 + i], xs + 16 + 4 * i, e1, k);
+    } else {
+      b0 = word_dot(A[5 + i], xs + 16 + 4 * i, b0, k);
+      e0 = word_dot(B[5 + i], xs + 16 + 4 * i, e0, k);
+    }
+  }
+  const float da0 = __half2float(__ushort_as_half(static_cast<unsigned short>(A[0] & 0xFFFFu)));
+  const float da1 = __half2float(__ushort_as_half(static_cast<unsigned short>(A[4] >> 16)));
+  const float db0 = __half2float(__ushort_as_half(static_cast<unsigned short>(B[0] & 0xFFFFu)));
+  const float db1 = __half2float(__ushort_as_half(static_cast<unsigned short>(B[4] >> 16)));
+  ta = fmaf(da1, hsum2(b0) + hsum2(b1), fmaf(da0, hsum2(a0) + hsum2(a1), 0.f));
+  tb = fmaf(db1, hsum2(e0) + hsum2(e1), fmaf(db0, hsum2(c0) + hsum2(c1), 0.f));
+}
+
 __device__ __forceinline__ void set_status(Control* ctl, int bits) {
   atomicOr(ctl ? &ctl->status : &g_status, bits);
 }
@@ -762,8 +804,11 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
             pa = sb + static_cast<size_t>(2 * t.team) * t.row_bytes;
             pb = pa + t.row_bytes;
           }
-          if (ra < n_rows) t0 = pair_dot(pa + static_cast<size_t>(t.j) * 36, xs2, 0.f, kk);
-          if (rb < n_rows) t1 = pair_dot(pb + static_cast<size_t>(t.j) * 36, xs2, 0.f, kk);
+          if (rb < n_rows) {
+            pair_dot2(pa + static_cast<size_t>(t.j) * 36, pb + static_cast<size_t>(t.j) * 36, xs2, t0, t1, kk);
+          } else if (ra < n_rows) {
+            t0 = pair_dot(pa + static_cast<size_t>(t.j) * 36, xs2, 0.f, kk);
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[slot]);
