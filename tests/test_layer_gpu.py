@@ -137,6 +137,20 @@ def test_protocol_selection():
     assert q4.q4_decoder_tagged(Stack(WIDE, 1, seed=38).dec)
 
 
+# hidden above the tagged staging budget (8192 fp32 norm inputs): the decoder
+# falls back to the flag-barrier program on its own
+BROAD = dict(hidden=10240, q_dim=2048, kv_dim=512, ffn=2048, head_dim=128)
+
+
+def test_wide_hidden_falls_back_to_flag_program():
+    st = Stack(BROAD, 1, seed=39)
+    assert not q4.q4_decoder_tagged(st.dec)
+    h0 = synth.activations(1, BROAD["hidden"], 40)
+    h1 = st.run(h0)
+    check_layer(BROAD, 39, 0, read_ws(st.ws, st.offs, BROAD), h1, h_in16=h0)
+    st.close()
+
+
 def test_tagged_wait_runs_out_and_reports():
     """A tagged input that never arrives: every wait gives up after its poll
     limit, the status word carries bit 16, and the context and the decoder

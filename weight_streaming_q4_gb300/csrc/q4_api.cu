@@ -640,22 +640,28 @@ int launch_layer_batched(const q4_layer_shape& sh, const uint8_t* wl, int layer,
   const int group = (Q / sh.head_dim) / (KV / sh.head_dim);
   // chunk c of the layer block (q|k|v, o, gate|up, down) must have landed before its product
   auto wait = [&](int c) { return chunk ? cudaStreamWaitEvent(s, chunk[c], 0) : cudaSuccess; };
-  if (layer == 0) Q4_CUDA(q4::glue_norm(h, nullptr, batch, H, sh.eps, w.x, s));
+  // resident weights: each launch may start (the products' weight copies)
+  // while the previous one finishes; a streamed layer waits on its copy events
+  const bool pdl = chunk == nullptr;
+  if (layer == 0) Q4_CUDA(q4::glue_norm(h, nullptr, batch, H, sh.eps, w.x, s, pdl));
   Q4_CUDA(wait(0));
-  Q4_CUDA(q4::mma_launch(wl + off[Q4_PROJ_Q], w.x, w.qkv, nqkv, H, batch, grid, kWaitLimit, &w.ctl->status, s));
-  Q4_CUDA(q4::glue_attn(w.qkv, batch, nqkv, Q, Q + KV, sh.head_dim, group, w.attn, s));
+  Q4_CUDA(q4::mma_launch(wl + off[Q4_PROJ_Q], w.x, w.qkv, nqkv, H, batch, grid, kWaitLimit, &w.ctl->status, s,
+                         nullptr, 0, pdl));
+  Q4_CUDA(q4::glue_attn(w.qkv, batch, nqkv, Q, Q + KV, sh.head_dim, group, w.attn, s, pdl));
   Q4_CUDA(wait(1));
-  Q4_CUDA(q4::mma_launch(wl + off[Q4_PROJ_O], w.attn, w.o, H, Q, batch, grid, kWaitLimit, &w.ctl->status, s));
-  Q4_CUDA(q4::glue_resid_norm(w.x, w.o, batch, H, sh.eps, w.t1, w.x2, s));
+  Q4_CUDA(q4::mma_launch(wl + off[Q4_PROJ_O], w.attn, w.o, H, Q, batch, grid, kWaitLimit, &w.ctl->status, s, nullptr,
+                         0, pdl));
+  Q4_CUDA(q4::glue_resid_norm(w.x, w.o, batch, H, sh.eps, w.t1, w.x2, s, pdl));
   Q4_CUDA(wait(2));
   // gate and up are consecutive in the block: one product of 2 ffn rows, split into g and u
   Q4_CUDA(q4::mma_launch(wl + off[Q4_PROJ_GATE], w.x2, w.g, 2 * F, H, batch, grid, kWaitLimit, &w.ctl->status, s,
-                         w.u, F));
-  Q4_CUDA(q4::glue_silu(w.g, w.u, static_cast<size_t>(batch) * F, w.act, s));
+                         w.u, F, pdl));
+  Q4_CUDA(q4::glue_silu(w.g, w.u, static_cast<size_t>(batch) * F, w.act, s, pdl));
   Q4_CUDA(wait(3));
-  Q4_CUDA(q4::mma_launch(wl + off[Q4_PROJ_DOWN], w.act, w.dn, H, F, batch, grid, kWaitLimit, &w.ctl->status, s));
+  Q4_CUDA(q4::mma_launch(wl + off[Q4_PROJ_DOWN], w.act, w.dn, H, F, batch, grid, kWaitLimit, &w.ctl->status, s,
+                         nullptr, 0, pdl));
   // the next layer's z goes to w.x; the last layer's to the caller's buffer
-  Q4_CUDA(q4::glue_resid_norm(w.x2, w.dn, batch, H, sh.eps, w.t2, layer + 1 == n_layers ? h : w.x, s));
+  Q4_CUDA(q4::glue_resid_norm(w.x2, w.dn, batch, H, sh.eps, w.t2, layer + 1 == n_layers ? h : w.x, s, pdl));
   return Q4_OK;
 }
 

@@ -287,6 +287,14 @@ __device__ __forceinline__ void st_relaxed_v4(void* p, uint4 v) {
                : "memory");
 }
 
+// Programmatic dependent launch.  griddep_launch_dependents lets the next
+// kernel of the stream (launched with programmatic stream serialisation) be
+// scheduled once every CTA of this one has issued it; griddep_wait blocks
+// until the kernels this one depends on have completed and their memory is
+// visible.  Without that launch attribute both are no-ops.
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Packed fp32x2 arithmetic (sm_100 family).
 __device__ __forceinline__ float2 f2_add(float2 a, float2 b) {
   unsigned long long ra = *reinterpret_cast<unsigned long long*>(&a);
@@ -326,16 +334,20 @@ cudaError_t tc_engine_launch(const EngineArgs& a, int grid, bool cooperative, cu
 cudaError_t tc_engine_read_status(int* out);
 cudaError_t mma_prepare();
 // y2/split: rows from `split` on go to y2 ([batch][n - split]); rows before to y ([batch][split]).
+// pdl: launch with programmatic stream serialisation (the weight copies start
+// while the previous kernel of the stream finishes; x is read after it).
 cudaError_t mma_launch(const uint8_t* w, const uint16_t* x, float* y, int n, int k, int batch, int grid,
-                       uint32_t wait_limit, int* status, cudaStream_t stream, float* y2 = nullptr, int split = 0);
+                       uint32_t wait_limit, int* status, cudaStream_t stream, float* y2 = nullptr, int split = 0,
+                       bool pdl = false);
 cudaError_t mma_read_status(int* out);
+// Glue launches; pdl as for mma_launch (each glue kernel waits for its inputs first).
 cudaError_t glue_norm(const uint16_t* src16, const float* src32, int batch, int dim, float eps, uint16_t* z,
-                      cudaStream_t s);
+                      cudaStream_t s, bool pdl = false);
 cudaError_t glue_resid_norm(const uint16_t* z, const float* o, int batch, int dim, float eps, float* t,
-                            uint16_t* z_out, cudaStream_t s);
+                            uint16_t* z_out, cudaStream_t s, bool pdl = false);
 cudaError_t glue_attn(const float* qkv, int batch, int ld, int q_dim, int v_off, int hd, int group, uint16_t* a,
-                      cudaStream_t s);
-cudaError_t glue_silu(const float* g, const float* u, size_t n, uint16_t* act, cudaStream_t s);
+                      cudaStream_t s, bool pdl = false);
+cudaError_t glue_silu(const float* g, const float* u, size_t n, uint16_t* act, cudaStream_t s, bool pdl = false);
 
 }  // namespace q4
 

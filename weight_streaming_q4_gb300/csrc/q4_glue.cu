@@ -32,6 +32,8 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 // z[b] = f16(t[b] * rsqrt(mean(t[b]^2) + eps)); t is binary16 (src16) or fp32 (src32).
 __global__ void __launch_bounds__(kGlueThreads) norm_kernel(const __half* src16, const float* src32, int dim, float eps,
                                                             __half* z) {
+  griddep_launch_dependents();
+  griddep_wait();
   __shared__ float red[kGlueThreads / 32];
   const size_t base = static_cast<size_t>(blockIdx.x) * dim;
   float ss = 0.f;
@@ -49,6 +51,8 @@ __global__ void __launch_bounds__(kGlueThreads) norm_kernel(const __half* src16,
 // t[b] = z[b] + o[b] (fp32); z_out[b] = f16(t[b] * rsqrt(mean(t[b]^2) + eps)).
 __global__ void __launch_bounds__(kGlueThreads) resid_norm_kernel(const __half* z, const float* o, int dim, float eps,
                                                                   float* t, __half* z_out) {
+  griddep_launch_dependents();
+  griddep_wait();
   __shared__ float red[kGlueThreads / 32];
   const size_t base = static_cast<size_t>(blockIdx.x) * dim;
   float ss = 0.f;
@@ -64,6 +68,8 @@ __global__ void __launch_bounds__(kGlueThreads) resid_norm_kernel(const __half* 
 // a[b][i] = f16(qkv[b][v_off + (i / hd / group) * hd + i % hd]), i < q_dim.
 __global__ void __launch_bounds__(kGlueThreads) attn_kernel(const float* qkv, int ld, int q_dim, int v_off, int hd,
                                                             int group, __half* a) {
+  griddep_launch_dependents();
+  griddep_wait();
   const size_t base = static_cast<size_t>(blockIdx.x);
   for (int i = threadIdx.x; i < q_dim; i += kGlueThreads) {
     const int src = v_off + ((i / hd) / group) * hd + (i % hd);
@@ -73,6 +79,8 @@ __global__ void __launch_bounds__(kGlueThreads) attn_kernel(const float* qkv, in
 
 // act = f16(g / (1 + exp(-g)) * u) over n values.
 __global__ void __launch_bounds__(kGlueThreads) silu_kernel(const float* g, const float* u, size_t n, __half* act) {
+  griddep_launch_dependents();
+  griddep_wait();
   for (size_t i = static_cast<size_t>(blockIdx.x) * kGlueThreads + threadIdx.x; i < n;
        i += static_cast<size_t>(gridDim.x) * kGlueThreads) {
     const float gv = g[i];
@@ -80,31 +88,41 @@ __global__ void __launch_bounds__(kGlueThreads) silu_kernel(const float* g, cons
   }
 }
 
+template <typename... P, typename... A>
+static cudaError_t glue_launch(void (*kern)(P...), unsigned grid, cudaStream_t s, bool pdl, A... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kGlueThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<P>(args)...);
+}
+
 cudaError_t glue_norm(const uint16_t* src16, const float* src32, int batch, int dim, float eps, uint16_t* z,
-                      cudaStream_t s) {
-  norm_kernel<<<batch, kGlueThreads, 0, s>>>(reinterpret_cast<const __half*>(src16), src32, dim, eps,
-                                             reinterpret_cast<__half*>(z));
-  return cudaGetLastError();
+                      cudaStream_t s, bool pdl) {
+  return glue_launch(norm_kernel, batch, s, pdl, reinterpret_cast<const __half*>(src16), src32, dim, eps,
+                     reinterpret_cast<__half*>(z));
 }
 
 cudaError_t glue_resid_norm(const uint16_t* z, const float* o, int batch, int dim, float eps, float* t,
-                            uint16_t* z_out, cudaStream_t s) {
-  resid_norm_kernel<<<batch, kGlueThreads, 0, s>>>(reinterpret_cast<const __half*>(z), o, dim, eps, t,
-                                                   reinterpret_cast<__half*>(z_out));
-  return cudaGetLastError();
+                            uint16_t* z_out, cudaStream_t s, bool pdl) {
+  return glue_launch(resid_norm_kernel, batch, s, pdl, reinterpret_cast<const __half*>(z), o, dim, eps, t,
+                     reinterpret_cast<__half*>(z_out));
 }
 
 cudaError_t glue_attn(const float* qkv, int batch, int ld, int q_dim, int v_off, int hd, int group, uint16_t* a,
-                      cudaStream_t s) {
-  attn_kernel<<<batch, kGlueThreads, 0, s>>>(qkv, ld, q_dim, v_off, hd, group, reinterpret_cast<__half*>(a));
-  return cudaGetLastError();
+                      cudaStream_t s, bool pdl) {
+  return glue_launch(attn_kernel, batch, s, pdl, qkv, ld, q_dim, v_off, hd, group, reinterpret_cast<__half*>(a));
 }
 
-cudaError_t glue_silu(const float* g, const float* u, size_t n, uint16_t* act, cudaStream_t s) {
+cudaError_t glue_silu(const float* g, const float* u, size_t n, uint16_t* act, cudaStream_t s, bool pdl) {
   const size_t blocks = (n + kGlueThreads - 1) / kGlueThreads;
-  silu_kernel<<<static_cast<unsigned>(blocks < 1024 ? blocks : 1024), kGlueThreads, 0, s>>>(
-      g, u, n, reinterpret_cast<__half*>(act));
-  return cudaGetLastError();
+  return glue_launch(silu_kernel, static_cast<unsigned>(blocks < 1024 ? blocks : 1024), s, pdl, g, u, n,
+                     reinterpret_cast<__half*>(act));
 }
 
 }  // namespace q4

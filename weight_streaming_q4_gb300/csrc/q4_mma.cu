@@ -14,9 +14,11 @@
 // Persistent, one CTA per SM, 17 warps: warp 16 streams 16-row x 2048-column
 // tiles of the weights into a ring of shared-memory stages with 1-D bulk TMA
 // copies (one per row segment, rows padded to keep the code-word loads free of
-// bank conflicts); warps 0-15 each take 4 of the stage's 64 blocks.  A row
-// tile's partial sums stay in registers across its column chunks and are
-// summed over the 16 warps in a fixed order when the tile ends.
+// bank conflicts); warps 0-15 each take 4 of the stage's 64 blocks.  A CTA
+// takes its row tiles in groups (8 tiles at batch <= 8, 4 above): chunk by
+// chunk, the x fragments of a warp's blocks are loaded once for the whole
+// group, every tile's partial sums stay in registers, and each tile is summed
+// over the 16 warps in a fixed order when the group ends.
 #include <cuda_fp16.h>
 #include <stdint.h>
 
@@ -56,6 +58,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const __grid_consta
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x, cta = blockIdx.x;
   const int nb = a.k / kQK;                                   // blocks per row
+  griddep_launch_dependents();
   const int chunks = (nb + kMmaChunkBlocks - 1) / kMmaChunkBlocks;
   const int tiles = (a.n + 15) / 16;
   const uint32_t row_bytes = static_cast<uint32_t>(nb) * kBlockBytes;
@@ -70,29 +73,38 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const __grid_consta
   }
   __syncthreads();
 
+  // The CTA's row tiles (cta, cta + G, ...) are taken in groups of TG: for
+  // each column chunk the producer copies the chunk of every tile of the
+  // group, so the consumers load that chunk's x fragments once per group and
+  // keep every tile's partial sums in registers.
+  constexpr int TG = NT == 1 ? 8 : 4;
   if (warp == kMmaWarps) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t it = 0;
-      for (int tile = cta; tile < tiles && !abort_flag; tile += G) {
-        const int row0 = tile * 16;
-        const int rows = min(16, a.n - row0);
-        for (int c = 0; c < chunks; ++c) {
-          const int stage = it % kMmaStages;
-          const uint32_t n = it / kMmaStages;
-          if (n > 0 && !mbar_wait_bounded(&empty_bar[stage], (n - 1) & 1, a.wait_limit)) {
-            atomicOr(a.status, ST_EMPTY_TIMEOUT);
-            abort_flag = 1;
-            break;
-          }
+      for (int g0 = cta; g0 < tiles && !abort_flag; g0 += G * TG) {
+        for (int c = 0; c < chunks && !abort_flag; ++c) {
           const int blk0 = c * kMmaChunkBlocks;
           const uint32_t seg = static_cast<uint32_t>(min(kMmaChunkBlocks, nb - blk0)) * kBlockBytes;
-          uint8_t* dst = g_mma_ring + static_cast<size_t>(stage) * kMmaStageBytes;
-          mbar_arrive_expect_tx(&full_bar[stage], seg * rows);
-          for (int r = 0; r < rows; ++r)
-            bulk_g2s(dst + r * kMmaRowPitch, a.w + static_cast<size_t>(row0 + r) * row_bytes + blk0 * kBlockBytes, seg,
-                     &full_bar[stage]);
-          ++it;
+          for (int q = 0; q < TG; ++q) {
+            const int tile = g0 + q * G;
+            if (tile >= tiles) break;
+            const int row0 = tile * 16;
+            const int rows = min(16, a.n - row0);
+            const int stage = it % kMmaStages;
+            const uint32_t n = it / kMmaStages;
+            if (n > 0 && !mbar_wait_bounded(&empty_bar[stage], (n - 1) & 1, a.wait_limit)) {
+              atomicOr(a.status, ST_EMPTY_TIMEOUT);
+              abort_flag = 1;
+              break;
+            }
+            uint8_t* dst = g_mma_ring + static_cast<size_t>(stage) * kMmaStageBytes;
+            mbar_arrive_expect_tx(&full_bar[stage], seg * rows);
+            for (int r = 0; r < rows; ++r)
+              bulk_g2s(dst + r * kMmaRowPitch, a.w + static_cast<size_t>(row0 + r) * row_bytes + blk0 * kBlockBytes,
+                       seg, &full_bar[stage]);
+            ++it;
+          }
         }
       }
       const uint32_t issued = it;
@@ -103,76 +115,100 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const __grid_consta
     }
   } else {
     // ------------------------------------------------------------ consumers
+    // the weights need nothing from the previous kernel; x and y do
+    griddep_wait();
     const int g = lane >> 2, t = lane & 3;
     uint32_t magic;
     asm volatile("mov.b32 %0, 0x64006400;" : "=r"(magic));
     uint32_t it = 0;
-    for (int tile = cta; tile < tiles; tile += G) {
-      float acc[NT][4];
+    for (int g0 = cta; g0 < tiles; g0 += G * TG) {
+      const int ntg = min(TG, (tiles - g0 + G - 1) / G);   // tiles in this group
+      float acc[TG][NT][4];
 #pragma unroll
-      for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+      for (int q = 0; q < TG; ++q)
+#pragma unroll
+        for (int j = 0; j < NT; ++j) acc[q][j][0] = acc[q][j][1] = acc[q][j][2] = acc[q][j][3] = 0.f;
       for (int c = 0; c < chunks; ++c) {
-        const int stage = it % kMmaStages;
-        const uint32_t n = it / kMmaStages;
-        if (!abort_flag && !mbar_wait_bounded(&full_bar[stage], n & 1, a.wait_limit)) {
-          atomicOr(a.status, ST_FULL_TIMEOUT);
-          abort_flag = 1;
-        }
-        const uint8_t* sb = g_mma_ring + static_cast<size_t>(stage) * kMmaStageBytes;
-        const uint8_t* rg = sb + g * kMmaRowPitch;
-        const uint8_t* rh = sb + (g + 8) * kMmaRowPitch;
         const int nblk = min(kMmaChunkBlocks, nb - c * kMmaChunkBlocks);
+        // this warp's blocks of the chunk: their x fragments, once for the group
+        uint32_t xf[kMmaChunkBlocks / kMmaWarps][NT][4];
 #pragma unroll
         for (int i = 0; i < kMmaChunkBlocks / kMmaWarps; ++i) {
-          const int b = warp + kMmaWarps * i;       // block within the chunk (parity = warp parity)
-          if (b < nblk) {
-            const int blk = c * kMmaChunkBlocks + b;
-            uint32_t gl02, gl13, gh02, gh13, hl02, hl13, hh02, hh13;
-            unpack_word(code_word(rg, b, t), magic, gl02, gl13, gh02, gh13);
-            unpack_word(code_word(rh, b, t), magic, hl02, hl13, hh02, hh13);
-            const float dg = row_scale(rg, b), dh = row_scale(rh, b);
+          const int b = warp + kMmaWarps * i;
 #pragma unroll
-            for (int j = 0; j < NT; ++j) {
-              uint32_t s0b0, s0b1, s1b0, s1b1;
-              x_frags(a.x, a.k, a.batch, 8 * j + g, blk, t, s0b0, s0b1, s1b0, s1b1);
-              float cb[4] = {0.f, 0.f, 0.f, 0.f};
-              mma16816(cb, gl02, hl02, gl13, hl13, s0b0, s0b1);
-              mma16816(cb, gh02, hh02, gh13, hh13, s1b0, s1b1);
-              acc[j][0] = fmaf(dg, cb[0], acc[j][0]);
-              acc[j][1] = fmaf(dg, cb[1], acc[j][1]);
-              acc[j][2] = fmaf(dh, cb[2], acc[j][2]);
-              acc[j][3] = fmaf(dh, cb[3], acc[j][3]);
-            }
+          for (int j = 0; j < NT; ++j) {
+            if (b < nblk)
+              x_frags(a.x, a.k, a.batch, 8 * j + g, c * kMmaChunkBlocks + b, t, xf[i][j][0], xf[i][j][1],
+                      xf[i][j][2], xf[i][j][3]);
+            else
+              xf[i][j][0] = xf[i][j][1] = xf[i][j][2] = xf[i][j][3] = 0u;
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[stage]);
-        ++it;
-      }
-      // the 16 warps' partial sums of this row tile, summed in a fixed order
 #pragma unroll
-      for (int j = 0; j < NT; ++j)
+        for (int q = 0; q < TG; ++q) {
+          if (q >= ntg) break;
+          const int stage = it % kMmaStages;
+          const uint32_t n = it / kMmaStages;
+          if (!abort_flag && !mbar_wait_bounded(&full_bar[stage], n & 1, a.wait_limit)) {
+            atomicOr(a.status, ST_FULL_TIMEOUT);
+            abort_flag = 1;
+          }
+          const uint8_t* sb = g_mma_ring + static_cast<size_t>(stage) * kMmaStageBytes;
+          const uint8_t* rg = sb + g * kMmaRowPitch;
+          const uint8_t* rh = sb + (g + 8) * kMmaRowPitch;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) red[warp][lane][4 * j + e] = acc[j][e];
-      named_bar_sync(1, kMmaWarps * 32);
-      const int row0 = tile * 16;
-      for (int o = tid; o < 16 * 8 * NT; o += kMmaWarps * 32) {
-        const int m = o % 16, col = o / 16;           // output row in the tile, batch column
-        const int j = col / 8, cc = col % 8;
-        // C fragment: lane (gm, tc) holds rows gm and gm+8, columns 2tc and 2tc+1
-        const int ln = (m % 8) * 4 + cc / 2;
-        const int e = (m >= 8 ? 2 : 0) + (cc & 1);
-        float s = 0.f;
-        for (int w = 0; w < kMmaWarps; ++w) s += red[w][ln][4 * j + e];
-        const int r = row0 + m;
-        if (col < a.batch && r < a.n) {
-          if (r < a.split)
-            a.y[static_cast<size_t>(col) * a.split + r] = s;
-          else
-            a.y2[static_cast<size_t>(col) * (a.n - a.split) + (r - a.split)] = s;
+          for (int i = 0; i < kMmaChunkBlocks / kMmaWarps; ++i) {
+            const int b = warp + kMmaWarps * i;       // block within the chunk (parity = warp parity)
+            if (b < nblk) {
+              uint32_t gl02, gl13, gh02, gh13, hl02, hl13, hh02, hh13;
+              unpack_word(code_word(rg, b, t), magic, gl02, gl13, gh02, gh13);
+              unpack_word(code_word(rh, b, t), magic, hl02, hl13, hh02, hh13);
+              const float dg = row_scale(rg, b), dh = row_scale(rh, b);
+#pragma unroll
+              for (int j = 0; j < NT; ++j) {
+                float cb[4] = {0.f, 0.f, 0.f, 0.f};
+                mma16816(cb, gl02, hl02, gl13, hl13, xf[i][j][0], xf[i][j][1]);
+                mma16816(cb, gh02, hh02, gh13, hh13, xf[i][j][2], xf[i][j][3]);
+                acc[q][j][0] = fmaf(dg, cb[0], acc[q][j][0]);
+                acc[q][j][1] = fmaf(dg, cb[1], acc[q][j][1]);
+                acc[q][j][2] = fmaf(dh, cb[2], acc[q][j][2]);
+                acc[q][j][3] = fmaf(dh, cb[3], acc[q][j][3]);
+              }
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty_bar[stage]);
+          ++it;
         }
       }
-      named_bar_sync(1, kMmaWarps * 32);
+      // each tile's 16 warps' partial sums, summed in a fixed order
+#pragma unroll
+      for (int q = 0; q < TG; ++q) {
+        if (q >= ntg) break;
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) red[warp][lane][4 * j + e] = acc[q][j][e];
+        named_bar_sync(1, kMmaWarps * 32);
+        const int row0 = (g0 + q * G) * 16;
+        for (int o = tid; o < 16 * 8 * NT; o += kMmaWarps * 32) {
+          const int m = o % 16, col = o / 16;           // output row in the tile, batch column
+          const int j = col / 8, cc = col % 8;
+          // C fragment: lane (gm, tc) holds rows gm and gm+8, columns 2tc and 2tc+1
+          const int ln = (m % 8) * 4 + cc / 2;
+          const int e = (m >= 8 ? 2 : 0) + (cc & 1);
+          float s = 0.f;
+          for (int w = 0; w < kMmaWarps; ++w) s += red[w][ln][4 * j + e];
+          const int r = row0 + m;
+          if (col < a.batch && r < a.n) {
+            if (r < a.split)
+              a.y[static_cast<size_t>(col) * a.split + r] = s;
+            else
+              a.y2[static_cast<size_t>(col) * (a.n - a.split) + (r - a.split)] = s;
+          }
+        }
+        named_bar_sync(1, kMmaWarps * 32);
+      }
     }
   }
   __syncthreads();
@@ -194,7 +230,7 @@ cudaError_t mma_prepare() {
 }
 
 cudaError_t mma_launch(const uint8_t* w, const uint16_t* x, float* y, int n, int k, int batch, int grid,
-                       uint32_t wait_limit, int* status, cudaStream_t stream, float* y2, int split) {
+                       uint32_t wait_limit, int* status, cudaStream_t stream, float* y2, int split, bool pdl) {
   MmaArgs a;
   a.y2 = y2;
   a.split = (y2 && split > 0 && split < n) ? split : n;
@@ -212,11 +248,17 @@ cudaError_t mma_launch(const uint8_t* w, const uint16_t* x, float* y, int n, int
   a.wait_limit = wait_limit;
   const int tiles = (n + 15) / 16;
   if (grid > tiles) grid = tiles;
-  if (batch <= 8)
-    mma_kernel<1><<<grid, kMmaThreads, kMmaStages * kMmaStageBytes, stream>>>(a);
-  else
-    mma_kernel<2><<<grid, kMmaThreads, kMmaStages * kMmaStageBytes, stream>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kMmaThreads);
+  cfg.dynamicSmemBytes = kMmaStages * kMmaStageBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return batch <= 8 ? cudaLaunchKernelEx(&cfg, mma_kernel<1>, a) : cudaLaunchKernelEx(&cfg, mma_kernel<2>, a);
 }
 
 }  // namespace q4
