@@ -221,6 +221,8 @@ typedef struct q4_decoder q4_decoder;
  *                  tensor-core: head_dim % 4 == 0, hidden, q_dim, ffn multiples
  *                  of 256 up to 30720); batch 2..16 runs one tensor-core product
  *                  launch per projection with glue launches between them
+ *                  (hidden, q_dim, ffn multiples of 256; kv_dim, head_dim
+ *                  multiples of 4)
  *   stream         used for the workspace initialisation (synchronised)
  * Errors: Q4_ERR_ARG, Q4_ERR_ALIGN, Q4_ERR_OOM (workspace too small), Q4_ERR_CUDA.
  */

@@ -666,7 +666,8 @@ int launch_layer_batched(const q4_layer_shape& sh, const uint8_t* wl, int layer,
 }
 
 bool batched_shape_ok(const q4_layer_shape& s) {
-  return s.hidden % 256 == 0 && s.q_dim % 256 == 0 && s.ffn % 256 == 0 && (s.q_dim + 2 * s.kv_dim) > 0;
+  return s.hidden % 256 == 0 && s.q_dim % 256 == 0 && s.ffn % 256 == 0 && (s.q_dim + 2 * s.kv_dim) > 0 &&
+         s.kv_dim % 4 == 0 && s.head_dim % 4 == 0;   // the glue moves 4 values at a time
 }
 
 // Launch phases [first_phase, first_phase + n_phases) of the program in the

@@ -14,8 +14,11 @@
 
 namespace q4 {
 
-constexpr int kGlueThreads = 256;
+constexpr int kGlueThreads = 256;    // element-wise kernels
+constexpr int kNormThreads = 1024;   // one CTA per batch row for the RMSNorms
 
+// Sum of v over the CTA (T threads), the same fixed order in every CTA.
+template <int T>
 __device__ __forceinline__ float block_sum(float v, float* red) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -24,56 +27,88 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   __syncthreads();
   float s = 0.f;
 #pragma unroll
-  for (int i = 0; i < kGlueThreads / 32; ++i) s += red[i];
+  for (int i = 0; i < T / 32; ++i) s += red[i];
   __syncthreads();
   return s;
 }
 
-// z[b] = f16(t[b] * rsqrt(mean(t[b]^2) + eps)); t is binary16 (src16) or fp32 (src32).
-__global__ void __launch_bounds__(kGlueThreads) norm_kernel(const __half* src16, const float* src32, int dim, float eps,
+__device__ __forceinline__ float4 load_h4(const __half* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
+__device__ __forceinline__ void store_h4(__half* p, float4 v, float r) {
+  const __half2 a = __floats2half2_rn(v.x * r, v.y * r);
+  const __half2 b = __floats2half2_rn(v.z * r, v.w * r);
+  uint2 u;
+  u.x = *reinterpret_cast<const uint32_t*>(&a);
+  u.y = *reinterpret_cast<const uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
+// z[b] = f16(t[b] * rsqrt(mean(t[b]^2) + eps)); t is binary16 (src16) or fp32
+// (src32); dim a multiple of 4.  One CTA per batch row, 4 values per thread
+// and step.
+__global__ void __launch_bounds__(kNormThreads) norm_kernel(const __half* src16, const float* src32, int dim, float eps,
                                                             __half* z) {
   griddep_launch_dependents();
   griddep_wait();
-  __shared__ float red[kGlueThreads / 32];
+  __shared__ float red[kNormThreads / 32];
   const size_t base = static_cast<size_t>(blockIdx.x) * dim;
   float ss = 0.f;
-  for (int i = threadIdx.x; i < dim; i += kGlueThreads) {
-    const float v = src16 ? __half2float(src16[base + i]) : src32[base + i];
-    ss = fmaf(v, v, ss);
+  for (int i = 4 * threadIdx.x; i < dim; i += 4 * kNormThreads) {
+    const float4 v = src16 ? load_h4(src16 + base + i) : *reinterpret_cast<const float4*>(src32 + base + i);
+    ss = fmaf(v.x, v.x, ss);
+    ss = fmaf(v.y, v.y, ss);
+    ss = fmaf(v.z, v.z, ss);
+    ss = fmaf(v.w, v.w, ss);
   }
-  const float r = rsqrtf(block_sum(ss, red) / static_cast<float>(dim) + eps);
-  for (int i = threadIdx.x; i < dim; i += kGlueThreads) {
-    const float v = src16 ? __half2float(src16[base + i]) : src32[base + i];
-    z[base + i] = __float2half_rn(v * r);
+  const float r = rsqrtf(block_sum<kNormThreads>(ss, red) / static_cast<float>(dim) + eps);
+  for (int i = 4 * threadIdx.x; i < dim; i += 4 * kNormThreads) {
+    const float4 v = src16 ? load_h4(src16 + base + i) : *reinterpret_cast<const float4*>(src32 + base + i);
+    store_h4(z + base + i, v, r);
   }
 }
 
 // t[b] = z[b] + o[b] (fp32); z_out[b] = f16(t[b] * rsqrt(mean(t[b]^2) + eps)).
-__global__ void __launch_bounds__(kGlueThreads) resid_norm_kernel(const __half* z, const float* o, int dim, float eps,
+// dim a multiple of 4; one CTA per batch row.
+__global__ void __launch_bounds__(kNormThreads) resid_norm_kernel(const __half* z, const float* o, int dim, float eps,
                                                                   float* t, __half* z_out) {
   griddep_launch_dependents();
   griddep_wait();
-  __shared__ float red[kGlueThreads / 32];
+  __shared__ float red[kNormThreads / 32];
   const size_t base = static_cast<size_t>(blockIdx.x) * dim;
   float ss = 0.f;
-  for (int i = threadIdx.x; i < dim; i += kGlueThreads) {
-    const float v = __half2float(z[base + i]) + o[base + i];
-    t[base + i] = v;
-    ss = fmaf(v, v, ss);
+  for (int i = 4 * threadIdx.x; i < dim; i += 4 * kNormThreads) {
+    const float4 a = load_h4(z + base + i);
+    const float4 b = *reinterpret_cast<const float4*>(o + base + i);
+    const float4 v = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+    *reinterpret_cast<float4*>(t + base + i) = v;
+    ss = fmaf(v.x, v.x, ss);
+    ss = fmaf(v.y, v.y, ss);
+    ss = fmaf(v.z, v.z, ss);
+    ss = fmaf(v.w, v.w, ss);
   }
-  const float r = rsqrtf(block_sum(ss, red) / static_cast<float>(dim) + eps);
-  for (int i = threadIdx.x; i < dim; i += kGlueThreads) z_out[base + i] = __float2half_rn(t[base + i] * r);
+  const float r = rsqrtf(block_sum<kNormThreads>(ss, red) / static_cast<float>(dim) + eps);
+  for (int i = 4 * threadIdx.x; i < dim; i += 4 * kNormThreads)
+    store_h4(z_out + base + i, *reinterpret_cast<const float4*>(t + base + i), r);
 }
 
-// a[b][i] = f16(qkv[b][v_off + (i / hd / group) * hd + i % hd]), i < q_dim.
+// a[b][i] = f16(qkv[b][v_off + (i / hd / group) * hd + i % hd]), i < q_dim;
+// 4 consecutive outputs per thread (hd, ld, v_off multiples of 4), the grid
+// spread over the batch rows and the output.
 __global__ void __launch_bounds__(kGlueThreads) attn_kernel(const float* qkv, int ld, int q_dim, int v_off, int hd,
-                                                            int group, __half* a) {
+                                                            int group, int batch, __half* a) {
   griddep_launch_dependents();
   griddep_wait();
-  const size_t base = static_cast<size_t>(blockIdx.x);
-  for (int i = threadIdx.x; i < q_dim; i += kGlueThreads) {
+  const int per_row = q_dim / 4;
+  for (int e = blockIdx.x * kGlueThreads + threadIdx.x; e < batch * per_row; e += gridDim.x * kGlueThreads) {
+    const int b = e / per_row, i = 4 * (e % per_row);
     const int src = v_off + ((i / hd) / group) * hd + (i % hd);
-    a[base * q_dim + i] = __float2half_rn(qkv[base * ld + src]);
+    const float4 v = *reinterpret_cast<const float4*>(qkv + static_cast<size_t>(b) * ld + src);
+    store_h4(a + static_cast<size_t>(b) * q_dim + i, v, 1.0f);
   }
 }
 
@@ -89,10 +124,11 @@ __global__ void __launch_bounds__(kGlueThreads) silu_kernel(const float* g, cons
 }
 
 template <typename... P, typename... A>
-static cudaError_t glue_launch(void (*kern)(P...), unsigned grid, cudaStream_t s, bool pdl, A... args) {
+static cudaError_t glue_launch(void (*kern)(P...), unsigned grid, unsigned threads, cudaStream_t s, bool pdl,
+                               A... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kGlueThreads);
+  cfg.blockDim = dim3(threads);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -104,24 +140,30 @@ static cudaError_t glue_launch(void (*kern)(P...), unsigned grid, cudaStream_t s
 
 cudaError_t glue_norm(const uint16_t* src16, const float* src32, int batch, int dim, float eps, uint16_t* z,
                       cudaStream_t s, bool pdl) {
-  return glue_launch(norm_kernel, batch, s, pdl, reinterpret_cast<const __half*>(src16), src32, dim, eps,
+  if (dim % 4) return cudaErrorInvalidValue;
+  return glue_launch(norm_kernel, batch, kNormThreads, s, pdl, reinterpret_cast<const __half*>(src16), src32, dim, eps,
                      reinterpret_cast<__half*>(z));
 }
 
 cudaError_t glue_resid_norm(const uint16_t* z, const float* o, int batch, int dim, float eps, float* t,
                             uint16_t* z_out, cudaStream_t s, bool pdl) {
-  return glue_launch(resid_norm_kernel, batch, s, pdl, reinterpret_cast<const __half*>(z), o, dim, eps, t,
-                     reinterpret_cast<__half*>(z_out));
+  if (dim % 4) return cudaErrorInvalidValue;
+  return glue_launch(resid_norm_kernel, batch, kNormThreads, s, pdl, reinterpret_cast<const __half*>(z), o, dim, eps,
+                     t, reinterpret_cast<__half*>(z_out));
 }
 
 cudaError_t glue_attn(const float* qkv, int batch, int ld, int q_dim, int v_off, int hd, int group, uint16_t* a,
                       cudaStream_t s, bool pdl) {
-  return glue_launch(attn_kernel, batch, s, pdl, qkv, ld, q_dim, v_off, hd, group, reinterpret_cast<__half*>(a));
+  if (hd % 4 || ld % 4 || v_off % 4 || q_dim % 4) return cudaErrorInvalidValue;
+  const int work = batch * (q_dim / 4);
+  const int grid = (work + kGlueThreads - 1) / kGlueThreads;
+  return glue_launch(attn_kernel, static_cast<unsigned>(grid < 1024 ? grid : 1024), kGlueThreads, s, pdl, qkv, ld,
+                     q_dim, v_off, hd, group, batch, reinterpret_cast<__half*>(a));
 }
 
 cudaError_t glue_silu(const float* g, const float* u, size_t n, uint16_t* act, cudaStream_t s, bool pdl) {
   const size_t blocks = (n + kGlueThreads - 1) / kGlueThreads;
-  return glue_launch(silu_kernel, static_cast<unsigned>(blocks < 1024 ? blocks : 1024), s, pdl, g, u, n,
+  return glue_launch(silu_kernel, static_cast<unsigned>(blocks < 1024 ? blocks : 1024), kGlueThreads, s, pdl, g, u, n,
                      reinterpret_cast<__half*>(act));
 }
 
