@@ -287,14 +287,6 @@ __device__ __forceinline__ void st_relaxed_v4(void* p, uint4 v) {
                : "memory");
 }
 
-// Programmatic dependent launch.  griddep_launch_dependents lets the next
-// kernel of the stream (launched with programmatic stream serialisation) be
-// scheduled once every CTA of this one has issued it; griddep_wait blocks
-// until the kernels this one depends on have completed and their memory is
-// visible.  Without that launch attribute both are no-ops.
-__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
 // Packed fp32x2 arithmetic (sm_100 family).
 __device__ __forceinline__ float2 f2_add(float2 a, float2 b) {
   unsigned long long ra = *reinterpret_cast<unsigned long long*>(&a);

@@ -10,6 +10,14 @@
 
 namespace q4 {
 
+// Programmatic dependent launch.  griddep_launch_dependents lets the next
+// kernel of the stream (launched with programmatic stream serialisation) be
+// scheduled once every CTA of this one has issued it; griddep_wait blocks
+// until the kernels this one depends on have completed and their memory is
+// visible.  Without that launch attribute both are no-ops.
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void mma16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                                          uint32_t b1) {
   asm volatile(

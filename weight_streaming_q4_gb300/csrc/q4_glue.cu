@@ -11,6 +11,7 @@
 #include <stdint.h>
 
 #include "q4_device.cuh"
+#include "q4_frag.cuh"
 
 namespace q4 {
 
