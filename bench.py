@@ -24,6 +24,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -57,16 +58,24 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(text: bytes) -> bytes:
+    """Source text without comments and with whitespace runs collapsed, so that
+    a documentation-only edit does not mark a profile stale."""
+    text = re.sub(rb"/\*.*?\*/", b" ", text, flags=re.S)
+    text = re.sub(rb"//[^\n]*", b" ", text)
+    return re.sub(rb"\s+", b" ", text).strip()
+
+
 def kernel_source_hash(kernel: str = "engine_kernel") -> str:
     """Hash of the device code a kernel is built from (the shared header up to
-    its host-side declarations)."""
+    its host-side declarations), comments and layout excluded."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "weight_streaming_q4_gb300", "csrc", f), "rb") as fh:
             text = fh.read()
         if f == "q4_device.cuh":
             text = text.split(b"// Host-side launchers")[0]
-        h.update(text)
+        h.update(_code_only(text))
     return h.hexdigest()[:16]
 
 
