@@ -588,8 +588,8 @@ __device__ void flush_rows_tagged(const Phase& ph, const Tile& t, const float* r
 }
 
 // flush_rows_tagged for the rare flush in the middle of a phase (its partial
-// buffer is full).  Kept inline: an out-of-line call inside the unit loop made
-// ptxas keep the loop's registers in local memory.
+// buffer is full).  Kept inline: an out-of-line call inside the unit loop
+// would add register saves around it.
 __device__ __forceinline__ void flush_rows_tagged_mid(const Phase& ph, const Tile& t, const float* red, int n_buf,
                                                    int u_first, int G, int tid, uint32_t tag, uint32_t limit,
                                                    Control* ctl) {
