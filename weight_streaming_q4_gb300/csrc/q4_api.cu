@@ -645,9 +645,10 @@ int launch_layer_batched(const q4_layer_shape& sh, const uint8_t* wl, int layer,
   const bool pdl = chunk == nullptr;
   if (layer == 0) Q4_CUDA(q4::glue_norm(h, nullptr, batch, H, sh.eps, w.x, s, pdl));
   Q4_CUDA(wait(0));
+  // the v rows of q|k|v also go out as the context-1 attention output a (binary16, gathered per head)
+  const q4::MmaGather gather{w.attn, Q + KV, KV, sh.head_dim, group, Q};
   Q4_CUDA(q4::mma_launch(wl + off[Q4_PROJ_Q], w.x, w.qkv, nqkv, H, batch, grid, kWaitLimit, &w.ctl->status, s,
-                         nullptr, 0, pdl));
-  Q4_CUDA(q4::glue_attn(w.qkv, batch, nqkv, Q, Q + KV, sh.head_dim, group, w.attn, s, pdl));
+                         nullptr, 0, pdl, &gather));
   Q4_CUDA(wait(1));
   Q4_CUDA(q4::mma_launch(wl + off[Q4_PROJ_O], w.attn, w.o, H, Q, batch, grid, kWaitLimit, &w.ctl->status, s, nullptr,
                          0, pdl));

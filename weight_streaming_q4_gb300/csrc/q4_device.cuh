@@ -326,19 +326,27 @@ cudaError_t tc_engine_launch(const EngineArgs& a, int grid, bool cooperative, cu
 cudaError_t tc_engine_read_status(int* out);
 cudaError_t mma_prepare();
 // y2/split: rows from `split` on go to y2 ([batch][n - split]); rows before to y ([batch][split]).
+// Rows [lo, lo + n_rows) of a product's output taken as value heads of head_dim
+// rows each and also written, rounded to binary16, as the context-1 attention
+// output: value row lo + vh * head_dim + i goes to out[b][(vh * group + h) *
+// head_dim + i] for h < group (out has ld values per batch row).
+struct MmaGather {
+  uint16_t* out;
+  int lo, n_rows, head_dim, group, ld;
+};
+
 // pdl: launch with programmatic stream serialisation (the weight copies start
 // while the previous kernel of the stream finishes; x is read after it).
+// gather: optional second output of some rows (see MmaGather).
 cudaError_t mma_launch(const uint8_t* w, const uint16_t* x, float* y, int n, int k, int batch, int grid,
                        uint32_t wait_limit, int* status, cudaStream_t stream, float* y2 = nullptr, int split = 0,
-                       bool pdl = false);
+                       bool pdl = false, const MmaGather* gather = nullptr);
 cudaError_t mma_read_status(int* out);
 // Glue launches; pdl as for mma_launch (each glue kernel waits for its inputs first).
 cudaError_t glue_norm(const uint16_t* src16, const float* src32, int batch, int dim, float eps, uint16_t* z,
                       cudaStream_t s, bool pdl = false);
 cudaError_t glue_resid_norm(const uint16_t* z, const float* o, int batch, int dim, float eps, float* t,
                             uint16_t* z_out, cudaStream_t s, bool pdl = false);
-cudaError_t glue_attn(const float* qkv, int batch, int ld, int q_dim, int v_off, int hd, int group, uint16_t* a,
-                      cudaStream_t s, bool pdl = false);
 cudaError_t glue_silu(const float* g, const float* u, size_t n, uint16_t* act, cudaStream_t s, bool pdl = false);
 
 }  // namespace q4

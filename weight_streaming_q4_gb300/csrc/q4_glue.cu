@@ -1,9 +1,9 @@
 // Decoder-layer glue between the projections, for batches of more than one
-// row (one CTA per batch row).  The batch-1 path folds the same steps into the
+// row.  (The context-1 attention gather is written by the q|k|v product's
+// epilogue itself.)  The batch-1 path folds the same steps into the
 // prologues and epilogues of the persistent engine; these kernels give the
 // same arithmetic as separate launches around the tensor-core product:
 //   norm          z  = f16(t / sqrt(mean(t^2) + eps))        (t binary16 or fp32)
-//   attention     a  = f16(v of the value head each query head is grouped with)
 //   resid_norm    t  = z + o (fp32);  z' = f16(t / sqrt(mean(t^2) + eps))
 //   silu_mul      act = f16(silu(g) * u)
 // Reductions run in a fixed order, so results do not depend on timing.
@@ -97,22 +97,6 @@ __global__ void __launch_bounds__(kNormThreads) resid_norm_kernel(const __half* 
     store_h4(z_out + base + i, *reinterpret_cast<const float4*>(t + base + i), r);
 }
 
-// a[b][i] = f16(qkv[b][v_off + (i / hd / group) * hd + i % hd]), i < q_dim;
-// 4 consecutive outputs per thread (hd, ld, v_off multiples of 4), the grid
-// spread over the batch rows and the output.
-__global__ void __launch_bounds__(kGlueThreads) attn_kernel(const float* qkv, int ld, int q_dim, int v_off, int hd,
-                                                            int group, int batch, __half* a) {
-  griddep_launch_dependents();
-  griddep_wait();
-  const int per_row = q_dim / 4;
-  for (int e = blockIdx.x * kGlueThreads + threadIdx.x; e < batch * per_row; e += gridDim.x * kGlueThreads) {
-    const int b = e / per_row, i = 4 * (e % per_row);
-    const int src = v_off + ((i / hd) / group) * hd + (i % hd);
-    const float4 v = *reinterpret_cast<const float4*>(qkv + static_cast<size_t>(b) * ld + src);
-    store_h4(a + static_cast<size_t>(b) * q_dim + i, v, 1.0f);
-  }
-}
-
 // act = f16(g / (1 + exp(-g)) * u) over n values.
 __global__ void __launch_bounds__(kGlueThreads) silu_kernel(const float* g, const float* u, size_t n, __half* act) {
   griddep_launch_dependents();
@@ -151,15 +135,6 @@ cudaError_t glue_resid_norm(const uint16_t* z, const float* o, int batch, int di
   if (dim % 4) return cudaErrorInvalidValue;
   return glue_launch(resid_norm_kernel, batch, kNormThreads, s, pdl, reinterpret_cast<const __half*>(z), o, dim, eps,
                      t, reinterpret_cast<__half*>(z_out));
-}
-
-cudaError_t glue_attn(const float* qkv, int batch, int ld, int q_dim, int v_off, int hd, int group, uint16_t* a,
-                      cudaStream_t s, bool pdl) {
-  if (hd % 4 || ld % 4 || v_off % 4 || q_dim % 4) return cudaErrorInvalidValue;
-  const int work = batch * (q_dim / 4);
-  const int grid = (work + kGlueThreads - 1) / kGlueThreads;
-  return glue_launch(attn_kernel, static_cast<unsigned>(grid < 1024 ? grid : 1024), kGlueThreads, s, pdl, qkv, ld,
-                     q_dim, v_off, hd, group, batch, reinterpret_cast<__half*>(a));
 }
 
 cudaError_t glue_silu(const float* g, const float* u, size_t n, uint16_t* act, cudaStream_t s, bool pdl) {

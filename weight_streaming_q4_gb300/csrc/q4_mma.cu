@@ -44,6 +44,7 @@ struct MmaArgs {
   int n, k, batch, split;
   uint32_t wait_limit;
   int* status;        // where timed-out waits are recorded (g_status_mma if none given)
+  MmaGather gather;   // gather.out null: none
 };
 
 extern __shared__ __align__(128) uint8_t g_mma_ring[];
@@ -205,6 +206,13 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const __grid_consta
               a.y[static_cast<size_t>(col) * a.split + r] = s;
             else
               a.y2[static_cast<size_t>(col) * (a.n - a.split) + (r - a.split)] = s;
+            const MmaGather& gt = a.gather;
+            if (gt.out && r >= gt.lo && r < gt.lo + gt.n_rows) {
+              const int vh = (r - gt.lo) / gt.head_dim, i = (r - gt.lo) % gt.head_dim;
+              const unsigned short hv = __half_as_ushort(__float2half_rn(s));
+              for (int h = 0; h < gt.group; ++h)
+                gt.out[static_cast<size_t>(col) * gt.ld + (vh * gt.group + h) * gt.head_dim + i] = hv;
+            }
           }
         }
         named_bar_sync(1, kMmaWarps * 32);
@@ -230,8 +238,11 @@ cudaError_t mma_prepare() {
 }
 
 cudaError_t mma_launch(const uint8_t* w, const uint16_t* x, float* y, int n, int k, int batch, int grid,
-                       uint32_t wait_limit, int* status, cudaStream_t stream, float* y2, int split, bool pdl) {
+                       uint32_t wait_limit, int* status, cudaStream_t stream, float* y2, int split, bool pdl,
+                       const MmaGather* gather) {
   MmaArgs a;
+  a.gather = gather ? *gather : MmaGather{nullptr, 0, 0, 1, 0, 0};
+  if (a.gather.out && (a.gather.head_dim < 1 || a.gather.group < 1)) return cudaErrorInvalidValue;
   a.y2 = y2;
   a.split = (y2 && split > 0 && split < n) ? split : n;
   if (!status) {
