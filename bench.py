@@ -236,8 +236,8 @@ def run_stack(args, torch, q4, model, synth, stream, barrier, gpu_index):
     q4.q4_decoder_destroy(dec)
     nbytes = layer_bytes * n_layers
     # batch 1: one persistent launch per token; batch B: per layer 4 tensor-core
-    # products + 3 glue launches, plus the first layer's input norm
-    launches = 1 if B == 1 else 7 * n_layers + 1
+    # products + 2 glue launches, plus the first layer's input norm
+    launches = 1 if B == 1 else 6 * n_layers + 1
     return dict(secs=secs, clocks=clocks, bytes_per_step=nbytes, launches_per_step=launches,
                 kernel_launches_per_step=1 if B == 1 else 4 * n_layers,
                 e2e_secs=e2e_secs, e2e_steps=e2e_steps, h2d=h0.numel() * 2, d2h=h0.numel() * 2,
@@ -440,7 +440,7 @@ def run_stream(args, torch, q4, model, synth, stream, barrier, gpu_index):
             f"{'chunked' if head['chunked'] else 'merged'} copies, batch {B}")
     out = dict(secs=head["secs"], clocks=head["clocks"], bytes_per_step=layer_bytes * n_layers,
                streamed_bytes_per_step=layer_bytes * (n_layers - head["resident_layers"]),
-               launches_per_step=n_layers if B == 1 else 7 * n_layers + 1,
+               launches_per_step=n_layers if B == 1 else 6 * n_layers + 1,
                kernel_launches_per_step=n_layers if B == 1 else 4 * n_layers,
                steps_override=steps, warmup_override=warm, h2d_peak_gbs=best,
                e2e_secs=e2e_secs, e2e_steps=e2e_steps, h2d=h0.numel() * 2, d2h=h0.numel() * 2,

@@ -655,9 +655,9 @@ int launch_layer_batched(const q4_layer_shape& sh, const uint8_t* wl, int layer,
   Q4_CUDA(q4::glue_resid_norm(w.x, w.o, batch, H, sh.eps, w.t1, w.x2, s, pdl));
   Q4_CUDA(wait(2));
   // gate and up are consecutive in the block: one product of 2 ffn rows, split into g and u
+  // (each tile pairs 8 rows of gate with the same 8 rows of up, so its epilogue also forms act)
   Q4_CUDA(q4::mma_launch(wl + off[Q4_PROJ_GATE], w.x2, w.g, 2 * F, H, batch, grid, kWaitLimit, &w.ctl->status, s,
-                         w.u, F, pdl));
-  Q4_CUDA(q4::glue_silu(w.g, w.u, static_cast<size_t>(batch) * F, w.act, s, pdl));
+                         w.u, F, pdl, nullptr, w.act));
   Q4_CUDA(wait(3));
   Q4_CUDA(q4::mma_launch(wl + off[Q4_PROJ_DOWN], w.act, w.dn, H, F, batch, grid, kWaitLimit, &w.ctl->status, s,
                          nullptr, 0, pdl));

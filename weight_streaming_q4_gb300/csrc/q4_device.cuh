@@ -338,16 +338,18 @@ struct MmaGather {
 // pdl: launch with programmatic stream serialisation (the weight copies start
 // while the previous kernel of the stream finishes; x is read after it).
 // gather: optional second output of some rows (see MmaGather).
+// act: gate|up pairing.  The n rows are two matrices of n/2 rows (split =
+// n/2, y2 given); each 16-row tile takes 8 rows of the first and the same 8
+// rows of the second, and the epilogue also writes act = f16(silu(y) * y2).
 cudaError_t mma_launch(const uint8_t* w, const uint16_t* x, float* y, int n, int k, int batch, int grid,
                        uint32_t wait_limit, int* status, cudaStream_t stream, float* y2 = nullptr, int split = 0,
-                       bool pdl = false, const MmaGather* gather = nullptr);
+                       bool pdl = false, const MmaGather* gather = nullptr, uint16_t* act = nullptr);
 cudaError_t mma_read_status(int* out);
 // Glue launches; pdl as for mma_launch (each glue kernel waits for its inputs first).
 cudaError_t glue_norm(const uint16_t* src16, const float* src32, int batch, int dim, float eps, uint16_t* z,
                       cudaStream_t s, bool pdl = false);
 cudaError_t glue_resid_norm(const uint16_t* z, const float* o, int batch, int dim, float eps, float* t,
                             uint16_t* z_out, cudaStream_t s, bool pdl = false);
-cudaError_t glue_silu(const float* g, const float* u, size_t n, uint16_t* act, cudaStream_t s, bool pdl = false);
 
 }  // namespace q4
 

@@ -1,11 +1,11 @@
 // Decoder-layer glue between the projections, for batches of more than one
-// row.  (The context-1 attention gather is written by the q|k|v product's
-// epilogue itself.)  The batch-1 path folds the same steps into the
-// prologues and epilogues of the persistent engine; these kernels give the
-// same arithmetic as separate launches around the tensor-core product:
+// row.  The context-1 attention gather and the SiLU-gated product are written
+// by the epilogues of the q|k|v and gate|up products themselves; the batch-1
+// path folds the same steps into the prologues and epilogues of the
+// persistent engine.  These kernels are the RMSNorms, as separate launches
+// around the tensor-core products:
 //   norm          z  = f16(t / sqrt(mean(t^2) + eps))        (t binary16 or fp32)
 //   resid_norm    t  = z + o (fp32);  z' = f16(t / sqrt(mean(t^2) + eps))
-//   silu_mul      act = f16(silu(g) * u)
 // Reductions run in a fixed order, so results do not depend on timing.
 #include <cuda_fp16.h>
 #include <stdint.h>
@@ -97,17 +97,6 @@ __global__ void __launch_bounds__(kNormThreads) resid_norm_kernel(const __half* 
     store_h4(z_out + base + i, *reinterpret_cast<const float4*>(t + base + i), r);
 }
 
-// act = f16(g / (1 + exp(-g)) * u) over n values.
-__global__ void __launch_bounds__(kGlueThreads) silu_kernel(const float* g, const float* u, size_t n, __half* act) {
-  griddep_launch_dependents();
-  griddep_wait();
-  for (size_t i = static_cast<size_t>(blockIdx.x) * kGlueThreads + threadIdx.x; i < n;
-       i += static_cast<size_t>(gridDim.x) * kGlueThreads) {
-    const float gv = g[i];
-    act[i] = __float2half_rn(gv / (1.0f + expf(-gv)) * u[i]);
-  }
-}
-
 template <typename... P, typename... A>
 static cudaError_t glue_launch(void (*kern)(P...), unsigned grid, unsigned threads, cudaStream_t s, bool pdl,
                                A... args) {
@@ -135,12 +124,6 @@ cudaError_t glue_resid_norm(const uint16_t* z, const float* o, int batch, int di
   if (dim % 4) return cudaErrorInvalidValue;
   return glue_launch(resid_norm_kernel, batch, kNormThreads, s, pdl, reinterpret_cast<const __half*>(z), o, dim, eps,
                      t, reinterpret_cast<__half*>(z_out));
-}
-
-cudaError_t glue_silu(const float* g, const float* u, size_t n, uint16_t* act, cudaStream_t s, bool pdl) {
-  const size_t blocks = (n + kGlueThreads - 1) / kGlueThreads;
-  return glue_launch(silu_kernel, static_cast<unsigned>(blocks < 1024 ? blocks : 1024), kGlueThreads, s, pdl, g, u, n,
-                     reinterpret_cast<__half*>(act));
 }
 
 }  // namespace q4

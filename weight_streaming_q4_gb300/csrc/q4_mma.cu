@@ -45,6 +45,7 @@ struct MmaArgs {
   uint32_t wait_limit;
   int* status;        // where timed-out waits are recorded (g_status_mma if none given)
   MmaGather gather;   // gather.out null: none
+  __half* act;        // gate|up pairing (see mma_launch), or null
 };
 
 extern __shared__ __align__(128) uint8_t g_mma_ring[];
@@ -61,7 +62,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const __grid_consta
   const int nb = a.k / kQK;                                   // blocks per row
   griddep_launch_dependents();
   const int chunks = (nb + kMmaChunkBlocks - 1) / kMmaChunkBlocks;
-  const int tiles = (a.n + 15) / 16;
+  // paired gate|up: tile t holds rows [8t, 8t + 8) of both halves
+  const bool paired = a.act != nullptr;
+  const int half = a.n / 2;
+  const int tiles = paired ? (half + 7) / 8 : (a.n + 15) / 16;
   const uint32_t row_bytes = static_cast<uint32_t>(nb) * kBlockBytes;
 
   if (tid == 0) {
@@ -90,8 +94,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const __grid_consta
           for (int q = 0; q < TG; ++q) {
             const int tile = g0 + q * G;
             if (tile >= tiles) break;
-            const int row0 = tile * 16;
-            const int rows = min(16, a.n - row0);
+            const int row0 = paired ? tile * 8 : tile * 16;
+            const int rows = paired ? min(8, half - row0) : min(16, a.n - row0);
             const int stage = it % kMmaStages;
             const uint32_t n = it / kMmaStages;
             if (n > 0 && !mbar_wait_bounded(&empty_bar[stage], (n - 1) & 1, a.wait_limit)) {
@@ -100,10 +104,15 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const __grid_consta
               break;
             }
             uint8_t* dst = g_mma_ring + static_cast<size_t>(stage) * kMmaStageBytes;
-            mbar_arrive_expect_tx(&full_bar[stage], seg * rows);
+            mbar_arrive_expect_tx(&full_bar[stage], seg * rows * (paired ? 2 : 1));
             for (int r = 0; r < rows; ++r)
               bulk_g2s(dst + r * kMmaRowPitch, a.w + static_cast<size_t>(row0 + r) * row_bytes + blk0 * kBlockBytes,
                        seg, &full_bar[stage]);
+            if (paired)
+              for (int r = 0; r < rows; ++r)
+                bulk_g2s(dst + (8 + r) * kMmaRowPitch,
+                         a.w + static_cast<size_t>(half + row0 + r) * row_bytes + blk0 * kBlockBytes, seg,
+                         &full_bar[stage]);
             ++it;
           }
         }
@@ -191,6 +200,29 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const __grid_consta
 #pragma unroll
           for (int e = 0; e < 4; ++e) red[warp][lane][4 * j + e] = acc[q][j][e];
         named_bar_sync(1, kMmaWarps * 32);
+        if (paired) {
+          // row m of the first half and row m of the second are rows m and m + 8 of the tile
+          const int row0 = (g0 + q * G) * 8;
+          for (int o = tid; o < 8 * 8 * NT; o += kMmaWarps * 32) {
+            const int m = o % 8, col = o / 8;
+            const int j = col / 8, cc = col % 8;
+            const int ln = m * 4 + cc / 2, e = cc & 1;
+            float gv = 0.f, uv = 0.f;
+            for (int w = 0; w < kMmaWarps; ++w) {
+              gv += red[w][ln][4 * j + e];
+              uv += red[w][ln][4 * j + 2 + e];
+            }
+            const int r = row0 + m;
+            if (col < a.batch && r < half) {
+              const size_t i = static_cast<size_t>(col) * half + r;
+              a.y[i] = gv;
+              a.y2[i] = uv;
+              a.act[i] = __float2half_rn(gv / (1.0f + expf(-gv)) * uv);
+            }
+          }
+          named_bar_sync(1, kMmaWarps * 32);
+          continue;
+        }
         const int row0 = (g0 + q * G) * 16;
         for (int o = tid; o < 16 * 8 * NT; o += kMmaWarps * 32) {
           const int m = o % 16, col = o / 16;           // output row in the tile, batch column
@@ -239,9 +271,11 @@ cudaError_t mma_prepare() {
 
 cudaError_t mma_launch(const uint8_t* w, const uint16_t* x, float* y, int n, int k, int batch, int grid,
                        uint32_t wait_limit, int* status, cudaStream_t stream, float* y2, int split, bool pdl,
-                       const MmaGather* gather) {
+                       const MmaGather* gather, uint16_t* act) {
   MmaArgs a;
   a.gather = gather ? *gather : MmaGather{nullptr, 0, 0, 1, 0, 0};
+  a.act = reinterpret_cast<__half*>(act);
+  if (act && (!y2 || n % 2 || split != n / 2)) return cudaErrorInvalidValue;
   if (a.gather.out && (a.gather.head_dim < 1 || a.gather.group < 1)) return cudaErrorInvalidValue;
   a.y2 = y2;
   a.split = (y2 && split > 0 && split < n) ? split : n;
@@ -257,7 +291,7 @@ cudaError_t mma_launch(const uint8_t* w, const uint16_t* x, float* y, int n, int
   a.k = k;
   a.batch = batch;
   a.wait_limit = wait_limit;
-  const int tiles = (n + 15) / 16;
+  const int tiles = act ? (n / 2 + 7) / 8 : (n + 15) / 16;
   if (grid > tiles) grid = tiles;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
