@@ -45,3 +45,22 @@ def test_two_replicas_take_the_slowest_rank():
     for rank, worst, gbs in got:
         assert worst == 0.75                       # both ranks see the slowest rank's time
         assert gbs == pytest.approx(2 * 1e9 / 0.075 / 1e9)   # two replicas' bytes over that time
+
+
+def _bench_module():
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_mod_hash", os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    return bench
+
+
+def test_profile_hash_ignores_comments_not_code():
+    """A profile's traffic stays valid across documentation edits of the kernel
+    source, and goes stale when the code itself changes."""
+    bench = _bench_module()
+    src = b"__device__ int f(int a) {\n  return a + 1;  // one more\n}\n"
+    doc = b"// what f does\n__device__ int f(int a) {\n  /* unchanged */ return a + 1;\n}\n"
+    code = b"__device__ int f(int a) {\n  return a + 2;\n}\n"
+    assert bench._code_only(src) == bench._code_only(doc)
+    assert bench._code_only(src) != bench._code_only(code)
