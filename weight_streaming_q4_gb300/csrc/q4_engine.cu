@@ -824,7 +824,14 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
           const int half = width >> 1;
           const bool upper = (lane & half) != 0;
           float r = (upper ? t1 : t0) + __shfl_xor_sync(0xffffffffu, upper ? t0 : t1, half);
-          for (int o = half >> 1; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+          if (width == 32) {   // the common case (teams of 32 or more threads), unrolled
+            r += __shfl_xor_sync(0xffffffffu, r, 8);
+            r += __shfl_xor_sync(0xffffffffu, r, 4);
+            r += __shfl_xor_sync(0xffffffffu, r, 2);
+            r += __shfl_xor_sync(0xffffffffu, r, 1);
+          } else {
+            for (int o = half >> 1; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+          }
           if (((lane & (width - 1)) & ~half) == 0) {   // lane 0 (row 0) and lane `half` (row 1) of the group
             const int slot = n_buf * t.spu + 2 * t.team + (upper ? 1 : 0);
             red[slot * t.tw + t.w_in_team] = r;
