@@ -243,7 +243,10 @@ int q4_layer_decode(q4_decoder *dec, uint16_t *hidden_io, void *stream);
 int q4_layer_decode_eager(q4_decoder *dec, uint16_t *hidden_io, void *stream);
 
 /* Status word of the decoder's kernels (synchronises `stream`): 0 = every
- * wait completed; otherwise bit flags; clears it.  Errors: Q4_ERR_CUDA. */
+ * wait completed; otherwise bit flags, clears it.  Bits: 1 a phase flag never
+ * came, 2 a weight copy never landed, 4 a ring stage was never released, 8 a
+ * copy was still in flight at exit, 16 a tagged input word never carried its
+ * tag.  Results of a call that set a bit are not valid.  Errors: Q4_ERR_CUDA. */
 int q4_decoder_status(q4_decoder *dec, void *stream, int *status_out);
 
 /* *tagged_out = 1 if the decoder's batch-1 CUDA-core engine passes tagged
