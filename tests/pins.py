@@ -295,6 +295,72 @@ def pin_glue(lib):
     assert np.array_equal(att.ravel(), expect)
 
 
+
+def _q4_matrix_of(n: int, k: int, row_fn) -> np.ndarray:
+    """A hand-built row-major Q4_0 matrix: row_fn(row) gives (d_bits, codes[k])."""
+    rows = []
+    for r in range(n):
+        d_bits, codes = row_fn(r)
+        codes = np.asarray(codes, dtype=np.int64)
+        for b in range(k // 32):
+            c = codes[32 * b:32 * b + 32]
+            rows.append(_block(d_bits, (c[:16] | (c[16:] << 4)).astype(np.uint8)))
+    return np.concatenate(rows)
+
+
+def _codes(k: int, col0: int | None = None, q0: int = 8, fill: int = 8) -> np.ndarray:
+    c = np.full(k, fill, dtype=np.int64)
+    if col0 is not None:
+        c[col0] = q0
+    return c
+
+
+def pin_layer_wiring(lib):
+    """Which tensor feeds which step of ora_layer, by closed forms.
+
+    Hand-built weights make every intermediate a known small number (z = 1
+    everywhere, d a power of two), so the layer output follows by hand:
+      A. v = 2 (Wv rows: one code 10 at column 0, d = 1), o = (a[0], 0, ...)
+         (Wo row 0: one code 9 at column 0), Wq and Wk random, Wdown zero:
+         the context-1 attention copies v, so t1 = z + o = (3, 1, ..., 1),
+         z1 = f16(t1 r) with r = 1/sqrt((9 + 63)/64 + eps), and t2 = z1.
+         Reading k or q for the attention, feeding z to Wo, or taking z as
+         the feed-forward residual base all change t2.
+      B. Wv zero (so t1 = z and z1 = f16(1/sqrt(1 + eps)) = 1), gate rows all
+         code 3 with d = 1/16 (g = -5/16 * 64 = -20), up rows all code 9 with
+         d = 1/64 (u = 1), Wdown row 0 one code 9 at column 0 (dn = (act[0], 0,
+         ...)): act[0] = f16(silu(-20) * 1) = -2^-24 (silu(-20) = -4.12e-8, the
+         nearest binary16 is the negative smallest subnormal), so
+         t2 = (1 - 2^-24, 1, ..., 1) and every output is binary16 1.0.  With
+         gate and up swapped act[0] = f16(silu(1) * -20) = -14.6; with Wdown
+         fed z1 instead of act, t2[0] = 2.
+    """
+    hid, qd, kvd, ffn, hd = 64, 64, 32, 128, 16
+    eps = 1e-5
+    one = int(_f16(1.0))
+    zero = lambda n, k: _q4_matrix_of(n, k, lambda r: (one, _codes(k)))
+    rnd = lambda n, k, p: synth.q4_matrix(n, k, 4, p)
+    z = np.full((1, hid), one, dtype=np.uint16)
+    # A
+    wv = _q4_matrix_of(kvd, hid, lambda r: (one, _codes(hid, 0, 10)))
+    wo = _q4_matrix_of(hid, qd, lambda r: (one, _codes(qd, 0, 9) if r == 0 else _codes(qd)))
+    wts = [rnd(qd, hid, 0), rnd(kvd, hid, 1), wv, wo, rnd(ffn, hid, 4), rnd(ffn, hid, 5), zero(hid, ffn)]
+    zo, t2 = ora.layer(wts, z, 1, hid, qd, kvd, ffn, hd, eps, lib=lib)
+    r = 1.0 / np.sqrt((9.0 + 63.0) / 64.0 + eps)
+    expect = np.concatenate([[3.0 * r], np.full(hid - 1, r)]).astype(np.float16).astype(np.float64)
+    assert np.array_equal(t2[0], expect), "A: t2 = f16(norm(z + Wo gather(v)))"
+    # B
+    d16, d64 = int(_f16(1 / 16)), int(_f16(1 / 64))
+    wg = _q4_matrix_of(ffn, hid, lambda r: (d16, _codes(hid, fill=3)))
+    wu = _q4_matrix_of(ffn, hid, lambda r: (d64, _codes(hid, fill=9)))
+    wd = _q4_matrix_of(hid, ffn, lambda r: (one, _codes(ffn, 0, 9) if r == 0 else _codes(ffn)))
+    wts = [rnd(qd, hid, 0), rnd(kvd, hid, 1), zero(kvd, hid), rnd(hid, qd, 3), wg, wu, wd]
+    zo, t2 = ora.layer(wts, z, 1, hid, qd, kvd, ffn, hd, eps, lib=lib)
+    assert t2[0, 0] == 1.0 - 2.0 ** -24, f"B: t2[0] = 1 + f16(silu(g) u), got {t2[0, 0]!r}"
+    assert np.all(t2[0, 1:] == 1.0), "B: rows of Wdown with no code read nothing"
+    assert np.all(zo == one), "B: output f16(norm(t2)) is 1.0 everywhere"
+
+
 def pin_attn_decode(lib):
     """Decode attention over a KV cache: closed forms of the softmax."""
     rng = np.random.default_rng(11)
@@ -351,4 +417,4 @@ def pin_attn_decode(lib):
 
 ALL_PINS = [pin_attn_decode, pin_half_decode_exhaustive, pin_half_encode, pin_golden_blocks, pin_distinct_positions,
             pin_block_indexing, pin_golden_gemv, pin_all_eight_is_zero, pin_single_nonzero,
-            pin_constant_codes, pin_brute_force, pin_invariants, pin_glue]
+            pin_constant_codes, pin_brute_force, pin_invariants, pin_glue, pin_layer_wiring]

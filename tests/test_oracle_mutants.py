@@ -40,6 +40,18 @@ MUTANTS = {
     "attn_group_modulo": ("int64_t g = h / group;", "int64_t g = h % n_kv;"),
     "attn_cache_stride": ("kc[t * kv_dim + g * head_dim + i]", "kc[t * head_dim + g * head_dim + i]"),
     "attn_signed_sabs": ("aabs += work[t] / den * fabs(v);", "aabs += work[t] / den * v;"),
+    "gate_up_swap": ("ora_silu_mul(g, u, (int64_t)batch * ffn, act);", "ora_silu_mul(u, g, (int64_t)batch * ffn, act);"),
+    "attn_reads_k": ("ora_attn_ctx1(v, batch, q_dim, kv_dim, head_dim, attn);",
+                     "ora_attn_ctx1(k, batch, q_dim, kv_dim, head_dim, attn);"),
+    "o_reads_z": ("ora_gemv(wts[3], attn, hidden, q_dim, batch, 0, hidden, o, 0);",
+                  "ora_gemv(wts[3], z, hidden, q_dim, batch, 0, hidden, o, 0);"),
+    "down_reads_z1": ("ora_gemv(wts[6], act, hidden, ffn, batch, 0, hidden, dn, 0);",
+                      "ora_gemv(wts[6], z1, hidden, ffn, batch, 0, hidden, dn, 0);"),
+    "ffn_residual_base_z": ("ora_add(z1, dn, (int64_t)batch * hidden, t2);", "ora_add(z, dn, (int64_t)batch * hidden, t2);"),
+    "attn_residual_base_dropped": ("ora_add(z, o, (int64_t)batch * hidden, t1);",
+                                   "ora_add(z1, o, (int64_t)batch * hidden, t1);"),
+    "k_weights_for_v": ("ora_gemv(wts[2], z, kv_dim, hidden, batch, 0, kv_dim, v, 0);",
+                        "ora_gemv(wts[1], z, kv_dim, hidden, batch, 0, kv_dim, v, 0);"),
     "attn_value_key_swap": ("double v = ora_half_to_double(vc[t * kv_dim + g * head_dim + i]);",
                             "double v = ora_half_to_double(kc[t * kv_dim + g * head_dim + i]);"),
 }
