@@ -54,6 +54,7 @@ def peaks():
 
 KERNEL_SOURCES = {
     "engine_kernel": ("q4_engine.cu", "q4_device.cuh", "q4_phase.cuh"),
+    "tc_engine_kernel": ("q4_tc_engine.cu", "q4_frag.cuh", "q4_device.cuh", "q4_phase.cuh"),
     "mma_kernel": ("q4_mma.cu", "q4_frag.cuh", "q4_device.cuh"),
 }
 
@@ -199,7 +200,8 @@ def run_stack(args, torch, q4, model, synth, stream, barrier, gpu_index):
     wbuf, ptrs = model.resident_layers(shape, n_layers, seed=0)
     ws, offs, ws_bytes = model.workspace(shape, n_layers, B)
     with torch.cuda.stream(stream):
-        mode = q4.Q4_DEC_FUSED | (q4.Q4_DEC_BARRIER if args.barrier else 0)
+        mode = q4.Q4_DEC_FUSED | (q4.Q4_DEC_BARRIER if args.barrier else 0) | (
+            q4.Q4_DEC_CUDA_CORE if args.cuda_core else 0)
         dec = q4.q4_decoder_create(shape, ptrs, B, ws, ws_bytes, mode, stream=stream)
         h0 = torch.from_numpy(synth.activations(B, cfg["hidden"], 0).reshape(-1).view("int16").copy())
         h = h0.cuda()
@@ -243,8 +245,11 @@ def run_stack(args, torch, q4, model, synth, stream, barrier, gpu_index):
                 e2e_secs=e2e_secs, e2e_steps=e2e_steps, h2d=h0.numel() * 2, d2h=h0.numel() * 2,
                 workload=(f"{'8B' if args.config == '8b' else '70B'}-shaped decoder stack, {n_layers} layers, "
                           f"batch {B}, HBM-resident, one CUDA-graph replay per step"),
-                kernel="engine_kernel" if B == 1 else "mma_kernel",
-                kernel_key=f"engine_kernel:{args.config}_stack" if B == 1 else f"mma_kernel:{args.config}_stack_b{B}",
+                kernel=(("engine_kernel" if args.barrier or args.cuda_core else "tc_engine_kernel") if B == 1
+                        else "mma_kernel"),
+                kernel_key=((f"engine_kernel:{args.config}_stack" if args.barrier or args.cuda_core
+                             else f"tc_engine_kernel:{args.config}_stack") if B == 1
+                            else f"mma_kernel:{args.config}_stack_b{B}"),
                 n_layers=n_layers, cfg=cfg, tagged=tagged)
 
 
@@ -293,7 +298,7 @@ def run_gemv(args, torch, q4, model, synth, stream, barrier, gpu_index):
     return dict(secs=secs, clocks=clocks, bytes_per_step=mb * copies, launches_per_step=copies,
                 e2e_secs=e2e_secs, e2e_steps=e2e_steps, e2e_bytes_per_step=mb, h2d=2 * k, d2h=4 * n,
                 workload=f"single Q4_0 product N=K=4096, batch 1, ring of {copies} weight copies (> L2)",
-                kernel_key="engine_kernel:gemv", cfg=dict(n=n, k=k, copies=copies))
+                kernel="tc_engine_kernel", kernel_key="tc_engine_kernel:gemv", cfg=dict(n=n, k=k, copies=copies))
 
 
 def run_stream(args, torch, q4, model, synth, stream, barrier, gpu_index):
@@ -394,7 +399,8 @@ def run_stream(args, torch, q4, model, synth, stream, barrier, gpu_index):
             keep = set(resident_set(n_layers, R, pat))
             host = [0 if i in keep else hptrs[i] for i in range(n_layers)]
             res = [dptrs[i] if i in keep else 0 for i in range(n_layers)]
-            flags = (q4.Q4_STREAM_CHUNKED if chunked else 0) | (q4.Q4_STREAM_BARRIER if args.barrier else 0)
+            flags = (q4.Q4_STREAM_CHUNKED if chunked else 0) | (q4.Q4_STREAM_BARRIER if args.barrier else 0) | (
+                q4.Q4_STREAM_CUDA_CORE if args.cuda_core else 0)
             ring = q4.q4_stream_create_ex(shape, host, res, B, bufs[0], bufs[1], stride, ws, ws_bytes, flags)
 
             def step():
@@ -667,6 +673,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--layers", type=int, default=0, help="run only this many layers of the stack (profiling)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline (profiling runs)")
+    ap.add_argument("--cuda-core", action="store_true",
+                    help="batch-1 stacks and rings: the CUDA-core engine instead of the tensor-core one (comparison)")
     ap.add_argument("--barrier", action="store_true",
                     help="batch-1 stacks: flag barrier after every phase instead of tagged words (comparison)")
     args = ap.parse_args()

@@ -85,8 +85,9 @@ size_t q4_matrix_bytes(int n, int k);
 #define Q4_KERNEL_STREAM 1   /* persistent TMA-ring kernel, CUDA-core exact products (batch 1) */
 #define Q4_KERNEL_SIMPLE 2   /* one warp per row, plain loads (any k % 32 == 0, any batch) */
 #define Q4_KERNEL_MMA 3      /* persistent TMA-ring kernel, tensor-core products (batch 1..16) */
-#define Q4_KERNEL_TC 4       /* the decoder's persistent tensor-core engine, one phase (batch 1,
-                                k % 256 == 0, k <= 30720) */
+#define Q4_KERNEL_TC 4       /* persistent tensor-core engine, one phase (batch 1, k % 256 == 0 and
+                                k <= 2048 or k % 2048 == 0, k <= 30720); what q4_gemv uses at
+                                batch 1 for those widths */
 
 /*
  * y[b][n] = sum_k W[n][k] * x[b][k], W dequantisation-free from its Q4_0 blocks
@@ -199,12 +200,15 @@ typedef struct q4_decoder q4_decoder;
 
 #define Q4_DEC_FUSED 0      /* the whole stack is one persistent launch (one graph node) */
 #define Q4_DEC_PER_LAYER 1  /* one launch per layer (one graph node per layer) */
-#define Q4_DEC_TENSOR_CORE 2  /* or-ed into the mode: batch 1 runs the tensor-core engine
-                                 (q4_tc_engine) instead of the exact CUDA-core engine */
-#define Q4_DEC_BARRIER 4    /* or-ed into the mode: the batch-1 CUDA-core engine meets at a flag
-                               barrier after every phase instead of passing tagged words (the
-                               default whenever hidden <= 9600 and kv_dim <= 14336); the two
-                               agree within the product error bound, not bit for bit */
+#define Q4_DEC_TENSOR_CORE 2  /* or-ed into the mode: batch 1 must run the tensor-core engine
+                                 (the default whenever the shape allows it; Q4_ERR_ARG if not) */
+#define Q4_DEC_BARRIER 4    /* or-ed into the mode: batch 1 runs the CUDA-core engine meeting at a
+                               flag barrier after every phase instead of passing tagged words */
+#define Q4_DEC_CUDA_CORE 8  /* or-ed into the mode: batch 1 runs the exact CUDA-core engine
+                               (tagged words between phases when the shape allows) instead of
+                               the tensor-core engine.  The engines and the two phase
+                               synchronisations agree within the product error bound, not bit
+                               for bit */
 
 /*
  * Create a decoder over n_layers HBM-resident layers and capture its CUDA
@@ -214,15 +218,15 @@ typedef struct q4_decoder q4_decoder;
  *   n_layers       1..1023; batch: 1 <= batch <= 16
  *   workspace      device, >= q4_workspace_layout() bytes, 256-byte aligned;
  *                  owned by the caller, must outlive the decoder
- *   mode           Q4_DEC_FUSED or Q4_DEC_PER_LAYER, optionally | Q4_DEC_TENSOR_CORE
- *                  and | Q4_DEC_BARRIER.
- *                  Batch 1 runs one persistent engine (CUDA-core by default:
- *                  head_dim % 64 == 0 and the widths of Q4_KERNEL_STREAM;
- *                  tensor-core: head_dim % 4 == 0, hidden, q_dim, ffn multiples
- *                  of 256 up to 30720); batch 2..16 runs one tensor-core product
- *                  launch per projection with glue launches between them
- *                  (hidden, q_dim, ffn multiples of 256; kv_dim, head_dim
- *                  multiples of 4)
+ *   mode           Q4_DEC_FUSED or Q4_DEC_PER_LAYER, optionally | Q4_DEC_TENSOR_CORE,
+ *                  | Q4_DEC_CUDA_CORE or | Q4_DEC_BARRIER.
+ *                  Batch 1 runs one persistent engine: tensor-core by default
+ *                  (hidden, q_dim, ffn widths of Q4_KERNEL_TC, hidden <= 8192,
+ *                  kv_dim and head_dim multiples of 4), else the CUDA-core one
+ *                  (head_dim % 64 == 0 and the widths of Q4_KERNEL_STREAM);
+ *                  batch 2..16 runs one tensor-core product launch per
+ *                  projection with glue launches between them (hidden, q_dim,
+ *                  ffn multiples of 256; kv_dim, head_dim multiples of 4)
  *   stream         used for the workspace initialisation (synchronised)
  * Errors: Q4_ERR_ARG, Q4_ERR_ALIGN, Q4_ERR_OOM (workspace too small), Q4_ERR_CUDA.
  */
@@ -249,9 +253,10 @@ int q4_layer_decode_eager(q4_decoder *dec, uint16_t *hidden_io, void *stream);
  * tag.  Results of a call that set a bit are not valid.  Errors: Q4_ERR_CUDA. */
 int q4_decoder_status(q4_decoder *dec, void *stream, int *status_out);
 
-/* *tagged_out = 1 if the decoder's batch-1 CUDA-core engine passes tagged
- * words between phases, 0 if it meets at a flag barrier after every phase (or
- * runs another engine or batch).  Host only.  Errors: Q4_ERR_ARG. */
+/* *tagged_out = 1 if the decoder's batch-1 engine passes tagged words
+ * between phases (always for the tensor-core engine), 0 if it meets at a flag
+ * barrier after every phase (or runs another batch).  Host only.
+ * Errors: Q4_ERR_ARG. */
 int q4_decoder_tagged(const q4_decoder *dec, int *tagged_out);
 
 /*
@@ -353,13 +358,13 @@ typedef struct q4_stream q4_stream;
 
 #define Q4_STREAM_POISON 1   /* after a layer's compute, overwrite its staging buffer's
                                 scales with NaN before the next copy lands (race check) */
-#define Q4_STREAM_TENSOR_CORE 2 /* batch 1 runs the tensor-core engine instead of the
-                                   exact CUDA-core engine */
+#define Q4_STREAM_TENSOR_CORE 2 /* batch 1 must run the tensor-core engine (as Q4_DEC_TENSOR_CORE) */
 #define Q4_STREAM_CHUNKED 4   /* copy each streamed layer as four chunks (q|k|v, o, gate|up,
                                  down), one event each; each of the layer's products starts as
                                  soon as its own chunk has landed (PIPO, "Data transfer suite":
                                  blockwise transfer) instead of after the whole block */
-#define Q4_STREAM_BARRIER 8   /* as Q4_DEC_BARRIER for the ring's batch-1 CUDA-core engine */
+#define Q4_STREAM_BARRIER 8   /* as Q4_DEC_BARRIER for the ring's batch-1 engine */
+#define Q4_STREAM_CUDA_CORE 16  /* as Q4_DEC_CUDA_CORE for the ring's batch-1 engine */
 
 /*
  * Create a double-buffered copy/compute ring (PipeLLM, "Layer 2"; PIPO,
@@ -372,7 +377,7 @@ typedef struct q4_stream q4_stream;
  *   dev_buf0/1       device, buf_bytes >= one layer block each, 256-byte aligned
  *   workspace        device, >= q4_workspace_layout(shape, n_layers, batch) bytes
  *   flags            0, or Q4_STREAM_POISON | Q4_STREAM_TENSOR_CORE | Q4_STREAM_CHUNKED |
- *                    Q4_STREAM_BARRIER
+ *                    Q4_STREAM_BARRIER | Q4_STREAM_CUDA_CORE
  * The handle creates its own copy stream and events.
  * Errors: Q4_ERR_ARG, Q4_ERR_ALIGN, Q4_ERR_OOM, Q4_ERR_CUDA.
  */

@@ -103,25 +103,32 @@ def test_decoder_checks(lib):
     assert f(ctypes.byref(h), ctypes.byref(shape), ptrs, 0, 1, 4096, ws_bytes, 0, None) == q4.Q4_ERR_ARG
     assert f(ctypes.byref(h), ctypes.byref(shape), ptrs, 2, 1, 4096 + 16, ws_bytes, 0, None) == q4.Q4_ERR_ALIGN
     assert f(ctypes.byref(h), ctypes.byref(shape), ptrs, 2, 1, 4096, ws_bytes - 1, 0, None) == q4.Q4_ERR_OOM
-    assert f(ctypes.byref(h), ctypes.byref(shape), ptrs, 2, 1, 4096, ws_bytes, 8, None) == q4.Q4_ERR_ARG   # unknown bit
+    assert f(ctypes.byref(h), ctypes.byref(shape), ptrs, 2, 1, 4096, ws_bytes, 16, None) == q4.Q4_ERR_ARG  # unknown bit
+    both = q4.Q4_DEC_TENSOR_CORE | q4.Q4_DEC_CUDA_CORE
+    assert f(ctypes.byref(h), ctypes.byref(shape), ptrs, 2, 1, 4096, ws_bytes, both, None) == q4.Q4_ERR_ARG
     bad = q4.LayerShape.of(hidden=256, q_dim=256, kv_dim=96, ffn=1024, head_dim=64)   # kv not whole heads
     assert f(ctypes.byref(h), ctypes.byref(bad), ptrs, 2, 1, 4096, ws_bytes, 0, None) == q4.Q4_ERR_ARG
     odd = q4.LayerShape.of(hidden=96, q_dim=96, kv_dim=96, ffn=96, head_dim=32)      # rows not 16-byte aligned
     assert f(ctypes.byref(h), ctypes.byref(odd), ptrs, 2, 1, 4096, ws_bytes, 0, None) == q4.Q4_ERR_ARG
     wide = q4.LayerShape.of(hidden=256, q_dim=256, kv_dim=128, ffn=768, head_dim=64)  # 768/64 threads: no team split
     tc = q4.Q4_DEC_FUSED | q4.Q4_DEC_TENSOR_CORE
-    assert f(ctypes.byref(h), ctypes.byref(wide), ptrs, 2, 1, 4096, ws_bytes, 0, None) == q4.Q4_ERR_ARG
+    core = q4.Q4_DEC_FUSED | q4.Q4_DEC_CUDA_CORE
+    assert f(ctypes.byref(h), ctypes.byref(wide), ptrs, 2, 1, 4096, ws_bytes, core, None) == q4.Q4_ERR_ARG
+    big = q4.LayerShape.of(hidden=16384, q_dim=256, kv_dim=128, ffn=1024, head_dim=64)  # tc: norm input > 8192
+    assert f(ctypes.byref(h), ctypes.byref(big), ptrs, 2, 1, 4096, 1 << 30, tc, None) == q4.Q4_ERR_ARG
+    chunked = q4.LayerShape.of(hidden=256, q_dim=256, kv_dim=128, ffn=3072, head_dim=64)  # tc: 3072 % 2048
+    assert f(ctypes.byref(h), ctypes.byref(chunked), ptrs, 2, 1, 4096, 1 << 30, tc, None) == q4.Q4_ERR_ARG
     ragged = q4.LayerShape.of(hidden=256, q_dim=256, kv_dim=128, ffn=1056, head_dim=64)  # ffn not 256-aligned
     assert f(ctypes.byref(h), ctypes.byref(ragged), ptrs, 2, 1, 4096, ws_bytes, tc, None) == q4.Q4_ERR_ARG
-    heads = q4.LayerShape.of(hidden=256, q_dim=256, kv_dim=128, ffn=1024, head_dim=32)  # tc only
-    assert f(ctypes.byref(h), ctypes.byref(heads), ptrs, 2, 1, 4096, ws_bytes, 0, None) == q4.Q4_ERR_ARG
+    heads = q4.LayerShape.of(hidden=256, q_dim=256, kv_dim=128, ffn=1024, head_dim=32)  # CUDA-core: head_dim % 64
+    assert f(ctypes.byref(h), ctypes.byref(heads), ptrs, 2, 1, 4096, ws_bytes, core, None) == q4.Q4_ERR_ARG
     # streaming ring
     s = ctypes.c_void_p()
     g = lib.q4_stream_create
     _, lb = q4.q4_layer_offsets(shape)
     assert g(ctypes.byref(s), ctypes.byref(shape), ptrs, 2, 1, 4096, 8192, lb - 1, 4096, ws_bytes, 0) == q4.Q4_ERR_OOM
     assert g(ctypes.byref(s), ctypes.byref(shape), ptrs, 2, 1, 4096, 8192 + 16, lb, 4096, ws_bytes, 0) == q4.Q4_ERR_ALIGN
-    assert g(ctypes.byref(s), ctypes.byref(shape), ptrs, 2, 1, 4096, 8192, lb, 4096, ws_bytes, 16) == q4.Q4_ERR_ARG
+    assert g(ctypes.byref(s), ctypes.byref(shape), ptrs, 2, 1, 4096, 8192, lb, 4096, ws_bytes, 32) == q4.Q4_ERR_ARG
     # partial residency: a layer needs a host block or a resident block; resident blocks 256-byte aligned
     gx = lib.q4_stream_create_ex
     none = (ctypes.c_void_p * 2)(None, None)

@@ -106,8 +106,11 @@ def test_stream_kernel_parity(n, k):
     assert_within_tol(y, y_ref, s_ref, f"stream {n}x{k}")
 
 
+# widths of one chunk (up to 2048 columns, unpadded rows) and of whole 64-block
+# chunks (padded rows, the last chunk's copy box running past the row end);
+# row counts that leave a ragged last tile
 TC_SHAPES = [(1, 256), (16, 256), (17, 512), (100, 2048), (129, 4096), (300, 4096), (61, 14336), (33, 28672),
-             (1000, 8192), (64, 2304), (5, 30720)]
+             (1000, 8192), (64, 1024), (5, 30720), (31, 6144), (4096, 4096)]
 
 
 @pytest.mark.parametrize("n,k", TC_SHAPES)
@@ -124,7 +127,7 @@ def test_tc_engine_rejects_unsupported_widths():
     x = torch.zeros(32768, dtype=torch.int16, device="cuda")
     y = torch.zeros(64, dtype=torch.float32, device="cuda")
     w = torch.zeros(q4.q4_matrix_bytes(4, 32768), dtype=torch.uint8, device="cuda")
-    for k in (96, 288, 32768):
+    for k in (96, 288, 2304, 3072, 32768):
         with pytest.raises(q4.Q4Error) as e:
             q4.q4_gemv_ex(w, x, y, 4, k, 1, q4.Q4_KERNEL_TC)
         assert e.value.status == q4.Q4_ERR_ARG
@@ -198,17 +201,22 @@ def test_stream_kernel_width_limit():
     assert not y.any()
 
 
-def test_deterministic_and_auto_is_stream():
+def test_deterministic_and_auto_is_tc():
     n, k = 512, 4096
     w = synth.q4_matrix(n, k, 1, synth.GEMV_TID)
     x = synth.activations(1, k, 1)
     a = run(w, x, n, k, 1, q4.Q4_KERNEL_AUTO)
-    b = run(w, x, n, k, 1, q4.Q4_KERNEL_STREAM)
-    c = run(w, x, n, k, 1, q4.Q4_KERNEL_STREAM)
+    b = run(w, x, n, k, 1, q4.Q4_KERNEL_TC)
+    c = run(w, x, n, k, 1, q4.Q4_KERNEL_TC)
     assert np.array_equal(a, b) and np.array_equal(b, c)
-    d = run(w, x, n, k, 1, q4.Q4_KERNEL_TC)
-    e = run(w, x, n, k, 1, q4.Q4_KERNEL_TC)
+    d = run(w, x, n, k, 1, q4.Q4_KERNEL_STREAM)
+    e = run(w, x, n, k, 1, q4.Q4_KERNEL_STREAM)
     assert np.array_equal(d, e)
+    # widths neither persistent engine takes go to the plain kernel
+    n, k = 64, 2304
+    w = synth.q4_matrix(n, k, 1, synth.GEMV_TID)
+    x = synth.activations(1, k, 1)
+    assert np.array_equal(run(w, x, n, k, 1, q4.Q4_KERNEL_AUTO), run(w, x, n, k, 1, q4.Q4_KERNEL_SIMPLE))
     # above the persistent engine's widths auto takes the plain CUDA-core kernel at batch 1
     n, k = 8, 34816
     w = synth.q4_matrix(n, k, 1, synth.GEMV_TID)

@@ -44,9 +44,9 @@ class Stack:
         q4.q4_decoder_destroy(self.dec)
 
 
-# the CUDA-core engine with tagged words between phases (default), the same
-# engine with a flag barrier after every phase, the tensor-core engine
-ENGINES = {"core": 0, "barrier": q4.Q4_DEC_BARRIER, "tc": q4.Q4_DEC_TENSOR_CORE}
+# the tensor-core engine (default), the CUDA-core engine with tagged words
+# between phases, the CUDA-core engine with a flag barrier after every phase
+ENGINES = {"tc": 0, "core": q4.Q4_DEC_CUDA_CORE, "barrier": q4.Q4_DEC_BARRIER}
 
 
 @pytest.mark.parametrize("engine", list(ENGINES))
@@ -105,16 +105,16 @@ def test_engines_agree_and_tc_head_dims():
     cfg = SMALL
     h0 = synth.activations(1, cfg["hidden"], 32)
     a = Stack(cfg, 2, seed=33, mode=q4.Q4_DEC_TENSOR_CORE).run(h0).view(np.float16).astype(np.float64)
-    b = Stack(cfg, 2, seed=33).run(h0).view(np.float16).astype(np.float64)
+    b = Stack(cfg, 2, seed=33, mode=q4.Q4_DEC_CUDA_CORE).run(h0).view(np.float16).astype(np.float64)
     assert np.linalg.norm(a - b) / np.linalg.norm(b) < 2e-3
-    odd = dict(hidden=768, q_dim=768, kv_dim=192, ffn=2816, head_dim=48)
+    odd = dict(hidden=768, q_dim=768, kv_dim=192, ffn=2048, head_dim=48)
     st = Stack(odd, 1, seed=34, mode=q4.Q4_DEC_TENSOR_CORE)
     h0 = synth.activations(1, odd["hidden"], 35)
     h1 = st.run(h0)
     check_layer(odd, 34, 0, read_ws(st.ws, st.offs, odd), h1, h_in16=h0)
     st.close()
     with pytest.raises(q4.Q4Error):
-        Stack(odd, 1, seed=34)
+        Stack(odd, 1, seed=34, mode=q4.Q4_DEC_CUDA_CORE)
 
 
 @pytest.mark.parametrize("cfg", [SMALL, WIDE], ids=["small", "wide"])
@@ -123,17 +123,19 @@ def test_tagged_and_barrier_programs_agree(cfg):
     compute the same layers; their RMSNorm sums of squares add up in different
     orders, so they agree within the products' error bound, not bit for bit."""
     h0 = synth.activations(1, cfg["hidden"], 36)
-    a = Stack(cfg, 3, seed=37).run(h0).view(np.float16).astype(np.float64)
+    a = Stack(cfg, 3, seed=37, mode=q4.Q4_DEC_CUDA_CORE).run(h0).view(np.float16).astype(np.float64)
     b = Stack(cfg, 3, seed=37, mode=q4.Q4_DEC_BARRIER).run(h0).view(np.float16).astype(np.float64)
     assert np.linalg.norm(a - b) / np.linalg.norm(b) < 2e-3
 
 
 def test_protocol_selection():
-    """Batch-1 CUDA-core decoders pass tagged words unless asked for the flag
-    barrier; the tensor-core engine always meets at flag barriers."""
+    """Batch-1 decoders pass tagged words unless asked for the flag barrier
+    (which only the CUDA-core engine has); the tensor-core engine always
+    passes tagged words."""
     assert Stack(SMALL, 1, seed=38).dec and q4.q4_decoder_tagged(Stack(SMALL, 1, seed=38).dec)
     assert not q4.q4_decoder_tagged(Stack(SMALL, 1, seed=38, mode=q4.Q4_DEC_BARRIER).dec)
-    assert not q4.q4_decoder_tagged(Stack(SMALL, 1, seed=38, mode=q4.Q4_DEC_TENSOR_CORE).dec)
+    assert q4.q4_decoder_tagged(Stack(SMALL, 1, seed=38, mode=q4.Q4_DEC_TENSOR_CORE).dec)
+    assert q4.q4_decoder_tagged(Stack(SMALL, 1, seed=38, mode=q4.Q4_DEC_CUDA_CORE).dec)
     assert q4.q4_decoder_tagged(Stack(WIDE, 1, seed=38).dec)
 
 
@@ -151,11 +153,12 @@ def test_wide_hidden_falls_back_to_flag_program():
     st.close()
 
 
-def test_tagged_wait_runs_out_and_reports():
+@pytest.mark.parametrize("engine", ["tc", "core"])
+def test_tagged_wait_runs_out_and_reports(engine):
     """A tagged input that never arrives: every wait gives up after its poll
     limit, the status word carries bit 16, and the context and the decoder
     stay usable (the next token is exact)."""
-    st = Stack(TINY, 2, seed=42)
+    st = Stack(TINY, 2, seed=42, mode=q4.Q4_DEC_FUSED | ENGINES[engine])
     h0 = synth.activations(1, TINY["hidden"], 43)
     a = st.run(h0)
     status = q4.q4_decoder_debug_stall(st.dec, 2000)

@@ -40,11 +40,11 @@ class Ring:
         q4.q4_stream_destroy(self.h)
 
 
-def resident(cfg, n_layers, seed, h_np, tokens=1, tc=False, barrier=False):
+def resident(cfg, n_layers, seed, h_np, tokens=1, core=False, barrier=False):
     shape = q4.LayerShape.of(**cfg)
     wbuf, ptrs = model.resident_layers(shape, n_layers, seed)
     ws, offs, nb = model.workspace(shape, n_layers, 1)
-    mode = q4.Q4_DEC_PER_LAYER | (q4.Q4_DEC_TENSOR_CORE if tc else 0) | (q4.Q4_DEC_BARRIER if barrier else 0)
+    mode = q4.Q4_DEC_PER_LAYER | (q4.Q4_DEC_CUDA_CORE if core else 0) | (q4.Q4_DEC_BARRIER if barrier else 0)
     dec = q4.q4_decoder_create(shape, ptrs, 1, ws, nb, mode)
     h = dev_u16(h_np.reshape(-1))
     for _ in range(tokens):
@@ -55,14 +55,14 @@ def resident(cfg, n_layers, seed, h_np, tokens=1, tc=False, barrier=False):
 
 
 @pytest.mark.parametrize("cfg,n_layers", [(TINY, 5), (SMALL, 4)], ids=["tiny5", "small4"])
-@pytest.mark.parametrize("flags", [0, q4.Q4_STREAM_POISON, q4.Q4_STREAM_POISON | q4.Q4_STREAM_TENSOR_CORE,
+@pytest.mark.parametrize("flags", [0, q4.Q4_STREAM_POISON, q4.Q4_STREAM_POISON | q4.Q4_STREAM_CUDA_CORE,
                                    q4.Q4_STREAM_POISON | q4.Q4_STREAM_BARRIER],
-                         ids=["plain", "poison", "poison-tc", "poison-barrier"])
+                         ids=["plain", "poison", "poison-core", "poison-barrier"])
 def test_streamed_equals_resident(cfg, n_layers, flags):
     h0 = synth.activations(1, cfg["hidden"], 50)
     ring = Ring(cfg, n_layers, seed=51, flags=flags)
     got = ring.run(h0, tokens=2)
-    ref = resident(cfg, n_layers, 51, h0, tokens=2, tc=bool(flags & q4.Q4_STREAM_TENSOR_CORE),
+    ref = resident(cfg, n_layers, 51, h0, tokens=2, core=bool(flags & q4.Q4_STREAM_CUDA_CORE),
                    barrier=bool(flags & q4.Q4_STREAM_BARRIER))
     assert np.array_equal(got, ref)
     assert np.all(np.isfinite(got.view(np.float16).astype(np.float64)))
@@ -107,15 +107,15 @@ def _mixed_ring(cfg, n_layers, seed, resident_mask, flags, batch=1):
 
 
 @pytest.mark.parametrize("flags", [q4.Q4_STREAM_CHUNKED, q4.Q4_STREAM_CHUNKED | q4.Q4_STREAM_POISON,
-                                   q4.Q4_STREAM_CHUNKED | q4.Q4_STREAM_TENSOR_CORE,
+                                   q4.Q4_STREAM_CHUNKED | q4.Q4_STREAM_CUDA_CORE,
                                    q4.Q4_STREAM_CHUNKED | q4.Q4_STREAM_BARRIER],
-                         ids=["chunked", "chunked-poison", "chunked-tc", "chunked-barrier"])
+                         ids=["chunked", "chunked-poison", "chunked-core", "chunked-barrier"])
 def test_chunked_copies_equal_resident(flags):
     cfg, L = SMALL, 4
     h0 = synth.activations(1, cfg["hidden"], 80)
     ring = Ring(cfg, L, seed=81, flags=flags)
     got = ring.run(h0, tokens=2)
-    ref = resident(cfg, L, 81, h0, tokens=2, tc=bool(flags & q4.Q4_STREAM_TENSOR_CORE),
+    ref = resident(cfg, L, 81, h0, tokens=2, core=bool(flags & q4.Q4_STREAM_CUDA_CORE),
                    barrier=bool(flags & q4.Q4_STREAM_BARRIER))
     assert np.array_equal(got, ref)
     ring.close()

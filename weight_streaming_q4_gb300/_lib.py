@@ -37,10 +37,12 @@ Q4_DEC_FUSED = 0
 Q4_DEC_PER_LAYER = 1
 Q4_DEC_TENSOR_CORE = 2
 Q4_DEC_BARRIER = 4
+Q4_DEC_CUDA_CORE = 8
 Q4_STREAM_POISON = 1
 Q4_STREAM_TENSOR_CORE = 2
 Q4_STREAM_CHUNKED = 4
 Q4_STREAM_BARRIER = 8
+Q4_STREAM_CUDA_CORE = 16
 
 WS_NAMES = ("control", "program", "qkv", "o", "gate", "up", "down", "act", "x", "attn", "x2", "t1", "t2", "flags", "xt", "vt", "actt")
 WS_COUNT = len(WS_NAMES)

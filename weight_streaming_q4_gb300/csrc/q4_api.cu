@@ -2,6 +2,7 @@
 // configuration, the decoder (phase programs + CUDA-graph capture) and the
 // double-buffered copy/compute ring.  Host code only; every arithmetic step
 // of the decode runs in the kernels of q4_engine.cu and q4_aux.cu.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
@@ -66,6 +67,9 @@ int device_info(DeviceInfo** out) {
     Q4_CUDA(q4::attn_prepare());
     Q4_CUDA(q4::engine_occupancy(&d.engine_blocks_per_sm));
     if (d.engine_blocks_per_sm < 1) return Q4_ERR_CUDA;
+    int tc_blocks = 0;
+    Q4_CUDA(q4::tc_engine_occupancy(&tc_blocks));
+    if (tc_blocks < 1) return Q4_ERR_CUDA;
     d.ready = true;
   }
   *out = &d;
@@ -88,31 +92,62 @@ bool engine_ok(int k) {
 // tensor-core products (q4_tc_engine.cu).
 enum Engine { ENG_CORE = 0, ENG_TC = 1 };
 
-// Whether the tensor-core engine can run rows of width k: whole 8-block
-// groups (row segments start 16-byte aligned) and an input that fits its
-// shared-memory buffer.
-bool tc_ok(int k) { return k >= 256 && k % 256 == 0 && k <= 30720; }
+// Whether the tensor-core engine can run rows of width k: whole 8-block row
+// segments (16-byte aligned), one column chunk or whole 64-block chunks, and
+// an input that fits its fragment buffer.
+bool tc_ok(int k) { return k >= 256 && k % 256 == 0 && (k <= 2048 || k % 2048 == 0) && k <= q4::kTcMaxK; }
 
-// Bytes of its upcoming weights each tensor-core CTA keeps requested into L2
-// beyond its ring; Q4_PREFETCH_BYTES in the environment overrides it.
-uint32_t tc_prefetch_bytes() {
-  static const uint32_t v = [] {
-    const char* e = getenv("Q4_PREFETCH_BYTES");
-    return e ? static_cast<uint32_t>(strtoul(e, nullptr, 10)) : 196608u;
+// TMA descriptors are encoded with the driver's cuTensorMapEncodeTiled,
+// reached through the runtime's entry-point query (no link-time dependency on
+// the driver library).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static const EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiledFn>(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(p);
   }();
-  return v;
+  return fn;
+}
+
+// Descriptor of a row-major Q4_0 matrix (n_rows x k) for the tensor-core
+// engine: 64-bit elements, row_bytes / 8 columns, box tc_pitch(k) / 8 columns
+// by box_rows rows.
+bool encode_rows(CUtensorMap* m, const uint8_t* w, int n_rows, int k, int box_rows) {
+  const EncodeTiledFn fn = encode_fn();
+  if (!fn || !w || !aligned(w, 16) || n_rows < 1) return false;
+  const cuuint64_t row_bytes = static_cast<cuuint64_t>(k / q4::kQK) * q4::kBlockBytes;
+  const cuuint64_t gdim[2] = {row_bytes / 8, static_cast<cuuint64_t>(n_rows)};
+  const cuuint64_t gstride[1] = {row_bytes};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(q4::tc_pitch(k) / 8), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estride[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint8_t*>(w), gdim, gstride, box, estride,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Fill the tiling fields of a phase.  CUDA-core engine: a work unit gives
 // every team two rows (two rows of one matrix, or the same row of both
-// matrices of a pair).  Tensor-core engine: a unit is one 16-row tile (8 rows
-// of each matrix of a pair).
-bool tile_phase(Phase& ph, int engine = ENG_CORE) {
+// matrices of a pair).  Tensor-core engine: a unit is one 32-row tile (16
+// rows of each matrix of a pair), and with `encode` the phase's TMA
+// descriptors are written (not for shape checks, which pass no weights).
+bool tile_phase(Phase& ph, int engine = ENG_CORE, bool encode = true) {
   if (engine == ENG_TC) {
     if (!tc_ok(ph.k)) return false;
     ph.teams = 0;
-    ph.rows_per_unit = ph.epi_kind == q4::EPI_SILU ? 8 : 16;
+    const bool dual = ph.epi_kind == q4::EPI_SILU;
+    ph.rows_per_unit = dual ? q4::kTcUnitRows / 2 : q4::kTcUnitRows;
     ph.units = (ph.n_rows + ph.rows_per_unit - 1) / ph.rows_per_unit;
+    if (encode && ph.n_rows > 0) {
+      if (!encode_rows(&ph.tm0, ph.w0, ph.n_rows, ph.k, ph.rows_per_unit)) return false;
+      if (dual && !encode_rows(&ph.tm1, ph.w1, ph.n_rows, ph.k, ph.rows_per_unit)) return false;
+    }
     return true;
   }
   if (!engine_ok(ph.k)) return false;
@@ -128,6 +163,30 @@ bool tile_phase(Phase& ph, int engine = ENG_CORE) {
   ph.rows_per_unit = ph.epi_kind == q4::EPI_SILU ? teams : 2 * teams;
   ph.units = (ph.n_rows + ph.rows_per_unit - 1) / ph.rows_per_unit;
   return true;
+}
+
+// Ring and buffers of a tensor-core launch whose phases have widths in
+// `ks`: stage stride = 32 rows of the widest pitch, fragment buffer = 2 bytes
+// per value of the widest input, as many stages (up to 8) as fit.
+struct TcGeom {
+  int stages = 0;
+  uint32_t stage_bytes = 0;
+  int xbuf_floats = 0;
+};
+
+bool tc_geom(std::initializer_list<int> ks, TcGeom* g) {
+  int kmax = 0, pmax = 0;
+  for (int k : ks) {
+    if (!tc_ok(k)) return false;
+    kmax = std::max(kmax, k);
+    pmax = std::max(pmax, q4::tc_pitch(k));
+  }
+  g->stage_bytes = static_cast<uint32_t>(pmax) * q4::kTcUnitRows;
+  g->xbuf_floats = (2 * kmax + 15) / 16 * 4;
+  int s = 8;
+  while (s >= 2 && q4::tc_smem_bytes(s, g->stage_bytes, g->xbuf_floats) > q4::kTcSmemLimit) --s;
+  g->stages = s;
+  return s >= 3;
 }
 
 }  // namespace
@@ -173,7 +232,7 @@ extern "C" int q4_gemv_ex(const void* w, const uint16_t* x, float* y, int n, int
   if (kernel == Q4_KERNEL_AUTO) {
     // batch 1: the CUDA-core engine (plain kernel for widths it cannot take);
     // batch 2..16: tensor cores when rows are 16-byte aligned
-    if (batch == 1) kernel = engine_ok(k) ? Q4_KERNEL_STREAM : Q4_KERNEL_SIMPLE;
+    if (batch == 1) kernel = tc_ok(k) ? Q4_KERNEL_TC : engine_ok(k) ? Q4_KERNEL_STREAM : Q4_KERNEL_SIMPLE;
     else if (k % 256 == 0) kernel = Q4_KERNEL_MMA;
     else kernel = Q4_KERNEL_SIMPLE;
   }
@@ -209,11 +268,15 @@ extern "C" int q4_gemv_ex(const void* w, const uint16_t* x, float* y, int n, int
   a.n_phases = 1;
   a.ctl = nullptr;
   a.wait_limit = kWaitLimit;
-  a.prefetch_bytes = engine == ENG_TC ? tc_prefetch_bytes() : 0;
   const int grid = ph.units < dev->sm_count ? ph.units : dev->sm_count;
-  if (engine == ENG_TC)
+  if (engine == ENG_TC) {
+    TcGeom g;
+    if (!tc_geom({k}, &g)) return Q4_ERR_ARG;
+    a.stages = g.stages;
+    a.stage_bytes = g.stage_bytes;
+    a.xbuf_floats = g.xbuf_floats;
     Q4_CUDA(q4::tc_engine_launch(a, grid, false, s));
-  else
+  } else
     Q4_CUDA(q4::engine_launch(a, grid, false, s));
   return Q4_OK;
 }
@@ -505,7 +568,7 @@ bool tagged_ok(const q4_layer_shape& s) {
 // the data dependences between the phases, orders each rewrite after every
 // read of the previous values.
 bool layer_phases_tagged(const q4_layer_shape& s, const uint8_t* wl, const uint16_t* in16, const Work& w,
-                         Phase out[4], bool last) {
+                         Phase out[4], bool last, int engine) {
   size_t off[7];
   if (q4_layer_offsets(&s, off, nullptr) != Q4_OK) return false;
   memset(out, 0, 4 * sizeof(Phase));
@@ -571,13 +634,13 @@ bool layer_phases_tagged(const q4_layer_shape& s, const uint8_t* wl, const uint1
   d.yt = w.t2t;
   d.yt_n = s.hidden;
   for (int i = 0; i < 4; ++i)
-    if (!tile_phase(out[i], ENG_CORE)) return false;
+    if (!tile_phase(out[i], engine, wl != nullptr)) return false;
   return true;
 }
 
 // The closing phase of a tagged program: CTA 0 writes f16(norm(t2)) to the
 // caller's hidden-state buffer.
-bool final_phase_tagged(const q4_layer_shape& s, uint16_t* h_out, const Work& w, Phase* out) {
+bool final_phase_tagged(const q4_layer_shape& s, uint16_t* h_out, const Work& w, Phase* out, int engine) {
   memset(out, 0, sizeof(Phase));
   out->x_src = w.t2t;
   out->x_kind = q4::X_TAG32_NORM;
@@ -586,7 +649,7 @@ bool final_phase_tagged(const q4_layer_shape& s, uint16_t* h_out, const Work& w,
   out->n_rows = 0;
   out->epi_kind = q4::EPI_F32;
   out->x_dbg = h_out;
-  return tile_phase(*out, ENG_CORE);
+  return tile_phase(*out, engine, false);
 }
 
 // Phase program of a whole stack: 4 phases per layer and the closing phase.
@@ -596,11 +659,11 @@ bool stack_program(const q4_layer_shape& s, const std::vector<const uint8_t*>& l
   prog.assign(4 * static_cast<size_t>(L) + 1, Phase());
   for (int l = 0; l < L; ++l) {
     const uint16_t* in16 = l == 0 ? h : nullptr;
-    if (!(tagged ? layer_phases_tagged(s, layers[l], in16, w, &prog[4 * l], l == L - 1)
+    if (!(tagged ? layer_phases_tagged(s, layers[l], in16, w, &prog[4 * l], l == L - 1, engine)
                  : layer_phases(s, layers[l], in16, w, &prog[4 * l], engine)))
       return false;
   }
-  if (!(tagged ? final_phase_tagged(s, h, w, &prog[4 * L]) : final_phase(s, h, w, &prog[4 * L], engine)))
+  if (!(tagged ? final_phase_tagged(s, h, w, &prog[4 * L], engine) : final_phase(s, h, w, &prog[4 * L], engine)))
     return false;
   // unit rotation over the whole program, so that any split into launches
   // (fused, per layer, per phase) gives every CTA the same rows; the phase
@@ -614,16 +677,40 @@ bool stack_program(const q4_layer_shape& s, const std::vector<const uint8_t*>& l
   return true;
 }
 
+// Ring and buffer geometry of a tensor-core layer program.
+bool tc_layer_geom(const q4_layer_shape& s, TcGeom* g) { return tc_geom({s.hidden, s.q_dim, s.ffn}, g); }
+
 int check_layer_shape_for_engine(const q4_layer_shape& s, int engine) {
-  // CUDA-core engine: a thread's 64 attention columns stay in one head;
-  // tensor-core engine: runs of 4 columns do
-  if (s.head_dim % (engine == ENG_TC ? 4 : q4::kKT)) return Q4_ERR_ARG;
   Phase tmp[5];
   Work w;
   memset(&w, 0, sizeof(w));
+  if (engine == ENG_TC) {
+    // tensor-core engine (tagged programs only): the RMSNorm inputs are staged
+    // in registers (hidden <= 8192), values move in runs of 4 that stay
+    // within one attention head
+    TcGeom g;
+    if (s.head_dim % 4 || s.kv_dim % 4 || s.hidden > 8192 || !tc_layer_geom(s, &g)) return Q4_ERR_ARG;
+    return layer_phases_tagged(s, nullptr, nullptr, w, tmp, false, ENG_TC) &&
+                   final_phase_tagged(s, nullptr, w, &tmp[4], ENG_TC)
+               ? Q4_OK
+               : Q4_ERR_ARG;
+  }
+  // CUDA-core engine: a thread's 64 attention columns stay in one head
+  if (s.head_dim % q4::kKT) return Q4_ERR_ARG;
   return layer_phases(s, nullptr, nullptr, w, tmp, engine) && final_phase(s, nullptr, w, &tmp[4], engine)
              ? Q4_OK
              : Q4_ERR_ARG;
+}
+
+// The batch-1 engine of a decoder or ring: the tensor-core engine unless the
+// CUDA-core one is asked for (or the flag barrier, which only it has) or the
+// shape does not fit the tensor-core engine.  -1 if the asked engine cannot
+// run the shape.
+int pick_engine(const q4_layer_shape& s, bool want_tc, bool want_core) {
+  if (want_tc && want_core) return -1;
+  if (!want_core && check_layer_shape_for_engine(s, ENG_TC) == Q4_OK) return ENG_TC;
+  if (want_tc) return -1;
+  return check_layer_shape_for_engine(s, ENG_CORE) == Q4_OK ? ENG_CORE : -1;
 }
 
 // One layer for a batch of more than one row: the tensor-core product for each
@@ -689,7 +776,12 @@ int launch_layers(const Work& w, int first_phase, int n_phases, int grid, cudaSt
     a.xbuf_floats = static_cast<int>(tagged_xbuf_bytes(shape) / 4);
   }
   if (engine == ENG_TC) {
-    a.prefetch_bytes = tc_prefetch_bytes();
+    TcGeom g;
+    if (!tc_layer_geom(shape, &g)) return Q4_ERR_ARG;
+    a.tagged = 1;
+    a.stages = g.stages;
+    a.stage_bytes = g.stage_bytes;
+    a.xbuf_floats = g.xbuf_floats;
     Q4_CUDA(q4::tc_engine_launch(a, grid, true, s));
   } else {
     Q4_CUDA(q4::engine_launch(a, grid, true, s));
@@ -762,12 +854,13 @@ extern "C" int q4_decoder_create(q4_decoder** out, const q4_layer_shape* shape, 
   if (!out || !shape_ok(shape) || !layer_weights || n_layers < 1 || !workspace) return Q4_ERR_ARG;
   if (batch < 1 || batch > q4::kMaxBatch) return Q4_ERR_ARG;
   if (4 * n_layers + 1 > static_cast<int>(q4::kPhasesPerEpoch)) return Q4_ERR_ARG;
-  const int kind = mode & ~(Q4_DEC_TENSOR_CORE | Q4_DEC_BARRIER);
+  const int kind = mode & ~(Q4_DEC_TENSOR_CORE | Q4_DEC_BARRIER | Q4_DEC_CUDA_CORE);
   if (kind != Q4_DEC_FUSED && kind != Q4_DEC_PER_LAYER) return Q4_ERR_ARG;
-  const int engine = (mode & Q4_DEC_TENSOR_CORE) ? ENG_TC : ENG_CORE;
   // batch 1: a persistent engine; larger batches: tensor-core products + glue
-  if (batch == 1 ? check_layer_shape_for_engine(*shape, engine) != Q4_OK : !batched_shape_ok(*shape))
-    return Q4_ERR_ARG;
+  const int engine = batch == 1 ? pick_engine(*shape, (mode & Q4_DEC_TENSOR_CORE) != 0,
+                                              (mode & (Q4_DEC_CUDA_CORE | Q4_DEC_BARRIER)) != 0)
+                                : ENG_CORE;
+  if (batch == 1 ? engine < 0 : !batched_shape_ok(*shape)) return Q4_ERR_ARG;
   if (!aligned(workspace, 256)) return Q4_ERR_ALIGN;
   for (int l = 0; l < n_layers; ++l) {
     if (!layer_weights[l]) return Q4_ERR_ARG;
@@ -787,7 +880,7 @@ extern "C" int q4_decoder_create(q4_decoder** out, const q4_layer_shape* shape, 
   d->batch = batch;
   d->mode = kind;
   d->engine = engine;
-  d->tagged = batch == 1 && engine == ENG_CORE && !(mode & Q4_DEC_BARRIER) && tagged_ok(*shape);
+  d->tagged = batch == 1 && (engine == ENG_TC || (!(mode & Q4_DEC_BARRIER) && tagged_ok(*shape)));
   d->grid = dev->sm_count < q4::kMaxGrid ? dev->sm_count : q4::kMaxGrid;   // one CTA per SM, co-resident
   d->layers.assign(reinterpret_cast<const uint8_t* const*>(layer_weights),
                    reinterpret_cast<const uint8_t* const*>(layer_weights) + n_layers);
@@ -860,7 +953,8 @@ int run_stack_in_workspace(const q4_layer_shape* shape, const void* const* layer
                            uint16_t* hidden_io, void* ws, size_t ws_bytes, cudaStream_t s) {
   if (!shape_ok(shape) || !layer_weights || n_layers < 1 || !hidden_io || !ws) return Q4_ERR_ARG;
   if (4 * n_layers + 1 > static_cast<int>(kPhasesPerEpoch)) return Q4_ERR_ARG;
-  if (check_layer_shape_for_engine(*shape, ENG_CORE) != Q4_OK) return Q4_ERR_ARG;
+  const int engine = pick_engine(*shape, false, false);
+  if (engine < 0) return Q4_ERR_ARG;
   if (!aligned(hidden_io, 16)) return Q4_ERR_ALIGN;
   for (int l = 0; l < n_layers; ++l) {
     if (!layer_weights[l]) return Q4_ERR_ARG;
@@ -876,8 +970,8 @@ int run_stack_in_workspace(const q4_layer_shape* shape, const void* const* layer
   std::vector<const uint8_t*> layers(reinterpret_cast<const uint8_t* const*>(layer_weights),
                                      reinterpret_cast<const uint8_t* const*>(layer_weights) + n_layers);
   std::vector<Phase> prog;
-  const bool tagged = tagged_ok(*shape);
-  if (!stack_program(*shape, layers, hidden_io, w, prog, ENG_CORE, tagged)) return Q4_ERR_ARG;
+  const bool tagged = engine == ENG_TC || tagged_ok(*shape);
+  if (!stack_program(*shape, layers, hidden_io, w, prog, engine, tagged)) return Q4_ERR_ARG;
   Q4_CUDA(cudaMemcpyAsync(w.prog, prog.data(), prog.size() * sizeof(Phase), cudaMemcpyHostToDevice, s));
   // control block, phase flags and tagged words start from zero: earlier calls
   // left their tags, and the epoch starts again at 0
@@ -886,7 +980,7 @@ int run_stack_in_workspace(const q4_layer_shape* shape, const void* const* layer
   Q4_CUDA(cudaMemsetAsync(static_cast<char*>(ws) + off[Q4_WS_XT], 0, off[Q4_WS_COUNT - 1] - off[Q4_WS_XT] +
                                                                        4 * static_cast<size_t>(shape->ffn), s));
   const int grid = dev->sm_count < kMaxGrid ? dev->sm_count : kMaxGrid;
-  return launch_layers(w, 0, static_cast<int>(prog.size()), grid, s, ENG_CORE, tagged, true, *shape);
+  return launch_layers(w, 0, static_cast<int>(prog.size()), grid, s, engine, tagged, true, *shape);
 }
 
 }  // namespace q4
@@ -901,7 +995,7 @@ extern "C" int q4_decoder_debug_stall(q4_decoder* d, uint32_t wait_limit, void* 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // the o-projection phase alone: its tagged input (v) was written under an
   // earlier epoch, so no word ever carries the tag it waits for
-  int st = launch_layers(d->w, 1, 1, d->grid, s, ENG_CORE, true, false, d->shape, wait_limit);
+  int st = launch_layers(d->w, 1, 1, d->grid, s, d->engine, true, false, d->shape, wait_limit);
   if (st != Q4_OK) return st;
   if ((st = read_status(d->w.ctl, s, status_out)) != Q4_OK) return st;
   // the launch left words under live tags: clear them and the flags
@@ -963,12 +1057,14 @@ extern "C" int q4_stream_create_ex(q4_stream** out, const q4_layer_shape* shape,
   if (!out || !shape_ok(shape) || !host_layers || n_layers < 1 || !dev_buf0 || !dev_buf1 || !workspace)
     return Q4_ERR_ARG;
   if (batch < 1 || batch > q4::kMaxBatch ||
-      (flags & ~(Q4_STREAM_POISON | Q4_STREAM_TENSOR_CORE | Q4_STREAM_CHUNKED | Q4_STREAM_BARRIER)))
+      (flags & ~(Q4_STREAM_POISON | Q4_STREAM_TENSOR_CORE | Q4_STREAM_CHUNKED | Q4_STREAM_BARRIER |
+                 Q4_STREAM_CUDA_CORE)))
     return Q4_ERR_ARG;
   if (4 * n_layers + 1 > static_cast<int>(q4::kPhasesPerEpoch)) return Q4_ERR_ARG;
-  const int engine = (flags & Q4_STREAM_TENSOR_CORE) ? ENG_TC : ENG_CORE;
-  if (batch == 1 ? check_layer_shape_for_engine(*shape, engine) != Q4_OK : !batched_shape_ok(*shape))
-    return Q4_ERR_ARG;
+  const int engine = batch == 1 ? pick_engine(*shape, (flags & Q4_STREAM_TENSOR_CORE) != 0,
+                                              (flags & (Q4_STREAM_CUDA_CORE | Q4_STREAM_BARRIER)) != 0)
+                                : ENG_CORE;
+  if (batch == 1 ? engine < 0 : !batched_shape_ok(*shape)) return Q4_ERR_ARG;
   if (!aligned(dev_buf0, 256) || !aligned(dev_buf1, 256) || !aligned(workspace, 256)) return Q4_ERR_ALIGN;
   size_t lo[7], layer_bytes = 0;
   q4_layer_offsets(shape, lo, &layer_bytes);
@@ -1009,7 +1105,7 @@ extern "C" int q4_stream_create_ex(q4_stream** out, const q4_layer_shape* shape,
   r->batch = batch;
   r->flags = flags;
   r->engine = engine;
-  r->tagged = batch == 1 && engine == ENG_CORE && !(flags & Q4_STREAM_BARRIER) && tagged_ok(*shape);
+  r->tagged = batch == 1 && (engine == ENG_TC || (!(flags & Q4_STREAM_BARRIER) && tagged_ok(*shape)));
   r->grid = dev->sm_count < q4::kMaxGrid ? dev->sm_count : q4::kMaxGrid;
   r->host.assign(host_layers, host_layers + n_layers);
   r->buf[0] = static_cast<uint8_t*>(dev_buf0);

@@ -3,6 +3,7 @@
 // wrappers for mbarriers, 1-D bulk TMA copies and bounded waits.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
 
@@ -114,7 +115,25 @@ struct Phase {
   int sync;               // SyncKind
   int xt_n;               // X_TAG16_ATTN: tagged values of v in x_src
   int pad2_;
+  // Tensor-core engine only: TMA descriptors of w0 and w1 (2-D, 64-bit elements:
+  // columns = row bytes / 8, rows = n_rows; box = tc_pitch(k) / 8 columns by
+  // the unit's rows), encoded on the host.
+  CUtensorMap tm0;
+  CUtensorMap tm1;
 };
+
+// Geometry of the tensor-core engine for rows of width k (k % 256 == 0 and
+// either k <= 2048 or k % 2048 == 0): a stage holds one column chunk of a
+// 32-row unit; a chunk is 64 blocks (the whole row when k <= 2048).  Staged
+// rows of wide matrices are 1168 bytes apart, 16 more than the chunk, so that
+// the 32-bit code-word loads of the 8 row groups of a tile fall in different
+// banks (the copy box reads 16 bytes of the next chunk, or zero-fills past the
+// row end); a row of at most 2048 columns is staged whole, unpadded.
+__host__ __device__ __forceinline__ int tc_chunk_blocks(int k) { return k <= 2048 ? k / 32 : 64; }
+__host__ __device__ __forceinline__ int tc_pitch(int k) { return k <= 2048 ? (k / 32) * 18 : 64 * 18 + 16; }
+__host__ __device__ __forceinline__ int tc_chunks(int k) { return (k / 32) / tc_chunk_blocks(k); }
+constexpr int kTcUnitRows = 32;   // rows of a unit (16 rows of each matrix of a gate|up pair)
+constexpr int kTcMaxK = 30720;    // widest row the engine's input buffer takes
 
 __host__ __device__ __forceinline__ int slice_t32(int e, int T) { return ((e & 63) >> 2) * T * 4 + (e >> 6) * 4 + (e & 3); }
 __host__ __device__ __forceinline__ int slice_t16(int e, int T) { return ((e & 63) >> 3) * T * 8 + (e >> 6) * 8 + (e & 7); }
@@ -141,15 +160,16 @@ struct EngineArgs {
   Control* ctl;            // required when n_phases > 1
   unsigned long long* flags;  // [2][kMaxGrid] end-of-phase flags, required when n_phases > 1
   uint32_t wait_limit;     // polls of one wait before it is declared failed
-  uint32_t prefetch_bytes; // tensor-core engine: weight bytes a CTA keeps requested into L2
-                           // beyond its shared-memory ring (0 = none)
+  uint32_t stage_bytes;    // tensor-core engine: bytes between ring stages (32 rows of the
+                           // widest pitch of the launch's phases)
   int tagged;              // CUDA-core engine: the phases exchange tagged words (phase tag =
                            // epoch * kPhasesPerEpoch + 1 + Phase::gidx) instead of meeting at
                            // a flag barrier after every phase
   int end_of_program;      // tagged: this launch runs the program's last phase, so the last
                            // CTA to leave advances the epoch
-  int stages;              // tagged: ring depth (5 or 6)
-  int xbuf_floats;         // tagged: floats of the staging buffer after the ring
+  int stages;              // tagged (and tensor-core engine): ring depth
+  int xbuf_floats;         // tagged: floats of the staging buffer after the ring (tensor-core
+                           // engine: of the fragment-order input buffer)
   Phase one;
 };
 
@@ -234,6 +254,23 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
+}
+
+// 2-D tensor copy global -> shared of the box at column x (64-bit elements, x
+// even so that the box starts 16-byte aligned) and row y of the tensor map,
+// completion counted on an mbarrier.  Out-of-range rows and columns are
+// filled with zeros (and still counted).
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Acquire a TMA descriptor that lives in global memory for the tensor-map proxy.
+__device__ __forceinline__ void tensormap_acquire(const CUtensorMap* map) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
 }
 
 // Ask for `bytes` at src to be brought into L2 (no completion tracking).
@@ -324,6 +361,10 @@ cudaError_t kv_append_launch(const float* k, const float* v, uint16_t* kc, uint1
 cudaError_t tc_engine_prepare();
 cudaError_t tc_engine_launch(const EngineArgs& a, int grid, bool cooperative, cudaStream_t stream);
 cudaError_t tc_engine_read_status(int* out);
+cudaError_t tc_engine_occupancy(int* blocks_per_sm);
+// Dynamic shared memory of a tensor-core launch, and the largest allowed.
+size_t tc_smem_bytes(int stages, uint32_t stage_bytes, int xbuf_floats);
+constexpr size_t kTcSmemLimit = 231424;
 cudaError_t mma_prepare();
 // y2/split: rows from `split` on go to y2 ([batch][n - split]); rows before to y ([batch][split]).
 // Rows [lo, lo + n_rows) of a product's output taken as value heads of head_dim

@@ -1,30 +1,46 @@
 // Persistent, warp-specialised Q4_0 matrix-vector engine on the tensor cores
-// (batch 1, sm_103a).
+// (batch 1, sm_103a): the default engine of batch-1 decoder stacks, streamed
+// rings and single products.
 //
-// Same phase programs as the CUDA-core engine (q4_engine.cu): a launch runs
-// a list of matrix-vector products with input prologues and output
-// epilogues, separated by per-CTA end-of-phase flags.  What differs is the
-// inner product and the way weights reach it:
+// Work unit = a tile of 32 matrix rows (16 rows of gate and the same 16 rows
+// of up for the paired feed-forward product) over the full width k, staged in
+// column chunks of 64 blocks.  Three kinds of warps:
 //
-// * Work unit = a tile of 16 matrix rows (or 8 rows of each matrix of a
-//   gate/up pair, stacked as one 16-row tile) over the full width k, staged
-//   in column chunks of 64 blocks.  Warp 16 (the producer) copies each
-//   chunk's 16 row segments with 1-D bulk TMA into an 8-deep ring of
-//   shared-memory stages; rows are padded so the code-word loads of the 8
-//   row groups fall in different banks.
-// * The 16 consumer warps take 4 of a chunk's 64 blocks each.  A lane turns
-//   its two code words (rows g and g+8) into exact binary16 (q - 8) values in
-//   registers and issues two mma.sync m16n8k16 (binary16 in, fp32
-//   accumulate) against the input, which the prologue stored once per phase
-//   in shared memory in fragment order (every column of the instruction sees
-//   the same x, so every lane ends with its rows' sums).  Each block's sum is
-//   scaled by its d once, in fp32: the products (q - 8) * x are exact, a
-//   block of all-8 codes contributes exactly zero and a block with one non-8
-//   code contributes exactly fl(d * (q - 8) * x).
-// * Besides the ring, the producer keeps up to `prefetch_bytes` of its
-//   upcoming units requested into L2 (cp.async.bulk.prefetch), across phase
-//   boundaries: weights never depend on the activations, so HBM keeps
-//   streaming while the consumers wait at a phase boundary.
+// * Warp 9, the producer: one lane walks the CTA's units of every phase of
+//   the launch and copies each chunk of a unit with one 2-D tensor TMA copy
+//   (box: 146 64-bit columns by 32 rows, so every staged row starts 1168 bytes
+//   after the previous one and the code-word loads of the 8 row groups of a
+//   tile fall in different banks) into a ring of shared-memory stages,
+//   completion counted on one mbarrier per stage.  Weights never depend on
+//   the activations, so the producer keeps streaming the next phase's weights
+//   while the other warps wait at a phase boundary.
+// * Warps 0-7, the consumers (two per SM sub-partition): each takes four
+//   pairs of blocks (an even block and the odd one after it) of every chunk
+//   and both 16-row halves of the tile, straight-line, so that the eight
+//   products of a stage give every warp enough independent work.  Lane (g, t) turns code word t of rows g and g + 8 of a block into
+//   exact binary16 values (q - 8) in registers (lop3 with the 0x6400 magic,
+//   one subtraction or fused scale per pair) and issues two mma.sync
+//   m16n8k16 (binary16 in, fp32 accumulate) against the input, which the
+//   phase prologue stored once per phase in shared memory in fragment order
+//   with x in every column of the instruction.  Each block's sum is scaled
+//   by its d once, in fp32: the products (q - 8) * x are exact, a block of
+//   all-8 codes contributes exactly zero and a block with one non-8 code
+//   contributes exactly fl(d * (q - 8) * x).  The even block's d arrives with
+//   lane 0's first code word and the odd block's with lane 3's second one, so
+//   no load is spent on the scales; lane 0 accumulates the even blocks and
+//   lane 3 the odd ones, and one shuffle adds them at the end of the unit.
+// * Warp 8, the epilogue: sums the 8 consumer warps' partials of each row
+//   of a unit in a fixed order as soon as the unit is done (two partial slots
+//   handed over with mbarriers) and stores the outputs, so the consumers
+//   never wait for an epilogue.
+//
+// Phases pass their outputs to the next phase as tagged words (the same
+// protocol as the CUDA-core engine's tagged programs, q4_engine.cu): a value
+// travels with the tag of the phase that wrote it in one aligned word, and a
+// CTA stages its whole input by polling the words until every tag matches;
+// one flag exchange per layer guards the rewrite of the tagged buffers.  An
+// RMSNorm input is staged in registers and its sum of squares taken in an
+// order that depends only on its length, so every CTA forms the same input.
 //
 // The method: PIPO's dequantisation-free 4-bit matrix-vector product
 // ("PIPO: Pipelined Offloading for Efficient Inference on Consumer
@@ -32,6 +48,7 @@
 // "Offloading architecture"), with the weights of later work prefetched
 // while the current work computes (PipeLLM page, "Layer 2: Asynchronous
 // Weight Prefetching").
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
 
@@ -43,18 +60,17 @@ namespace q4 {
 
 __device__ int g_status_tc;   // status bits of launches without a control block
 
-constexpr int kTcWarps = 16;                          // consumer warps
+constexpr int kTcWarps = 8;                       // consumer warps (two per SM sub-partition)
 constexpr int kTcConsumers = kTcWarps * 32;
-constexpr int kTcThreads = kTcConsumers + 32;         // + the producer warp
-constexpr int kTcChunk = 64;                          // blocks per staged row segment (2048 columns)
-constexpr int kTcPitch = kTcChunk * kBlockBytes + 16; // 1168 B: rows 4 banks apart
-constexpr int kTcStageBytes = 16 * kTcPitch;          // 18688 B
-constexpr int kTcStages = 8;
-constexpr int kTcMaxK = 30720;
-constexpr int kTcXBytes = kTcMaxK * 2;                // the phase input in fragment order
-constexpr int kTcRedUnits = 16;                       // units buffered before a flush
-constexpr int kTcSmem = kTcStages * kTcStageBytes + kTcXBytes;
-constexpr uint32_t kTcPrefetchPiece = 16384;          // bytes per L2 prefetch instruction
+constexpr int kTcPairsPerWarp = 32 / kTcWarps;    // block pairs of a 64-block chunk per warp
+constexpr int kTcEpiWarp = kTcWarps;              // warp 8
+constexpr int kTcProdWarp = kTcWarps + 1;         // warp 9
+constexpr int kTcThreads = (kTcWarps + 2) * 32;
+constexpr int kTcMaxStages = 8;
+constexpr int kTcRedSlots = 2;                    // unit partial slots between consumers and epilogue
+constexpr int kTcRedBytes = kTcRedSlots * kTcWarps * kTcUnitRows * 4;
+constexpr int kTcNormChunks = 8;                  // 4-value chunks of an RMSNorm input per consumer thread
+constexpr int kTcDynSmemMax = 231424;
 
 extern __shared__ __align__(128) uint8_t g_tc_smem[];
 
@@ -66,239 +82,415 @@ __device__ __forceinline__ const Phase& phase_at(const EngineArgs& a, int p) {
   return a.phases ? a.phases[p] : a.one;
 }
 
-// This CTA's walk over its units of all phases (units u0, u0 + G, ... of each
-// phase, u0 = (cta - base) mod G rotating so that the phases' first units go
-// to different CTAs).
-struct Walk {
-  int p, u;
-};
-
 __device__ __forceinline__ int first_unit(const Phase& ph, int cta, int G) { return (cta - ph.base % G + G) % G; }
 
-__device__ __forceinline__ void walk_settle(Walk& w, const EngineArgs& a, int cta, int G) {
-  while (w.p < a.n_phases) {
-    if (w.u < phase_at(a, w.p).units) return;
-    ++w.p;
-    if (w.p < a.n_phases) w.u = first_unit(phase_at(a, w.p), cta, G);
+// ------------------------------------------------------------------ input
+
+// Four consecutive input values e..e+3 (e % 4 == 0), as binary16 pairs
+// h01 = (x_e, x_e+1) and h23 = (x_e+2, x_e+3), into the fragment-order buffer:
+// lane quarter t of block b holds x[32b + 4t + {0, 2, 1, 3}] and the same 16
+// further on, the k order in which unpack_word delivers the codes.
+__device__ __forceinline__ void frag_store4(uint8_t* xf, int e, uint32_t h01, uint32_t h23) {
+  const int b = e >> 5, i = e & 31;
+  const int off = ((b << 2) + ((i & 15) >> 2)) * 16 + ((i >> 4) << 3);
+  *reinterpret_cast<uint2*>(xf + off) = make_uint2(__byte_perm(h01, h23, 0x5410), __byte_perm(h01, h23, 0x7632));
+}
+
+// CTA 0 also leaves the formed input of a phase: natural binary16 in x_dbg and
+// tagged binary16 words in xr_out (the residual base a later phase reads).
+__device__ __forceinline__ void store_formed4(const Phase& ph, int e, uint32_t h01, uint32_t h23, uint32_t tag16) {
+  if (ph.x_dbg) *reinterpret_cast<uint2*>(ph.x_dbg + e) = make_uint2(h01, h23);
+  if (ph.xr_out) {
+    const uint32_t t = tag16 << 16;
+    st_relaxed_v4(ph.xr_out + e, make_uint4((h01 & 0xFFFFu) | t, (h01 >> 16) | t, (h23 & 0xFFFFu) | t, (h23 >> 16) | t));
   }
 }
 
-// Request unit (p, u)'s rows into L2, the pieces spread over the warp's lanes.
-__device__ __forceinline__ uint32_t prefetch_unit(const Phase& ph, int u, int lane) {
-  const uint32_t row_bytes = static_cast<uint32_t>(ph.k / kQK) * kBlockBytes;
-  const int row0 = u * ph.rows_per_unit;
-  const int rows = min(ph.rows_per_unit, ph.n_rows - row0);
-  const uint32_t bytes = static_cast<uint32_t>(rows) * row_bytes;   // rows of a unit are contiguous
-  const int mats = ph.epi_kind == EPI_SILU ? 2 : 1;
-  const uint32_t pieces = (bytes + kTcPrefetchPiece - 1) / kTcPrefetchPiece;
-  for (uint32_t i = lane; i < mats * pieces; i += 32) {
-    const uint8_t* base = (i < pieces ? ph.w0 : ph.w1) + static_cast<size_t>(row0) * row_bytes;
-    const uint32_t off = (i % pieces) * kTcPrefetchPiece;
-    bulk_prefetch_l2(base + off, min(kTcPrefetchPiece, bytes - off));
-  }
-  return bytes * mats;
-}
-
-// The phase input in fragment order: for block b and lane quarter t, 16
-// bytes holding x[32b + 4t + {0, 2, 1, 3}] and x[32b + 16 + 4t + {0, 2, 1, 3}]
-// (the k order in which unpack_word delivers the weights).  The values are
-// formed per XKind; CTA 0 also stores the formed x in natural order to
-// x_dbg when asked.  All loads of a pass are issued before its arithmetic.
-__device__ void tc_form_x(const Phase& ph, uint4* xf, float sumsq, int tid, bool dbg) {
-  const bool norm = ph.x_kind == X_NORM16 || ph.x_kind == X_NORM32;
-  const float r = norm ? rsqrtf(sumsq / static_cast<float>(ph.k) + ph.eps) : 1.0f;
-  const int nf = ph.k >> 3;
-  constexpr int kPass = 4;
-  for (int f0 = tid; f0 < nf; f0 += kPass * kTcConsumers) {
-    float v[kPass][8];
+// The RMSNorm input of a phase (k values, at most 8192): staged in
+// registers, 4 consecutive values per chunk, chunk i = tid + c * 256.  Tagged
+// fp32 words are polled until every tag is `want`; a plain binary16 input is
+// read once.  The sum of squares runs over each thread's chunks in order,
+// then the warp tree, then the 8 warps in order: an order fixed by k alone.
+// Returns the scale 1 / sqrt(mean(t^2) + eps); v holds the values.
+__device__ __forceinline__ float stage_norm(const Phase& ph, uint32_t want, uint32_t limit, Control* ctl, float* red_cta,
+                                            int tid, float (&v)[kTcNormChunks][4]) {
+  const int n4 = ph.k >> 2;
+  if (ph.x_kind == X_NORM16) {
 #pragma unroll
-    for (int q = 0; q < kPass; ++q) {
-      const int f = f0 + q * kTcConsumers;
-      if (f >= nf) break;
-      const int e0 = 32 * (f >> 2) + 4 * (f & 3);
+    for (int c = 0; c < kTcNormChunks; ++c) {
+      const int i = tid + c * kTcConsumers;
+      if (i < n4) {
+        const uint2 u = __ldcg(reinterpret_cast<const uint2*>(ph.x_src) + i);
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+        v[c][0] = a.x;
+        v[c][1] = a.y;
+        v[c][2] = b.x;
+        v[c][3] = b.y;
+      }
+    }
+  } else {   // X_TAG32_NORM: 64-bit words {fp32 value, tag}
+    const uint4* src = static_cast<const uint4*>(ph.x_src);
+    bool ok = false;
+    for (uint32_t it = 0; it < limit && !ok; ++it) {
+      ok = true;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int e = e0 + 16 * h;
-        if (ph.x_kind == X_F16 || ph.x_kind == X_NORM16) {
-          const uint2 u = __ldcg(reinterpret_cast<const uint2*>(static_cast<const __half*>(ph.x_src) + e));
-          const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
-          const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
-          v[q][4 * h] = a.x;
-          v[q][4 * h + 1] = a.y;
-          v[q][4 * h + 2] = b.x;
-          v[q][4 * h + 3] = b.y;
-        } else {
-          int src = e;
-          if (ph.x_kind == X_ATTN) src = ph.attn_off + ((e / ph.head_dim) / ph.group) * ph.head_dim + e % ph.head_dim;
-          const float4 a = __ldcg(reinterpret_cast<const float4*>(static_cast<const float*>(ph.x_src) + src));
-          v[q][4 * h] = a.x;
-          v[q][4 * h + 1] = a.y;
-          v[q][4 * h + 2] = a.z;
-          v[q][4 * h + 3] = a.w;
+      for (int c = 0; c < kTcNormChunks; ++c) {
+        const int i = tid + c * kTcConsumers;
+        if (i < n4) {
+          const uint4 a = ld_relaxed_v4(src + 2 * i);
+          const uint4 b = ld_relaxed_v4(src + 2 * i + 1);
+          ok &= a.y == want && a.w == want && b.y == want && b.w == want;
+          v[c][0] = __uint_as_float(a.x);
+          v[c][1] = __uint_as_float(a.z);
+          v[c][2] = __uint_as_float(b.x);
+          v[c][3] = __uint_as_float(b.z);
         }
       }
+      if (!ok && it >= 2) __nanosleep(32);
     }
-#pragma unroll
-    for (int q = 0; q < kPass; ++q) {
-      const int f = f0 + q * kTcConsumers;
-      if (f >= nf) break;
-      __half2 h[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        h[i] = norm ? __floats2half2_rn(v[q][2 * i] * r, v[q][2 * i + 1] * r)
-                    : __floats2half2_rn(v[q][2 * i], v[q][2 * i + 1]);
-      // natural order: h[0] = (e0, e0+1), h[1] = (e0+2, e0+3), h[2], h[3] the same 16 further
-      uint4 o;
-      o.x = __byte_perm(*reinterpret_cast<uint32_t*>(&h[0]), *reinterpret_cast<uint32_t*>(&h[1]), 0x5410);
-      o.y = __byte_perm(*reinterpret_cast<uint32_t*>(&h[0]), *reinterpret_cast<uint32_t*>(&h[1]), 0x7632);
-      o.z = __byte_perm(*reinterpret_cast<uint32_t*>(&h[2]), *reinterpret_cast<uint32_t*>(&h[3]), 0x5410);
-      o.w = __byte_perm(*reinterpret_cast<uint32_t*>(&h[2]), *reinterpret_cast<uint32_t*>(&h[3]), 0x7632);
-      xf[f] = o;
-      if (dbg) {
-        const int e0 = 32 * (f >> 2) + 4 * (f & 3);
-        uint2 lo, hi;
-        lo.x = *reinterpret_cast<uint32_t*>(&h[0]);
-        lo.y = *reinterpret_cast<uint32_t*>(&h[1]);
-        hi.x = *reinterpret_cast<uint32_t*>(&h[2]);
-        hi.y = *reinterpret_cast<uint32_t*>(&h[3]);
-        *reinterpret_cast<uint2*>(ph.x_dbg + e0) = lo;
-        *reinterpret_cast<uint2*>(ph.x_dbg + e0 + 16) = hi;
-      }
-    }
+    if (!ok) tc_set_status(ctl, ST_DATA_TIMEOUT);
   }
-}
-
-// Sum the 16 warps' partials of the n_buf buffered units (the CTA's units
-// u_first, u_first + G, ...) in a fixed order and run the epilogue of their
-// rows.  All consumer threads take part.  Returns the thread's sum of squares
-// of the residual sums it wrote (EPI_RESID), for the next RMSNorm.
-__device__ float tc_flush(const Phase& ph, const float* red, int n_buf, int u_first, int G, int tid, bool reuse) {
-  named_bar_sync(1, kTcConsumers);
   float ss = 0.f;
-  if (ph.epi_kind != EPI_SILU) {
-    for (int o = tid; o < n_buf * 16; o += kTcConsumers) {
-      const int s = o >> 4, m = o & 15;
-      const float* pr = red + s * kTcWarps * 16 + m;
-      float v = 0.f;
 #pragma unroll
-      for (int w = 0; w < kTcWarps; ++w) v += pr[w * 16];
-      const int n = (u_first + s * G) * 16 + m;
-      if (n < ph.n_rows) {
-        ph.y[n] = v;
-        if (ph.epi_kind == EPI_RESID) {
-          const float tv = __half2float(__ushort_as_half(ph.res[n])) + v;
-          ph.y2[n] = tv;
-          ss = fmaf(tv, tv, ss);
+  for (int c = 0; c < kTcNormChunks; ++c)
+    if (tid + c * kTcConsumers < n4)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) ss = fmaf(v[c][q], v[c][q], ss);
+  ss = warp_sum(ss);
+  if ((tid & 31) == 0) red_cta[tid >> 5] = ss;
+  named_bar_sync(1, kTcConsumers);
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < kTcWarps; ++w) tot += red_cta[w];
+  return rsqrtf(tot / static_cast<float>(ph.k) + ph.eps);
+}
+
+// Tagged binary16 words (X_TAG16: x = the k values; X_TAG16_ATTN: the xt_n
+// values of v, each 4-value chunk of a value head copied to the `group` query
+// heads that read it) polled until every tag is `want16`, into the fragment
+// buffer.  Each pass reloads all of the thread's chunks and stores them.
+__device__ __forceinline__ void stage_tag16(const Phase& ph, uint8_t* xf, uint32_t want16, uint32_t limit, Control* ctl,
+                                            int tid, bool cta0) {
+  const bool attn = ph.x_kind == X_TAG16_ATTN;
+  const int n4 = (attn ? ph.xt_n : ph.k) >> 2;
+  const uint4* src = static_cast<const uint4*>(ph.x_src);
+  const uint32_t want = want16 << 16;
+  bool ok = false;
+  for (uint32_t it = 0; it < limit && !ok; ++it) {
+    ok = true;
+    for (int i = tid; i < n4; i += kTcConsumers) {
+      const uint4 w = ld_relaxed_v4(src + i);
+      ok &= (((w.x ^ want) | (w.y ^ want) | (w.z ^ want) | (w.w ^ want)) >> 16) == 0u;
+      const uint32_t h01 = __byte_perm(w.x, w.y, 0x5410), h23 = __byte_perm(w.z, w.w, 0x5410);
+      const int e = 4 * i;
+      if (!attn) {
+        frag_store4(xf, e, h01, h23);
+      } else {
+        const int hd = ph.head_dim;
+        const int x0 = (e / hd) * ph.group * hd + e % hd;
+        for (int h = 0; h < ph.group; ++h) frag_store4(xf, x0 + h * hd, h01, h23);
+      }
+    }
+    if (!ok && it >= 2) __nanosleep(32);
+  }
+  if (!ok) tc_set_status(ctl, ST_DATA_TIMEOUT);
+  if (cta0 && (ph.x_dbg || ph.xr_out)) {
+    // The formed x in natural order.  Its chunks were polled by other threads:
+    // after the barrier every word carries its tag (re-checked, bounded).
+    named_bar_sync(1, kTcConsumers);
+    const int k4 = ph.k >> 2;
+    for (int i = tid; i < k4; i += kTcConsumers) {
+      int s = i;
+      if (attn) {
+        const int e = 4 * i, hd = ph.head_dim;
+        s = (((e / hd) / ph.group) * hd + e % hd) >> 2;
+      }
+      uint4 w = ld_relaxed_v4(src + s);
+      for (uint32_t it = 0; (((w.x ^ want) | (w.y ^ want) | (w.z ^ want) | (w.w ^ want)) >> 16) != 0u && it < limit;
+           ++it)
+        w = ld_relaxed_v4(src + s);
+      store_formed4(ph, 4 * i, __byte_perm(w.x, w.y, 0x5410), __byte_perm(w.z, w.w, 0x5410), want16);
+    }
+  }
+}
+
+// A plain binary16 input (single products) into the fragment buffer.
+__device__ __forceinline__ void stage_plain16(const Phase& ph, uint8_t* xf, int tid) {
+  const int n4 = ph.k >> 2;
+  for (int i = tid; i < n4; i += kTcConsumers) {
+    const uint2 u = __ldcg(reinterpret_cast<const uint2*>(ph.x_src) + i);
+    frag_store4(xf, 4 * i, u.x, u.y);
+  }
+}
+
+// The prologue of a phase for a CTA that reads its input: wait for the
+// previous layer's flags where the phase asks for it, stage the whole input
+// in fragment order (normalised for the RMSNorm inputs), meet at a barrier of
+// the consumer warps.  Out of line: the unit loop's registers are allocated
+// without the staging loads.
+__device__ __noinline__ void tc_prologue(const Phase& ph, unsigned tag, uint32_t lim, Control* ctl,
+                                         const unsigned long long* flags, uint8_t* xf, float* red_cta, int tid,
+                                         bool cta0) {
+  const int warp = tid >> 5, lane = tid & 31;
+  if (ph.sync == SYNC_WAIT && warp == 0) wait_phase_flags(flags, tag - 1u, lane, lim, ctl);
+  if (ph.sync == SYNC_WAIT) named_bar_sync(1, kTcConsumers);
+  if (ph.x_kind == X_NORM16 || ph.x_kind == X_TAG32_NORM) {
+    float v[kTcNormChunks][4];
+    const float r = stage_norm(ph, tag - 1u, lim, ctl, red_cta, tid, v);
+    const int n4 = ph.k >> 2;
+#pragma unroll
+    for (int c = 0; c < kTcNormChunks; ++c) {
+      const int i = tid + c * kTcConsumers;
+      if (i < n4) {
+        const __half2 a = __floats2half2_rn(v[c][0] * r, v[c][1] * r);
+        const __half2 b = __floats2half2_rn(v[c][2] * r, v[c][3] * r);
+        const uint32_t h01 = *reinterpret_cast<const uint32_t*>(&a), h23 = *reinterpret_cast<const uint32_t*>(&b);
+        frag_store4(xf, 4 * i, h01, h23);
+        if (cta0) store_formed4(ph, 4 * i, h01, h23, tag & 0xFFFFu);
+      }
+    }
+  } else if (ph.x_kind == X_F16) {
+    stage_plain16(ph, xf, tid);
+  } else {
+    stage_tag16(ph, xf, (tag - 1u) & 0xFFFFu, lim, ctl, tid, cta0);
+  }
+  named_bar_sync(1, kTcConsumers);
+}
+
+// ------------------------------------------------------------------ compute
+
+__device__ __forceinline__ float lo_half_f(uint32_t w) { return __low2float(*reinterpret_cast<const __half2*>(&w)); }
+__device__ __forceinline__ float hi_half_f(uint32_t w) { return __high2float(*reinterpret_cast<const __half2*>(&w)); }
+
+// One block pair (even block, odd block after it) of tile rows g and g + 8:
+// rg, rh point at the pair's 36 bytes in the two staged rows.  ee/eh collect
+// the even block (valid in lane quarter 0), og/oh the odd one (quarter 3).
+__device__ __forceinline__ void pair_mma(const uint8_t* rg, const uint8_t* rh, int t, const uint4& xe, const uint4& xo,
+                                         uint32_t magic, float& eg, float& eh, float& og, float& oh) {
+  const uint32_t* pg = reinterpret_cast<const uint32_t*>(rg);
+  const uint32_t* ph = reinterpret_cast<const uint32_t*>(rh);
+  const uint32_t g0 = pg[t], g1 = pg[t + 1], go = pg[5 + t];
+  const uint32_t h0 = ph[t], h1 = ph[t + 1], ho = ph[5 + t];
+  uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+  // even block: its code bytes start 2 bytes into the pair, word t is a funnel of words t, t+1
+  unpack_word(__funnelshift_r(g0, g1, 16), magic, a0, a1, a2, a3);
+  unpack_word(__funnelshift_r(h0, h1, 16), magic, b0, b1, b2, b3);
+  float c[4] = {0.f, 0.f, 0.f, 0.f};
+  mma16816(c, a0, b0, a1, b1, xe.x, xe.y);
+  mma16816(c, a2, b2, a3, b3, xe.z, xe.w);
+  eg = fmaf(lo_half_f(g0), c[0], eg);   // quarter 0: word 0 starts with the even block's d
+  eh = fmaf(lo_half_f(h0), c[2], eh);
+  // odd block: code words 5..8 of the pair, 4-byte aligned
+  unpack_word(go, magic, a0, a1, a2, a3);
+  unpack_word(ho, magic, b0, b1, b2, b3);
+  float e[4] = {0.f, 0.f, 0.f, 0.f};
+  mma16816(e, a0, b0, a1, b1, xo.x, xo.y);
+  mma16816(e, a2, b2, a3, b3, xo.z, xo.w);
+  og = fmaf(hi_half_f(g1), e[0], og);   // quarter 3: word 4 ends with the odd block's d
+  oh = fmaf(hi_half_f(h1), e[2], oh);
+}
+
+// The products of one unit for one consumer warp, chunk by chunk as the
+// stages land: four block pairs of every chunk (pairs warp + 8q) and
+// both 16-row halves of the tile.  WIDE: rows wider than 2048 columns (64-block
+// chunks, 1168-byte staged rows), with the geometry as constants; otherwise
+// the chunk is the whole row.  acc[m] = {even-block sums of rows g, g + 8,
+// odd-block sums of rows g, g + 8} of half m.
+template <bool WIDE>
+__device__ __forceinline__ void unit_products(const uint8_t* ring, uint32_t SB, int S, int& slot, uint32_t& use,
+                                              uint64_t* full_bar, uint64_t* empty_bar, volatile int* abort_flag,
+                                              const uint4* xf4, int chunks, int cb_rt, int pitch_rt, int warp,
+                                              int lane, uint32_t magic, uint32_t wait_limit, Control* ctl,
+                                              float (&acc)[2][4]) {
+  const int cb = WIDE ? 64 : cb_rt;
+  const int pitch = WIDE ? 64 * kBlockBytes + 16 : pitch_rt;
+  const int g = lane >> 2, t = lane & 3;
+  for (int c = 0; c < chunks; ++c) {
+    // After a failed wait the CTA keeps walking its units without waiting
+    // (reading whatever the stage holds) so that every barrier is still
+    // reached; the launch then reports the failure in its status.
+    if (!*abort_flag && !mbar_wait_bounded(&full_bar[slot], use & 1, wait_limit)) {
+      tc_set_status(ctl, ST_FULL_TIMEOUT);
+      *abort_flag = 1;
+    }
+    const uint8_t* sb = ring + static_cast<size_t>(slot) * SB;
+#pragma unroll(WIDE ? kTcPairsPerWarp : 1)
+    for (int q = 0; q < kTcPairsPerWarp; ++q) {
+      const int pp = warp + kTcWarps * q;   // block pair of the chunk
+      if (WIDE || 2 * pp < cb) {
+        const int blk = c * cb + 2 * pp;
+        const uint4 xe = xf4[blk * 4 + t], xo = xf4[(blk + 1) * 4 + t];
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          const uint8_t* rg = sb + (m * 16 + g) * pitch + 36 * pp;
+          pair_mma(rg, rg + 8 * pitch, t, xe, xo, magic, acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
         }
       }
     }
-  } else {
-    for (int o = tid; o < n_buf * 8; o += kTcConsumers) {
-      const int s = o >> 3, m = o & 7;
-      const float* pr = red + s * kTcWarps * 16 + m;
-      float g = 0.f, u = 0.f;
-#pragma unroll
-      for (int w = 0; w < kTcWarps; ++w) {
-        g += pr[w * 16];
-        u += pr[w * 16 + 8];
-      }
-      const int n = (u_first + s * G) * 8 + m;
-      if (n < ph.n_rows) {
-        ph.y[n] = g;
-        ph.y2[n] = u;
-        ph.aux16[n] = __half_as_ushort(__float2half_rn(silu_mul(g, u)));
-      }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty_bar[slot]);
+    if (++slot == S) {
+      slot = 0;
+      ++use;
     }
   }
-  if (reuse) named_bar_sync(1, kTcConsumers);   // red is written again in this phase
-  return ss;
 }
+
+// ------------------------------------------------------------------ epilogue
+
+// A tagged residual input word, polled until it carries tag16.
+__device__ __forceinline__ unsigned short tc_tagged_res(const uint32_t* p, uint32_t tag16, uint32_t limit,
+                                                        Control* ctl) {
+  uint32_t w = ld_relaxed_b32(p);
+  for (uint32_t it = 0; (w >> 16) != tag16 && it < limit; ++it) {
+    __nanosleep(32);
+    w = ld_relaxed_b32(p);
+  }
+  if ((w >> 16) != tag16) tc_set_status(ctl, ST_DATA_TIMEOUT);
+  return static_cast<unsigned short>(w & 0xFFFFu);
+}
+
+// The outputs of one row (lane) of a finished unit.  Tagged programs hand the
+// next phase its input as tagged words with this phase's tag; the plain
+// outputs are written where the phase has them.
+__device__ __forceinline__ void tc_epilogue_row(const Phase& ph, int n, float v, float u2, bool tagged, uint32_t tag,
+                                                uint32_t lim, Control* ctl) {
+  const uint32_t tag16 = tag & 0xFFFFu;
+  if (ph.epi_kind == EPI_SILU) {
+    if (ph.y) ph.y[n] = v;
+    if (ph.y2) ph.y2[n] = u2;
+    const unsigned short a16 = __half_as_ushort(__float2half_rn(silu_mul(v, u2)));
+    if (ph.aux16) ph.aux16[n] = a16;
+    if (tagged) st_relaxed_b32(static_cast<uint32_t*>(ph.yt) + n, (tag16 << 16) | a16);
+  } else if (ph.epi_kind == EPI_RESID) {
+    if (ph.y) ph.y[n] = v;
+    const unsigned short rv = tc_tagged_res(ph.res_t + n, (tag - 1u) & 0xFFFFu, lim, ctl);
+    const float tv = __half2float(__ushort_as_half(rv)) + v;
+    if (ph.y2) ph.y2[n] = tv;
+    st_relaxed_b64(static_cast<unsigned long long*>(ph.yt) + n,
+                   (static_cast<unsigned long long>(tag) << 32) | __float_as_uint(tv));
+  } else {
+    if (ph.y) ph.y[n] = v;
+    const int e = n - ph.yt_off;
+    if (tagged && ph.yt && e >= 0 && e < ph.yt_n)
+      st_relaxed_b32(static_cast<uint32_t*>(ph.yt) + e, (tag16 << 16) | __half_as_ushort(__float2half_rn(v)));
+  }
+}
+
+// ------------------------------------------------------------------ kernel
 
 __global__ void __launch_bounds__(kTcThreads, 1) tc_engine_kernel(const __grid_constant__ EngineArgs a) {
-  __shared__ __align__(8) uint64_t full_bar[kTcStages];
-  __shared__ __align__(8) uint64_t empty_bar[kTcStages];
-  __shared__ float red[kTcRedUnits * kTcWarps * 16];
+  __shared__ __align__(8) uint64_t full_bar[kTcMaxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kTcMaxStages];
+  __shared__ __align__(8) uint64_t rfull_bar[kTcRedSlots];
+  __shared__ __align__(8) uint64_t rempty_bar[kTcRedSlots];
   __shared__ float red_cta[kTcWarps];
   __shared__ volatile int abort_flag;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x, cta = blockIdx.x;
-  uint8_t* ring = g_tc_smem;
-  uint4* xf = reinterpret_cast<uint4*>(g_tc_smem + kTcStages * kTcStageBytes);
+  const int S = a.stages;
+  const uint32_t SB = a.stage_bytes;
+  uint8_t* const ring = g_tc_smem;
+  uint8_t* const xf = g_tc_smem + static_cast<size_t>(S) * SB;
+  float* const red = reinterpret_cast<float*>(xf + 4 * static_cast<size_t>(a.xbuf_floats));
+  const bool tagged = a.tagged != 0;
 
   if (tid == 0) {
-    for (int s = 0; s < kTcStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], kTcWarps);
+    }
+    for (int s = 0; s < kTcRedSlots; ++s) {
+      mbar_init(&rfull_bar[s], kTcWarps);
+      mbar_init(&rempty_bar[s], 1);
     }
     fence_mbar_init();
     abort_flag = 0;
   }
   __syncthreads();
 
-  if (warp == kTcWarps) {
+  const unsigned tag0 = tagged ? a.ctl->epoch * kPhasesPerEpoch + 1u : 0u;
+
+  if (warp == kTcProdWarp) {
     // ------------------------------------------------------------ producer
-    uint32_t it = 0;
-    Walk pf{0, first_unit(phase_at(a, 0), cta, G)};   // the L2 prefetch cursor runs ahead of the copies
-    walk_settle(pf, a, cta, G);
-    unsigned long long copied = 0, requested = 0;
-    bool stop = false;
-    for (int p = 0; p < a.n_phases && !stop; ++p) {
-      const Phase& ph = phase_at(a, p);
-      const uint32_t row_bytes = static_cast<uint32_t>(ph.k / kQK) * kBlockBytes;
-      const int nb = ph.k / kQK;
-      const int chunks = (nb + kTcChunk - 1) / kTcChunk;
-      const bool dual = ph.epi_kind == EPI_SILU;
-      const int rpu = ph.rows_per_unit;
-      for (int u = first_unit(ph, cta, G); u < ph.units && !stop; u += G) {
-        const int row0 = u * rpu;
-        const int rows = min(rpu, ph.n_rows - row0);
-        if (a.prefetch_bytes) {
-          while (pf.p < a.n_phases && requested < copied + a.prefetch_bytes) {
-            requested += prefetch_unit(phase_at(a, pf.p), pf.u, lane);
-            pf.u += G;
-            walk_settle(pf, a, cta, G);
-          }
+    if (lane == 0) {
+      uint32_t it = 0;
+      int slot = 0;
+      uint32_t use = 0;
+      for (int p = 0; p < a.n_phases && !abort_flag; ++p) {
+        const Phase& ph = phase_at(a, p);
+        if (a.phases && ph.units > 0) {
+          // descriptors written by the host into global memory: order their use
+          // through the tensor-map proxy after the generic-proxy writes
+          tensormap_acquire(&ph.tm0);
+          if (ph.epi_kind == EPI_SILU) tensormap_acquire(&ph.tm1);
         }
-        for (int c = 0; c < chunks; ++c) {
-          const int stage = it % kTcStages;
-          const uint32_t n = it / kTcStages;
-          int ok = 1;
-          if (lane == 0 && n > 0 && !mbar_wait_bounded(&empty_bar[stage], (n - 1) & 1, a.wait_limit)) {
-            tc_set_status(a.ctl, ST_EMPTY_TIMEOUT);
-            abort_flag = 1;
-            ok = 0;
-          }
-          ok = __shfl_sync(0xffffffffu, ok, 0) && !abort_flag;
-          if (!ok) {
-            stop = true;
-            break;
-          }
-          const int blk0 = c * kTcChunk;
-          const uint32_t seg = static_cast<uint32_t>(min(kTcChunk, nb - blk0)) * kBlockBytes;
-          if (lane == 0) mbar_arrive_expect_tx(&full_bar[stage], seg * rows * (dual ? 2 : 1));
-          __syncwarp();
-          if (lane < 16) {
-            const int r = dual ? (lane & 7) : lane;
-            if (r < rows) {
-              const uint8_t* src = (dual && lane >= 8 ? ph.w1 : ph.w0) + static_cast<size_t>(row0 + r) * row_bytes +
-                                   static_cast<size_t>(blk0) * kBlockBytes;
-              bulk_g2s(ring + static_cast<size_t>(stage) * kTcStageBytes + lane * kTcPitch, src, seg,
-                       &full_bar[stage]);
+        const int chunks = tc_chunks(ph.k);
+        const int cx = tc_chunk_blocks(ph.k) * kBlockBytes / 8;   // chunk stride in 64-bit columns
+        const int pitch = tc_pitch(ph.k);
+        const bool dual = ph.epi_kind == EPI_SILU;
+        const uint32_t bytes = static_cast<uint32_t>(pitch) * kTcUnitRows;
+        const int units = ph.units;
+        for (int u = first_unit(ph, cta, G); u < units && !abort_flag; u += G) {
+          for (int c = 0; c < chunks; ++c) {
+            if (use > 0 && !mbar_wait_bounded(&empty_bar[slot], (use - 1) & 1, a.wait_limit)) {
+              tc_set_status(a.ctl, ST_EMPTY_TIMEOUT);
+              abort_flag = 1;
+              break;
+            }
+            uint8_t* dst = ring + static_cast<size_t>(slot) * SB;
+            mbar_arrive_expect_tx(&full_bar[slot], bytes);
+            if (dual) {
+              tma_load_2d(dst, &ph.tm0, c * cx, u * (kTcUnitRows / 2), &full_bar[slot]);
+              tma_load_2d(dst + (kTcUnitRows / 2) * pitch, &ph.tm1, c * cx, u * (kTcUnitRows / 2), &full_bar[slot]);
+            } else {
+              tma_load_2d(dst, &ph.tm0, c * cx, u * kTcUnitRows, &full_bar[slot]);
+            }
+            ++it;
+            if (++slot == S) {
+              slot = 0;
+              ++use;
             }
           }
-          ++it;
         }
-        copied += static_cast<unsigned long long>(rows) * row_bytes * (dual ? 2 : 1);
+      }
+      // Drain: no copy may still be in flight when the CTA exits.
+      const uint32_t issued = it;
+      for (int s = 0; s < S && static_cast<uint32_t>(s) < issued; ++s) {
+        const uint32_t last = (issued - 1 - s) / S;
+        if (!mbar_wait_bounded(&full_bar[s], last & 1, a.wait_limit)) tc_set_status(a.ctl, ST_DRAIN_TIMEOUT);
       }
     }
-    // Drain: no copy may still be in flight when the CTA exits.
-    if (lane == 0) {
-      const uint32_t issued = it;
-      for (int s = 0; s < kTcStages && static_cast<uint32_t>(s) < issued; ++s) {
-        const uint32_t last = (issued - 1 - s) / kTcStages;
-        if (!mbar_wait_bounded(&full_bar[s], last & 1, a.wait_limit)) tc_set_status(a.ctl, ST_DRAIN_TIMEOUT);
+  } else if (warp == kTcEpiWarp) {
+    // ------------------------------------------------------------ epilogue
+    int rs = 0;
+    uint32_t ruse = 0;
+    const uint32_t st0 = tagged ? ld_relaxed_b32(&a.ctl->status) : 0u;
+    for (int p = 0; p < a.n_phases; ++p) {
+      const Phase& ph = phase_at(a, p);
+      const unsigned tag = tag0 + static_cast<unsigned>(ph.gidx);
+      const bool dual = ph.epi_kind == EPI_SILU;
+      const int units = ph.units;
+      for (int u = first_unit(ph, cta, G); u < units; u += G) {
+        // once a wait of this launch has run out, the residual polls give up at once
+        const uint32_t lim = tagged && ld_relaxed_b32(&a.ctl->status) != st0 ? 0u : a.wait_limit;
+        if (!mbar_wait_bounded(&rfull_bar[rs], ruse & 1, a.wait_limit)) tc_set_status(a.ctl, ST_FULL_TIMEOUT);
+        const float* pr = red + rs * (kTcWarps * kTcUnitRows);
+        float v = 0.f, u2 = 0.f;
+#pragma unroll
+        for (int w = 0; w < kTcWarps; ++w) v += pr[w * kTcUnitRows + lane];
+        if (dual) u2 = __shfl_down_sync(0xffffffffu, v, 16);   // up row r sits 16 rows below gate row r
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&rempty_bar[rs]);
+        if (++rs == kTcRedSlots) {
+          rs = 0;
+          ++ruse;
+        }
+        const int n = u * (dual ? kTcUnitRows / 2 : kTcUnitRows) + lane;
+        if ((!dual || lane < kTcUnitRows / 2) && n < ph.n_rows) tc_epilogue_row(ph, n, v, u2, tagged, tag, lim, a.ctl);
       }
     }
   } else {
@@ -306,130 +498,94 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_engine_kernel(const __grid_c
     const int g = lane >> 2, t = lane & 3;
     uint32_t magic;
     asm volatile("mov.b32 %0, 0x64006400;" : "=r"(magic));
-    uint32_t it = 0;
-    const unsigned tag0 = a.n_phases > 1 ? a.ctl->epoch * kPhasesPerEpoch + 1u : 0u;   // tag of phase 0
+    int slot = 0;
+    uint32_t use = 0;
+    int rs = 0;
+    uint32_t ruse = 0;
+    const uint32_t st0 = tagged ? ld_relaxed_b32(&a.ctl->status) : 0u;
     for (int p = 0; p < a.n_phases; ++p) {
       const Phase& ph = phase_at(a, p);
-      const int units = ph.units;
-      const int nb = ph.k / kQK;
-      const int chunks = (nb + kTcChunk - 1) / kTcChunk;
+      const unsigned tag = tag0 + static_cast<unsigned>(ph.gidx);
+      const uint32_t lim = tagged && ld_relaxed_b32(&a.ctl->status) != st0 ? 0u : a.wait_limit;
       const int u0 = first_unit(ph, cta, G);
-      // Every CTA waits for all CTAs' flags of the previous phase, even with no
-      // units of its own here: a CTA may never publish phase p's flag while
-      // another can still be reading phase p - 2's flags from the same slot.
-      float sumsq = 0.f;
-      if (p > 0) {
-        // one warp polls every CTA's flag, the CTA barrier releases the others
-        if (warp == 0) {
-          const float v = wait_phase_flags(a.flags + ((p - 1) & 1) * kMaxGrid, tag0 + (p - 1), lane,
-                                           a.wait_limit, a.ctl);
-          if (lane == 0) red_cta[0] = v;
-        }
-        named_bar_sync(1, kTcConsumers);
-        sumsq = red_cta[0];
-      }
-      if (u0 < units || (ph.x_dbg && cta == 0)) {
-        if (p == 0 && ph.x_kind == X_NORM32) sumsq = sum_ss_array(ph.ss_in, lane);   // from an earlier launch
-        if (ph.x_kind == X_NORM16) sumsq = input_sumsq16(ph, lane);
-        tc_form_x(ph, xf, sumsq, tid, ph.x_dbg != nullptr && cta == 0);
-        named_bar_sync(1, kTcConsumers);   // xf complete before any warp reads it
-      }
-      int n_buf = 0, u_first = u0;
-      float ss = 0.f;
+      const bool cta0 = cta == 0 && (ph.x_dbg || ph.xr_out);
+      // every consumer warp is done with the previous phase's input
+      named_bar_sync(1, kTcConsumers);
+      if (u0 < ph.units || cta0) tc_prologue(ph, tag, lim, a.ctl, a.flags, xf, red_cta, tid, cta0);
+      if (ph.sync == SYNC_PUBLISH && tid == 0) st_release_u64(a.flags + cta, static_cast<unsigned long long>(tag) << 32);
+      asm volatile("" ::: "memory");
+      const int chunks = tc_chunks(ph.k);
+      const int cb = tc_chunk_blocks(ph.k);
+      const int pitch = tc_pitch(ph.k);
+      const bool wide = ph.k > 2048;
+      const int units = ph.units;
+      const uint4* xf4 = reinterpret_cast<const uint4*>(xf);
       for (int u = u0; u < units; u += G) {
-        if (n_buf == kTcRedUnits) {
-          ss += tc_flush(ph, red, n_buf, u_first, G, tid, true);
-          n_buf = 0;
-          u_first = u;
-        }
-        float acc0 = 0.f, acc1 = 0.f;
-        for (int c = 0; c < chunks; ++c) {
-          const int stage = it % kTcStages;
-          const uint32_t n = it / kTcStages;
-          // After a failed wait the CTA keeps walking its units without
-          // waiting so that every barrier is still reached; the launch then
-          // reports the failure in its status.
-          if (!abort_flag && !mbar_wait_bounded(&full_bar[stage], n & 1, a.wait_limit)) {
-            tc_set_status(a.ctl, ST_FULL_TIMEOUT);
-            abort_flag = 1;
-          }
-          const uint8_t* sb = ring + static_cast<size_t>(stage) * kTcStageBytes;
-          const uint8_t* rg = sb + g * kTcPitch;
-          const uint8_t* rh = sb + (g + 8) * kTcPitch;
-          const int nblk = min(kTcChunk, nb - c * kTcChunk);
+        float acc[2][4] = {};
+        if (wide)
+          unit_products<true>(ring, SB, S, slot, use, full_bar, empty_bar, &abort_flag, xf4, chunks, cb, pitch, warp,
+                              lane, magic, a.wait_limit, a.ctl, acc);
+        else
+          unit_products<false>(ring, SB, S, slot, use, full_bar, empty_bar, &abort_flag, xf4, chunks, cb, pitch, warp,
+                               lane, magic, a.wait_limit, a.ctl, acc);
+        // lane (g, 0) adds the odd blocks of lane (g, 3); rows g and g + 8 of each half
+        float r[2][2];
 #pragma unroll
-          for (int i = 0; i < kTcChunk / kTcWarps; ++i) {
-            const int b = warp + kTcWarps * i;   // block within the chunk (parity = warp parity)
-            if (b < nblk) {
-              const uint4 xv = xf[(c * kTcChunk + b) * 4 + t];
-              uint32_t gl02, gl13, gh02, gh13, hl02, hl13, hh02, hh13;
-              unpack_word(code_word(rg, b, t), magic, gl02, gl13, gh02, gh13);
-              unpack_word(code_word(rh, b, t), magic, hl02, hl13, hh02, hh13);
-              const float dg = row_scale(rg, b), dh = row_scale(rh, b);
-              float cb[4] = {0.f, 0.f, 0.f, 0.f};
-              mma16816(cb, gl02, hl02, gl13, hl13, xv.x, xv.y);
-              mma16816(cb, gh02, hh02, gh13, hh13, xv.z, xv.w);
-              acc0 = fmaf(dg, cb[0], acc0);
-              acc1 = fmaf(dh, cb[2], acc1);
-            }
-          }
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) r[m][h] = acc[m][h] + __shfl_sync(0xffffffffu, acc[m][2 + h], lane | 3);
+        if (ruse > 0) {
+          // slot rs's previous unit (use ruse - 1) has been read by the epilogue
+          if (lane == 0 && !mbar_wait_bounded(&rempty_bar[rs], (ruse - 1) & 1, a.wait_limit))
+            tc_set_status(a.ctl, ST_EMPTY_TIMEOUT);
           __syncwarp();
-          if (lane == 0) mbar_arrive(&empty_bar[stage]);
-          ++it;
         }
-        // lanes (g, 0) hold the sums of tile rows g and g + 8
+        float* pr = red + rs * (kTcWarps * kTcUnitRows) + warp * kTcUnitRows;
         if (t == 0) {
-          float* pr = red + (n_buf * kTcWarps + warp) * 16;
-          pr[g] = acc0;
-          pr[g + 8] = acc1;
+          pr[g] = r[0][0];
+          pr[g + 8] = r[0][1];
+          pr[16 + g] = r[1][0];
+          pr[24 + g] = r[1][1];
         }
-        ++n_buf;
-      }
-      ss += tc_flush(ph, red, n_buf, u_first, G, tid, false);
-      // phase end: publish this CTA's flag (its outputs are written; the sum of
-      // squares of its residual sums rides along for the next RMSNorm)
-      const bool resid = ph.epi_kind == EPI_RESID && ph.ss_out != nullptr;
-      if (p + 1 < a.n_phases || resid) {
-        ss = warp_sum(ss);
-        if (lane == 0) red_cta[warp] = ss;
-        named_bar_sync(1, kTcConsumers);
-        if (tid == 0) {
-          float tot = 0.f;
-          for (int w = 0; w < kTcWarps; ++w) tot += red_cta[w];
-          if (resid) ph.ss_out[cta] = tot;
-          if (p + 1 < a.n_phases) {
-            const unsigned long long f =
-                (static_cast<unsigned long long>(tag0 + p) << 32) | __float_as_uint(tot);
-            st_release_u64(a.flags + (p & 1) * kMaxGrid + cta, f);
-          }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&rfull_bar[rs]);
+        if (++rs == kTcRedSlots) {
+          rs = 0;
+          ++ruse;
         }
-        named_bar_sync(1, kTcConsumers);   // red_cta is read again at the next phase start
       }
     }
   }
 
   __syncthreads();
-  if (a.n_phases > 1 && tid == 0) {
-    // The last CTA to leave advances the epoch (so the next launch's tags are
-    // new) and resets the departure count.
+  if (tagged && tid == 0) {
+    // The last CTA to leave advances the epoch when the launch ends the
+    // program (so the next program's tags are new) and resets the count.
     __threadfence();
     const unsigned long long left = atomicAdd(&a.ctl->depart, 1ull);
     if (left == static_cast<unsigned long long>(G) - 1) {
       a.ctl->depart = 0ull;
-      atomicAdd(&a.ctl->epoch, 1u);
+      if (a.end_of_program) atomicAdd(&a.ctl->epoch, 1u);
     }
   }
 }
 
 cudaError_t tc_engine_prepare() {
-  return cudaFuncSetAttribute(tc_engine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+  return cudaFuncSetAttribute(tc_engine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcDynSmemMax);
+}
+
+size_t tc_smem_bytes(int stages, uint32_t stage_bytes, int xbuf_floats) {
+  return static_cast<size_t>(stages) * stage_bytes + 4 * static_cast<size_t>(xbuf_floats) + kTcRedBytes;
 }
 
 cudaError_t tc_engine_launch(const EngineArgs& a, int grid, bool cooperative, cudaStream_t stream) {
+  const size_t smem = tc_smem_bytes(a.stages, a.stage_bytes, a.xbuf_floats);
+  if (a.stages < 2 || a.stages > kTcMaxStages || smem > static_cast<size_t>(kTcDynSmemMax) || a.stage_bytes % 128)
+    return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kTcThreads);
-  cfg.dynamicSmemBytes = kTcSmem;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
@@ -437,6 +593,10 @@ cudaError_t tc_engine_launch(const EngineArgs& a, int grid, bool cooperative, cu
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, tc_engine_kernel, a);
+}
+
+cudaError_t tc_engine_occupancy(int* blocks_per_sm) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, tc_engine_kernel, kTcThreads, kTcDynSmemMax);
 }
 
 cudaError_t tc_engine_read_status(int* out) {
