@@ -287,7 +287,7 @@ int q4_decoder_destroy(q4_decoder *dec);
  *
  * The array is Q4_NOALLOC_SCRATCH_BYTES (1 MiB) on every GPU that loads the
  * library, held until the process exits; it fits a batch-1 stack of the
- * 70B shape with up to 284 layers (an 8B-shaped one with 812).  Larger
+ * 70B shape with up to 106 layers (an 8B-shaped one with 304).  Larger
  * stacks return Q4_ERR_OOM.
  * The first call on a device looks up the array's device address on that
  * device (make that first call before any stream capture).  Every call
@@ -295,6 +295,9 @@ int q4_decoder_destroy(q4_decoder *dec);
  * the GPU (different streams, or different threads without ordering) race:
  * issue them on one stream.  The control block is cleared by every call.
  * Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
+ * The call copies its phase program from host memory that lives only for the
+ * call, so it runs eagerly: on a stream that is being captured it returns
+ * Q4_ERR_ARG and enqueues nothing.
  *   shape, layer_weights, n_layers   as for q4_decoder_create (batch 1)
  *   hidden_io  device, binary16 [1][hidden], updated as by q4_layer_decode
  *   stream     the work is enqueued asynchronously on it (eager launches)
@@ -304,6 +307,13 @@ int q4_decoder_destroy(q4_decoder *dec);
 #define Q4_NOALLOC_SCRATCH_BYTES (1u << 20)
 int q4_layer_decode_noalloc(const q4_layer_shape *shape, const void *const *layer_weights, int n_layers,
                             uint16_t *hidden_io, void *stream);
+
+/* Status word of the kernels of the last q4_layer_decode_noalloc call on the
+ * current device (bits as for q4_decoder_status; 0 = every wait completed):
+ * synchronises `stream`, reads the word from the static array's control
+ * block and clears it.  Read it after each call: the next call clears it.
+ * Errors: Q4_ERR_ARG, Q4_ERR_CUDA. */
+int q4_noalloc_status(void *stream, int *status_out);
 
 /* Size in bytes of the static scratch array used by q4_layer_decode_noalloc. */
 size_t q4_noalloc_scratch_bytes(void);

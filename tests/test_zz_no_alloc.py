@@ -44,11 +44,53 @@ def test_noalloc_matches_workspace_decoder_on_two_calls(cfg, n_layers):
         q4.q4_layer_decode(dec, h_ref)
         q4.q4_layer_decode_noalloc(shape, ptrs, h_new)
         torch.cuda.synchronize()
+        assert q4.q4_noalloc_status() == 0, f"call {call}: a wait of the no-alloc kernels ran out"
         a, b = host_u16(h_ref), host_u16(h_new)
         assert np.all(np.isfinite(b.view(np.float16).astype(np.float64))), f"call {call}"
         assert f16_ulps(a, b).max() == 0, f"call {call}: outputs differ"
     assert q4.q4_decoder_status(dec) == 0
     q4.q4_decoder_destroy(dec)
+
+
+def test_noalloc_on_a_side_stream_between_graph_replays():
+    """Calls on a non-default stream, interleaved on that stream with graph
+    replays of a decoder that owns its workspace: each no-alloc call gives,
+    bit for bit, what the decoder gives for the same input."""
+    shape = q4.LayerShape.of(**TINY)
+    wbuf, ptrs = model.resident_layers(shape, 2, seed=92)
+    ws, offs, nb = model.workspace(shape, 2, 1)
+    dec = q4.q4_decoder_create(shape, ptrs, 1, ws, nb, q4.Q4_DEC_FUSED)
+    s = torch.cuda.Stream()
+    h0 = synth.activations(1, TINY["hidden"], 93)
+    with torch.cuda.stream(s):
+        h_ref, h_new = dev_u16(h0.reshape(-1)), dev_u16(h0.reshape(-1))
+        for call in range(3):
+            q4.q4_layer_decode(dec, h_ref, stream=s)
+            q4.q4_layer_decode_noalloc(shape, ptrs, h_new, stream=s)
+            q4.q4_layer_decode(dec, h_ref, stream=s)          # a replay right after, on the same stream
+            q4.q4_layer_decode_noalloc(shape, ptrs, h_new, stream=s)
+            assert q4.q4_noalloc_status(stream=s) == 0, f"call {call}"
+            assert np.array_equal(host_u16(h_ref), host_u16(h_new)), f"call {call}: outputs differ"
+    assert q4.q4_decoder_status(dec, stream=s) == 0
+    q4.q4_decoder_destroy(dec)
+
+
+def test_noalloc_refuses_stream_capture():
+    """The call runs eagerly only: on a stream being captured it returns an
+    argument error and enqueues nothing."""
+    shape = q4.LayerShape.of(**TINY)
+    wbuf, ptrs = model.resident_layers(shape, 1, seed=94)
+    h = dev_u16(synth.activations(1, TINY["hidden"], 95).reshape(-1))
+    before = host_u16(h)
+    g = torch.cuda.CUDAGraph()
+    side = torch.empty(16, device="cuda")
+    with torch.cuda.graph(g):
+        side.add_(1.0)
+        with pytest.raises(q4.Q4Error) as e:
+            q4.q4_layer_decode_noalloc(shape, ptrs, h, stream=torch.cuda.current_stream())
+    assert e.value.status == q4.Q4_ERR_ARG
+    torch.cuda.synchronize()
+    assert np.array_equal(host_u16(h), before)
 
 
 def test_noalloc_rejects_a_stack_beyond_the_array():

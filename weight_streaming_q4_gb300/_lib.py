@@ -91,6 +91,7 @@ def _declare(lib):
         "q4_decoder_destroy": ([c_p], c_int),
         "q4_layer_decode_noalloc": ([ctypes.POINTER(LayerShape), ctypes.POINTER(c_p), c_int, c_p, c_p], c_int),
         "q4_noalloc_scratch_bytes": ([], c_size),
+        "q4_noalloc_status": ([c_p, ctypes.POINTER(c_int)], c_int),
         "q4_stream_create": ([ctypes.POINTER(c_p), ctypes.POINTER(LayerShape), ctypes.POINTER(c_p), c_int, c_int,
                               c_p, c_p, c_size, c_p, c_size, c_int], c_int),
         "q4_stream_create_ex": ([ctypes.POINTER(c_p), ctypes.POINTER(LayerShape), ctypes.POINTER(c_p),
@@ -248,6 +249,12 @@ def q4_layer_decode_noalloc(shape: LayerShape, layer_ptrs, hidden, stream=None):
 
 def q4_noalloc_scratch_bytes() -> int:
     return lib().q4_noalloc_scratch_bytes()
+
+
+def q4_noalloc_status(stream=None) -> int:
+    v = c_int(0)
+    _check(lib().q4_noalloc_status(_stream(stream), ctypes.byref(v)), "q4_noalloc_status")
+    return v.value
 
 
 def q4_stream_create(shape: LayerShape, host_ptrs, batch: int, buf0, buf1, buf_bytes: int, workspace,

@@ -983,6 +983,8 @@ int run_stack_in_workspace(const q4_layer_shape* shape, const void* const* layer
   return launch_layers(w, 0, static_cast<int>(prog.size()), grid, s, engine, tagged, true, *shape);
 }
 
+int record_cuda_error(cudaError_t e) { return cuda_fail(e); }
+
 }  // namespace q4
 
 extern "C" int q4_decoder_status(q4_decoder* d, void* stream, int* status_out) {

@@ -396,6 +396,8 @@ cudaError_t glue_resid_norm(const uint16_t* z, const float* o, int batch, int di
 
 struct q4_layer_shape;
 namespace q4 {
+// Host helper (q4_api.cu): keep a CUDA error for q4_last_cuda_error(); returns Q4_ERR_CUDA.
+int record_cuda_error(cudaError_t e);
 // Host helper (q4_api.cu): one eager run of a layer stack inside a given workspace.
 int run_stack_in_workspace(const q4_layer_shape* shape, const void* const* layer_weights, int n_layers,
                            uint16_t* hidden_io, void* ws, size_t ws_bytes, cudaStream_t s);

@@ -30,7 +30,7 @@
 //   no load is spent on the scales; lane 0 accumulates the even blocks and
 //   lane 3 the odd ones, and one shuffle adds them at the end of the unit.
 // * Warp 8, the epilogue: sums the 8 consumer warps' partials of each row
-//   of a unit in a fixed order as soon as the unit is done (two partial slots
+//   of a unit in a fixed order as soon as the unit is done (eight partial slots
 //   handed over with mbarriers) and stores the outputs, so the consumers
 //   never wait for an epilogue.
 //
@@ -67,7 +67,7 @@ constexpr int kTcEpiWarp = kTcWarps;              // warp 8
 constexpr int kTcProdWarp = kTcWarps + 1;         // warp 9
 constexpr int kTcThreads = (kTcWarps + 2) * 32;
 constexpr int kTcMaxStages = 8;
-constexpr int kTcRedSlots = 2;                    // unit partial slots between consumers and epilogue
+constexpr int kTcRedSlots = 8;                    // unit partial slots between consumers and epilogue
 constexpr int kTcRedBytes = kTcRedSlots * kTcWarps * kTcUnitRows * 4;
 constexpr int kTcNormChunks = 8;                  // 4-value chunks of an RMSNorm input per consumer thread
 constexpr int kTcDynSmemMax = 231424;
@@ -291,6 +291,19 @@ __device__ __forceinline__ void pair_mma(const uint8_t* rg, const uint8_t* rh, i
   oh = fmaf(hi_half_f(h1), e[2], oh);
 }
 
+// Wait for a stage to land.  The common case (the copy has landed) is one
+// non-blocking test; after a failed wait the CTA keeps walking its units
+// without waiting (reading whatever the stage holds) so that every barrier is
+// still reached, and the launch reports the failure in its status.
+__device__ __forceinline__ void stage_wait(uint64_t* bar, uint32_t parity, uint32_t limit, volatile int* abort_flag,
+                                           Control* ctl) {
+  if (mbar_test_wait(bar, parity)) return;
+  if (!*abort_flag && !mbar_wait_bounded(bar, parity, limit)) {
+    tc_set_status(ctl, ST_FULL_TIMEOUT);
+    *abort_flag = 1;
+  }
+}
+
 // The products of one unit for one consumer warp, chunk by chunk as the
 // stages land: four block pairs of every chunk (pairs warp + 8q) and
 // both 16-row halves of the tile.  WIDE: rows wider than 2048 columns (64-block
@@ -307,13 +320,7 @@ __device__ __forceinline__ void unit_products(const uint8_t* ring, uint32_t SB, 
   const int pitch = WIDE ? 64 * kBlockBytes + 16 : pitch_rt;
   const int g = lane >> 2, t = lane & 3;
   for (int c = 0; c < chunks; ++c) {
-    // After a failed wait the CTA keeps walking its units without waiting
-    // (reading whatever the stage holds) so that every barrier is still
-    // reached; the launch then reports the failure in its status.
-    if (!*abort_flag && !mbar_wait_bounded(&full_bar[slot], use & 1, wait_limit)) {
-      tc_set_status(ctl, ST_FULL_TIMEOUT);
-      *abort_flag = 1;
-    }
+    stage_wait(&full_bar[slot], use & 1, wait_limit, abort_flag, ctl);
     const uint8_t* sb = ring + static_cast<size_t>(slot) * SB;
 #pragma unroll(WIDE ? kTcPairsPerWarp : 1)
     for (int q = 0; q < kTcPairsPerWarp; ++q) {
@@ -339,10 +346,10 @@ __device__ __forceinline__ void unit_products(const uint8_t* ring, uint32_t SB, 
 
 // ------------------------------------------------------------------ epilogue
 
-// A tagged residual input word, polled until it carries tag16.
-__device__ __forceinline__ unsigned short tc_tagged_res(const uint32_t* p, uint32_t tag16, uint32_t limit,
+// A tagged residual input word (w: its value loaded earlier), polled until it
+// carries tag16.
+__device__ __forceinline__ unsigned short tc_tagged_res(const uint32_t* p, uint32_t w, uint32_t tag16, uint32_t limit,
                                                         Control* ctl) {
-  uint32_t w = ld_relaxed_b32(p);
   for (uint32_t it = 0; (w >> 16) != tag16 && it < limit; ++it) {
     __nanosleep(32);
     w = ld_relaxed_b32(p);
@@ -354,8 +361,8 @@ __device__ __forceinline__ unsigned short tc_tagged_res(const uint32_t* p, uint3
 // The outputs of one row (lane) of a finished unit.  Tagged programs hand the
 // next phase its input as tagged words with this phase's tag; the plain
 // outputs are written where the phase has them.
-__device__ __forceinline__ void tc_epilogue_row(const Phase& ph, int n, float v, float u2, bool tagged, uint32_t tag,
-                                                uint32_t lim, Control* ctl) {
+__device__ __forceinline__ void tc_epilogue_row(const Phase& ph, int n, float v, float u2, uint32_t res_w, bool tagged,
+                                                uint32_t tag, uint32_t lim, Control* ctl) {
   const uint32_t tag16 = tag & 0xFFFFu;
   if (ph.epi_kind == EPI_SILU) {
     if (ph.y) ph.y[n] = v;
@@ -365,7 +372,7 @@ __device__ __forceinline__ void tc_epilogue_row(const Phase& ph, int n, float v,
     if (tagged) st_relaxed_b32(static_cast<uint32_t*>(ph.yt) + n, (tag16 << 16) | a16);
   } else if (ph.epi_kind == EPI_RESID) {
     if (ph.y) ph.y[n] = v;
-    const unsigned short rv = tc_tagged_res(ph.res_t + n, (tag - 1u) & 0xFFFFu, lim, ctl);
+    const unsigned short rv = tc_tagged_res(ph.res_t + n, res_w, (tag - 1u) & 0xFFFFu, lim, ctl);
     const float tv = __half2float(__ushort_as_half(rv)) + v;
     if (ph.y2) ph.y2[n] = tv;
     st_relaxed_b64(static_cast<unsigned long long*>(ph.yt) + n,
@@ -477,6 +484,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_engine_kernel(const __grid_c
       for (int u = first_unit(ph, cta, G); u < units; u += G) {
         // once a wait of this launch has run out, the residual polls give up at once
         const uint32_t lim = tagged && ld_relaxed_b32(&a.ctl->status) != st0 ? 0u : a.wait_limit;
+        const int n = u * (dual ? kTcUnitRows / 2 : kTcUnitRows) + lane;
+        const bool row_ok = (!dual || lane < kTcUnitRows / 2) && n < ph.n_rows;
+        // the residual base of this row was written phases ago: its load
+        // overlaps the wait for the unit's partials
+        const uint32_t res_w = row_ok && ph.epi_kind == EPI_RESID ? ld_relaxed_b32(ph.res_t + n) : 0u;
         if (!mbar_wait_bounded(&rfull_bar[rs], ruse & 1, a.wait_limit)) tc_set_status(a.ctl, ST_FULL_TIMEOUT);
         const float* pr = red + rs * (kTcWarps * kTcUnitRows);
         float v = 0.f, u2 = 0.f;
@@ -489,8 +501,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_engine_kernel(const __grid_c
           rs = 0;
           ++ruse;
         }
-        const int n = u * (dual ? kTcUnitRows / 2 : kTcUnitRows) + lane;
-        if ((!dual || lane < kTcUnitRows / 2) && n < ph.n_rows) tc_epilogue_row(ph, n, v, u2, tagged, tag, lim, a.ctl);
+        if (row_ok) tc_epilogue_row(ph, n, v, u2, res_w, tagged, tag, lim, a.ctl);
       }
     }
   } else {
