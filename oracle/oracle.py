@@ -66,9 +66,10 @@ def _declare(lib):
     lib.ora_add.argtypes = [_P, _P, _I64, _P]
     lib.ora_silu_mul.argtypes = [_P, _P, _I64, _P]
     lib.ora_layer.argtypes = [_P, _P, _INT, _I64, _I64, _I64, _I64, _I64, _DBL, _P, _P, _P, _P]
+    lib.ora_layer_kv.argtypes = [_P, _P, _I64, _I64, _I64, _I64, _I64, _DBL, _P, _P, _I64, _P, _P, _P, _P]
     for name in ("ora_half_to_double_n", "ora_double_to_half_n", "ora_dequant", "ora_gemv",
                  "ora_gemv_rows", "ora_rmsnorm", "ora_rmsnorm_d", "ora_attn_ctx1", "ora_attn_decode", "ora_add",
-                 "ora_silu_mul", "ora_layer"):
+                 "ora_silu_mul", "ora_layer", "ora_layer_kv"):
         getattr(lib, name).restype = None
     return lib
 
@@ -244,6 +245,26 @@ def layer(weights, z, batch: int, hidden: int, q_dim: int, kv_dim: int, ffn: int
     out = np.empty((batch, hidden), dtype=np.uint16)
     lib.ora_layer(arr, _ptr(zb), batch, hidden, q_dim, kv_dim, ffn, head_dim, eps,
                   _ptr(work), _ptr(work16), _ptr(t2), _ptr(out))
+    return out, t2
+
+
+def layer_kv(weights, z, k_cache, v_cache, pos: int, hidden: int, q_dim: int, kv_dim: int, ffn: int,
+             head_dim: int = 128, eps: float = 1e-5, lib=None):
+    """One decoder layer of one token at position ``pos`` over a binary16 KV
+    cache (arrays [capacity][kv_dim] of uint16, updated in row ``pos``).
+    Returns (z_out bits, t2 doubles)."""
+    lib = lib or load()
+    ws = [_u8(w) for w in weights]
+    arr = (ctypes.c_void_p * 7)(*[w.ctypes.data for w in ws])
+    zb = _u16(z).reshape(-1)
+    assert k_cache.dtype == np.uint16 and v_cache.dtype == np.uint16
+    assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous and pos < k_cache.shape[0]
+    work = np.empty(q_dim + 2 * kv_dim + 3 * hidden + 2 * ffn + 2 * q_dim + pos + 1, dtype=np.float64)
+    work16 = np.empty(hidden + q_dim + ffn, dtype=np.uint16)
+    t2 = np.empty(hidden, dtype=np.float64)
+    out = np.empty(hidden, dtype=np.uint16)
+    lib.ora_layer_kv(arr, _ptr(zb), hidden, q_dim, kv_dim, ffn, head_dim, eps, _ptr(k_cache), _ptr(v_cache), pos,
+                     _ptr(work), _ptr(work16), _ptr(t2), _ptr(out))
     return out, t2
 
 

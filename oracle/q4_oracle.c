@@ -319,3 +319,52 @@ void ora_layer(const uint8_t *const *wts, const uint16_t *z, int batch, int64_t 
     ora_add(z1, dn, (int64_t)batch * hidden, t2);
     ora_rmsnorm_d(t2, batch, hidden, eps, z_out);
 }
+
+/* One decoder layer of one token at position pos with a per-layer KV cache
+ * (batch 1): the layer of ora_layer with the context-1 attention replaced by
+ * decode attention over the cache.  The cache rows 0..pos-1 hold the earlier
+ * tokens' binary16 keys and values; this token's k and v are rounded to
+ * binary16 and stored in row pos (the cache the layer carries, PIPO summary,
+ * Method, "Offloading architecture"), then every query head attends over
+ * rows 0..pos (ora_attn_decode) and the attention output is rounded to
+ * binary16 before the o projection.  With pos = 0 the softmax over one key is
+ * 1 and the layer is ora_layer.  kc, vc: [capacity][kv_dim] binary16,
+ * updated in row pos.  work must hold q_dim + 2*kv_dim + 3*hidden + 2*ffn +
+ * 2*q_dim + (pos + 1) doubles, work16 hidden + q_dim + ffn binary16 values. */
+void ora_layer_kv(const uint8_t *const *wts, const uint16_t *z, int64_t hidden, int64_t q_dim, int64_t kv_dim,
+                  int64_t ffn, int64_t head_dim, double eps, uint16_t *kc, uint16_t *vc, int64_t pos,
+                  double *work, uint16_t *work16, double *t2, uint16_t *z_out)
+{
+    double *q = work;
+    double *k = q + q_dim;
+    double *v = k + kv_dim;
+    double *o = v + kv_dim;
+    double *t1 = o + hidden;
+    double *dn = t1 + hidden;
+    double *g = dn + hidden;
+    double *u = g + ffn;
+    double *att = u + ffn;
+    double *sabs = att + q_dim;
+    double *aw = sabs + q_dim;
+    uint16_t *attn = work16;
+    uint16_t *z1 = attn + q_dim;
+    uint16_t *act = z1 + hidden;
+    int64_t n_q = q_dim / head_dim, n_kv = kv_dim / head_dim;
+
+    ora_gemv(wts[0], z, q_dim, hidden, 1, 0, q_dim, q, 0);
+    ora_gemv(wts[1], z, kv_dim, hidden, 1, 0, kv_dim, k, 0);
+    ora_gemv(wts[2], z, kv_dim, hidden, 1, 0, kv_dim, v, 0);
+    ora_double_to_half_n(k, kv_dim, kc + pos * kv_dim);
+    ora_double_to_half_n(v, kv_dim, vc + pos * kv_dim);
+    ora_attn_decode(q, kc, vc, pos + 1, n_q, n_kv, head_dim, att, sabs, aw);
+    ora_double_to_half_n(att, q_dim, attn);
+    ora_gemv(wts[3], attn, hidden, q_dim, 1, 0, hidden, o, 0);
+    ora_add(z, o, hidden, t1);
+    ora_rmsnorm_d(t1, 1, hidden, eps, z1);
+    ora_gemv(wts[4], z1, ffn, hidden, 1, 0, ffn, g, 0);
+    ora_gemv(wts[5], z1, ffn, hidden, 1, 0, ffn, u, 0);
+    ora_silu_mul(g, u, ffn, act);
+    ora_gemv(wts[6], act, hidden, ffn, 1, 0, hidden, dn, 0);
+    ora_add(z1, dn, hidden, t2);
+    ora_rmsnorm_d(t2, 1, hidden, eps, z_out);
+}

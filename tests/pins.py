@@ -361,6 +361,50 @@ def pin_layer_wiring(lib):
     assert np.all(zo == one), "B: output f16(norm(t2)) is 1.0 everywhere"
 
 
+
+def pin_layer_kv(lib):
+    """The KV-cache layer: at position 0 the softmax over one key is 1 and the
+    layer is the context-1 layer; the cache row of the token is f16(k), f16(v);
+    with Wq (or Wk) all code 8 every score is 0, the softmax is uniform and the
+    attention output is the mean of the cached values, which hand-built values
+    make a closed form: cached value rows all 1 and the token's own v = 4
+    (Wv rows one code 12 at column 0, d = 1, z = 1) give a = f16((pos + 4) / (pos + 1))."""
+    hid, qd, kvd, ffn, hd = 64, 64, 32, 128, 16
+    eps = 1e-5
+    one = int(_f16(1.0))
+    rnd = lambda n, k, p: synth.q4_matrix(n, k, 4, p)
+    zero = lambda n, k: _q4_matrix_of(n, k, lambda r: (one, _codes(k)))
+    rng = np.random.default_rng(12)
+    z = ora.rmsnorm(_f16(rng.standard_normal((1, hid))), 1, hid, eps, lib=lib)
+    wts = [rnd(n, k, p) for p, (n, k) in enumerate(synth.layer_dims(hid, qd, kvd, ffn))]
+    cap = 8
+    kc = np.zeros((cap, kvd), np.uint16)
+    vc = np.zeros((cap, kvd), np.uint16)
+    zo, t2 = ora.layer_kv(wts, z, kc, vc, 0, hid, qd, kvd, ffn, hd, eps, lib=lib)
+    zr, t2r = ora.layer(wts, z, 1, hid, qd, kvd, ffn, hd, eps, lib=lib)
+    assert np.array_equal(zo, zr.reshape(-1)) and np.array_equal(t2, t2r.reshape(-1)), "pos 0 is the context-1 layer"
+    kref = ora.double_to_half(ora.gemv(wts[1], z, kvd, hid, lib=lib)[0][0], lib=lib)
+    vref = ora.double_to_half(ora.gemv(wts[2], z, kvd, hid, lib=lib)[0][0], lib=lib)
+    assert np.array_equal(kc[0], kref) and np.array_equal(vc[0], vref), "cache row 0 = f16(k), f16(v)"
+    assert not kc[1:].any() and not vc[1:].any(), "only the token's row is written"
+    # uniform scores: Wq all code 8; cached values 1, own value 4 -> attention (pos + 4) / (pos + 1);
+    # Wo row 0 one code 9 at column 0 -> o = (a[0], 0, ...); Wdown zero -> t2 = z1 = f16(norm(z + o))
+    zc = np.full((1, hid), one, np.uint16)
+    wv = _q4_matrix_of(kvd, hid, lambda r: (one, _codes(hid, 0, 12)))
+    wo = _q4_matrix_of(hid, qd, lambda r: (one, _codes(qd, 0, 9) if r == 0 else _codes(qd)))
+    w2 = [zero(qd, hid), rnd(kvd, hid, 1), wv, wo, rnd(ffn, hid, 4), rnd(ffn, hid, 5), zero(hid, ffn)]
+    for pos in (1, 3, 6):
+        kc = _f16(rng.standard_normal((cap, kvd)))
+        vc = np.full((cap, kvd), one, np.uint16)
+        zo, t2 = ora.layer_kv(w2, zc, kc, vc, pos, hid, qd, kvd, ffn, hd, eps, lib=lib)
+        a0 = float(np.float16((pos + 4.0) / (pos + 1.0)))
+        t1 = np.concatenate([[1.0 + a0], np.ones(hid - 1)])
+        r = 1.0 / np.sqrt((t1 ** 2).mean() + eps)
+        expect = (t1 * r).astype(np.float16).astype(np.float64)
+        assert np.array_equal(t2, expect), f"uniform scores at pos {pos}"
+        assert np.all(vc[pos] == int(_f16(4.0))) and np.all(vc[pos + 1:] == one), "v row pos = f16(v) only"
+
+
 def pin_attn_decode(lib):
     """Decode attention over a KV cache: closed forms of the softmax."""
     rng = np.random.default_rng(11)
@@ -417,4 +461,4 @@ def pin_attn_decode(lib):
 
 ALL_PINS = [pin_attn_decode, pin_half_decode_exhaustive, pin_half_encode, pin_golden_blocks, pin_distinct_positions,
             pin_block_indexing, pin_golden_gemv, pin_all_eight_is_zero, pin_single_nonzero,
-            pin_constant_codes, pin_brute_force, pin_invariants, pin_glue, pin_layer_wiring]
+            pin_constant_codes, pin_brute_force, pin_invariants, pin_glue, pin_layer_wiring, pin_layer_kv]

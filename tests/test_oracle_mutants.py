@@ -52,6 +52,11 @@ MUTANTS = {
                                    "ora_add(z1, o, (int64_t)batch * hidden, t1);"),
     "k_weights_for_v": ("ora_gemv(wts[2], z, kv_dim, hidden, batch, 0, kv_dim, v, 0);",
                         "ora_gemv(wts[1], z, kv_dim, hidden, batch, 0, kv_dim, v, 0);"),
+    "kv_row_off_by_one": ("ora_double_to_half_n(v, kv_dim, vc + pos * kv_dim);",
+                          "ora_double_to_half_n(v, kv_dim, vc + (pos + 1) * kv_dim);"),
+    "kv_context_excludes_token": ("ora_attn_decode(q, kc, vc, pos + 1, n_q, n_kv, head_dim, att, sabs, aw);",
+                                  "ora_attn_decode(q, kc, vc, pos > 0 ? pos : 1, n_q, n_kv, head_dim, att, sabs, aw);"),
+    "kv_k_into_v": ("ora_double_to_half_n(v, kv_dim, vc + pos * kv_dim);", "ora_double_to_half_n(k, kv_dim, vc + pos * kv_dim);"),
     "attn_value_key_swap": ("double v = ora_half_to_double(vc[t * kv_dim + g * head_dim + i]);",
                             "double v = ora_half_to_double(kc[t * kv_dim + g * head_dim + i]);"),
 }
