@@ -250,7 +250,8 @@ int q4_layer_decode_eager(q4_decoder *dec, uint16_t *hidden_io, void *stream);
  * wait completed; otherwise bit flags, clears it.  Bits: 1 a phase flag never
  * came, 2 a weight copy never landed, 4 a ring stage was never released, 8 a
  * copy was still in flight at exit, 16 a tagged input word never carried its
- * tag.  Results of a call that set a bit are not valid.  Errors: Q4_ERR_CUDA. */
+ * tag, 32 a KV decoder's position was outside its bucket.  Results of a call
+ * that set a bit are not valid.  Errors: Q4_ERR_CUDA. */
 int q4_decoder_status(q4_decoder *dec, void *stream, int *status_out);
 
 /* *tagged_out = 1 if the decoder's batch-1 engine passes tagged words
@@ -273,6 +274,55 @@ int q4_decoder_tagged(const q4_decoder *dec, int *tagged_out);
 int q4_decoder_debug_stall(q4_decoder *dec, uint32_t wait_limit, void *stream, int *status_out);
 
 int q4_decoder_destroy(q4_decoder *dec);
+
+/* ------------------------------------------------------- decoder with KV caches */
+
+/*
+ * Per-layer KV caches for decoding a sequence (the decode loop PipeLLM
+ * captures per context-length bucket, "Layer 1: CUDA Graph Compilation";
+ * the per-layer KV cache PIPO moves with the layer, Method, "Offloading
+ * architecture").  All device memory, owned by the caller.
+ *   capacity     the bucket: positions per cache (a multiple of 128, as for
+ *                q4_attn_decode)
+ *   k_layers[l], v_layers[l]   binary16 [capacity][kv_dim] caches of layer l,
+ *                16-byte aligned
+ *   pos          device int: the position of the next token (0 for the first);
+ *                every decode call reads it and advances it by one
+ *   attn_workspace, attn_workspace_bytes   >= q4_attn_workspace_bytes(n_q,
+ *                n_kv, head_dim, capacity); zeroed by q4_decoder_create_kv and
+ *                left reusable by every call
+ */
+typedef struct q4_kv_cache {
+  int capacity;
+  uint16_t *const *k_layers;
+  uint16_t *const *v_layers;
+  int *pos;
+  void *attn_workspace;
+  size_t attn_workspace_bytes;
+} q4_kv_cache;
+
+/*
+ * A batch-1 decoder whose layers attend over their KV caches instead of the
+ * context-1 stand-in: per layer, the q|k|v product; the token's k and v
+ * rounded to binary16 into row *pos of the layer's caches (q4_kv_append); the
+ * attention of every query head over rows 0..*pos (q4_attn_decode, output
+ * binary16); the o, gate|up and down products as in q4_layer_decode.  After
+ * the last layer *pos advances by one.  With *pos = 0 the result equals the
+ * context-1 decoder's bit for bit.  Keys are cached without a position
+ * encoding (the library applies none).  The tensor-core engine runs the
+ * products (shape as for Q4_DEC_TENSOR_CORE; head_dim 64, 128, 192 or 256);
+ * each layer is two engine launches around the two attention kernels, and
+ * q4_layer_decode replays them from one CUDA graph (one graph serves every
+ * position of the bucket: the kernels read *pos).  *pos must stay below
+ * capacity: otherwise the cache row is not written, the attention covers the
+ * capacity only, and the decoder's status word (q4_decoder_status) gets bit
+ * 32; the caller moves to a larger bucket before that.
+ *   other arguments as for q4_decoder_create (batch 1)
+ * Errors: Q4_ERR_ARG, Q4_ERR_ALIGN, Q4_ERR_OOM, Q4_ERR_CUDA.
+ */
+int q4_decoder_create_kv(q4_decoder **out, const q4_layer_shape *shape, const void *const *layer_weights,
+                         int n_layers, const q4_kv_cache *kv, void *workspace, size_t workspace_bytes,
+                         void *stream);
 
 /* ------------------------------------------------------- decoder without allocation */
 

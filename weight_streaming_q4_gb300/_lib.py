@@ -68,6 +68,12 @@ class LayerShape(ctypes.Structure):
         return cls(hidden, q_dim, kv_dim, ffn, head_dim, eps)
 
 
+class KVCache(ctypes.Structure):
+    """q4_kv_cache."""
+    _fields_ = [("capacity", c_int), ("k_layers", ctypes.POINTER(c_p)), ("v_layers", ctypes.POINTER(c_p)),
+                ("pos", c_p), ("attn_workspace", c_p), ("attn_workspace_bytes", c_size)]
+
+
 def _declare(lib):
     sig = {
         "q4_status_string": ([c_int], ctypes.c_char_p),
@@ -89,6 +95,8 @@ def _declare(lib):
         "q4_decoder_tagged": ([c_p, ctypes.POINTER(c_int)], c_int),
         "q4_decoder_debug_stall": ([c_p, ctypes.c_uint32, c_p, ctypes.POINTER(c_int)], c_int),
         "q4_decoder_destroy": ([c_p], c_int),
+        "q4_decoder_create_kv": ([ctypes.POINTER(c_p), ctypes.POINTER(LayerShape), ctypes.POINTER(c_p), c_int,
+                                  ctypes.POINTER(KVCache), c_p, c_size, c_p], c_int),
         "q4_layer_decode_noalloc": ([ctypes.POINTER(LayerShape), ctypes.POINTER(c_p), c_int, c_p, c_p], c_int),
         "q4_noalloc_scratch_bytes": ([], c_size),
         "q4_noalloc_status": ([c_p, ctypes.POINTER(c_int)], c_int),
@@ -199,6 +207,21 @@ def q4_workspace_layout(shape: LayerShape, n_layers: int, batch: int):
     _check(lib().q4_workspace_layout(ctypes.byref(shape), n_layers, batch, offs, ctypes.byref(total)),
            "q4_workspace_layout")
     return dict(zip(WS_NAMES, list(offs))), total.value
+
+
+def q4_decoder_create_kv(shape: LayerShape, layer_ptrs, capacity: int, k_layers, v_layers, pos, attn_workspace,
+                         attn_workspace_bytes: int, workspace, workspace_bytes: int, stream=None):
+    """Batch-1 decoder with decode attention over per-layer KV caches (device
+    pointers or tensors; ``pos`` a device int32)."""
+    h = c_p()
+    arr = (c_p * len(layer_ptrs))(*[int(p) for p in layer_ptrs])
+    ks = (c_p * len(k_layers))(*[_ptr(t) for t in k_layers])
+    vs = (c_p * len(v_layers))(*[_ptr(t) for t in v_layers])
+    kv = KVCache(capacity, ks, vs, _ptr(pos), _ptr(attn_workspace), attn_workspace_bytes)
+    kv._keep = (ks, vs)
+    _check(lib().q4_decoder_create_kv(ctypes.byref(h), ctypes.byref(shape), arr, len(layer_ptrs), ctypes.byref(kv),
+                                      _ptr(workspace), workspace_bytes, _stream(stream)), "q4_decoder_create_kv")
+    return h
 
 
 def q4_decoder_create(shape: LayerShape, layer_ptrs, batch: int, workspace, workspace_bytes: int,

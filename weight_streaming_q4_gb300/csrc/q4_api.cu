@@ -568,7 +568,7 @@ bool tagged_ok(const q4_layer_shape& s) {
 // the data dependences between the phases, orders each rewrite after every
 // read of the previous values.
 bool layer_phases_tagged(const q4_layer_shape& s, const uint8_t* wl, const uint16_t* in16, const Work& w,
-                         Phase out[4], bool last, int engine) {
+                         Phase out[4], bool last, int engine, bool kv = false) {
   size_t off[7];
   if (q4_layer_offsets(&s, off, nullptr) != Q4_OK) return false;
   memset(out, 0, 4 * sizeof(Phase));
@@ -633,6 +633,16 @@ bool layer_phases_tagged(const q4_layer_shape& s, const uint8_t* wl, const uint1
   d.y2 = last ? w.t2 : nullptr;
   d.yt = w.t2t;
   d.yt_n = s.hidden;
+  if (kv) {
+    // decode attention over the layer's KV cache runs between the q|k|v phase
+    // and the o phase (separate launches): q, k, v go out in plain fp32 for
+    // every layer, and the o phase reads the attention output, binary16, plain
+    a.y = w.qkv;
+    a.yt = nullptr;
+    b.x_src = w.attn;
+    b.x_kind = q4::X_F16;
+    b.x_dbg = nullptr;
+  }
   for (int i = 0; i < 4; ++i)
     if (!tile_phase(out[i], engine, wl != nullptr)) return false;
   return true;
@@ -654,12 +664,12 @@ bool final_phase_tagged(const q4_layer_shape& s, uint16_t* h_out, const Work& w,
 
 // Phase program of a whole stack: 4 phases per layer and the closing phase.
 bool stack_program(const q4_layer_shape& s, const std::vector<const uint8_t*>& layers, uint16_t* h,
-                   const Work& w, std::vector<Phase>& prog, int engine, bool tagged) {
+                   const Work& w, std::vector<Phase>& prog, int engine, bool tagged, bool kv = false) {
   const int L = static_cast<int>(layers.size());
   prog.assign(4 * static_cast<size_t>(L) + 1, Phase());
   for (int l = 0; l < L; ++l) {
     const uint16_t* in16 = l == 0 ? h : nullptr;
-    if (!(tagged ? layer_phases_tagged(s, layers[l], in16, w, &prog[4 * l], l == L - 1, engine)
+    if (!(tagged ? layer_phases_tagged(s, layers[l], in16, w, &prog[4 * l], l == L - 1, engine, kv)
                  : layer_phases(s, layers[l], in16, w, &prog[4 * l], engine)))
       return false;
   }
@@ -805,6 +815,12 @@ struct q4_decoder {
   q4_layer_shape shape;
   int n_layers = 0, batch = 1, mode = Q4_DEC_FUSED, grid = 0, engine = ENG_CORE;
   bool tagged = false;   // batch-1 CUDA-core engine with tagged words between phases
+  // decode attention over per-layer KV caches (q4_decoder_create_kv)
+  bool kv = false;
+  int capacity = 0;
+  std::vector<uint16_t*> kc, vc;
+  int* pos = nullptr;
+  void* attn_ws = nullptr;
   std::vector<const uint8_t*> layers;
   Work w;
   uint16_t* cur_h = nullptr;
@@ -824,7 +840,7 @@ static int decoder_write_program(q4_decoder* d, uint16_t* h, cudaStream_t s) {
     return Q4_OK;
   }
   std::vector<Phase> prog;
-  if (!stack_program(d->shape, d->layers, h, d->w, prog, d->engine, d->tagged)) return Q4_ERR_ARG;
+  if (!stack_program(d->shape, d->layers, h, d->w, prog, d->engine, d->tagged, d->kv)) return Q4_ERR_ARG;
   // pageable source: the runtime stages it before returning, so `prog` may go
   Q4_CUDA(cudaMemcpyAsync(d->w.prog, prog.data(), prog.size() * sizeof(Phase), cudaMemcpyHostToDevice, s));
   d->cur_h = h;
@@ -838,6 +854,25 @@ static int decoder_enqueue(q4_decoder* d, cudaStream_t s) {
       int st = launch_layer_batched(d->shape, d->layers[l], l, L, d->cur_h, d->w, d->batch, d->grid, s);
       if (st != Q4_OK) return st;
     }
+    return Q4_OK;
+  }
+  if (d->kv) {
+    // per layer: the q|k|v phase; this token's k and v into row *pos of the
+    // layer's caches; attention over rows 0..*pos; the o, gate|up and down
+    // phases; after the last layer the position advances
+    const q4_layer_shape& sh = d->shape;
+    for (int l = 0; l < L; ++l) {
+      int st = launch_layers(d->w, 4 * l, 1, d->grid, s, d->engine, true, false, sh);
+      if (st != Q4_OK) return st;
+      const float* qkv = d->w.qkv;
+      Q4_CUDA(q4::kv_append_launch(qkv + sh.q_dim, qkv + sh.q_dim + sh.kv_dim, d->kc[l], d->vc[l], d->pos, d->capacity,
+                                   sh.kv_dim, s, &d->w.ctl->status));
+      Q4_CUDA(q4::attn_launch(qkv, d->kc[l], d->vc[l], d->pos, d->capacity, sh.q_dim / sh.head_dim,
+                              sh.kv_dim / sh.head_dim, sh.head_dim, d->w.attn, d->attn_ws, s, 1));
+      st = launch_layers(d->w, 4 * l + 1, l == L - 1 ? 4 : 3, d->grid, s, d->engine, true, l == L - 1, sh);
+      if (st != Q4_OK) return st;
+    }
+    Q4_CUDA(q4::pos_advance_launch(d->pos, s));
     return Q4_OK;
   }
   if (d->mode == Q4_DEC_FUSED) return launch_layers(d->w, 0, 4 * L + 1, d->grid, s, d->engine, d->tagged, true, d->shape);
@@ -889,6 +924,43 @@ extern "C" int q4_decoder_create(q4_decoder** out, const q4_layer_shape* shape, 
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) {
     delete d;
+    return cuda_fail(e);
+  }
+  *out = d;
+  return Q4_OK;
+}
+
+extern "C" int q4_decoder_create_kv(q4_decoder** out, const q4_layer_shape* shape, const void* const* layer_weights,
+                                    int n_layers, const q4_kv_cache* kv, void* workspace, size_t workspace_bytes,
+                                    void* stream) {
+  if (!out || !shape_ok(shape) || !kv || !kv->k_layers || !kv->v_layers || !kv->pos || !kv->attn_workspace)
+    return Q4_ERR_ARG;
+  const int n_q = shape->q_dim / shape->head_dim, n_kv = shape->kv_dim / shape->head_dim;
+  const size_t aws = q4_attn_workspace_bytes(n_q, n_kv, shape->head_dim, kv->capacity);
+  if (aws == 0) return Q4_ERR_ARG;   // bucket or head shape the attention does not take
+  if (check_layer_shape_for_engine(*shape, ENG_TC) != Q4_OK) return Q4_ERR_ARG;
+  if (kv->attn_workspace_bytes < aws) return Q4_ERR_OOM;
+  if (!aligned(kv->pos, 4) || !aligned(kv->attn_workspace, 16)) return Q4_ERR_ALIGN;
+  for (int l = 0; l < n_layers; ++l) {
+    if (!kv->k_layers[l] || !kv->v_layers[l]) return Q4_ERR_ARG;
+    if (!aligned(kv->k_layers[l], 16) || !aligned(kv->v_layers[l], 16)) return Q4_ERR_ALIGN;
+  }
+  q4_decoder* d = nullptr;
+  int st = q4_decoder_create(&d, shape, layer_weights, n_layers, 1, workspace, workspace_bytes,
+                             Q4_DEC_PER_LAYER | Q4_DEC_TENSOR_CORE, stream);
+  if (st != Q4_OK) return st;
+  d->kv = true;
+  d->capacity = kv->capacity;
+  d->kc.assign(kv->k_layers, kv->k_layers + n_layers);
+  d->vc.assign(kv->v_layers, kv->v_layers + n_layers);
+  d->pos = kv->pos;
+  d->attn_ws = kv->attn_workspace;
+  // the attention's arrival counters start at zero (each call leaves them so)
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(kv->attn_workspace, 0, aws, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) {
+    q4_decoder_destroy(d);
     return cuda_fail(e);
   }
   *out = d;

@@ -40,7 +40,8 @@ struct AttnArgs {
   const float* q;        // fp32 [n_q][hd]
   const __half* k;       // binary16 [capacity][n_kv * hd]
   const __half* v;
-  const int* ctx_len;    // positions in use
+  const int* ctx_len;    // positions in use (plus ctx_add)
+  int ctx_add;
   float* part;           // fp32 [n_q][n_chunks][hd + 2]: m, l, o[0..hd)
   unsigned* arrive;      // [n_kv] chunks of the value head done (the last one combines and resets it)
   __half* out;           // binary16 [n_q][hd]
@@ -56,7 +57,7 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
 
 // Clamp the positions in use to [1, capacity].
 __device__ __forceinline__ int attn_ctx(const AttnArgs& a) {
-  const int c = *a.ctx_len;
+  const int c = *a.ctx_len + a.ctx_add;
   return c < 1 ? 1 : (c > a.capacity ? a.capacity : c);
 }
 
@@ -265,9 +266,12 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const __grid_constan
 
 // k_cache[pos][i] = f16(k[i]), v_cache[pos][i] = f16(v[i]), pos read from device memory.
 __global__ void kv_append_kernel(const float* k, const float* v, __half* kc, __half* vc, const int* pos,
-                                 int capacity, int kv_dim) {
+                                 int capacity, int kv_dim, int* status) {
   const int p = *pos;
-  if (p < 0 || p >= capacity) return;
+  if (p < 0 || p >= capacity) {
+    if (status && blockIdx.x == 0 && threadIdx.x == 0) atomicOr(status, ST_KV_POS);
+    return;
+  }
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < kv_dim; i += gridDim.x * blockDim.x) {
     kc[static_cast<size_t>(p) * kv_dim + i] = __float2half_rn(k[i]);
     vc[static_cast<size_t>(p) * kv_dim + i] = __float2half_rn(v[i]);
@@ -304,8 +308,9 @@ cudaError_t attn_prepare() {
 }
 
 cudaError_t attn_launch(const float* q, const uint16_t* k, const uint16_t* v, const int* ctx_len, int capacity,
-                        int n_q, int n_kv, int hd, uint16_t* out, void* ws, cudaStream_t s) {
+                        int n_q, int n_kv, int hd, uint16_t* out, void* ws, cudaStream_t s, int ctx_add) {
   AttnArgs a;
+  a.ctx_add = ctx_add;
   a.q = q;
   a.k = reinterpret_cast<const __half*>(k);
   a.v = reinterpret_cast<const __half*>(v);
@@ -338,11 +343,20 @@ cudaError_t attn_launch(const float* q, const uint16_t* k, const uint16_t* v, co
   return cudaGetLastError();
 }
 
+// The decoder's position counter advances by one after a token.
+__global__ void pos_advance_kernel(int* pos) { *pos += 1; }
+
+cudaError_t pos_advance_launch(int* pos, cudaStream_t s) {
+  pos_advance_kernel<<<1, 1, 0, s>>>(pos);
+  return cudaGetLastError();
+}
+
 cudaError_t kv_append_launch(const float* k, const float* v, uint16_t* kc, uint16_t* vc, const int* pos, int capacity,
-                             int kv_dim, cudaStream_t s) {
+                             int kv_dim, cudaStream_t s, int* status) {
   const int threads = 256, blocks = (kv_dim + threads - 1) / threads;
   kv_append_kernel<<<blocks < 64 ? blocks : 64, threads, 0, s>>>(k, v, reinterpret_cast<__half*>(kc),
-                                                                  reinterpret_cast<__half*>(vc), pos, capacity, kv_dim);
+                                                                  reinterpret_cast<__half*>(vc), pos, capacity, kv_dim,
+                                                                  status);
   return cudaGetLastError();
 }
 

@@ -179,6 +179,7 @@ enum StatusBits : int {
   ST_EMPTY_TIMEOUT = 4,
   ST_DRAIN_TIMEOUT = 8,
   ST_DATA_TIMEOUT = 16,    // a tagged input word never carried the expected tag
+  ST_KV_POS = 32,          // a KV decoder's position was outside 0..capacity-1
 };
 
 // ------------------------------------------------------------------ PTX
@@ -354,10 +355,14 @@ cudaError_t poison_launch(uint8_t* buf, size_t n_blocks, cudaStream_t stream);
 cudaError_t attn_prepare();
 size_t attn_workspace_bytes(int n_q, int n_kv, int hd, int capacity);
 int attn_chunk(int capacity, int n_kv);
+// ctx_add: the positions in use are *ctx_len + ctx_add (the decoder passes its
+// position counter and 1).
 cudaError_t attn_launch(const float* q, const uint16_t* k, const uint16_t* v, const int* ctx_len, int capacity,
-                        int n_q, int n_kv, int hd, uint16_t* out, void* ws, cudaStream_t s);
+                        int n_q, int n_kv, int hd, uint16_t* out, void* ws, cudaStream_t s, int ctx_add = 0);
+cudaError_t pos_advance_launch(int* pos, cudaStream_t s);
+// status (nullable): ST_KV_POS is or-ed in when *pos is outside 0..capacity-1.
 cudaError_t kv_append_launch(const float* k, const float* v, uint16_t* kc, uint16_t* vc, const int* pos, int capacity,
-                             int kv_dim, cudaStream_t s);
+                             int kv_dim, cudaStream_t s, int* status = nullptr);
 cudaError_t tc_engine_prepare();
 cudaError_t tc_engine_launch(const EngineArgs& a, int grid, bool cooperative, cudaStream_t stream);
 cudaError_t tc_engine_read_status(int* out);
