@@ -458,6 +458,90 @@ def run_stream(args, torch, q4, model, synth, stream, barrier, gpu_index):
     return out
 
 
+def run_kv(args, torch, q4, model, synth, stream, barrier, gpu_index):
+    """The 8B stack decoding with per-layer KV caches: each step is one token
+    at a fixed position (the position counter is set back before the token),
+    attending over `ctx` cached positions in every layer; one CUDA graph per
+    bucket (bucket = ctx).  Bytes per step = the weights plus the KV-cache
+    rows read (32 layers x 2 x ctx x kv_dim x 2 B)."""
+    cfg, n_layers = stack_cfg("8b")
+    if args.layers:
+        n_layers = args.layers
+    shape = q4.LayerShape.of(**cfg)
+    layer_bytes = q4.q4_layer_offsets(shape)[1]
+    wbuf, ptrs = model.resident_layers(shape, n_layers, seed=0)
+    ws, offs, ws_bytes = model.workspace(shape, n_layers, 1)
+    kvd, hd = cfg["kv_dim"], cfg["head_dim"]
+    n_q, n_kv = cfg["q_dim"] // hd, kvd // hd
+    contexts = [int(c) for c in str(args.kv_contexts).split(",")]
+    if not contexts or any(c < 128 or c % 128 for c in contexts):
+        raise SystemExit("--kv-contexts: multiples of 128")
+    h0 = torch.from_numpy(synth.activations(1, cfg["hidden"], 0).reshape(-1).view("int16").copy())
+    h = h0.cuda()
+    per = {}
+    for ctx in contexts:
+        cap = ctx
+        kc = torch.empty(n_layers, cap * kvd, dtype=torch.int16, device="cuda")
+        vc = torch.empty(n_layers, cap * kvd, dtype=torch.int16, device="cuda")
+        for l in range(n_layers):
+            synth.device_fill_normal_f16(kc[l].data_ptr(), cap * kvd, seed=0, tid=0x40000000 + 2 * l)
+            synth.device_fill_normal_f16(vc[l].data_ptr(), cap * kvd, seed=0, tid=0x40000001 + 2 * l)
+        pos = torch.zeros(1, dtype=torch.int32, device="cuda")
+        pos0 = torch.full((1,), ctx - 1, dtype=torch.int32, device="cuda")
+        awb = q4.q4_attn_workspace_bytes(n_q, n_kv, hd, cap)
+        aws = torch.empty(awb, dtype=torch.uint8, device="cuda")
+        torch.cuda.synchronize()
+        dec = q4.q4_decoder_create_kv(shape, ptrs, cap, list(kc), list(vc), pos, aws, awb, ws, ws_bytes,
+                                      stream=stream)
+
+        def step():
+            pos.copy_(pos0, non_blocking=True)    # the token at position ctx-1 (a device copy, no kernel)
+            q4.q4_layer_decode(dec, h, stream=stream)
+
+        with torch.cuda.stream(stream):
+            secs, clocks = time_region(torch, stream, step, args.steps, args.warmup, barrier, gpu_index)
+        status = q4.q4_decoder_status(dec, stream=stream)
+        if status != 0:
+            raise RuntimeError(f"KV decoder kernels reported status {status}")
+        kv_bytes = n_layers * 2 * ctx * kvd * 2
+        t = secs / args.steps
+        per[ctx] = dict(secs=secs, clocks=clocks, ms_per_step=round(t * 1e3, 4), tokens_per_s=round(1 / t, 2),
+                        kv_bytes_per_step=kv_bytes, dec=dec, keep=(kc, vc, pos, pos0, aws), step=step)
+    head = per[contexts[-1]]
+    step = head["step"]
+    hin = h0.pin_memory()
+    hout = torch.empty_like(hin).pin_memory()
+    e2e_steps = max(10, args.steps // 4)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            h.copy_(hin, non_blocking=True)
+            step()
+            hout.copy_(h, non_blocking=True)
+            stream.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            h.copy_(hin, non_blocking=True)
+            step()
+            hout.copy_(h, non_blocking=True)
+            stream.synchronize()
+    e2e_secs = time.perf_counter() - t0
+    for r in per.values():
+        q4.q4_decoder_destroy(r.pop("dec"))
+    ctx = contexts[-1]
+    wbytes = layer_bytes * n_layers
+    return dict(secs=head["secs"], clocks=head["clocks"], bytes_per_step=wbytes + head["kv_bytes_per_step"],
+                launches_per_step=4 * n_layers + 1, kernel_launches_per_step=2 * n_layers,
+                e2e_secs=e2e_secs, e2e_steps=e2e_steps, h2d=h0.numel() * 2, d2h=h0.numel() * 2,
+                workload=(f"8B-shaped decoder stack with per-layer binary16 KV caches, {n_layers} layers, batch 1, "
+                          f"one token at position {ctx - 1} (context {ctx}, bucket {ctx}), HBM-resident, "
+                          f"one CUDA-graph replay per step"),
+                kernel="tc_engine_kernel", kernel_key=None, n_layers=n_layers, cfg=cfg, tagged=True,
+                kv_contexts={str(c): {k: v for k, v in r.items() if k in ("ms_per_step", "tokens_per_s",
+                                                                          "kv_bytes_per_step")}
+                             for c, r in per.items()},
+                weight_bytes_per_step=wbytes)
+
+
 def run_attn(args, torch, q4, model, synth, stream, barrier, gpu_index):
     """Decode attention over the KV caches of all 32 layers of the 8B shape
     (32 query heads, 8 value heads, head_dim 128), one CUDA graph per context
@@ -656,13 +740,59 @@ def cpu_attn_rate(budget_s: float):
 
 # ------------------------------------------------------------------ main
 
+def extra_result(r, steps, peak):
+    """Short summary of another workload's run, added to the default line."""
+    per_step = r["secs"] / steps
+    kl = r.get("kernel_launches_per_step", r["launches_per_step"])
+    achieved = r["bytes_per_step"] / per_step / 1e9
+    d = {"workload": r["workload"], "ms_per_token": round(per_step * 1e3, 4), "tokens_per_s": round(1 / per_step, 2),
+         "gbs": round(achieved, 2), "hbm_frac_of_measured": round(achieved / peak, 4),
+         "launches_per_token": r["launches_per_step"], "engine_launches_per_token": kl, "steps": steps,
+         "clocks_sm_mhz": (r["clocks"] or {}).get("sm_mhz")}
+    if "streamed_bytes_per_step" in r:
+        sb = r["streamed_bytes_per_step"]
+        d["host_link"] = {"achieved_gbs": round(sb / per_step / 1e9, 2),
+                          "pinned_h2d_peak_gbs": round(r["h2d_peak_gbs"], 2),
+                          "frac": round(sb / per_step / 1e9 / r["h2d_peak_gbs"], 4) if sb else None,
+                          "streamed_bytes_per_token": sb, "distinct_host_layers": r["distinct"]}
+        d["hbm_frac_of_measured"] = None
+        d["gbs_note"] = "weight bytes per token over the token time, most of them copied over the host link"
+    if "kv_contexts" in r:
+        d["kv_contexts"] = r["kv_contexts"]
+        d["weight_bytes_per_token"] = r["weight_bytes_per_step"]
+        d["gbs_note"] = "weight bytes and KV-cache bytes read per token over the token time"
+    return d
+
+
+def run_extras(args, torch, q4, model, synth, stream, barrier, gpu_index, peak):
+    import copy
+    extras = {}
+    for name, runner, overrides in (("70b", run_stack, {}), ("70b_stream", run_stream, {"resident_frac": 0.0}),
+                                    ("8b_kv", run_kv, {})):
+        a = copy.copy(args)
+        a.config = {"70b": "70b", "70b_stream": "70b-stream", "8b_kv": "8b-kv"}[name]
+        a.steps, a.warmup, a.layers = min(args.steps, 50), min(args.warmup, 5), 0
+        for k, v in overrides.items():
+            setattr(a, k, v)
+        try:
+            r = runner(a, torch, q4, model, synth, stream, barrier, gpu_index)
+            extras[name] = extra_result(r, r.get("steps_override", a.steps), peak)
+        except Exception as e:   # an extra never hides the headline number
+            extras[name] = {"failed": f"{type(e).__name__}: {e}"}
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return extras
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", default="8b",
-                    choices=["8b", "gemv", "70b", "70b-stream", "stream-sweep", "sweep", "attn"])
+                    choices=["8b", "gemv", "70b", "70b-stream", "stream-sweep", "sweep", "attn", "8b-kv"])
+    ap.add_argument("--kv-contexts", default="1024,4096",
+                    help="8b-kv: contexts timed (multiples of 128); the last one is the line's value")
     ap.add_argument("--resident-frac", type=float, default=0.0,
                     help="70b-stream: fraction of the layers (a prefix) kept resident in HBM")
     ap.add_argument("--chunked", action="store_true", help="70b-stream: copy each layer as four chunks")
@@ -673,6 +803,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--layers", type=int, default=0, help="run only this many layers of the stack (profiling)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline (profiling runs)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="8b at N=1: skip the 70b, 70b-stream and 8b-kv results added to the line")
     ap.add_argument("--cuda-core", action="store_true",
                     help="batch-1 stacks and rings: the CUDA-core engine instead of the tensor-core one (comparison)")
     ap.add_argument("--barrier", action="store_true",
@@ -700,7 +832,7 @@ def main():
                                                                                "stream-sweep")):
         raise SystemExit("--batch: 1..16, for the 8b, 70b and stream configs")
     runner = {"8b": run_stack, "70b": run_stack, "gemv": run_gemv, "70b-stream": run_stream,
-              "stream-sweep": run_stream, "sweep": run_sweep, "attn": run_attn}[args.config]
+              "stream-sweep": run_stream, "sweep": run_sweep, "attn": run_attn, "8b-kv": run_kv}[args.config]
     r = runner(args, torch, q4, model, synth, stream, barrier, local_rank)
     steps = r.get("steps_override", args.steps)
     warmup = r.get("warmup_override", args.warmup)
@@ -764,6 +896,14 @@ def main():
         out["roofline"]["timing"] = "step time / launches of the kernel per step (glue launches included)"
     if "sweep" in r:
         out["sweep"] = r["sweep"]
+    if "kv_contexts" in r:
+        out["tokens_per_s"] = round(world / per_step, 2)
+        out["kv_contexts"] = r["kv_contexts"]
+        out["config"]["n_layers"] = r["n_layers"]
+        out["config"]["weight_bytes_per_token"] = r["weight_bytes_per_step"]
+        out["metric_note"] = "value counts the weight bytes and the KV-cache bytes read per token"
+        out["roofline"]["timing"] = ("step time / 2 engine launches per layer (attention, cache append and "
+                                     "position launches included)")
     if "attn_buckets" in r:
         out["attn_buckets"] = r["attn_buckets"]
         out["metric_note"] = "value = GB/s of KV-cache bytes read (keys and values), not weight bytes"
@@ -776,6 +916,8 @@ def main():
             out["e2e"]["note"] = r["e2e_note"]
     out["gpu_launches"] = r["launches_per_step"] * steps
     out["clocks"] = r["clocks"]
+    if args.config == "8b" and args.batch == 1 and world == 1 and not args.no_extras and not args.layers:
+        out["extra"] = run_extras(args, torch, q4, model, synth, stream, barrier, local_rank, peak)
     # the CPU oracle on a bounded sample of the same workload (rank 0 only)
     if args.no_cpu:
         out["cpu_baseline"] = None
@@ -786,7 +928,7 @@ def main():
             gbs_cpu, cores, nbytes, t = cpu_attn_rate(args.cpu_budget)
         else:
             gbs_cpu, cores, nbytes, t = cpu_oracle_rate("gemv" if args.config == "gemv" else
-                                                        ("8b" if args.config in ("8b", "sweep") else "70b"),
+                                                        ("8b" if args.config in ("8b", "sweep", "8b-kv") else "70b"),
                                                         args.cpu_budget)
         what = ("KV-cache bytes of whole 8B-head attention calls at context 4096" if args.config == "attn" else
                 "weight bytes of row-sampled projections of the same workload")
@@ -805,7 +947,7 @@ def reference_config(args, world):
     if args.config == "gemv":
         return {"workload": "single Q4_0 product N=K=4096, batch 1", "batch": 1,
                 "parallelism": f"replicas x{world}"}
-    name = "8b" if args.config in ("8b", "sweep") else "70b"
+    name = "8b" if args.config in ("8b", "sweep", "8b-kv") else "70b"
     cfg, n_layers = stack_cfg(name)
     if args.layers:
         n_layers = args.layers

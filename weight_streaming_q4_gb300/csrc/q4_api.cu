@@ -633,6 +633,11 @@ bool layer_phases_tagged(const q4_layer_shape& s, const uint8_t* wl, const uint1
   d.y2 = last ? w.t2 : nullptr;
   d.yt = w.t2t;
   d.yt_n = s.hidden;
+  // Tensor-core engine: the v rows, the only ones the context-1 o phase reads,
+  // are the phase's first units, so they are done in the first round of
+  // units and the CTAs with a second q|k|v unit do it while the o phase starts.
+  if (engine == ENG_TC && !kv && a.n_rows % q4::kTcUnitRows == 0 && (s.q_dim + s.kv_dim) % q4::kTcUnitRows == 0)
+    a.row_rot = s.q_dim + s.kv_dim;
   if (kv) {
     // decode attention over the layer's KV cache runs between the q|k|v phase
     // and the o phase (separate launches): q, k, v go out in plain fp32 for

@@ -114,7 +114,8 @@ struct Phase {
   int gidx;               // index of the phase in the whole program (its tag offset)
   int sync;               // SyncKind
   int xt_n;               // X_TAG16_ATTN: tagged values of v in x_src
-  int pad2_;
+  int row_rot;            // tensor-core engine: unit u covers rows from (u * rows_per_unit +
+                          // row_rot) mod n_rows (row_rot and n_rows multiples of the unit)
   // Tensor-core engine only: TMA descriptors of w0 and w1 (2-D, 64-bit elements:
   // columns = row bytes / 8, rows = n_rows; box = tc_pitch(k) / 8 columns by
   // the unit's rows), encoded on the host.
@@ -302,6 +303,16 @@ __device__ __forceinline__ uint4 ld_relaxed_v4(const void* p) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p)
                : "memory");
+  return v;
+}
+
+// As ld_relaxed_v4 without the compiler memory barrier (other memory
+// accesses may move across it; the load itself is kept and not merged).
+__device__ __forceinline__ uint4 ld_relaxed_v4_nb(const void* p) {
+  uint4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
   return v;
 }
 

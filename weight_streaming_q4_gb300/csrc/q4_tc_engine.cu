@@ -83,6 +83,11 @@ __device__ __forceinline__ const Phase& phase_at(const EngineArgs& a, int p) {
 }
 
 __device__ __forceinline__ int first_unit(const Phase& ph, int cta, int G) { return (cta - ph.base % G + G) % G; }
+// First row of unit u (rpu rows per unit), after the phase's row rotation.
+__device__ __forceinline__ int unit_row0(const Phase& ph, int u, int rpu) {
+  const int r = u * rpu + ph.row_rot;
+  return r >= ph.n_rows ? r - ph.n_rows : r;
+}
 
 // ------------------------------------------------------------------ input
 
@@ -106,15 +111,38 @@ __device__ __forceinline__ void store_formed4(const Phase& ph, int e, uint32_t h
   }
 }
 
+// Warp 0: wait until every CTA's phase flag carries `tag` or a later one
+// (the tagged programs' once-per-layer exchange; the flags' low words are
+// unused), bounded by `limit` polls.
+__device__ __forceinline__ void tc_wait_flags(const unsigned long long* flags, unsigned tag, int lane, uint32_t limit,
+                                              Control* ctl) {
+  const int G = static_cast<int>(gridDim.x);
+  bool ok = false;
+  for (uint32_t it = 0; it < limit && !ok; ++it) {
+    bool mine = true;
+    for (int i = lane; i < G; i += 32)
+      mine &= static_cast<int>(static_cast<unsigned>(ld_relaxed_u64(flags + i) >> 32) - tag) >= 0;
+    ok = __all_sync(0xffffffffu, mine);
+    if (!ok && it > 16) __nanosleep(64);
+  }
+  if (!ok && lane == 0) tc_set_status(ctl, ST_FLAG_TIMEOUT);
+  __threadfence();
+}
+
 // The RMSNorm input of a phase (k values, at most 8192): staged in
 // registers, 4 consecutive values per chunk, chunk i = tid + c * 256.  Tagged
 // fp32 words are polled until every tag is `want`; a plain binary16 input is
 // read once.  The sum of squares runs over each thread's chunks in order,
 // then the warp tree, then the 8 warps in order: an order fixed by k alone.
+// With `flags` set, warp 0 first waits for the layer's phase flags (tag
+// flag_tag) while the other warps already poll the input: the flags guard the
+// phase's first tagged write, which follows the reduction's barrier.
 // Returns the scale 1 / sqrt(mean(t^2) + eps); v holds the values.
 __device__ __forceinline__ float stage_norm(const Phase& ph, uint32_t want, uint32_t limit, Control* ctl, float* red_cta,
-                                            int tid, float (&v)[kTcNormChunks][4]) {
+                                            int tid, float (&v)[kTcNormChunks][4], const unsigned long long* flags,
+                                            unsigned flag_tag) {
   const int n4 = ph.k >> 2;
+  if (flags && tid < 32) tc_wait_flags(flags, flag_tag, tid, limit, ctl);
   if (ph.x_kind == X_NORM16) {
 #pragma unroll
     for (int c = 0; c < kTcNormChunks; ++c) {
@@ -179,8 +207,11 @@ __device__ __forceinline__ void stage_tag16(const Phase& ph, uint8_t* xf, uint32
   bool ok = false;
   for (uint32_t it = 0; it < limit && !ok; ++it) {
     ok = true;
+    // loads without a compiler memory barrier: the unrolled loop keeps
+    // several in flight ahead of the shared-memory stores
+#pragma unroll 4
     for (int i = tid; i < n4; i += kTcConsumers) {
-      const uint4 w = ld_relaxed_v4(src + i);
+      const uint4 w = ld_relaxed_v4_nb(src + i);
       ok &= (((w.x ^ want) | (w.y ^ want) | (w.z ^ want) | (w.w ^ want)) >> 16) == 0u;
       const uint32_t h01 = __byte_perm(w.x, w.y, 0x5410), h23 = __byte_perm(w.z, w.w, 0x5410);
       const int e = 4 * i;
@@ -233,11 +264,13 @@ __device__ __noinline__ void tc_prologue(const Phase& ph, unsigned tag, uint32_t
                                          const unsigned long long* flags, uint8_t* xf, float* red_cta, int tid,
                                          bool cta0) {
   const int warp = tid >> 5, lane = tid & 31;
-  if (ph.sync == SYNC_WAIT && warp == 0) wait_phase_flags(flags, tag - 1u, lane, lim, ctl);
-  if (ph.sync == SYNC_WAIT) named_bar_sync(1, kTcConsumers);
-  if (ph.x_kind == X_NORM16 || ph.x_kind == X_TAG32_NORM) {
+  const bool norm = ph.x_kind == X_NORM16 || ph.x_kind == X_TAG32_NORM;
+  if (ph.sync == SYNC_WAIT && !norm && warp == 0) tc_wait_flags(flags, tag - 1u, lane, lim, ctl);
+  if (ph.sync == SYNC_WAIT && !norm) named_bar_sync(1, kTcConsumers);
+  if (norm) {
     float v[kTcNormChunks][4];
-    const float r = stage_norm(ph, tag - 1u, lim, ctl, red_cta, tid, v);
+    const float r = stage_norm(ph, tag - 1u, lim, ctl, red_cta, tid, v, ph.sync == SYNC_WAIT ? flags : nullptr,
+                               tag - 1u);
     const int n4 = ph.k >> 2;
 #pragma unroll
     for (int c = 0; c < kTcNormChunks; ++c) {
@@ -451,10 +484,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_engine_kernel(const __grid_c
             uint8_t* dst = ring + static_cast<size_t>(slot) * SB;
             mbar_arrive_expect_tx(&full_bar[slot], bytes);
             if (dual) {
-              tma_load_2d(dst, &ph.tm0, c * cx, u * (kTcUnitRows / 2), &full_bar[slot]);
-              tma_load_2d(dst + (kTcUnitRows / 2) * pitch, &ph.tm1, c * cx, u * (kTcUnitRows / 2), &full_bar[slot]);
+              const int r0 = unit_row0(ph, u, kTcUnitRows / 2);
+              tma_load_2d(dst, &ph.tm0, c * cx, r0, &full_bar[slot]);
+              tma_load_2d(dst + (kTcUnitRows / 2) * pitch, &ph.tm1, c * cx, r0, &full_bar[slot]);
             } else {
-              tma_load_2d(dst, &ph.tm0, c * cx, u * kTcUnitRows, &full_bar[slot]);
+              tma_load_2d(dst, &ph.tm0, c * cx, unit_row0(ph, u, kTcUnitRows), &full_bar[slot]);
             }
             ++it;
             if (++slot == S) {
@@ -484,7 +518,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_engine_kernel(const __grid_c
       for (int u = first_unit(ph, cta, G); u < units; u += G) {
         // once a wait of this launch has run out, the residual polls give up at once
         const uint32_t lim = tagged && ld_relaxed_b32(&a.ctl->status) != st0 ? 0u : a.wait_limit;
-        const int n = u * (dual ? kTcUnitRows / 2 : kTcUnitRows) + lane;
+        const int n = unit_row0(ph, u, dual ? kTcUnitRows / 2 : kTcUnitRows) + lane;
         const bool row_ok = (!dual || lane < kTcUnitRows / 2) && n < ph.n_rows;
         // the residual base of this row was written phases ago: its load
         // overlaps the wait for the unit's partials
