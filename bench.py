@@ -301,6 +301,94 @@ def run_gemv(args, torch, q4, model, synth, stream, barrier, gpu_index):
                 kernel="tc_engine_kernel", kernel_key="tc_engine_kernel:gemv", cfg=dict(n=n, k=k, copies=copies))
 
 
+def h2d_multi_stream(torch, blocks, nbytes, counts=(1, 2, 4)):
+    """Pinned host -> HBM GB/s with n copies of nbytes in flight on n streams."""
+    streams = [torch.cuda.Stream() for _ in range(max(counts))]
+    dst = [torch.empty(nbytes, dtype=torch.uint8, device="cuda") for _ in range(max(counts))]
+    out = {}
+    for n in counts:
+        best = 0.0
+        for _ in range(3):
+            torch.cuda.synchronize()
+            ev0 = torch.cuda.Event(enable_timing=True)
+            ev0.record(streams[0])
+            for s in streams[1:n]:
+                s.wait_event(ev0)
+            for j in range(n):
+                with torch.cuda.stream(streams[j]):
+                    for r in range(2):
+                        dst[j].copy_(blocks[(2 * j + r) % len(blocks)][:nbytes], non_blocking=True)
+            for s in streams[1:n]:
+                e = torch.cuda.Event()
+                e.record(s)
+                streams[0].wait_event(e)
+            ev1 = torch.cuda.Event(enable_timing=True)
+            ev1.record(streams[0])
+            torch.cuda.synchronize()
+            best = max(best, 2 * n * nbytes / (ev0.elapsed_time(ev1) / 1e3) / 1e9)
+        out[str(n)] = round(best, 2)
+    del dst
+    torch.cuda.empty_cache()
+    return out
+
+
+def numa_report(blocks):
+    """NUMA nodes of the host, the GPU's affinity node and where the pinned blocks' pages are."""
+    import ctypes, platform
+    from collections import Counter
+    rep = {}
+    try:
+        rep["host_nodes"] = len([d for d in os.listdir("/sys/devices/system/node") if d.startswith("node")])
+        bus = subprocess.run(["nvidia-smi", "--query-gpu=pci.bus_id", "--format=csv,noheader", "-i",
+                              str(int(os.environ.get("LOCAL_RANK", 0)))], capture_output=True, text=True,
+                             timeout=30).stdout.strip().lower()
+        for cand in (bus, bus[4:]):
+            p = f"/sys/bus/pci/devices/{cand}/numa_node"
+            if os.path.exists(p):
+                rep["gpu_numa_node"] = int(open(p).read().strip())
+                break
+        nr = {"aarch64": 239, "x86_64": 279}.get(platform.machine())
+        if nr is not None:
+            libc = ctypes.CDLL(None, use_errno=True)
+            ps = os.sysconf("SC_PAGE_SIZE")
+            cnt = Counter()
+            for b in blocks:
+                n = 16
+                pages = (ctypes.c_void_p * n)(*[(b.data_ptr() + i * (b.numel() // n)) // ps * ps for i in range(n)])
+                status = (ctypes.c_int * n)()
+                if libc.syscall(nr, 0, n, pages, None, status, 0) == 0:   # query only: no move
+                    cnt.update(int(x) for x in status)
+            rep["pinned_page_nodes"] = {str(k): v for k, v in sorted(cnt.items())}
+    except Exception as e:   # a report, never a failure
+        rep["error"] = str(e)
+    return rep
+
+
+def timeline_summary(tl):
+    """Per-layer [copy begin, copy end, compute begin, compute end] (ns) of one
+    ring token -> medians and how much of the compute ran under a copy."""
+    import numpy as np
+    tl = tl.astype(np.int64)
+    streamed = tl[:, 0] > 0
+    t0 = min(tl[streamed, 0].min() if streamed.any() else tl[:, 2].min(), tl[:, 2].min())
+    rel = (tl - t0) / 1e6
+    rel[~streamed, :2] = np.nan
+    copy = rel[:, 1] - rel[:, 0]
+    comp = rel[:, 3] - rel[:, 2]
+    wait = np.r_[rel[0, 2], rel[1:, 2] - rel[:-1, 3]]   # compute stream idle before each layer
+    spans = [(a, b) for a, b in rel[streamed, :2]]
+    covered = 0.0
+    for a, b in rel[:, 2:4]:
+        covered += sum(max(0.0, min(b, y) - max(a, x)) for x, y in spans)
+    end = np.nanmax(rel[:, 3])
+    return {"token_ms": round(float(end), 3), "copy_ms_median": round(float(np.nanmedian(copy)), 4),
+            "compute_ms_median": round(float(np.median(comp)), 4),
+            "compute_wait_ms_median": round(float(np.median(wait[1:])), 4),
+            "copy_engine_busy_frac": round(float(np.nansum(copy) / end), 4),
+            "compute_under_copy_frac": round(float(covered / comp.sum()), 4),
+            "first_layers_ms": [[round(float(v), 3) for v in r] for r in rel[:4]]}
+
+
 def run_stream(args, torch, q4, model, synth, stream, barrier, gpu_index):
     """70B-shaped stack through the copy/compute ring.  --resident-frac keeps
     that fraction of the layers (a prefix) resident in HBM; --chunked copies
@@ -324,18 +412,12 @@ def run_stream(args, torch, q4, model, synth, stream, barrier, gpu_index):
     ws, offs, ws_bytes = model.workspace(shape, n_layers, B)
     h0 = torch.from_numpy(synth.activations(B, cfg["hidden"], 0).reshape(-1).view("int16").copy())
     h = h0.cuda()
-    # pinned host -> HBM copy peak, same transfer size as the ring
+    # pinned host -> HBM copy peak at the ring's transfer size, with 1, 2 and 4
+    # copies in flight on separate streams (the link's limit, not one stream's)
     cs = torch.cuda.Stream()
-    best = 0.0
-    for _ in range(5):
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ev0.record(cs)
-        with torch.cuda.stream(cs):
-            for i in range(4):
-                bufs[i & 1].copy_(blocks[i % len(blocks)], non_blocking=True)
-        ev1.record(cs)
-        torch.cuda.synchronize()
-        best = max(best, 4 * stride / (ev0.elapsed_time(ev1) / 1e3) / 1e9)
+    h2d_streams = h2d_multi_stream(torch, blocks, stride)
+    best = max(h2d_streams.values())
+    numa = numa_report(blocks)
 
     # each host block's own copy speed (blocks in slow host memory show up here)
     def block_speed(blk, i):
@@ -391,17 +473,23 @@ def run_stream(args, torch, q4, model, synth, stream, barrier, gpu_index):
     for frac in fracs:
         R = int(round(frac * n_layers))
         if sweep:
-            combos += [(R, "prefix", False), (R, "prefix", True)] + ([(R, "spread", False)] if 0 < R < n_layers else [])
+            combos += [(R, "prefix", False, False), (R, "prefix", True, False)] + (
+                [(R, "spread", False, False)] if 0 < R < n_layers else [])
         else:
-            combos.append((R, args.resident_pattern, args.chunked))
-    for ci, (R, pat, chunked) in enumerate(combos):
+            combos.append((R, args.resident_pattern, args.chunked, args.single_buffer))
+    if getattr(args, "with_single", False) and not sweep:
+        # the memory-efficient mode on the same pinned blocks: one staging buffer,
+        # merged and chunked copies
+        combos += [(combos[0][0], combos[0][1], False, True), (combos[0][0], combos[0][1], True, True)]
+    for ci, (R, pat, chunked, single) in enumerate(combos):
         if True:
             keep = set(resident_set(n_layers, R, pat))
             host = [0 if i in keep else hptrs[i] for i in range(n_layers)]
             res = [dptrs[i] if i in keep else 0 for i in range(n_layers)]
             flags = (q4.Q4_STREAM_CHUNKED if chunked else 0) | (q4.Q4_STREAM_BARRIER if args.barrier else 0) | (
-                q4.Q4_STREAM_CUDA_CORE if args.cuda_core else 0)
-            ring = q4.q4_stream_create_ex(shape, host, res, B, bufs[0], bufs[1], stride, ws, ws_bytes, flags)
+                q4.Q4_STREAM_CUDA_CORE if args.cuda_core else 0) | (q4.Q4_STREAM_SINGLE_BUFFER if single else 0)
+            ring = q4.q4_stream_create_ex(shape, host, res, B, bufs[0], None if single else bufs[1], stride, ws,
+                                          ws_bytes, flags)
 
             def step():
                 q4.q4_stream_layers(ring, h, stream=stream)
@@ -410,15 +498,22 @@ def run_stream(args, torch, q4, model, synth, stream, barrier, gpu_index):
             if q4.q4_stream_status(ring, stream=stream) != 0:
                 raise RuntimeError("stream ring kernels reported a failed wait")
             t = secs / steps
-            runs.append(dict(resident_layers=R, placement=pat, chunked=chunked, secs=secs, clocks=clocks,
+            runs.append(dict(resident_layers=R, placement=pat, chunked=chunked, single_buffer=single, secs=secs,
+                             clocks=clocks,
                              ms_per_token=round(t * 1e3, 3), tokens_per_s=round(B / t, 3),
                              weight_gbs=round(layer_bytes * n_layers / t / 1e9, 2),
                              host_link_gbs=round(layer_bytes * (n_layers - R) / t / 1e9, 2),
                              host_link_frac=round(layer_bytes * (n_layers - R) / t / 1e9 / best, 4)))
-            last_ring = ring
-            if ci != len(combos) - 1:
-                q4.q4_stream_destroy(ring)
+            q4.q4_stream_destroy(ring)
     head = runs[0]
+    # the first configuration again (rings share the workspace) for the end-to-end run
+    R, pat, chunked, single = combos[0]
+    keep = set(resident_set(n_layers, R, pat))
+    flags = (q4.Q4_STREAM_CHUNKED if chunked else 0) | (q4.Q4_STREAM_BARRIER if args.barrier else 0) | (
+        q4.Q4_STREAM_CUDA_CORE if args.cuda_core else 0) | (q4.Q4_STREAM_SINGLE_BUFFER if single else 0)
+    last_ring = q4.q4_stream_create_ex(shape, [0 if i in keep else hptrs[i] for i in range(n_layers)],
+                                       [dptrs[i] if i in keep else 0 for i in range(n_layers)], B, bufs[0],
+                                       None if single else bufs[1], stride, ws, ws_bytes, flags)
     # end to end through the public call: the step's input copied in from pinned
     # host memory and its result read back, every step
     hin = h0.pin_memory()
@@ -439,21 +534,40 @@ def run_stream(args, torch, q4, model, synth, stream, barrier, gpu_index):
     e2e_secs = time.perf_counter() - t0
     tagged = q4.q4_stream_tagged(last_ring)
     q4.q4_stream_destroy(last_ring)
-    R = runs[-1]["resident_layers"]
+    R = runs[0]["resident_layers"]
     desc = (f"70B-shaped stack, {n_layers} layers, {n_layers - head['resident_layers']} streamed from pinned host "
-            f"memory ({distinct} distinct layer blocks) through two HBM layer buffers"
+            f"memory ({distinct} distinct layer blocks) through {'one HBM layer buffer' if head['single_buffer'] else 'two HBM layer buffers'}"
             f"{', ' + str(head['resident_layers']) + ' resident (' + head['placement'] + ')' if head['resident_layers'] else ''}, "
-            f"{'chunked' if head['chunked'] else 'merged'} copies, batch {B}")
+            f"{'chunked' if head['chunked'] else 'merged'} copies, "
+            f"{'one staging buffer' if head['single_buffer'] else 'two staging buffers'}, batch {B}")
+    # per-layer copy/compute timeline of one token of the headline configuration
+    R0, pat0, chunked0, single0 = combos[0]
+    timelines = {}
+    for single_t in ([single0] + ([not single0] if getattr(args, "with_single", False) else [])):
+        flags = (q4.Q4_STREAM_CHUNKED if chunked0 else 0) | (q4.Q4_STREAM_BARRIER if args.barrier else 0) | (
+            q4.Q4_STREAM_CUDA_CORE if args.cuda_core else 0) | (q4.Q4_STREAM_SINGLE_BUFFER if single_t else 0) | (
+            q4.Q4_STREAM_TIMELINE)
+        keep = set(resident_set(n_layers, R0, pat0))
+        tl_ring = q4.q4_stream_create_ex(shape, [0 if i in keep else hptrs[i] for i in range(n_layers)],
+                                         [dptrs[i] if i in keep else 0 for i in range(n_layers)], B, bufs[0],
+                                         None if single_t else bufs[1], stride, ws, ws_bytes, flags)
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                q4.q4_stream_layers(tl_ring, h, stream=stream)
+        tl = q4.q4_stream_timeline(tl_ring, n_layers, stream=stream)
+        q4.q4_stream_destroy(tl_ring)
+        timelines["single_buffer" if single_t else "double_buffer"] = timeline_summary(tl)
     out = dict(secs=head["secs"], clocks=head["clocks"], bytes_per_step=layer_bytes * n_layers,
                streamed_bytes_per_step=layer_bytes * (n_layers - head["resident_layers"]),
+               h2d_streams=h2d_streams, numa=numa, timelines=timelines,
                launches_per_step=n_layers if B == 1 else 6 * n_layers + 1,
                kernel_launches_per_step=n_layers if B == 1 else 4 * n_layers,
                steps_override=steps, warmup_override=warm, h2d_peak_gbs=best,
                e2e_secs=e2e_secs, e2e_steps=e2e_steps, h2d=h0.numel() * 2, d2h=h0.numel() * 2,
-               e2e_note=f"measured on the last configuration run ({R} resident layers)",
-               workload=desc, kernel="engine_kernel" if B == 1 else "mma_kernel",
+               e2e_note=f"measured on the first configuration run ({R} resident layers)",
+               workload=desc, kernel=("engine_kernel" if args.barrier or args.cuda_core else "tc_engine_kernel") if B == 1 else "mma_kernel",
                kernel_key=None, cfg=cfg, distinct=distinct, host_blocks=host_blocks, tagged=tagged)
-    if sweep:
+    if sweep or len(runs) > 1:
         out["residency_sweep"] = [{k: v for k, v in r.items() if k not in ("secs", "clocks")} for r in runs]
     return out
 
@@ -754,9 +868,13 @@ def extra_result(r, steps, peak):
         d["host_link"] = {"achieved_gbs": round(sb / per_step / 1e9, 2),
                           "pinned_h2d_peak_gbs": round(r["h2d_peak_gbs"], 2),
                           "frac": round(sb / per_step / 1e9 / r["h2d_peak_gbs"], 4) if sb else None,
-                          "streamed_bytes_per_token": sb, "distinct_host_layers": r["distinct"]}
+                          "streamed_bytes_per_token": sb, "distinct_host_layers": r["distinct"],
+                          "peak_by_concurrent_streams": r["h2d_streams"], "numa": r["numa"]}
+        d["timelines"] = r["timelines"]
         d["hbm_frac_of_measured"] = None
         d["gbs_note"] = "weight bytes per token over the token time, most of them copied over the host link"
+    if "residency_sweep" in r:
+        d["modes"] = r["residency_sweep"]
     if "kv_contexts" in r:
         d["kv_contexts"] = r["kv_contexts"]
         d["weight_bytes_per_token"] = r["weight_bytes_per_step"]
@@ -767,7 +885,7 @@ def extra_result(r, steps, peak):
 def run_extras(args, torch, q4, model, synth, stream, barrier, gpu_index, peak):
     import copy
     extras = {}
-    for name, runner, overrides in (("70b", run_stack, {}), ("70b_stream", run_stream, {"resident_frac": 0.0}),
+    for name, runner, overrides in (("70b", run_stack, {}), ("70b_stream", run_stream, {"resident_frac": 0.0, "with_single": True}),
                                     ("8b_kv", run_kv, {})):
         a = copy.copy(args)
         a.config = {"70b": "70b", "70b_stream": "70b-stream", "8b_kv": "8b-kv"}[name]
@@ -796,6 +914,10 @@ def main():
     ap.add_argument("--resident-frac", type=float, default=0.0,
                     help="70b-stream: fraction of the layers (a prefix) kept resident in HBM")
     ap.add_argument("--chunked", action="store_true", help="70b-stream: copy each layer as four chunks")
+    ap.add_argument("--single-buffer", action="store_true",
+                    help="70b-stream: one staging buffer (memory-efficient mode)")
+    ap.add_argument("--with-single", action="store_true",
+                    help="70b-stream: also time the single-buffer mode (merged and chunked) on the same blocks")
     ap.add_argument("--resident-pattern", default="prefix", choices=["prefix", "spread"],
                     help="70b-stream: which layers stay resident")
     ap.add_argument("--batch", type=int, default=1, help="activation rows per step (1..16)")
@@ -881,7 +1003,9 @@ def main():
         out["host_link"] = {"achieved_gbs": round(sb / per_step / 1e9, 2),
                             "pinned_h2d_peak_gbs": round(r["h2d_peak_gbs"], 2),
                             "frac": round(sb / per_step / 1e9 / r["h2d_peak_gbs"], 4) if sb else None,
-                            "streamed_bytes_per_token": sb}
+                            "streamed_bytes_per_token": sb,
+                            "peak_by_concurrent_streams": r["h2d_streams"], "numa": r["numa"]}
+        out["timelines"] = r["timelines"]
         out["config"]["distinct_host_layers"] = r["distinct"]
         out["host_link"]["host_blocks"] = r["host_blocks"]
         if "residency_sweep" in r:

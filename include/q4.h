@@ -425,6 +425,15 @@ typedef struct q4_stream q4_stream;
                                  blockwise transfer) instead of after the whole block */
 #define Q4_STREAM_BARRIER 8   /* as Q4_DEC_BARRIER for the ring's batch-1 engine */
 #define Q4_STREAM_CUDA_CORE 16  /* as Q4_DEC_CUDA_CORE for the ring's batch-1 engine */
+#define Q4_STREAM_SINGLE_BUFFER 32 /* memory-efficient mode (PIPO, Method, "Two pipeline modes"):
+                                   one staging buffer (dev_buf0; dev_buf1 may be null); the copy
+                                   of a streamed layer starts once the compute of the layer before
+                                   it has released the buffer.  With Q4_STREAM_CHUNKED a layer's
+                                   products still start as their own chunks land */
+#define Q4_STREAM_TIMELINE 64 /* record per layer the GPU's global timer (ns) when the copy
+                                 stream starts and ends the layer's copy and when the compute
+                                 stream starts and ends its compute (one-thread stamp kernels on
+                                 both streams); read with q4_stream_timeline */
 
 /*
  * Create a double-buffered copy/compute ring (PipeLLM, "Layer 2"; PIPO,
@@ -435,9 +444,11 @@ typedef struct q4_stream q4_stream;
  *                    layer i's merged block, 16-byte aligned, read only
  *   n_layers >= 1;  batch 1..16
  *   dev_buf0/1       device, buf_bytes >= one layer block each, 256-byte aligned
+ *                    (dev_buf1 unused and may be null with Q4_STREAM_SINGLE_BUFFER)
  *   workspace        device, >= q4_workspace_layout(shape, n_layers, batch) bytes
  *   flags            0, or Q4_STREAM_POISON | Q4_STREAM_TENSOR_CORE | Q4_STREAM_CHUNKED |
- *                    Q4_STREAM_BARRIER | Q4_STREAM_CUDA_CORE
+ *                    Q4_STREAM_BARRIER | Q4_STREAM_CUDA_CORE | Q4_STREAM_SINGLE_BUFFER |
+ *                    Q4_STREAM_TIMELINE
  * The handle creates its own copy stream and events.
  * Errors: Q4_ERR_ARG, Q4_ERR_ALIGN, Q4_ERR_OOM, Q4_ERR_CUDA.
  */
@@ -472,6 +483,15 @@ int q4_stream_layers(q4_stream *st, uint16_t *hidden_io, void *compute_stream, i
 
 /* Status word of the ring's kernels (synchronises compute_stream); clears it. */
 int q4_stream_status(q4_stream *st, void *compute_stream, int *status_out);
+
+/* The copy/compute timeline of the last q4_stream_layers call of a ring
+ * created with Q4_STREAM_TIMELINE (PipeLLM, "Layer 2: Asynchronous Weight
+ * Prefetching": the copy of layer i+1 overlaps the compute of layer i).
+ * Synchronises compute_stream and the ring's copy stream, then writes
+ * out_ns[4 i .. 4 i + 3] = copy begin, copy end, compute begin, compute end of
+ * layer i (GPU global timer, ns; the copy pair is 0 for a resident layer).
+ * n >= 4 * n_layers.  Errors: Q4_ERR_ARG (no timeline, n too small), Q4_ERR_CUDA. */
+int q4_stream_timeline(q4_stream *st, unsigned long long *out_ns, int n, void *compute_stream);
 
 /* As q4_decoder_tagged for a ring.  Host only.  Errors: Q4_ERR_ARG. */
 int q4_stream_tagged(const q4_stream *st, int *tagged_out);

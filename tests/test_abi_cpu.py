@@ -128,7 +128,12 @@ def test_decoder_checks(lib):
     _, lb = q4.q4_layer_offsets(shape)
     assert g(ctypes.byref(s), ctypes.byref(shape), ptrs, 2, 1, 4096, 8192, lb - 1, 4096, ws_bytes, 0) == q4.Q4_ERR_OOM
     assert g(ctypes.byref(s), ctypes.byref(shape), ptrs, 2, 1, 4096, 8192 + 16, lb, 4096, ws_bytes, 0) == q4.Q4_ERR_ALIGN
-    assert g(ctypes.byref(s), ctypes.byref(shape), ptrs, 2, 1, 4096, 8192, lb, 4096, ws_bytes, 32) == q4.Q4_ERR_ARG
+    assert g(ctypes.byref(s), ctypes.byref(shape), ptrs, 2, 1, 4096, 8192, lb, 4096, ws_bytes, 128) == q4.Q4_ERR_ARG
+    # the second staging buffer is required unless the ring runs single-buffered
+    assert g(ctypes.byref(s), ctypes.byref(shape), ptrs, 2, 1, 4096, None, lb, 4096, ws_bytes, 0) == q4.Q4_ERR_ARG
+    single = q4.Q4_STREAM_SINGLE_BUFFER
+    assert g(ctypes.byref(s), ctypes.byref(shape), ptrs, 2, 1, 4096 + 16, None, lb, 4096, ws_bytes,
+             single) == q4.Q4_ERR_ALIGN
     # partial residency: a layer needs a host block or a resident block; resident blocks 256-byte aligned
     gx = lib.q4_stream_create_ex
     none = (ctypes.c_void_p * 2)(None, None)

@@ -23,10 +23,11 @@ class Ring:
         self.shape = q4.LayerShape.of(**cfg)
         self.blocks, self.hptrs = model.host_layers(self.shape, n_layers, seed, distinct=distinct)
         stride = model.layer_stride(self.shape)
-        self.bufs = [torch.empty(stride, dtype=torch.uint8, device="cuda") for _ in range(2)]
+        single = bool(flags & q4.Q4_STREAM_SINGLE_BUFFER)
+        self.bufs = [torch.empty(stride, dtype=torch.uint8, device="cuda") for _ in range(1 if single else 2)]
         self.ws, self.offs, self.ws_bytes = model.workspace(self.shape, n_layers, 1)
-        self.h = q4.q4_stream_create(self.shape, self.hptrs, 1, self.bufs[0], self.bufs[1], stride, self.ws,
-                                     self.ws_bytes, flags)
+        self.h = q4.q4_stream_create(self.shape, self.hptrs, 1, self.bufs[0], None if single else self.bufs[1],
+                                     stride, self.ws, self.ws_bytes, flags)
 
     def run(self, h_np, tokens=1, timeout_us=0):
         h = dev_u16(h_np.reshape(-1))
@@ -92,17 +93,18 @@ def test_host_timeout_returns_and_work_completes():
     ring.close()
 
 
-def _mixed_ring(cfg, n_layers, seed, resident_mask, flags, batch=1):
+def _mixed_ring(cfg, n_layers, seed, resident_mask, flags, batch=1, single=False):
     """A ring where layer i is resident (device block) when resident_mask[i], else streamed."""
     shape = q4.LayerShape.of(**cfg)
     blocks, hptrs = model.host_layers(shape, n_layers, seed)
     wbuf, dptrs = model.resident_layers(shape, n_layers, seed)
     stride = model.layer_stride(shape)
-    bufs = [torch.empty(stride, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    bufs = [torch.empty(stride, dtype=torch.uint8, device="cuda") for _ in range(1 if single else 2)]
     ws, offs, nb = model.workspace(shape, n_layers, batch)
     host = [0 if m else hptrs[i] for i, m in enumerate(resident_mask)]
     res = [dptrs[i] if m else 0 for i, m in enumerate(resident_mask)]
-    h = q4.q4_stream_create_ex(shape, host, res, batch, bufs[0], bufs[1], stride, ws, nb, flags)
+    h = q4.q4_stream_create_ex(shape, host, res, batch, bufs[0], None if single else bufs[1], stride, ws, nb,
+                               flags)
     return h, (blocks, wbuf, bufs, ws)
 
 
@@ -181,3 +183,72 @@ def test_fused_per_layer_and_per_phase_schedules_identical(cfg):
     outs.append(ring.run(h0))
     ring.close()
     assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
+SB = q4.Q4_STREAM_SINGLE_BUFFER
+
+
+@pytest.mark.parametrize("flags", [SB | q4.Q4_STREAM_POISON, SB | q4.Q4_STREAM_POISON | q4.Q4_STREAM_CHUNKED,
+                                   SB | q4.Q4_STREAM_POISON | q4.Q4_STREAM_CUDA_CORE,
+                                   SB | q4.Q4_STREAM_POISON | q4.Q4_STREAM_BARRIER],
+                         ids=["single", "single-chunked", "single-core", "single-barrier"])
+def test_single_buffer_equals_resident(flags):
+    """One staging buffer: every streamed layer overwrites the block the layer
+    before it computed on (poisoned after each compute), over three tokens."""
+    cfg, L = SMALL, 5
+    h0 = synth.activations(1, cfg["hidden"], 90)
+    ring = Ring(cfg, L, seed=91, flags=flags)
+    got = ring.run(h0, tokens=3)
+    ref = resident(cfg, L, 91, h0, tokens=3, core=bool(flags & q4.Q4_STREAM_CUDA_CORE),
+                   barrier=bool(flags & q4.Q4_STREAM_BARRIER))
+    assert np.array_equal(got, ref)
+    ring.close()
+
+
+def test_single_buffer_partial_residency_and_batch():
+    """Single buffer with every other layer resident, batch 1 and batch 4."""
+    cfg, L = SMALL, 6
+    mask = [i % 2 == 1 for i in range(L)]
+    for batch in (1, 4):
+        h0 = synth.activations(batch, cfg["hidden"], 92)
+        flags = SB | q4.Q4_STREAM_POISON
+        h, keep = _mixed_ring(cfg, L, 93, mask, flags, batch=batch, single=True)
+        x = dev_u16(h0.reshape(-1))
+        for _ in range(2):
+            q4.q4_stream_layers(h, x)
+        torch.cuda.synchronize()
+        assert q4.q4_stream_status(h) == 0
+        got = host_u16(x).reshape(batch, -1)
+        h2, keep2 = _mixed_ring(cfg, L, 93, [True] * L, 0, batch=batch)
+        y = dev_u16(h0.reshape(-1))
+        for _ in range(2):
+            q4.q4_stream_layers(h2, y)
+        torch.cuda.synchronize()
+        assert np.array_equal(got, host_u16(y).reshape(batch, -1))
+        q4.q4_stream_destroy(h)
+        q4.q4_stream_destroy(h2)
+
+
+@pytest.mark.parametrize("single", [False, True], ids=["double", "single"])
+def test_timeline_orders_copies_and_compute(single):
+    """The ring's GPU timestamps obey its synchronisation: a layer computes
+    after its copy ended; a buffer is overwritten only after the compute that
+    read it ended (layer i + 2 with two buffers, i + 1 with one); layers
+    compute in order.  Results stay equal to the resident stack."""
+    cfg, L = SMALL, 6
+    flags = q4.Q4_STREAM_TIMELINE | (SB if single else 0)
+    h0 = synth.activations(1, cfg["hidden"], 94)
+    ring = Ring(cfg, L, seed=95, flags=flags)
+    got = ring.run(h0, tokens=2)
+    tl = q4.q4_stream_timeline(ring.h, L).astype(np.int64)
+    assert (tl > 0).all()
+    cb, ce, kb, ke = tl[:, 0], tl[:, 1], tl[:, 2], tl[:, 3]
+    assert (ce >= cb).all() and (ke >= kb).all()
+    assert (kb >= ce).all()                      # compute waits for its own copy
+    assert (kb[1:] >= ke[:-1]).all()             # one compute stream
+    step = 1 if single else 2
+    assert (cb[step:] >= ke[:-step]).all()       # buffer reuse after its reader finished
+    assert np.array_equal(got, resident(cfg, L, 95, h0, tokens=2))
+    with pytest.raises(q4.Q4Error):
+        q4.q4_stream_timeline(ring.h, L - 1)      # buffer too small
+    ring.close()

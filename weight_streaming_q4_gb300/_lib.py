@@ -43,6 +43,8 @@ Q4_STREAM_TENSOR_CORE = 2
 Q4_STREAM_CHUNKED = 4
 Q4_STREAM_BARRIER = 8
 Q4_STREAM_CUDA_CORE = 16
+Q4_STREAM_SINGLE_BUFFER = 32
+Q4_STREAM_TIMELINE = 64
 
 WS_NAMES = ("control", "program", "qkv", "o", "gate", "up", "down", "act", "x", "attn", "x2", "t1", "t2", "flags", "xt", "vt", "actt")
 WS_COUNT = len(WS_NAMES)
@@ -110,6 +112,7 @@ def _declare(lib):
         "q4_kv_append": ([c_p, c_p, c_p, c_p, c_p, c_int, c_int, c_p], c_int),
         "q4_stream_status": ([c_p, c_p, ctypes.POINTER(c_int)], c_int),
         "q4_stream_tagged": ([c_p, ctypes.POINTER(c_int)], c_int),
+        "q4_stream_timeline": ([c_p, c_p, c_int, c_p], c_int),
         "q4_stream_destroy": ([c_p], c_int),
     }
     for name, (args, res) in sig.items():
@@ -321,6 +324,15 @@ def q4_kv_append(k, v, k_cache, v_cache, pos, capacity: int, kv_dim: int, stream
 
 def q4_stream_layers(st, hidden, stream=None, timeout_us: int = 0):
     return _check(lib().q4_stream_layers(st, _ptr(hidden), _stream(stream), timeout_us), "q4_stream_layers")
+
+
+def q4_stream_timeline(st, n_layers: int, stream=None):
+    """[n_layers][4] globaltimer ns: copy begin, copy end, compute begin, compute end."""
+    import numpy as np
+    out = np.zeros(4 * n_layers, dtype=np.uint64)
+    _check(lib().q4_stream_timeline(st, out.ctypes.data_as(ctypes.c_void_p), out.size, _stream(stream)),
+           "q4_stream_timeline")
+    return out.reshape(n_layers, 4)
 
 
 def q4_stream_tagged(st) -> bool:

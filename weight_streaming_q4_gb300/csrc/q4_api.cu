@@ -1120,6 +1120,8 @@ struct q4_stream {
   cudaEvent_t loaded[2][4] = {}, freed[2] = {nullptr, nullptr};
   cudaEvent_t start = nullptr, done = nullptr;
   bool used[2] = {false, false};   // a buffer's `freed` event has been recorded
+  unsigned long long* stamps = nullptr;   // Q4_STREAM_TIMELINE: [layer][copy begin, copy end,
+                                          // compute begin, compute end], globaltimer ns
 };
 
 extern "C" int q4_stream_create(q4_stream** out, const q4_layer_shape* shape, const void* const* host_layers,
@@ -1133,18 +1135,20 @@ extern "C" int q4_stream_create_ex(q4_stream** out, const q4_layer_shape* shape,
                                    const void* const* resident_layers, int n_layers, int batch, void* dev_buf0,
                                    void* dev_buf1, size_t buf_bytes, void* workspace, size_t workspace_bytes,
                                    int flags) {
-  if (!out || !shape_ok(shape) || !host_layers || n_layers < 1 || !dev_buf0 || !dev_buf1 || !workspace)
+  const bool single = (flags & Q4_STREAM_SINGLE_BUFFER) != 0;
+  if (!out || !shape_ok(shape) || !host_layers || n_layers < 1 || !dev_buf0 || (!dev_buf1 && !single) || !workspace)
     return Q4_ERR_ARG;
   if (batch < 1 || batch > q4::kMaxBatch ||
       (flags & ~(Q4_STREAM_POISON | Q4_STREAM_TENSOR_CORE | Q4_STREAM_CHUNKED | Q4_STREAM_BARRIER |
-                 Q4_STREAM_CUDA_CORE)))
+                 Q4_STREAM_CUDA_CORE | Q4_STREAM_SINGLE_BUFFER | Q4_STREAM_TIMELINE)))
     return Q4_ERR_ARG;
   if (4 * n_layers + 1 > static_cast<int>(q4::kPhasesPerEpoch)) return Q4_ERR_ARG;
   const int engine = batch == 1 ? pick_engine(*shape, (flags & Q4_STREAM_TENSOR_CORE) != 0,
                                               (flags & (Q4_STREAM_CUDA_CORE | Q4_STREAM_BARRIER)) != 0)
                                 : ENG_CORE;
   if (batch == 1 ? engine < 0 : !batched_shape_ok(*shape)) return Q4_ERR_ARG;
-  if (!aligned(dev_buf0, 256) || !aligned(dev_buf1, 256) || !aligned(workspace, 256)) return Q4_ERR_ALIGN;
+  if (!aligned(dev_buf0, 256) || (!single && !aligned(dev_buf1, 256)) || !aligned(workspace, 256))
+    return Q4_ERR_ALIGN;
   size_t lo[7], layer_bytes = 0;
   q4_layer_offsets(shape, lo, &layer_bytes);
   if (buf_bytes < layer_bytes) return Q4_ERR_OOM;
@@ -1172,7 +1176,7 @@ extern "C" int q4_stream_create_ex(q4_stream** out, const q4_layer_shape* shape,
     if (res)
       r->resident[l] = static_cast<const uint8_t*>(res);
     else
-      r->slot[l] = (si++) & 1;   // streamed layers alternate between the two buffers
+      r->slot[l] = single ? 0 : (si++) & 1;   // streamed layers alternate between the two buffers
   }
   r->chunk_off[0] = 0;
   r->chunk_off[1] = lo[Q4_PROJ_O];
@@ -1188,7 +1192,7 @@ extern "C" int q4_stream_create_ex(q4_stream** out, const q4_layer_shape* shape,
   r->grid = dev->sm_count < q4::kMaxGrid ? dev->sm_count : q4::kMaxGrid;
   r->host.assign(host_layers, host_layers + n_layers);
   r->buf[0] = static_cast<uint8_t*>(dev_buf0);
-  r->buf[1] = static_cast<uint8_t*>(dev_buf1);
+  r->buf[1] = single ? nullptr : static_cast<uint8_t*>(dev_buf1);
   r->layer_bytes = layer_bytes;
   r->w = carve(workspace, off, shape->hidden);
   cudaError_t e = cudaStreamCreateWithFlags(&r->copy, cudaStreamNonBlocking);
@@ -1199,6 +1203,11 @@ extern "C" int q4_stream_create_ex(q4_stream** out, const q4_layer_shape* shape,
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&r->start, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&r->done, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaMemset(workspace, 0, need);
+  if (e == cudaSuccess && (flags & Q4_STREAM_TIMELINE)) {
+    const size_t sb = 4 * static_cast<size_t>(n_layers) * sizeof(unsigned long long);
+    e = cudaMalloc(&r->stamps, sb);
+    if (e == cudaSuccess) e = cudaMemset(r->stamps, 0, sb);
+  }
   if (e != cudaSuccess) {
     q4_stream_destroy(r);
     return cuda_fail(e);
@@ -1231,16 +1240,19 @@ extern "C" int q4_stream_layers(q4_stream* r, uint16_t* hidden_io, void* compute
   for (int i = 0; i < r->n_layers; ++i) {
     const int b = r->slot[i];
     const uint8_t* wl = b < 0 ? r->resident[i] : r->buf[b];
+    unsigned long long* ts = r->stamps ? r->stamps + 4 * static_cast<size_t>(i) : nullptr;
     if (b >= 0) {
       // copy stream: layer i into buffer b once the last layer computed on b has released it
       if (r->used[b]) Q4_CUDA(cudaStreamWaitEvent(r->copy, r->freed[b], 0));
       r->used[b] = true;
+      if (ts) Q4_CUDA(q4::stamp_launch(ts + 0, r->copy));
       for (int c = 0; c < n_chunks; ++c) {
         const size_t lo = chunked ? r->chunk_off[c] : 0, hi = chunked ? r->chunk_off[c + 1] : r->layer_bytes;
         Q4_CUDA(cudaMemcpyAsync(r->buf[b] + lo, static_cast<const uint8_t*>(r->host[i]) + lo, hi - lo,
                                 cudaMemcpyHostToDevice, r->copy));
         Q4_CUDA(cudaEventRecord(r->loaded[b][c], r->copy));
       }
+      if (ts) Q4_CUDA(q4::stamp_launch(ts + 1, r->copy));
     }
     const bool last = i == r->n_layers - 1;
     int st = Q4_OK;
@@ -1252,16 +1264,19 @@ extern "C" int q4_stream_layers(q4_stream* r, uint16_t* hidden_io, void* compute
                                 b < 0 ? nullptr : ev);
     } else if (b < 0 || !chunked) {
       if (b >= 0) Q4_CUDA(cudaStreamWaitEvent(cs, r->loaded[b][0], 0));
+      if (ts) Q4_CUDA(q4::stamp_launch(ts + 2, cs));
       st = launch_layers(r->w, 4 * i, last ? 5 : 4, r->grid, cs, r->engine, r->tagged, last, r->shape);
     } else {
       // chunked: phase p of the layer starts once chunk p has landed (one launch per phase)
       for (int p = 0; p < 4 && st == Q4_OK; ++p) {
         Q4_CUDA(cudaStreamWaitEvent(cs, r->loaded[b][p], 0));
+        if (ts && p == 0) Q4_CUDA(q4::stamp_launch(ts + 2, cs));
         st = launch_layers(r->w, 4 * i + p, (last && p == 3) ? 2 : 1, r->grid, cs, r->engine, r->tagged,
                            last && p == 3, r->shape);
       }
     }
     if (st != Q4_OK) return st;
+    if (ts) Q4_CUDA(q4::stamp_launch(ts + 3, cs));
     if (b >= 0) {
       if (r->flags & Q4_STREAM_POISON) Q4_CUDA(q4::poison_launch(r->buf[b], n_blocks, cs));
       Q4_CUDA(cudaEventRecord(r->freed[b], cs));
@@ -1288,6 +1303,15 @@ extern "C" int q4_stream_status(q4_stream* r, void* compute_stream, int* status_
   return read_status(r->w.ctl, static_cast<cudaStream_t>(compute_stream), status_out);
 }
 
+extern "C" int q4_stream_timeline(q4_stream* r, unsigned long long* out_ns, int n, void* compute_stream) {
+  if (!r || !out_ns || !r->stamps || n < 4 * r->n_layers) return Q4_ERR_ARG;
+  Q4_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(compute_stream)));
+  Q4_CUDA(cudaStreamSynchronize(r->copy));
+  Q4_CUDA(cudaMemcpy(out_ns, r->stamps, 4 * static_cast<size_t>(r->n_layers) * sizeof(unsigned long long),
+                     cudaMemcpyDeviceToHost));
+  return Q4_OK;
+}
+
 extern "C" int q4_stream_tagged(const q4_stream* r, int* tagged_out) {
   if (!r || !tagged_out) return Q4_ERR_ARG;
   *tagged_out = r->tagged ? 1 : 0;
@@ -1304,6 +1328,7 @@ extern "C" int q4_stream_destroy(q4_stream* r) {
   }
   if (r->start) cudaEventDestroy(r->start);
   if (r->done) cudaEventDestroy(r->done);
+  if (r->stamps) cudaFree(r->stamps);
   if (r->copy) cudaStreamDestroy(r->copy);
   delete r;
   return Q4_OK;

@@ -107,4 +107,18 @@ cudaError_t poison_launch(uint8_t* buf, size_t n_blocks, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// The GPU's global nanosecond timer, written when the stream reaches this
+// point (copy/compute timelines of the ring: stamps on both streams share
+// one clock).
+__global__ void stamp_kernel(unsigned long long* out) {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  *out = t;
+}
+
+cudaError_t stamp_launch(unsigned long long* out, cudaStream_t stream) {
+  stamp_kernel<<<1, 1, 0, stream>>>(out);
+  return cudaGetLastError();
+}
+
 }  // namespace q4

@@ -363,6 +363,7 @@ cudaError_t simple_launch(const uint8_t* w, const uint16_t* x, float* y, int n, 
                           cudaStream_t stream);
 cudaError_t dequant_launch(const uint8_t* w, float* out, int n, int k, cudaStream_t stream);
 cudaError_t poison_launch(uint8_t* buf, size_t n_blocks, cudaStream_t stream);
+cudaError_t stamp_launch(unsigned long long* out, cudaStream_t stream);
 cudaError_t attn_prepare();
 size_t attn_workspace_bytes(int n_q, int n_kv, int hd, int capacity);
 int attn_chunk(int capacity, int n_kv);
