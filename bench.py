@@ -55,6 +55,7 @@ def peaks():
 KERNEL_SOURCES = {
     "engine_kernel": ("q4_engine.cu", "q4_device.cuh", "q4_phase.cuh"),
     "tc_engine_kernel": ("q4_tc_engine.cu", "q4_frag.cuh", "q4_device.cuh", "q4_phase.cuh"),
+    "oneshot_kernel": ("q4_oneshot.cu", "q4_frag.cuh", "q4_device.cuh"),
     "mma_kernel": ("q4_mma.cu", "q4_frag.cuh", "q4_device.cuh"),
 }
 
@@ -298,7 +299,7 @@ def run_gemv(args, torch, q4, model, synth, stream, barrier, gpu_index):
     return dict(secs=secs, clocks=clocks, bytes_per_step=mb * copies, launches_per_step=copies,
                 e2e_secs=e2e_secs, e2e_steps=e2e_steps, e2e_bytes_per_step=mb, h2d=2 * k, d2h=4 * n,
                 workload=f"single Q4_0 product N=K=4096, batch 1, ring of {copies} weight copies (> L2)",
-                kernel="tc_engine_kernel", kernel_key="tc_engine_kernel:gemv", cfg=dict(n=n, k=k, copies=copies))
+                kernel="oneshot_kernel", kernel_key="oneshot_kernel:gemv", cfg=dict(n=n, k=k, copies=copies))
 
 
 def h2d_multi_stream(torch, blocks, nbytes, counts=(1, 2, 4)):

@@ -87,7 +87,16 @@ size_t q4_matrix_bytes(int n, int k);
 #define Q4_KERNEL_MMA 3      /* persistent TMA-ring kernel, tensor-core products (batch 1..16) */
 #define Q4_KERNEL_TC 4       /* persistent tensor-core engine, one phase (batch 1, k % 256 == 0 and
                                 k <= 2048 or k % 2048 == 0, k <= 30720); what q4_gemv uses at
-                                batch 1 for those widths */
+                                batch 1 for those widths above 64 MB of weights */
+#define Q4_KERNEL_ONESHOT 5  /* one-shot tensor-core kernel for a single product: a CTA per 16
+                                rows, the whole tile fetched at once by bulk copies, launched with
+                                programmatic stream serialisation so that consecutive launches
+                                overlap: a launch fetches its weights, reads x and computes while
+                                the one before it finishes, and stores y after it; the launcher
+                                asks for that only when w and x do not overlap the y of a
+                                one-shot product on the same stream that may still be running
+                                (batch 1, k % 512 == 0, 11 k + 256 <= 231424: k <= 20992); what
+                                q4_gemv uses at batch 1 for those widths up to 64 MB of weights */
 
 /*
  * y[b][n] = sum_k W[n][k] * x[b][k], W dequantisation-free from its Q4_0 blocks

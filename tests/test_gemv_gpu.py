@@ -12,7 +12,7 @@ from pins import golden_blocks
 pytestmark = pytest.mark.gpu
 
 KERNELS = {"stream": q4.Q4_KERNEL_STREAM, "simple": q4.Q4_KERNEL_SIMPLE, "mma": q4.Q4_KERNEL_MMA,
-           "tc": q4.Q4_KERNEL_TC}
+           "tc": q4.Q4_KERNEL_TC, "oneshot": q4.Q4_KERNEL_ONESHOT}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -123,6 +123,76 @@ def test_tc_engine_parity(n, k):
     assert q4.q4_device_status() == 0
 
 
+# one-shot kernel: widths from 512 to the shared-memory limit (11 k + 256 <=
+# 231424 bytes: k <= 20992), row counts with a ragged last 16-row tile
+ONESHOT_SHAPES = [(1, 512), (15, 512), (16, 1024), (17, 4096), (300, 4096), (61, 14336), (33, 20992),
+                  (4096, 4096), (1000, 8192), (100, 2560)]
+
+
+@pytest.mark.parametrize("n,k", ONESHOT_SHAPES)
+def test_oneshot_parity(n, k):
+    w = synth.q4_matrix(n, k, 20, synth.GEMV_TID)
+    x = synth.activations(1, k, 21)
+    y = run(w, x, n, k, 1, q4.Q4_KERNEL_ONESHOT)
+    y_ref, s_ref = ora.gemv(w, x, n, k, threads=8)
+    assert_within_tol(y, y_ref, s_ref, f"oneshot {n}x{k}")
+    assert q4.q4_device_status() == 0
+
+
+def test_oneshot_rejects_and_orders_back_to_back_launches():
+    w = dev_u8(synth.q4_matrix(64, 4096, 22, synth.GEMV_TID))
+    x = dev_u16(synth.activations(1, 21504, 23).reshape(-1))
+    y = torch.empty(64, dtype=torch.float32, device="cuda")
+    for k, batch in ((256, 1), (4096 + 256, 1), (21504, 1), (4096, 2)):   # width, shared memory, batch
+        with pytest.raises(q4.Q4Error):
+            q4.q4_gemv_ex(w, x, y, 4, k, batch, q4.Q4_KERNEL_ONESHOT)
+    # launches that overlap their setup with the previous one still write y in
+    # stream order: alternate two matrices into one y, eagerly and from a graph
+    n, k = 1000, 4096
+    wa, wb = (synth.q4_matrix(n, k, s, synth.GEMV_TID) for s in (24, 25))
+    xs = synth.activations(1, k, 26)
+    da, db, dx = dev_u8(wa), dev_u8(wb), dev_u16(xs.reshape(-1))
+    y = torch.empty(n, dtype=torch.float32, device="cuda")
+    ya, yb = run(wa, xs, n, k, 1, q4.Q4_KERNEL_ONESHOT), run(wb, xs, n, k, 1, q4.Q4_KERNEL_ONESHOT)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for i in range(41):
+            q4.q4_gemv_ex(da if i % 2 == 0 else db, dx, y, n, k, 1, q4.Q4_KERNEL_ONESHOT, stream=s)
+        s.synchronize()
+        assert np.array_equal(host_f32(y), ya[0])
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for i in range(40):
+                q4.q4_gemv_ex(da if i % 2 == 0 else db, dx, y, n, k, 1, q4.Q4_KERNEL_ONESHOT, stream=s)
+        g.replay()
+        s.synchronize()
+    assert np.array_equal(host_f32(y), yb[0])
+    assert q4.q4_device_status() == 0
+
+
+def test_oneshot_input_from_the_previous_output():
+    """x of a product is the memory of the previous one-shot product's y (its
+    fp32 bits read as binary16): the launcher must not start the second one
+    early, so it sees the whole first output."""
+    n1, k1, n2, k2 = 2048, 4096, 512, 4096          # y1: 2048 fp32 = 4096 binary16
+    w1 = synth.q4_matrix(n1, k1, 27, synth.GEMV_TID)
+    w2 = synth.q4_matrix(n2, k2, 28, synth.GEMV_TID)
+    d1, d2 = dev_u8(w1), dev_u8(w2)
+    x1 = dev_u16(synth.activations(1, k1, 29).reshape(-1))
+    buf = torch.empty(n1, dtype=torch.float32, device="cuda")
+    y2 = torch.empty(n2, dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            buf.fill_(0.0)
+            q4.q4_gemv_ex(d1, x1, buf, n1, k1, 1, q4.Q4_KERNEL_ONESHOT, stream=s)
+            q4.q4_gemv_ex(d2, buf, y2, n2, k2, 1, q4.Q4_KERNEL_ONESHOT, stream=s)
+        s.synchronize()
+    x2 = buf.detach().cpu().view(torch.int16).numpy().view(np.uint16).copy()
+    ref = run(w2, x2, n2, k2, 1, q4.Q4_KERNEL_ONESHOT)
+    assert np.array_equal(host_f32(y2), ref[0], equal_nan=True)
+
+
 def test_tc_engine_rejects_unsupported_widths():
     x = torch.zeros(32768, dtype=torch.int16, device="cuda")
     y = torch.zeros(64, dtype=torch.float32, device="cuda")
@@ -201,14 +271,26 @@ def test_stream_kernel_width_limit():
     assert not y.any()
 
 
-def test_deterministic_and_auto_is_tc():
+def test_deterministic_and_auto_choice():
     n, k = 512, 4096
     w = synth.q4_matrix(n, k, 1, synth.GEMV_TID)
     x = synth.activations(1, k, 1)
     a = run(w, x, n, k, 1, q4.Q4_KERNEL_AUTO)
-    b = run(w, x, n, k, 1, q4.Q4_KERNEL_TC)
-    c = run(w, x, n, k, 1, q4.Q4_KERNEL_TC)
+    b = run(w, x, n, k, 1, q4.Q4_KERNEL_ONESHOT)
+    c = run(w, x, n, k, 1, q4.Q4_KERNEL_ONESHOT)
     assert np.array_equal(a, b) and np.array_equal(b, c)
+    t1, t2 = run(w, x, n, k, 1, q4.Q4_KERNEL_TC), run(w, x, n, k, 1, q4.Q4_KERNEL_TC)
+    assert np.array_equal(t1, t2)
+    # above 64 MB of weights auto takes the persistent engine
+    nb, kb = 65536, 2048
+    wd = torch.empty(q4.q4_matrix_bytes(nb, kb), dtype=torch.uint8, device="cuda")
+    synth.device_fill_q4(wd.data_ptr(), nb * kb // 32, seed=1, tid=synth.GEMV_TID)
+    xd = dev_u16(synth.activations(1, kb, 1).reshape(-1))
+    ya, yt = (torch.empty(nb, dtype=torch.float32, device="cuda") for _ in range(2))
+    q4.q4_gemv_ex(wd, xd, ya, nb, kb, 1, q4.Q4_KERNEL_AUTO)
+    q4.q4_gemv_ex(wd, xd, yt, nb, kb, 1, q4.Q4_KERNEL_TC)
+    torch.cuda.synchronize()
+    assert torch.equal(ya, yt)
     d = run(w, x, n, k, 1, q4.Q4_KERNEL_STREAM)
     e = run(w, x, n, k, 1, q4.Q4_KERNEL_STREAM)
     assert np.array_equal(d, e)

@@ -32,6 +32,7 @@ Q4_KERNEL_STREAM = 1
 Q4_KERNEL_SIMPLE = 2
 Q4_KERNEL_MMA = 3
 Q4_KERNEL_TC = 4
+Q4_KERNEL_ONESHOT = 5
 
 Q4_DEC_FUSED = 0
 Q4_DEC_PER_LAYER = 1

@@ -64,6 +64,7 @@ int device_info(DeviceInfo** out) {
     Q4_CUDA(q4::engine_prepare());
     Q4_CUDA(q4::mma_prepare());
     Q4_CUDA(q4::tc_engine_prepare());
+    Q4_CUDA(q4::oneshot_prepare());
     Q4_CUDA(q4::attn_prepare());
     Q4_CUDA(q4::engine_occupancy(&d.engine_blocks_per_sm));
     if (d.engine_blocks_per_sm < 1) return Q4_ERR_CUDA;
@@ -230,14 +231,29 @@ extern "C" int q4_gemv_ex(const void* w, const uint16_t* x, float* y, int n, int
   if (st != Q4_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (kernel == Q4_KERNEL_AUTO) {
-    // batch 1: the CUDA-core engine (plain kernel for widths it cannot take);
-    // batch 2..16: tensor cores when rows are 16-byte aligned
-    if (batch == 1) kernel = tc_ok(k) ? Q4_KERNEL_TC : engine_ok(k) ? Q4_KERNEL_STREAM : Q4_KERNEL_SIMPLE;
+    // batch 1: the one-shot kernel up to 64 MB of weights (it overlaps
+    // consecutive launches), the persistent tensor-core engine above that (its
+    // ring streams large matrices faster), else the CUDA-core engine or the
+    // plain kernel for widths they cannot take; batch 2..16: tensor cores when
+    // rows are 16-byte aligned
+    const size_t bytes = static_cast<size_t>(n) * (k / q4::kQK) * q4::kBlockBytes;
+    if (batch == 1)
+      kernel = q4::oneshot_ok(n, k) && bytes <= (size_t(64) << 20) ? Q4_KERNEL_ONESHOT
+               : tc_ok(k)                                          ? Q4_KERNEL_TC
+               : engine_ok(k)                                      ? Q4_KERNEL_STREAM
+                                                                   : Q4_KERNEL_SIMPLE;
     else if (k % 256 == 0) kernel = Q4_KERNEL_MMA;
     else kernel = Q4_KERNEL_SIMPLE;
   }
   if (kernel == Q4_KERNEL_SIMPLE) {
     Q4_CUDA(q4::simple_launch(static_cast<const uint8_t*>(w), x, y, n, k, batch, s));
+    return Q4_OK;
+  }
+  if (kernel == Q4_KERNEL_ONESHOT) {
+    if (batch != 1 || !q4::oneshot_ok(n, k)) return Q4_ERR_ARG;
+    DeviceInfo* dev = nullptr;
+    if ((st = device_info(&dev)) != Q4_OK) return st;
+    Q4_CUDA(q4::oneshot_launch(static_cast<const uint8_t*>(w), x, y, n, k, kWaitLimit, s));
     return Q4_OK;
   }
   if (kernel == Q4_KERNEL_MMA) {
@@ -290,9 +306,10 @@ extern "C" int q4_device_status(void) {
   int v = 0, m = 0;
   Q4_CUDA(q4::engine_read_status(&v));
   Q4_CUDA(q4::mma_read_status(&m));
-  int tc = 0;
+  int tc = 0, os = 0;
   Q4_CUDA(q4::tc_engine_read_status(&tc));
-  return v | m | tc;
+  Q4_CUDA(q4::oneshot_read_status(&os));
+  return v | m | tc | os;
 }
 
 extern "C" int q4_dequant_debug(const void* w, float* w_out, int n, int k, void* stream) {
@@ -1250,9 +1267,11 @@ extern "C" int q4_stream_layers(q4_stream* r, uint16_t* hidden_io, void* compute
         const size_t lo = chunked ? r->chunk_off[c] : 0, hi = chunked ? r->chunk_off[c + 1] : r->layer_bytes;
         Q4_CUDA(cudaMemcpyAsync(r->buf[b] + lo, static_cast<const uint8_t*>(r->host[i]) + lo, hi - lo,
                                 cudaMemcpyHostToDevice, r->copy));
+        // the copy-end stamp precedes the last chunk's event, so the compute
+        // that waits for that event stamps its start after it
+        if (ts && c == n_chunks - 1) Q4_CUDA(q4::stamp_launch(ts + 1, r->copy));
         Q4_CUDA(cudaEventRecord(r->loaded[b][c], r->copy));
       }
-      if (ts) Q4_CUDA(q4::stamp_launch(ts + 1, r->copy));
     }
     const bool last = i == r->n_layers - 1;
     int st = Q4_OK;

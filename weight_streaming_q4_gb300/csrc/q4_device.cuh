@@ -375,6 +375,14 @@ cudaError_t pos_advance_launch(int* pos, cudaStream_t s);
 // status (nullable): ST_KV_POS is or-ed in when *pos is outside 0..capacity-1.
 cudaError_t kv_append_launch(const float* k, const float* v, uint16_t* kc, uint16_t* vc, const int* pos, int capacity,
                              int kv_dim, cudaStream_t s, int* status = nullptr);
+// One-shot batch-1 product (q4_oneshot.cu): 16-row tiles, one CTA each.
+constexpr int kOsSmemMax = 231424;   // dynamic bytes; with the static ones within the 227 KB a CTA may use
+bool oneshot_ok(int n, int k);
+size_t oneshot_smem_bytes(int k);
+cudaError_t oneshot_prepare();
+cudaError_t oneshot_launch(const uint8_t* w, const uint16_t* x, float* y, int n, int k, uint32_t wait_limit,
+                           cudaStream_t stream);
+cudaError_t oneshot_read_status(int* out);
 cudaError_t tc_engine_prepare();
 cudaError_t tc_engine_launch(const EngineArgs& a, int grid, bool cooperative, cudaStream_t stream);
 cudaError_t tc_engine_read_status(int* out);

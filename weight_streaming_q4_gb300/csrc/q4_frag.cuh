@@ -54,6 +54,37 @@ __device__ __forceinline__ void unpack_word(uint32_t w, uint32_t magic, uint32_t
   h13 = *reinterpret_cast<uint32_t*>(&D);
 }
 
+__device__ __forceinline__ float lo_half_f(uint32_t w) { return __low2float(*reinterpret_cast<const __half2*>(&w)); }
+__device__ __forceinline__ float hi_half_f(uint32_t w) { return __high2float(*reinterpret_cast<const __half2*>(&w)); }
+
+// One block pair (even block, odd block after it) of tile rows g and g + 8:
+// rg, rh point at the pair's 36 bytes in the two staged rows.  ee/eh collect
+// the even block (valid in lane quarter 0), og/oh the odd one (quarter 3).
+__device__ __forceinline__ void pair_mma(const uint8_t* rg, const uint8_t* rh, int t, const uint4& xe, const uint4& xo,
+                                         uint32_t magic, float& eg, float& eh, float& og, float& oh) {
+  const uint32_t* pg = reinterpret_cast<const uint32_t*>(rg);
+  const uint32_t* ph = reinterpret_cast<const uint32_t*>(rh);
+  const uint32_t g0 = pg[t], g1 = pg[t + 1], go = pg[5 + t];
+  const uint32_t h0 = ph[t], h1 = ph[t + 1], ho = ph[5 + t];
+  uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+  // even block: its code bytes start 2 bytes into the pair, word t is a funnel of words t, t+1
+  unpack_word(__funnelshift_r(g0, g1, 16), magic, a0, a1, a2, a3);
+  unpack_word(__funnelshift_r(h0, h1, 16), magic, b0, b1, b2, b3);
+  float c[4] = {0.f, 0.f, 0.f, 0.f};
+  mma16816(c, a0, b0, a1, b1, xe.x, xe.y);
+  mma16816(c, a2, b2, a3, b3, xe.z, xe.w);
+  eg = fmaf(lo_half_f(g0), c[0], eg);   // quarter 0: word 0 starts with the even block's d
+  eh = fmaf(lo_half_f(h0), c[2], eh);
+  // odd block: code words 5..8 of the pair, 4-byte aligned
+  unpack_word(go, magic, a0, a1, a2, a3);
+  unpack_word(ho, magic, b0, b1, b2, b3);
+  float e[4] = {0.f, 0.f, 0.f, 0.f};
+  mma16816(e, a0, b0, a1, b1, xo.x, xo.y);
+  mma16816(e, a2, b2, a3, b3, xo.z, xo.w);
+  og = fmaf(hi_half_f(g1), e[0], og);   // quarter 3: word 4 ends with the odd block's d
+  oh = fmaf(hi_half_f(h1), e[2], oh);
+}
+
 // The B fragments of one block for batch column `col`: x elements in the
 // k order of unpack_word (zero for columns beyond the batch).
 __device__ __forceinline__ void x_frags(const __half* x, int k, int batch, int col, int blk, int t, uint32_t& s0b0,
