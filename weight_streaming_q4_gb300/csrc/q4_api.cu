@@ -879,19 +879,20 @@ static int decoder_enqueue(q4_decoder* d, cudaStream_t s) {
     return Q4_OK;
   }
   if (d->kv) {
-    // per layer: the q|k|v phase; this token's k and v into row *pos of the
-    // layer's caches; attention over rows 0..*pos; the o, gate|up and down
-    // phases; after the last layer the position advances
+    // layer l: the q|k|v phase; one attention kernel that stores this token's
+    // k and v in row *pos of the layer's caches and attends over rows
+    // 0..*pos; then one engine launch runs the o, gate|up and down phases of
+    // layer l and the q|k|v phase of layer l + 1 (or the closing phase).
+    // After the last layer the position advances.
     const q4_layer_shape& sh = d->shape;
+    int st = launch_layers(d->w, 0, 1, d->grid, s, d->engine, true, false, sh);
+    if (st != Q4_OK) return st;
     for (int l = 0; l < L; ++l) {
-      int st = launch_layers(d->w, 4 * l, 1, d->grid, s, d->engine, true, false, sh);
-      if (st != Q4_OK) return st;
       const float* qkv = d->w.qkv;
-      Q4_CUDA(q4::kv_append_launch(qkv + sh.q_dim, qkv + sh.q_dim + sh.kv_dim, d->kc[l], d->vc[l], d->pos, d->capacity,
-                                   sh.kv_dim, s, &d->w.ctl->status));
+      const q4::AttnAppend app = {qkv + sh.q_dim, qkv + sh.q_dim + sh.kv_dim, d->pos, &d->w.ctl->status};
       Q4_CUDA(q4::attn_launch(qkv, d->kc[l], d->vc[l], d->pos, d->capacity, sh.q_dim / sh.head_dim,
-                              sh.kv_dim / sh.head_dim, sh.head_dim, d->w.attn, d->attn_ws, s, 1));
-      st = launch_layers(d->w, 4 * l + 1, l == L - 1 ? 4 : 3, d->grid, s, d->engine, true, l == L - 1, sh);
+                              sh.kv_dim / sh.head_dim, sh.head_dim, d->w.attn, d->attn_ws, s, 1, &app));
+      st = launch_layers(d->w, 4 * l + 1, 4, d->grid, s, d->engine, true, l == L - 1, sh);
       if (st != Q4_OK) return st;
     }
     Q4_CUDA(q4::pos_advance_launch(d->pos, s));

@@ -42,6 +42,16 @@ struct AttnArgs {
   const __half* v;
   const int* ctx_len;    // positions in use (plus ctx_add)
   int ctx_add;
+  // with new_k set, the token's own key and value (fp32 [n_kv * hd]) go into
+  // row *pos of the caches (kw, vw: the same arrays as k, v) as part of this
+  // kernel: the CTA whose chunk holds that row uses them directly and stores
+  // them; *pos outside 0..capacity-1 sets ST_KV_POS in *status and stores nothing
+  const float* new_k;
+  const float* new_v;
+  const int* pos;
+  __half* kw;
+  __half* vw;
+  int* status;
   float* part;           // fp32 [n_q][n_chunks][hd + 2]: m, l, o[0..hd)
   unsigned* arrive;      // [n_kv] chunks of the value head done (the last one combines and resets it)
   __half* out;           // binary16 [n_q][hd]
@@ -114,11 +124,39 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const __grid_constan
   float* red = ps + group * P;
   __shared__ int is_last;
   const int cpr = hd / 8;            // 16-byte chunks per row
+  // the row of this token's own key and value, when this kernel appends them
+  int own = -1;
+  if (a.new_k) {
+    const int p = *a.pos;
+    if (p < 0 || p >= a.capacity) {
+      if (g == 0 && c == 0 && tid == 0) atomicOr(a.status, ST_KV_POS);
+    } else if (p >= t0 && p < t0 + nt) {
+      own = p - t0;
+    }
+  }
   for (int i = tid; i < nt * cpr; i += kAttnThreads) {
     const int t = i / cpr, cc = i % cpr;
     const size_t src = static_cast<size_t>(t0 + t) * kv_dim + static_cast<size_t>(g) * hd + cc * 8;
-    cp_async16(ks + t * hd + ((cc ^ (t & 7)) * 8), a.k + src);
-    cp_async16(vs + t * hd + cc * 8, a.v + src);
+    if (t == own) {
+      // f16 of the fp32 key and value, into shared memory and the caches
+      const float* kf = a.new_k + static_cast<size_t>(g) * hd + cc * 8;
+      const float* vf = a.new_v + static_cast<size_t>(g) * hd + cc * 8;
+      uint4 kh, vh;
+      __half2* k2 = reinterpret_cast<__half2*>(&kh);
+      __half2* v2 = reinterpret_cast<__half2*>(&vh);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        k2[e] = __floats2half2_rn(kf[2 * e], kf[2 * e + 1]);
+        v2[e] = __floats2half2_rn(vf[2 * e], vf[2 * e + 1]);
+      }
+      *reinterpret_cast<uint4*>(ks + t * hd + ((cc ^ (t & 7)) * 8)) = kh;
+      *reinterpret_cast<uint4*>(vs + t * hd + cc * 8) = vh;
+      *reinterpret_cast<uint4*>(a.kw + src) = kh;
+      *reinterpret_cast<uint4*>(a.vw + src) = vh;
+    } else {
+      cp_async16(ks + t * hd + ((cc ^ (t & 7)) * 8), a.k + src);
+      cp_async16(vs + t * hd + cc * 8, a.v + src);
+    }
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
   for (int i = tid; i < group * hd; i += kAttnThreads)
@@ -308,9 +346,16 @@ cudaError_t attn_prepare() {
 }
 
 cudaError_t attn_launch(const float* q, const uint16_t* k, const uint16_t* v, const int* ctx_len, int capacity,
-                        int n_q, int n_kv, int hd, uint16_t* out, void* ws, cudaStream_t s, int ctx_add) {
+                        int n_q, int n_kv, int hd, uint16_t* out, void* ws, cudaStream_t s, int ctx_add,
+                        const AttnAppend* app) {
   AttnArgs a;
   a.ctx_add = ctx_add;
+  a.new_k = app ? app->k : nullptr;
+  a.new_v = app ? app->v : nullptr;
+  a.pos = app ? app->pos : nullptr;
+  a.kw = reinterpret_cast<__half*>(const_cast<uint16_t*>(k));
+  a.vw = reinterpret_cast<__half*>(const_cast<uint16_t*>(v));
+  a.status = app ? app->status : nullptr;
   a.q = q;
   a.k = reinterpret_cast<const __half*>(k);
   a.v = reinterpret_cast<const __half*>(v);

@@ -368,9 +368,19 @@ cudaError_t attn_prepare();
 size_t attn_workspace_bytes(int n_q, int n_kv, int hd, int capacity);
 int attn_chunk(int capacity, int n_kv);
 // ctx_add: the positions in use are *ctx_len + ctx_add (the decoder passes its
-// position counter and 1).
+// position counter and 1).  With `app`, the kernel also stores the token's key
+// and value (fp32 app->k, app->v) as binary16 in row *app->pos of the caches
+// (which must be row ctx - 1) and attends to them; *pos outside the bucket sets
+// ST_KV_POS in *app->status.
+struct AttnAppend {
+  const float* k;
+  const float* v;
+  const int* pos;
+  int* status;
+};
 cudaError_t attn_launch(const float* q, const uint16_t* k, const uint16_t* v, const int* ctx_len, int capacity,
-                        int n_q, int n_kv, int hd, uint16_t* out, void* ws, cudaStream_t s, int ctx_add = 0);
+                        int n_q, int n_kv, int hd, uint16_t* out, void* ws, cudaStream_t s, int ctx_add = 0,
+                        const AttnAppend* app = nullptr);
 cudaError_t pos_advance_launch(int* pos, cudaStream_t s);
 // status (nullable): ST_KV_POS is or-ed in when *pos is outside 0..capacity-1.
 cudaError_t kv_append_launch(const float* k, const float* v, uint16_t* kc, uint16_t* vc, const int* pos, int capacity,
