@@ -387,24 +387,23 @@ size_t q4_noalloc_scratch_bytes(void);
  * architecture").  For query head h and its value head g = h / (n_q/n_kv):
  *   s_t = q[h] . k[t][g] / sqrt(head_dim) for t < ctx,
  *   out[h] = f16(sum_t softmax(s)_t v[t][g]),
- * scores and weights in fp32 (max-shifted softmax, split over chunks of 128
- * positions and combined in a fixed order).  Keys are stored as the model uses them (any
+ * scores and weights in fp32: one thread-block cluster per value head (16
+ * CTAs where the GPU schedules clusters that large, else 8) splits the context,
+ * each CTA keeps a running max-shifted softmax state over rounds of up to 256
+ * positions, and the states are combined through distributed shared memory in
+ * rank order (a fixed order).  Keys are stored as the model uses them (any
  * position encoding already applied).
  *   q                 device, fp32 [n_q_heads * head_dim]
  *   k_cache, v_cache  device, binary16 [capacity][n_kv_heads * head_dim], read only
  *   ctx_len           device int, the positions in use (clamped to 1..capacity);
  *                     read by the kernels, so a graph captured for one bucket
  *                     serves every length up to its capacity
- *   capacity          the bucket: a multiple of 128, at most 65536 (and small enough
- *                     that every chunk's max and sum of a value head's query heads fit
- *                     the combining CTA's shared memory: 8 * group * chunks + 4 * group
- *                     <= 2 * chunk * head_dim bytes; Q4_ERR_ARG otherwise)
+ *   capacity          the bucket: a multiple of 128, at most 65536
  *   n_q_heads, n_kv_heads  n_q a multiple of n_kv, at most 16 query heads per value head
  *   head_dim          64, 128, 192 or 256
  *   out               device, binary16 [n_q_heads * head_dim], written
- *   workspace         device, >= q4_attn_workspace_bytes(...) (partial results and
- *                     per-head arrival counters): zero-filled before its first use,
- *                     left reusable by every call; one call at a time per workspace
+ *   workspace         device, >= q4_attn_workspace_bytes(...) (16 bytes, reserved:
+ *                     the partial results stay in the cluster's shared memory)
  * Pointers 16-byte aligned (ctx_len 4).  Asynchronous on `stream`.
  * Errors: Q4_ERR_ARG, Q4_ERR_ALIGN, Q4_ERR_OOM, Q4_ERR_CUDA.
  */

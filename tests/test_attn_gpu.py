@@ -137,5 +137,16 @@ def test_argument_checks():
             q4.q4_attn_decode(t, t, t, ctx, cap, nq, nkv, hd, t, t, 1 << 17)
         assert e.value.status == q4.Q4_ERR_ARG
     with pytest.raises(q4.Q4Error) as e:
-        q4.q4_attn_decode(t, t, t, ctx, 512, 32, 8, 128, t, t, 16)
+        q4.q4_attn_decode(t, t, t, ctx, 512, 32, 8, 128, t, t, q4.q4_attn_workspace_bytes(32, 8, 128, 512) - 1)
     assert e.value.status == q4.Q4_ERR_OOM
+
+
+@pytest.mark.parametrize("cap,ctx,hd", [(16384, 16384, 128), (16384, 9000, 128), (8192, 8192, 256),
+                                        (65536, 40000, 64)])
+def test_long_buckets_take_several_rounds(cap, ctx, hd):
+    """Spans longer than one round of positions per CTA: the running softmax
+    state is rescaled across rounds (and rounds of 128 positions at head_dim
+    256)."""
+    n_q, n_kv = 8, 2
+    q, kc, vc = make_case(n_q, n_kv, hd, cap, seed=ctx % 97 + hd, q_scale=0.5)
+    check(Attn(q, kc, vc, n_q, n_kv, hd, cap).run(ctx), q, kc, vc, ctx, n_q, n_kv, hd, f"cap {cap} ctx {ctx}")

@@ -1359,10 +1359,7 @@ extern "C" int q4_stream_destroy(q4_stream* r) {
 static bool attn_shape_ok(int capacity, int n_q, int n_kv, int hd) {
   if (capacity < 128 || capacity % 128 || capacity > 65536) return false;
   if (n_kv < 1 || n_q < n_kv || n_q % n_kv || n_q / n_kv > 16) return false;
-  if (hd < 64 || hd > 256 || hd % 64) return false;
-  // the combining CTA keeps every chunk's max and sum of its group's heads in its key buffer
-  const int chunk = q4::attn_chunk(capacity, n_kv), group = n_q / n_kv;
-  return static_cast<size_t>(2 * group) * (capacity / chunk) * 4 + 4 * group <= static_cast<size_t>(chunk) * hd * 2;
+  return hd >= 64 && hd <= 256 && hd % 64 == 0;
 }
 
 extern "C" size_t q4_attn_workspace_bytes(int n_q_heads, int n_kv_heads, int head_dim, int capacity) {

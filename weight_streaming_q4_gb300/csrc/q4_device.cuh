@@ -366,7 +366,10 @@ cudaError_t poison_launch(uint8_t* buf, size_t n_blocks, cudaStream_t stream);
 cudaError_t stamp_launch(unsigned long long* out, cudaStream_t stream);
 cudaError_t attn_prepare();
 size_t attn_workspace_bytes(int n_q, int n_kv, int hd, int capacity);
-int attn_chunk(int capacity, int n_kv);
+// The cluster attention kernel (q4_attn_cluster.cu): cluster size chosen at
+// prepare time (16 or 8 CTAs per value head).
+cudaError_t attn_cluster_prepare();
+int attn_cluster_size();
 // ctx_add: the positions in use are *ctx_len + ctx_add (the decoder passes its
 // position counter and 1).  With `app`, the kernel also stores the token's key
 // and value (fp32 app->k, app->v) as binary16 in row *app->pos of the caches
@@ -381,6 +384,9 @@ struct AttnAppend {
 cudaError_t attn_launch(const float* q, const uint16_t* k, const uint16_t* v, const int* ctx_len, int capacity,
                         int n_q, int n_kv, int hd, uint16_t* out, void* ws, cudaStream_t s, int ctx_add = 0,
                         const AttnAppend* app = nullptr);
+cudaError_t attn_cluster_launch(const float* q, const uint16_t* k, const uint16_t* v, const int* ctx_len, int ctx_add,
+                                int capacity, int n_q, int n_kv, int hd, uint16_t* out, const AttnAppend* app,
+                                cudaStream_t s);
 cudaError_t pos_advance_launch(int* pos, cudaStream_t s);
 // status (nullable): ST_KV_POS is or-ed in when *pos is outside 0..capacity-1.
 cudaError_t kv_append_launch(const float* k, const float* v, uint16_t* kc, uint16_t* vc, const int* pos, int capacity,
