@@ -645,7 +645,7 @@ def run_kv(args, torch, q4, model, synth, stream, barrier, gpu_index):
     ctx = contexts[-1]
     wbytes = layer_bytes * n_layers
     return dict(secs=head["secs"], clocks=head["clocks"], bytes_per_step=wbytes + head["kv_bytes_per_step"],
-                launches_per_step=4 * n_layers + 1, kernel_launches_per_step=2 * n_layers,
+                launches_per_step=2 * n_layers + 2, kernel_launches_per_step=n_layers + 1,
                 e2e_secs=e2e_secs, e2e_steps=e2e_steps, h2d=h0.numel() * 2, d2h=h0.numel() * 2,
                 workload=(f"8B-shaped decoder stack with per-layer binary16 KV caches, {n_layers} layers, batch 1, "
                           f"one token at position {ctx - 1} (context {ctx}, bucket {ctx}), HBM-resident, "
@@ -722,7 +722,7 @@ def run_attn(args, torch, q4, model, synth, stream, barrier, gpu_index):
                 e2e_secs=e2e_secs, e2e_steps=e2e_steps, h2d=q_host.numel() * 4, d2h=out.numel() * 2,
                 workload=(f"decode attention, 8B heads (32 q, 8 kv, head_dim 128), {L} layers' binary16 KV caches, "
                           f"context {cap} (bucket {cap}), one CUDA graph per bucket"),
-                kernel="attn_partial_kernel", kernel_key=None, cfg=dict(n_q=n_q, n_kv=n_kv, hd=hd),
+                kernel="attn_cluster_kernel", kernel_key=None, cfg=dict(n_q=n_q, n_kv=n_kv, hd=hd),
                 attn_buckets={str(b): {k: v for k, v in r.items() if k not in ("secs", "clocks")}
                               for b, r in per.items()})
 
@@ -1027,8 +1027,8 @@ def main():
         out["config"]["n_layers"] = r["n_layers"]
         out["config"]["weight_bytes_per_token"] = r["weight_bytes_per_step"]
         out["metric_note"] = "value counts the weight bytes and the KV-cache bytes read per token"
-        out["roofline"]["timing"] = ("step time / 2 engine launches per layer (attention, cache append and "
-                                     "position launches included)")
+        out["roofline"]["timing"] = ("step time / engine launches per step (one per layer and the first "
+                                     "q|k|v; attention and position launches included)")
     if "attn_buckets" in r:
         out["attn_buckets"] = r["attn_buckets"]
         out["metric_note"] = "value = GB/s of KV-cache bytes read (keys and values), not weight bytes"
