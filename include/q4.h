@@ -119,6 +119,23 @@ int q4_gemv_ex(const void *w, const uint16_t *x, float *y, int n, int k, int bat
 int q4_device_status(void);
 
 /*
+ * Tracing: the phase timeline of the tensor-core engine's last launches, in
+ * the timeline build of the library only (libq4_tl.so, compiled with
+ * Q4_TIMELINE; the Python module weight_streaming_q4_gb300.timeline builds,
+ * runs and summarises it).  For CTA c (< 256), program phase p (< 64) and event
+ * e (< 6), out[(c * 64 + p) * 6 + e] = the GPU's global timer (ns) when
+ *   e = 0 the CTA's consumers reached the phase, 1 passed their barrier,
+ *       2 had staged the phase's input, 3 handed their last unit to the
+ *       epilogue, 4 the epilogue stored the last unit, 5 the producer issued
+ *       the phase's last copy (0 = the event did not happen).
+ *   out, n   host, n >= 256 * 64 * 6 values
+ *   clear    nonzero: zero the timeline after the copy
+ * Synchronous.  Errors: Q4_ERR_ARG (n too small, or a build without the
+ * timeline), Q4_ERR_CUDA.
+ */
+int q4_timeline_read(unsigned long long *out, size_t n, int clear);
+
+/*
  * Debug: w_out[n][k] = (q - 8) * d as fp32 for every weight (exact: every
  * such value is a float).  Checks the block layout bit for bit.
  *   w      device, Q4_0 [n][k/32] blocks; w_out device, fp32 [n][k]

@@ -114,6 +114,7 @@ def _declare(lib):
         "q4_stream_status": ([c_p, c_p, ctypes.POINTER(c_int)], c_int),
         "q4_stream_tagged": ([c_p, ctypes.POINTER(c_int)], c_int),
         "q4_stream_timeline": ([c_p, c_p, c_int, c_p], c_int),
+        "q4_timeline_read": ([c_p, c_size, c_int], c_int),
         "q4_stream_destroy": ([c_p], c_int),
     }
     for name, (args, res) in sig.items():
@@ -131,6 +132,13 @@ def lib():
         if not os.path.exists(path):
             raise ImportError(f"libq4.so is not built ({path}); run weight_streaming_q4_gb300.build.build()")
         _lib = _declare(ctypes.CDLL(path))
+    return _lib
+
+
+def use_library(path: str):
+    """Bind every call to another build of the library (the timeline build)."""
+    global _lib
+    _lib = _declare(ctypes.CDLL(path))
     return _lib
 
 
@@ -334,6 +342,18 @@ def q4_stream_timeline(st, n_layers: int, stream=None):
     _check(lib().q4_stream_timeline(st, out.ctypes.data_as(ctypes.c_void_p), out.size, _stream(stream)),
            "q4_stream_timeline")
     return out.reshape(n_layers, 4)
+
+
+TIMELINE_CTAS, TIMELINE_PHASES, TIMELINE_EVENTS = 256, 64, 6
+
+
+def q4_timeline_read(clear: bool = True):
+    """[CTA][phase][event] globaltimer ns of the engine's last launches (timeline build only)."""
+    import numpy as np
+    out = np.zeros(TIMELINE_CTAS * TIMELINE_PHASES * TIMELINE_EVENTS, dtype=np.uint64)
+    _check(lib().q4_timeline_read(out.ctypes.data_as(ctypes.c_void_p), out.size, 1 if clear else 0),
+           "q4_timeline_read")
+    return out.reshape(TIMELINE_CTAS, TIMELINE_PHASES, TIMELINE_EVENTS)
 
 
 def q4_stream_tagged(st) -> bool:

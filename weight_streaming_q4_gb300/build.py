@@ -81,3 +81,27 @@ def build(force: bool = False, verbose: bool = False) -> dict:
 if __name__ == "__main__":
     for k, v in build(verbose=True).items():
         print(k, v)
+
+
+def build_timeline(force: bool = False) -> str:
+    """The timeline build of libq4.so (libq4_tl.so: the engine stamps the GPU's
+    global timer at every phase, read with q4_timeline_read)."""
+    out_dir = os.path.join(OUT, "timeline")
+    os.makedirs(out_dir, exist_ok=True)
+    nvcc = _nvcc()
+    headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
+    headers.append(os.path.join(INCLUDE, "q4.h"))
+    jobs, objs = [], []
+    for s in LIBS["libq4.so"]:
+        src = os.path.join(CSRC, s)
+        obj = os.path.join(out_dir, s.replace(".cu", ".o"))
+        objs.append(obj)
+        if force or _stale(obj, [src, *headers]):
+            jobs.append([nvcc, *NVCC_FLAGS, "-DQ4_TIMELINE", "-c", src, "-o", obj])
+    with ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 4))) as ex:
+        list(ex.map(_run, jobs))
+    target = os.path.join(out_dir, "libq4_tl.so")
+    if force or _stale(target, objs):
+        _run([nvcc, *ARCH, "-shared", "-Xcompiler", "-fPIC", *objs, "-o", target + ".tmp"])
+        os.replace(target + ".tmp", target)
+    return target

@@ -301,6 +301,14 @@ extern "C" int q4_gemv(const void* w, const uint16_t* x, float* y, int n, int k,
   return q4_gemv_ex(w, x, y, n, k, batch, Q4_KERNEL_AUTO, stream);
 }
 
+extern "C" int q4_timeline_read(unsigned long long* out, size_t n, int clear) {
+  if (!out) return Q4_ERR_ARG;
+  const cudaError_t e = q4::tc_timeline_read(out, n, clear != 0);
+  if (e == cudaErrorNotSupported || e == cudaErrorInvalidValue) return Q4_ERR_ARG;
+  Q4_CUDA(e);
+  return Q4_OK;
+}
+
 extern "C" int q4_device_status(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return cuda_fail(cudaGetLastError());
   int v = 0, m = 0;

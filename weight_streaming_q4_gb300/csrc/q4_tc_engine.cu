@@ -60,6 +60,25 @@ namespace q4 {
 
 __device__ int g_status_tc;   // status bits of launches without a control block
 
+// Timeline build (-DQ4_TIMELINE, libq4_tl.so): the GPU's global timer at six
+// points of every phase of every CTA, indexed by the phase's place in the
+// program: 0 consumers reach the phase, 1 after their barrier, 2 input staged,
+// 3 last unit handed to the epilogue, 4 last unit stored by the epilogue,
+// 5 last stage issued by the producer.  Other builds compile the stamps away.
+constexpr int kTlCtas = 256, kTlPhases = 64, kTlEvents = 6;
+#ifdef Q4_TIMELINE
+__device__ unsigned long long g_tc_tl[kTlCtas * kTlPhases * kTlEvents];
+__device__ __forceinline__ void tc_stamp(int phase, int event) {
+  if (phase < kTlPhases) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    g_tc_tl[(blockIdx.x * kTlPhases + phase) * kTlEvents + event] = t;
+  }
+}
+#else
+__device__ __forceinline__ void tc_stamp(int, int) {}
+#endif
+
 constexpr int kTcWarps = 8;                       // consumer warps (two per SM sub-partition)
 constexpr int kTcConsumers = kTcWarps * 32;
 constexpr int kTcPairsPerWarp = 32 / kTcWarps;    // block pairs of a 64-block chunk per warp
@@ -460,6 +479,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_engine_kernel(const __grid_c
               tma_load_2d(dst, &ph.tm0, c * cx, unit_row0(ph, u, kTcUnitRows), &full_bar[slot]);
             }
             ++it;
+            tc_stamp(ph.gidx, 5);
             if (++slot == S) {
               slot = 0;
               ++use;
@@ -505,6 +525,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_engine_kernel(const __grid_c
           ++ruse;
         }
         if (row_ok) tc_epilogue_row(ph, n, v, u2, res_w, tagged, tag, lim, a.ctl);
+        if (lane == 0) tc_stamp(ph.gidx, 4);
       }
     }
   } else {
@@ -524,8 +545,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_engine_kernel(const __grid_c
       const int u0 = first_unit(ph, cta, G);
       const bool cta0 = cta == 0 && (ph.x_dbg || ph.xr_out);
       // every consumer warp is done with the previous phase's input
+      if (tid == 0) tc_stamp(ph.gidx, 0);
       named_bar_sync(1, kTcConsumers);
+      if (tid == 0) tc_stamp(ph.gidx, 1);
       if (u0 < ph.units || cta0) tc_prologue(ph, tag, lim, a.ctl, a.flags, xf, red_cta, tid, cta0);
+      if (tid == 0) tc_stamp(ph.gidx, 2);
       if (ph.sync == SYNC_PUBLISH && tid == 0) st_release_u64(a.flags + cta, static_cast<unsigned long long>(tag) << 32);
       asm volatile("" ::: "memory");
       const int chunks = tc_chunks(ph.k);
@@ -563,6 +587,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_engine_kernel(const __grid_c
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&rfull_bar[rs]);
+        if (tid == 0) tc_stamp(ph.gidx, 3);
         if (++rs == kTcRedSlots) {
           rs = 0;
           ++ruse;
@@ -582,6 +607,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_engine_kernel(const __grid_c
       if (a.end_of_program) atomicAdd(&a.ctl->epoch, 1u);
     }
   }
+}
+
+// Copy the timeline of the last launches out (and clear it): Q4_ERR_ARG-like
+// cudaErrorNotSupported in a build without stamps.
+cudaError_t tc_timeline_read(unsigned long long* out, size_t n, bool clear) {
+#ifdef Q4_TIMELINE
+  const size_t total = static_cast<size_t>(kTlCtas) * kTlPhases * kTlEvents;
+  if (n < total) return cudaErrorInvalidValue;
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_tc_tl, total * sizeof(unsigned long long));
+  if (e == cudaSuccess && clear) {
+    static unsigned long long zero[kTlCtas * kTlPhases * kTlEvents];
+    e = cudaMemcpyToSymbol(g_tc_tl, zero, sizeof(zero));
+  }
+  return e;
+#else
+  (void)out;
+  (void)n;
+  (void)clear;
+  return cudaErrorNotSupported;
+#endif
 }
 
 cudaError_t tc_engine_prepare() {
