@@ -65,8 +65,8 @@ __device__ int g_status_tc;   // status bits of launches without a control block
 // program: 0 consumers reach the phase, 1 after their barrier, 2 input staged,
 // 3 last unit handed to the epilogue, 4 last unit stored by the epilogue,
 // 5 last stage issued by the producer.  Other builds compile the stamps away.
-constexpr int kTlCtas = 256, kTlPhases = 64, kTlEvents = 6;
 #ifdef Q4_TIMELINE
+constexpr int kTlCtas = 256, kTlPhases = 64, kTlEvents = 6;
 __device__ unsigned long long g_tc_tl[kTlCtas * kTlPhases * kTlEvents];
 __device__ __forceinline__ void tc_stamp(int phase, int event) {
   if (phase < kTlPhases) {
