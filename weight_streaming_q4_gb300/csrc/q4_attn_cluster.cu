@@ -6,22 +6,26 @@
 // ("Layer 1: CUDA Graph Compilation": buckets of 512, 1024, 2048 and 4096
 // positions), and PIPO moves each layer's KV cache with the layer ("PIPO:
 // Pipelined Offloading for Efficient Inference on Consumer Devices", Method,
-// "Offloading architecture").  The work reads every cached key and value once,
-// so it is bound by HBM bandwidth: CUDA cores, no tensor cores.
+// "Offloading architecture").  The work reads every cached key and value once
+// and should be bound by HBM bandwidth; on CUDA cores its score and value
+// steps were long dependent chains (latency-bound), hence the tensor cores.
 //
 // Value head g is one cluster of C CTAs (16 where the GPU schedules clusters
 // that large, else 8); CTA r takes positions [r * span, (r + 1) * span) of the
 // context, span = capacity / C.  A CTA copies its keys and values into shared
 // memory with 16-byte asynchronous copies, a round of 64 KB (128 positions at
-// head_dim 128) at a time with every copy of the round in flight at once, and
-// keeps a running softmax state per query head of the
-// group: the maximum m, l = sum exp(s - m) and o = sum exp(s - m) v, rescaled
-// when a later round raises m.  Scores use q pre-scaled by 1/sqrt(head_dim).
-// The C states of a head then meet through distributed shared memory: each
-// CTA of the cluster finishes a slice of the group's outputs, reading every
-// CTA's m, l and o, M = max m_r, L = sum l_r exp(m_r - M),
-// out = f16(sum o_r exp(m_r - M) / L), ranks in order.  Nothing goes through
-// global memory between the CTAs and every sum runs in a fixed order.
+// head_dim 128) at a time with every copy of the round in flight, and keeps a
+// running softmax state per query head of the group: the maximum m,
+// l = sum exp(s - m) and o = sum exp(s - m) v, rescaled when a later round
+// raises m.  The scores q . k / sqrt(head_dim) and the products of the weights
+// with the values run on the tensor cores, with the fp32 query and the fp32
+// weights each split into two binary16 parts (about 22 bits kept; keys and
+// values are binary16 already), fp32 accumulation.  The C states of a head
+// then meet through distributed shared memory: each CTA of the cluster
+// finishes a slice of the group's outputs, reading every CTA's m, l and o,
+// M = max m_r, L = sum l_r exp(m_r - M), out = f16(sum o_r exp(m_r - M) / L),
+// ranks in order.  Nothing goes through global memory between the CTAs and
+// every sum runs in a fixed order.
 //
 // The number of positions in use is read from device memory, so one captured
 // graph serves every length up to its bucket's capacity.  With the append
@@ -69,57 +73,81 @@ __device__ __forceinline__ void ac_cp16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
 
-// Block-wide max (or sum) of v[0..group) for every head at once: one
-// shuffle tree per head, one shared-memory exchange, warps in order.
-template <bool kMax, int GMAX>
-__device__ __forceinline__ void ac_reduce(float* v, int group, float* red) {
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-#pragma unroll
-  for (int j = 0; j < GMAX; ++j) {
-    if (j < group) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float x = __shfl_xor_sync(0xffffffffu, v[j], o);
-        v[j] = kMax ? fmaxf(v[j], x) : v[j] + x;
-      }
-      if (lane == 0) red[j * kAcWarps + w] = v[j];
-    }
-  }
-  __syncthreads();
-#pragma unroll
-  for (int j = 0; j < GMAX; ++j) {
-    if (j < group) {
-      float r = red[j * kAcWarps];
-#pragma unroll
-      for (int i = 1; i < kAcWarps; ++i) r = kMax ? fmaxf(r, red[j * kAcWarps + i]) : r + red[j * kAcWarps + i];
-      v[j] = r;
-    }
-  }
-  __syncthreads();
+// ldmatrix: 8x8 binary16 matrices from shared memory, one row address per
+// lane (lanes 8i..8i+7: the rows of matrix i); .trans delivers each matrix
+// transposed.
+__device__ __forceinline__ void ldsm_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3, const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t& r0, uint32_t& r1, const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3, const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x2_t(uint32_t& r0, uint32_t& r1, const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];"
+               : "=r"(r0), "=r"(r1)
+               : "r"(smem_u32(p)));
+}
+// d += a * b, binary16 in, fp32 accumulate (m16n8k16).
+__device__ __forceinline__ void ac_mma(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                       uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// A value split into two binary16 parts (hi = f16(v), lo = f16(v - hi)), so
+// that a pair of binary16 products carries about 22 bits of v.
+__device__ __forceinline__ void split_half(float v, __half& hi, __half& lo) {
+  hi = __float2half_rn(v);
+  lo = __float2half_rn(v - __half2float(hi));
 }
 
 }  // namespace
 
-// One CTA per (rank r of the cluster, value head g), 256 threads.  GMAX (a
-// power of two >= group) bounds the unrolled loops over the group's heads.
-template <int GMAX>
-__global__ void __launch_bounds__(kAcThreads) attn_cluster_kernel(const __grid_constant__ AcArgs a) {
+// One CTA per (rank r of the cluster, value head g), 256 threads, the score
+// and value steps on the tensor cores (mma.sync m16n8k16, binary16 in, fp32
+// accumulate).  Scores:
+// A = a tile of 16 positions x 16 dimensions of keys (ldmatrix from the
+// swizzled key rows), B = q as two binary16 parts (hi + lo, about 22 bits of
+// the fp32 query), heads in the n dimension (NTS tiles of 8 heads).  Values:
+// A = the weights exp(s - m) as two binary16 parts, heads x positions, B = a
+// tile of values (ldmatrix.trans from the swizzled value rows), warp w taking
+// NTV tiles of 8 dimensions; the running output stays in the accumulator
+// registers and is rescaled when a round raises m.  Softmax maxima and sums
+// per head by shuffles and one shared-memory exchange; positions past the
+// context get weight 0 (their value rows in the last tile are zeroed while
+// the round's copies are in flight, so no stale bits can make a NaN).  The
+// first round's copies are issued before q is staged, so q's load overlaps
+// them.
+template <int NTS, int NTV>
+__global__ void __launch_bounds__(kAcThreads) attn_mma_kernel(const __grid_constant__ AcArgs a) {
   extern __shared__ __align__(16) unsigned char sm[];
-  __shared__ float red[kAcMaxGroup * kAcWarps];
-  __shared__ float st_m[kAcMaxGroup], st_l[kAcMaxGroup], st_c[kAcMaxGroup];
+  __shared__ float wred[kAcWarps][kAcMaxGroup];
+  __shared__ float hm[kAcMaxGroup], hl[kAcMaxGroup], hc[kAcMaxGroup];
   cg::cluster_group cluster = cg::this_cluster();
   const int C = static_cast<int>(cluster.num_blocks());
   const int r = static_cast<int>(cluster.block_rank());
-  const int g = blockIdx.y, tid = threadIdx.x;
+  const int g = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gq = lane >> 2, tq = lane & 3;
   const int group = a.n_q / a.n_kv, hd = a.hd, kv_dim = a.n_kv * hd, R = a.round;
-  const int cpr = hd / 8;   // 16-byte chunks per row
-  // shared memory: keys [R][hd] (16-byte chunks swizzled by position), values
-  // [R][hd], q [group][hd], weights [group][R], this CTA's o [group][hd]
+  const int cpr = hd / 8;          // 16-byte chunks per row
+  const int QS = hd + 8, PS = R + 8;   // padded rows of q and of the weights (conflict-free ldmatrix)
+  // shared memory: keys, values [R][hd] (16-byte chunks swizzled by position),
+  // q hi/lo [16][QS], weights hi/lo [16][PS], this CTA's o [group][hd]
   __half* ks = reinterpret_cast<__half*>(sm);
   __half* vs = ks + R * hd;
-  float* qs = reinterpret_cast<float*>(vs + R * hd);
-  float* ps = qs + group * hd;
-  float* osm = ps + group * R;
+  __half* qh = vs + R * hd;
+  __half* ql = qh + 16 * QS;
+  __half* ph = ql + 16 * QS;
+  __half* pl = ph + 16 * PS;
+  float* osm = reinterpret_cast<float*>(pl + 16 * PS);
 
   int ctx = *a.ctx_len + a.ctx_add;
   ctx = ctx < 1 ? 1 : (ctx > a.capacity ? a.capacity : ctx);
@@ -134,24 +162,18 @@ __global__ void __launch_bounds__(kAcThreads) attn_cluster_kernel(const __grid_c
       own = p;
     }
   }
-  for (int i = tid; i < group * hd; i += kAcThreads) qs[i] = a.q[static_cast<size_t>(g * group) * hd + i] * a.scale;
-
-  // running softmax state: per head m, l (all threads hold the same values);
-  // o [group][hd] in shared memory (osm)
-  const int pairs = hd / 2;
-  const int Q = kAcThreads / pairs;   // position subsets of the value pass
-  float m_run[GMAX], l_run[GMAX];
-#pragma unroll
-  for (int j = 0; j < GMAX; ++j) {
-    m_run[j] = -INFINITY;
-    l_run[j] = 0.f;
+  if (tid < kAcMaxGroup) {
+    hm[tid] = -INFINITY;
+    hl[tid] = 0.f;
   }
-  for (int i = tid; i < group * hd; i += kAcThreads) osm[i] = 0.f;
+  float oacc[NTV][4];
+#pragma unroll
+  for (int nt = 0; nt < NTV; ++nt) oacc[nt][0] = oacc[nt][1] = oacc[nt][2] = oacc[nt][3] = 0.f;
+  const int d0 = warp * 8 * NTV;   // this warp's first value dimension
 
-  const int tp = kAcThreads / R;   // threads per position (1, 2 or 4)
-  const int t = tid / tp, sub = tid % tp;
   for (int r0 = lo; r0 < hi; r0 += R) {
     const int np = hi - r0 < R ? hi - r0 : R;
+    const int ntiles = (np + 15) >> 4;
     // keys, then values, all copies of the round in flight
     for (int i = tid; i < np * cpr; i += kAcThreads) {
       const int tt = i / cpr, cc = i % cpr;
@@ -173,7 +195,7 @@ __global__ void __launch_bounds__(kAcThreads) attn_cluster_kernel(const __grid_c
     for (int i = tid; i < np * cpr; i += kAcThreads) {
       const int tt = i / cpr, cc = i % cpr;
       const size_t src = static_cast<size_t>(r0 + tt) * kv_dim + static_cast<size_t>(g) * hd + cc * 8;
-      __half* dst = vs + tt * hd + cc * 8;
+      __half* dst = vs + tt * hd + ((cc ^ (tt & 7)) * 8);
       if (r0 + tt == own) {
         const float* f = a.new_v + static_cast<size_t>(g) * hd + cc * 8;
         uint4 h;
@@ -187,127 +209,186 @@ __global__ void __launch_bounds__(kAcThreads) attn_cluster_kernel(const __grid_c
       }
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
+    // while the copies fly: value rows of the last tile past the context hold
+    // 0 (never stale bits that could be NaN), and on the first round q and the
+    // weights' rows of heads past the group are zeroed and q staged
+    for (int i = tid; i < (ntiles * 16 - np) * cpr; i += kAcThreads)
+      reinterpret_cast<uint4*>(vs + (np + i / cpr) * hd)[i % cpr] = make_uint4(0u, 0u, 0u, 0u);
+    if (r0 == lo) {
+      uint4* z = reinterpret_cast<uint4*>(qh);
+      for (int i = tid; i < (2 * 16 * QS + 2 * 16 * PS) / 8; i += kAcThreads) z[i] = make_uint4(0u, 0u, 0u, 0u);
+      __syncthreads();
+      for (int i = tid; i < group * hd; i += kAcThreads) {
+        const int j = i / hd, d = i % hd;
+        __half h, l;
+        split_half(a.q[static_cast<size_t>(g * group) * hd + i] * a.scale, h, l);
+        qh[j * QS + d] = h;
+        ql[j * QS + d] = l;
+      }
+    }
     asm volatile("cp.async.wait_group 1;" ::: "memory");   // the keys
     __syncthreads();
 
-    // scores of position t over dims [sub * hd / tp, (sub + 1) * hd / tp)
-    float s[GMAX];
+    // scores of the warp's position tiles (tile = 16 positions): sc[slot][nt]
+    // = rows: positions tile*16 + gq (+8), columns: heads nt*8 + 2tq (+1)
+    float sc[2][NTS][4];
 #pragma unroll
-    for (int j = 0; j < GMAX; ++j) s[j] = 0.f;
-    if (t < np) {
-      const int c_lo = sub * (cpr / tp), c_hi = c_lo + cpr / tp;
-#pragma unroll 2
-      for (int cc = c_lo; cc < c_hi; ++cc) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(ks + t * hd + ((cc ^ (t & 7)) * 8));
-        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-        float kf[8];
+    for (int ti = 0; ti < 2; ++ti) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
-          kf[2 * e] = f.x;
-          kf[2 * e + 1] = f.y;
-        }
+      for (int nt = 0; nt < NTS; ++nt) sc[ti][nt][0] = sc[ti][nt][1] = sc[ti][nt][2] = sc[ti][nt][3] = 0.f;
+      const int tl = warp + 8 * ti;
+      if (tl < ntiles) {
+        const int mi = lane >> 3;
+        const int krow = tl * 16 + (lane & 7) + (mi & 1) * 8;
+        for (int kk = 0; kk < hd / 16; ++kk) {
+          uint32_t a0, a1, a2, a3;
+          const int chunk = 2 * kk + (mi >> 1);
+          ldsm_x4(a0, a1, a2, a3, ks + krow * hd + ((chunk ^ (krow & 7)) * 8));
 #pragma unroll
-        for (int j = 0; j < GMAX; ++j) {
-          if (j < group) {
-            const float4 qa = *reinterpret_cast<const float4*>(qs + j * hd + cc * 8);
-            const float4 qb = *reinterpret_cast<const float4*>(qs + j * hd + cc * 8 + 4);
-            s[j] = fmaf(qa.x, kf[0], s[j]);
-            s[j] = fmaf(qa.y, kf[1], s[j]);
-            s[j] = fmaf(qa.z, kf[2], s[j]);
-            s[j] = fmaf(qa.w, kf[3], s[j]);
-            s[j] = fmaf(qb.x, kf[4], s[j]);
-            s[j] = fmaf(qb.y, kf[5], s[j]);
-            s[j] = fmaf(qb.z, kf[6], s[j]);
-            s[j] = fmaf(qb.w, kf[7], s[j]);
+          for (int nt = 0; nt < NTS; ++nt) {
+            const int qoff = (nt * 8 + (lane & 7)) * QS + 16 * kk + (mi & 1) * 8;
+            uint32_t b0, b1, c0, c1;
+            ldsm_x2(b0, b1, qh + qoff);
+            ldsm_x2(c0, c1, ql + qoff);
+            ac_mma(sc[ti][nt], a0, a1, a2, a3, b0, b1);
+            ac_mma(sc[ti][nt], a0, a1, a2, a3, c0, c1);
           }
         }
       }
     }
-    // the tp slices of a position are adjacent lanes
-    for (int o = tp >> 1; o > 0; o >>= 1) {
+    // the round's maximum per head: the lane's positions, the warp (shuffles
+    // over gq), then the warps in order
+    float mx[NTS][2];
 #pragma unroll
-      for (int j = 0; j < GMAX; ++j) s[j] += __shfl_xor_sync(0xffffffffu, s[j], o);
+    for (int nt = 0; nt < NTS; ++nt) {
+      mx[nt][0] = mx[nt][1] = -INFINITY;
+#pragma unroll
+      for (int ti = 0; ti < 2; ++ti) {
+        const int p0 = (warp + 8 * ti) * 16 + gq;
+        if (p0 < np) {
+          mx[nt][0] = fmaxf(mx[nt][0], sc[ti][nt][0]);
+          mx[nt][1] = fmaxf(mx[nt][1], sc[ti][nt][1]);
+        }
+        if (p0 + 8 < np) {
+          mx[nt][0] = fmaxf(mx[nt][0], sc[ti][nt][2]);
+          mx[nt][1] = fmaxf(mx[nt][1], sc[ti][nt][3]);
+        }
+      }
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        mx[nt][0] = fmaxf(mx[nt][0], __shfl_xor_sync(0xffffffffu, mx[nt][0], o));
+        mx[nt][1] = fmaxf(mx[nt][1], __shfl_xor_sync(0xffffffffu, mx[nt][1], o));
+      }
+      if (gq == 0) {
+        wred[warp][nt * 8 + 2 * tq] = mx[nt][0];
+        wred[warp][nt * 8 + 2 * tq + 1] = mx[nt][1];
+      }
     }
-    // the round's maximum, the new running maximum, the rescale of the old state
-    float m_new[GMAX], corr[GMAX], l_r[GMAX];
-#pragma unroll
-    for (int j = 0; j < GMAX; ++j) m_new[j] = t < np ? s[j] : -INFINITY;
-    ac_reduce<true, GMAX>(m_new, group, red);
-#pragma unroll
-    for (int j = 0; j < GMAX; ++j) {
-      m_new[j] = fmaxf(m_new[j], m_run[j]);
-      corr[j] = expf(m_run[j] - m_new[j]);   // 0 on the first round (m_run = -inf)
-      const float p = (t < np && sub == 0) ? expf(s[j] - m_new[j]) : 0.f;
-      if (j < group && sub == 0 && t < R) ps[j * R + t] = p;
-      l_r[j] = p;
+    __syncthreads();
+    if (tid < group) {
+      float bm = wred[0][tid];
+      for (int w = 1; w < kAcWarps; ++w) bm = fmaxf(bm, wred[w][tid]);
+      const float m_new = fmaxf(hm[tid], bm);
+      hc[tid] = expf(hm[tid] - m_new);   // 0 on the first round (m = -inf)
+      hm[tid] = m_new;
     }
-    ac_reduce<false, GMAX>(l_r, group, red);   // its barriers also publish ps
+    __syncthreads();
+    // weights exp(s - m) of the group's heads (0 past the context), as binary16
+    // hi + lo, and their sums per head
+    float sm_[NTS][2];
 #pragma unroll
-    for (int j = 0; j < GMAX; ++j) {
-      l_run[j] = fmaf(l_run[j], corr[j], l_r[j]);
-      m_run[j] = m_new[j];
+    for (int nt = 0; nt < NTS; ++nt) {
+      const int h0 = nt * 8 + 2 * tq;
+      const float m0 = h0 < group ? hm[h0] : 0.f, m1 = h0 + 1 < group ? hm[h0 + 1] : 0.f;
+      sm_[nt][0] = sm_[nt][1] = 0.f;
+#pragma unroll
+      for (int ti = 0; ti < 2; ++ti) {
+        const int tl = warp + 8 * ti;
+        if (tl < ntiles) {
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int pos = tl * 16 + gq + 8 * hh;
+            const float p0 = (pos < np && h0 < group) ? expf(sc[ti][nt][2 * hh] - m0) : 0.f;
+            const float p1 = (pos < np && h0 + 1 < group) ? expf(sc[ti][nt][2 * hh + 1] - m1) : 0.f;
+            sm_[nt][0] += p0;
+            sm_[nt][1] += p1;
+            if (h0 < group) split_half(p0, ph[h0 * PS + pos], pl[h0 * PS + pos]);
+            if (h0 + 1 < group) split_half(p1, ph[(h0 + 1) * PS + pos], pl[(h0 + 1) * PS + pos]);
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        sm_[nt][0] += __shfl_xor_sync(0xffffffffu, sm_[nt][0], o);
+        sm_[nt][1] += __shfl_xor_sync(0xffffffffu, sm_[nt][1], o);
+      }
+    }
+    __syncthreads();   // every warp has read the maxima's exchange buffer
+#pragma unroll
+    for (int nt = 0; nt < NTS; ++nt) {
+      if (gq == 0) {
+        wred[warp][nt * 8 + 2 * tq] = sm_[nt][0];
+        wred[warp][nt * 8 + 2 * tq + 1] = sm_[nt][1];
+      }
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");   // the values
     __syncthreads();
-    // weighted values: thread (element pair e2, position subset qq) sums
-    // positions qq, qq + Q, ... for every head of the group (each value pair
-    // is loaded once), into the key buffer (free now) as part[qq][j][hd]
-    float* part = reinterpret_cast<float*>(ks);
     if (tid < group) {
-      float cj = corr[0];
-#pragma unroll
-      for (int jj = 1; jj < GMAX; ++jj)
-        if (jj == tid) cj = corr[jj];
-      st_c[tid] = cj;
+      float ls = wred[0][tid];
+      for (int w = 1; w < kAcWarps; ++w) ls += wred[w][tid];
+      hl[tid] = fmaf(hl[tid], hc[tid], ls);
     }
+    // weighted values: oacc = oacc * corr + P V over the round's positions
     {
-      const int e2 = tid % pairs, qq = tid / pairs;
-      if (qq < Q) {
-        float a0[GMAX], a1[GMAX];
+      const float c0 = gq < group ? hc[gq] : 0.f, c1 = gq + 8 < group ? hc[gq + 8] : 0.f;
 #pragma unroll
-        for (int jj = 0; jj < GMAX; ++jj) a0[jj] = a1[jj] = 0.f;
-        const __half* vp = vs + 2 * e2;
-#pragma unroll 4
-        for (int tt = qq; tt < np; tt += Q) {
-          const float2 v2 = __half22float2(*reinterpret_cast<const __half2*>(vp + tt * hd));
+      for (int nt = 0; nt < NTV; ++nt) {
+        oacc[nt][0] *= c0;
+        oacc[nt][1] *= c0;
+        oacc[nt][2] *= c1;
+        oacc[nt][3] *= c1;
+      }
+      const int mi = lane >> 3;
+      for (int kk = 0; kk < ntiles; ++kk) {
+        uint32_t a0, a1, a2, a3, e0, e1, e2, e3;
+        const int poff = ((lane & 7) + (mi & 1) * 8) * PS + 16 * kk + (mi >> 1) * 8;
+        ldsm_x4(a0, a1, a2, a3, ph + poff);
+        ldsm_x4(e0, e1, e2, e3, pl + poff);
+        const int vrow = 16 * kk + (lane & 7) + (mi & 1) * 8;
 #pragma unroll
-          for (int jj = 0; jj < GMAX; ++jj) {
-            if (jj < group) {
-              const float p = ps[jj * R + tt];
-              a0[jj] = fmaf(p, v2.x, a0[jj]);
-              a1[jj] = fmaf(p, v2.y, a1[jj]);
-            }
-          }
+        for (int nt = 0; nt + 1 < NTV; nt += 2) {
+          const int chunk = ((d0 + nt * 8) >> 3) + (mi >> 1);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(b0, b1, b2, b3, vs + vrow * hd + ((chunk ^ (vrow & 7)) * 8));
+          ac_mma(oacc[nt], a0, a1, a2, a3, b0, b1);
+          ac_mma(oacc[nt], e0, e1, e2, e3, b0, b1);
+          ac_mma(oacc[nt + 1], a0, a1, a2, a3, b2, b3);
+          ac_mma(oacc[nt + 1], e0, e1, e2, e3, b2, b3);
         }
-#pragma unroll
-        for (int jj = 0; jj < GMAX; ++jj) {
-          if (jj < group)
-            *reinterpret_cast<float2*>(part + (qq * group + jj) * hd + 2 * e2) = make_float2(a0[jj], a1[jj]);
+        if (NTV & 1) {
+          const int chunk = (d0 + (NTV - 1) * 8) >> 3;
+          uint32_t b0, b1;
+          ldsm_x2_t(b0, b1, vs + vrow * hd + ((chunk ^ (vrow & 7)) * 8));
+          ac_mma(oacc[NTV - 1], a0, a1, a2, a3, b0, b1);
+          ac_mma(oacc[NTV - 1], e0, e1, e2, e3, b0, b1);
         }
       }
-    }
-    __syncthreads();
-    // the subsets in order, then the running state: o = o * corr + round
-    for (int it = tid; it < group * hd; it += kAcThreads) {
-      float sum = part[it];
-      for (int qq = 1; qq < Q; ++qq) sum += part[qq * group * hd + it];
-      osm[it] = fmaf(osm[it], st_c[it / hd], sum);
     }
     __syncthreads();   // the round's buffers are free for the next one
   }
 
-  // this CTA's m and l into its shared memory (o is there already), for the cluster
-  if (tid < group) {
-    float mj = m_run[0], lj = l_run[0];
+  // this CTA's state for the cluster: m and l (hm, hl) and o [group][hd]
 #pragma unroll
-    for (int j = 1; j < GMAX; ++j)
-      if (j == tid) {
-        mj = m_run[j];
-        lj = l_run[j];
-      }
-    st_m[tid] = mj;
-    st_l[tid] = lj;
+  for (int nt = 0; nt < NTV; ++nt) {
+    const int d = d0 + nt * 8 + 2 * tq;
+    if (gq < group) {
+      osm[gq * hd + d] = oacc[nt][0];
+      osm[gq * hd + d + 1] = oacc[nt][1];
+    }
+    if (gq + 8 < group) {
+      osm[(gq + 8) * hd + d] = oacc[nt][2];
+      osm[(gq + 8) * hd + d + 1] = oacc[nt][3];
+    }
   }
   cluster.sync();
   // (1) every rank's m and l of the group's heads, loaded together;
@@ -321,8 +402,8 @@ __global__ void __launch_bounds__(kAcThreads) attn_cluster_kernel(const __grid_c
   float* ro = rL + kAcMaxGroup;                // [per][C] o
   if (tid < C * group) {
     const int rr = tid / group, j = tid % group;
-    rm[tid] = *cluster.map_shared_rank(st_m + j, rr);
-    rl[tid] = *cluster.map_shared_rank(st_l + j, rr);
+    rm[tid] = *cluster.map_shared_rank(hm + j, rr);
+    rl[tid] = *cluster.map_shared_rank(hl + j, rr);
   }
   const int total = group * hd, per = (total + C - 1) / C;
   const int i0 = r * per, n_out = i0 + per < total ? per : (total > i0 ? total - i0 : 0);
@@ -356,36 +437,46 @@ namespace {
 
 int g_ac_cluster = 0;   // cluster size chosen by attn_cluster_prepare: 16 or 8
 
-template <int GMAX>
-cudaError_t ac_set_attrs(bool nonportable) {
-  cudaError_t e = cudaFuncSetAttribute(attn_cluster_kernel<GMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+template <int NTS, int NTV>
+cudaError_t ac_set_attr(bool nonportable) {
+  cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel<NTS, NTV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kAcSmemMax));
   if (e == cudaSuccess && nonportable)
-    e = cudaFuncSetAttribute(attn_cluster_kernel<GMAX>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = cudaFuncSetAttribute(attn_mma_kernel<NTS, NTV>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return e;
+}
+
+cudaError_t ac_set_attrs(bool nonportable) {
+  cudaError_t e = ac_set_attr<1, 1>(nonportable);
+  if (e == cudaSuccess) e = ac_set_attr<1, 2>(nonportable);
+  if (e == cudaSuccess) e = ac_set_attr<1, 3>(nonportable);
+  if (e == cudaSuccess) e = ac_set_attr<1, 4>(nonportable);
+  if (e == cudaSuccess) e = ac_set_attr<2, 1>(nonportable);
+  if (e == cudaSuccess) e = ac_set_attr<2, 2>(nonportable);
+  if (e == cudaSuccess) e = ac_set_attr<2, 3>(nonportable);
+  if (e == cudaSuccess) e = ac_set_attr<2, 4>(nonportable);
   return e;
 }
 
 }  // namespace
 
 // Positions per round: 64 KB of keys and values (256 positions at head_dim
-// 64, 128 at 128, 64 above), so that a cluster's CTAs use about 70 KB of
-// shared memory at the common shapes and every value head's cluster is
-// resident at once (at 139 KB per CTA a GB300 holds only 7 clusters of 16).
+// 64, 128 at 128, 64 above), so that a cluster's CTAs use under 105 KB of
+// shared memory, two fit on an SM, and every value head's cluster is resident
+// at once (at 139 KB per CTA a GB300 holds only 7 clusters of 16).
 int attn_cluster_round(int hd) { return hd <= 64 ? 256 : hd <= 128 ? 128 : 64; }
 
 size_t attn_cluster_smem(int group, int hd) {
   const int R = attn_cluster_round(hd);
-  return static_cast<size_t>(2) * R * hd * sizeof(__half) + static_cast<size_t>(group) * hd * 4 * 2 +
-         static_cast<size_t>(group) * R * 4;
+  return static_cast<size_t>(2) * R * hd * 2 + static_cast<size_t>(2) * 16 * (hd + 8) * 2 +
+         static_cast<size_t>(2) * 16 * (R + 8) * 2 + static_cast<size_t>(group) * hd * 4;
 }
 
 // Cluster size: 16 when one such cluster with the largest shared memory fits
 // on the GPU, else the portable 8.
 cudaError_t attn_cluster_prepare() {
   cudaError_t e = cudaSuccess;
-  bool big = ac_set_attrs<1>(true) == cudaSuccess && ac_set_attrs<2>(true) == cudaSuccess &&
-             ac_set_attrs<4>(true) == cudaSuccess && ac_set_attrs<8>(true) == cudaSuccess &&
-             ac_set_attrs<16>(true) == cudaSuccess;
+  bool big = ac_set_attrs(true) == cudaSuccess;
   cudaGetLastError();   // a refused attribute is not an error of the library
   if (big) {
     cudaLaunchConfig_t cfg = {};
@@ -400,16 +491,10 @@ cudaError_t attn_cluster_prepare() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    big = cudaOccupancyMaxActiveClusters(&n, attn_cluster_kernel<16>, &cfg) == cudaSuccess && n >= 1;
+    big = cudaOccupancyMaxActiveClusters(&n, attn_mma_kernel<2, 4>, &cfg) == cudaSuccess && n >= 1;
     cudaGetLastError();
   }
-  if (!big) {
-    e = ac_set_attrs<1>(false);
-    if (e == cudaSuccess) e = ac_set_attrs<2>(false);
-    if (e == cudaSuccess) e = ac_set_attrs<4>(false);
-    if (e == cudaSuccess) e = ac_set_attrs<8>(false);
-    if (e == cudaSuccess) e = ac_set_attrs<16>(false);
-  }
+  if (!big) e = ac_set_attrs(false);
   g_ac_cluster = big ? 16 : 8;
   return e;
 }
@@ -454,12 +539,19 @@ cudaError_t attn_cluster_launch(const float* q, const uint16_t* k, const uint16_
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // the loops over the group's heads are unrolled to the next power of two
-  if (group <= 1) return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<1>, a);
-  if (group <= 2) return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<2>, a);
-  if (group <= 4) return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<4>, a);
-  if (group <= 8) return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<8>, a);
-  return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<16>, a);
+  // score tiles of 8 heads: 1 up to 8 query heads per value head, else 2;
+  // value tiles of 8 dimensions per warp: head_dim / 64
+  const int ntv = hd / 64;
+  if (group <= 8) {
+    if (ntv == 1) return cudaLaunchKernelEx(&cfg, attn_mma_kernel<1, 1>, a);
+    if (ntv == 2) return cudaLaunchKernelEx(&cfg, attn_mma_kernel<1, 2>, a);
+    if (ntv == 3) return cudaLaunchKernelEx(&cfg, attn_mma_kernel<1, 3>, a);
+    return cudaLaunchKernelEx(&cfg, attn_mma_kernel<1, 4>, a);
+  }
+  if (ntv == 1) return cudaLaunchKernelEx(&cfg, attn_mma_kernel<2, 1>, a);
+  if (ntv == 2) return cudaLaunchKernelEx(&cfg, attn_mma_kernel<2, 2>, a);
+  if (ntv == 3) return cudaLaunchKernelEx(&cfg, attn_mma_kernel<2, 3>, a);
+  return cudaLaunchKernelEx(&cfg, attn_mma_kernel<2, 4>, a);
 }
 
 }  // namespace q4
