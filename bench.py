@@ -57,6 +57,7 @@ KERNEL_SOURCES = {
     "tc_engine_kernel": ("q4_tc_engine.cu", "q4_frag.cuh", "q4_device.cuh", "q4_phase.cuh"),
     "oneshot_kernel": ("q4_oneshot.cu", "q4_frag.cuh", "q4_device.cuh"),
     "mma_kernel": ("q4_mma.cu", "q4_frag.cuh", "q4_device.cuh"),
+    "bt_engine_kernel": ("q4_bt_engine.cu", "q4_frag.cuh", "q4_device.cuh", "q4_phase.cuh"),
 }
 
 
@@ -202,7 +203,7 @@ def run_stack(args, torch, q4, model, synth, stream, barrier, gpu_index):
     ws, offs, ws_bytes = model.workspace(shape, n_layers, B)
     with torch.cuda.stream(stream):
         mode = q4.Q4_DEC_FUSED | (q4.Q4_DEC_BARRIER if args.barrier else 0) | (
-            q4.Q4_DEC_CUDA_CORE if args.cuda_core else 0)
+            q4.Q4_DEC_CUDA_CORE if args.cuda_core else 0) | (q4.Q4_DEC_BATCH_ENGINE if args.batch_engine else 0)
         dec = q4.q4_decoder_create(shape, ptrs, B, ws, ws_bytes, mode, stream=stream)
         h0 = torch.from_numpy(synth.activations(B, cfg["hidden"], 0).reshape(-1).view("int16").copy())
         h = h0.cuda()
@@ -238,18 +239,21 @@ def run_stack(args, torch, q4, model, synth, stream, barrier, gpu_index):
     tagged = q4.q4_decoder_tagged(dec)
     q4.q4_decoder_destroy(dec)
     nbytes = layer_bytes * n_layers
-    # batch 1: one persistent launch per token; batch B: per layer 4 tensor-core
-    # products + 2 glue launches, plus the first layer's input norm
-    launches = 1 if B == 1 else 6 * n_layers + 1
+    # batch 1 and the batched engine: one persistent launch per token; the
+    # per-product path: per layer 4 tensor-core products + 2 glue launches,
+    # plus the first layer's input norm
+    batched = 2 <= B <= 8 and args.batch_engine
+    launches = 1 if B == 1 or batched else 6 * n_layers + 1
     return dict(secs=secs, clocks=clocks, bytes_per_step=nbytes, launches_per_step=launches,
-                kernel_launches_per_step=1 if B == 1 else 4 * n_layers,
+                kernel_launches_per_step=1 if B == 1 or batched else 4 * n_layers,
                 e2e_secs=e2e_secs, e2e_steps=e2e_steps, h2d=h0.numel() * 2, d2h=h0.numel() * 2,
                 workload=(f"{'8B' if args.config == '8b' else '70B'}-shaped decoder stack, {n_layers} layers, "
                           f"batch {B}, HBM-resident, one CUDA-graph replay per step"),
                 kernel=(("engine_kernel" if args.barrier or args.cuda_core else "tc_engine_kernel") if B == 1
-                        else "mma_kernel"),
+                        else "bt_engine_kernel" if batched else "mma_kernel"),
                 kernel_key=((f"engine_kernel:{args.config}_stack" if args.barrier or args.cuda_core
                              else f"tc_engine_kernel:{args.config}_stack") if B == 1
+                            else f"bt_engine_kernel:{args.config}_stack_b{B}" if batched
                             else f"mma_kernel:{args.config}_stack_b{B}"),
                 n_layers=n_layers, cfg=cfg, tagged=tagged)
 
@@ -932,6 +936,9 @@ def main():
                     help="batch-1 stacks and rings: the CUDA-core engine instead of the tensor-core one (comparison)")
     ap.add_argument("--barrier", action="store_true",
                     help="batch-1 stacks: flag barrier after every phase instead of tagged words (comparison)")
+    ap.add_argument("--batch-engine", action="store_true",
+                    help="batch 2..8 stacks: the persistent batched engine instead of one product launch per "
+                         "projection (comparison)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank, world, local_rank = dist_env()

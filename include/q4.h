@@ -235,6 +235,12 @@ typedef struct q4_decoder q4_decoder;
                                the tensor-core engine.  The engines and the two phase
                                synchronisations agree within the product error bound, not bit
                                for bit */
+#define Q4_DEC_BATCH_ENGINE 16  /* or-ed into the mode: batch 2..8 runs the persistent batched
+                                   tensor-core engine (the whole stack in one launch, phases
+                                   meeting at flag barriers) instead of one product launch per
+                                   projection; Q4_ERR_ARG for shapes it does not take.  The two
+                                   agree within the product error bound, not bit for bit; on a
+                                   GB300 the per-product launches are the faster */
 
 /*
  * Create a decoder over n_layers HBM-resident layers and capture its CUDA
@@ -252,7 +258,14 @@ typedef struct q4_decoder q4_decoder;
  *                  (head_dim % 64 == 0 and the widths of Q4_KERNEL_STREAM);
  *                  batch 2..16 runs one tensor-core product launch per
  *                  projection with glue launches between them (hidden, q_dim,
- *                  ffn multiples of 256; kv_dim, head_dim multiples of 4)
+ *                  ffn multiples of 256; kv_dim, head_dim multiples of 4), or,
+ *                  with Q4_DEC_BATCH_ENGINE at batch 2..8, the persistent
+ *                  batched engine: the whole stack in one launch
+ *                  (Q4_DEC_FUSED) or one per layer, the batch rows as the
+ *                  columns of the instruction, each stage carrying its weights
+ *                  and its chunk of the input (hidden, q_dim, ffn of the widths
+ *                  of Q4_KERNEL_TC, n_layers <= 682).  In every case the rows
+ *                  of a batch do not affect one another
  *   stream         used for the workspace initialisation (synchronised)
  * Errors: Q4_ERR_ARG, Q4_ERR_ALIGN, Q4_ERR_OOM (workspace too small), Q4_ERR_CUDA.
  */

@@ -103,7 +103,7 @@ def test_decoder_checks(lib):
     assert f(ctypes.byref(h), ctypes.byref(shape), ptrs, 0, 1, 4096, ws_bytes, 0, None) == q4.Q4_ERR_ARG
     assert f(ctypes.byref(h), ctypes.byref(shape), ptrs, 2, 1, 4096 + 16, ws_bytes, 0, None) == q4.Q4_ERR_ALIGN
     assert f(ctypes.byref(h), ctypes.byref(shape), ptrs, 2, 1, 4096, ws_bytes - 1, 0, None) == q4.Q4_ERR_OOM
-    assert f(ctypes.byref(h), ctypes.byref(shape), ptrs, 2, 1, 4096, ws_bytes, 16, None) == q4.Q4_ERR_ARG  # unknown bit
+    assert f(ctypes.byref(h), ctypes.byref(shape), ptrs, 2, 1, 4096, ws_bytes, 32, None) == q4.Q4_ERR_ARG  # unknown bit
     both = q4.Q4_DEC_TENSOR_CORE | q4.Q4_DEC_CUDA_CORE
     assert f(ctypes.byref(h), ctypes.byref(shape), ptrs, 2, 1, 4096, ws_bytes, both, None) == q4.Q4_ERR_ARG
     bad = q4.LayerShape.of(hidden=256, q_dim=256, kv_dim=96, ffn=1024, head_dim=64)   # kv not whole heads

@@ -1,4 +1,6 @@
-"""Decoder stack and streamed ring at batch 2..16 (tensor-core products + glue kernels)."""
+"""Decoder stack and streamed ring at batch 2..16: the per-product path
+(tensor-core products + glue kernels, the default) and the persistent batched
+engine (batch 2..8, Q4_DEC_BATCH_ENGINE)."""
 import numpy as np
 import pytest
 import torch
@@ -49,10 +51,26 @@ class Stack:
         q4.q4_decoder_destroy(self.dec)
 
 
+BT = q4.Q4_DEC_FUSED | q4.Q4_DEC_BATCH_ENGINE
+
+
 @pytest.mark.parametrize("batch", [2, 8, 9, 16])
 @pytest.mark.parametrize("cfg", [TINY, SMALL, ODD], ids=["tiny", "small", "odd"])
 def test_one_layer_step_by_step(cfg, batch):
     st = Stack(cfg, 1, seed=81, batch=batch)
+    h0 = synth.activations(batch, cfg["hidden"], 82)
+    h1 = st.run(h0)
+    check_layer(cfg, 81, 0, st.state(), h1, h_in16=h0)
+    st.close()
+
+
+@pytest.mark.parametrize("batch", [2, 3, 5, 8])
+@pytest.mark.parametrize("cfg", [TINY, SMALL, MID], ids=["tiny", "small", "mid"])
+def test_batched_engine_one_layer_step_by_step(cfg, batch):
+    """The batched engine: every projection against the oracle fed the GPU's
+    own input, every glue step (RMSNorms, attention gather, SiLU product,
+    residual sums); batch 2, 3, 5, 8 use fragment buffers of 2, 4, 8, 8 columns."""
+    st = Stack(cfg, 1, seed=81, batch=batch, mode=BT)
     h0 = synth.activations(batch, cfg["hidden"], 82)
     h1 = st.run(h0)
     check_layer(cfg, 81, 0, st.state(), h1, h_in16=h0)
@@ -72,29 +90,72 @@ def test_last_layer_of_a_stack_wide_down():
     prev.close()
 
 
-def test_rows_do_not_depend_on_the_batch():
+@pytest.mark.parametrize("engine", ["per_product", "batched"])
+def test_rows_do_not_depend_on_the_batch(engine):
     """Each batch row's result is the same whatever the other rows hold and
-    whatever the batch size (one or two n-tiles of the tensor-core product)."""
+    whatever the batch size, within one engine (the per-product path: one or
+    two n-tiles of the tensor-core product; the batched engine: fragment
+    buffers of 2, 4 or 8 columns)."""
     cfg = SMALL
-    h16 = synth.activations(16, cfg["hidden"], 90)
-    full = Stack(cfg, 2, seed=91, batch=16)
+    extra = q4.Q4_DEC_BATCH_ENGINE if engine == "batched" else 0
+    full_b = 16 if engine == "per_product" else 8
+    h16 = synth.activations(full_b, cfg["hidden"], 90)
+    full = Stack(cfg, 2, seed=91, batch=full_b, mode=q4.Q4_DEC_FUSED | extra)
     a = full.run(h16)
     for b in (2, 5, 8):
-        part = Stack(cfg, 2, seed=91, batch=b, ptrs=full.ptrs)
+        if b >= full_b:
+            continue
+        part = Stack(cfg, 2, seed=91, batch=b, ptrs=full.ptrs, mode=q4.Q4_DEC_FUSED | extra)
         got = part.run(h16[:b])
         assert np.array_equal(got, a[:b]), b
         part.close()
     # change the other rows: row 0 unchanged
     h_mix = h16.copy()
-    h_mix[1:] = synth.activations(15, cfg["hidden"], 92)
+    h_mix[1:] = synth.activations(full_b - 1, cfg["hidden"], 92)
     assert np.array_equal(full.run(h_mix)[0], a[0])
     full.close()
 
 
-def test_graph_eager_and_pointer_change_identical():
+@pytest.mark.parametrize("cfg", [TINY, SMALL], ids=["tiny", "small"])
+def test_batched_engine_fused_per_layer_identical(cfg):
+    """The batched engine's whole-stack launch and its per-layer launches give
+    the same bits (the same units on the same CTAs, sums in the same order)."""
+    B, L = 6, 3
+    h0 = synth.activations(B, cfg["hidden"], 88)
+    fused = Stack(cfg, L, seed=89, batch=B, mode=BT)
+    per = Stack(cfg, L, seed=89, batch=B, mode=q4.Q4_DEC_PER_LAYER | q4.Q4_DEC_BATCH_ENGINE, ptrs=fused.ptrs)
+    a = fused.run(h0, reps=2)
+    b = per.run(h0, reps=2)
+    assert np.array_equal(a, b)
+    fused.close()
+    per.close()
+
+
+def test_batched_engine_agrees_with_per_product():
+    """The batched engine and the per-product path compute the same layer; their
+    projections agree within the product error bound, so one layer's output
+    (binary16) agrees closely row by row, and each stage of the batched engine
+    checks against the oracle."""
+    cfg, B = SMALL, 8
+    h0 = synth.activations(B, cfg["hidden"], 86)
+    a = Stack(cfg, 1, seed=87, batch=B, mode=BT)
+    b = Stack(cfg, 1, seed=87, batch=B, ptrs=a.ptrs)
+    ha, hb = a.run(h0), b.run(h0)
+    sa, sb = a.state(), b.state()
+    assert np.array_equal(sa["x"], sb["x"])          # the same input RMSNorm
+    check_layer(cfg, 87, 0, sa, ha, h_in16=h0)
+    fa, fb = ha.view(np.float16).astype(np.float64), hb.view(np.float16).astype(np.float64)
+    for r in range(B):
+        assert np.linalg.norm(fa[r] - fb[r]) <= 2e-3 * np.linalg.norm(fb[r]), r
+    a.close()
+    b.close()
+
+
+@pytest.mark.parametrize("mode", [q4.Q4_DEC_FUSED, BT], ids=["per_product", "batched"])
+def test_graph_eager_and_pointer_change_identical(mode):
     cfg, B = TINY, 4
     h0 = synth.activations(B, cfg["hidden"], 93)
-    st = Stack(cfg, 3, seed=94, batch=B)
+    st = Stack(cfg, 3, seed=94, batch=B, mode=mode)
     a = st.run(h0, graph=True, reps=2)
     b = st.run(h0, graph=False, reps=2)
     c = st.run(h0, graph=True, reps=2)     # a new buffer: captured again
@@ -142,12 +203,13 @@ def test_streamed_equals_resident(flags):
     ref.close()
 
 
-def test_8b_stack_batch8_full_size():
+@pytest.mark.parametrize("mode", [q4.Q4_DEC_FUSED, BT], ids=["per_product", "batched"])
+def test_8b_stack_batch8_full_size(mode):
     cfg = dict(synth.LLAMA_8B)
     L = cfg.pop("n_layers")
     B = 8
-    st = Stack(cfg, L, seed=0, batch=B)
-    prev = Stack(cfg, L - 1, seed=0, batch=B, ptrs=st.ptrs[:-1])
+    st = Stack(cfg, L, seed=0, batch=B, mode=mode)
+    prev = Stack(cfg, L - 1, seed=0, batch=B, ptrs=st.ptrs[:-1], mode=mode)
     h0 = synth.activations(B, cfg["hidden"], 1)
     prev.run(h0)
     t_prev = prev.state()["t2"]
@@ -170,3 +232,11 @@ def test_batched_shape_limits():
     bad = q4.LayerShape.of(**dict(TINY, ffn=1056))     # ffn a multiple of 32, not of 256
     with pytest.raises(q4.Q4Error):
         q4.q4_decoder_create(bad, ptrs, 4, ws, nb)
+    # the batched engine: batch 2..8 and widths of whole 2048-column chunks
+    with pytest.raises(q4.Q4Error):
+        q4.q4_decoder_create(shape, ptrs, 9, ws, nb, BT)
+    odd = q4.LayerShape.of(**ODD)
+    wodd, podd = model.resident_layers(odd, 1, 1)
+    wso, _, nbo = model.workspace(odd, 1, 4)
+    with pytest.raises(q4.Q4Error):
+        q4.q4_decoder_create(odd, podd, 4, wso, nbo, BT)

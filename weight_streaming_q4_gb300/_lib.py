@@ -39,6 +39,7 @@ Q4_DEC_PER_LAYER = 1
 Q4_DEC_TENSOR_CORE = 2
 Q4_DEC_BARRIER = 4
 Q4_DEC_CUDA_CORE = 8
+Q4_DEC_BATCH_ENGINE = 16
 Q4_STREAM_POISON = 1
 Q4_STREAM_TENSOR_CORE = 2
 Q4_STREAM_CHUNKED = 4

@@ -20,7 +20,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC, *ARCH]
 
 LIBS = {
-    "libq4.so": ["q4_engine.cu", "q4_tc_engine.cu", "q4_oneshot.cu", "q4_mma.cu", "q4_glue.cu", "q4_attn.cu", "q4_attn_cluster.cu", "q4_aux.cu", "q4_api.cu", "q4_noalloc.cu"],
+    "libq4.so": ["q4_engine.cu", "q4_tc_engine.cu", "q4_bt_engine.cu", "q4_oneshot.cu", "q4_mma.cu", "q4_glue.cu", "q4_attn.cu", "q4_attn_cluster.cu", "q4_aux.cu", "q4_api.cu", "q4_noalloc.cu"],
     "libq4synth.so": ["synth.cu"],
 }
 

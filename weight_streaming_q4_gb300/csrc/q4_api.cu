@@ -66,6 +66,7 @@ int device_info(DeviceInfo** out) {
     Q4_CUDA(q4::tc_engine_prepare());
     Q4_CUDA(q4::oneshot_prepare());
     Q4_CUDA(q4::attn_prepare());
+    Q4_CUDA(q4::bt_engine_prepare());
     Q4_CUDA(q4::engine_occupancy(&d.engine_blocks_per_sm));
     if (d.engine_blocks_per_sm < 1) return Q4_ERR_CUDA;
     int tc_blocks = 0;
@@ -91,7 +92,7 @@ bool engine_ok(int k) {
 
 // The two persistent engines: exact CUDA-core products (q4_engine.cu) and
 // tensor-core products (q4_tc_engine.cu).
-enum Engine { ENG_CORE = 0, ENG_TC = 1 };
+enum Engine { ENG_CORE = 0, ENG_TC = 1, ENG_BT = 2 };
 
 // Whether the tensor-core engine can run rows of width k: whole 8-block row
 // segments (16-byte aligned), one column chunk or whole 64-block chunks, and
@@ -303,9 +304,16 @@ extern "C" int q4_gemv(const void* w, const uint16_t* x, float* y, int n, int k,
 
 extern "C" int q4_timeline_read(unsigned long long* out, size_t n, int clear) {
   if (!out) return Q4_ERR_ARG;
-  const cudaError_t e = q4::tc_timeline_read(out, n, clear != 0);
+  cudaError_t e = q4::tc_timeline_read(out, n, clear != 0);
   if (e == cudaErrorNotSupported || e == cudaErrorInvalidValue) return Q4_ERR_ARG;
   Q4_CUDA(e);
+  // the batched engine keeps its own timeline: merged in (of two stamps of
+  // one slot, only the engine that ran has written one)
+  std::vector<unsigned long long> bt(n);
+  e = q4::bt_timeline_read(bt.data(), n, clear != 0);
+  if (e == cudaErrorNotSupported || e == cudaErrorInvalidValue) return Q4_ERR_ARG;
+  Q4_CUDA(e);
+  for (size_t i = 0; i < n; ++i) out[i] = std::max(out[i], bt[i]);
   return Q4_OK;
 }
 
@@ -356,9 +364,15 @@ extern "C" int q4_workspace_layout(const q4_layer_shape* s, int n_layers, int ba
                                    size_t* total_bytes) {
   if (!shape_ok(s) || n_layers < 1 || batch < 1 || batch > q4::kMaxBatch || !offsets) return Q4_ERR_ARG;
   const size_t B = static_cast<size_t>(batch);
+  const size_t L = static_cast<size_t>(n_layers);
+  // batch 2..16: the batched engine's program, its input fragments (z and the
+  // attention output after the tagged-word regions' place, act after v's) and
+  // its per-CTA sums of squares after the flags
+  const size_t prog = std::max(sizeof(Phase) * (4 * L + 1), batch > 1 ? sizeof(q4::BtPhase) * (6 * L + 1) : 0);
+  const size_t frag = 2 * static_cast<size_t>(q4::kBtCols);   // fragment bytes per value
   const size_t sizes[Q4_WS_COUNT] = {
       sizeof(Control),
-      sizeof(Phase) * (4 * static_cast<size_t>(n_layers) + 1),
+      prog,
       4 * B * (s->q_dim + 2 * s->kv_dim),
       4 * B * s->hidden,
       4 * B * s->ffn,
@@ -370,12 +384,13 @@ extern "C" int q4_workspace_layout(const q4_layer_shape* s, int n_layers, int ba
       2 * B * s->hidden,
       4 * B * s->hidden,
       4 * B * s->hidden,
-      8 * 2 * static_cast<size_t>(q4::kMaxGrid) + 4 * 2 * static_cast<size_t>(q4::kMaxGrid),
+      8 * 2 * static_cast<size_t>(q4::kMaxGrid) + 4 * 2 * static_cast<size_t>(q4::kMaxGrid) +
+          4 * static_cast<size_t>(q4::kBtCols) * q4::kMaxGrid,
       // batch-1 engine inputs: fp32 t1/t2 slice-transposed, or (tagged programs)
       // tagged t1 and t2 (64-bit words) and the tagged residual bases z and z1
-      24 * static_cast<size_t>(s->hidden),
+      std::max(24 * static_cast<size_t>(s->hidden), batch > 1 ? frag * (s->hidden + s->q_dim) : 0),
       4 * static_cast<size_t>(s->kv_dim),
-      4 * static_cast<size_t>(s->ffn),
+      std::max(4 * static_cast<size_t>(s->ffn), batch > 1 ? frag * s->ffn : 0),
   };
   size_t pos = 0;
   for (int i = 0; i < Q4_WS_COUNT; ++i) {
@@ -401,6 +416,10 @@ struct Work {
   // the same regions in a tagged program: tagged t1, t2 (fp32), z, z1, v, act (binary16)
   unsigned long long *t1t, *t2t;
   uint32_t *zt, *z1t, *vtag, *acttag;
+  // batched engine: input fragments of q|k|v and gate|up (z, z1), of o (the
+  // attention output) and of down (act); per-CTA sums of squares
+  uint8_t *zf, *af, *actf;
+  float* ss8;
 };
 
 Work carve(void* ws, const size_t* off, int hidden) {
@@ -431,6 +450,10 @@ Work carve(void* ws, const size_t* off, int hidden) {
   w.z1t = w.zt + hidden;
   w.vtag = reinterpret_cast<uint32_t*>(b + off[Q4_WS_VT]);
   w.acttag = reinterpret_cast<uint32_t*>(b + off[Q4_WS_ACTT]);
+  w.zf = reinterpret_cast<uint8_t*>(b + off[Q4_WS_XT]);
+  w.af = w.zf + 2 * static_cast<size_t>(q4::kBtCols) * hidden;
+  w.actf = reinterpret_cast<uint8_t*>(b + off[Q4_WS_ACTT]);
+  w.ss8 = w.ss2 + q4::kMaxGrid;
   return w;
 }
 
@@ -798,6 +821,123 @@ bool batched_shape_ok(const q4_layer_shape& s) {
          s.kv_dim % 4 == 0 && s.head_dim % 4 == 0;   // the glue moves 4 values at a time
 }
 
+// ---------------------------------------------------------------- batched engine
+//
+// Batch 2..8: one persistent launch of q4_bt_engine.cu runs the stack (the
+// same layer arithmetic as launch_layer_batched, within the product error
+// bound of it: the sums run in another order).  The program has 6 phases per
+// layer (q|k|v, o, RMSNorm, gate|up, down, RMSNorm) after one RMSNorm of the
+// caller's binary16 state.
+
+bool bt_fits(const q4_layer_shape& s, int batch, int* stages, uint32_t* stage_bytes, uint32_t* x_off) {
+  const int ks[3] = {s.hidden, s.q_dim, s.ffn};
+  return q4::bt_geom(ks, 3, q4::bt_cols(batch), stages, stage_bytes, x_off);
+}
+
+bool bt_shape_ok(const q4_layer_shape& s, int n_layers) {
+  int st = 0;
+  uint32_t sb = 0, xo = 0;
+  return 6 * n_layers + 1 <= static_cast<int>(q4::kPhasesPerEpoch) && batched_shape_ok(s) &&
+         bt_fits(s, q4::kBtCols, &st, &sb, &xo);
+}
+
+bool bt_stack_program(const q4_layer_shape& s, const std::vector<const uint8_t*>& layers, uint16_t* h, const Work& w,
+                      std::vector<q4::BtPhase>& prog) {
+  size_t off[7];
+  if (q4_layer_offsets(&s, off, nullptr) != Q4_OK) return false;
+  const int L = static_cast<int>(layers.size());
+  const int H = s.hidden, Q = s.q_dim, KV = s.kv_dim, F = s.ffn;
+  prog.assign(6 * static_cast<size_t>(L) + 1, q4::BtPhase{});
+  int base = 0;
+  // an RMSNorm of H values per batch row into z (natural) and the z fragments
+  auto form = [&](q4::BtPhase& f, const float* src32, const uint16_t* src16, uint16_t* out16) {
+    f.kind = q4::BT_FORM;
+    f.k = H;
+    f.src32 = src32;
+    f.src16 = src16;
+    f.ss = w.ss8;
+    f.out16 = out16;
+    f.out_frag = w.zf;
+    f.eps = s.eps;
+  };
+  // a product phase: 32-row units (16 rows of each matrix of a gate|up pair)
+  auto unit = [&](q4::BtPhase& p, int kind, const uint8_t* w0, const uint8_t* w1, int n, int k,
+                  const uint8_t* xf) -> bool {
+    p.kind = kind;
+    p.n_rows = n;
+    p.k = k;
+    p.x_frag = xf;
+    const int rows = kind == q4::BT_SILU ? q4::kTcUnitRows / 2 : q4::kTcUnitRows;
+    p.units = (n + rows - 1) / rows;
+    p.base = base;
+    base += p.units;
+    if (!encode_rows(&p.tm0, w0, n, k, rows)) return false;
+    return kind != q4::BT_SILU || encode_rows(&p.tm1, w1, n, k, rows);
+  };
+  form(prog[0], nullptr, h, w.x);
+  for (int l = 0; l < L; ++l) {
+    const uint8_t* wl = layers[l];
+    q4::BtPhase* P = &prog[1 + 6 * static_cast<size_t>(l)];
+    // q, k, v: one matrix of q_dim + 2 kv_dim rows; the v rows also go out as
+    // the context-1 attention output a (binary16, gathered per head)
+    if (!unit(P[0], q4::BT_PLAIN, wl + off[Q4_PROJ_Q], nullptr, Q + 2 * KV, H, w.zf)) return false;
+    P[0].y = w.qkv;
+    P[0].out16 = w.attn;
+    P[0].out_frag = w.af;
+    P[0].out_ld = Q;
+    P[0].g_lo = Q + KV;
+    P[0].g_n = KV;
+    P[0].head_dim = s.head_dim;
+    P[0].group = (Q / s.head_dim) / (KV / s.head_dim);
+    if ((Q + 2 * KV) % q4::kTcUnitRows == 0 && (Q + KV) % q4::kTcUnitRows == 0) {
+      // value rows first: a CTA publishes q|k|v (the o phase's input is
+      // ready) once its units among the first KV / 32 are stored
+      P[0].row_rot = Q + KV;
+      P[0].early_units = (KV + q4::kTcUnitRows - 1) / q4::kTcUnitRows;
+    }
+    // o with the residual base z: t1
+    if (!unit(P[1], q4::BT_RESID, wl + off[Q4_PROJ_O], nullptr, H, Q, w.af)) return false;
+    P[1].y = w.o;
+    P[1].y2 = w.t1;
+    P[1].res = w.x;
+    P[1].ss = w.ss8;
+    form(P[2], w.t1, nullptr, w.x2);
+    if (!unit(P[3], q4::BT_SILU, wl + off[Q4_PROJ_GATE], wl + off[Q4_PROJ_UP], F, H, w.zf)) return false;
+    P[3].y = w.g;
+    P[3].y2 = w.u;
+    P[3].out16 = w.act;
+    P[3].out_frag = w.actf;
+    // down with the residual base z1: t2, normalised into the next layer's z
+    // (the last layer's into the caller's buffer)
+    if (!unit(P[4], q4::BT_RESID, wl + off[Q4_PROJ_DOWN], nullptr, H, F, w.actf)) return false;
+    P[4].y = w.dn;
+    P[4].y2 = w.t2;
+    P[4].res = w.x2;
+    P[4].ss = w.ss8;
+    form(P[5], w.t2, nullptr, l + 1 == L ? h : w.x);
+  }
+  for (size_t i = 0; i < prog.size(); ++i) prog[i].gidx = static_cast<int>(i);
+  return true;
+}
+
+// Phases [first, first + n) of the batched program in the workspace.
+int launch_bt(const Work& w, int first, int n, int grid, int batch, bool end, const q4_layer_shape& s,
+              cudaStream_t st) {
+  q4::BtArgs a;
+  memset(&a, 0, sizeof(a));
+  a.phases = reinterpret_cast<const q4::BtPhase*>(w.prog) + first;
+  a.n_phases = n;
+  a.ctl = w.ctl;
+  a.flags = w.flags;
+  a.wait_limit = kWaitLimit;
+  a.batch = batch;
+  a.cols = q4::bt_cols(batch);
+  a.end_of_program = end ? 1 : 0;
+  if (!bt_fits(s, batch, &a.stages, &a.stage_bytes, &a.x_off)) return Q4_ERR_ARG;
+  Q4_CUDA(q4::bt_engine_launch(a, grid, st));
+  return Q4_OK;
+}
+
 // Launch phases [first_phase, first_phase + n_phases) of the program in the
 // workspace; `end` = they include the program's last phase.
 int launch_layers(const Work& w, int first_phase, int n_phases, int grid, cudaStream_t s, int engine, bool tagged,
@@ -859,7 +999,14 @@ struct q4_decoder {
 };
 
 static int decoder_write_program(q4_decoder* d, uint16_t* h, cudaStream_t s) {
-  if (d->batch > 1) {   // the batched path passes pointers as launch arguments
+  if (d->engine == ENG_BT) {
+    std::vector<q4::BtPhase> prog;
+    if (!bt_stack_program(d->shape, d->layers, h, d->w, prog)) return Q4_ERR_ARG;
+    Q4_CUDA(cudaMemcpyAsync(d->w.prog, prog.data(), prog.size() * sizeof(q4::BtPhase), cudaMemcpyHostToDevice, s));
+    d->cur_h = h;
+    return Q4_OK;
+  }
+  if (d->batch > 1) {   // the per-product path passes pointers as launch arguments
     d->cur_h = h;
     if (d->exec) {        // re-capture with the new buffer
       cudaGraphExecDestroy(d->exec);
@@ -879,6 +1026,14 @@ static int decoder_write_program(q4_decoder* d, uint16_t* h, cudaStream_t s) {
 
 static int decoder_enqueue(q4_decoder* d, cudaStream_t s) {
   const int L = d->n_layers;
+  if (d->engine == ENG_BT) {
+    if (d->mode == Q4_DEC_FUSED) return launch_bt(d->w, 0, 6 * L + 1, d->grid, d->batch, true, d->shape, s);
+    for (int l = 0; l < L; ++l) {   // the first launch also runs the first RMSNorm
+      int st = launch_bt(d->w, l == 0 ? 0 : 6 * l + 1, l == 0 ? 7 : 6, d->grid, d->batch, l == L - 1, d->shape, s);
+      if (st != Q4_OK) return st;
+    }
+    return Q4_OK;
+  }
   if (d->batch > 1) {
     for (int l = 0; l < L; ++l) {
       int st = launch_layer_batched(d->shape, d->layers[l], l, L, d->cur_h, d->w, d->batch, d->grid, s);
@@ -920,12 +1075,15 @@ extern "C" int q4_decoder_create(q4_decoder** out, const q4_layer_shape* shape, 
   if (!out || !shape_ok(shape) || !layer_weights || n_layers < 1 || !workspace) return Q4_ERR_ARG;
   if (batch < 1 || batch > q4::kMaxBatch) return Q4_ERR_ARG;
   if (4 * n_layers + 1 > static_cast<int>(q4::kPhasesPerEpoch)) return Q4_ERR_ARG;
-  const int kind = mode & ~(Q4_DEC_TENSOR_CORE | Q4_DEC_BARRIER | Q4_DEC_CUDA_CORE);
+  const int kind = mode & ~(Q4_DEC_TENSOR_CORE | Q4_DEC_BARRIER | Q4_DEC_CUDA_CORE | Q4_DEC_BATCH_ENGINE);
   if (kind != Q4_DEC_FUSED && kind != Q4_DEC_PER_LAYER) return Q4_ERR_ARG;
-  // batch 1: a persistent engine; larger batches: tensor-core products + glue
+  // batch 1: a persistent engine; larger batches: tensor-core products +
+  // glue, or (asked for, batch 2..8) the persistent batched engine
+  const bool bt = batch > 1 && (mode & Q4_DEC_BATCH_ENGINE);
+  if (bt && (batch > q4::kBtCols || !bt_shape_ok(*shape, n_layers))) return Q4_ERR_ARG;
   const int engine = batch == 1 ? pick_engine(*shape, (mode & Q4_DEC_TENSOR_CORE) != 0,
                                               (mode & (Q4_DEC_CUDA_CORE | Q4_DEC_BARRIER)) != 0)
-                                : ENG_CORE;
+                                : (bt ? ENG_BT : ENG_CORE);
   if (batch == 1 ? engine < 0 : !batched_shape_ok(*shape)) return Q4_ERR_ARG;
   if (!aligned(workspace, 256)) return Q4_ERR_ALIGN;
   for (int l = 0; l < n_layers; ++l) {

@@ -153,6 +153,86 @@ struct Control {
 // programs use flags[cta] alone, with a zero low word.
 constexpr unsigned kPhasesPerEpoch = 4096;
 
+// ------------------------------------------------------------------ batched engine
+//
+// The persistent tensor-core engine for batches of 2..8 rows (q4_bt_engine.cu).
+// The batch is the n dimension of the instruction (8 columns), so an input is
+// 8 x k binary16 values: too many to keep a whole phase input in shared memory
+// next to the ring.  Instead every phase input lives in global memory as
+// fragments (column b of the instruction = batch row b, k in the order the
+// code unpacking delivers it) and each ring stage carries the chunk of
+// fragments its weights need, copied with one bulk copy.  The phases meet at a
+// flag barrier (all CTAs), and each RMSNorm is its own small phase (BT_FORM):
+// every CTA normalises a slice of the rows' values into the next fragments.
+enum BtKind : int {
+  BT_PLAIN = 0,   // y = W x; optionally rows [g_lo, g_lo + g_n) gathered per head (context-1 attention)
+  BT_RESID = 1,   // y = W x; y2 = t = res + y (fp32); sums of squares of t per CTA and batch row
+  BT_SILU = 2,    // gate|up pair: y = g, y2 = u, act = f16(silu(g) * u)
+  BT_FORM = 3,    // z = f16(t * rsqrt(mean(t^2) + eps)) for every batch row (no weights)
+};
+constexpr int kBtCols = 8;            // batch columns (one n-tile of the instruction)
+
+// Fragment buffers hold `cols` columns (the batch rounded up to 2, 4 or 8;
+// the instruction's other columns are zero): 64 * cols bytes per 32-value
+// block.  Byte offset of value e of batch row b: block e / 32, lane
+// (b, (e % 16) / 4), bytes 0-7 for e % 32 < 16 else 8-15, halves in the order
+// 4t, 4t+2, 4t+1, 4t+3.
+__host__ __device__ __forceinline__ int bt_cols(int batch) { return batch <= 2 ? 2 : batch <= 4 ? 4 : 8; }
+__host__ __device__ __forceinline__ uint32_t bt_frag_off(int b, int e, int cols) {
+  const int i = e & 31, j = e & 3;
+  return static_cast<uint32_t>((e >> 5) * 64 * cols + (b * 4 + ((i & 15) >> 2)) * 16 + ((i >> 4) << 3) +
+                               (((j & 1) << 1) | (j >> 1)) * 2);
+}
+
+struct BtPhase {
+  CUtensorMap tm0;          // unit phases: the weights (descriptors as the batch-1 tensor-core engine's)
+  CUtensorMap tm1;          // BT_SILU: up
+  const uint8_t* x_frag;    // unit phases: input fragments, k * 16 bytes
+  float* y;                 // fp32 [batch][n_rows] (BT_SILU: g)
+  float* y2;                // BT_SILU: u; BT_RESID: t
+  const uint16_t* res;      // BT_RESID: binary16 [batch][n_rows]
+  uint16_t* out16;          // binary16 natural output: BT_PLAIN the gathered heads, BT_SILU act, BT_FORM z
+  uint8_t* out_frag;        // the same values as fragments (the next phase's input)
+  const float* src32;       // BT_FORM: fp32 t [batch][k], its sums of squares in ss
+  const uint16_t* src16;    // BT_FORM: binary16 [batch][k] (sums of squares taken from it)
+  float* ss;                // BT_RESID: out, BT_FORM: in; [grid][kBtCols]
+  int kind;
+  int gidx;                 // index of the phase in the whole program (its tag offset)
+  int k;                    // unit phases: row width; BT_FORM: values per batch row
+  int n_rows;
+  int units;
+  int base;                 // units of earlier phases: unit u goes to CTA (base + u) mod G
+  int out_ld;               // BT_PLAIN: row stride of out16
+  int g_lo, g_n, head_dim, group;
+  float eps;
+  int row_rot;              // unit u covers rows from (u * 32 + row_rot) mod n_rows (multiples of 32)
+  int early_units;          // BT_PLAIN: units [0, early_units) hold the gathered rows; a CTA
+                            // publishes the phase once its units among them are stored (0: at the end)
+};
+
+struct BtArgs {
+  const BtPhase* phases;    // device array
+  int n_phases;
+  Control* ctl;
+  unsigned long long* flags;   // [kMaxGrid] per-CTA flags, the phase tag in the high word
+  uint32_t wait_limit;
+  uint32_t stage_bytes;     // bytes between ring stages
+  uint32_t x_off;           // offset of the fragment chunk inside a stage
+  int stages;
+  int batch;
+  int cols;                 // bt_cols(batch): columns of the fragment buffers
+  int end_of_program;       // the last CTA to leave advances the epoch
+};
+
+cudaError_t bt_engine_prepare();
+// Ring geometry for phases of widths ks (each tc_chunk_blocks-compatible) and
+// fragment buffers of `cols` columns: false if it does not fit.
+bool bt_geom(const int* ks, int n, int cols, int* stages, uint32_t* stage_bytes, uint32_t* x_off);
+cudaError_t bt_engine_launch(const BtArgs& a, int grid, cudaStream_t stream);
+// Timeline of the batched engine's phases (libq4_tl.so only), laid out as
+// tc_timeline_read's.
+cudaError_t bt_timeline_read(unsigned long long* out, size_t n, bool clear);
+
 // Arguments of one launch of the engine kernel: either a device array of
 // phases or a single phase passed by value.
 struct EngineArgs {
