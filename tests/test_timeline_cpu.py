@@ -35,3 +35,34 @@ def test_summary_splits_a_layer():
     assert abs(lay["spread_us"] - 4 * 0.15) < 0.05
     assert abs(lay["boundaries_us"] - 4 * 2.0) < 0.05
     assert 0 < lay["unit_loop_frac"] < 1
+
+
+def test_batched_summary_splits_a_layer():
+    """The batched engine's layout: phase 0 an RMSNorm, then q|k|v, o, norm,
+    gate|up, down, norm per layer; a layer spans the previous layer's last
+    RMSNorm (slowest CTA published) to its own, and its product loops are the
+    median CTA's first stage landed -> last unit of the four product phases."""
+    n_layers, grid = 3, 4
+    loop_us = {1: 2.0, 2: 2.0, 4: 18.0, 5: 10.0}   # by position in the layer
+    tl = np.zeros((_lib.TIMELINE_CTAS, _lib.TIMELINE_PHASES, _lib.TIMELINE_EVENTS), np.uint64)
+    t = 1_000_000.0
+    for p in range(6 * n_layers + 1):
+        pos = 0 if p == 0 else (p - 1) % 6 + 1
+        dur = loop_us.get(pos, 0.0)
+        for c in range(grid):
+            tl[c, p, 0] = t * 1e3
+            tl[c, p, 1] = (t + 0.5) * 1e3
+            tl[c, p, 2] = (t + 1.0) * 1e3
+            if dur:
+                tl[c, p, 3] = (t + 1.0 + dur) * 1e3
+                tl[c, p, 5] = (t + 0.8) * 1e3
+            tl[c, p, 4] = (t + 1.0 + dur + 1.5 + 0.1 * c) * 1e3
+        t += 1.0 + dur + 1.5 + 0.1 * (grid - 1) + 2.0
+    r = timeline.summarise_batched(tl, n_layers, grid)
+    assert [p["kind"] for p in r["phases"][:7]] == ["norm", "q|k|v", "o", "norm", "gate|up", "down", "norm"]
+    assert len(r["layers"]) == n_layers - 1
+    for lay in r["layers"]:
+        assert abs(lay["unit_loops_us"] - sum(loop_us.values())) < 1e-6
+        per_phase = 1.0 + 1.5 + 0.1 * (grid - 1) + 2.0
+        assert abs(lay["us"] - (sum(loop_us.values()) + 6 * per_phase)) < 1e-6
+        assert abs(lay["rest_us"] - 6 * per_phase) < 1e-6
