@@ -726,7 +726,7 @@ def run_attn(args, torch, q4, model, synth, stream, barrier, gpu_index):
                 e2e_secs=e2e_secs, e2e_steps=e2e_steps, h2d=q_host.numel() * 4, d2h=out.numel() * 2,
                 workload=(f"decode attention, 8B heads (32 q, 8 kv, head_dim 128), {L} layers' binary16 KV caches, "
                           f"context {cap} (bucket {cap}), one CUDA graph per bucket"),
-                kernel="attn_cluster_kernel", kernel_key=None, cfg=dict(n_q=n_q, n_kv=n_kv, hd=hd),
+                kernel="attn_mma_kernel", kernel_key=None, cfg=dict(n_q=n_q, n_kv=n_kv, hd=hd),
                 attn_buckets={str(b): {k: v for k, v in r.items() if k not in ("secs", "clocks")}
                               for b, r in per.items()})
 
