@@ -753,13 +753,14 @@ def run_sweep(args, torch, q4, model, synth, stream, barrier, gpu_index):
     nmax = max(n for n, _ in dims)
     x = torch.from_numpy(synth.activations(16, kmax, 0).reshape(-1).view("int16").copy()).cuda()
     y = torch.empty(16 * nmax, dtype=torch.float32, device="cuda")
-    kernels = {"engine": q4.Q4_KERNEL_STREAM, "mma": q4.Q4_KERNEL_MMA, "simple": q4.Q4_KERNEL_SIMPLE}
+    kernels = {"oneshot": q4.Q4_KERNEL_ONESHOT, "tc_engine": q4.Q4_KERNEL_TC, "engine": q4.Q4_KERNEL_STREAM,
+               "mma": q4.Q4_KERNEL_MMA, "simple": q4.Q4_KERNEL_SIMPLE}
     nbytes = layer_bytes * n_layers
     steps = max(5, min(args.steps, 50))
     results = {}
     for B in (1, 2, 4, 8, 16):
         for name, kern in kernels.items():
-            if name == "engine" and B != 1:
+            if name in ("oneshot", "tc_engine", "engine") and B != 1:   # batch-1 kernels
                 continue
 
             def enqueue():

@@ -19,14 +19,14 @@ def _built():
 
 
 class Ring:
-    def __init__(self, cfg, n_layers, seed, flags=0, distinct=None):
+    def __init__(self, cfg, n_layers, seed, flags=0, distinct=None, batch=1):
         self.shape = q4.LayerShape.of(**cfg)
         self.blocks, self.hptrs = model.host_layers(self.shape, n_layers, seed, distinct=distinct)
         stride = model.layer_stride(self.shape)
         single = bool(flags & q4.Q4_STREAM_SINGLE_BUFFER)
         self.bufs = [torch.empty(stride, dtype=torch.uint8, device="cuda") for _ in range(1 if single else 2)]
-        self.ws, self.offs, self.ws_bytes = model.workspace(self.shape, n_layers, 1)
-        self.h = q4.q4_stream_create(self.shape, self.hptrs, 1, self.bufs[0], None if single else self.bufs[1],
+        self.ws, self.offs, self.ws_bytes = model.workspace(self.shape, n_layers, batch)
+        self.h = q4.q4_stream_create(self.shape, self.hptrs, batch, self.bufs[0], None if single else self.bufs[1],
                                      stride, self.ws, self.ws_bytes, flags)
 
     def run(self, h_np, tokens=1, timeout_us=0):
@@ -41,18 +41,18 @@ class Ring:
         q4.q4_stream_destroy(self.h)
 
 
-def resident(cfg, n_layers, seed, h_np, tokens=1, core=False, barrier=False):
+def resident(cfg, n_layers, seed, h_np, tokens=1, core=False, barrier=False, batch=1):
     shape = q4.LayerShape.of(**cfg)
     wbuf, ptrs = model.resident_layers(shape, n_layers, seed)
-    ws, offs, nb = model.workspace(shape, n_layers, 1)
+    ws, offs, nb = model.workspace(shape, n_layers, batch)
     mode = q4.Q4_DEC_PER_LAYER | (q4.Q4_DEC_CUDA_CORE if core else 0) | (q4.Q4_DEC_BARRIER if barrier else 0)
-    dec = q4.q4_decoder_create(shape, ptrs, 1, ws, nb, mode)
+    dec = q4.q4_decoder_create(shape, ptrs, batch, ws, nb, mode)
     h = dev_u16(h_np.reshape(-1))
     for _ in range(tokens):
         q4.q4_layer_decode(dec, h)
     torch.cuda.synchronize()
     q4.q4_decoder_destroy(dec)
-    return host_u16(h).reshape(1, -1)
+    return host_u16(h).reshape(batch, -1)
 
 
 @pytest.mark.parametrize("cfg,n_layers", [(TINY, 5), (SMALL, 4)], ids=["tiny5", "small4"])
@@ -229,16 +229,18 @@ def test_single_buffer_partial_residency_and_batch():
         q4.q4_stream_destroy(h2)
 
 
+@pytest.mark.parametrize("batch", [1, 4])
 @pytest.mark.parametrize("single", [False, True], ids=["double", "single"])
-def test_timeline_orders_copies_and_compute(single):
+def test_timeline_orders_copies_and_compute(single, batch):
     """The ring's GPU timestamps obey its synchronisation: a layer computes
     after its copy ended; a buffer is overwritten only after the compute that
     read it ended (layer i + 2 with two buffers, i + 1 with one); layers
-    compute in order.  Results stay equal to the resident stack."""
+    compute in order.  Results stay equal to the resident stack (batch 4: the
+    per-product path)."""
     cfg, L = SMALL, 6
     flags = q4.Q4_STREAM_TIMELINE | (SB if single else 0)
-    h0 = synth.activations(1, cfg["hidden"], 94)
-    ring = Ring(cfg, L, seed=95, flags=flags)
+    h0 = synth.activations(batch, cfg["hidden"], 94)
+    ring = Ring(cfg, L, seed=95, flags=flags, batch=batch)
     got = ring.run(h0, tokens=2)
     tl = q4.q4_stream_timeline(ring.h, L).astype(np.int64)
     assert (tl > 0).all()
@@ -248,7 +250,7 @@ def test_timeline_orders_copies_and_compute(single):
     assert (kb[1:] >= ke[:-1]).all()             # one compute stream
     step = 1 if single else 2
     assert (cb[step:] >= ke[:-step]).all()       # buffer reuse after its reader finished
-    assert np.array_equal(got, resident(cfg, L, 95, h0, tokens=2))
+    assert np.array_equal(got.reshape(batch, -1), resident(cfg, L, 95, h0, tokens=2, batch=batch))
     with pytest.raises(q4.Q4Error):
         q4.q4_stream_timeline(ring.h, L - 1)      # buffer too small
     ring.close()

@@ -1446,6 +1446,10 @@ extern "C" int q4_stream_layers(q4_stream* r, uint16_t* hidden_io, void* compute
       // batched: each projection waits for its own chunk (or the whole block)
       cudaEvent_t ev[4];
       for (int c = 0; c < 4; ++c) ev[c] = r->loaded[b < 0 ? 0 : b][chunked ? c : 0];
+      if (ts) {   // the layer's compute starts once its first chunk (or block) has landed
+        if (b >= 0) Q4_CUDA(cudaStreamWaitEvent(cs, ev[0], 0));
+        Q4_CUDA(q4::stamp_launch(ts + 2, cs));
+      }
       st = launch_layer_batched(r->shape, wl, i, r->n_layers, hidden_io, r->w, r->batch, r->grid, cs,
                                 b < 0 ? nullptr : ev);
     } else if (b < 0 || !chunked) {
