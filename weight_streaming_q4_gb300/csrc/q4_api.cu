@@ -940,10 +940,13 @@ int launch_bt(const Work& w, int first, int n, int grid, int batch, bool end, co
 
 // Launch phases [first_phase, first_phase + n_phases) of the program in the
 // workspace; `end` = they include the program's last phase.
+// pdl (tensor-core engine): EngineArgs::pdl; with bit 0 the launch is not
+// cooperative (it may start while the kernel ahead of it still runs).
 int launch_layers(const Work& w, int first_phase, int n_phases, int grid, cudaStream_t s, int engine, bool tagged,
-                  bool end, const q4_layer_shape& shape, uint32_t wait_limit = kWaitLimit) {
+                  bool end, const q4_layer_shape& shape, uint32_t wait_limit = kWaitLimit, int pdl = 0) {
   EngineArgs a;
   memset(&a, 0, sizeof(a));
+  a.pdl = engine == ENG_TC ? pdl : 0;
   a.phases = w.prog + first_phase;
   a.n_phases = n_phases;
   a.ctl = w.ctl;
@@ -962,7 +965,7 @@ int launch_layers(const Work& w, int first_phase, int n_phases, int grid, cudaSt
     a.stages = g.stages;
     a.stage_bytes = g.stage_bytes;
     a.xbuf_floats = g.xbuf_floats;
-    Q4_CUDA(q4::tc_engine_launch(a, grid, true, s));
+    Q4_CUDA(q4::tc_engine_launch(a, grid, (a.pdl & 1) == 0, s));
   } else {
     Q4_CUDA(q4::engine_launch(a, grid, true, s));
   }
@@ -1046,16 +1049,21 @@ static int decoder_enqueue(q4_decoder* d, cudaStream_t s) {
     // k and v in row *pos of the layer's caches and attends over rows
     // 0..*pos; then one engine launch runs the o, gate|up and down phases of
     // layer l and the q|k|v phase of layer l + 1 (or the closing phase).
-    // After the last layer the position advances.
+    // After the last layer the position advances.  Programmatic dependent
+    // launches chain them: an engine launch lets the attention after it start
+    // (copying cached keys and values) as its CTAs leave; the attention, once
+    // it has waited for that engine launch, lets the next engine launch start
+    // (streaming weights) while it computes.
     const q4_layer_shape& sh = d->shape;
-    int st = launch_layers(d->w, 0, 1, d->grid, s, d->engine, true, false, sh);
+    int st = launch_layers(d->w, 0, 1, d->grid, s, d->engine, true, false, sh, kWaitLimit, 2);
     if (st != Q4_OK) return st;
     for (int l = 0; l < L; ++l) {
       const float* qkv = d->w.qkv;
-      const q4::AttnAppend app = {qkv + sh.q_dim, qkv + sh.q_dim + sh.kv_dim, d->pos, &d->w.ctl->status};
+      const q4::AttnAppend app = {qkv + sh.q_dim, qkv + sh.q_dim + sh.kv_dim, d->pos, &d->w.ctl->status, 1};
       Q4_CUDA(q4::attn_launch(qkv, d->kc[l], d->vc[l], d->pos, d->capacity, sh.q_dim / sh.head_dim,
                               sh.kv_dim / sh.head_dim, sh.head_dim, d->w.attn, d->attn_ws, s, 1, &app));
-      st = launch_layers(d->w, 4 * l + 1, 4, d->grid, s, d->engine, true, l == L - 1, sh);
+      st = launch_layers(d->w, 4 * l + 1, 4, d->grid, s, d->engine, true, l == L - 1, sh, kWaitLimit,
+                         l == L - 1 ? 1 : 3);
       if (st != Q4_OK) return st;
     }
     Q4_CUDA(q4::pos_advance_launch(d->pos, s));

@@ -38,6 +38,7 @@
 #include <stdint.h>
 
 #include "q4_device.cuh"
+#include "q4_frag.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -67,7 +68,21 @@ struct AcArgs {
   int span;              // positions per CTA
   int round;             // positions per round (64 KB of keys and values)
   float scale;           // 1 / sqrt(hd)
+  int pdl;               // launched as a programmatic dependent of the kernel that wrote q and the
+                         // token's key and value: the first round's cached rows are copied
+                         // before waiting for it
 };
+
+// The token's own key or value chunk cc (8 values) as binary16: into the
+// staged row (swizzled chunk) and the cache.
+__device__ __forceinline__ void ac_put_own(const float* f, __half* dst_smem, __half* dst_cache) {
+  uint4 h;
+  __half2* h2 = reinterpret_cast<__half2*>(&h);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) h2[e] = __floats2half2_rn(f[2 * e], f[2 * e + 1]);
+  *reinterpret_cast<uint4*>(dst_smem) = h;
+  *reinterpret_cast<uint4*>(dst_cache) = h;
+}
 
 __device__ __forceinline__ void ac_cp16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
@@ -174,41 +189,47 @@ __global__ void __launch_bounds__(kAcThreads) attn_mma_kernel(const __grid_const
   for (int r0 = lo; r0 < hi; r0 += R) {
     const int np = hi - r0 < R ? hi - r0 : R;
     const int ntiles = (np + 15) >> 4;
+    // a programmatic dependent launch writes the token's own row of its first
+    // round after the wait (it comes from the kernel ahead of this one)
+    const bool defer_own = a.pdl && r0 == lo;
     // keys, then values, all copies of the round in flight
     for (int i = tid; i < np * cpr; i += kAcThreads) {
       const int tt = i / cpr, cc = i % cpr;
       const size_t src = static_cast<size_t>(r0 + tt) * kv_dim + static_cast<size_t>(g) * hd + cc * 8;
       __half* dst = ks + tt * hd + ((cc ^ (tt & 7)) * 8);
-      if (r0 + tt == own) {
-        const float* f = a.new_k + static_cast<size_t>(g) * hd + cc * 8;
-        uint4 h;
-        __half2* h2 = reinterpret_cast<__half2*>(&h);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) h2[e] = __floats2half2_rn(f[2 * e], f[2 * e + 1]);
-        *reinterpret_cast<uint4*>(dst) = h;
-        *reinterpret_cast<uint4*>(a.kw + src) = h;
-      } else {
+      if (r0 + tt != own)
         ac_cp16(dst, a.k + src);
-      }
+      else if (!defer_own)
+        ac_put_own(a.new_k + static_cast<size_t>(g) * hd + cc * 8, dst, a.kw + src);
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
     for (int i = tid; i < np * cpr; i += kAcThreads) {
       const int tt = i / cpr, cc = i % cpr;
       const size_t src = static_cast<size_t>(r0 + tt) * kv_dim + static_cast<size_t>(g) * hd + cc * 8;
       __half* dst = vs + tt * hd + ((cc ^ (tt & 7)) * 8);
-      if (r0 + tt == own) {
-        const float* f = a.new_v + static_cast<size_t>(g) * hd + cc * 8;
-        uint4 h;
-        __half2* h2 = reinterpret_cast<__half2*>(&h);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) h2[e] = __floats2half2_rn(f[2 * e], f[2 * e + 1]);
-        *reinterpret_cast<uint4*>(dst) = h;
-        *reinterpret_cast<uint4*>(a.vw + src) = h;
-      } else {
+      if (r0 + tt != own)
         ac_cp16(dst, a.v + src);
-      }
+      else if (!defer_own)
+        ac_put_own(a.new_v + static_cast<size_t>(g) * hd + cc * 8, dst, a.vw + src);
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
+    if (r0 == lo && a.pdl) {
+      // the cached rows are on their way: now wait for the kernel that wrote q
+      // and the token's key and value, and only then let the next kernel
+      // start (so it cannot overlap that one)
+      griddep_wait();
+      griddep_launch_dependents();
+      if (own >= r0 && own < r0 + np) {
+        const int tt = own - r0;
+        const size_t src = static_cast<size_t>(own) * kv_dim + static_cast<size_t>(g) * hd;
+        for (int cc = tid; cc < cpr; cc += kAcThreads) {
+          ac_put_own(a.new_k + static_cast<size_t>(g) * hd + cc * 8, ks + tt * hd + ((cc ^ (tt & 7)) * 8),
+                     a.kw + src + cc * 8);
+          ac_put_own(a.new_v + static_cast<size_t>(g) * hd + cc * 8, vs + tt * hd + ((cc ^ (tt & 7)) * 8),
+                     a.vw + src + cc * 8);
+        }
+      }
+    }
     // while the copies fly: value rows of the last tile past the context hold
     // 0 (never stale bits that could be NaN), and on the first round q and the
     // weights' rows of heads past the group are zeroed and q staged
@@ -377,6 +398,10 @@ __global__ void __launch_bounds__(kAcThreads) attn_mma_kernel(const __grid_const
     __syncthreads();   // the round's buffers are free for the next one
   }
 
+  if (a.pdl && lo >= hi) {   // a CTA past the context: nothing was copied early
+    griddep_wait();
+    griddep_launch_dependents();
+  }
   // this CTA's state for the cluster: m and l (hm, hl) and o [group][hd]
 #pragma unroll
   for (int nt = 0; nt < NTV; ++nt) {
@@ -526,19 +551,22 @@ cudaError_t attn_cluster_launch(const float* q, const uint16_t* k, const uint16_
   a.span = (capacity + C - 1) / C;
   a.round = attn_cluster_round(hd);
   a.scale = 1.0f / sqrtf(static_cast<float>(hd));
+  a.pdl = app && app->pdl ? 1 : 0;
   const int group = n_q / n_kv;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C, n_kv);
   cfg.blockDim = dim3(kAcThreads);
   cfg.dynamicSmemBytes = attn_cluster_smem(group, hd);
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = a.pdl ? 2 : 1;
   // score tiles of 8 heads: 1 up to 8 query heads per value head, else 2;
   // value tiles of 8 dimensions per warp: head_dim / 64
   const int ntv = hd / 64;

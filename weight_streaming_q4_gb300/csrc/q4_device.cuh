@@ -251,6 +251,10 @@ struct EngineArgs {
   int stages;              // tagged (and tensor-core engine): ring depth
   int xbuf_floats;         // tagged: floats of the staging buffer after the ring (tensor-core
                            // engine: of the fragment-order input buffer)
+  int pdl;                 // tensor-core engine, programmatic dependent launch: bit 0 = this launch
+                           // may start before the kernel ahead of it ends (the producer streams
+                           // weights at once; the other warps wait for that kernel before they
+                           // touch any data); bit 1 = let the next such launch start early
   Phase one;
 };
 
@@ -460,6 +464,8 @@ struct AttnAppend {
   const float* v;
   const int* pos;
   int* status;
+  int pdl;   // launch as a programmatic dependent of the kernel that wrote q, k and v (the
+             // cached rows of the first round are copied while that kernel finishes)
 };
 cudaError_t attn_launch(const float* q, const uint16_t* k, const uint16_t* v, const int* ctx_len, int capacity,
                         int n_q, int n_kv, int hd, uint16_t* out, void* ws, cudaStream_t s, int ctx_add = 0,
@@ -483,6 +489,8 @@ cudaError_t oneshot_read_status(int* out);
 // phase and event the global timer; n >= 256 * 64 * 6 values.
 cudaError_t tc_timeline_read(unsigned long long* out, size_t n, bool clear);
 cudaError_t tc_engine_prepare();
+// With a.pdl bit 0 the launch carries programmatic stream serialisation (and
+// must not be cooperative).
 cudaError_t tc_engine_launch(const EngineArgs& a, int grid, bool cooperative, cudaStream_t stream);
 cudaError_t tc_engine_read_status(int* out);
 cudaError_t tc_engine_occupancy(int* blocks_per_sm);

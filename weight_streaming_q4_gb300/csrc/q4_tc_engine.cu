@@ -439,6 +439,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_engine_kernel(const __grid_c
     abort_flag = 0;
   }
   __syncthreads();
+  // programmatic dependent launch: the next launch may be scheduled (it waits
+  // for this one before it reads anything this one writes); the weights need
+  // nothing from the launch before this one, everything else does
+  if (a.pdl & 2) griddep_launch_dependents();
+  if ((a.pdl & 1) && warp != kTcProdWarp) griddep_wait();
 
   const unsigned tag0 = tagged ? a.ctl->epoch * kPhasesPerEpoch + 1u : 0u;
 
@@ -646,9 +651,15 @@ cudaError_t tc_engine_launch(const EngineArgs& a, int grid, bool cooperative, cu
   cfg.blockDim = dim3(kTcThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
+  if ((a.pdl & 1) && cooperative) return cudaErrorInvalidValue;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = cooperative ? 1 : 0;
+  if (a.pdl & 1) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+  } else {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = cooperative ? 1 : 0;
+  }
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, tc_engine_kernel, a);
