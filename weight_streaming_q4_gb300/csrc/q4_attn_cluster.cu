@@ -11,7 +11,8 @@
 // steps were long dependent chains (latency-bound), hence the tensor cores.
 //
 // Value head g is one cluster of C CTAs (16 where the GPU schedules clusters
-// that large, else 8); CTA r takes positions [r * span, (r + 1) * span) of the
+// that large and the bucket holds more than 1024 positions, else 8); CTA r
+// takes positions [r * span, (r + 1) * span) of the
 // context, span = capacity / C.  A CTA copies its keys and values into shared
 // memory with 16-byte asynchronous copies, a round of 64 KB (128 positions at
 // head_dim 128) at a time with every copy of the round in flight, and keeps a
@@ -524,12 +525,13 @@ cudaError_t attn_cluster_prepare() {
   return e;
 }
 
-int attn_cluster_size() { return g_ac_cluster; }
-
 cudaError_t attn_cluster_launch(const float* q, const uint16_t* k, const uint16_t* v, const int* ctx_len, int ctx_add,
                                 int capacity, int n_q, int n_kv, int hd, uint16_t* out, const AttnAppend* app,
                                 cudaStream_t s) {
-  const int C = g_ac_cluster;
+  // 16 CTAs per value head where the GPU schedules such clusters, except up to
+  // 1024 positions: there 8 (fewer partial states to combine outweighs the
+  // copies' parallelism; measured on the 8B heads at 512, 1024 and 2048)
+  const int C = g_ac_cluster == 16 && capacity <= 1024 ? 8 : g_ac_cluster;
   if (C != 8 && C != 16) return cudaErrorInitializationError;
   AcArgs a;
   a.q = q;

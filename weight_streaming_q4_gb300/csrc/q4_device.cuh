@@ -450,10 +450,9 @@ cudaError_t poison_launch(uint8_t* buf, size_t n_blocks, cudaStream_t stream);
 cudaError_t stamp_launch(unsigned long long* out, cudaStream_t stream);
 cudaError_t attn_prepare();
 size_t attn_workspace_bytes(int n_q, int n_kv, int hd, int capacity);
-// The cluster attention kernel (q4_attn_cluster.cu): cluster size chosen at
-// prepare time (16 or 8 CTAs per value head).
+// The cluster attention kernel (q4_attn_cluster.cu): prepare decides whether
+// the GPU schedules clusters of 16 CTAs per value head (else 8).
 cudaError_t attn_cluster_prepare();
-int attn_cluster_size();
 // ctx_add: the positions in use are *ctx_len + ctx_add (the decoder passes its
 // position counter and 1).  With `app`, the kernel also stores the token's key
 // and value (fp32 app->k, app->v) as binary16 in row *app->pos of the caches
