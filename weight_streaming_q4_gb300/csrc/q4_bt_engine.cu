@@ -19,10 +19,14 @@
 // is copied once every CTA has published the previous phase).
 //
 // Phases (per layer): q|k|v (v also gathered per head as the context-1
-// attention output), o (+ residual), RMSNorm, gate|up (+ SiLU product), down
-// (+ residual), RMSNorm.  Every phase ends with each CTA publishing a flag;
-// an RMSNorm phase (BT_FORM) sums the per-CTA sums of squares of the residual
-// phase before it in CTA order and normalises its slice of the values.
+// attention output; value rows first, published once they are stored), o
+// (+ residual), RMSNorm, gate|up (+ SiLU product), down (+ residual),
+// RMSNorm; and one RMSNorm of the caller's binary16 state before the first
+// layer.  Every phase ends with each CTA publishing a flag.  An RMSNorm after
+// a residual phase (BT_FORM) is the epilogue warp's: once every CTA has
+// published the residual phase it sums their sums of squares in CTA order and
+// normalises the rows its own CTA produced; the first one is the consumers',
+// each CTA normalising a slice of the rows.
 //
 // The method: PIPO's dequantisation-free 4-bit matrix-vector product for
 // small batches ("PIPO: Pipelined Offloading for Efficient Inference on
@@ -64,7 +68,7 @@ extern __shared__ __align__(128) uint8_t g_bt_smem[];
 // last unit to the epilogue, 4 the epilogue publishes the phase, 5 the producer
 // issues its first input chunk (every CTA has published the phase before).
 // RMSNorm phases: 0 reached, 1 the previous phase seen from every CTA, 2 the
-// slice formed, 4 published.  Other builds compile the stamps away.
+// rows formed, 4 published.  Other builds compile the stamps away.
 #ifdef Q4_TIMELINE
 constexpr int kBtTlCtas = 256, kBtTlPhases = 64, kBtTlEvents = 6;
 __device__ unsigned long long g_bt_tl[kBtTlCtas * kBtTlPhases * kBtTlEvents];

@@ -163,7 +163,8 @@ constexpr unsigned kPhasesPerEpoch = 4096;
 // code unpacking delivers it) and each ring stage carries the chunk of
 // fragments its weights need, copied with one bulk copy.  The phases meet at a
 // flag barrier (all CTAs), and each RMSNorm is its own small phase (BT_FORM):
-// every CTA normalises a slice of the rows' values into the next fragments.
+// every CTA normalises rows' values into the next fragments (after a residual
+// phase the rows it produced there; the first one a slice of the caller's).
 enum BtKind : int {
   BT_PLAIN = 0,   // y = W x; optionally rows [g_lo, g_lo + g_n) gathered per head (context-1 attention)
   BT_RESID = 1,   // y = W x; y2 = t = res + y (fp32); sums of squares of t per CTA and batch row
