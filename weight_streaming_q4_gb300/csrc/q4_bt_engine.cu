@@ -339,8 +339,9 @@ __device__ __forceinline__ void bt_frag_rows(uint8_t* frag, int e_grp, bool ok, 
 
 // The epilogue of unit u for the warp (lane = row of the unit; v: its 8 batch
 // columns; u2: the up row of a gate|up pair; rv: the residual base of a
-// residual phase).  Natural-order outputs per lane, the next phase's
-// fragments per group of four rows.
+// residual phase, whose sums go to t_out and their squares into ss).
+// Natural-order outputs per lane, the next phase's fragments per group of
+// four rows.
 __device__ __forceinline__ void bt_epilogue_unit(const BtPhase& ph, int u, int lane, int batch, int cols,
                                                  const float (&v)[kBtCols], const float (&u2)[kBtCols],
                                                  const unsigned short (&rv)[kBtCols], float (&ss)[kBtCols],
