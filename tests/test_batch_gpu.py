@@ -223,6 +223,24 @@ def test_8b_stack_batch8_full_size(mode):
     prev.close()
 
 
+@pytest.mark.parametrize("mode", [q4.Q4_DEC_FUSED, BT], ids=["per_product", "batched"])
+def test_70b_shape_batch8_two_layers(mode):
+    """70B-shaped layers (hidden 8192, ffn 28672: 4- and 14-chunk rows) at batch
+    8: the second layer checked step by step on sampled rows."""
+    cfg = dict(synth.LLAMA_70B)
+    cfg.pop("n_layers")
+    B, L = 8, 2
+    st = Stack(cfg, L, seed=5, batch=B, mode=mode)
+    prev = Stack(cfg, L - 1, seed=5, batch=B, ptrs=st.ptrs[:-1], mode=mode)
+    h0 = synth.activations(B, cfg["hidden"], 6)
+    prev.run(h0)
+    t_prev = prev.state()["t2"]
+    hL = st.run(h0)
+    check_layer(cfg, 5, L - 1, st.state(), hL, t_prev=t_prev, rows=sampled_rows(64, 3))
+    st.close()
+    prev.close()
+
+
 def test_batched_shape_limits():
     shape = q4.LayerShape.of(**TINY)
     wbuf, ptrs = model.resident_layers(shape, 1, 1)
