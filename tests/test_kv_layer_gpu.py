@@ -118,6 +118,27 @@ def test_tokens_step_by_step(cfg, tokens):
     kv.close()
 
 
+@pytest.mark.parametrize("pos", [200, 1500, 4095])
+def test_long_context_positions(pos):
+    """A 4096-position bucket (clusters of 16 CTAs, 256 positions each, two
+    rounds of 128 at head_dim 128): earlier rows filled with seeded binary16
+    values, the token's row in the second round of CTA 0 (200), of CTA 5
+    (1500) and of the last CTA (4095); the last layer checked step by step."""
+    cfg, L, cap = SMALL, 2, 4096
+    kv = KVStack(cfg, L, seed=130, capacity=cap)
+    for l in range(L):
+        synth.device_fill_normal_f16(kv.kc[l].data_ptr(), cap * cfg["kv_dim"], seed=131, tid=2 * l)
+        synth.device_fill_normal_f16(kv.vc[l].data_ptr(), cap * cfg["kv_dim"], seed=131, tid=2 * l + 1)
+    kv.pos.fill_(pos)
+    torch.cuda.synchronize()
+    kc0, vc0 = kv.cache(L - 1)
+    kv.run(synth.activations(1, cfg["hidden"], 132))
+    kc, vc = kv.cache(L - 1)
+    check_kv_layer(cfg, 130, L - 1, read_ws(kv.ws, kv.offs, cfg), kc, vc, kc0, vc0, pos)
+    assert int(kv.pos.item()) == pos + 1
+    kv.close()
+
+
 def test_chain_against_the_oracle():
     """Three layers, eight tokens (graph and eager calls alternating): the
     GPU's outputs against the oracle's own chain of KV layers (drift gate)."""
