@@ -300,15 +300,18 @@ int q4_decoder_status(q4_decoder *dec, void *stream, int *status_out);
 int q4_decoder_tagged(const q4_decoder *dec, int *tagged_out);
 
 /*
- * Failure-detection hook for tests (tagged decoders, after one decode call):
- * runs the decoder's o-projection phase alone with a wait limit of wait_limit
- * polls.  Its tagged input was written under an earlier epoch, so no word
- * ever carries the tag it waits for: every wait gives up after wait_limit
- * polls, the kernel sets status bit 16 (a tagged input never arrived) and
- * returns.  The call synchronises `stream`, reads and clears the status word
- * into *status_out, and clears the tagged words so that the next decode call
- * runs normally.  Errors: Q4_ERR_ARG (not a tagged decoder, no decode call
- * yet, wait_limit 0), Q4_ERR_CUDA.
+ * Failure-detection hook for tests (tagged decoders and the batched engine,
+ * after one decode call): runs the decoder's o-projection phase alone with a
+ * wait limit of wait_limit polls.  Its tagged input was written under an
+ * earlier epoch, so no word ever carries the tag it waits for: every wait
+ * gives up after wait_limit polls, the kernel sets status bit 16 (a tagged
+ * input never arrived) and returns.  The batched engine runs its first
+ * layer's q|k|v and o phases with every awaited flag tag one epoch ahead:
+ * the flag waits give up (status bit 1) and the stage waits behind them
+ * (bits 2 and 8).  The call synchronises `stream`, reads and clears the status
+ * word into *status_out, and clears the tagged words (the flags) so that the
+ * next decode call runs normally.  Errors: Q4_ERR_ARG (neither kind of
+ * decoder, no decode call yet, wait_limit 0), Q4_ERR_CUDA.
  */
 int q4_decoder_debug_stall(q4_decoder *dec, uint32_t wait_limit, void *stream, int *status_out);
 

@@ -241,6 +241,20 @@ def test_70b_shape_batch8_two_layers(mode):
     prev.close()
 
 
+def test_batched_engine_wait_runs_out_and_reports():
+    """Flags that never carry the awaited tag: every wait of the batched engine
+    gives up after its poll limit, the status word reports it (bit 1), and the
+    decoder stays usable (the next token equals the first)."""
+    st = Stack(TINY, 2, seed=44, batch=4, mode=BT)
+    h0 = synth.activations(4, TINY["hidden"], 45)
+    a = st.run(h0)
+    status = q4.q4_decoder_debug_stall(st.dec, 2000)
+    assert status & 1
+    b = st.run(h0)
+    assert np.array_equal(a, b)
+    st.close()
+
+
 def test_batched_shape_limits():
     shape = q4.LayerShape.of(**TINY)
     wbuf, ptrs = model.resident_layers(shape, 1, 1)

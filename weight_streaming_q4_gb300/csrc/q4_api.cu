@@ -920,16 +920,18 @@ bool bt_stack_program(const q4_layer_shape& s, const std::vector<const uint8_t*>
   return true;
 }
 
-// Phases [first, first + n) of the batched program in the workspace.
+// Phases [first, first + n) of the batched program in the workspace (stall:
+// BtArgs::stall, with its own wait limit).
 int launch_bt(const Work& w, int first, int n, int grid, int batch, bool end, const q4_layer_shape& s,
-              cudaStream_t st) {
+              cudaStream_t st, uint32_t stall = 0, uint32_t wait_limit = kWaitLimit) {
   q4::BtArgs a;
   memset(&a, 0, sizeof(a));
   a.phases = reinterpret_cast<const q4::BtPhase*>(w.prog) + first;
   a.n_phases = n;
   a.ctl = w.ctl;
   a.flags = w.flags;
-  a.wait_limit = kWaitLimit;
+  a.wait_limit = wait_limit;
+  a.stall = stall;
   a.batch = batch;
   a.cols = q4::bt_cols(batch);
   a.end_of_program = end ? 1 : 0;
@@ -1262,8 +1264,20 @@ extern "C" int q4_decoder_status(q4_decoder* d, void* stream, int* status_out) {
 }
 
 extern "C" int q4_decoder_debug_stall(q4_decoder* d, uint32_t wait_limit, void* stream, int* status_out) {
-  if (!d || !status_out || !d->tagged || !d->cur_h || wait_limit < 1) return Q4_ERR_ARG;
+  if (!d || !status_out || !d->cur_h || wait_limit < 1) return Q4_ERR_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (d->engine == ENG_BT) {
+    // the first layer's q|k|v and o phases alone, every awaited flag tag an
+    // epoch ahead: the o phase's input is never released, every wait runs out
+    int st = launch_bt(d->w, 1, 2, d->grid, d->batch, false, d->shape, s, q4::kPhasesPerEpoch, wait_limit);
+    if (st != Q4_OK) return st;
+    if ((st = read_status(d->w.ctl, s, status_out)) != Q4_OK) return st;
+    // the launch published flags of this epoch: clear them
+    Q4_CUDA(cudaMemsetAsync(d->w.flags, 0, 2 * q4::kMaxGrid * sizeof(unsigned long long), s));
+    Q4_CUDA(cudaStreamSynchronize(s));
+    return Q4_OK;
+  }
+  if (!d->tagged) return Q4_ERR_ARG;
   // the o-projection phase alone: its tagged input (v) was written under an
   // earlier epoch, so no word ever carries the tag it waits for
   int st = launch_layers(d->w, 1, 1, d->grid, s, d->engine, true, false, d->shape, wait_limit);

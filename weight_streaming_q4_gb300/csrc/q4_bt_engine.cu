@@ -417,7 +417,7 @@ __device__ void bt_form_rows(const BtArgs& a, int p, unsigned tag0, int lane, co
   const int G = static_cast<int>(gridDim.x), cta = static_cast<int>(blockIdx.x);
   const int u0 = bt_first_unit(rp, cta, G);
   if (u0 >= rp.units) return;
-  bt_wait_flags(a.flags, tag0 + static_cast<unsigned>(rp.gidx), lane, a.wait_limit, a.ctl);
+  bt_wait_flags(a.flags, tag0 + a.stall + static_cast<unsigned>(rp.gidx), lane, a.wait_limit, a.ctl);
   if (lane == 0) bt_stamp(ph.gidx, 1);
   // the 8 partials of CTA c are contiguous: two 16-byte loads, all of the
   // lane's CTAs in flight together
@@ -553,7 +553,8 @@ __global__ void __launch_bounds__(kBtThreads, 1) bt_engine_kernel(const __grid_c
         }
       }
       if (nx < nw) {
-        if (xp > ready && bt_flags_seen(a.flags, tag0 + static_cast<unsigned>(a.phases[xp - 1].gidx), lane)) {
+        if (xp > ready &&
+            bt_flags_seen(a.flags, tag0 + a.stall + static_cast<unsigned>(a.phases[xp - 1].gidx), lane)) {
           ready = xp;
           fence_acq_rel_gpu();
           fence_proxy_async_global();
@@ -634,7 +635,8 @@ __global__ void __launch_bounds__(kBtThreads, 1) bt_engine_kernel(const __grid_c
       // the residual base was written by other CTAs before they published the
       // phases up to the previous one: seen here, before its loads are issued
       if (ph.kind == BT_RESID && p > 0 && u0 < ph.units)
-        bt_wait_flags(a.flags, tag0 + static_cast<unsigned>(a.phases[p - 1].gidx), lane, a.wait_limit, a.ctl);
+        bt_wait_flags(a.flags, tag0 + a.stall + static_cast<unsigned>(a.phases[p - 1].gidx), lane, a.wait_limit,
+                      a.ctl);
       for (int u = u0, ord = 0; u < ph.units; u += G, ++ord) {
         const int n = dual ? u * (kTcUnitRows / 2) + lane : u * kTcUnitRows + lane;
         const bool row_ok = (!dual || lane < kTcUnitRows / 2) && n < ph.n_rows;
@@ -713,7 +715,8 @@ __global__ void __launch_bounds__(kBtThreads, 1) bt_engine_kernel(const __grid_c
       if (ph.kind == BT_FORM && ph.src32) continue;   // the epilogue warp's
       if (ph.kind == BT_FORM) {
         if (p > 0 && warp == 0)
-          bt_wait_flags(a.flags, tag0 + static_cast<unsigned>(a.phases[p - 1].gidx), lane, a.wait_limit, a.ctl);
+          bt_wait_flags(a.flags, tag0 + a.stall + static_cast<unsigned>(a.phases[p - 1].gidx), lane, a.wait_limit,
+                      a.ctl);
         named_bar_sync(1, kBtConsumers);
         if (tid == 0) bt_stamp(ph.gidx, 1);
         bt_form16(ph, a.batch, a.cols, rsm, red_cta, tid);

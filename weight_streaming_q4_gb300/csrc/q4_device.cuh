@@ -223,6 +223,8 @@ struct BtArgs {
   int batch;
   int cols;                 // bt_cols(batch): columns of the fragment buffers
   int end_of_program;       // the last CTA to leave advances the epoch
+  uint32_t stall;           // failure-detection hook: added to every awaited flag tag (0 normally;
+                            // kPhasesPerEpoch: a tag no CTA publishes, so every such wait runs out)
 };
 
 cudaError_t bt_engine_prepare();
