@@ -150,8 +150,11 @@ namespace {
 // Per stream, the y ranges of the one-shot products that may still be running
 // when the next one starts early: a launch that starts early may overlap every
 // such product before it (each started early in turn), so the chain is kept
-// until a launch that waits for its predecessor as usual ends it.
-constexpr int kOsChain = 8;
+// until a launch that waits for its predecessor as usual ends it.  A full
+// chain ends too: 64 entries, so that a ring of a few dozen independent
+// products runs without a drained launch between them (one every 8 launches
+// cost 0.3 us per product on N = K = 4096).
+constexpr int kOsChain = 64;
 struct Chain {
   cudaStream_t stream;
   int n;
