@@ -193,6 +193,34 @@ def test_oneshot_input_from_the_previous_output():
     assert np.array_equal(host_f32(y2), ref[0], equal_nan=True)
 
 
+def test_oneshot_long_chain_then_a_dependent_product():
+    """80 independent one-shot products into distinct slices of one buffer
+    (more than the launcher's list of early-started products holds, so the
+    list is ended and restarted on the way), then a product whose x is the
+    memory of eight late slices: it must wait and see those slices whole."""
+    n, k, count, first = 256, 4096, 80, 66           # x of the last product: slices 66..73
+    w1 = synth.q4_matrix(n, k, 30, synth.GEMV_TID)
+    w2 = synth.q4_matrix(n, k, 32, synth.GEMV_TID)
+    xs = synth.activations(1, k, 31)
+    d1, d2, dx = dev_u8(w1), dev_u8(w2), dev_u16(xs.reshape(-1))
+    ys = torch.empty(count * n, dtype=torch.float32, device="cuda")
+    y2 = torch.empty(n, dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            ys.fill_(0.0)
+            for i in range(count):
+                q4.q4_gemv_ex(d1, dx, ys[i * n:(i + 1) * n], n, k, 1, q4.Q4_KERNEL_ONESHOT, stream=s)
+            q4.q4_gemv_ex(d2, ys[first * n:(first + 8) * n], y2, n, k, 1, q4.Q4_KERNEL_ONESHOT, stream=s)
+        s.synchronize()
+    y1 = run(w1, xs, n, k, 1, q4.Q4_KERNEL_ONESHOT)[0]
+    assert np.array_equal(host_f32(ys).reshape(count, n), np.broadcast_to(y1, (count, n)))
+    x2 = ys[first * n:(first + 8) * n].detach().cpu().view(torch.int16).numpy().view(np.uint16).copy()
+    ref = run(w2, x2, n, k, 1, q4.Q4_KERNEL_ONESHOT)
+    assert np.array_equal(host_f32(y2), ref[0], equal_nan=True)
+    assert q4.q4_device_status() == 0
+
+
 def test_tc_engine_rejects_unsupported_widths():
     x = torch.zeros(32768, dtype=torch.int16, device="cuda")
     y = torch.zeros(64, dtype=torch.float32, device="cuda")
