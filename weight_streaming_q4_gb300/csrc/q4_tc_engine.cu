@@ -216,35 +216,52 @@ __device__ __forceinline__ float stage_norm(const Phase& ph, uint32_t want, uint
 // Tagged binary16 words (X_TAG16: x = the k values; X_TAG16_ATTN: the xt_n
 // values of v, each 4-value chunk of a value head copied to the `group` query
 // heads that read it) polled until every tag is `want16`, into the fragment
-// buffer.  Each pass reloads all of the thread's chunks and stores them.
+// buffer.
 __device__ __forceinline__ void stage_tag16(const Phase& ph, uint8_t* xf, uint32_t want16, uint32_t limit, Control* ctl,
                                             int tid, bool cta0) {
   const bool attn = ph.x_kind == X_TAG16_ATTN;
   const int n4 = (attn ? ph.xt_n : ph.k) >> 2;
   const uint4* src = static_cast<const uint4*>(ph.x_src);
   const uint32_t want = want16 << 16;
-  bool ok = false;
-  for (uint32_t it = 0; it < limit && !ok; ++it) {
-    ok = true;
-    // loads without a compiler memory barrier: the unrolled loop keeps
-    // several in flight ahead of the shared-memory stores
-#pragma unroll 4
-    for (int i = tid; i < n4; i += kTcConsumers) {
-      const uint4 w = ld_relaxed_v4_nb(src + i);
-      ok &= (((w.x ^ want) | (w.y ^ want) | (w.z ^ want) | (w.w ^ want)) >> 16) == 0u;
-      const uint32_t h01 = __byte_perm(w.x, w.y, 0x5410), h23 = __byte_perm(w.z, w.w, 0x5410);
-      const int e = 4 * i;
-      if (!attn) {
-        frag_store4(xf, e, h01, h23);
-      } else {
-        const int hd = ph.head_dim;
-        const int x0 = (e / hd) * ph.group * hd + e % hd;
-        for (int h = 0; h < ph.group; ++h) frag_store4(xf, x0 + h * hd, h01, h23);
+  // The thread's chunks in batches of 4, each batch polled until its tags
+  // match before the next is read: the values arrive roughly in row order,
+  // so once the last ones land only the last batches are still to be read.
+  bool all_ok = true;
+  for (int i0 = tid; i0 < n4; i0 += 4 * kTcConsumers) {
+    uint32_t lo[4], hi[4];
+    bool ok;
+    uint32_t it = 0;
+    do {   // at least one read, so lo and hi always hold the loaded words
+      ok = true;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int i = i0 + j * kTcConsumers;
+        if (i < n4) {
+          const uint4 w = ld_relaxed_v4_nb(src + i);
+          ok &= (((w.x ^ want) | (w.y ^ want) | (w.z ^ want) | (w.w ^ want)) >> 16) == 0u;
+          lo[j] = __byte_perm(w.x, w.y, 0x5410);
+          hi[j] = __byte_perm(w.z, w.w, 0x5410);
+        }
+      }
+      if (!ok && it >= 2) __nanosleep(32);
+    } while (!ok && ++it < limit);
+    all_ok &= ok;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = i0 + j * kTcConsumers;
+      if (i < n4) {
+        const int e = 4 * i;
+        if (!attn) {
+          frag_store4(xf, e, lo[j], hi[j]);
+        } else {
+          const int hd = ph.head_dim;
+          const int x0 = (e / hd) * ph.group * hd + e % hd;
+          for (int h = 0; h < ph.group; ++h) frag_store4(xf, x0 + h * hd, lo[j], hi[j]);
+        }
       }
     }
-    if (!ok && it >= 2) __nanosleep(32);
   }
-  if (!ok) tc_set_status(ctl, ST_DATA_TIMEOUT);
+  if (!all_ok) tc_set_status(ctl, ST_DATA_TIMEOUT);
   if (cta0 && (ph.x_dbg || ph.xr_out)) {
     // The formed x in natural order.  Its chunks were polled by other threads:
     // after the barrier every word carries its tag (re-checked, bounded).
