@@ -130,21 +130,31 @@ __device__ __forceinline__ void store_formed4(const Phase& ph, int e, uint32_t h
   }
 }
 
-// Warp 0: wait until every CTA's phase flag carries `tag` or a later one
-// (the tagged programs' once-per-layer exchange; the flags' low words are
-// unused), bounded by `limit` polls.
-__device__ __forceinline__ void tc_wait_flags(const unsigned long long* flags, unsigned tag, int lane, uint32_t limit,
-                                              Control* ctl) {
+// The consumer threads together: wait until every CTA's phase flag carries
+// `tag` or a later one.  Thread i reads flag i (one load per thread, all in
+// flight at once) and the CTA decides by one barrier reduction per poll, so
+// every thread polls as often as the others (a thread whose own limit has run
+// out votes to stop); the longest limit bounds the wait.  Each thread fences
+// after it, before any later access.
+__device__ __forceinline__ void tc_wait_flags_cta(const unsigned long long* flags, unsigned tag, int tid,
+                                                  uint32_t limit, Control* ctl) {
   const int G = static_cast<int>(gridDim.x);
-  bool ok = false;
-  for (uint32_t it = 0; it < limit && !ok; ++it) {
-    bool mine = true;
-    for (int i = lane; i < G; i += 32)
-      mine &= static_cast<int>(static_cast<unsigned>(ld_relaxed_u64(flags + i) >> 32) - tag) >= 0;
-    ok = __all_sync(0xffffffffu, mine);
-    if (!ok && it > 16) __nanosleep(64);
+  bool mine = false;
+  for (uint32_t it = 0;; ++it) {
+    mine = tid >= G || static_cast<int>(static_cast<unsigned>(ld_relaxed_u64(flags + tid) >> 32) - tag) >= 0;
+    uint32_t stop;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, 1, %2, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(stop)
+        : "r"(static_cast<uint32_t>(mine || it + 1 >= limit)), "n"(kTcConsumers)
+        : "memory");
+    if (stop) break;
+    if (it > 16) __nanosleep(64);
   }
-  if (!ok && lane == 0) tc_set_status(ctl, ST_FLAG_TIMEOUT);
+  if (!mine) tc_set_status(ctl, ST_FLAG_TIMEOUT);
   __threadfence();
 }
 
@@ -153,15 +163,15 @@ __device__ __forceinline__ void tc_wait_flags(const unsigned long long* flags, u
 // fp32 words are polled until every tag is `want`; a plain binary16 input is
 // read once.  The sum of squares runs over each thread's chunks in order,
 // then the warp tree, then the 8 warps in order: an order fixed by k alone.
-// With `flags` set, warp 0 first waits for the layer's phase flags (tag
-// flag_tag) while the other warps already poll the input: the flags guard the
-// phase's first tagged write, which follows the reduction's barrier.
+// With `flags` set, the consumers first wait for the layer's phase flags (tag
+// flag_tag): the flags guard the phase's first tagged write, which follows
+// the reduction's barrier.
 // Returns the scale 1 / sqrt(mean(t^2) + eps); v holds the values.
 __device__ __forceinline__ float stage_norm(const Phase& ph, uint32_t want, uint32_t limit, Control* ctl, float* red_cta,
                                             int tid, float (&v)[kTcNormChunks][4], const unsigned long long* flags,
                                             unsigned flag_tag) {
   const int n4 = ph.k >> 2;
-  if (flags && tid < 32) tc_wait_flags(flags, flag_tag, tid, limit, ctl);
+  if (flags) tc_wait_flags_cta(flags, flag_tag, tid, limit, ctl);
   if (ph.x_kind == X_NORM16) {
 #pragma unroll
     for (int c = 0; c < kTcNormChunks; ++c) {
@@ -299,9 +309,8 @@ __device__ __forceinline__ void stage_plain16(const Phase& ph, uint8_t* xf, int 
 __device__ __noinline__ void tc_prologue(const Phase& ph, unsigned tag, uint32_t lim, Control* ctl,
                                          const unsigned long long* flags, uint8_t* xf, float* red_cta, int tid,
                                          bool cta0) {
-  const int warp = tid >> 5, lane = tid & 31;
   const bool norm = ph.x_kind == X_NORM16 || ph.x_kind == X_TAG32_NORM;
-  if (ph.sync == SYNC_WAIT && !norm && warp == 0) tc_wait_flags(flags, tag - 1u, lane, lim, ctl);
+  if (ph.sync == SYNC_WAIT && !norm) tc_wait_flags_cta(flags, tag - 1u, tid, lim, ctl);
   if (ph.sync == SYNC_WAIT && !norm) named_bar_sync(1, kTcConsumers);
   if (norm) {
     float v[kTcNormChunks][4];
