@@ -305,7 +305,9 @@ int q4_decoder_tagged(const q4_decoder *dec, int *tagged_out);
  * wait limit of wait_limit polls.  Its tagged input was written under an
  * earlier epoch, so no word ever carries the tag it waits for: every wait
  * gives up after wait_limit polls, the kernel sets status bit 16 (a tagged
- * input never arrived) and returns.  The batched engine runs its first
+ * input never arrived) and returns.  The tensor-core engine first runs the
+ * gate|up phase alone: its wait for the o phase's flags of the current epoch
+ * (never published) gives up too (bit 1).  The batched engine runs its first
  * layer's q|k|v and o phases with every awaited flag tag one epoch ahead:
  * the flag waits give up (status bit 1) and the stage waits behind them
  * (bits 2 and 8).  The call synchronises `stream`, reads and clears the status

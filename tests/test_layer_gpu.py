@@ -156,13 +156,16 @@ def test_wide_hidden_falls_back_to_flag_program():
 @pytest.mark.parametrize("engine", ["tc", "core"])
 def test_tagged_wait_runs_out_and_reports(engine):
     """A tagged input that never arrives: every wait gives up after its poll
-    limit, the status word carries bit 16, and the context and the decoder
+    limit, the status word carries bit 16 (and, on the tensor-core engine, bit
+    1 for a phase-flag wait that ran out), and the context and the decoder
     stay usable (the next token is exact)."""
     st = Stack(TINY, 2, seed=42, mode=q4.Q4_DEC_FUSED | ENGINES[engine])
     h0 = synth.activations(1, TINY["hidden"], 43)
     a = st.run(h0)
     status = q4.q4_decoder_debug_stall(st.dec, 2000)
     assert status & 16
+    if engine == "tc":
+        assert status & 1
     b = st.run(h0)
     assert np.array_equal(a, b)
     st.close()

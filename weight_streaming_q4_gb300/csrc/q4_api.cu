@@ -1278,9 +1278,16 @@ extern "C" int q4_decoder_debug_stall(q4_decoder* d, uint32_t wait_limit, void* 
     return Q4_OK;
   }
   if (!d->tagged) return Q4_ERR_ARG;
+  int st;
+  if (d->engine == ENG_TC) {
+    // the gate|up phase alone first: it waits for the o phase's flags of this
+    // epoch, which no CTA has published, and for its tagged input (t1)
+    st = launch_layers(d->w, 2, 1, d->grid, s, d->engine, true, false, d->shape, wait_limit);
+    if (st != Q4_OK) return st;
+  }
   // the o-projection phase alone: its tagged input (v) was written under an
   // earlier epoch, so no word ever carries the tag it waits for
-  int st = launch_layers(d->w, 1, 1, d->grid, s, d->engine, true, false, d->shape, wait_limit);
+  st = launch_layers(d->w, 1, 1, d->grid, s, d->engine, true, false, d->shape, wait_limit);
   if (st != Q4_OK) return st;
   if ((st = read_status(d->w.ctl, s, status_out)) != Q4_OK) return st;
   // the launch left words under live tags: clear them and the flags
