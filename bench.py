@@ -194,6 +194,7 @@ def time_region(torch, stream, fn, steps, warmup, barrier, gpu_index):
 
 def run_stack(args, torch, q4, model, synth, stream, barrier, gpu_index):
     cfg, n_layers = stack_cfg(args.config)
+    full_layers = n_layers
     if args.layers:
         n_layers = args.layers   # a shorter stack of the same shape (small profiling case)
     B = args.batch
@@ -251,10 +252,12 @@ def run_stack(args, torch, q4, model, synth, stream, barrier, gpu_index):
                           f"batch {B}, HBM-resident, one CUDA-graph replay per step"),
                 kernel=(("engine_kernel" if args.barrier or args.cuda_core else "tc_engine_kernel") if B == 1
                         else "bt_engine_kernel" if batched else "mma_kernel"),
-                kernel_key=((f"engine_kernel:{args.config}_stack" if args.barrier or args.cuda_core
-                             else f"tc_engine_kernel:{args.config}_stack") if B == 1
-                            else f"bt_engine_kernel:{args.config}_stack_b{B}" if batched
-                            else f"mma_kernel:{args.config}_stack_b{B}"),
+                # the traffic records are for the whole stack: none for fewer layers
+                kernel_key=(((f"engine_kernel:{args.config}_stack" if args.barrier or args.cuda_core
+                              else f"tc_engine_kernel:{args.config}_stack") if B == 1
+                             else f"bt_engine_kernel:{args.config}_stack_b{B}" if batched
+                             else f"mma_kernel:{args.config}_stack_b{B}")
+                            if n_layers == full_layers else None),
                 n_layers=n_layers, cfg=cfg, tagged=tagged)
 
 
