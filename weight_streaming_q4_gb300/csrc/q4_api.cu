@@ -193,6 +193,12 @@ bool tc_geom(std::initializer_list<int> ks, TcGeom* g) {
 
 }  // namespace
 
+namespace q4 {
+bool encode_q4_rows(CUtensorMap* m, const uint8_t* w, int n_rows, int k, int box_rows) {
+  return encode_rows(m, w, n_rows, k, box_rows);
+}
+}  // namespace q4
+
 // ===================================================================== misc
 
 extern "C" const char* q4_status_string(int s) {

@@ -520,6 +520,10 @@ cudaError_t mma_launch(const uint8_t* w, const uint16_t* x, float* y, int n, int
                        uint32_t wait_limit, int* status, cudaStream_t stream, float* y2 = nullptr, int split = 0,
                        bool pdl = false, const MmaGather* gather = nullptr, uint16_t* act = nullptr);
 cudaError_t mma_read_status(int* out);
+// Host: the TMA descriptor of a row-major Q4_0 matrix (n_rows x k; 64-bit
+// elements, box tc_pitch(k) / 8 columns by box_rows rows); false if the
+// driver cannot encode it.
+bool encode_q4_rows(CUtensorMap* m, const uint8_t* w, int n_rows, int k, int box_rows);
 // Glue launches; pdl as for mma_launch (each glue kernel waits for its inputs first).
 cudaError_t glue_norm(const uint16_t* src16, const float* src32, int batch, int dim, float eps, uint16_t* z,
                       cudaStream_t s, bool pdl = false);

@@ -12,9 +12,10 @@
 // serves batch sizes below 16).
 //
 // Persistent, one CTA per SM, 17 warps: warp 16 streams 16-row x 2048-column
-// tiles of the weights into a ring of shared-memory stages with 1-D bulk TMA
-// copies (one per row segment, rows padded to keep the code-word loads free of
-// bank conflicts); warps 0-15 each take 4 of the stage's 64 blocks.  A CTA
+// tiles of the weights into a ring of shared-memory stages (rows padded to
+// keep the code-word loads free of bank conflicts), with one 2-D tensor copy
+// per stage and matrix where the rows are whole chunks, else a 1-D bulk copy
+// per row segment; warps 0-15 each take 4 of the stage's 64 blocks.  A CTA
 // takes its row tiles in groups (8 tiles at batch <= 8, 4 above): chunk by
 // chunk, the x fragments of a warp's blocks are loaded once for the whole
 // group, every tile's partial sums stay in registers, and each tile is summed
@@ -37,6 +38,8 @@ constexpr int kMmaStageBytes = 16 * kMmaRowPitch;                  // 18688 B
 constexpr int kMmaStages = 10;
 
 struct MmaArgs {
+  CUtensorMap tm;     // with use_tm: the weights' TMA descriptor (box 146 x 16 rows, 8 when paired)
+  int use_tm;
   const uint8_t* w;   // Q4_0 [n][k/32]
   const __half* x;    // binary16 [batch][k]
   float* y;           // fp32 [batch][split]: rows below `split`
@@ -104,6 +107,16 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const __grid_consta
               break;
             }
             uint8_t* dst = g_mma_ring + static_cast<size_t>(stage) * kMmaStageBytes;
+            if (a.use_tm) {
+              // one 2-D tensor copy per matrix: the whole padded stage (rows past
+              // the matrix read as zeros, and count in full)
+              const int cx = c * (kMmaChunkBlocks * kBlockBytes / 8);
+              mbar_arrive_expect_tx(&full_bar[stage], kMmaStageBytes);
+              tma_load_2d(dst, &a.tm, cx, row0, &full_bar[stage]);
+              if (paired) tma_load_2d(dst + 8 * kMmaRowPitch, &a.tm, cx, half + row0, &full_bar[stage]);
+              ++it;
+              continue;
+            }
             mbar_arrive_expect_tx(&full_bar[stage], seg * rows * (paired ? 2 : 1));
             for (int r = 0; r < rows; ++r)
               bulk_g2s(dst + r * kMmaRowPitch, a.w + static_cast<size_t>(row0 + r) * row_bytes + blk0 * kBlockBytes,
@@ -291,6 +304,15 @@ cudaError_t mma_launch(const uint8_t* w, const uint16_t* x, float* y, int n, int
   a.k = k;
   a.batch = batch;
   a.wait_limit = wait_limit;
+  // rows of whole 2048-column chunks, more than one (the descriptor's box is
+  // then the padded 1168-byte stage row), one n-tile: one tensor copy per
+  // stage (and matrix) instead of a bulk copy per row, which bounded the
+  // producer (at two n-tiles the consumers bound it and the row copies were
+  // measured faster)
+  a.use_tm = batch <= 8 && k % (kMmaChunkBlocks * kQK) == 0 && tc_pitch(k) == kMmaRowPitch &&
+                     encode_q4_rows(&a.tm, w, n, k, act ? 8 : 16)
+                 ? 1
+                 : 0;
   const int tiles = act ? (n / 2 + 7) / 8 : (n + 15) / 16;
   if (grid > tiles) grid = tiles;
   cudaLaunchConfig_t cfg = {};
