@@ -2,15 +2,18 @@
 // launch path for a single product (q4_gemv), without the persistent
 // engine's ring, warp roles or phase program.
 //
-// Each CTA takes a tile of 16 rows over the full width k.  One thread issues
-// every row of the tile as two 1-D bulk copies (the two halves of the row,
-// each counted on its own mbarrier) as soon as the CTA starts, so all of the
-// tile's bytes are in flight at once; the rows land at a pitch of row bytes +
-// 16 so that the code-word loads of the 8 row groups fall in different banks.
+// Each CTA takes a tile of 16 rows over the full width k.  As soon as the CTA
+// starts, one thread puts all of the tile's bytes in flight: where the rows
+// are whole 2048-column chunks (at least two), one 2-D tensor copy per chunk,
+// each counted on its own mbarrier, the rows of a chunk landing at a padded
+// 1168-byte pitch; otherwise every row as two 1-D bulk copies (its two
+// halves, on two mbarriers) at a pitch of row bytes + 16.  Either padding puts
+// the code-word loads of the 8 row groups in different banks.
 // Meanwhile the 256 threads stage x in fragment order.  The 8 warps split the
 // width: warp w takes block pairs [w * pp, (w + 1) * pp) and runs the exact
 // binary16 (q - 8) unpack and mma.sync m16n8k16 of the persistent engine on
-// them (q4_frag.cuh), waiting only for the half of the row its pairs lie in.
+// them (q4_frag.cuh), waiting only for the chunks (or half) of the row its
+// pairs lie in.
 // The warps' partial sums meet in shared memory and are added in warp order
 // (a fixed order: the result does not depend on timing).
 //
@@ -40,6 +43,22 @@ namespace {
 constexpr int kOsWarps = 8;
 constexpr int kOsThreads = kOsWarps * 32;
 constexpr int kOsRows = 16;
+// Rows of whole 2048-column chunks, more than one: the tile is staged chunk by
+// chunk, each chunk one 2-D tensor copy of 16 rows at a padded 1168-byte
+// pitch (the copy's box: 146 64-bit columns, the last 16 bytes of a row
+// belonging to the next chunk or read as zeros past the row's end).
+constexpr int kOsChunkPitch = 64 * kBlockBytes + 16;
+constexpr int kOsChunkBytes = kOsRows * kOsChunkPitch;
+constexpr int kOsMaxChunks = 12;
+
+struct OsArgs {
+  CUtensorMap tm;     // TM: the weights' descriptor (box 146 64-bit columns by 16 rows)
+  const uint8_t* w;
+  const __half* x;
+  float* y;
+  int n, k;
+  uint32_t wait_limit;
+};
 
 __device__ int g_status_os;   // status bits (a copy that never landed)
 
@@ -56,17 +75,23 @@ __device__ __forceinline__ void os_stage_x(const __half* x, uint8_t* xf, int k, 
 
 }  // namespace
 
-__global__ void __launch_bounds__(kOsThreads, 2) oneshot_kernel(const uint8_t* __restrict__ w, const __half* x,
-                                                                float* y, int n, int k, uint32_t wait_limit) {
+template <bool TM>
+__global__ void __launch_bounds__(kOsThreads, 2) oneshot_kernel(const __grid_constant__ OsArgs a) {
   extern __shared__ __align__(128) uint8_t sm[];
-  __shared__ __align__(8) uint64_t bar[2];
+  __shared__ __align__(8) uint64_t bar[TM ? kOsMaxChunks : 2];
+  const uint8_t* __restrict__ w = a.w;
+  const __half* x = a.x;
+  float* y = a.y;
+  const int n = a.n, k = a.k;
+  const uint32_t wait_limit = a.wait_limit;
+  const int chunks = TM ? k >> 11 : 2;   // TM: 2048-column chunks; else the two halves of each row
   __shared__ float part[kOsWarps][kOsRows];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int row_bytes = (k >> 5) * kBlockBytes, half = row_bytes >> 1, pitch = row_bytes + 16;
   const int n0 = blockIdx.x * kOsRows;
   const int rows = n - n0 < kOsRows ? n - n0 : kOsRows;
   uint8_t* xf = sm;                          // k * 2 bytes, fragment order
-  uint8_t* tile = sm + 2 * k;                // 16 rows at `pitch`
+  uint8_t* tile = sm + 2 * k;                // 16 rows at `pitch` (TM: chunk by chunk)
 
   griddep_launch_dependents();
   // Everything but the store of y runs before the wait for the kernel before
@@ -74,15 +99,22 @@ __global__ void __launch_bounds__(kOsThreads, 2) oneshot_kernel(const uint8_t* _
   // it writes nothing but its y, and the launcher starts this kernel early
   // only when w and x do not overlap that y.
   if (tid == 0) {
-    mbar_init(&bar[0], 1);
-    mbar_init(&bar[1], 1);
+    for (int c = 0; c < chunks; ++c) mbar_init(&bar[c], 1);
     fence_mbar_init();
-    mbar_arrive_expect_tx(&bar[0], static_cast<uint32_t>(rows) * half);
-    mbar_arrive_expect_tx(&bar[1], static_cast<uint32_t>(rows) * half);
-    for (int r = 0; r < rows; ++r) {
-      const uint8_t* src = w + static_cast<size_t>(n0 + r) * row_bytes;
-      bulk_g2s(tile + r * pitch, src, half, &bar[0]);
-      bulk_g2s(tile + r * pitch + half, src + half, half, &bar[1]);
+    if (TM) {
+      // rows past n read as zeros and count in full
+      for (int c = 0; c < chunks; ++c) {
+        mbar_arrive_expect_tx(&bar[c], kOsChunkBytes);
+        tma_load_2d(tile + c * kOsChunkBytes, &a.tm, c * (64 * kBlockBytes / 8), n0, &bar[c]);
+      }
+    } else {
+      mbar_arrive_expect_tx(&bar[0], static_cast<uint32_t>(rows) * half);
+      mbar_arrive_expect_tx(&bar[1], static_cast<uint32_t>(rows) * half);
+      for (int r = 0; r < rows; ++r) {
+        const uint8_t* src = w + static_cast<size_t>(n0 + r) * row_bytes;
+        bulk_g2s(tile + r * pitch, src, half, &bar[0]);
+        bulk_g2s(tile + r * pitch + half, src + half, half, &bar[1]);
+      }
     }
   }
   os_stage_x(x, xf, k, tid);
@@ -97,16 +129,21 @@ __global__ void __launch_bounds__(kOsThreads, 2) oneshot_kernel(const uint8_t* _
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   bool ok = true;
   if (p0 < p1) {
-    if (2 * p0 < pairs) ok &= mbar_wait_bounded(&bar[0], 0, wait_limit);
-    if (2 * p1 > pairs) ok &= mbar_wait_bounded(&bar[1], 0, wait_limit);
+    if (TM) {
+      for (int c = p0 >> 5; c <= (p1 - 1) >> 5; ++c) ok &= mbar_wait_bounded(&bar[c], 0, wait_limit);
+    } else {
+      if (2 * p0 < pairs) ok &= mbar_wait_bounded(&bar[0], 0, wait_limit);
+      if (2 * p1 > pairs) ok &= mbar_wait_bounded(&bar[1], 0, wait_limit);
+    }
     uint32_t magic;
     asm volatile("mov.b32 %0, 0x64006400;" : "=r"(magic));
     const uint4* xf4 = reinterpret_cast<const uint4*>(xf);
 #pragma unroll 2
     for (int p = p0; p < p1; ++p) {
       const uint4 xe = xf4[(2 * p) * 4 + t], xo = xf4[(2 * p + 1) * 4 + t];
-      const uint8_t* rg = tile + g * pitch + 36 * p;
-      pair_mma(rg, rg + 8 * pitch, t, xe, xo, magic, acc[0], acc[1], acc[2], acc[3]);
+      const uint8_t* rg = TM ? tile + (p >> 5) * kOsChunkBytes + g * kOsChunkPitch + 36 * (p & 31)
+                             : tile + g * pitch + 36 * p;
+      pair_mma(rg, rg + 8 * (TM ? kOsChunkPitch : pitch), t, xe, xo, magic, acc[0], acc[1], acc[2], acc[3]);
     }
   }
   // lane (g, 0) adds the odd blocks of lane (g, 3)
@@ -127,13 +164,19 @@ __global__ void __launch_bounds__(kOsThreads, 2) oneshot_kernel(const uint8_t* _
   }
   // no copy may still be in flight into this CTA's shared memory at exit
   if (tid == 0 && !ok) {
-    if (!mbar_wait_bounded(&bar[0], 0, wait_limit) || !mbar_wait_bounded(&bar[1], 0, wait_limit))
-      atomicOr(&g_status_os, ST_DRAIN_TIMEOUT);
+    bool drained = true;
+    for (int c = 0; c < chunks; ++c) drained &= mbar_wait_bounded(&bar[c], 0, wait_limit);
+    if (!drained) atomicOr(&g_status_os, ST_DRAIN_TIMEOUT);
   }
 }
 
-// Shared memory of a CTA for width k: x in fragment order and 16 padded rows.
+// Whether a row of width k is staged chunk by chunk with tensor copies.
+bool oneshot_tm(int k) { return k % 2048 == 0 && k / 2048 >= 2 && k / 2048 <= kOsMaxChunks; }
+
+// Shared memory of a CTA for width k: x in fragment order and 16 padded rows
+// (chunk by chunk when they are staged with tensor copies).
 size_t oneshot_smem_bytes(int k) {
+  if (oneshot_tm(k)) return 2 * static_cast<size_t>(k) + static_cast<size_t>(k / 2048) * kOsChunkBytes;
   return 2 * static_cast<size_t>(k) + static_cast<size_t>(kOsRows) * ((k >> 5) * kBlockBytes + 16);
 }
 
@@ -142,7 +185,9 @@ bool oneshot_ok(int n, int k) {
 }
 
 cudaError_t oneshot_prepare() {
-  return cudaFuncSetAttribute(oneshot_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kOsSmemMax);
+  cudaError_t e = cudaFuncSetAttribute(oneshot_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kOsSmemMax);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(oneshot_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kOsSmemMax);
 }
 
 namespace {
@@ -207,7 +252,15 @@ cudaError_t oneshot_launch(const uint8_t* w, const uint16_t* x, float* y, int n,
   attr[0].val.programmaticStreamSerializationAllowed = early ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, oneshot_kernel, w, reinterpret_cast<const __half*>(x), y, n, k, wait_limit);
+  OsArgs a;
+  a.w = w;
+  a.x = reinterpret_cast<const __half*>(x);
+  a.y = y;
+  a.n = n;
+  a.k = k;
+  a.wait_limit = wait_limit;
+  if (oneshot_tm(k) && encode_q4_rows(&a.tm, w, n, k, kOsRows)) return cudaLaunchKernelEx(&cfg, oneshot_kernel<true>, a);
+  return cudaLaunchKernelEx(&cfg, oneshot_kernel<false>, a);
 }
 
 cudaError_t oneshot_read_status(int* out) {
