@@ -17,6 +17,7 @@ namespace q4 {
 
 constexpr int kGlueThreads = 256;    // element-wise kernels
 constexpr int kNormThreads = 1024;   // one CTA per batch row for the RMSNorms
+constexpr int kNormKeep = 4;          // 4-value steps a thread keeps in registers
 
 // Sum of v over the CTA (T threads), the same fixed order in every CTA.
 template <int T>
@@ -81,20 +82,26 @@ __global__ void __launch_bounds__(kNormThreads) resid_norm_kernel(const __half* 
   griddep_wait();
   __shared__ float red[kNormThreads / 32];
   const size_t base = static_cast<size_t>(blockIdx.x) * dim;
+  // the thread's sums stay in registers for rows of up to kNormKeep steps
+  // (16384 values); longer rows read them back
+  float4 keep[kNormKeep];
   float ss = 0.f;
-  for (int i = 4 * threadIdx.x; i < dim; i += 4 * kNormThreads) {
+  int j = 0;
+  for (int i = 4 * threadIdx.x; i < dim; i += 4 * kNormThreads, ++j) {
     const float4 a = load_h4(z + base + i);
     const float4 b = *reinterpret_cast<const float4*>(o + base + i);
     const float4 v = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
     *reinterpret_cast<float4*>(t + base + i) = v;
+    if (j < kNormKeep) keep[j] = v;
     ss = fmaf(v.x, v.x, ss);
     ss = fmaf(v.y, v.y, ss);
     ss = fmaf(v.z, v.z, ss);
     ss = fmaf(v.w, v.w, ss);
   }
   const float r = rsqrtf(block_sum<kNormThreads>(ss, red) / static_cast<float>(dim) + eps);
-  for (int i = 4 * threadIdx.x; i < dim; i += 4 * kNormThreads)
-    store_h4(z_out + base + i, *reinterpret_cast<const float4*>(t + base + i), r);
+  j = 0;
+  for (int i = 4 * threadIdx.x; i < dim; i += 4 * kNormThreads, ++j)
+    store_h4(z_out + base + i, j < kNormKeep ? keep[j] : *reinterpret_cast<const float4*>(t + base + i), r);
 }
 
 template <typename... P, typename... A>
