@@ -274,15 +274,17 @@ def run_gemv(args, torch, q4, model, synth, stream, barrier, gpu_index):
     x = torch.from_numpy(synth.activations(1, k, 0).reshape(-1).view("int16").copy()).cuda()
     y = torch.empty(n, dtype=torch.float32, device="cuda")
     torch.cuda.synchronize()
-    # one step = one pass over the ring, captured as a CUDA graph
+    # one step = one pass over the ring, captured as a CUDA graph; the
+    # products are independent and nothing else runs between them, so they are
+    # chained calls (each may start while the one before it finishes)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         for c in range(copies):   # first launches outside capture
-            q4.q4_gemv(w.data_ptr() + c * mb, x, y, n, k, 1, stream=stream)
+            q4.q4_gemv(w.data_ptr() + c * mb, x, y, n, k, 1, stream=stream, chain=True)
         stream.synchronize()
         with torch.cuda.graph(g, stream=stream):
             for c in range(copies):
-                q4.q4_gemv(w.data_ptr() + c * mb, x, y, n, k, 1, stream=stream)
+                q4.q4_gemv(w.data_ptr() + c * mb, x, y, n, k, 1, stream=stream, chain=True)
 
     def step():
         g.replay()
@@ -756,8 +758,9 @@ def run_sweep(args, torch, q4, model, synth, stream, barrier, gpu_index):
     nmax = max(n for n, _ in dims)
     x = torch.from_numpy(synth.activations(16, kmax, 0).reshape(-1).view("int16").copy()).cuda()
     y = torch.empty(16 * nmax, dtype=torch.float32, device="cuda")
-    kernels = {"oneshot": q4.Q4_KERNEL_ONESHOT, "tc_engine": q4.Q4_KERNEL_TC, "engine": q4.Q4_KERNEL_STREAM,
-               "mma": q4.Q4_KERNEL_MMA, "simple": q4.Q4_KERNEL_SIMPLE}
+    # the one-shot products are chained calls: independent, nothing in between
+    kernels = {"oneshot": q4.Q4_KERNEL_ONESHOT | q4.Q4_GEMV_CHAIN, "tc_engine": q4.Q4_KERNEL_TC,
+               "engine": q4.Q4_KERNEL_STREAM, "mma": q4.Q4_KERNEL_MMA, "simple": q4.Q4_KERNEL_SIMPLE}
     nbytes = layer_bytes * n_layers
     steps = max(5, min(args.steps, 50))
     results = {}

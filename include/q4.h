@@ -89,14 +89,23 @@ size_t q4_matrix_bytes(int n, int k);
                                 k <= 2048 or k % 2048 == 0, k <= 30720); what q4_gemv uses at
                                 batch 1 for those widths above 64 MB of weights */
 #define Q4_KERNEL_ONESHOT 5  /* one-shot tensor-core kernel for a single product: a CTA per 16
-                                rows, the whole tile fetched at once by bulk copies, launched with
-                                programmatic stream serialisation so that consecutive launches
-                                overlap: a launch fetches its weights, reads x and computes while
-                                the one before it finishes, and stores y after it; the launcher
-                                asks for that only when w and x do not overlap the y of a
-                                one-shot product on the same stream that may still be running
-                                (batch 1, k % 512 == 0, 11 k + 256 <= 231424: k <= 20992); what
-                                q4_gemv uses at batch 1 for those widths up to 64 MB of weights */
+                                rows, the whole tile fetched at once by tensor or bulk copies
+                                (batch 1, k % 512 == 0, shared memory within 231424 bytes: k <=
+                                20992); what q4_gemv uses at batch 1 for those widths up to 64 MB
+                                of weights */
+
+/* Flag for q4_gemv_ex's kernel argument (OR it in): a chained call.  A
+ * one-shot product launched with it may start before the kernel before it on
+ * the stream has ended: it fetches its weights, reads x and computes while
+ * that kernel finishes, and stores y only after it (programmatic stream
+ * serialisation), so that back-to-back independent products overlap.  The
+ * caller promises that no kernel it enqueued since the last q4_gemv call on
+ * the stream writes this call's w or x (their reads may run ahead of that
+ * kernel's end); the library itself never starts a call early whose w or x
+ * overlap the y of a one-shot product on the same stream that may still be
+ * running.  Without the flag every call starts after the work before it, as
+ * usual.  Other kernels ignore the flag. */
+#define Q4_GEMV_CHAIN 0x100
 
 /*
  * y[b][n] = sum_k W[n][k] * x[b][k], W dequantisation-free from its Q4_0 blocks

@@ -87,6 +87,8 @@ def test_argument_checks_launch_nothing(lib):
     assert lib.q4_gemv_ex(A, A, A, 4, 256, 2, q4.Q4_KERNEL_STREAM, None) == q4.Q4_ERR_ARG
     assert lib.q4_gemv_ex(A, A, A, 4, 30720, 1, q4.Q4_KERNEL_STREAM, None) == q4.Q4_ERR_ARG   # 2 rows > a stage
     assert lib.q4_gemv_ex(A, A, A, 4, 256, 1, 99, None) == q4.Q4_ERR_ARG
+    assert lib.q4_gemv_ex(A, A, A, 4, 256, 1, 99 | q4.Q4_GEMV_CHAIN, None) == q4.Q4_ERR_ARG   # the flag alone
+    assert lib.q4_gemv_ex(A, A, A, 4, 96, 1, q4.Q4_KERNEL_TC | q4.Q4_GEMV_CHAIN, None) == q4.Q4_ERR_ARG
     assert lib.q4_gemv_ex(A, A, A, 4, 96, 1, q4.Q4_KERNEL_TC, None) == q4.Q4_ERR_ARG       # tc needs k % 256
     assert lib.q4_gemv_ex(A, A, A, 4, 32768, 1, q4.Q4_KERNEL_TC, None) == q4.Q4_ERR_ARG    # x buffer limit
     assert lib.q4_gemv_ex(A, A, A, 4, 256, 3, q4.Q4_KERNEL_TC, None) == q4.Q4_ERR_ARG      # batch 1 only

@@ -139,6 +139,9 @@ def test_oneshot_parity(n, k):
     assert q4.q4_device_status() == 0
 
 
+CHAIN = q4.Q4_KERNEL_ONESHOT | q4.Q4_GEMV_CHAIN   # chained calls: each may start before the one ahead ends
+
+
 def test_oneshot_rejects_and_orders_back_to_back_launches():
     w = dev_u8(synth.q4_matrix(64, 4096, 22, synth.GEMV_TID))
     x = dev_u16(synth.activations(1, 21504, 23).reshape(-1))
@@ -157,13 +160,13 @@ def test_oneshot_rejects_and_orders_back_to_back_launches():
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
         for i in range(41):
-            q4.q4_gemv_ex(da if i % 2 == 0 else db, dx, y, n, k, 1, q4.Q4_KERNEL_ONESHOT, stream=s)
+            q4.q4_gemv_ex(da if i % 2 == 0 else db, dx, y, n, k, 1, CHAIN, stream=s)
         s.synchronize()
         assert np.array_equal(host_f32(y), ya[0])
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=s):
             for i in range(40):
-                q4.q4_gemv_ex(da if i % 2 == 0 else db, dx, y, n, k, 1, q4.Q4_KERNEL_ONESHOT, stream=s)
+                q4.q4_gemv_ex(da if i % 2 == 0 else db, dx, y, n, k, 1, CHAIN, stream=s)
         g.replay()
         s.synchronize()
     assert np.array_equal(host_f32(y), yb[0])
@@ -185,8 +188,8 @@ def test_oneshot_input_from_the_previous_output():
     with torch.cuda.stream(s):
         for _ in range(3):
             buf.fill_(0.0)
-            q4.q4_gemv_ex(d1, x1, buf, n1, k1, 1, q4.Q4_KERNEL_ONESHOT, stream=s)
-            q4.q4_gemv_ex(d2, buf, y2, n2, k2, 1, q4.Q4_KERNEL_ONESHOT, stream=s)
+            q4.q4_gemv_ex(d1, x1, buf, n1, k1, 1, CHAIN, stream=s)
+            q4.q4_gemv_ex(d2, buf, y2, n2, k2, 1, CHAIN, stream=s)
         s.synchronize()
     x2 = buf.detach().cpu().view(torch.int16).numpy().view(np.uint16).copy()
     ref = run(w2, x2, n2, k2, 1, q4.Q4_KERNEL_ONESHOT)
@@ -210,8 +213,8 @@ def test_oneshot_long_chain_then_a_dependent_product():
         for _ in range(3):
             ys.fill_(0.0)
             for i in range(count):
-                q4.q4_gemv_ex(d1, dx, ys[i * n:(i + 1) * n], n, k, 1, q4.Q4_KERNEL_ONESHOT, stream=s)
-            q4.q4_gemv_ex(d2, ys[first * n:(first + 8) * n], y2, n, k, 1, q4.Q4_KERNEL_ONESHOT, stream=s)
+                q4.q4_gemv_ex(d1, dx, ys[i * n:(i + 1) * n], n, k, 1, CHAIN, stream=s)
+            q4.q4_gemv_ex(d2, ys[first * n:(first + 8) * n], y2, n, k, 1, CHAIN, stream=s)
         s.synchronize()
     y1 = run(w1, xs, n, k, 1, q4.Q4_KERNEL_ONESHOT)[0]
     assert np.array_equal(host_f32(ys).reshape(count, n), np.broadcast_to(y1, (count, n)))

@@ -33,6 +33,7 @@ Q4_KERNEL_SIMPLE = 2
 Q4_KERNEL_MMA = 3
 Q4_KERNEL_TC = 4
 Q4_KERNEL_ONESHOT = 5
+Q4_GEMV_CHAIN = 0x100      # OR into q4_gemv_ex's kernel: a chained one-shot call
 
 Q4_DEC_FUSED = 0
 Q4_DEC_PER_LAYER = 1
@@ -191,7 +192,11 @@ def q4_matrix_bytes(n: int, k: int) -> int:
     return lib().q4_matrix_bytes(n, k)
 
 
-def q4_gemv(w, x, y, n: int, k: int, batch: int = 1, stream=None):
+def q4_gemv(w, x, y, n: int, k: int, batch: int = 1, stream=None, chain: bool = False):
+    if chain:   # Q4_GEMV_CHAIN: may overlap the product before it on the stream
+        _check(lib().q4_gemv_ex(_ptr(w), _ptr(x), _ptr(y), n, k, batch, Q4_KERNEL_AUTO | Q4_GEMV_CHAIN,
+                                _stream(stream)), "q4_gemv_ex")
+        return
     _check(lib().q4_gemv(_ptr(w), _ptr(x), _ptr(y), n, k, batch, _stream(stream)), "q4_gemv")
 
 

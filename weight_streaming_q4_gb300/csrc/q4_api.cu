@@ -237,6 +237,8 @@ extern "C" int q4_gemv_ex(const void* w, const uint16_t* x, float* y, int n, int
   int st = check_gemv(w, x, y, n, k, batch);
   if (st != Q4_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool chain = (kernel & Q4_GEMV_CHAIN) != 0;
+  kernel &= ~Q4_GEMV_CHAIN;
   if (kernel == Q4_KERNEL_AUTO) {
     // batch 1: the one-shot kernel up to 64 MB of weights (it overlaps
     // consecutive launches), the persistent tensor-core engine above that (its
@@ -260,7 +262,7 @@ extern "C" int q4_gemv_ex(const void* w, const uint16_t* x, float* y, int n, int
     if (batch != 1 || !q4::oneshot_ok(n, k)) return Q4_ERR_ARG;
     DeviceInfo* dev = nullptr;
     if ((st = device_info(&dev)) != Q4_OK) return st;
-    Q4_CUDA(q4::oneshot_launch(static_cast<const uint8_t*>(w), x, y, n, k, kWaitLimit, s));
+    Q4_CUDA(q4::oneshot_launch(static_cast<const uint8_t*>(w), x, y, n, k, kWaitLimit, chain, s));
     return Q4_OK;
   }
   if (kernel == Q4_KERNEL_MMA) {

@@ -484,8 +484,11 @@ constexpr int kOsSmemMax = 231424;   // dynamic bytes; with the static ones with
 bool oneshot_ok(int n, int k);
 size_t oneshot_smem_bytes(int k);
 cudaError_t oneshot_prepare();
+// chain: the launch may start before the kernel ahead of it on the stream
+// ends (Q4_GEMV_CHAIN's contract), unless w or x overlap the y of a one-shot
+// product on the stream that may still be running.
 cudaError_t oneshot_launch(const uint8_t* w, const uint16_t* x, float* y, int n, int k, uint32_t wait_limit,
-                           cudaStream_t stream);
+                           bool chain, cudaStream_t stream);
 cudaError_t oneshot_read_status(int* out);
 // Timeline of the tensor-core engine's phases (libq4_tl.so only): per CTA,
 // phase and event the global timer; n >= 256 * 64 * 6 values.

@@ -17,13 +17,15 @@
 // The warps' partial sums meet in shared memory and are added in warp order
 // (a fixed order: the result does not depend on timing).
 //
-// The kernel is launched with programmatic stream serialisation: it lets the
-// next kernel of the stream start at once, and each CTA fetches its weights,
-// stages x and computes before it waits for the kernel before it
-// (griddepcontrol.wait) and stores y, so back-to-back products overlap almost
-// entirely.  The launcher asks for that only when the product's w and x do
-// not overlap the y of any one-shot product on the same stream that may still
-// be running; otherwise the kernel starts after its predecessor as usual.
+// A chained call (Q4_GEMV_CHAIN) is launched with programmatic stream
+// serialisation: it lets the next kernel of the stream start at once, and
+// each CTA fetches its weights, stages x and computes before it waits for the
+// kernel before it (griddepcontrol.wait) and stores y, so back-to-back
+// products overlap almost entirely.  The caller vouches that nothing it
+// enqueued since the last product writes w or x; the launcher itself starts a
+// call early only when its w and x do not overlap the y of any one-shot
+// product on the same stream that may still be running.  Any other call
+// starts after its predecessor as usual (its wait then returns at once).
 //
 // The method: PIPO's dequantisation-free 4-bit matrix-vector product
 // ("PIPO: Pipelined Offloading for Efficient Inference on Consumer Devices",
@@ -214,22 +216,22 @@ bool overlaps(uintptr_t a, size_t na, uintptr_t lo, uintptr_t hi) { return a < h
 }  // namespace
 
 cudaError_t oneshot_launch(const uint8_t* w, const uint16_t* x, float* y, int n, int k, uint32_t wait_limit,
-                           cudaStream_t stream) {
+                           bool chain, cudaStream_t stream) {
   if (!oneshot_ok(n, k)) return cudaErrorInvalidValue;
   const uintptr_t wa = reinterpret_cast<uintptr_t>(w), xa = reinterpret_cast<uintptr_t>(x);
   const size_t w_bytes = static_cast<size_t>(n) * (k >> 5) * kBlockBytes, x_bytes = 2 * static_cast<size_t>(k);
-  bool early = true;
+  bool early = chain;   // only a chained call may start before the work ahead of it
   {
     std::lock_guard<std::mutex> lock(g_chain_mu);
     int i = 0;
     while (i < g_chain_n && g_chain[i].stream != stream) ++i;
-    if (i == g_chain_n) {   // a new stream (or one that replaces a remembered one: no early start)
+    if (i == g_chain_n) {   // a new stream (or one that replaces a remembered one): no early start
       if (g_chain_n < 16) {
         ++g_chain_n;
       } else {
         i = static_cast<int>(reinterpret_cast<uintptr_t>(stream) % 16);
-        early = false;
       }
+      early = false;
       g_chain[i].stream = stream;
       g_chain[i].n = 0;
     }
