@@ -103,8 +103,9 @@ size_t q4_matrix_bytes(int n, int k);
  * the stream writes this call's w or x (their reads may run ahead of that
  * kernel's end); the library itself never starts a call early whose w or x
  * overlap the y of a one-shot product on the same stream that may still be
- * running.  Without the flag every call starts after the work before it, as
- * usual.  Other kernels ignore the flag. */
+ * running, and a product that another kernel computes on the stream ends that
+ * list (the next chained call starts after it).  Without the flag every call
+ * starts after the work before it, as usual.  Other kernels ignore the flag. */
 #define Q4_GEMV_CHAIN 0x100
 
 /*

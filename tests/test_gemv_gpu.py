@@ -196,6 +196,33 @@ def test_oneshot_input_from_the_previous_output():
     assert np.array_equal(host_f32(y2), ref[0], equal_nan=True)
 
 
+def test_chained_product_after_another_kernel_product():
+    """A chained one-shot product whose x is the output of the product before
+    it, computed by the batched tensor-core kernel: that launch ends the
+    stream's list of early starts, so the chained call waits for it."""
+    n1, k1, n2, k2 = 2048, 4096, 512, 4096          # y1: 2048 fp32 = 4096 binary16
+    w0 = synth.q4_matrix(n1, k1, 33, synth.GEMV_TID)
+    w1 = synth.q4_matrix(n1, k1, 34, synth.GEMV_TID)
+    w2 = synth.q4_matrix(n2, k2, 35, synth.GEMV_TID)
+    d0, d1, d2 = dev_u8(w0), dev_u8(w1), dev_u8(w2)
+    x1 = dev_u16(synth.activations(1, k1, 36).reshape(-1))
+    y0 = torch.empty(n1, dtype=torch.float32, device="cuda")
+    buf = torch.empty(n1, dtype=torch.float32, device="cuda")
+    y2 = torch.empty(n2, dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            buf.fill_(0.0)
+            q4.q4_gemv_ex(d0, x1, y0, n1, k1, 1, CHAIN, stream=s)            # the stream is on the list
+            q4.q4_gemv_ex(d1, x1, buf, n1, k1, 1, q4.Q4_KERNEL_MMA, stream=s)
+            q4.q4_gemv_ex(d2, buf, y2, n2, k2, 1, CHAIN, stream=s)
+        s.synchronize()
+    x2 = buf.detach().cpu().view(torch.int16).numpy().view(np.uint16).copy()
+    ref = run(w2, x2, n2, k2, 1, q4.Q4_KERNEL_ONESHOT)
+    assert np.array_equal(host_f32(y2), ref[0], equal_nan=True)
+    assert q4.q4_device_status() == 0
+
+
 def test_oneshot_long_chain_then_a_dependent_product():
     """80 independent one-shot products into distinct slices of one buffer
     (more than the launcher's list of early-started products holds, so the

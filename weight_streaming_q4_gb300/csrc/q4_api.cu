@@ -254,6 +254,8 @@ extern "C" int q4_gemv_ex(const void* w, const uint16_t* x, float* y, int n, int
     else if (k % 256 == 0) kernel = Q4_KERNEL_MMA;
     else kernel = Q4_KERNEL_SIMPLE;
   }
+  // only one-shot products know how to follow one another early
+  if (kernel != Q4_KERNEL_ONESHOT) q4::oneshot_chain_break(s);
   if (kernel == Q4_KERNEL_SIMPLE) {
     Q4_CUDA(q4::simple_launch(static_cast<const uint8_t*>(w), x, y, n, k, batch, s));
     return Q4_OK;

@@ -490,6 +490,9 @@ cudaError_t oneshot_prepare();
 cudaError_t oneshot_launch(const uint8_t* w, const uint16_t* x, float* y, int n, int k, uint32_t wait_limit,
                            bool chain, cudaStream_t stream);
 cudaError_t oneshot_read_status(int* out);
+// A product of another kernel was launched on `stream`: the next one-shot
+// product there does not start early.
+void oneshot_chain_break(cudaStream_t stream);
 // Timeline of the tensor-core engine's phases (libq4_tl.so only): per CTA,
 // phase and event the global timer; n >= 256 * 64 * 6 values.
 cudaError_t tc_timeline_read(unsigned long long* out, size_t n, bool clear);

@@ -265,6 +265,18 @@ cudaError_t oneshot_launch(const uint8_t* w, const uint16_t* x, float* y, int n,
   return cudaLaunchKernelEx(&cfg, oneshot_kernel<false>, a);
 }
 
+// Another kernel of the library's products was launched on the stream: the
+// next one-shot product on it starts after it as usual (the list only knows
+// one-shot products' outputs).
+void oneshot_chain_break(cudaStream_t stream) {
+  std::lock_guard<std::mutex> lock(g_chain_mu);
+  for (int i = 0; i < g_chain_n; ++i)
+    if (g_chain[i].stream == stream) {
+      g_chain[i] = g_chain[--g_chain_n];
+      return;
+    }
+}
+
 cudaError_t oneshot_read_status(int* out) {
   int zero = 0;
   cudaError_t e = cudaMemcpyFromSymbol(out, g_status_os, sizeof(int));
